@@ -1,0 +1,12 @@
+"""CPU oracle (test infrastructure only).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The CUDA library never does.
+"""
+from .w4_oracle import (padded_k, rtn_quantize, pack_nibbles, unpack_nibbles,
+                        pack_rtn, dequantize_f64, bf16_to_f64, w4a16_linear,
+                        w4a8_quantize_act, w4a8_linear, int32_worst_case)
+
+__all__ = ["padded_k", "rtn_quantize", "pack_nibbles", "unpack_nibbles",
+           "pack_rtn", "dequantize_f64", "bf16_to_f64", "w4a16_linear",
+           "w4a8_quantize_act", "w4a8_linear", "int32_worst_case"]

@@ -1,0 +1,241 @@
+"""CPU oracle for the group-wise INT4 weight-only linear layer (W4A16, W4A8).
+
+TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only the test suite, the smoke check
+and the CPU-baseline leg of the benchmark may import this module.  It shares
+no code, table or helper with the CUDA library; it is written from the pages'
+formulas and checked against them by the pins in ``tests/test_oracle_*.py``.
+
+Sources (page title, section):
+
+[P1] "Lab 5: Gemma4 端到端推理优化", section "INT4 线性量化":
+     q = clip(round(r/s + z), qmin, qmax), r_hat = s (q - z); one parameter set
+     per output channel and per group_size input columns; symmetric codes
+     stored as q+8 in [0,15] with s = max|r|/7; asymmetric s = (rmax-rmin)/15,
+     z = round(-rmin/s); two codes per uint8, low nibble first; the input
+     dimension is padded up to a multiple of group_size and padded positions
+     must dequantize to zero.
+[P1u] same page, section "量化正确性修正": unpack low and high nibbles
+     independently, then interleave.
+[P1a] same page, section "融合INT4反量化与矩阵乘": the additive offset of an
+     asymmetric group is (8 - z) s when codes are read as (q - 8).
+[P2] "【infra之路】12-投机解码、量化与推理引擎对比", section 2.2: symmetric INT8,
+     scale = max/127, per-value error <= scale/2.
+[P4] "Jetson Orin AGX INT4 推理优化实践：super 分支从 9 tok/s 到 24 tok/s",
+     section "从 FP 线性层到 INT4 DP4A 的数学推导": per-row INT4 weights
+     q^W = clip(round(W/s^W), -8, 7); dynamic per-token INT8 activations
+     s^x = max|x|/127, q^x = clip(round(x/s^x), -127, 127);
+     acc_j = sum_i q^W_ji q^x_i; y_j = s^W_j s^x acc_j + b_j.
+     Section "INT32 accumulator 是否安全": worst case K * 8 * 127.
+     Section "DP4A 做了什么": a uint32 holds eight codes [w7 ... w0].
+
+Readings where the pages are silent (each is also listed in the design notes):
+ (i)   round() is round-half-to-even (IEEE rint).
+ (ii)  r/s, max/7, (rmax-rmin)/15, -rmin/s and r/s + z are each one IEEE
+       fp32 operation with round-to-nearest-even (no reciprocal, no fusion).
+ (iv)  padded positions take part in the group statistics as zeros.
+ (v)   asymmetric: rmin = min(0, min r), rmax = max(0, max r), so z is in
+       [0, 15] and 0 is exactly representable.
+ (vi)  an all-zero group stores s = 0 (and z = 0); its codes are 8 (sym) or
+       0 (asym) and dequantize to exactly 0; no division by zero happens.
+ (viii) the W4A8 weight scale is max|row|/7 (the symmetric rule of [P1]),
+       codes stored as q+8 like W4A16.
+ Matmuls are done in fp64 on exactly dequantized weights (s * (code - z) is
+ exact in fp64), the W4A8 dot product in int64.
+
+Functions that have no pin of their own: none (see the pins' module).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+F32 = np.float32
+
+
+def padded_k(K: int, group_size: int) -> int:
+    """K rounded up to a multiple of group_size [P1]."""
+    return -(-K // group_size) * group_size
+
+
+# ---------------------------------------------------------------------------
+# Quantise [P1], readings (i), (ii), (iv)-(vi)
+# ---------------------------------------------------------------------------
+
+def rtn_quantize(W, group_size: int, symmetric: bool):
+    """Round-to-nearest INT4 quantisation of W [N, K] (fp32).
+
+    Returns (codes uint8 [N, Kp] in [0, 15], scales fp32 [N, Ng],
+    zeros uint8 [N, Ng] or None when symmetric)."""
+    W = np.asarray(W, dtype=F32)
+    N, K = W.shape
+    G = int(group_size)
+    Kp = padded_k(K, G)
+    Ng = Kp // G
+    Wp = np.zeros((N, Kp), dtype=F32)
+    Wp[:, :K] = W                                   # (iv) pads are zeros
+    R = Wp.reshape(N, Ng, G)
+    if symmetric:
+        maxabs = np.abs(R).max(axis=2)              # exact in fp32
+        s = (maxabs / F32(7.0)).astype(F32)         # (ii) one fp32 division
+        nz = s != 0
+        s_div = np.where(nz, s, F32(1.0)).astype(F32)
+        q = np.rint(R / s_div[:, :, None])          # fp32 r/s, then rint (i)
+        q = np.clip(q, -8, 7)
+        q = np.where(nz[:, :, None], q, 0)          # (vi)
+        codes = (q + 8).astype(np.uint8)            # stored code = q + 8
+        zeros = None
+    else:
+        rmin = np.minimum(R.min(axis=2), F32(0.0))  # (v)
+        rmax = np.maximum(R.max(axis=2), F32(0.0))
+        s = ((rmax - rmin).astype(F32) / F32(15.0)).astype(F32)
+        nz = s != 0
+        s_div = np.where(nz, s, F32(1.0)).astype(F32)
+        z = np.clip(np.rint((-rmin) / s_div), 0, 15).astype(F32)
+        z = np.where(nz, z, F32(0.0)).astype(F32)   # (vi)
+        t = (R / s_div[:, :, None]).astype(F32) + z[:, :, None]   # fp32 add
+        q = np.clip(np.rint(t.astype(F32)), 0, 15)
+        q = np.where(nz[:, :, None], q, 0)
+        codes = q.astype(np.uint8)
+        zeros = z.astype(np.uint8)
+    return codes.reshape(N, Kp), s.astype(F32), zeros
+
+
+# ---------------------------------------------------------------------------
+# Pack / unpack [P1], [P1u], [P4] "DP4A 做了什么"
+# ---------------------------------------------------------------------------
+
+def pack_nibbles(codes):
+    """Two codes per byte: column 2j in bits 0-3, column 2j+1 in bits 4-7."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    even = codes[:, 0::2].astype(np.uint16)
+    odd = codes[:, 1::2].astype(np.uint16)
+    return (even | (odd << 4)).astype(np.uint8)
+
+
+def unpack_nibbles(packed):
+    """Inverse of pack_nibbles.  Low and high nibbles are computed from the
+    packed bytes first and written into a fresh array [P1u]."""
+    packed = np.asarray(packed, dtype=np.uint8)
+    N, B = packed.shape
+    out = np.empty((N, 2 * B), dtype=np.uint8)
+    low = packed & np.uint8(0x0F)
+    high = packed >> np.uint8(4)
+    out[:, 0::2] = low
+    out[:, 1::2] = high
+    return out
+
+
+def pack_rtn(W, group_size: int, symmetric: bool):
+    """What w4_pack_rtn returns: (packed uint8 [N, Kp/2], scales fp32
+    [N, Ng], zeros uint8 [N, Ng] or None)."""
+    codes, s, z = rtn_quantize(W, group_size, symmetric)
+    return pack_nibbles(codes), s, z
+
+
+# ---------------------------------------------------------------------------
+# Dequantise and matmul in fp64 [P1]
+# ---------------------------------------------------------------------------
+
+def dequantize_f64(packed, scales, zeros, group_size: int, rows=None):
+    """W_hat[n, k] = s[n, k // G] * (code[n, k] - z[n, k // G]) in fp64, with
+    z = 8 for symmetric groups.  Exact: s is fp32 and code - z a small
+    integer.  ``rows`` selects output channels (all when None)."""
+    packed = np.asarray(packed)
+    scales = np.asarray(scales, dtype=F32)
+    if rows is not None:
+        rows = np.asarray(rows)
+        packed = packed[rows]
+        scales = scales[rows]
+        zeros = None if zeros is None else np.asarray(zeros)[rows]
+    codes = unpack_nibbles(packed).astype(np.float64)
+    N, Kp = codes.shape
+    G = int(group_size)
+    Ng = Kp // G
+    if zeros is None:
+        zf = np.full((N, Ng), 8.0)
+    else:
+        zf = np.asarray(zeros, dtype=np.float64)
+    sf = scales.astype(np.float64)
+    c3 = codes.reshape(N, Ng, G)
+    return (sf[:, :, None] * (c3 - zf[:, :, None])).reshape(N, Kp)
+
+
+def bf16_to_f64(x):
+    """Accepts a torch bf16 tensor, or an fp32 array holding bf16 values,
+    and returns the exact fp64 values."""
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            x = x.detach().to("cpu").float().numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    x = np.asarray(x, dtype=F32)
+    if np.any(x.view(np.uint32) & np.uint32(0xFFFF)):
+        raise ValueError("activations are not bf16 values")
+    return x.astype(np.float64)
+
+
+def w4a16_linear(x, packed, scales, zeros, bias, K: int, group_size: int,
+                 rows=None):
+    """y[m, n] = sum_{k<K} x[m, k] * W_hat[n, k] + b[n] in fp64.
+
+    ``x`` holds bf16 values [M, K].  ``rows`` restricts the output channels
+    computed (returns y[:, rows]).  The contraction is a library fp64 matmul
+    of the exactly dequantised weights."""
+    xd = bf16_to_f64(x)
+    Wd = dequantize_f64(packed, scales, zeros, group_size, rows=rows)[:, :K]
+    y = xd @ Wd.T
+    if bias is not None:
+        b = np.asarray(bias, dtype=np.float64)
+        y = y + (b if rows is None else b[np.asarray(rows)])[None, :]
+    return y
+
+
+# ---------------------------------------------------------------------------
+# W4A8 [P4]
+# ---------------------------------------------------------------------------
+
+def w4a8_quantize_act(x, Kp: int):
+    """Per-token dynamic INT8: s_x = fp32(max|x| / 127),
+    q_x = clip(rint(fp32(x / s_x)), -127, 127); columns K..Kp-1 are 0.
+    Returns (qx int8 [M, Kp], sx fp32 [M])."""
+    xf = bf16_to_f64(x).astype(F32)
+    M, K = xf.shape
+    maxabs = np.abs(xf).max(axis=1) if K > 0 else np.zeros(M, F32)
+    sx = (maxabs.astype(F32) / F32(127.0)).astype(F32)
+    nz = sx != 0
+    s_div = np.where(nz, sx, F32(1.0)).astype(F32)
+    q = np.clip(np.rint((xf / s_div[:, None]).astype(F32)), -127, 127)
+    q = np.where(nz[:, None], q, 0)
+    qx = np.zeros((M, Kp), dtype=np.int8)
+    qx[:, :K] = q.astype(np.int8)
+    return qx, sx
+
+
+def w4a8_linear(qx, sx, packed, w_scales, bias, rows=None):
+    """acc[m, n] = sum_k (code[n, k] - 8) * qx[m, k] over all Kp columns, in
+    int64; y = s_W[n] * s_x[m] * acc + b[n] in fp64.  Per-row weight scale
+    (one group spanning the padded row).  Returns (acc int64, y fp64)."""
+    packed = np.asarray(packed)
+    ws = np.asarray(w_scales, dtype=F32).reshape(packed.shape[0], -1)
+    if ws.shape[1] != 1:
+        raise ValueError("w4a8 oracle takes one weight scale per row")
+    ws = ws[:, 0]
+    if rows is not None:
+        rows = np.asarray(rows)
+        packed = packed[rows]
+        ws = ws[rows]
+    q = unpack_nibbles(packed).astype(np.int64) - 8
+    qx64 = np.asarray(qx, dtype=np.int64)
+    acc = qx64 @ q.T
+    y = (ws.astype(np.float64)[None, :] * np.asarray(sx, np.float64)[:, None]
+         * acc.astype(np.float64))
+    if bias is not None:
+        b = np.asarray(bias, dtype=np.float64)
+        y = y + (b if rows is None else b[rows])[None, :]
+    return acc, y
+
+
+def int32_worst_case(K: int) -> int:
+    """Largest |acc| of an INT4 x INT8 dot product of length K [P4]:
+    |q^W| <= 8 and |q^x| <= 127."""
+    return K * 8 * 127

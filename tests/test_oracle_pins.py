@@ -1,0 +1,359 @@
+"""Pins for the CPU oracle: closed forms, invariants, worked numbers from the
+pages, and brute force on tiny inputs.  Every check here is computed
+independently of the oracle's own code path, so a dropped term, a wrong sign,
+a swapped nibble or a transposed operand in the oracle fails at least one.
+"""
+import json
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _rand_w(N, K, seed, std=0.02, outlier_cols=0):
+    rng = np.random.default_rng(seed)
+    W = (rng.standard_normal((N, K)) * std).astype(np.float32)
+    if outlier_cols:
+        cols = rng.permutation(K)[:outlier_cols]
+        W[:, cols] *= np.float32(20.0)
+    return W
+
+
+def _bf16_round(a):
+    """Round fp32 values to bf16 (nearest-even) and return them as fp32."""
+    a = np.asarray(a, dtype=np.float32)
+    u = a.view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    return u.astype(np.uint32).view(np.float32)
+
+
+# ---------------------------------------------------------------------------
+# Quantisation closed forms (page "Lab 5: Gemma4 端到端推理优化", INT4 线性量化)
+# ---------------------------------------------------------------------------
+
+def test_symmetric_closed_form_and_ties():
+    # One group of 32 with max|r| = 7/8, so s = 1/8 exactly; r = k/8 gives
+    # q = k exactly, r = +-1.5/8 and 0.5/8 are ties (half to even).
+    r = np.zeros(32, np.float32)
+    r[:8] = [0.875, -0.875, 0.125, -0.25, 0.0625, 0.1875, -0.1875, -0.3125]
+    codes, s, z = O.rtn_quantize(r[None, :], 32, True)
+    assert z is None
+    assert s[0, 0] == np.float32(0.125)
+    q = codes[0].astype(int) - 8
+    assert list(q[:8]) == [7, -7, 1, -2, 0, 2, -2, -2]
+    assert all(q[8:] == 0)
+
+
+def test_asymmetric_closed_form():
+    # rmin = -1, rmax = 2: s = 3/15 (fp32), z = round(1/s) = 5.
+    r = np.linspace(-1.0, 2.0, 32).astype(np.float32)
+    codes, s, z = O.rtn_quantize(r[None, :], 32, False)
+    assert s[0, 0] == np.float32(3.0) / np.float32(15.0)
+    assert z[0, 0] == 5
+    assert codes[0, 0] == 0 and codes[0, -1] == 15
+    r2 = r.copy()
+    r2[7] = 0.0
+    c2, s2, z2 = O.rtn_quantize(r2[None, :], 32, False)
+    assert c2[0, 7] == z2[0, 0]           # zero maps onto the zero point
+    W = O.dequantize_f64(O.pack_nibbles(c2), s2, z2, 32)
+    assert W[0, 7] == 0.0
+
+
+def test_asymmetric_positive_group_includes_zero():
+    # Reading (v): the range is widened to contain 0, so z stays in [0, 15].
+    r = np.linspace(0.5, 1.5, 32).astype(np.float32)
+    codes, s, z = O.rtn_quantize(r[None, :], 32, False)
+    assert z[0, 0] == 0
+    assert s[0, 0] == np.float32(1.5) / np.float32(15.0)
+    r = -r
+    codes, s, z = O.rtn_quantize(r[None, :], 32, False)
+    assert z[0, 0] == 15
+
+
+@pytest.mark.parametrize("symmetric", [True, False])
+def test_zero_group(symmetric):
+    W = np.zeros((2, 64), np.float32)
+    W[1, 40] = 0.5
+    codes, s, z = O.rtn_quantize(W, 32, symmetric)
+    assert s[0, 0] == 0 and s[0, 1] == 0 and s[1, 0] == 0
+    Wd = O.dequantize_f64(O.pack_nibbles(codes), s, z, 32)
+    assert np.all(Wd[0] == 0.0) and np.all(Wd[1, :32] == 0.0)
+    assert Wd[1, 40] == pytest.approx(0.5, rel=1e-6)
+
+
+@pytest.mark.parametrize("symmetric", [True, False])
+@pytest.mark.parametrize("G", [32, 128])
+def test_codes_are_nearest_grid_point(symmetric, G):
+    """Brute force: every code is the grid point s*(c - z), c in 0..15,
+    nearest to r (ties, and values within fp32 rounding of a tie, may go
+    either way)."""
+    W = _rand_w(24, 256, seed=G + symmetric, outlier_cols=3)
+    codes, s, z = O.rtn_quantize(W, G, symmetric)
+    N, Kp = codes.shape
+    Ng = Kp // G
+    zz = np.full((N, Ng), 8) if z is None else z.astype(int)
+    grid_c = np.arange(16)
+    for n in range(N):
+        for g in range(Ng):
+            sg = float(s[n, g])
+            r = W[n, g * G:(g + 1) * G].astype(np.float64)
+            dist = np.abs(r[:, None] - sg * (grid_c[None, :] - zz[n, g]))
+            best = dist.argmin(axis=1)
+            got = codes[n, g * G:(g + 1) * G].astype(int)
+            d_got = dist[np.arange(G), got]
+            d_best = dist[np.arange(G), best]
+            # equal distance (a tie) is fine; anything else must match
+            assert np.all(d_got <= d_best + 1e-6 * sg), (n, g)
+
+
+@pytest.mark.parametrize("symmetric", [True, False])
+def test_rtn_error_at_most_half_step(symmetric):
+    """|r - r_hat| <= s/2 for every element (the half-step bound of
+    symmetric INT8 on page 2, section 2.2, carried to the INT4 grid)."""
+    W = _rand_w(64, 384, seed=7, outlier_cols=4)
+    packed, s, z = O.pack_rtn(W, 32, symmetric)
+    Wd = O.dequantize_f64(packed, s, z, 32)[:, :384]
+    step = np.repeat(s.astype(np.float64), 32, axis=1)[:, :384]
+    assert np.all(np.abs(W - Wd) <= step / 2 * (1 + 1e-6))
+
+
+# ---------------------------------------------------------------------------
+# Packing
+# ---------------------------------------------------------------------------
+
+def test_pack_bit_layout_and_round_trip():
+    rng = np.random.default_rng(1)
+    codes = rng.integers(0, 16, size=(5, 64)).astype(np.uint8)
+    p = O.pack_nibbles(codes)
+    assert p.shape == (5, 32)
+    for n in range(5):
+        for j in range(32):
+            assert int(p[n, j]) == int(codes[n, 2 * j]) | (int(codes[n, 2 * j + 1]) << 4)
+    # a little-endian uint32 holds eight codes [w7 ... w0] (page 4, DP4A 做了什么)
+    words = p.view("<u4")
+    for n in range(5):
+        for w in range(8):
+            expect = sum(int(codes[n, 8 * w + i]) << (4 * i) for i in range(8))
+            assert int(words[n, w]) == expect
+    assert np.array_equal(O.unpack_nibbles(p), codes)
+
+
+def test_unpack_in_place_mistake_is_caught():
+    """Page 'Lab 5', section 量化正确性修正: interleaving into the packed uint8
+    storage itself corrupts the codes; the oracle's unpack does not."""
+    rng = np.random.default_rng(2)
+    codes = rng.integers(0, 16, size=(3, 64)).astype(np.uint8)
+    packed = O.pack_nibbles(codes)
+
+    def naive_in_place(pk):
+        buf = np.zeros((pk.shape[0], pk.shape[1] * 2), np.uint8)
+        buf[:, :pk.shape[1]] = pk          # codes live in the same storage
+        view = buf
+        src = view[:, :pk.shape[1]]
+        view[:, 0::2] = src & 0x0F         # overwrites bytes still to be read
+        view[:, 1::2] = src >> 4
+        return view
+
+    assert not np.array_equal(naive_in_place(packed), codes)
+    assert np.array_equal(O.unpack_nibbles(packed), codes)
+
+
+def test_bytes_per_row_matches_page_table():
+    g = _golden("p4_bytes_per_row.json")
+    H = g["H"]
+    W = _rand_w(2, H, seed=3)
+    packed, s, _ = O.pack_rtn(W, 128, True)
+    assert packed.shape[1] == g["int4_row_bytes"]
+    assert 2 * H == g["fp16_row_bytes"] and H == g["int8_row_bytes"]
+
+
+# ---------------------------------------------------------------------------
+# Padding (page 'Lab 5', INT4 线性量化: padded positions dequantize to zero)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("symmetric", [True, False])
+def test_padding_dequantizes_to_zero_and_changes_nothing(symmetric):
+    K, G = 100, 32          # Kp = 128
+    W = _rand_w(8, K, seed=4)
+    packed, s, z = O.pack_rtn(W, G, symmetric)
+    assert packed.shape[1] == 64
+    Wd = O.dequantize_f64(packed, s, z, G)
+    assert np.all(Wd[:, K:] == 0.0)
+    assert not np.any(np.signbit(Wd[:, K:]))
+    # appending explicit zero columns to W and x leaves y unchanged
+    Wz = np.zeros((8, 128), np.float32)
+    Wz[:, :K] = W
+    p2, s2, z2 = O.pack_rtn(Wz, G, symmetric)
+    assert np.array_equal(p2, packed) and np.array_equal(s2, s)
+    rng = np.random.default_rng(5)
+    x = _bf16_round(rng.standard_normal((3, K)))
+    xz = np.zeros((3, 128), np.float32)
+    xz[:, :K] = x
+    y1 = O.w4a16_linear(x, packed, s, z, None, K, G)
+    y2 = O.w4a16_linear(xz, p2, s2, z2, None, 128, G)
+    assert np.array_equal(y1, y2)
+
+
+def test_additive_offset_identity():
+    """Page 'Lab 5', 融合INT4反量化与矩阵乘: with codes read as (q - 8), an
+    asymmetric group needs the additive offset (8 - z) s:
+    s (q - z) == s (q - 8) + (8 - z) s, exactly in fp64."""
+    W = _rand_w(16, 256, seed=6, outlier_cols=2)
+    codes, s, z = O.rtn_quantize(W, 32, False)
+    sf = np.repeat(s.astype(np.float64), 32, axis=1)
+    zf = np.repeat(z.astype(np.float64), 32, axis=1)
+    c = codes.astype(np.float64)
+    lhs = O.dequantize_f64(O.pack_nibbles(codes), s, z, 32)
+    rhs = sf * (c - 8) + (8 - zf) * sf
+    assert np.array_equal(lhs, rhs)
+    assert np.array_equal(lhs, sf * (c - zf))
+
+
+# ---------------------------------------------------------------------------
+# Matmul
+# ---------------------------------------------------------------------------
+
+def test_dyadic_inputs_give_exact_integer_result():
+    """x in {0, +-1/4, +-1/2, +-1}, group maxima 7 * 2^-e so that s = 2^-e:
+    every product and partial sum is exact in fp64, so the oracle must equal
+    an integer computation done here with Python ints."""
+    rng = np.random.default_rng(8)
+    M, N, K, G = 3, 5, 64, 32
+    qs = rng.integers(-7, 8, size=(N, K))
+    e = rng.integers(2, 6, size=(N, K // G))
+    W = np.zeros((N, K), np.float32)
+    for n in range(N):
+        for g in range(K // G):
+            qs[n, g * G] = 7                        # pin the group max to 7 s
+            W[n, g * G:(g + 1) * G] = qs[n, g * G:(g + 1) * G] * 2.0 ** -int(e[n, g])
+    x4 = rng.integers(-4, 5, size=(M, K))
+    x4[np.abs(x4) == 3] = 0
+    x = (x4 / 4.0).astype(np.float32)
+    packed, s, z = O.pack_rtn(W, G, True)
+    y = O.w4a16_linear(x, packed, s, z, None, K, G)
+    # exact: y * 4 * 2^emax is an integer
+    for m in range(M):
+        for n in range(N):
+            tot = Fraction(0)
+            for k in range(K):
+                tot += Fraction(int(x4[m, k]), 4) * Fraction(int(qs[n, k]), 2 ** int(e[n, k // G]))
+            assert Fraction(y[m, n]) == tot
+
+
+@pytest.mark.parametrize("symmetric", [True, False])
+def test_tiny_brute_force_triple_loop(symmetric):
+    """Independent triple loop with exact rationals, from the codes, scales
+    and zeros, for M, N, K in 1..3 x 1..5 x 32..64, with bias."""
+    rng = np.random.default_rng(9)
+    for (M, N, K, G) in [(1, 1, 32, 32), (2, 3, 40, 32), (3, 5, 64, 32), (1, 4, 64, 64)]:
+        W = _rand_w(N, K, seed=M * 100 + N * 10 + K)
+        x = _bf16_round(rng.standard_normal((M, K)))
+        b = rng.standard_normal(N).astype(np.float32)
+        codes, s, z = O.rtn_quantize(W, G, symmetric)
+        packed = O.pack_nibbles(codes)
+        y = O.w4a16_linear(x, packed, s, z, b, K, G)
+        for m in range(M):
+            for n in range(N):
+                tot = Fraction(float(b[n]))
+                for k in range(K):
+                    g = k // G
+                    zp = 8 if z is None else int(z[n, g])
+                    w = Fraction(float(s[n, g])) * (int(codes[n, k]) - zp)
+                    tot += Fraction(float(x[m, k])) * w
+                assert abs(y[m, n] - float(tot)) <= 1e-12 * max(1.0, abs(float(tot)))
+
+
+# ---------------------------------------------------------------------------
+# W4A8 (page 'Jetson Orin AGX INT4 推理优化实践')
+# ---------------------------------------------------------------------------
+
+def test_int32_bound_worked_number_and_worst_case():
+    g = _golden("p4_int32_bound.json")
+    assert g["max_abs_qw"] * g["max_abs_qx"] == g["per_term"]
+    assert O.int32_worst_case(g["H"]) == g["bound"]
+    assert g["bound"] < g["int32_max"] == 2 ** 31 - 1
+    # worst-case synthetic input: all codes 0 (q = -8) and all qx = 127
+    K = 18944
+    packed = np.zeros((2, K // 2), np.uint8)
+    qx = np.full((1, K), 127, np.int8)
+    acc, y = O.w4a8_linear(qx, np.ones(1, np.float32), packed,
+                           np.ones(2, np.float32), None)
+    assert acc[0, 0] == -O.int32_worst_case(K) == -8 * 127 * K
+    assert abs(acc[0, 0]) < 2 ** 31 - 1
+
+
+def test_w4a8_reduction_sums_codes():
+    """With qx = 1 and s_x = s_W = 1, acc_j is the row sum of the signed
+    codes q = code - 8."""
+    rng = np.random.default_rng(10)
+    codes = rng.integers(0, 16, size=(7, 96)).astype(np.uint8)
+    packed = O.pack_nibbles(codes)
+    qx = np.ones((1, 96), np.int8)
+    acc, y = O.w4a8_linear(qx, np.ones(1, np.float32), packed,
+                           np.ones(7, np.float32), None)
+    assert np.array_equal(acc[0], codes.astype(np.int64).sum(axis=1) - 8 * 96)
+    assert np.array_equal(y[0], acc[0].astype(np.float64))
+
+
+def test_w4a8_matches_its_definition_by_loop():
+    rng = np.random.default_rng(11)
+    N, K = 6, 64
+    W = _rand_w(N, K, seed=12)
+    packed, ws, _ = O.pack_rtn(W, K, True)          # per-row scale
+    x = _bf16_round(rng.standard_normal((2, K)))
+    qx, sx = O.w4a8_quantize_act(x, K)
+    b = rng.standard_normal(N).astype(np.float32)
+    acc, y = O.w4a8_linear(qx, sx, packed, ws, b)
+    codes = O.unpack_nibbles(packed).astype(int)
+    for m in range(2):
+        for n in range(N):
+            a = sum((codes[n, k] - 8) * int(qx[m, k]) for k in range(K))
+            assert acc[m, n] == a
+            expect = float(ws[n, 0]) * float(sx[m]) * a + float(b[n])
+            assert y[m, n] == pytest.approx(expect, rel=1e-15, abs=1e-15)
+
+
+def test_int8_activation_examples_from_page_2():
+    g = _golden("p2_int8_examples.json")
+    rng = np.random.default_rng(13)
+    # max 1.0: scale ~ 0.0078, error <= 0.0039
+    x = _bf16_round(np.clip(rng.standard_normal((1, 512)) * 0.3, -0.99, 0.99))
+    x[0, 17] = g["int8_symmetric"]["max"]
+    qx, sx = O.w4a8_quantize_act(x, 512)
+    assert sx[0] == np.float32(1.0) / np.float32(127.0)
+    assert abs(float(sx[0]) - g["int8_symmetric"]["scale_approx"]) < 1e-4
+    err = np.abs(qx[0].astype(np.float64) * float(sx[0]) - x[0])
+    assert err.max() <= float(sx[0]) / 2 * (1 + 1e-6)
+    assert err.max() <= g["int8_symmetric"]["max_error_approx"] + 1e-4
+    assert qx[0, 17] == 127
+    # one outlier of 5.0 among small values: scale ~ 0.039, 0.05 -> 1 -> 0.039
+    ex = g["outlier_example"]
+    x = _bf16_round(np.full((1, 64), ex["normal_value"], np.float32))
+    x[0, 3] = ex["outlier"]
+    qx, sx = O.w4a8_quantize_act(x, 64)
+    assert abs(float(sx[0]) - ex["scale_approx"]) < 5e-4
+    assert qx[0, 0] == ex["code"]
+    assert abs(qx[0, 0] * float(sx[0]) - ex["dequant_approx"]) < 5e-4
+    rel = abs(qx[0, 0] * float(sx[0]) - float(x[0, 0])) / float(x[0, 0])
+    assert abs(rel - ex["rel_error_approx"]) < 0.015
+
+
+def test_activation_quantize_closed_form_and_padding():
+    x = np.zeros((2, 30), np.float32)
+    x[0, :4] = [1.0, -0.5, 0.25, 0.0]
+    qx, sx = O.w4a8_quantize_act(x, 32)
+    assert qx.shape == (2, 32) and qx.dtype == np.int8
+    assert sx[0] == np.float32(1.0) / np.float32(127.0)
+    assert list(qx[0, :4]) == [127, -64, 32, 0]    # 63.5 -> 64 (half-even), 31.75 -> 32
+    assert np.all(qx[:, 30:] == 0)
+    assert sx[1] == 0 and np.all(qx[1] == 0)       # all-zero token
