@@ -1,0 +1,171 @@
+/*
+ * w4.h - C ABI of libw4: the group-wise INT4 weight-only quantized linear
+ * layer y = x * W_hat^T (+ b) on one NVIDIA GB300 (sm_103a).
+ *
+ * Definitions this library implements (page title, section):
+ *
+ *  [LAB5] "Lab 5: Gemma4 端到端推理优化", section "INT4 线性量化":
+ *     q = clip(round(r/s + z), qmin, qmax), r_hat = s (q - z); one (s, z) per
+ *     output channel and per group_size input columns.  Symmetric groups use
+ *     s = max|r| / 7 and store the code q + 8 in [0, 15] (r_hat = s (code-8));
+ *     asymmetric groups use s = (r_max - r_min) / 15, z = round(-r_min / s).
+ *     Two codes per uint8, the earlier column in the low nibble.  K is padded
+ *     up to a multiple of group_size and padded positions dequantize to 0.
+ *  [LAB5-F] same page, sections "融合INT4反量化与矩阵乘" and
+ *     "Prefill和Decode分流": dequantize in registers next to the matmul for
+ *     small M (decode); for large M the layer is a dense GEMM.
+ *  [ORIN] "Jetson Orin AGX INT4 推理优化实践：super 分支从 9 tok/s 到 24 tok/s",
+ *     section "从 FP 线性层到 INT4 DP4A 的数学推导": per-row INT4 weights,
+ *     per-token dynamic INT8 activations s_x = max|x| / 127,
+ *     q_x = clip(round(x / s_x), -127, 127), acc_j = sum_i q^W_ji q^x_i in
+ *     int32, y_j = s^W_j s_x acc_j + b_j; section "INT32 accumulator 是否安全".
+ *
+ * Conventions for every entry point
+ *  - Matrices are row-major.  W is [N, K] (out x in); x is [M, K]; y is [M, N].
+ *  - Kp = ceil(K / group_size) * group_size;  Ng = Kp / group_size.
+ *  - bf16 tensors are passed as uint16_t bit patterns (IEEE bfloat16).
+ *  - All data pointers are DEVICE pointers owned by the caller.  The library
+ *    never allocates, frees or synchronizes (except w4_get_device_error).
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream); every
+ *    call only enqueues work on it and returns.
+ *  - Return value: W4_OK (0) or a negative W4_ERR_* code.  Arguments are
+ *    checked on the host before anything is enqueued; a failed check leaves
+ *    every output untouched.  w4_error_string() names a code.
+ *  - group_size must be a positive multiple of 32 (each packed group is a
+ *    whole number of 16-byte words).
+ *  - Weights (packed, scales, zeros) are assumed constant while a call that
+ *    reads them is in flight.
+ */
+#ifndef W4_H_
+#define W4_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define W4_API __attribute__((visibility("default")))
+#else
+#define W4_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define W4_OK                       0
+#define W4_ERR_INVALID_ARG         -1  /* a size or flag is out of range      */
+#define W4_ERR_NULL_PTR            -2  /* a required pointer is NULL          */
+#define W4_ERR_MISALIGNED          -3  /* packed/x/qx not 16-byte aligned     */
+#define W4_ERR_UNSUPPORTED_GROUP   -4  /* group_size not a positive mult. of 32,
+                                          or not one group per row for W4A8  */
+#define W4_ERR_K_TOO_LARGE         -5  /* W4A8: Kp * 15 * 127 >= 2^31         */
+#define W4_ERR_WORKSPACE           -6  /* workspace NULL or too small         */
+#define W4_ERR_CUDA                -7  /* a CUDA runtime call failed          */
+#define W4_ERR_UNSUPPORTED_SHAPE   -8  /* shape outside what a kernel takes   */
+#define W4_ERR_DEVICE_TIMEOUT      -9  /* a kernel's bounded wait ran out     */
+
+/* Largest padded K accepted by the W4A8 path: the kernels accumulate
+ * code (0..15) x q_x (-127..127) products in int32, so Kp * 15 * 127 must
+ * stay below 2^31 ([ORIN], "INT32 accumulator 是否安全", for the signed
+ * form K * 8 * 127).                                                       */
+#define W4_W4A8_MAX_KP 1127288
+
+/* ---------------------------------------------------------------------------
+ * w4_pack_rtn - round-to-nearest INT4 quantisation and packing ([LAB5]).
+ *
+ *  W       [N, K] fp32 input weights.
+ *  packed  [N, Kp/2] uint8 out: byte j of a row holds column 2j in bits 0-3
+ *          and column 2j+1 in bits 4-7; 16-byte aligned.
+ *  scales  [N, Ng] fp32 out.
+ *  zeros   [N, Ng] uint8 out when symmetric == 0; must be NULL when
+ *          symmetric != 0 (symmetric codes are q + 8).
+ *  Rounding: each division is one IEEE fp32 division rounded to nearest
+ *  even, round() is round-half-to-even, pads count as zeros in the group
+ *  statistics, an asymmetric range is widened to contain 0, and an all-zero
+ *  group stores s = 0 (z = 0).  Codes are bit-identical to a scalar fp32
+ *  evaluation of the formulas in that order.
+ * ------------------------------------------------------------------------- */
+W4_API int w4_pack_rtn(const float* W, int N, int K, int group_size, int symmetric,
+                uint8_t* packed, float* scales, uint8_t* zeros, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * w4a16_workspace_bytes - bytes of device workspace w4a16_linear needs for
+ * this shape on the CURRENT device (split-K partial sums and arrival
+ * counters).  May be 0.  The workspace must be zero-filled once before its
+ * first use; every call leaves its counters at zero again, so it can be
+ * reused by later calls on the same stream without clearing.
+ * ------------------------------------------------------------------------- */
+W4_API size_t w4a16_workspace_bytes(int M, int N, int K, int group_size);
+
+/* ---------------------------------------------------------------------------
+ * w4a16_linear - y = x * W_hat^T (+ bias), W_hat = s (code - z) per group
+ * ([LAB5]); bf16 activations and outputs, fp32 accumulation.
+ *
+ *  x        [M, K] bf16, 16-byte aligned.
+ *  packed   [N, Kp/2] uint8 from w4_pack_rtn, 16-byte aligned.
+ *  scales   [N, Ng] fp32.
+ *  zeros    [N, Ng] uint8, or NULL for symmetric groups (z = 8).
+ *  bias     [N] fp32 or NULL.
+ *  y        [M, N] bf16 out.
+ *  symmetric must agree with zeros == NULL.
+ *  M <= 16 runs the decode kernel (dequantize in registers, one pass over the
+ *  weights); larger M runs the tensor-core prefill kernel, which requires
+ *  K % 8 == 0.  workspace: see w4a16_workspace_bytes.  Calls that share a
+ *  workspace must not overlap on the GPU.
+ * ------------------------------------------------------------------------- */
+W4_API int w4a16_linear(const uint16_t* x, const uint8_t* packed, const float* scales,
+                 const uint8_t* zeros, const float* bias, uint16_t* y,
+                 int M, int N, int K, int group_size, int symmetric,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * w4a8_quantize_act - per-token dynamic INT8 activations ([ORIN]):
+ *  s_x[m] = fp32(max_k |x[m,k]| / 127),
+ *  qx[m,k] = clip(round(fp32(x[m,k] / s_x[m])), -127, 127) for k < K, 0 for
+ *  K <= k < Kp; an all-zero token gets s_x = 0 and qx = 0.
+ *
+ *  x   [M, K] bf16;  qx [M, Kp] int8 out (16-byte aligned);  sx [M] fp32 out.
+ * ------------------------------------------------------------------------- */
+W4_API int w4a8_quantize_act(const uint16_t* x, int M, int K, int group_size,
+                      int8_t* qx, float* sx, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * w4a8_workspace_bytes - as w4a16_workspace_bytes, for w4a8_linear.
+ * ------------------------------------------------------------------------- */
+W4_API size_t w4a8_workspace_bytes(int M, int N, int K, int group_size);
+
+/* ---------------------------------------------------------------------------
+ * w4a8_linear - INT4 x INT8 integer linear layer ([ORIN]):
+ *  acc[m,n] = sum_{k < Kp} (code[n,k] - 8) * qx[m,k]   (exact, int32)
+ *  y[m,n]   = s_W[n] * s_x[m] * acc[m,n] + bias[n]      (fp32, stored bf16)
+ *
+ *  qx, sx     from w4a8_quantize_act (same K and group_size).
+ *  packed     [N, Kp/2] uint8 symmetric codes from w4_pack_rtn with
+ *             group_size == Kp (one scale per row), 16-byte aligned.
+ *  w_scales   [N] fp32 (the [N, 1] scales of that packing).
+ *  bias       [N] fp32 or NULL.
+ *  y          [M, N] bf16 out.
+ *  acc_out    [M, N] int32 out, or NULL.
+ *  Requires M <= 16, group_size == Kp and Kp <= W4_W4A8_MAX_KP.
+ * ------------------------------------------------------------------------- */
+W4_API int w4a8_linear(const int8_t* qx, const float* sx, const uint8_t* packed,
+                const float* w_scales, const float* bias, uint16_t* y,
+                int32_t* acc_out, int M, int N, int K, int group_size,
+                void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * w4_get_device_error - synchronizes `stream`, then returns and clears the
+ * library's device-side error flag on the current device: W4_OK, or
+ * W4_ERR_DEVICE_TIMEOUT when a kernel gave up on a bounded wait (its outputs
+ * are then unspecified).  Returns W4_ERR_CUDA if the synchronization fails.
+ * ------------------------------------------------------------------------- */
+W4_API int w4_get_device_error(void* stream);
+
+/* w4_error_string - static description of a W4_* code (never NULL). */
+W4_API const char* w4_error_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4_H_ */

@@ -1,0 +1,15 @@
+"""Python binding of libw4 (the INT4 weight-only linear layer for GB300).
+
+The functions here carry the names of the C entry points in ``include/w4.h``
+and only marshal arguments: they check dtypes and shapes of torch CUDA
+tensors, allocate outputs with torch when the caller passes none, and call
+the library through ctypes on the current torch stream.  Every step of the
+computation runs in the library's CUDA kernels; there is no fallback.
+"""
+from ._lib import (W4Error, lib_path, load, w4_pack_rtn, w4a16_workspace_bytes,
+                   w4a16_linear, w4a8_quantize_act, w4a8_workspace_bytes, w4a8_linear,
+                   w4_get_device_error, w4_error_string, padded_k, EXPORTED)
+
+__all__ = ["W4Error", "lib_path", "load", "w4_pack_rtn", "w4a16_workspace_bytes",
+           "w4a16_linear", "w4a8_quantize_act", "w4a8_workspace_bytes", "w4a8_linear",
+           "w4_get_device_error", "w4_error_string", "padded_k", "EXPORTED"]

@@ -1,0 +1,228 @@
+"""ctypes binding of libw4.so (see include/w4.h for the contract)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libw4.so")
+
+_c_int, _c_size, _vp = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
+
+# name -> (restype, argtypes); mirrors include/w4.h
+_SIGS = {
+    "w4_pack_rtn": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _vp, _vp]),
+    "w4a16_workspace_bytes": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
+    "w4a16_linear": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
+                              _c_int, _vp, _c_size, _vp]),
+    "w4a8_quantize_act": (_c_int, [_vp, _c_int, _c_int, _c_int, _vp, _vp, _vp]),
+    "w4a8_workspace_bytes": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
+    "w4a8_linear": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
+                             _vp, _c_size, _vp]),
+    "w4_get_device_error": (_c_int, [_vp]),
+    "w4_error_string": (ctypes.c_char_p, [_c_int]),
+}
+EXPORTED = tuple(_SIGS)
+
+_lib = None
+_lock = threading.Lock()
+
+
+class W4Error(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        self.code = code
+        super().__init__(f"{fn} failed: {code} ({w4_error_string(code)})")
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Load libw4.so (built by __graft_entry__.build()); raises if missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(f"libw4.so is not built ({_LIB_PATH}); "
+                                   "run int4_weight_only_gb300.build.build()")
+            lib = ctypes.CDLL(_LIB_PATH)
+            for name, (res, args) in _SIGS.items():
+                f = getattr(lib, name)
+                f.restype, f.argtypes = res, args
+            _lib = lib
+    return _lib
+
+
+def w4_error_string(code: int) -> str:
+    return load().w4_error_string(int(code)).decode()
+
+
+def padded_k(K: int, group_size: int) -> int:
+    return -(-K // group_size) * group_size
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(t: torch.Tensor, stream=None):
+    if stream is None:
+        stream = torch.cuda.current_stream(t.device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t, dtype, shape, name):
+    if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _check(fn: str, rc: int):
+    if rc != 0:
+        raise W4Error(fn, rc)
+
+
+# ------------------------------------------------------------- workspace
+_ws = {}
+
+
+def _workspace(device: torch.device, nbytes: int) -> Optional[torch.Tensor]:
+    """A per-device zero-filled scratch buffer (grown on demand); the kernels
+    leave its counters at zero after each call."""
+    if nbytes == 0:
+        return None
+    idx = device.index if device.index is not None else torch.cuda.current_device()
+    buf = _ws.get(idx)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.zeros(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+        _ws[idx] = buf
+    return buf
+
+
+# ------------------------------------------------------------- entry points
+def w4_pack_rtn(W: torch.Tensor, group_size: int, symmetric: bool,
+                packed=None, scales=None, zeros=None, stream=None
+                ) -> Tuple[torch.Tensor, torch.Tensor, Optional[torch.Tensor]]:
+    """RTN INT4 quantize + pack W [N, K] fp32 -> (packed [N, Kp/2] u8,
+    scales [N, Ng] f32, zeros [N, Ng] u8 or None)."""
+    N, K = W.shape
+    _need(W, torch.float32, (N, K), "W")
+    Kp = padded_k(K, group_size)
+    Ng = Kp // group_size if group_size > 0 else 0
+    dev = W.device
+    if packed is None:
+        packed = torch.empty(N, Kp // 2, dtype=torch.uint8, device=dev)
+    if scales is None:
+        scales = torch.empty(N, Ng, dtype=torch.float32, device=dev)
+    if not symmetric and zeros is None:
+        zeros = torch.empty(N, Ng, dtype=torch.uint8, device=dev)
+    _need(packed, torch.uint8, (N, Kp // 2), "packed")
+    _need(scales, torch.float32, (N, Ng), "scales")
+    if zeros is not None:
+        _need(zeros, torch.uint8, (N, Ng), "zeros")
+    rc = load().w4_pack_rtn(_ptr(W), N, K, int(group_size), 1 if symmetric else 0,
+                            _ptr(packed), _ptr(scales), _ptr(zeros), _stream(W, stream))
+    _check("w4_pack_rtn", rc)
+    return packed, scales, zeros
+
+
+def w4a16_workspace_bytes(M: int, N: int, K: int, group_size: int) -> int:
+    return int(load().w4a16_workspace_bytes(M, N, K, group_size))
+
+
+def w4a8_workspace_bytes(M: int, N: int, K: int, group_size: int) -> int:
+    return int(load().w4a8_workspace_bytes(M, N, K, group_size))
+
+
+def w4a16_linear(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
+                 zeros: Optional[torch.Tensor], bias: Optional[torch.Tensor], N: int, K: int,
+                 group_size: int, y=None, workspace=None, stream=None) -> torch.Tensor:
+    """y [M, N] bf16 = x [M, K] bf16 . W_hat^T (+ bias)."""
+    M = x.shape[0]
+    _need(x, torch.bfloat16, (M, K), "x")
+    Kp = padded_k(K, group_size)
+    Ng = Kp // group_size
+    _need(packed, torch.uint8, (N, Kp // 2), "packed")
+    _need(scales, torch.float32, (N, Ng), "scales")
+    if zeros is not None:
+        _need(zeros, torch.uint8, (N, Ng), "zeros")
+    if bias is not None:
+        _need(bias, torch.float32, (N,), "bias")
+    if y is None:
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=x.device)
+    _need(y, torch.bfloat16, (M, N), "y")
+    lib = load()
+    if workspace is None:
+        workspace = _workspace(x.device, lib.w4a16_workspace_bytes(M, N, K, group_size))
+    wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.w4a16_linear(_ptr(x), _ptr(packed), _ptr(scales), _ptr(zeros), _ptr(bias),
+                          _ptr(y), M, N, K, int(group_size), 1 if zeros is None else 0,
+                          _ptr(workspace), wsb, _stream(x, stream))
+    _check("w4a16_linear", rc)
+    return y
+
+
+def w4a8_quantize_act(x: torch.Tensor, group_size: int, qx=None, sx=None, stream=None):
+    """Per-token INT8 activations: (qx [M, Kp] int8, sx [M] fp32)."""
+    M, K = x.shape
+    _need(x, torch.bfloat16, (M, K), "x")
+    Kp = padded_k(K, group_size)
+    if qx is None:
+        qx = torch.empty(M, Kp, dtype=torch.int8, device=x.device)
+    if sx is None:
+        sx = torch.empty(M, dtype=torch.float32, device=x.device)
+    _need(qx, torch.int8, (M, Kp), "qx")
+    _need(sx, torch.float32, (M,), "sx")
+    rc = load().w4a8_quantize_act(_ptr(x), M, K, int(group_size), _ptr(qx), _ptr(sx),
+                                  _stream(x, stream))
+    _check("w4a8_quantize_act", rc)
+    return qx, sx
+
+
+def w4a8_linear(qx: torch.Tensor, sx: torch.Tensor, packed: torch.Tensor,
+                w_scales: torch.Tensor, bias: Optional[torch.Tensor], N: int, K: int,
+                group_size: int, y=None, acc_out=None, want_acc: bool = False,
+                workspace=None, stream=None):
+    """(y [M, N] bf16, acc [M, N] int32 or None)."""
+    M, Kp = qx.shape
+    _need(qx, torch.int8, (M, padded_k(K, group_size)), "qx")
+    _need(sx, torch.float32, (M,), "sx")
+    _need(packed, torch.uint8, (N, Kp // 2), "packed")
+    if w_scales.dim() == 2:
+        w_scales = w_scales.reshape(-1)
+    _need(w_scales, torch.float32, (N,), "w_scales")
+    if bias is not None:
+        _need(bias, torch.float32, (N,), "bias")
+    if y is None:
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=qx.device)
+    _need(y, torch.bfloat16, (M, N), "y")
+    if acc_out is None and want_acc:
+        acc_out = torch.empty(M, N, dtype=torch.int32, device=qx.device)
+    if acc_out is not None:
+        _need(acc_out, torch.int32, (M, N), "acc_out")
+    lib = load()
+    if workspace is None:
+        workspace = _workspace(qx.device, lib.w4a8_workspace_bytes(M, N, K, group_size))
+    wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.w4a8_linear(_ptr(qx), _ptr(sx), _ptr(packed), _ptr(w_scales), _ptr(bias),
+                         _ptr(y), _ptr(acc_out), M, N, K, int(group_size), _ptr(workspace),
+                         wsb, _stream(qx, stream))
+    _check("w4a8_linear", rc)
+    return y, acc_out
+
+
+def w4_get_device_error(stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(load().w4_get_device_error(ctypes.c_void_p(s.cuda_stream)))

@@ -1,0 +1,260 @@
+// api.cu - the extern "C" entry points of libw4 (declared in include/w4.h):
+// argument checks on the host, kernel selection, tensor-map encoding, and
+// the device error flag.  No entry point allocates or frees device memory.
+#include "w4_internal.h"
+
+#include <cstring>
+#include <cudaTypedefs.h>
+#include <mutex>
+
+namespace w4 {
+
+__device__ int g_device_error;           // set by bounded waits that give up
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+int device_index() {
+    int d = 0;
+    if (cudaGetDevice(&d) != cudaSuccess) return -1;
+    return d;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+}  // namespace
+
+int current_sm_count() {
+    static int cache[kMaxDevices] = {0};
+    const int d = device_index();
+    if (d < 0) return 0;
+    if (d < kMaxDevices && cache[d] > 0) return cache[d];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d) != cudaSuccess) return 0;
+    if (d < kMaxDevices) cache[d] = n;
+    return n;
+}
+
+int* device_error_flag() {
+    static int* cache[kMaxDevices] = {nullptr};
+    const int d = device_index();
+    if (d < 0) return nullptr;
+    if (d < kMaxDevices && cache[d]) return cache[d];
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    if (d < kMaxDevices) cache[d] = static_cast<int*>(p);
+    return static_cast<int*>(p);
+}
+
+bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                    uint64_t dim0, uint64_t dim1, uint64_t row_stride_bytes,
+                    uint32_t box0, uint32_t box1, CUtensorMapSwizzle swizzle) {
+    auto fn = get_encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {dim0, dim1};
+    cuuint64_t strides[1] = {row_stride_bytes};
+    cuuint32_t box[2] = {box0, box1};
+    cuuint32_t estr[2] = {1, 1};
+    std::memset(map, 0, sizeof(*map));
+    return fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+namespace {
+
+int check_group(int K, int G) {
+    if (G <= 0 || (G % 32) != 0) return W4_ERR_UNSUPPORTED_GROUP;
+    if (K <= 0) return W4_ERR_INVALID_ARG;
+    return W4_OK;
+}
+
+long long padded_k(int K, int G) { return ((long long)K + G - 1) / G * G; }
+
+// Workspace layout: [tickets: NB ints, padded to 256 B][partials].
+int split_workspace(const GemvPlan& p, void* ws, size_t ws_bytes, int** tickets, void** part) {
+    *tickets = nullptr;
+    *part = nullptr;
+    if (p.S <= 1) return W4_OK;
+    if (!ws) return W4_ERR_WORKSPACE;
+    if (ws_bytes < p.ws_bytes) return W4_ERR_WORKSPACE;
+    if (!aligned16(ws)) return W4_ERR_MISALIGNED;
+    *tickets = static_cast<int*>(ws);
+    *part = static_cast<uint8_t*>(ws) + ((size_t)p.NB * 4 + 255) / 256 * 256;
+    return W4_OK;
+}
+
+}  // namespace
+}  // namespace w4
+
+using namespace w4;
+
+extern "C" {
+
+int w4_pack_rtn(const float* W, int N, int K, int group_size, int symmetric,
+                uint8_t* packed, float* scales, uint8_t* zeros, void* stream) {
+    if (!W || !packed || !scales) return W4_ERR_NULL_PTR;
+    if (symmetric && zeros) return W4_ERR_INVALID_ARG;
+    if (!symmetric && !zeros) return W4_ERR_NULL_PTR;
+    if (N <= 0) return W4_ERR_INVALID_ARG;
+    int rc = check_group(K, group_size);
+    if (rc) return rc;
+    if (padded_k(K, group_size) > 0x7fffffffLL) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(packed)) return W4_ERR_MISALIGNED;
+    if (!aligned4(W) || !aligned4(scales)) return W4_ERR_MISALIGNED;
+    return launch_pack_rtn(W, N, K, group_size, symmetric ? 1 : 0, packed, scales, zeros,
+                           static_cast<cudaStream_t>(stream));
+}
+
+size_t w4a16_workspace_bytes(int M, int N, int K, int group_size) {
+    if (M <= 0 || N <= 0 || check_group(K, group_size)) return 0;
+    const long long Kp = padded_k(K, group_size);
+    if (M <= 16) {
+        GemvPlan p;
+        if (!plan_gemv(M, N, (int)Kp, 2, current_sm_count(), &p)) return 0;
+        return p.ws_bytes;
+    }
+    return 0;
+}
+
+int w4a16_linear(const uint16_t* x, const uint8_t* packed, const float* scales,
+                 const uint8_t* zeros, const float* bias, uint16_t* y, int M, int N, int K,
+                 int group_size, int symmetric, void* workspace, size_t workspace_bytes,
+                 void* stream) {
+    if (!x || !packed || !scales || !y) return W4_ERR_NULL_PTR;
+    if (symmetric && zeros) return W4_ERR_INVALID_ARG;
+    if (!symmetric && !zeros) return W4_ERR_NULL_PTR;
+    if (M < 0 || N <= 0) return W4_ERR_INVALID_ARG;
+    int rc = check_group(K, group_size);
+    if (rc) return rc;
+    const long long Kp = padded_k(K, group_size);
+    if (Kp > 0x7fffffffLL) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(x) || !aligned16(packed)) return W4_ERR_MISALIGNED;
+    if (!aligned4(scales) || (bias && !aligned4(bias)) || (reinterpret_cast<uintptr_t>(y) & 1))
+        return W4_ERR_MISALIGNED;
+    if (M == 0) return W4_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (M > 16) return W4_ERR_UNSUPPORTED_SHAPE;
+
+    GemvPlan p;
+    if (!plan_gemv(M, N, (int)Kp, 2, current_sm_count(), &p)) return W4_ERR_UNSUPPORTED_SHAPE;
+    GemvArgs a{};
+    rc = split_workspace(p, workspace, workspace_bytes, &a.tickets, &a.partial);
+    if (rc) return rc;
+    CUtensorMap tm;
+    if (!encode_tmap_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, packed, (uint64_t)(Kp / 2),
+                        (uint64_t)N, (uint64_t)(Kp / 2), kGemvStageK / 2, kGemvRows,
+                        CU_TENSOR_MAP_SWIZZLE_128B))
+        return W4_ERR_CUDA;
+    a.x = x; a.scales = scales; a.zeros = zeros; a.bias = bias; a.y = y;
+    a.err = device_error_flag();
+    if (!a.err) return W4_ERR_CUDA;
+    a.M = M; a.N = N; a.K = K; a.Kp = (int)Kp; a.G = group_size; a.Ng = (int)(Kp / group_size);
+    a.nst = p.nst; a.S = p.S; a.spl = p.spl; a.units = p.units; a.XS = p.XS;
+    return launch_w4a16_gemv(tm, a, p, st);
+}
+
+int w4a8_quantize_act(const uint16_t* x, int M, int K, int group_size, int8_t* qx,
+                      float* sx, void* stream) {
+    if (!x || !qx || !sx) return W4_ERR_NULL_PTR;
+    if (M < 0) return W4_ERR_INVALID_ARG;
+    int rc = check_group(K, group_size);
+    if (rc) return rc;
+    const long long Kp = padded_k(K, group_size);
+    if (Kp > 0x7fffffffLL) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(qx) || !aligned4(sx) || (reinterpret_cast<uintptr_t>(x) & 1))
+        return W4_ERR_MISALIGNED;
+    if (M == 0) return W4_OK;
+    return launch_act_quant(x, M, K, (int)Kp, qx, sx, static_cast<cudaStream_t>(stream));
+}
+
+size_t w4a8_workspace_bytes(int M, int N, int K, int group_size) {
+    if (M <= 0 || M > 16 || N <= 0 || check_group(K, group_size)) return 0;
+    GemvPlan p;
+    if (!plan_gemv(M, N, (int)padded_k(K, group_size), 1, current_sm_count(), &p)) return 0;
+    return p.ws_bytes;
+}
+
+int w4a8_linear(const int8_t* qx, const float* sx, const uint8_t* packed,
+                const float* w_scales, const float* bias, uint16_t* y, int32_t* acc_out,
+                int M, int N, int K, int group_size, void* workspace, size_t workspace_bytes,
+                void* stream) {
+    if (!qx || !sx || !packed || !w_scales || !y) return W4_ERR_NULL_PTR;
+    if (M < 0 || N <= 0) return W4_ERR_INVALID_ARG;
+    int rc = check_group(K, group_size);
+    if (rc) return rc;
+    const long long Kp = padded_k(K, group_size);
+    if (Kp != group_size) return W4_ERR_UNSUPPORTED_GROUP;
+    if (Kp > W4_W4A8_MAX_KP) return W4_ERR_K_TOO_LARGE;
+    if (!aligned16(qx) || !aligned16(packed)) return W4_ERR_MISALIGNED;
+    if (!aligned4(sx) || !aligned4(w_scales) || (bias && !aligned4(bias)) ||
+        (acc_out && !aligned4(acc_out)) || (reinterpret_cast<uintptr_t>(y) & 1))
+        return W4_ERR_MISALIGNED;
+    if (M == 0) return W4_OK;
+    if (M > 16) return W4_ERR_UNSUPPORTED_SHAPE;
+    GemvPlan p;
+    if (!plan_gemv(M, N, (int)Kp, 1, current_sm_count(), &p)) return W4_ERR_UNSUPPORTED_SHAPE;
+    GemvArgs a{};
+    rc = split_workspace(p, workspace, workspace_bytes, &a.tickets, &a.partial);
+    if (rc) return rc;
+    CUtensorMap tm;
+    if (!encode_tmap_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, packed, (uint64_t)(Kp / 2),
+                        (uint64_t)N, (uint64_t)(Kp / 2), kGemvStageK / 2, kGemvRows,
+                        CU_TENSOR_MAP_SWIZZLE_128B))
+        return W4_ERR_CUDA;
+    a.x = qx; a.sx = sx; a.scales = w_scales; a.bias = bias; a.y = y; a.acc_out = acc_out;
+    a.err = device_error_flag();
+    if (!a.err) return W4_ERR_CUDA;
+    a.M = M; a.N = N; a.K = K; a.Kp = (int)Kp; a.G = group_size; a.Ng = 1;
+    a.nst = p.nst; a.S = p.S; a.spl = p.spl; a.units = p.units; a.XS = p.XS;
+    return launch_w4a8_gemv(tm, a, p, static_cast<cudaStream_t>(stream));
+}
+
+int w4_get_device_error(void* stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return W4_ERR_CUDA;
+    int* flag = device_error_flag();
+    if (!flag) return W4_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, flag, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return W4_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpy(flag, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+        return W4_ERR_CUDA;
+    return v;
+}
+
+const char* w4_error_string(int code) {
+    switch (code) {
+        case W4_OK: return "ok";
+        case W4_ERR_INVALID_ARG: return "invalid argument (size or flag out of range)";
+        case W4_ERR_NULL_PTR: return "a required pointer is NULL";
+        case W4_ERR_MISALIGNED: return "pointer misaligned (packed, x and qx need 16 bytes)";
+        case W4_ERR_UNSUPPORTED_GROUP:
+            return "group_size must be a positive multiple of 32 (W4A8: one group per row)";
+        case W4_ERR_K_TOO_LARGE: return "padded K exceeds the int32 accumulator bound";
+        case W4_ERR_WORKSPACE: return "workspace missing or smaller than required";
+        case W4_ERR_CUDA: return "CUDA runtime error";
+        case W4_ERR_UNSUPPORTED_SHAPE: return "shape not supported by the kernels";
+        case W4_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait timed out";
+        default: return "unknown error code";
+    }
+}
+
+}  // extern "C"

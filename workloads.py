@@ -157,3 +157,21 @@ WORKLOADS = {
     "prefill_7b": prefill_7b,
     "w4a8_7b": w4a8_7b,
 }
+
+
+def make_random_format(N: int, K: int, group_size: int, symmetric: bool, seed: int):
+    """Arbitrary valid packed weights (every nibble value 0..15 occurs,
+    including the code 0 that round-to-nearest with s = max/7 never emits),
+    positive fp32 scales and, for asymmetric groups, zero points in
+    [0, 15].  Returns (packed uint8 [N, Kp/2], scales fp32 [N, Ng],
+    zeros uint8 [N, Ng] or None) as CPU tensors."""
+    Kp = -(-K // group_size) * group_size
+    Ng = Kp // group_size
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    packed = torch.randint(0, 256, (N, Kp // 2), generator=g, dtype=torch.int64).to(torch.uint8)
+    scales = (torch.rand(N, Ng, generator=g, dtype=torch.float32) * 0.01 + 1e-4)
+    zeros = None
+    if not symmetric:
+        zeros = torch.randint(0, 16, (N, Ng), generator=g, dtype=torch.int64).to(torch.uint8)
+    return packed, scales, zeros
