@@ -1,0 +1,466 @@
+#!/usr/bin/env python
+"""Benchmark of the INT4 weight-only linear layer on GB300.
+
+A step is one decode pass over the four 7B projections at M=1 (fused QKV
+4608x3584, O 3584x3584, fused gate|up 37888x3584, down 3584x18944; G=128,
+symmetric), each a w4a16_linear call.  `value` is the algorithmic bytes of a
+step (packed weights + scales + activations + outputs) divided by the device
+time of a step, summed over ranks (each rank runs its own replica: weak
+scaling, no collective on the data path).  The same run also measures the
+other workloads (prefill GEMM in TFLOP/s, the W4A8 integer path, batched
+asymmetric decode), reported as sub-objects of the one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as WL  # noqa: E402
+
+METRIC = "W4A16 GEMV HBM GB/s (M=1) & prefill TFLOP/s (M=2048) vs GB300 roofline"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_BYTES = 129 * 1024 * 1024
+
+
+# ---------------------------------------------------------------- helpers
+def algorithmic_bytes(lin: WL.Linear, M: int) -> int:
+    """Bytes a linear must move at least once: packed codes, scales, zero
+    points (asymmetric), activations and outputs (+ bias)."""
+    Kp = -(-lin.K // lin.group_size) * lin.group_size
+    Ng = Kp // lin.group_size
+    b = lin.N * Kp // 2 + 4 * lin.N * Ng
+    if not lin.symmetric:
+        b += lin.N * Ng
+    if lin.kind == "w4a8":
+        b += M * Kp + 4 * M
+    else:
+        b += 2 * M * lin.K
+    b += 2 * M * lin.N
+    if lin.bias:
+        b += 4 * lin.N
+    return b
+
+
+def load_peaks():
+    """(hbm GB/s, bf16 burst TFLOP/s, bf16 sustained TFLOP/s, kind)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return (float(d["hbm_gbs"]), float(d["bf16_tflops"]),
+                float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured")
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def source_digest(files) -> str:
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+DECODE_SOURCES = ["int4_weight_only_gb300/csrc/gemv.cu",
+                  "int4_weight_only_gb300/csrc/w4_device.cuh",
+                  "int4_weight_only_gb300/csrc/w4_internal.h"]
+
+
+def recorded_traffic(kernel: str, digest: str):
+    """DRAM bytes from a committed ncu summary (profiles/traffic.json), if
+    it was taken on the current kernel source; otherwise None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        e = d.get(kernel)
+        if e and e.get("source_digest") == digest:
+            return e
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            uuid = str(torch.cuda.get_device_properties(self.dev).uuid)
+            sel = ["-i", uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"]
+        except Exception:
+            sel = []
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "50"] + sel
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        time.sleep(0.15)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[2:6]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def make_graph(fn, nsteps: int):
+    """Capture `nsteps` calls fn(i) into one CUDA graph."""
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s, capture_error_mode="thread_local"):
+            for i in range(nsteps):
+                fn(i)
+    torch.cuda.current_stream().wait_stream(s)
+    return g
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world <= 1:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def time_graph_steps(step_fn, K, R, world):
+    """Replay graphs holding exactly K calls step_fn(i); returns seconds."""
+    g_full = make_graph(step_fn, R)
+    g_rem = make_graph(step_fn, K % R) if K % R else None
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0.record()
+    for _ in range(K // R):
+        g_full.replay()
+    if g_rem is not None:
+        g_rem.replay()
+    ev1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    return ev0.elapsed_time(ev1) / 1e3
+
+
+# ---------------------------------------------------------------- our arm
+class DecodeSet:
+    """Device-resident rotated copies of a set of linears (M <= 16) so that a
+    sequence of steps never re-reads weights from L2."""
+
+    def __init__(self, w4, lins, M, min_bytes):
+        self.w4, self.lins, self.M = w4, lins, M
+        self.bytes_step = sum(algorithmic_bytes(l, M) for l in lins)
+        self.R = max(2, math.ceil(min_bytes / self.bytes_step))
+        base = []
+        for lin in lins:
+            inp = WL.make_inputs(lin, M)
+            p, s, z = w4.w4_pack_rtn(inp.W.cuda(), lin.group_size, lin.symmetric)
+            b = inp.bias.cuda() if inp.bias is not None else None
+            base.append((p, s, z, b))
+        torch.cuda.synchronize()
+        self.copies = []
+        for r in range(self.R):
+            cp = []
+            for li, (p, s, z, b) in enumerate(base):
+                lin = lins[li]
+                xr = WL.make_activations(lin.K, M, seed=10_000 + 97 * r + li).cuda()
+                cp.append(dict(p=p.clone(), s=s.clone(), z=None if z is None else z.clone(),
+                               b=b, x=xr,
+                               y=torch.empty(M, lin.N, dtype=torch.bfloat16, device="cuda")))
+            self.copies.append(cp)
+        del base
+        torch.cuda.synchronize()
+
+    def call(self, li, r):
+        lin, d = self.lins[li], self.copies[r % self.R][li]
+        self.w4.w4a16_linear(d["x"], d["p"], d["s"], d["z"], d["b"], lin.N, lin.K,
+                             lin.group_size, y=d["y"])
+
+    def step(self, i):
+        for li in range(len(self.lins)):
+            self.call(li, i)
+
+
+def measure_linears(ds: DecodeSet, reps: int):
+    out = []
+    for li, lin in enumerate(ds.lins):
+        n = reps * ds.R
+        sec = time_graph_steps(lambda i, li=li: ds.call(li, i), n, ds.R, 1)
+        us = sec / n * 1e6
+        b = algorithmic_bytes(lin, ds.M)
+        out.append({"name": lin.name, "N": lin.N, "K": lin.K, "M": ds.M,
+                    "group_size": lin.group_size, "symmetric": lin.symmetric,
+                    "us": round(us, 3), "GB/s": round(b / (us * 1e-6) / 1e9, 1)})
+    return out
+
+
+def measure_e2e(w4, ds: DecodeSet, K: int):
+    """Same metric through the public API, per step: pinned host activations
+    copied in, four w4a16_linear calls, outputs copied back to pinned host
+    memory; no graphs, host overhead included."""
+    hx = [d["x"].cpu().pin_memory() for d in ds.copies[0]]
+    hy = [torch.empty(d["y"].shape, dtype=torch.bfloat16).pin_memory() for d in ds.copies[0]]
+    h2d = sum(h.numel() * h.element_size() for h in hx)
+    d2h = sum(h.numel() * h.element_size() for h in hy)
+
+    def step(i):
+        c = ds.copies[i % ds.R]
+        for lin, d, h, o in zip(ds.lins, c, hx, hy):
+            d["x"].copy_(h, non_blocking=True)
+            w4.w4a16_linear(d["x"], d["p"], d["s"], d["z"], d["b"], lin.N, lin.K,
+                            lin.group_size, y=d["y"])
+            o.copy_(d["y"], non_blocking=True)
+
+    for i in range(5):
+        step(i)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(K):
+        step(i)
+    torch.cuda.synchronize()
+    return time.perf_counter() - t0, h2d, d2h
+
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def _oracle_row_sample(lins, frac, seed):
+    """Oracle packing of a fixed random row sample of each linear (RTN is
+    row-independent, so the sampled rows pack exactly as in the full
+    matrix)."""
+    import oracle as O
+    out = []
+    rng = np.random.default_rng(seed)
+    for lin in lins:
+        inp = WL.make_inputs(lin)
+        n = max(1, int(round(lin.N * frac)))
+        rows = np.sort(rng.choice(lin.N, n, replace=False))
+        W = inp.W.numpy()[rows]
+        out.append((lin, inp.x, O.pack_rtn(W, lin.group_size, lin.symmetric),
+                    algorithmic_bytes(lin, 1) * n / lin.N))
+    return out
+
+
+def _oracle_step(sample):
+    import oracle as O
+    by = 0.0
+    for lin, x, (op, os_, oz), b in sample:
+        O.w4a16_linear(x, op, os_, oz, None, lin.K, lin.group_size)
+        by += b
+    return by
+
+
+def cpu_baseline_decode(lins, frac=1 / 16, budget_s=12.0):
+    """The oracle as it stands, timed on a bounded sample of the step: the
+    four decode linears at M=1 restricted to a fixed 1/16 row sample
+    (oracle packing outside the timing; dequantize + fp64 matvec inside)."""
+    sample = _oracle_row_sample(lins, frac, seed=7)
+    by, t, n = 0.0, 0.0, 0
+    while t < budget_s and n < 50:
+        t0 = time.perf_counter()
+        by += _oracle_step(sample)
+        t += time.perf_counter() - t0
+        n += 1
+    return {"value": round(by / t / 1e9, 4), "unit": "GB/s", "cores": blas_threads(),
+            "kind": "oracle",
+            "sample": f"{n} passes of oracle w4a16_linear (numpy, fp64 dequantize + matvec) over "
+                      f"a fixed {frac:.4f} row sample of each of the four 7B decode linears, "
+                      f"M=1; {t:.1f} s"}
+
+
+def run_ours(args, world, rank):
+    import int4_weight_only_gb300 as w4
+    from int4_weight_only_gb300 import build as b
+    b.build()
+    w4.load()
+    dev = torch.cuda.current_device()
+    hbm, bf16, bf16_sus, peak_kind = load_peaks()
+
+    lins = WL.decode_7b(1)
+    ds = DecodeSet(w4, lins, 1, min_bytes=3 * L2_BYTES)
+    for i in range(max(args.warmup, 3)):
+        ds.step(i)
+    torch.cuda.synchronize()
+    with ClockSampler(dev) as clk:
+        sec = time_graph_steps(ds.step, args.steps, ds.R, world)
+    sec = max_over_ranks(sec, world)
+    value = ds.bytes_step * args.steps * world / sec / 1e9
+    res = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(sec / args.steps * 1e3, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded Gaussian weights and activations, 7B decode shapes)",
+        "config": {
+            "workload": "decode_7b M=1: qkv 4608x3584, o 3584x3584, gate_up 37888x3584, "
+                        "down 3584x18944; int4 G=128 symmetric; bf16 activations",
+            "M": 1, "bytes_per_step": ds.bytes_step,
+            "l2": f"rotating {ds.R} weight/activation copies ({ds.R * ds.bytes_step / 1e6:.0f} MB "
+                  f"> 2x L2) so every step reads cold HBM",
+            "timing": "CUDA graphs of the w4a16_linear calls, CUDA events, max over ranks",
+            "parallelism": f"replicas x{world}",
+        },
+        "gpu_launches": 4 * args.steps,
+        "clocks": clk.summary(),
+    }
+    tr = recorded_traffic("k_w4a16_gemv", source_digest(DECODE_SOURCES))
+    res["roofline"] = {
+        "kernel": "k_w4a16_gemv (all four launches of a step)", "bound": "hbm",
+        "achieved": round(value / world, 1), "peak": hbm, "unit": "GB/s",
+        "frac": round(value / world / hbm, 4), "peak_kind": f"{peak_kind} hbm_gbs",
+        "traffic": None if tr is None else tr["dram_bytes_per_step"],
+        "algorithmic_bytes_per_step": ds.bytes_step,
+    }
+    res["per_linear"] = measure_linears(ds, reps=200)
+    ke = min(args.steps, 2000)
+    dt, h2d, d2h = measure_e2e(w4, ds, ke)
+    dt = max_over_ranks(dt, world)
+    res["e2e"] = {"value": round(ds.bytes_step * ke * world / dt / 1e9, 1), "unit": "GB/s",
+                  "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                  "ms_per_step": round(dt / ke * 1e3, 4), "steps": ke}
+    del ds
+    torch.cuda.empty_cache()
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline_decode(lins)
+    return res
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args):
+    """The CPU oracle, as it stands, on the same workload and metric: each
+    step runs the four decode linears at M=1 on a fixed row sample, sized so
+    that warm-up plus timed steps take about two minutes."""
+    lins = WL.decode_7b(1)
+    total = args.steps + args.warmup
+    probe = _oracle_row_sample(lins, 1 / 256, seed=3)
+    t0 = time.perf_counter()
+    _oracle_step(probe)
+    t1 = max(time.perf_counter() - t0, 1e-4)
+    frac = min(1 / 8, (1 / 256) * (120.0 / total) / t1)
+    frac = max(frac, 1.0 / min(l.N for l in lins))
+    sample = _oracle_row_sample(lins, frac, seed=5)
+    for _ in range(args.warmup):
+        _oracle_step(sample)
+    t0 = time.perf_counter()
+    by = 0.0
+    for _ in range(args.steps):
+        by += _oracle_step(sample)
+    dt = time.perf_counter() - t0
+    v = by / dt / 1e9
+    desc = (f"oracle w4a16_linear (numpy fp64) on a fixed {frac:.5f} row sample of each of the "
+            f"four 7B decode linears per step, M=1")
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "decode_7b M=1: qkv 4608x3584, o 3584x3584, gate_up "
+                                   "37888x3584, down 3584x18944; int4 G=128 symmetric "
+                                   "(row sample per step)", "M": 1},
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": blas_threads(),
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    res = run_ours(args, world, rank)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
