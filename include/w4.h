@@ -63,6 +63,12 @@ extern "C" {
 #define W4_ERR_CUDA                -7  /* a CUDA runtime call failed          */
 #define W4_ERR_UNSUPPORTED_SHAPE   -8  /* shape outside what a kernel takes   */
 #define W4_ERR_DEVICE_TIMEOUT      -9  /* a kernel's bounded wait ran out     */
+#define W4_ERR_SCRATCH_LIMIT      -10  /* shape needs more split-K scratch than
+                                          W4_NOALLOC_SCRATCH_BYTES            */
+
+/* Size of the library's built-in split-K scratch used by
+ * w4a16_linear_noalloc (4 MiB, held by every GPU that loads the library).  */
+#define W4_NOALLOC_SCRATCH_BYTES (4 << 20)
 
 /* Largest padded K accepted by the W4A8 path: the kernels accumulate
  * code (0..15) x q_x (-127..127) products in int32, so Kp * 15 * 127 must
@@ -87,6 +93,32 @@ extern "C" {
  * ------------------------------------------------------------------------- */
 W4_API int w4_pack_rtn(const float* W, int N, int K, int group_size, int symmetric,
                 uint8_t* packed, float* scales, uint8_t* zeros, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * w4a16_linear_noalloc - w4a16_linear for callers that cannot allocate
+ * device memory: a plugin that is handed only its input and output
+ * buffers, or a runtime that forbids cudaMalloc after start-up (it can
+ * synchronize the device and can fail under a fixed memory budget).  The
+ * pages have no counterpart; this is a library convenience.
+ *
+ *  Same arguments and results as w4a16_linear with M <= 16 (the decode
+ *  kernel), but no workspace argument: split-K partial sums and arrival
+ *  counters live in a W4_NOALLOC_SCRATCH_BYTES array inside the library.
+ *  Shapes whose split needs more scratch than that return
+ *  W4_ERR_SCRATCH_LIMIT before anything is enqueued; M > 16 returns
+ *  W4_ERR_UNSUPPORTED_SHAPE.  Nothing is allocated: no cudaMalloc, no
+ *  cudaFree.
+ *  The first call on a device looks up the array's device address (with
+ *  that device current); make that first call before any stream capture.
+ *  Each call clears the counters on `stream` before its kernel.  All calls
+ *  share the one array and it keeps the previous call's contents, so calls
+ *  that overlap on the GPU (different streams or threads) race and must be
+ *  serialized by the caller.
+ * ------------------------------------------------------------------------- */
+W4_API int w4a16_linear_noalloc(const uint16_t* x, const uint8_t* packed,
+                                const float* scales, const uint8_t* zeros,
+                                const float* bias, uint16_t* y, int M, int N, int K,
+                                int group_size, int symmetric, void* stream);
 
 /* ---------------------------------------------------------------------------
  * w4a16_workspace_bytes - bytes of device workspace w4a16_linear needs for

@@ -17,6 +17,8 @@ _c_int, _c_size, _vp = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
 _SIGS = {
     "w4_pack_rtn": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _vp, _vp]),
     "w4a16_workspace_bytes": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
+    "w4a16_linear_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
+                                      _c_int, _c_int, _vp]),
     "w4a16_linear": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
                               _c_int, _vp, _c_size, _vp]),
     "w4a8_quantize_act": (_c_int, [_vp, _c_int, _c_int, _c_int, _vp, _vp, _vp]),
@@ -171,6 +173,32 @@ def w4a16_linear(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
                           _ptr(y), M, N, K, int(group_size), 1 if zeros is None else 0,
                           _ptr(workspace), wsb, _stream(x, stream))
     _check("w4a16_linear", rc)
+    return y
+
+
+def w4a16_linear_noalloc(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
+                         zeros: Optional[torch.Tensor], bias: Optional[torch.Tensor], N: int,
+                         K: int, group_size: int, y=None, stream=None) -> torch.Tensor:
+    """w4a16_linear (M <= 16) with the library's built-in split-K scratch;
+    for callers that cannot allocate device memory.  Calls must not overlap
+    on the GPU."""
+    M = x.shape[0]
+    _need(x, torch.bfloat16, (M, K), "x")
+    Kp = padded_k(K, group_size)
+    Ng = Kp // group_size
+    _need(packed, torch.uint8, (N, Kp // 2), "packed")
+    _need(scales, torch.float32, (N, Ng), "scales")
+    if zeros is not None:
+        _need(zeros, torch.uint8, (N, Ng), "zeros")
+    if bias is not None:
+        _need(bias, torch.float32, (N,), "bias")
+    if y is None:
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=x.device)
+    _need(y, torch.bfloat16, (M, N), "y")
+    rc = load().w4a16_linear_noalloc(_ptr(x), _ptr(packed), _ptr(scales), _ptr(zeros),
+                                     _ptr(bias), _ptr(y), M, N, K, int(group_size),
+                                     1 if zeros is None else 0, _stream(x, stream))
+    _check("w4a16_linear_noalloc", rc)
     return y
 
 

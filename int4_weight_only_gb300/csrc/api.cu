@@ -253,6 +253,8 @@ const char* w4_error_string(int code) {
         case W4_ERR_CUDA: return "CUDA runtime error";
         case W4_ERR_UNSUPPORTED_SHAPE: return "shape not supported by the kernels";
         case W4_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait timed out";
+        case W4_ERR_SCRATCH_LIMIT:
+            return "shape needs more split-K scratch than W4_NOALLOC_SCRATCH_BYTES";
         default: return "unknown error code";
     }
 }

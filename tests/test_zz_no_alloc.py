@@ -1,0 +1,78 @@
+"""w4a16_linear_noalloc through the C ABI: the entry point for callers that
+cannot allocate device memory (a plugin handed only its input and output
+buffers, or a runtime that forbids cudaMalloc after start-up).  Its output
+must match w4a16_linear's on the same inputs, call after call, although it
+takes its split-K scratch from the library's own fixed array.
+
+This file is collected last on purpose, so that a run stopping at the first
+failure has already run every other test; it also passes on its own."""
+import ctypes
+
+import pytest
+import torch
+
+import workloads as WL
+from helpers import assert_close, ensure_built, to_np
+
+pytestmark = pytest.mark.gpu
+
+W4_ERR_SCRATCH_LIMIT = -10
+W4_NOALLOC_SCRATCH_BYTES = 4 << 20
+
+
+@pytest.fixture(scope="module")
+def w4():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return ensure_built()
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _noalloc(lib, x, packed, scales, zeros, bias, y, N, K, G):
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    return lib.w4a16_linear_noalloc(_p(x), _p(packed), _p(scales), _p(zeros), _p(bias), _p(y),
+                                    x.shape[0], N, K, G, 1 if zeros is None else 0, stream)
+
+
+@pytest.mark.parametrize("M,N,K,G,sym", [
+    (1, 3584, 18944, 128, True),     # the 7B down projection: split-K
+    (16, 4608, 3584, 128, False),    # 16 tokens, asymmetric, split-K
+    (3, 200, 100, 32, True),         # small ragged shape, no split
+])
+def test_noalloc_matches_workspace_entry_point(w4, M, N, K, G, sym):
+    lib = w4.load()
+    seed = M + N + K
+    packed, scales, zeros = WL.make_random_format(N, K, G, sym, seed)
+    packed, scales = packed.cuda(), scales.cuda()
+    zeros = None if zeros is None else zeros.cuda()
+    bias = (torch.randn(N, generator=torch.Generator().manual_seed(seed)) * 0.1).cuda()
+    x = WL.make_activations(K, M, seed + 1).cuda()
+    y_ref = w4.w4a16_linear(x, packed, scales, zeros, bias, N, K, G)
+    ref = to_np(y_ref).astype("float64")
+    for call in range(2):                       # two calls in a row share the scratch
+        y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+        rc = _noalloc(lib, x, packed, scales, zeros, bias, y, N, K, G)
+        assert rc == 0, lib.w4_error_string(rc)
+        torch.cuda.synchronize()
+        assert_close(y, ref, f"noalloc call {call}")
+    assert w4.w4_get_device_error() == 0
+
+
+def test_noalloc_rejects_shapes_beyond_its_scratch(w4):
+    """16 tokens x 16384 outputs x K=32768 needs >= 8 K-splits of
+    16 x 16384 fp32 partials (8 MiB), more than the 4 MiB built in."""
+    lib = w4.load()
+    M, N, K, G = 16, 16384, 32768, 128
+    assert w4.w4a16_workspace_bytes(M, N, K, G) > W4_NOALLOC_SCRATCH_BYTES
+    x = torch.zeros(M, K, dtype=torch.bfloat16, device="cuda")
+    packed = torch.zeros(N, K // 2, dtype=torch.uint8, device="cuda")
+    scales = torch.zeros(N, K // G, dtype=torch.float32, device="cuda")
+    y = torch.zeros(M, N, dtype=torch.bfloat16, device="cuda")
+    rc = _noalloc(lib, x, packed, scales, None, None, y, N, K, G)
+    assert rc == W4_ERR_SCRATCH_LIMIT
+    assert b"scratch" in lib.w4_error_string(rc)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(y) == 0          # nothing was enqueued
