@@ -150,7 +150,13 @@ int w4a16_linear(const uint16_t* x, const uint8_t* packed, const float* scales,
         return W4_ERR_MISALIGNED;
     if (M == 0) return W4_OK;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (M > 16) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (M > 16) {
+        if (K % 8 != 0) return W4_ERR_UNSUPPORTED_SHAPE;
+        int* err = device_error_flag();
+        if (!err) return W4_ERR_CUDA;
+        return launch_w4a16_gemm(x, packed, scales, zeros, bias, y, M, N, K, (int)Kp,
+                                 group_size, err, current_sm_count(), st);
+    }
 
     GemvPlan p;
     if (!plan_gemv(M, N, (int)Kp, 2, current_sm_count(), &p)) return W4_ERR_UNSUPPORTED_SHAPE;

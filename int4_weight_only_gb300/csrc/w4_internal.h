@@ -63,6 +63,12 @@ int launch_w4a16_gemv(const CUtensorMap& tmW, const GemvArgs& a, const GemvPlan&
 int launch_w4a8_gemv(const CUtensorMap& tmW, const GemvArgs& a, const GemvPlan& p,
                      cudaStream_t stream);
 
+// ---------------------------------------------------------------- prefill
+// Tensor-core kernel for M > 16 (requires K % 8 == 0 and 16-byte aligned x).
+int launch_w4a16_gemm(const uint16_t* x, const uint8_t* packed, const float* scales,
+                      const uint8_t* zeros, const float* bias, uint16_t* y, int M, int N, int K,
+                      int Kp, int G, int* err, int sm_count, cudaStream_t stream);
+
 // ---------------------------------------------------------------- others
 int launch_pack_rtn(const float* W, int N, int K, int G, int symmetric,
                     uint8_t* packed, float* scales, uint8_t* zeros,
