@@ -342,6 +342,109 @@ def cpu_baseline_decode(lins, frac=1 / 16, budget_s=12.0):
                       f"M=1; {t:.1f} s"}
 
 
+def measure_prefill(w4, M, bf16_peak, peak_kind, reps=20):
+    """Prefill GEMM at the 7B MLP shapes, TFLOP/s = 2*M*N*K / time."""
+    lins = WL.prefill_7b(M)
+    ds = DecodeSet(w4, lins, M, min_bytes=2 * L2_BYTES)
+    for i in range(3):
+        ds.step(i)
+    torch.cuda.synchronize()
+    out, tot_f, tot_s = [], 0.0, 0.0
+    for li, lin in enumerate(lins):
+        n = reps * ds.R
+        sec = time_graph_steps(lambda i, li=li: ds.call(li, i), n, ds.R, 1) / n
+        fl = 2.0 * M * lin.N * lin.K
+        tot_f += fl
+        tot_s += sec
+        out.append({"name": lin.name, "M": M, "N": lin.N, "K": lin.K, "us": round(sec * 1e6, 2),
+                    "TFLOP/s": round(fl / sec / 1e12, 1)})
+    del ds
+    torch.cuda.empty_cache()
+    tf = tot_f / tot_s / 1e12
+    return {"M": M, "value": round(tf, 1), "unit": "TFLOP/s", "per_linear": out,
+            "roofline": {"kernel": "k_w4a16_gemm_tc", "bound": "tensor", "achieved": round(tf, 1),
+                         "peak": bf16_peak, "unit": "TFLOP/s", "frac": round(tf / bf16_peak, 4),
+                         "peak_kind": f"{peak_kind} bf16_tflops (burst, kernel timed alone)",
+                         "traffic": None}}
+
+
+class W4A8Set:
+    """Rotated copies of the W4A8 linears: per call, dynamic INT8 activation
+    quantization then the integer GEMV."""
+
+    def __init__(self, w4, lins, min_bytes):
+        self.w4, self.lins = w4, lins
+        self.bytes_lin = [algorithmic_bytes(l, 1) for l in lins]
+        self.R = max(2, math.ceil(min_bytes / sum(self.bytes_lin)))
+        self.copies = []
+        base = []
+        for lin in lins:
+            inp = WL.make_inputs(lin)
+            p, sc, _ = w4.w4_pack_rtn(inp.W.cuda(), lin.group_size, True)
+            base.append((p, sc, inp.bias.cuda() if inp.bias is not None else None))
+        for r in range(self.R):
+            cp = []
+            for li, (p, sc, b) in enumerate(base):
+                lin = lins[li]
+                x = WL.make_activations(lin.K, 1, seed=20_000 + 31 * r + li,
+                                        outlier_frac=lin.x_outlier_frac).cuda()
+                qx, sx = w4.w4a8_quantize_act(x, lin.group_size)
+                cp.append(dict(p=p.clone(), s=sc.clone(), b=b, x=x, qx=qx, sx=sx,
+                               y=torch.empty(1, lin.N, dtype=torch.bfloat16, device="cuda")))
+            self.copies.append(cp)
+        torch.cuda.synchronize()
+
+    def call(self, li, r, quant=True):
+        lin, d = self.lins[li], self.copies[r % self.R][li]
+        if quant:
+            self.w4.w4a8_quantize_act(d["x"], lin.group_size, qx=d["qx"], sx=d["sx"])
+        self.w4.w4a8_linear(d["qx"], d["sx"], d["p"], d["s"], d["b"], lin.N, lin.K,
+                            lin.group_size, y=d["y"])
+
+
+def measure_w4a8(w4, hbm, reps=200):
+    """W4A8 linears at M=1: integer GEMV alone (GB/s) and quantize + GEMV."""
+    lins = WL.w4a8_7b()
+    ws = W4A8Set(w4, lins, min_bytes=3 * L2_BYTES)
+    out = []
+    for li, lin in enumerate(lins):
+        n = reps * ws.R
+        for q in (False, True):
+            ws.call(li, 0, q)
+        t_lin = time_graph_steps(lambda i, li=li: ws.call(li, i, False), n, ws.R, 1) / n
+        t_all = time_graph_steps(lambda i, li=li: ws.call(li, i, True), n, ws.R, 1) / n
+        b = ws.bytes_lin[li]
+        out.append({"name": lin.name, "N": lin.N, "K": lin.K, "Kp": lin.group_size,
+                    "linear_us": round(t_lin * 1e6, 3), "linear_GB/s": round(b / t_lin / 1e9, 1),
+                    "quant+linear_us": round(t_all * 1e6, 3)})
+    tb = sum(ws.bytes_lin)
+    tt = sum(o["linear_us"] for o in out) * 1e-6
+    del ws
+    torch.cuda.empty_cache()
+    v = tb / tt / 1e9
+    return {"value": round(v, 1), "unit": "GB/s", "per_linear": out,
+            "roofline": {"kernel": "k_w4a8_gemv", "bound": "hbm", "achieved": round(v, 1),
+                         "peak": hbm, "unit": "GB/s", "frac": round(v / hbm, 4)}}
+
+
+def measure_decode_12b(w4, hbm, reps=100):
+    """Batched asymmetric G=32 decode at 12B-class shapes, M in {1,4,8,16}."""
+    out = []
+    for M in (1, 4, 8, 16):
+        lins = WL.decode_12b(M)
+        ds = DecodeSet(w4, lins, M, min_bytes=3 * L2_BYTES)
+        ds.step(0)
+        torch.cuda.synchronize()
+        per = measure_linears(ds, reps)
+        tb = sum(algorithmic_bytes(l, M) for l in lins)
+        tt = sum(p["us"] for p in per) * 1e-6
+        out.append({"M": M, "GB/s": round(tb / tt / 1e9, 1), "frac": round(tb / tt / 1e9 / hbm, 4),
+                    "per_linear": per})
+        del ds
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, world, rank):
     import int4_weight_only_gb300 as w4
     from int4_weight_only_gb300 import build as b
@@ -394,6 +497,10 @@ def run_ours(args, world, rank):
                   "ms_per_step": round(dt / ke * 1e3, 4), "steps": ke}
     del ds
     torch.cuda.empty_cache()
+    if not args.decode_only:
+        res["prefill"] = [measure_prefill(w4, M, bf16, peak_kind) for M in (2048, 512)]
+        res["w4a8"] = measure_w4a8(w4, hbm)
+        res["decode_12b"] = measure_decode_12b(w4, hbm)
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline_decode(lins)
     return res
@@ -437,6 +544,29 @@ def run_reference(args):
             "gpu_launches": 0}
 
 
+def run_case(args):
+    """A few calls of one named linear: the small command profilers run."""
+    import int4_weight_only_gb300 as w4
+    from int4_weight_only_gb300 import build as b
+    b.build()
+    allw = (WL.tiny() + WL.decode_7b(args.M) + WL.decode_12b(args.M) + WL.prefill_7b(args.M)
+            + WL.w4a8_7b())
+    lin = next(l for l in allw if l.name.startswith(args.case))
+    inp = WL.make_inputs(lin, args.M)
+    p, sc, z = w4.w4_pack_rtn(inp.W.cuda(), lin.group_size, lin.symmetric)
+    x = inp.x.cuda()
+    bias = inp.bias.cuda() if inp.bias is not None else None
+    for _ in range(args.reps):
+        if lin.kind == "w4a8":
+            qx, sx = w4.w4a8_quantize_act(x, lin.group_size)
+            w4.w4a8_linear(qx, sx, p, sc, bias, lin.N, lin.K, lin.group_size)
+        else:
+            w4.w4a16_linear(x, p, sc, z, bias, lin.N, lin.K, lin.group_size)
+    torch.cuda.synchronize()
+    print(json.dumps({"case": lin.name, "M": args.M, "reps": args.reps,
+                      "device_error": w4.w4_get_device_error()}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -444,7 +574,16 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="time only the decode step (skip the other workloads)")
+    ap.add_argument("--case", default=None,
+                    help="run --reps calls of the workload linear whose name starts with this")
+    ap.add_argument("--M", type=int, default=1)
+    ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args()
+    if args.case:
+        run_case(args)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
