@@ -163,17 +163,13 @@ int w4a16_linear(const uint16_t* x, const uint8_t* packed, const float* scales,
     GemvArgs a{};
     rc = split_workspace(p, workspace, workspace_bytes, &a.tickets, &a.partial);
     if (rc) return rc;
-    CUtensorMap tm;
-    if (!encode_tmap_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, packed, (uint64_t)(Kp / 2),
-                        (uint64_t)N, (uint64_t)(Kp / 2), kGemvStageK / 2, kGemvRows,
-                        CU_TENSOR_MAP_SWIZZLE_128B))
-        return W4_ERR_CUDA;
     a.x = x; a.scales = scales; a.zeros = zeros; a.bias = bias; a.y = y;
     a.err = device_error_flag();
     if (!a.err) return W4_ERR_CUDA;
     a.M = M; a.N = N; a.K = K; a.Kp = (int)Kp; a.G = group_size; a.Ng = (int)(Kp / group_size);
-    a.nst = p.nst; a.S = p.S; a.spl = p.spl; a.units = p.units; a.XS = p.XS;
-    return launch_w4a16_gemv(tm, a, p, st);
+    a.R = p.R; a.SKE = p.SKE; a.nst = p.nst; a.S = p.S; a.spl = p.spl; a.units = p.units;
+    a.XS = p.XS; a.red = p.red;
+    return launch_w4a16_gemv(packed, a, p, st);
 }
 
 int w4a8_quantize_act(const uint16_t* x, int M, int K, int group_size, int8_t* qx,
@@ -219,17 +215,13 @@ int w4a8_linear(const int8_t* qx, const float* sx, const uint8_t* packed,
     GemvArgs a{};
     rc = split_workspace(p, workspace, workspace_bytes, &a.tickets, &a.partial);
     if (rc) return rc;
-    CUtensorMap tm;
-    if (!encode_tmap_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, packed, (uint64_t)(Kp / 2),
-                        (uint64_t)N, (uint64_t)(Kp / 2), kGemvStageK / 2, kGemvRows,
-                        CU_TENSOR_MAP_SWIZZLE_128B))
-        return W4_ERR_CUDA;
     a.x = qx; a.sx = sx; a.scales = w_scales; a.bias = bias; a.y = y; a.acc_out = acc_out;
     a.err = device_error_flag();
     if (!a.err) return W4_ERR_CUDA;
     a.M = M; a.N = N; a.K = K; a.Kp = (int)Kp; a.G = group_size; a.Ng = 1;
-    a.nst = p.nst; a.S = p.S; a.spl = p.spl; a.units = p.units; a.XS = p.XS;
-    return launch_w4a8_gemv(tm, a, p, static_cast<cudaStream_t>(stream));
+    a.R = p.R; a.SKE = p.SKE; a.nst = p.nst; a.S = p.S; a.spl = p.spl; a.units = p.units;
+    a.XS = p.XS; a.red = p.red;
+    return launch_w4a8_gemv(packed, a, p, static_cast<cudaStream_t>(stream));
 }
 
 int w4_get_device_error(void* stream) {

@@ -7,25 +7,37 @@
 // "从 FP 线性层到 INT4 DP4A 的数学推导" and "DP4A 做了什么"):
 // acc = sum (code - 8) q_x in int32, y = s_W s_x acc + b.
 //
-// Structure (both kernels): one CTA per SM, 8 consumer warps + 1 producer
-// warp.  The producer streams 128-row x 256-column tiles of the packed
-// weights (16 KB, 128-byte swizzled) into a 6-deep shared-memory ring with
-// TMA; each consumer warp owns 16 rows of the tile and reads its fragments
-// with ldmatrix.  A unit of work is (128-row block, K slice); units are dealt
-// round-robin to the persistent CTAs, and K slices (split-K) are combined by
-// the last CTA to finish a row block, in a fixed order.
+// Structure (both kernels): persistent CTAs of 8 consumer warps + 1
+// producer warp, one or two CTAs per SM.  A unit of work is (block of R
+// output rows, slice of the padded K), R in {16, 32, 64, 128}; units are dealt
+// round-robin to the CTAs.  The producer streams 16 KB stages of packed
+// weights (128/R TMA boxes of R rows x 128 bytes, 128-byte swizzle) into a
+// 4-deep ring.  Each stage holds eight 16-row x 256-column boxes; consumer
+// warp w takes row tile w % (R/16) and k-phase w / (R/16), i.e. exactly one
+// such box per stage, and reads it with ldmatrix.  Partial sums of the
+// k-phases are added in shared memory in a fixed order; K slices of a row
+// block (split-K) are added by the last CTA to finish it, also in a fixed
+// order, so results are deterministic.
 //
 // W4A16 inner product: each 32-bit ldmatrix word holds 8 codes of one row;
-// they become four bf16x2 words (c - z exact) that feed mma.sync m16n8k16
-// directly as the A operand (16 weight rows), with the activations as the B
-// operand (8 tokens per n-tile).  The order of k inside a 32-column chunk is
-// permuted identically on both operands, so no data shuffles are needed.  All
-// 16 columns of one MMA come from one 32-column chunk and hence one group:
-// the group scale is applied to the fp32 partial sums, not to the weights.
+// one LOP3 per pair ORs the code into the mantissa of bf16 128.0, and these
+// words (128 + code, exact) feed mma.sync m16n8k16 directly as the A operand
+// (16 weight rows), with the activations as the B operand (8 tokens per
+// n-tile).  The order of k inside a 32-column chunk is permuted identically on
+// both operands, so no data shuffles are needed.  All MMAs between two
+// flushes see columns of one group: at the flush the (128 + z) * sum(x) term
+// of that run of columns is removed and the group scale applied to the fp32
+// partial sums, so the weights stay exact.
+//
+// Launch: programmatic dependent launch.  Before waiting for the previous
+// kernel on the stream, the producer only prefetches the first stages of its
+// first unit into L2; all shared-memory copies and every access to x, the
+// workspace and y come after griddepcontrol.wait.
 #include "w4_device.cuh"
 #include "w4_internal.h"
 
 #include <algorithm>
+#include <cstdlib>
 
 namespace w4 {
 namespace {
@@ -33,9 +45,7 @@ namespace {
 constexpr int CW = kGemvConsumerWarps;
 constexpr int NCT = CW * 32;
 constexpr int NS = kGemvStages;
-constexpr int ROWS = kGemvRows;
-constexpr int STAGE_K = kGemvStageK;
-constexpr int STAGE_BYTES = ROWS * (STAGE_K / 2);      // 16 KB
+constexpr int STAGE_BYTES = kGemvStageBytes;
 
 struct SmemCtl {
     uint64_t full[NS];
@@ -44,7 +54,8 @@ struct SmemCtl {
     int last;
     int sumq[16];
 };
-constexpr int kCtlBytes = (int)((sizeof(SmemCtl) + 127) / 128 * 128);
+constexpr int kCtlBytes = 256;
+static_assert(sizeof(SmemCtl) <= kCtlBytes, "control block");
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
     const uint32_t s = smem_u32(p);
@@ -68,9 +79,37 @@ __device__ __forceinline__ void lds64(uint32_t addr, uint32_t& a, uint32_t& b) {
     asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(a), "=r"(b) : "r"(addr));
 }
 
+__device__ __forceinline__ void grid_dep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dep_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int c0, int c1) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                 :: "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1) : "memory");
+}
+
 // Producer: one thread streams every stage of every unit of this CTA.
 __device__ void gemv_producer(const CUtensorMap* tm, uint8_t* wbuf, SmemCtl* ctl,
                               const GemvArgs& a) {
+    const int boxes = 128 / a.R;
+    const int box_bytes = a.R * 128;
+    const int kbytes = a.Kp / 2;
+    // Warm L2 with the first stages of the first unit while the previous
+    // kernel on the stream may still be running (weights are read only).
+    if ((int)blockIdx.x < a.units) {
+        int rb, s, ks0, ks1;
+        unit_coords(blockIdx.x, a, rb, s, ks0, ks1);
+        for (int ks = ks0; ks < min(ks1, ks0 + NS); ++ks)
+            for (int b = 0; b < boxes; ++b) {
+                const int kb = ks * (a.SKE / 2) + b * 128;
+                if (kb < kbytes) tma_prefetch_l2_2d(tm, kb, rb * a.R);
+            }
+    }
+    grid_dep_wait();
     const uint64_t pol = policy_evict_first();
     uint32_t it = 0;
     bool ok = true;
@@ -84,9 +123,12 @@ __device__ void gemv_producer(const CUtensorMap* tm, uint8_t* wbuf, SmemCtl* ctl
                 ok = false;
                 break;
             }
-            mbar_arrive_expect_tx(&ctl->full[slot], STAGE_BYTES);
-            tma_load_2d(wbuf + slot * STAGE_BYTES, tm, ks * (STAGE_K / 2), rb * ROWS,
-                        &ctl->full[slot], pol);
+            const int kb0 = ks * (a.SKE / 2);
+            const int nbox = min(boxes, (kbytes - kb0 + 127) / 128);   // boxes inside Kp
+            mbar_arrive_expect_tx(&ctl->full[slot], nbox * box_bytes);
+            for (int b = 0; b < nbox; ++b)
+                tma_load_2d(wbuf + slot * STAGE_BYTES + b * box_bytes, tm, kb0 + b * 128,
+                            rb * a.R, &ctl->full[slot], pol);
         }
     }
     if (!ok || ctl->abort) {
@@ -99,9 +141,15 @@ __device__ void gemv_producer(const CUtensorMap* tm, uint8_t* wbuf, SmemCtl* ctl
 
 // Activations of one unit into shared memory, bf16, columns [k0, k0+nk).
 // Within every 8-column block the order is (0,4,1,5,2,6,3,7), the order in
-// which nibbles_to_bf16x2 emits weights; columns >= K are zero.
-__device__ void stage_x_bf16(uint8_t* xbuf, const uint16_t* x, int M, int K, int XS,
-                             int k0, int nk, int tid) {
+// which nibbles_to_bf16x2_biased emits weights; columns >= K are zero.  One
+// thread per 8-column block; nk is a multiple of 256, so the 32 blocks a warp
+// handles belong to one token and every run of CPG*4 lanes is one segment of
+// CPG*32 columns.  The segment's sum of x (blocks added by a fixed butterfly)
+// goes to xseg[segment * M + token].
+template <int CPG>
+__device__ void stage_x_bf16(uint8_t* xbuf, float* xseg, const uint16_t* x, int M, int K,
+                             int XS, int k0, int nk, int tid) {
+    constexpr int LPS = CPG * 4;            // lanes (blocks) per segment
     const int nb = nk >> 3;
     const bool vec = (K & 7) == 0;
     for (int idx = tid; idx < M * nb; idx += NCT) {
@@ -119,6 +167,15 @@ __device__ void stage_x_bf16(uint8_t* xbuf, const uint16_t* x, int M, int K, int
 #pragma unroll
             for (int j = 0; j < 4; ++j) q[j] = (uint32_t)e[2 * j] | ((uint32_t)e[2 * j + 1] << 16);
         }
+        float sum = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            sum += __uint_as_float(q[j] << 16);
+            sum += __uint_as_float(q[j] & 0xFFFF0000u);
+        }
+#pragma unroll
+        for (int o = 1; o < LPS; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        if ((b % LPS) == 0) xseg[(b / LPS) * M + m] = sum;
         uint4 o;
         o.x = __byte_perm(q[0], q[2], 0x5410);   // (x0, x4)
         o.y = __byte_perm(q[0], q[2], 0x7632);   // (x1, x5)
@@ -130,7 +187,8 @@ __device__ void stage_x_bf16(uint8_t* xbuf, const uint16_t* x, int M, int K, int
 
 // INT8 activations of one unit, order (0,2,4,6 | 1,3,5,7) per 8-column
 // block to match the byte lanes of (v & 0x0F0F0F0F) and ((v >> 4) & ...);
-// also accumulates sum(q_x) per token into ctl->sumq.
+// also accumulates sum(q_x) over the slice per token into ctl->sumq (which
+// the caller zeroed).
 __device__ void stage_x_s8(uint8_t* xbuf, SmemCtl* ctl, const int8_t* qx, int M, int Kp,
                            int XS, int k0, int nk, int tid) {
     const int nb = nk >> 3;
@@ -155,33 +213,105 @@ __device__ void stage_x_s8(uint8_t* xbuf, SmemCtl* ctl, const int8_t* qx, int M,
     }
 }
 
+// Shared layout of one CTA; identical for both kernels.
+struct Smem {
+    uint8_t* wbuf;
+    SmemCtl* ctl;
+    float* red;
+    uint8_t* xbuf;
+    float* xseg;      // W4A16: per-segment sums of x, after M * XS bytes of xbuf
+};
+
+__device__ __forceinline__ Smem gemv_init(const CUtensorMap* tm, const GemvArgs& a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = align1024(smem_raw);
+    Smem sm;
+    sm.wbuf = base;
+    sm.ctl = reinterpret_cast<SmemCtl*>(base + NS * STAGE_BYTES);
+    sm.red = reinterpret_cast<float*>(base + NS * STAGE_BYTES + kCtlBytes);
+    sm.xbuf = base + NS * STAGE_BYTES + kCtlBytes + a.red;
+    sm.xseg = reinterpret_cast<float*>(sm.xbuf + (size_t)a.M * a.XS);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(&sm.ctl->full[i], 1);
+            mbar_init(&sm.ctl->empty[i], CW);
+        }
+        sm.ctl->abort = 0;
+        sm.ctl->last = 0;
+        for (int i = 0; i < 16; ++i) sm.ctl->sumq[i] = 0;
+        fence_mbar_init();
+    }
+    if (threadIdx.x == NCT) tma_prefetch_desc(tm);
+    grid_dep_launch();
+    __syncthreads();
+    return sm;
+}
+
+// Split-K hand-off: after this CTA's partials are written, the last CTA of
+// row block rb sees ctl->last set.  All consumer threads call it.
+__device__ __forceinline__ bool split_k_arrive(const GemvArgs& a, SmemCtl* ctl, int rb) {
+    __threadfence();
+    named_bar_sync(1, NCT);
+    if (threadIdx.x == 0) ctl->last = (atomicAdd(&a.tickets[rb], 1) == a.S - 1);
+    named_bar_sync(1, NCT);
+    const bool last = ctl->last;
+    if (last) __threadfence();
+    return last;
+}
+
 template <int NT, int CPG, bool ASYM>
-__device__ void w4a16_consumer(uint8_t* wbuf, uint8_t* xbuf, SmemCtl* ctl, const GemvArgs& a) {
+__device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
     constexpr int SEG = 8 / CPG;
+    constexpr int LOG_CPG = CPG == 8 ? 3 : CPG == 4 ? 2 : CPG == 2 ? 1 : 0;
+    constexpr bool PF = SEG <= 2;           // scales one stage ahead when they are few
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int tig = lane & 3, gid = lane >> 2;
+    const int WR = a.R / 16, WK = CW / WR;
+    const int rt = warp % WR, kp = warp / WR;
     const uint16_t* x = static_cast<const uint16_t*>(a.x);
-    const uint32_t wbuf_u = smem_u32(wbuf), xbuf_u = smem_u32(xbuf);
+    const uint32_t wbuf_u = smem_u32(sm.wbuf), xbuf_u = smem_u32(sm.xbuf);
     const int lj = lane >> 3, li = lane & 7;
-    const uint32_t l_rowoff = (uint32_t)(warp * 16 + ((lj & 1) << 3) + li) * 128u;
-    const int l_chi = lj >> 1;
+    // this warp's 16 x 256 box inside a stage, and the ldmatrix row and
+    // swizzled chunk offset of this lane for each chunk pair
+    const uint32_t l_off = (uint32_t)(kp * a.R * 128 + (rt * 16 + ((lj & 1) << 3) + li) * 128);
+    uint32_t l_cp[4];
+#pragma unroll
+    for (int cp = 0; cp < 4; ++cp) l_cp[cp] = l_off + ((uint32_t)((2 * cp + (lj >> 1)) ^ li) << 4);
     uint32_t xrow[NT];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
-        xrow[nt] = xbuf_u + (uint32_t)(min(nt * 8 + gid, a.M - 1) * a.XS + tig * 16);
+        xrow[nt] = xbuf_u + (uint32_t)(min(nt * 8 + gid, a.M - 1) * a.XS + tig * 16 + kp * 512);
+    int xt[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        xt[nt][0] = min(nt * 8 + 2 * tig, a.M - 1);
+        xt[nt][1] = min(nt * 8 + 2 * tig + 1, a.M - 1);
+    }
+    // group of a segment: segments of CPG*32 columns tile the groups exactly,
+    // so g = segment / (G / (CPG*32)), a shift when that ratio is a power of 2
+    const int gdiv = a.G / (CPG * 32);
+    const int gshift = (gdiv & (gdiv - 1)) == 0 ? __ffs(gdiv) - 1 : -1;
+    const float zc[4] = {0.f, 0.f, 0.f, 0.f};
 
+    grid_dep_wait();
     uint32_t it = 0;
+    int prev0 = -1, prev1 = -1;
     for (int u = blockIdx.x; u < a.units; u += gridDim.x) {
         int rb, s, ks0, ks1;
         unit_coords(u, a, rb, s, ks0, ks1);
-        const int row0 = rb * ROWS + warp * 16;
+        const int row0 = rb * a.R + rt * 16;
         const int nr = min(row0 + gid, a.N - 1), nr8 = min(row0 + gid + 8, a.N - 1);
         const float* sc_r = a.scales + (size_t)nr * a.Ng;
         const float* sc_r8 = a.scales + (size_t)nr8 * a.Ng;
 
         named_bar_sync(1, NCT);
-        stage_x_bf16(xbuf, x, a.M, a.K, a.XS, ks0 * STAGE_K, (ks1 - ks0) * STAGE_K, tid);
-        named_bar_sync(1, NCT);
+        if (ks0 != prev0 || ks1 != prev1) {
+            stage_x_bf16<CPG>(sm.xbuf, sm.xseg, x, a.M, a.K, a.XS, ks0 * a.SKE,
+                              (ks1 - ks0) * a.SKE, tid);
+            named_bar_sync(1, NCT);
+            prev0 = ks0;
+            prev1 = ks1;
+        }
 
         float acc[NT][4];
 #pragma unroll
@@ -189,95 +319,109 @@ __device__ void w4a16_consumer(uint8_t* wbuf, uint8_t* xbuf, SmemCtl* ctl, const
 #pragma unroll
             for (int j = 0; j < 4; ++j) acc[nt][j] = 0.f;
 
-        for (int ks = ks0; ks < ks1; ++ks, ++it) {
-            const int slot = it % NS;
-            float sr[SEG], sr8[SEG];
-            uint32_t zr[SEG], zr8[SEG];
+        // The MMA sums x * (128 + code) over each run of CPG chunks (one
+        // group); the flush removes (128 + z) * sum(x) of that run and applies
+        // the scale: acc += s * (tmp - (128 + z) * xs).
+        float sr[SEG], sr8[SEG], cz[SEG], cz8[SEG];
+        auto load_scales = [&](int kw, float* r_, float* r8_, float* z_, float* z8_) {
 #pragma unroll
             for (int j = 0; j < SEG; ++j) {
-                const int g = min((ks * STAGE_K + j * CPG * 32) / a.G, a.Ng - 1);
-                sr[j] = __ldg(sc_r + g);
-                sr8[j] = __ldg(sc_r8 + g);
+                const int sg = (kw >> (5 + LOG_CPG)) + j;
+                const int g = min(gshift >= 0 ? (sg >> gshift) : sg / gdiv, a.Ng - 1);
+                r_[j] = __ldg(sc_r + g);
+                r8_[j] = __ldg(sc_r8 + g);
                 if (ASYM) {
-                    zr[j] = (0x4300u + __ldg(a.zeros + (size_t)nr * a.Ng + g)) * 0x10001u;
-                    zr8[j] = (0x4300u + __ldg(a.zeros + (size_t)nr8 * a.Ng + g)) * 0x10001u;
+                    z_[j] = 128.f + (float)__ldg(a.zeros + (size_t)nr * a.Ng + g);
+                    z8_[j] = 128.f + (float)__ldg(a.zeros + (size_t)nr8 * a.Ng + g);
                 } else {
-                    zr[j] = zr8[j] = 0x43084308u;          // 128 + 8
+                    z_[j] = z8_[j] = 136.f;                 // 128 + 8
                 }
             }
-            if (mbar_wait(&ctl->full[slot], (it / NS) & 1, &ctl->abort, a.err)) {
-                const uint32_t wst = wbuf_u + slot * STAGE_BYTES + l_rowoff;
-                const uint32_t xoff = (uint32_t)(ks - ks0) * (STAGE_K * 2);
-                float tmp[NT][4];
+        };
+        if (PF) load_scales(min(ks0 * a.SKE + kp * 256, a.Kp - 1), sr, sr8, cz, cz8);
+
+        for (int ks = ks0; ks < ks1; ++ks, ++it) {
+            const int slot = it % NS;
+            const int kw = ks * a.SKE + kp * 256;          // first column of this warp's box
+            float nsr[SEG], nsr8[SEG], ncz[SEG], ncz8[SEG];
+            if (PF && ks + 1 < ks1)
+                load_scales(min(kw + a.SKE, a.Kp - 1), nsr, nsr8, ncz, ncz8);
+            if (kw < a.Kp) {
+                if (!PF) load_scales(kw, sr, sr8, cz, cz8);
+                if (mbar_wait(&sm.ctl->full[slot], (it / NS) & 1, &sm.ctl->abort, a.err)) {
+                    const uint32_t wst = wbuf_u + slot * STAGE_BYTES;
+                    const uint32_t xoff = (uint32_t)(ks - ks0) * (uint32_t)(a.SKE * 2);
+                    const float* xs_st =
+                        sm.xseg + (((ks - ks0) * a.SKE + kp * 256) >> (5 + LOG_CPG)) * a.M;
+                    float tmp[NT][4];
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
+                    for (int cp = 0; cp < 4; ++cp) {
+                        uint32_t r[4];
+                        ldmatrix_x4(wst + l_cp[cp], r[0], r[1], r[2], r[3]);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) tmp[nt][j] = 0.f;
-#pragma unroll
-                for (int cp = 0; cp < 4; ++cp) {
-                    uint32_t r[4];
-                    ldmatrix_x4(wst + ((uint32_t)((2 * cp + l_chi) ^ li) << 4), r[0], r[1], r[2], r[3]);
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int c = 2 * cp + h;
-                        const int seg = c / CPG;
-                        uint32_t P[4], Q[4];
-                        nibbles_to_bf16x2(r[2 * h], zr[seg], P);
-                        nibbles_to_bf16x2(r[2 * h + 1], zr8[seg], Q);
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) {
-                            uint32_t X[4];
-                            lds128(xrow[nt] + xoff + c * 64, X);
-                            mma_bf16_16816(tmp[nt], P[0], Q[0], P[1], Q[1], X[0], X[1], tmp[nt]);
-                            mma_bf16_16816(tmp[nt], P[2], Q[2], P[3], Q[3], X[2], X[3], tmp[nt]);
-                        }
-                        if ((c + 1) % CPG == 0) {
+                        for (int h = 0; h < 2; ++h) {
+                            const int c = 2 * cp + h;
+                            const int seg = c / CPG;
+                            uint32_t P[4], Q[4];
+                            nibbles_to_bf16x2_biased(r[2 * h], P);
+                            nibbles_to_bf16x2_biased(r[2 * h + 1], Q);
 #pragma unroll
                             for (int nt = 0; nt < NT; ++nt) {
-                                acc[nt][0] = fmaf(sr[seg], tmp[nt][0], acc[nt][0]);
-                                acc[nt][1] = fmaf(sr[seg], tmp[nt][1], acc[nt][1]);
-                                acc[nt][2] = fmaf(sr8[seg], tmp[nt][2], acc[nt][2]);
-                                acc[nt][3] = fmaf(sr8[seg], tmp[nt][3], acc[nt][3]);
+                                uint32_t X[4];
+                                lds128(xrow[nt] + xoff + c * 64, X);
+                                mma_bf16_16816(tmp[nt], P[0], Q[0], P[1], Q[1], X[0], X[1],
+                                               (c % CPG == 0) ? zc : tmp[nt]);
+                                mma_bf16_16816(tmp[nt], P[2], Q[2], P[3], Q[3], X[2], X[3], tmp[nt]);
+                            }
+                            if ((c + 1) % CPG == 0) {
 #pragma unroll
-                                for (int j = 0; j < 4; ++j) tmp[nt][j] = 0.f;
+                                for (int nt = 0; nt < NT; ++nt) {
+                                    const float xs0 = xs_st[seg * a.M + xt[nt][0]];
+                                    const float xs1 = xs_st[seg * a.M + xt[nt][1]];
+                                    acc[nt][0] = fmaf(sr[seg], fmaf(-cz[seg], xs0, tmp[nt][0]), acc[nt][0]);
+                                    acc[nt][1] = fmaf(sr[seg], fmaf(-cz[seg], xs1, tmp[nt][1]), acc[nt][1]);
+                                    acc[nt][2] = fmaf(sr8[seg], fmaf(-cz8[seg], xs0, tmp[nt][2]), acc[nt][2]);
+                                    acc[nt][3] = fmaf(sr8[seg], fmaf(-cz8[seg], xs1, tmp[nt][3]), acc[nt][3]);
+                                }
                             }
                         }
                     }
                 }
             }
+            if (PF) {
+#pragma unroll
+                for (int j = 0; j < SEG; ++j) {
+                    sr[j] = nsr[j]; sr8[j] = nsr8[j]; cz[j] = ncz[j]; cz8[j] = ncz8[j];
+                }
+            }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl->empty[slot]);
+            if (lane == 0) mbar_arrive(&sm.ctl->empty[slot]);
+        }
+
+        // ---- add the k-phases of each row tile, in order 0, 1, ..., WK-1
+        if (WK > 1) {
+            if (kp > 0) {
+                float* dst = sm.red + ((kp - 1) * WR + rt) * (NT * 4 * 32) + lane;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) dst[(nt * 4 + j) * 32] = acc[nt][j];
+            }
+            named_bar_sync(1, NCT);
+            if (kp == 0) {
+                for (int q = 1; q < WK; ++q) {
+                    const float* src = sm.red + ((q - 1) * WR + rt) * (NT * 4 * 32) + lane;
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) acc[nt][j] += src[(nt * 4 + j) * 32];
+                }
+            }
         }
 
         // ---- epilogue: thread holds (token 8nt + 2tig + (j&1), row gid + 8(j>>1))
         if (a.S == 1) {
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int t = nt * 8 + 2 * tig + (j & 1);
-                    const int n = row0 + gid + 8 * (j >> 1);
-                    if (t < a.M && n < a.N) {
-                        const float b = a.bias ? __ldg(a.bias + n) : 0.f;
-                        a.y[(size_t)t * a.N + n] = f32_to_bf16_bits(acc[nt][j] + b);
-                    }
-                }
-        } else {
-            float* part = static_cast<float*>(a.partial);
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int t = nt * 8 + 2 * tig + (j & 1);
-                    const int n = row0 + gid + 8 * (j >> 1);
-                    if (t < a.M && n < a.N) part[((size_t)s * a.M + t) * a.N + n] = acc[nt][j];
-                }
-            __threadfence();
-            named_bar_sync(1, NCT);
-            if (tid == 0) ctl->last = (atomicAdd(&a.tickets[rb], 1) == a.S - 1);
-            named_bar_sync(1, NCT);
-            if (ctl->last) {
-                __threadfence();
+            if (kp == 0) {
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -285,13 +429,40 @@ __device__ void w4a16_consumer(uint8_t* wbuf, uint8_t* xbuf, SmemCtl* ctl, const
                         const int t = nt * 8 + 2 * tig + (j & 1);
                         const int n = row0 + gid + 8 * (j >> 1);
                         if (t < a.M && n < a.N) {
-                            float v = 0.f;
-                            for (int q = 0; q < a.S; ++q)
-                                v += ld_cg_f32(part + ((size_t)q * a.M + t) * a.N + n);
                             const float b = a.bias ? __ldg(a.bias + n) : 0.f;
-                            a.y[(size_t)t * a.N + n] = f32_to_bf16_bits(v + b);
+                            a.y[(size_t)t * a.N + n] = f32_to_bf16_bits(acc[nt][j] + b);
                         }
                     }
+            }
+        } else {
+            float* part = static_cast<float*>(a.partial);
+            if (kp == 0) {
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int t = nt * 8 + 2 * tig + (j & 1);
+                        const int n = row0 + gid + 8 * (j >> 1);
+                        if (t < a.M && n < a.N) part[((size_t)s * a.M + t) * a.N + n] = acc[nt][j];
+                    }
+            }
+            if (split_k_arrive(a, sm.ctl, rb)) {
+                if (kp == 0) {
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int t = nt * 8 + 2 * tig + (j & 1);
+                            const int n = row0 + gid + 8 * (j >> 1);
+                            if (t < a.M && n < a.N) {
+                                float v = 0.f;
+                                for (int q = 0; q < a.S; ++q)
+                                    v += ld_cg_f32(part + ((size_t)q * a.M + t) * a.N + n);
+                                const float b = a.bias ? __ldg(a.bias + n) : 0.f;
+                                a.y[(size_t)t * a.N + n] = f32_to_bf16_bits(v + b);
+                            }
+                        }
+                }
                 if (tid == 0) a.tickets[rb] = 0;
             }
         }
@@ -299,30 +470,41 @@ __device__ void w4a16_consumer(uint8_t* wbuf, uint8_t* xbuf, SmemCtl* ctl, const
 }
 
 template <int MT>
-__device__ void w4a8_consumer(uint8_t* wbuf, uint8_t* xbuf, SmemCtl* ctl, const GemvArgs& a) {
+__device__ void w4a8_consumer(const Smem& sm, const GemvArgs& a) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int tig = lane & 3, gid = lane >> 2;
+    const int WR = a.R / 16, WK = CW / WR;
+    const int rt = warp % WR, kp = warp / WR;
     const int8_t* qx = static_cast<const int8_t*>(a.x);
-    const uint32_t wbuf_u = smem_u32(wbuf), xbuf_u = smem_u32(xbuf);
+    const uint32_t wbuf_u = smem_u32(sm.wbuf), xbuf_u = smem_u32(sm.xbuf);
     const int lj = lane >> 3, li = lane & 7;
-    const uint32_t l_rowoff = (uint32_t)(warp * 16 + ((lj & 1) << 3) + li) * 128u;
-    const int l_chi = lj >> 1;
+    const uint32_t l_off = (uint32_t)(kp * a.R * 128 + (rt * 16 + ((lj & 1) << 3) + li) * 128);
+    uint32_t l_cp[4];
+#pragma unroll
+    for (int cp = 0; cp < 4; ++cp) l_cp[cp] = l_off + ((uint32_t)((2 * cp + (lj >> 1)) ^ li) << 4);
     uint32_t xrow[MT];
 #pragma unroll
     for (int m = 0; m < MT; ++m)
-        xrow[m] = xbuf_u + (uint32_t)(min(m, a.M - 1) * a.XS + tig * 8);
+        xrow[m] = xbuf_u + (uint32_t)(min(m, a.M - 1) * a.XS + tig * 8 + kp * 256);
+    int* red = reinterpret_cast<int*>(sm.red);
 
+    grid_dep_wait();
     uint32_t it = 0;
+    int prev0 = -1, prev1 = -1;
     for (int u = blockIdx.x; u < a.units; u += gridDim.x) {
         int rb, s, ks0, ks1;
         unit_coords(u, a, rb, s, ks0, ks1);
-        const int row0 = rb * ROWS + warp * 16;
+        const int row0 = rb * a.R + rt * 16;
 
         named_bar_sync(1, NCT);
-        if (tid < 16) ctl->sumq[tid] = 0;
-        named_bar_sync(1, NCT);
-        stage_x_s8(xbuf, ctl, qx, a.M, a.Kp, a.XS, ks0 * STAGE_K, (ks1 - ks0) * STAGE_K, tid);
-        named_bar_sync(1, NCT);
+        if (ks0 != prev0 || ks1 != prev1) {
+            if (tid < 16) sm.ctl->sumq[tid] = 0;
+            named_bar_sync(1, NCT);
+            stage_x_s8(sm.xbuf, sm.ctl, qx, a.M, a.Kp, a.XS, ks0 * a.SKE, (ks1 - ks0) * a.SKE, tid);
+            named_bar_sync(1, NCT);
+            prev0 = ks0;
+            prev1 = ks1;
+        }
 
         int acc[MT][2];
 #pragma unroll
@@ -330,13 +512,15 @@ __device__ void w4a8_consumer(uint8_t* wbuf, uint8_t* xbuf, SmemCtl* ctl, const 
 
         for (int ks = ks0; ks < ks1; ++ks, ++it) {
             const int slot = it % NS;
-            if (mbar_wait(&ctl->full[slot], (it / NS) & 1, &ctl->abort, a.err)) {
-                const uint32_t wst = wbuf_u + slot * STAGE_BYTES + l_rowoff;
-                const uint32_t xoff = (uint32_t)(ks - ks0) * STAGE_K;
+            const int kw = ks * a.SKE + kp * 256;
+            if (kw < a.Kp &&
+                mbar_wait(&sm.ctl->full[slot], (it / NS) & 1, &sm.ctl->abort, a.err)) {
+                const uint32_t wst = wbuf_u + slot * STAGE_BYTES;
+                const uint32_t xoff = (uint32_t)(ks - ks0) * (uint32_t)a.SKE;
 #pragma unroll
                 for (int cp = 0; cp < 4; ++cp) {
                     uint32_t r[4];
-                    ldmatrix_x4(wst + ((uint32_t)((2 * cp + l_chi) ^ li) << 4), r[0], r[1], r[2], r[3]);
+                    ldmatrix_x4(wst + l_cp[cp], r[0], r[1], r[2], r[3]);
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const int c = 2 * cp + h;
@@ -355,10 +539,10 @@ __device__ void w4a8_consumer(uint8_t* wbuf, uint8_t* xbuf, SmemCtl* ctl, const 
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl->empty[slot]);
+            if (lane == 0) mbar_arrive(&sm.ctl->empty[slot]);
         }
 
-        // reduce over the four lanes that share a row, remove the +8 offset
+        // lanes sharing a row, then the k-phases (exact integers)
 #pragma unroll
         for (int m = 0; m < MT; ++m)
 #pragma unroll
@@ -366,171 +550,253 @@ __device__ void w4a8_consumer(uint8_t* wbuf, uint8_t* xbuf, SmemCtl* ctl, const 
                 int v = acc[m][h];
                 v += __shfl_xor_sync(0xffffffffu, v, 1);
                 v += __shfl_xor_sync(0xffffffffu, v, 2);
-                acc[m][h] = v - 8 * ctl->sumq[min(m, a.M - 1)];
+                acc[m][h] = v;
             }
+        if (WK > 1) {
+            if (kp > 0) {
+                int* dst = red + ((kp - 1) * WR + rt) * (MT * 2 * 32) + lane;
+#pragma unroll
+                for (int m = 0; m < MT; ++m)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) dst[(m * 2 + h) * 32] = acc[m][h];
+            }
+            named_bar_sync(1, NCT);
+            if (kp == 0) {
+                for (int q = 1; q < WK; ++q) {
+                    const int* src = red + ((q - 1) * WR + rt) * (MT * 2 * 32) + lane;
+#pragma unroll
+                    for (int m = 0; m < MT; ++m)
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) acc[m][h] += src[(m * 2 + h) * 32];
+                }
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) acc[m][h] -= 8 * sm.ctl->sumq[min(m, a.M - 1)];
+
         int32_t* part = static_cast<int32_t*>(a.partial);
+        bool write = kp == 0;
         if (a.S > 1) {
+            if (kp == 0) {
+#pragma unroll
+                for (int m = 0; m < MT; ++m)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int n = row0 + gid + 8 * h;
+                        if (m < a.M && (m & 3) == tig && n < a.N)
+                            part[((size_t)s * a.M + m) * a.N + n] = acc[m][h];
+                    }
+            }
+            const bool last = split_k_arrive(a, sm.ctl, rb);
+            write = write && last;
+            if (last && tid == 0) a.tickets[rb] = 0;
+        }
+        if (write) {
 #pragma unroll
             for (int m = 0; m < MT; ++m)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int n = row0 + gid + 8 * h;
-                    if (m < a.M && (m & 3) == tig && n < a.N)
-                        part[((size_t)s * a.M + m) * a.N + n] = acc[m][h];
-                }
-            __threadfence();
-            named_bar_sync(1, NCT);
-            if (tid == 0) ctl->last = (atomicAdd(&a.tickets[rb], 1) == a.S - 1);
-            named_bar_sync(1, NCT);
-            if (!ctl->last) continue;
-            __threadfence();
-        }
-#pragma unroll
-        for (int m = 0; m < MT; ++m)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int n = row0 + gid + 8 * h;
-                if (m < a.M && (m & 3) == tig && n < a.N) {
-                    int v = acc[m][h];
-                    if (a.S > 1) {
-                        v = 0;
-                        for (int q = 0; q < a.S; ++q)
-                            v += ld_cg_s32(part + ((size_t)q * a.M + m) * a.N + n);
+                    if (m < a.M && (m & 3) == tig && n < a.N) {
+                        int v = acc[m][h];
+                        if (a.S > 1) {
+                            v = 0;
+                            for (int q = 0; q < a.S; ++q)
+                                v += ld_cg_s32(part + ((size_t)q * a.M + m) * a.N + n);
+                        }
+                        if (a.acc_out) a.acc_out[(size_t)m * a.N + n] = v;
+                        const float sc = __ldg(a.scales + n) * __ldg(a.sx + m);
+                        const float b = a.bias ? __ldg(a.bias + n) : 0.f;
+                        a.y[(size_t)m * a.N + n] = f32_to_bf16_bits(fmaf(sc, (float)v, b));
                     }
-                    if (a.acc_out) a.acc_out[(size_t)m * a.N + n] = v;
-                    const float sc = __ldg(a.scales + n) * __ldg(a.sx + m);
-                    const float b = a.bias ? __ldg(a.bias + n) : 0.f;
-                    a.y[(size_t)m * a.N + n] = f32_to_bf16_bits(fmaf(sc, (float)v, b));
                 }
-            }
-        if (a.S > 1 && tid == 0) a.tickets[rb] = 0;
-    }
-}
-
-__device__ __forceinline__ void gemv_init(uint8_t*& wbuf, uint8_t*& xbuf, SmemCtl*& ctl,
-                                          const CUtensorMap* tm) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* base = align1024(smem_raw);
-    wbuf = base;
-    ctl = reinterpret_cast<SmemCtl*>(base + NS * STAGE_BYTES);
-    xbuf = base + NS * STAGE_BYTES + kCtlBytes;
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < NS; ++i) {
-            mbar_init(&ctl->full[i], 1);
-            mbar_init(&ctl->empty[i], CW);
         }
-        ctl->abort = 0;
-        ctl->last = 0;
-        for (int i = 0; i < 16; ++i) ctl->sumq[i] = 0;
-        fence_mbar_init();
     }
-    if (threadIdx.x == NCT) tma_prefetch_desc(tm);
-    __syncthreads();
 }
 
+// Kernel instances that the plan may place two to an SM (M <= 8 for W4A16,
+// M <= 4 for W4A8) are compiled for two resident CTAs of 288 threads.
 template <int NT, int CPG, bool ASYM>
-__global__ void __launch_bounds__(kGemvThreads, 1)
-k_w4a16_gemv(const __grid_constant__ CUtensorMap tmW, const GemvArgs a) {
-    uint8_t *wbuf, *xbuf;
-    SmemCtl* ctl;
-    gemv_init(wbuf, xbuf, ctl, &tmW);
+__device__ __forceinline__ void w4a16_body(const CUtensorMap* tm, const GemvArgs& a) {
+    const Smem sm = gemv_init(tm, a);
     if (threadIdx.x >= NCT) {
-        if (threadIdx.x == NCT) gemv_producer(&tmW, wbuf, ctl, a);
+        if (threadIdx.x == NCT) gemv_producer(tm, sm.wbuf, sm.ctl, a);
     } else {
-        w4a16_consumer<NT, CPG, ASYM>(wbuf, xbuf, ctl, a);
+        w4a16_consumer<NT, CPG, ASYM>(sm, a);
+    }
+}
+
+template <int CPG, bool ASYM>
+__global__ void __launch_bounds__(kGemvThreads, 2)
+k_w4a16_gemv_m8(const __grid_constant__ CUtensorMap tmW, const GemvArgs a) {
+    w4a16_body<1, CPG, ASYM>(&tmW, a);
+}
+
+template <int CPG, bool ASYM>
+__global__ void __launch_bounds__(kGemvThreads, 1)
+k_w4a16_gemv_m16(const __grid_constant__ CUtensorMap tmW, const GemvArgs a) {
+    w4a16_body<2, CPG, ASYM>(&tmW, a);
+}
+
+template <int MT>
+__device__ __forceinline__ void w4a8_body(const CUtensorMap* tm, const GemvArgs& a) {
+    const Smem sm = gemv_init(tm, a);
+    if (threadIdx.x >= NCT) {
+        if (threadIdx.x == NCT) gemv_producer(tm, sm.wbuf, sm.ctl, a);
+    } else {
+        w4a8_consumer<MT>(sm, a);
     }
 }
 
 template <int MT>
+__global__ void __launch_bounds__(kGemvThreads, 2)
+k_w4a8_gemv_m4(const __grid_constant__ CUtensorMap tmW, const GemvArgs a) {
+    w4a8_body<MT>(&tmW, a);
+}
+
+template <int MT>
 __global__ void __launch_bounds__(kGemvThreads, 1)
-k_w4a8_gemv(const __grid_constant__ CUtensorMap tmW, const GemvArgs a) {
-    uint8_t *wbuf, *xbuf;
-    SmemCtl* ctl;
-    gemv_init(wbuf, xbuf, ctl, &tmW);
-    if (threadIdx.x >= NCT) {
-        if (threadIdx.x == NCT) gemv_producer(&tmW, wbuf, ctl, a);
-    } else {
-        w4a8_consumer<MT>(wbuf, xbuf, ctl, a);
-    }
+k_w4a8_gemv_m16(const __grid_constant__ CUtensorMap tmW, const GemvArgs a) {
+    w4a8_body<MT>(&tmW, a);
 }
 
 template <typename Kern>
-int launch(Kern kern, const CUtensorMap& tm, const GemvArgs& a, const GemvPlan& p,
+int launch(Kern kern, const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
            cudaStream_t stream) {
+    CUtensorMap tm;
+    if (!encode_tmap_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, packed, (uint64_t)(a.Kp / 2),
+                        (uint64_t)a.N, (uint64_t)(a.Kp / 2), 128, (uint32_t)p.R,
+                        CU_TENSOR_MAP_SWIZZLE_128B))
+        return W4_ERR_CUDA;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)p.smem) != cudaSuccess)
         return W4_ERR_CUDA;
-    kern<<<p.grid, kGemvThreads, p.smem, stream>>>(tm, a);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.grid);
+    cfg.blockDim = dim3(kGemvThreads);
+    cfg.dynamicSmemBytes = p.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, tm, a) != cudaSuccess) return W4_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? W4_OK : W4_ERR_CUDA;
 }
 
 template <int NT, bool ASYM>
-int launch_w4a16_cpg(int cpg, const CUtensorMap& tm, const GemvArgs& a, const GemvPlan& p,
+int launch_w4a16_cpg(int cpg, const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
                      cudaStream_t st) {
+    if (NT == 1) {
+        switch (cpg) {
+            case 8: return launch(k_w4a16_gemv_m8<8, ASYM>, packed, a, p, st);
+            case 4: return launch(k_w4a16_gemv_m8<4, ASYM>, packed, a, p, st);
+            case 2: return launch(k_w4a16_gemv_m8<2, ASYM>, packed, a, p, st);
+            default: return launch(k_w4a16_gemv_m8<1, ASYM>, packed, a, p, st);
+        }
+    }
     switch (cpg) {
-        case 8: return launch(k_w4a16_gemv<NT, 8, ASYM>, tm, a, p, st);
-        case 4: return launch(k_w4a16_gemv<NT, 4, ASYM>, tm, a, p, st);
-        case 2: return launch(k_w4a16_gemv<NT, 2, ASYM>, tm, a, p, st);
-        default: return launch(k_w4a16_gemv<NT, 1, ASYM>, tm, a, p, st);
+        case 8: return launch(k_w4a16_gemv_m16<8, ASYM>, packed, a, p, st);
+        case 4: return launch(k_w4a16_gemv_m16<4, ASYM>, packed, a, p, st);
+        case 2: return launch(k_w4a16_gemv_m16<2, ASYM>, packed, a, p, st);
+        default: return launch(k_w4a16_gemv_m16<1, ASYM>, packed, a, p, st);
     }
 }
 
 }  // namespace
 
-bool plan_gemv(int M, int N, int Kp, int act_bytes, int sm_count, GemvPlan* p) {
-    if (M < 1 || M > 16 || N < 1 || Kp < 1) return false;
-    const int nst = (Kp + STAGE_K - 1) / STAGE_K;
-    const int NB = (N + ROWS - 1) / ROWS;
-    const size_t cap = 232448;                       // 227 KB opt-in per CTA
-    const size_t fixed = 1024 + (size_t)NS * STAGE_BYTES + kCtlBytes;
+bool plan_gemv(int M, int N, int Kp, int act_bytes, int sm_count, GemvPlan* out) {
+    if (M < 1 || M > 16 || N < 1 || Kp < 1 || sm_count < 1) return false;
     const int pad = act_bytes == 2 ? 64 : 16;
-    const long per_tok = (long)((cap - fixed) / (size_t)M) - pad;
-    const int spl_max = (int)(per_tok / (STAGE_K * act_bytes));
-    if (spl_max < 1) return false;
-    const int s_min = (nst + spl_max - 1) / spl_max;
+    // cross-warp reduction buffer: per thread NT*4 floats (W4A16) or MT*2 ints (W4A8)
+    const int red = act_bytes == 2
+        ? CW * 32 * ((M > 8 ? 2 : 1) * 4) * 4
+        : CW * 32 * (M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16) * 2 * 4;
+    const size_t fixed = 1024 + (size_t)NS * STAGE_BYTES + kCtlBytes + red;
+    // W4A16 also keeps one fp32 sum of x per token and 32 columns of the slice
+    auto xseg_bytes = [&](int slice) -> size_t {
+        return act_bytes == 2 ? (size_t)M * (slice / 32) * 4 : 0;
+    };
+    const double wbytes = (double)N * Kp / 2.0;
+    const double bw_total = 6.5e12, bw_sm = 70e9;
     double best = 1e30;
-    for (int S = s_min; S <= nst; ++S) {
-        const int spl = (nst + S - 1) / S;
-        const int Se = (nst + spl - 1) / spl;
-        if (spl > spl_max) continue;
-        const int units = NB * Se;
-        const int grid = std::min(units, sm_count);
-        const int waves = (units + grid - 1) / grid;
-        const double cost = (double)waves * spl + (Se > 1 ? 1.0 * waves : 0.0);
-        if (cost < best - 1e-9) {
-            best = cost;
-            p->nst = nst; p->NB = NB; p->S = Se; p->spl = spl; p->units = units;
-            p->grid = grid;
+    bool found = false;
+    // two CTAs per SM only for the kernel instances compiled for it
+    const int cps_max = (act_bytes == 2 ? M <= 8 : M <= 4) ? 2 : 1;
+    // W4_GEMV_ROWS (16, 32, 64 or 128) pins the row-block size for tuning.
+    static const int forced_r = [] {
+        const char* e = std::getenv("W4_GEMV_ROWS");
+        const int v = e ? std::atoi(e) : 0;
+        return (v == 16 || v == 32 || v == 64 || v == 128) ? v : 0;
+    }();
+    for (int cps = cps_max; cps >= 1; --cps) {
+        // per-CTA shared memory: two CTAs share the SM's 228 KB (1 KB reserved each)
+        const size_t cap = cps == 2 ? 115712 : 232448;
+        if (fixed >= cap) continue;
+        const long per_tok = (long)((cap - fixed) / (size_t)M) - pad;
+        for (int R = 16; R <= 128; R *= 2) {
+            if (forced_r && R != forced_r) continue;
+            const int SKE = 32768 / R;
+            const int nst = (Kp + SKE - 1) / SKE;
+            const int NB = (N + R - 1) / R;
+            const int spl_max =
+                (int)(per_tok / ((long)SKE * act_bytes + (act_bytes == 2 ? SKE / 8 : 0)));
+            if (spl_max < 1) continue;
+            const int s_min = (nst + spl_max - 1) / spl_max;
+            for (int S = s_min; S <= nst && S <= s_min + 64; ++S) {
+                const int spl = (nst + S - 1) / S;
+                const int Se = (nst + spl - 1) / spl;
+                if (spl > spl_max) continue;
+                const int units = NB * Se;
+                const int grid = std::min(units, cps * sm_count);
+                const int per_cta = (units + grid - 1) / grid;
+                const int ctas_on_sm = (grid + sm_count - 1) / sm_count;
+                const double unit_bytes = (double)R * std::min(spl * SKE, Kp) / 2.0;
+                const double sm_bytes = (double)per_cta * ctas_on_sm * unit_bytes;
+                double t = std::max(wbytes / bw_total, sm_bytes / bw_sm);
+                t += per_cta * 0.3e-6 + (Se > 1 ? 1.5e-6 : 0.0);
+                if (t < best * (1 - 1e-9)) {
+                    best = t;
+                    found = true;
+                    GemvPlan p;
+                    p.R = R; p.SKE = SKE; p.NB = NB; p.nst = nst; p.S = Se; p.spl = spl;
+                    p.units = units; p.grid = grid; p.cps = cps; p.red = red;
+                    p.XS = spl * SKE * act_bytes + pad;
+                    p.smem = fixed + (size_t)M * p.XS + xseg_bytes(spl * SKE);
+                    p.ws_bytes = 0;
+                    if (Se > 1)
+                        p.ws_bytes = ((size_t)NB * 4 + 255) / 256 * 256 + (size_t)Se * M * N * 4;
+                    *out = p;
+                }
+                if (Se == nst) break;
+            }
         }
-        if (Se == nst) break;
     }
-    p->XS = p->spl * STAGE_K * act_bytes + pad;
-    p->smem = fixed + (size_t)M * p->XS;
-    p->ws_bytes = 0;
-    if (p->S > 1)
-        p->ws_bytes = (((size_t)p->NB * 4 + 255) / 256) * 256 + (size_t)p->S * M * N * 4;
-    return true;
+    return found;
 }
 
-int launch_w4a16_gemv(const CUtensorMap& tm, const GemvArgs& a, const GemvPlan& p,
+int launch_w4a16_gemv(const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
                       cudaStream_t st) {
     const int gq = a.G / 32;
     const int cpg = (gq % 8 == 0) ? 8 : (gq % 4 == 0) ? 4 : (gq % 2 == 0) ? 2 : 1;
     const bool asym = a.zeros != nullptr;
     if (a.M <= 8)
-        return asym ? launch_w4a16_cpg<1, true>(cpg, tm, a, p, st)
-                    : launch_w4a16_cpg<1, false>(cpg, tm, a, p, st);
-    return asym ? launch_w4a16_cpg<2, true>(cpg, tm, a, p, st)
-                : launch_w4a16_cpg<2, false>(cpg, tm, a, p, st);
+        return asym ? launch_w4a16_cpg<1, true>(cpg, packed, a, p, st)
+                    : launch_w4a16_cpg<1, false>(cpg, packed, a, p, st);
+    return asym ? launch_w4a16_cpg<2, true>(cpg, packed, a, p, st)
+                : launch_w4a16_cpg<2, false>(cpg, packed, a, p, st);
 }
 
-int launch_w4a8_gemv(const CUtensorMap& tm, const GemvArgs& a, const GemvPlan& p,
+int launch_w4a8_gemv(const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
                      cudaStream_t st) {
-    if (a.M <= 1) return launch(k_w4a8_gemv<1>, tm, a, p, st);
-    if (a.M <= 2) return launch(k_w4a8_gemv<2>, tm, a, p, st);
-    if (a.M <= 4) return launch(k_w4a8_gemv<4>, tm, a, p, st);
-    if (a.M <= 8) return launch(k_w4a8_gemv<8>, tm, a, p, st);
-    return launch(k_w4a8_gemv<16>, tm, a, p, st);
+    if (a.M <= 1) return launch(k_w4a8_gemv_m4<1>, packed, a, p, st);
+    if (a.M <= 2) return launch(k_w4a8_gemv_m4<2>, packed, a, p, st);
+    if (a.M <= 4) return launch(k_w4a8_gemv_m4<4>, packed, a, p, st);
+    if (a.M <= 8) return launch(k_w4a8_gemv_m16<8>, packed, a, p, st);
+    return launch(k_w4a8_gemv_m16<16>, packed, a, p, st);
 }
 
 }  // namespace w4

@@ -85,16 +85,12 @@ extern "C" int w4a16_linear_noalloc(const uint16_t* x, const uint8_t* packed,
         a.tickets = static_cast<int*>(base);
         a.partial = static_cast<unsigned char*>(base) + ticket_bytes;
     }
-    CUtensorMap tm;
-    if (!encode_tmap_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, packed, (uint64_t)(Kp / 2),
-                        (uint64_t)N, (uint64_t)(Kp / 2), kGemvStageK / 2, kGemvRows,
-                        CU_TENSOR_MAP_SWIZZLE_128B))
-        return W4_ERR_CUDA;
     a.x = x; a.scales = scales; a.zeros = zeros; a.bias = bias; a.y = y;
     a.err = device_error_flag();
     if (!a.err) return W4_ERR_CUDA;
     a.M = M; a.N = N; a.K = K; a.Kp = (int)Kp; a.G = group_size;
     a.Ng = (int)(Kp / group_size);
-    a.nst = p.nst; a.S = p.S; a.spl = p.spl; a.units = p.units; a.XS = p.XS;
-    return launch_w4a16_gemv(tm, a, p, st);
+    a.R = p.R; a.SKE = p.SKE; a.nst = p.nst; a.S = p.S; a.spl = p.spl; a.units = p.units;
+    a.XS = p.XS; a.red = p.red;
+    return launch_w4a16_gemv(packed, a, p, st);
 }

@@ -162,6 +162,16 @@ __device__ __forceinline__ void nibbles_to_bf16x2(uint32_t v, uint32_t zb, uint3
     o[3] = sub_bf16x2(and_or(v >> 12, m, e), zb);
 }
 
+// Same eight codes -> four bf16x2 words (128 + c_i, 128 + c_{i+4}), exact;
+// the caller removes the 128 + z offset after the dot product.
+__device__ __forceinline__ void nibbles_to_bf16x2_biased(uint32_t v, uint32_t* o) {
+    const uint32_t m = 0x000F000Fu, e = 0x43004300u;
+    o[0] = and_or(v, m, e);
+    o[1] = and_or(v >> 4, m, e);
+    o[2] = and_or(v >> 8, m, e);
+    o[3] = and_or(v >> 12, m, e);
+}
+
 // ---------------------------------------------------------------- integer
 // d = c + sum_i a.u8[i] * b.s8[i]
 __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {

@@ -19,22 +19,27 @@ bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* bas
                     uint32_t box0, uint32_t box1, CUtensorMapSwizzle swizzle);
 
 // ---------------------------------------------------------------- decode
-// Decode kernels: one CTA per SM; a unit of work is (block of 128 output
-// rows, slice of the padded K).  Slices are whole 256-column stages.
-constexpr int kGemvRows = 128;          // rows per unit (8 consumer warps x 16)
-constexpr int kGemvStageK = 256;        // K columns per pipeline stage
-constexpr int kGemvStages = 6;          // pipeline depth
+// Decode kernels (M <= 16): persistent CTAs of 8 consumer warps + 1 producer
+// warp; a unit of work is (block of R output rows, slice of the padded K).
+// A pipeline stage is 16 KB of packed weights: 128/R boxes of R rows x 128
+// bytes (256 columns each), i.e. R rows x 32768/R columns.
+constexpr int kGemvStages = 4;                 // pipeline depth (16 KB stages)
+constexpr int kGemvStageBytes = 16384;
 constexpr int kGemvConsumerWarps = 8;
 constexpr int kGemvThreads = 32 * (kGemvConsumerWarps + 1);
 
 struct GemvPlan {
+    int R = 0;         // rows per unit (16, 32, 64 or 128)
+    int SKE = 0;       // K columns per stage (32768 / R)
     int NB = 0;        // row blocks
     int nst = 0;       // stages over Kp
-    int S = 0;         // K splits
+    int S = 0;         // K splits (global, combined by the last CTA)
     int spl = 0;       // stages per split
     int units = 0;     // NB * S
     int grid = 0;      // CTAs launched
+    int cps = 0;       // CTAs per SM the plan is sized for
     int XS = 0;        // activation row stride in shared memory (bytes)
+    int red = 0;       // bytes of the cross-warp reduction buffer
     size_t smem = 0;   // dynamic shared memory (bytes)
     size_t ws_bytes = 0;
 };
@@ -55,12 +60,14 @@ struct GemvArgs {
     int* tickets;             // [NB] arrival counters
     int* err;                 // device error flag
     int M, N, K, Kp, G, Ng;
-    int nst, S, spl, units, XS;
+    int R, SKE, nst, S, spl, units, XS, red;
 };
 
-int launch_w4a16_gemv(const CUtensorMap& tmW, const GemvArgs& a, const GemvPlan& p,
+// The launchers encode the tensor map of `packed` for the plan's box shape
+// and launch with programmatic dependent launch enabled.
+int launch_w4a16_gemv(const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
                       cudaStream_t stream);
-int launch_w4a8_gemv(const CUtensorMap& tmW, const GemvArgs& a, const GemvPlan& p,
+int launch_w4a8_gemv(const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
                      cudaStream_t stream);
 
 // ---------------------------------------------------------------- prefill
