@@ -127,7 +127,7 @@ size_t w4a16_workspace_bytes(int M, int N, int K, int group_size) {
     const long long Kp = padded_k(K, group_size);
     if (M <= 16) {
         GemvPlan p;
-        if (!plan_gemv(M, N, (int)Kp, 2, current_sm_count(), &p)) return 0;
+        if (!plan_gemv(M, N, (int)Kp, group_size, 2, current_sm_count(), &p)) return 0;
         return p.ws_bytes;
     }
     return 0;
@@ -159,11 +159,12 @@ int w4a16_linear(const uint16_t* x, const uint8_t* packed, const float* scales,
     }
 
     GemvPlan p;
-    if (!plan_gemv(M, N, (int)Kp, 2, current_sm_count(), &p)) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (!plan_gemv(M, N, (int)Kp, group_size, 2, current_sm_count(), &p)) return W4_ERR_UNSUPPORTED_SHAPE;
     GemvArgs a{};
     rc = split_workspace(p, workspace, workspace_bytes, &a.tickets, &a.partial);
     if (rc) return rc;
     a.x = x; a.scales = scales; a.zeros = zeros; a.bias = bias; a.y = y;
+    a.xtma = (K % 8) == 0;
     a.err = device_error_flag();
     if (!a.err) return W4_ERR_CUDA;
     a.M = M; a.N = N; a.K = K; a.Kp = (int)Kp; a.G = group_size; a.Ng = (int)(Kp / group_size);
@@ -189,7 +190,7 @@ int w4a8_quantize_act(const uint16_t* x, int M, int K, int group_size, int8_t* q
 size_t w4a8_workspace_bytes(int M, int N, int K, int group_size) {
     if (M <= 0 || M > 16 || N <= 0 || check_group(K, group_size)) return 0;
     GemvPlan p;
-    if (!plan_gemv(M, N, (int)padded_k(K, group_size), 1, current_sm_count(), &p)) return 0;
+    if (!plan_gemv(M, N, (int)padded_k(K, group_size), group_size, 1, current_sm_count(), &p)) return 0;
     return p.ws_bytes;
 }
 
@@ -211,7 +212,7 @@ int w4a8_linear(const int8_t* qx, const float* sx, const uint8_t* packed,
     if (M == 0) return W4_OK;
     if (M > 16) return W4_ERR_UNSUPPORTED_SHAPE;
     GemvPlan p;
-    if (!plan_gemv(M, N, (int)Kp, 1, current_sm_count(), &p)) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (!plan_gemv(M, N, (int)Kp, group_size, 1, current_sm_count(), &p)) return W4_ERR_UNSUPPORTED_SHAPE;
     GemvArgs a{};
     rc = split_workspace(p, workspace, workspace_bytes, &a.tickets, &a.partial);
     if (rc) return rc;

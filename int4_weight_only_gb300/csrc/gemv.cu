@@ -20,14 +20,17 @@
 // order, so results are deterministic.
 //
 // W4A16 inner product: each 32-bit ldmatrix word holds 8 codes of one row;
-// one LOP3 per pair ORs the code into the mantissa of bf16 128.0, and these
-// words (128 + code, exact) feed mma.sync m16n8k16 directly as the A operand
-// (16 weight rows), with the activations as the B operand (8 tokens per
-// n-tile).  The order of k inside a 32-column chunk is permuted identically on
-// both operands, so no data shuffles are needed.  All MMAs between two
-// flushes see columns of one group: at the flush the (128 + z) * sum(x) term
-// of that run of columns is removed and the group scale applied to the fp32
-// partial sums, so the weights stay exact.
+// one LOP3 per pair ORs the codes into the mantissa of fp16 1024.0 (both
+// nibbles of a byte fit the 10-bit mantissa, as 1024 + c and 1024 + 16c), and
+// these exact words feed mma.sync m16n8k16 (fp16 inputs, fp32 accumulation)
+// directly as the A operand (16 weight rows), with the activations as the B
+// operand (8 tokens per n-tile).  The activations are converted to fp16
+// exactly: each group's run of columns is scaled by a power of two first (and
+// scaled back at the flush), odd columns also by 1/16.  The order of k inside a 32-column chunk is permuted
+// identically on both operands, so no data shuffles are needed.  All MMAs
+// between two flushes see columns of one group: at the flush the offset
+// terms of that run of columns are removed and the group scale applied to the
+// fp32 partial sums, so the weights stay exact.
 //
 // Launch: programmatic dependent launch.  Before waiting for the previous
 // kernel on the stream, the producer only prefetches the first stages of its
@@ -52,7 +55,9 @@ struct SmemCtl {
     uint64_t empty[NS];
     int abort;
     int last;
-    int sumq[16];
+    int sumq[16];          // W4A8: sum of q_x over the slice, per token
+    uint64_t xfull;        // activation slice landed (TMA staging)
+    uint64_t xempty;       // consumers released the activation buffer
 };
 constexpr int kCtlBytes = 256;
 static_assert(sizeof(SmemCtl) <= kCtlBytes, "control block");
@@ -93,8 +98,8 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int c
 }
 
 // Producer: one thread streams every stage of every unit of this CTA.
-__device__ void gemv_producer(const CUtensorMap* tm, uint8_t* wbuf, SmemCtl* ctl,
-                              const GemvArgs& a) {
+__device__ void gemv_producer(const CUtensorMap* tm, uint8_t* wbuf, uint8_t* xbuf,
+                              SmemCtl* ctl, const GemvArgs& a) {
     const int boxes = 128 / a.R;
     const int box_bytes = a.R * 128;
     const int kbytes = a.Kp / 2;
@@ -111,11 +116,31 @@ __device__ void gemv_producer(const CUtensorMap* tm, uint8_t* wbuf, SmemCtl* ctl
     }
     grid_dep_wait();
     const uint64_t pol = policy_evict_first();
-    uint32_t it = 0;
+    uint32_t it = 0, xi = 0;
+    int pv0 = -1, pv1 = -1;
     bool ok = true;
     for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
         int rb, s, ks0, ks1;
         unit_coords(u, a, rb, s, ks0, ks1);
+        if (a.xtma && (ks0 != pv0 || ks1 != pv1)) {
+            // the activation slice goes out before this unit's weights
+            if (xi > 0 && !mbar_wait(&ctl->xempty, (xi - 1) & 1, &ctl->abort, a.err)) {
+                ok = false;
+                break;
+            }
+            const int k0 = ks0 * a.SKE;
+            const int ncol = min((ks1 - ks0) * a.SKE, a.K - k0);
+            const uint32_t nbytes = ncol > 0 ? (uint32_t)ncol * 2u : 0u;
+            mbar_arrive_expect_tx(&ctl->xfull, nbytes * (uint32_t)a.M);
+            if (nbytes)
+                for (int m = 0; m < a.M; ++m)
+                    bulk_load(xbuf + (size_t)m * a.XS,
+                              static_cast<const uint16_t*>(a.x) + (size_t)m * a.K + k0, nbytes,
+                              &ctl->xfull);
+            ++xi;
+            pv0 = ks0;
+            pv1 = ks1;
+        }
         for (int ks = ks0; ks < ks1; ++ks, ++it) {
             const int slot = it % NS;
             if (it >= (uint32_t)NS &&
@@ -136,19 +161,29 @@ __device__ void gemv_producer(const CUtensorMap* tm, uint8_t* wbuf, SmemCtl* ctl
         const uint32_t first = it > (uint32_t)NS ? it - NS : 0;
         for (uint32_t j = first; j < it; ++j)
             mbar_wait_drain(&ctl->full[j % NS], (j / NS) & 1, a.err);
+        if (xi > 0) mbar_wait_drain(&ctl->xfull, (xi - 1) & 1, a.err);
     }
 }
 
-// Activations of one unit into shared memory, bf16, columns [k0, k0+nk).
-// Within every 8-column block the order is (0,4,1,5,2,6,3,7), the order in
-// which nibbles_to_bf16x2_biased emits weights; columns >= K are zero.  One
-// thread per 8-column block; nk is a multiple of 256, so the 32 blocks a warp
-// handles belong to one token and every run of CPG*4 lanes is one segment of
-// CPG*32 columns.  The segment's sum of x (blocks added by a fixed butterfly)
-// goes to xseg[segment * M + token].
-template <int CPG>
-__device__ void stage_x_bf16(uint8_t* xbuf, float* xseg, const uint16_t* x, int M, int K,
-                             int XS, int k0, int nk, int tid) {
+// Activations of one unit into shared memory as fp16, columns [k0, k0+nk).
+// One thread per 8-column block; nk is a multiple of 256, so the 32 blocks
+// of a warp belong to one token and every run of CPG*4 lanes is one segment
+// of CPG*32 columns (one group's share of a box).  bf16 values are exactly
+// representable in fp16 once a segment is scaled by a power of two 2^-e that
+// puts its max|x| in [2^14, 2^15); odd columns of every 8-column block are
+// further divided by 16 (exact) to match the 1024 + 16c weights of
+// nibbles_to_f16x2_biased, and each block is stored in the order
+// (0,4,1,5,2,6,3,7).  Columns >= K are zero.  Per segment and token,
+// xseg[4 * (segment * M + token) + {0, 1, 2}] holds u = 2^e,
+// u * (1024 E + 64 O) and u * (E + O), with E and O the sums of the scaled
+// x over even and odd columns (added in a fixed butterfly order): the MMA of
+// the segment then equals u^-1 * (sum (c - z) x) + C0 + z * C1.
+// FROM_SMEM: the raw bf16 slice was already copied into xbuf (row m at
+// m * XS, natural order) and is converted in place; columns >= K hold stale
+// data there and are replaced by zeros.
+template <int CPG, bool FROM_SMEM>
+__device__ void stage_x_f16(uint8_t* xbuf, float* xseg, const uint16_t* x, int M, int K,
+                            int XS, int k0, int nk, int tid) {
     constexpr int LPS = CPG * 4;            // lanes (blocks) per segment
     const int nb = nk >> 3;
     const bool vec = (K & 7) == 0;
@@ -157,7 +192,14 @@ __device__ void stage_x_bf16(uint8_t* xbuf, float* xseg, const uint16_t* x, int 
         const int k = k0 + b * 8;
         uint32_t q[4];
         const uint16_t* src = x + (size_t)m * K + k;
-        if (vec && k + 8 <= K) {
+        if (FROM_SMEM) {
+            if (k < K) {
+                const uint4 v = *reinterpret_cast<const uint4*>(xbuf + (size_t)m * XS + b * 16);
+                q[0] = v.x; q[1] = v.y; q[2] = v.z; q[3] = v.w;
+            } else {
+                q[0] = q[1] = q[2] = q[3] = 0u;
+            }
+        } else if (vec && k + 8 <= K) {
             const uint4 v = __ldg(reinterpret_cast<const uint4*>(src));
             q[0] = v.x; q[1] = v.y; q[2] = v.z; q[3] = v.w;
         } else {
@@ -167,21 +209,37 @@ __device__ void stage_x_bf16(uint8_t* xbuf, float* xseg, const uint16_t* x, int 
 #pragma unroll
             for (int j = 0; j < 4; ++j) q[j] = (uint32_t)e[2 * j] | ((uint32_t)e[2 * j + 1] << 16);
         }
-        float sum = 0.f;
+        unsigned mx = 0;                      // bits of max|x| (non-negative floats order as ints)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            mx = max(mx, max((q[j] << 16) & 0x7FFFFFFFu, q[j] & 0x7FFF0000u));
+#pragma unroll
+        for (int o = 1; o < LPS; o <<= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        const int E = (int)(mx >> 23) - 127;
+        const int e = mx == 0 ? 0 : max(E - 14, -100);
+        const float sc = __int_as_float((127 - e) << 23);
+        float v[8];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            sum += __uint_as_float(q[j] << 16);
-            sum += __uint_as_float(q[j] & 0xFFFF0000u);
+            v[2 * j] = __uint_as_float(q[j] << 16) * sc;
+            v[2 * j + 1] = __uint_as_float(q[j] & 0xFFFF0000u) * sc;
         }
+        float se = (v[0] + v[2]) + (v[4] + v[6]);
+        float so = (v[1] + v[3]) + (v[5] + v[7]);
 #pragma unroll
-        for (int o = 1; o < LPS; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-        if ((b % LPS) == 0) xseg[(b / LPS) * M + m] = sum;
-        uint4 o;
-        o.x = __byte_perm(q[0], q[2], 0x5410);   // (x0, x4)
-        o.y = __byte_perm(q[0], q[2], 0x7632);   // (x1, x5)
-        o.z = __byte_perm(q[1], q[3], 0x5410);   // (x2, x6)
-        o.w = __byte_perm(q[1], q[3], 0x7632);   // (x3, x7)
-        *reinterpret_cast<uint4*>(xbuf + (size_t)m * XS + b * 16) = o;
+        for (int o = 1; o < LPS; o <<= 1) {
+            se += __shfl_xor_sync(0xffffffffu, se, o);
+            so += __shfl_xor_sync(0xffffffffu, so, o);
+        }
+        if ((b % LPS) == 0) {
+            const float u = __int_as_float((127 + e) << 23);
+            *reinterpret_cast<float4*>(xseg + 4 * ((b / LPS) * M + m)) =
+                make_float4(u, u * fmaf(1024.f, se, 64.f * so), u * (se + so), 0.f);
+        }
+        const float s16 = 0.0625f;
+        *reinterpret_cast<uint4*>(xbuf + (size_t)m * XS + b * 16) =
+            make_uint4(pack_f16x2(v[0], v[4]), pack_f16x2(v[1] * s16, v[5] * s16),
+                       pack_f16x2(v[2], v[6]), pack_f16x2(v[3] * s16, v[7] * s16));
     }
 }
 
@@ -236,6 +294,8 @@ __device__ __forceinline__ Smem gemv_init(const CUtensorMap* tm, const GemvArgs&
             mbar_init(&sm.ctl->full[i], 1);
             mbar_init(&sm.ctl->empty[i], CW);
         }
+        mbar_init(&sm.ctl->xfull, 1);
+        mbar_init(&sm.ctl->xempty, 1);
         sm.ctl->abort = 0;
         sm.ctl->last = 0;
         for (int i = 0; i < 16; ++i) sm.ctl->sumq[i] = 0;
@@ -264,50 +324,70 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
     constexpr int SEG = 8 / CPG;
     constexpr int LOG_CPG = CPG == 8 ? 3 : CPG == 4 ? 2 : CPG == 2 ? 1 : 0;
     constexpr bool PF = SEG <= 2;           // scales one stage ahead when they are few
+    // kernel arguments in registers (asm statements with memory clobbers
+    // would otherwise force re-reads from parameter space)
+    const int M = a.M, N = a.N, K = a.K, Kp = a.Kp, Ng = a.Ng, SKE = a.SKE, XS = a.XS;
+    const int units = a.units, Sp = a.S, spl = a.spl, nst = a.nst, R = a.R;
+    const float* __restrict__ scales = a.scales;
+    const uint8_t* __restrict__ zeros = a.zeros;
+    const float* __restrict__ bias = a.bias;
+    uint16_t* __restrict__ y = a.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int tig = lane & 3, gid = lane >> 2;
-    const int WR = a.R / 16, WK = CW / WR;
+    const int WR = R / 16, WK = CW / WR;
     const int rt = warp % WR, kp = warp / WR;
     const uint16_t* x = static_cast<const uint16_t*>(a.x);
     const uint32_t wbuf_u = smem_u32(sm.wbuf), xbuf_u = smem_u32(sm.xbuf);
     const int lj = lane >> 3, li = lane & 7;
     // this warp's 16 x 256 box inside a stage, and the ldmatrix row and
     // swizzled chunk offset of this lane for each chunk pair
-    const uint32_t l_off = (uint32_t)(kp * a.R * 128 + (rt * 16 + ((lj & 1) << 3) + li) * 128);
+    const uint32_t l_off = (uint32_t)(kp * R * 128 + (rt * 16 + ((lj & 1) << 3) + li) * 128);
     uint32_t l_cp[4];
 #pragma unroll
     for (int cp = 0; cp < 4; ++cp) l_cp[cp] = l_off + ((uint32_t)((2 * cp + (lj >> 1)) ^ li) << 4);
     uint32_t xrow[NT];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-        xrow[nt] = xbuf_u + (uint32_t)(min(nt * 8 + gid, a.M - 1) * a.XS + tig * 16 + kp * 512);
     int xt[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-        xt[nt][0] = min(nt * 8 + 2 * tig, a.M - 1);
-        xt[nt][1] = min(nt * 8 + 2 * tig + 1, a.M - 1);
+        xrow[nt] = xbuf_u + (uint32_t)(min(nt * 8 + gid, M - 1) * XS + tig * 16 + kp * 512);
+        xt[nt][0] = 4 * min(nt * 8 + 2 * tig, M - 1);
+        xt[nt][1] = 4 * min(nt * 8 + 2 * tig + 1, M - 1);
     }
     // group of a segment: segments of CPG*32 columns tile the groups exactly,
     // so g = segment / (G / (CPG*32)), a shift when that ratio is a power of 2
     const int gdiv = a.G / (CPG * 32);
     const int gshift = (gdiv & (gdiv - 1)) == 0 ? __ffs(gdiv) - 1 : -1;
     const float zc[4] = {0.f, 0.f, 0.f, 0.f};
+    SmemCtl* ctl = sm.ctl;
+    const bool xtma = a.xtma != 0;
 
     grid_dep_wait();
-    uint32_t it = 0;
+    uint32_t it = 0, xi = 0;
     int prev0 = -1, prev1 = -1;
-    for (int u = blockIdx.x; u < a.units; u += gridDim.x) {
-        int rb, s, ks0, ks1;
-        unit_coords(u, a, rb, s, ks0, ks1);
-        const int row0 = rb * a.R + rt * 16;
-        const int nr = min(row0 + gid, a.N - 1), nr8 = min(row0 + gid + 8, a.N - 1);
-        const float* sc_r = a.scales + (size_t)nr * a.Ng;
-        const float* sc_r8 = a.scales + (size_t)nr8 * a.Ng;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+        const int rb = u / Sp, s = u - rb * Sp;
+        const int ks0 = s * spl, ks1 = min(ks0 + spl, nst);
+        const int row0 = rb * R + rt * 16;
+        const int nr = min(row0 + gid, N - 1), nr8 = min(row0 + gid + 8, N - 1);
+        const float* sc_r = scales + (size_t)nr * Ng;
+        const float* sc_r8 = scales + (size_t)nr8 * Ng;
+        const uint8_t* zp_r = ASYM ? zeros + (size_t)nr * Ng : nullptr;
+        const uint8_t* zp_r8 = ASYM ? zeros + (size_t)nr8 * Ng : nullptr;
 
         named_bar_sync(1, NCT);
         if (ks0 != prev0 || ks1 != prev1) {
-            stage_x_bf16<CPG>(sm.xbuf, sm.xseg, x, a.M, a.K, a.XS, ks0 * a.SKE,
-                              (ks1 - ks0) * a.SKE, tid);
+            if (xtma) {
+                // everyone is past the previous slice: release its buffer,
+                // then wait for this slice's copy and convert it in place
+                if (xi > 0 && tid == 0) mbar_arrive(&ctl->xempty);
+                if (mbar_wait(&ctl->xfull, xi & 1, &ctl->abort, a.err))
+                    stage_x_f16<CPG, true>(sm.xbuf, sm.xseg, x, M, K, XS, ks0 * SKE,
+                                           (ks1 - ks0) * SKE, tid);
+                ++xi;
+            } else {
+                stage_x_f16<CPG, false>(sm.xbuf, sm.xseg, x, M, K, XS, ks0 * SKE,
+                                        (ks1 - ks0) * SKE, tid);
+            }
             named_bar_sync(1, NCT);
             prev0 = ks0;
             prev1 = ks1;
@@ -319,69 +399,80 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) acc[nt][j] = 0.f;
 
-        // The MMA sums x * (128 + code) over each run of CPG chunks (one
-        // group); the flush removes (128 + z) * sum(x) of that run and applies
-        // the scale: acc += s * (tmp - (128 + z) * xs).
-        float sr[SEG], sr8[SEG], cz[SEG], cz8[SEG];
+        // The MMA sums x' * w' over each run of CPG chunks (one group), with
+        // w' = 1024 + c on even and 1024 + 16c on odd columns and x' the
+        // segment's scaled activations (odd ones / 16); with the segment's
+        // (u, C0, C1) from staging, acc += s * (u * tmp - C0 - z * C1).
+        float sr[SEG], sr8[SEG], zr[SEG], zr8[SEG];
         auto load_scales = [&](int kw, float* r_, float* r8_, float* z_, float* z8_) {
 #pragma unroll
             for (int j = 0; j < SEG; ++j) {
                 const int sg = (kw >> (5 + LOG_CPG)) + j;
-                const int g = min(gshift >= 0 ? (sg >> gshift) : sg / gdiv, a.Ng - 1);
+                const int g = min(gshift >= 0 ? (sg >> gshift) : sg / gdiv, Ng - 1);
                 r_[j] = __ldg(sc_r + g);
                 r8_[j] = __ldg(sc_r8 + g);
                 if (ASYM) {
-                    z_[j] = 128.f + (float)__ldg(a.zeros + (size_t)nr * a.Ng + g);
-                    z8_[j] = 128.f + (float)__ldg(a.zeros + (size_t)nr8 * a.Ng + g);
-                } else {
-                    z_[j] = z8_[j] = 136.f;                 // 128 + 8
+                    z_[j] = (float)__ldg(zp_r + g);
+                    z8_[j] = (float)__ldg(zp_r8 + g);
                 }
             }
         };
-        if (PF) load_scales(min(ks0 * a.SKE + kp * 256, a.Kp - 1), sr, sr8, cz, cz8);
+        if (PF) load_scales(min(ks0 * SKE + kp * 256, Kp - 1), sr, sr8, zr, zr8);
 
         for (int ks = ks0; ks < ks1; ++ks, ++it) {
             const int slot = it % NS;
-            const int kw = ks * a.SKE + kp * 256;          // first column of this warp's box
-            float nsr[SEG], nsr8[SEG], ncz[SEG], ncz8[SEG];
+            const int kw = ks * SKE + kp * 256;            // first column of this warp's box
+            float nsr[SEG], nsr8[SEG], nzr[SEG], nzr8[SEG];
             if (PF && ks + 1 < ks1)
-                load_scales(min(kw + a.SKE, a.Kp - 1), nsr, nsr8, ncz, ncz8);
-            if (kw < a.Kp) {
-                if (!PF) load_scales(kw, sr, sr8, cz, cz8);
-                if (mbar_wait(&sm.ctl->full[slot], (it / NS) & 1, &sm.ctl->abort, a.err)) {
+                load_scales(min(kw + SKE, Kp - 1), nsr, nsr8, nzr, nzr8);
+            if (kw < Kp) {
+                if (!PF) load_scales(kw, sr, sr8, zr, zr8);
+                if (mbar_wait(&ctl->full[slot], (it / NS) & 1, &ctl->abort, a.err)) {
                     const uint32_t wst = wbuf_u + slot * STAGE_BYTES;
-                    const uint32_t xoff = (uint32_t)(ks - ks0) * (uint32_t)(a.SKE * 2);
+                    const uint32_t xoff = (uint32_t)(ks - ks0) * (uint32_t)(SKE * 2);
                     const float* xs_st =
-                        sm.xseg + (((ks - ks0) * a.SKE + kp * 256) >> (5 + LOG_CPG)) * a.M;
+                        sm.xseg + 4 * ((((ks - ks0) * SKE + kp * 256) >> (5 + LOG_CPG)) * M);
                     float tmp[NT][4];
 #pragma unroll
                     for (int cp = 0; cp < 4; ++cp) {
                         uint32_t r[4];
-                        ldmatrix_x4(wst + l_cp[cp], r[0], r[1], r[2], r[3]);
+                        ldmatrix_x4_nc(wst + l_cp[cp], r[0], r[1], r[2], r[3]);
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
                             const int c = 2 * cp + h;
                             const int seg = c / CPG;
                             uint32_t P[4], Q[4];
-                            nibbles_to_bf16x2_biased(r[2 * h], P);
-                            nibbles_to_bf16x2_biased(r[2 * h + 1], Q);
+                            nibbles_to_f16x2_biased(r[2 * h], P);
+                            nibbles_to_f16x2_biased(r[2 * h + 1], Q);
 #pragma unroll
                             for (int nt = 0; nt < NT; ++nt) {
                                 uint32_t X[4];
                                 lds128(xrow[nt] + xoff + c * 64, X);
-                                mma_bf16_16816(tmp[nt], P[0], Q[0], P[1], Q[1], X[0], X[1],
-                                               (c % CPG == 0) ? zc : tmp[nt]);
-                                mma_bf16_16816(tmp[nt], P[2], Q[2], P[3], Q[3], X[2], X[3], tmp[nt]);
+                                mma_f16_16816(tmp[nt], P[0], Q[0], P[1], Q[1], X[0], X[1],
+                                              (c % CPG == 0) ? zc : tmp[nt]);
+                                mma_f16_16816(tmp[nt], P[2], Q[2], P[3], Q[3], X[2], X[3], tmp[nt]);
                             }
                             if ((c + 1) % CPG == 0) {
 #pragma unroll
                                 for (int nt = 0; nt < NT; ++nt) {
-                                    const float xs0 = xs_st[seg * a.M + xt[nt][0]];
-                                    const float xs1 = xs_st[seg * a.M + xt[nt][1]];
-                                    acc[nt][0] = fmaf(sr[seg], fmaf(-cz[seg], xs0, tmp[nt][0]), acc[nt][0]);
-                                    acc[nt][1] = fmaf(sr[seg], fmaf(-cz[seg], xs1, tmp[nt][1]), acc[nt][1]);
-                                    acc[nt][2] = fmaf(sr8[seg], fmaf(-cz8[seg], xs0, tmp[nt][2]), acc[nt][2]);
-                                    acc[nt][3] = fmaf(sr8[seg], fmaf(-cz8[seg], xs1, tmp[nt][3]), acc[nt][3]);
+                                    const float4 e0 = *reinterpret_cast<const float4*>(
+                                        xs_st + 4 * seg * M + xt[nt][0]);
+                                    const float4 e1 = *reinterpret_cast<const float4*>(
+                                        xs_st + 4 * seg * M + xt[nt][1]);
+                                    float c00, c01, c10, c11;   // C0 + z C1 per (row, token)
+                                    if (ASYM) {
+                                        c00 = fmaf(zr[seg], e0.z, e0.y);
+                                        c01 = fmaf(zr[seg], e1.z, e1.y);
+                                        c10 = fmaf(zr8[seg], e0.z, e0.y);
+                                        c11 = fmaf(zr8[seg], e1.z, e1.y);
+                                    } else {
+                                        c00 = c10 = fmaf(8.f, e0.z, e0.y);
+                                        c01 = c11 = fmaf(8.f, e1.z, e1.y);
+                                    }
+                                    acc[nt][0] = fmaf(sr[seg], fmaf(e0.x, tmp[nt][0], -c00), acc[nt][0]);
+                                    acc[nt][1] = fmaf(sr[seg], fmaf(e1.x, tmp[nt][1], -c01), acc[nt][1]);
+                                    acc[nt][2] = fmaf(sr8[seg], fmaf(e0.x, tmp[nt][2], -c10), acc[nt][2]);
+                                    acc[nt][3] = fmaf(sr8[seg], fmaf(e1.x, tmp[nt][3], -c11), acc[nt][3]);
                                 }
                             }
                         }
@@ -391,11 +482,12 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
             if (PF) {
 #pragma unroll
                 for (int j = 0; j < SEG; ++j) {
-                    sr[j] = nsr[j]; sr8[j] = nsr8[j]; cz[j] = ncz[j]; cz8[j] = ncz8[j];
+                    sr[j] = nsr[j]; sr8[j] = nsr8[j];
+                    if (ASYM) { zr[j] = nzr[j]; zr8[j] = nzr8[j]; }
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.ctl->empty[slot]);
+            if (lane == 0) mbar_arrive(&ctl->empty[slot]);
         }
 
         // ---- add the k-phases of each row tile, in order 0, 1, ..., WK-1
@@ -420,7 +512,7 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
         }
 
         // ---- epilogue: thread holds (token 8nt + 2tig + (j&1), row gid + 8(j>>1))
-        if (a.S == 1) {
+        if (Sp == 1) {
             if (kp == 0) {
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
@@ -428,9 +520,9 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
                     for (int j = 0; j < 4; ++j) {
                         const int t = nt * 8 + 2 * tig + (j & 1);
                         const int n = row0 + gid + 8 * (j >> 1);
-                        if (t < a.M && n < a.N) {
-                            const float b = a.bias ? __ldg(a.bias + n) : 0.f;
-                            a.y[(size_t)t * a.N + n] = f32_to_bf16_bits(acc[nt][j] + b);
+                        if (t < M && n < N) {
+                            const float b = bias ? __ldg(bias + n) : 0.f;
+                            y[(size_t)t * N + n] = f32_to_bf16_bits(acc[nt][j] + b);
                         }
                     }
             }
@@ -443,10 +535,10 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
                     for (int j = 0; j < 4; ++j) {
                         const int t = nt * 8 + 2 * tig + (j & 1);
                         const int n = row0 + gid + 8 * (j >> 1);
-                        if (t < a.M && n < a.N) part[((size_t)s * a.M + t) * a.N + n] = acc[nt][j];
+                        if (t < M && n < N) part[((size_t)s * M + t) * N + n] = acc[nt][j];
                     }
             }
-            if (split_k_arrive(a, sm.ctl, rb)) {
+            if (split_k_arrive(a, ctl, rb)) {
                 if (kp == 0) {
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt)
@@ -454,12 +546,12 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
                         for (int j = 0; j < 4; ++j) {
                             const int t = nt * 8 + 2 * tig + (j & 1);
                             const int n = row0 + gid + 8 * (j >> 1);
-                            if (t < a.M && n < a.N) {
+                            if (t < M && n < N) {
                                 float v = 0.f;
-                                for (int q = 0; q < a.S; ++q)
-                                    v += ld_cg_f32(part + ((size_t)q * a.M + t) * a.N + n);
-                                const float b = a.bias ? __ldg(a.bias + n) : 0.f;
-                                a.y[(size_t)t * a.N + n] = f32_to_bf16_bits(v + b);
+                                for (int q = 0; q < Sp; ++q)
+                                    v += ld_cg_f32(part + ((size_t)q * M + t) * N + n);
+                                const float b = bias ? __ldg(bias + n) : 0.f;
+                                y[(size_t)t * N + n] = f32_to_bf16_bits(v + b);
                             }
                         }
                 }
@@ -622,7 +714,7 @@ template <int NT, int CPG, bool ASYM>
 __device__ __forceinline__ void w4a16_body(const CUtensorMap* tm, const GemvArgs& a) {
     const Smem sm = gemv_init(tm, a);
     if (threadIdx.x >= NCT) {
-        if (threadIdx.x == NCT) gemv_producer(tm, sm.wbuf, sm.ctl, a);
+        if (threadIdx.x == NCT) gemv_producer(tm, sm.wbuf, sm.xbuf, sm.ctl, a);
     } else {
         w4a16_consumer<NT, CPG, ASYM>(sm, a);
     }
@@ -644,7 +736,7 @@ template <int MT>
 __device__ __forceinline__ void w4a8_body(const CUtensorMap* tm, const GemvArgs& a) {
     const Smem sm = gemv_init(tm, a);
     if (threadIdx.x >= NCT) {
-        if (threadIdx.x == NCT) gemv_producer(tm, sm.wbuf, sm.ctl, a);
+        if (threadIdx.x == NCT) gemv_producer(tm, sm.wbuf, sm.xbuf, sm.ctl, a);
     } else {
         w4a8_consumer<MT>(sm, a);
     }
@@ -708,17 +800,19 @@ int launch_w4a16_cpg(int cpg, const uint8_t* packed, const GemvArgs& a, const Ge
 
 }  // namespace
 
-bool plan_gemv(int M, int N, int Kp, int act_bytes, int sm_count, GemvPlan* out) {
-    if (M < 1 || M > 16 || N < 1 || Kp < 1 || sm_count < 1) return false;
+bool plan_gemv(int M, int N, int Kp, int G, int act_bytes, int sm_count, GemvPlan* out) {
+    if (M < 1 || M > 16 || N < 1 || Kp < 1 || G < 32 || sm_count < 1) return false;
+    const int gq = G / 32;
+    const int cpg = (gq % 8 == 0) ? 8 : (gq % 4 == 0) ? 4 : (gq % 2 == 0) ? 2 : 1;
     const int pad = act_bytes == 2 ? 64 : 16;
     // cross-warp reduction buffer: per thread NT*4 floats (W4A16) or MT*2 ints (W4A8)
     const int red = act_bytes == 2
         ? CW * 32 * ((M > 8 ? 2 : 1) * 4) * 4
         : CW * 32 * (M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16) * 2 * 4;
     const size_t fixed = 1024 + (size_t)NS * STAGE_BYTES + kCtlBytes + red;
-    // W4A16 also keeps one fp32 sum of x per token and 32 columns of the slice
+    // W4A16 also keeps four floats per token and segment of cpg*32 columns
     auto xseg_bytes = [&](int slice) -> size_t {
-        return act_bytes == 2 ? (size_t)M * (slice / 32) * 4 : 0;
+        return act_bytes == 2 ? (size_t)M * (slice / (cpg * 32)) * 16 : 0;
     };
     const double wbytes = (double)N * Kp / 2.0;
     const double bw_total = 6.5e12, bw_sm = 70e9;
@@ -743,7 +837,7 @@ bool plan_gemv(int M, int N, int Kp, int act_bytes, int sm_count, GemvPlan* out)
             const int nst = (Kp + SKE - 1) / SKE;
             const int NB = (N + R - 1) / R;
             const int spl_max =
-                (int)(per_tok / ((long)SKE * act_bytes + (act_bytes == 2 ? SKE / 8 : 0)));
+                (int)(per_tok / ((long)SKE * act_bytes + (act_bytes == 2 ? SKE / (2 * cpg) : 0)));
             if (spl_max < 1) continue;
             const int s_min = (nst + spl_max - 1) / spl_max;
             for (int S = s_min; S <= nst && S <= s_min + 64; ++S) {

@@ -69,7 +69,7 @@ extern "C" int w4a16_linear_noalloc(const uint16_t* x, const uint8_t* packed,
     if (M > 16) return W4_ERR_UNSUPPORTED_SHAPE;
 
     GemvPlan p;
-    if (!plan_gemv(M, N, (int)Kp, 2, current_sm_count(), &p)) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (!plan_gemv(M, N, (int)Kp, group_size, 2, current_sm_count(), &p)) return W4_ERR_UNSUPPORTED_SHAPE;
     if (p.ws_bytes > (size_t)W4_NOALLOC_SCRATCH_BYTES) return W4_ERR_SCRATCH_LIMIT;
 
     GemvArgs a{};
@@ -86,6 +86,7 @@ extern "C" int w4a16_linear_noalloc(const uint16_t* x, const uint8_t* packed,
         a.partial = static_cast<unsigned char*>(base) + ticket_bytes;
     }
     a.x = x; a.scales = scales; a.zeros = zeros; a.bias = bias; a.y = y;
+    a.xtma = (K % 8) == 0;
     a.err = device_error_flag();
     if (!a.err) return W4_ERR_CUDA;
     a.M = M; a.N = N; a.K = K; a.Kp = (int)Kp; a.G = group_size;

@@ -100,6 +100,17 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
         : "memory");
 }
 
+// 1D bulk copy global -> shared (16-byte aligned, size a multiple of 16),
+// completion signalled on `bar` as transaction bytes.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        :: "r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes),
+           "r"(smem_u32(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -125,12 +136,32 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr) : "memory");
 }
 
+// Same, without a memory clobber: for reads of shared memory whose ordering
+// is already fixed by a preceding mbarrier wait.
+__device__ __forceinline__ void ldmatrix_x4_nc(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                               uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+
 // D = A * B + C, m16n8k16, bf16 inputs, fp32 accumulators.
 __device__ __forceinline__ void mma_bf16_16816(float* d, uint32_t a0, uint32_t a1,
                                                uint32_t a2, uint32_t a3,
                                                uint32_t b0, uint32_t b1, const float* c) {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%10, %11, %12, %13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1),
+          "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
+}
+
+// D = A * B + C, m16n8k16, fp16 inputs, fp32 accumulators.
+__device__ __forceinline__ void mma_f16_16816(float* d, uint32_t a0, uint32_t a1,
+                                              uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1, const float* c) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
         "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%10, %11, %12, %13};"
         : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1),
@@ -170,6 +201,26 @@ __device__ __forceinline__ void nibbles_to_bf16x2_biased(uint32_t v, uint32_t* o
     o[1] = and_or(v >> 4, m, e);
     o[2] = and_or(v >> 8, m, e);
     o[3] = and_or(v >> 12, m, e);
+}
+
+// Eight codes c0..c7 of v -> four fp16x2 words, exact:
+//   (1024 + c0, 1024 + c4), (1024 + 16 c1, 1024 + 16 c5),
+//   (1024 + c2, 1024 + c6), (1024 + 16 c3, 1024 + 16 c7).
+// fp16 1024.0 (0x6400) has ten mantissa bits of spacing 1, so both nibbles
+// of a byte can be OR-ed in place; only one shift (by 8) is needed.
+__device__ __forceinline__ void nibbles_to_f16x2_biased(uint32_t v, uint32_t* o) {
+    const uint32_t e = 0x64006400u;
+    const uint32_t w = v >> 8;
+    o[0] = and_or(v, 0x000F000Fu, e);
+    o[1] = and_or(v, 0x00F000F0u, e);
+    o[2] = and_or(w, 0x000F000Fu, e);
+    o[3] = and_or(w, 0x00F000F0u, e);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
 }
 
 // ---------------------------------------------------------------- integer

@@ -46,7 +46,7 @@ struct GemvPlan {
 
 // act_bytes: bytes per activation element (2 for bf16, 1 for int8).
 // Returns false if no plan fits (M too large).
-bool plan_gemv(int M, int N, int Kp, int act_bytes, int sm_count, GemvPlan* plan);
+bool plan_gemv(int M, int N, int Kp, int G, int act_bytes, int sm_count, GemvPlan* plan);
 
 struct GemvArgs {
     const void* x;            // bf16 [M, K] (W4A16) or int8 [M, Kp] (W4A8)
@@ -61,6 +61,7 @@ struct GemvArgs {
     int* err;                 // device error flag
     int M, N, K, Kp, G, Ng;
     int R, SKE, nst, S, spl, units, XS, red;
+    int xtma;                 // activation rows are 16-byte aligned: stage them with TMA
 };
 
 // The launchers encode the tensor map of `packed` for the plan's box shape
