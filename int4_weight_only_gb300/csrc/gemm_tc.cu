@@ -11,14 +11,14 @@
 // D[128 weight rows x 256 tokens] (fp32, TMEM) += W_hat[128 x 64] * x[256 x 64]^T
 // per 64-column stage; W_hat = s (code - z) is rounded once to bf16.
 //
-// Warp roles (320 threads, one CTA per SM, persistent over output tiles):
+// Warp roles (448 threads, one CTA per SM, persistent over output tiles):
 //   warp 0     TMA: x tile (256 tokens x 64 columns, bf16, 128-byte swizzle)
 //              and packed tile (128 rows x 32 bytes) into a 4-stage ring
 //   warp 1     allocates 512 TMEM columns (two 256-column accumulators);
 //              one thread issues tcgen05.mma (M=128, N=256, K=16) x 4 per stage
-//   warps 2-5  dequantize one weight row each into the 128-byte-swizzled
-//              K-major bf16 A operand (3-stage ring)
-//   warps 6-9  epilogue: tcgen05.ld of the accumulator, + bias, bf16 stores
+//   warps 2-9  dequantize (one weight row and 32 columns per thread) into
+//              the 128-byte-swizzled K-major bf16 A operand (3-stage ring)
+//   warps 10-13 epilogue: tcgen05.ld of the accumulator, + bias, bf16 stores
 // Every mbarrier wait is bounded; a failed wait raises the CTA abort flag and
 // the device error flag, in-flight copies and MMAs are drained before exit.
 #include "w4_device.cuh"
@@ -35,7 +35,7 @@ constexpr int NSA = 3;                  // dequantized A stages
 constexpr int X_BYTES = BN * BK * 2;    // 32 KB
 constexpr int P_BYTES = BM * BK / 2;    // 4 KB
 constexpr int A_BYTES = BM * BK * 2;    // 16 KB
-constexpr int THREADS = 320;
+constexpr int THREADS = 448;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
 
@@ -84,7 +84,7 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NST; ++i) { mbar_init(&ctl->tfull[i], 1); mbar_init(&ctl->tempty[i], 1); }
-        for (int i = 0; i < NSA; ++i) { mbar_init(&ctl->afull[i], 128); mbar_init(&ctl->aempty[i], 1); }
+        for (int i = 0; i < NSA; ++i) { mbar_init(&ctl->afull[i], 256); mbar_init(&ctl->aempty[i], 1); }
         for (int i = 0; i < 2; ++i) { mbar_init(&ctl->accfull[i], 1); mbar_init(&ctl->accempty[i], 128); }
         mbar_init(&ctl->drain, 1);
         ctl->abort = 0;
@@ -162,35 +162,43 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
             tc_commit(&ctl->drain);
             mbar_wait_drain(&ctl->drain, 0, a.err);
         }
-    } else if (warp < 6) {
+    } else if (warp < 10) {
         // ------------------------------------------------------------ dequantize
-        const int r = (warp - 2) * 32 + lane;            // weight row within the tile
+        // 256 threads: weight row r of the tile, columns [32 h, 32 h + 32) of
+        // each 64-column stage
+        const int dw = warp - 2;
+        const int r = (dw & 3) * 32 + lane, h = dw >> 2;
         uint32_t it = 0, ia = 0;
         for (int u = blockIdx.x; u < a.ntiles; u += gridDim.x) {
             const int nb = u / a.TB;
             const int n = min(nb * BM + r, a.N - 1);
             const float* srow = a.scales + (size_t)n * a.Ng;
             const uint8_t* zrow = a.zeros ? a.zeros + (size_t)n * a.Ng : nullptr;
+            // scale (and offset -(128 + z) s) of this thread's 32 columns,
+            // loaded one stage ahead
+            auto group_of = [&](int ks) { return min((ks * BK + 32 * h) / a.G, a.Ng - 1); };
+            float sc = __ldg(srow + group_of(0));
+            float zz = zrow ? (float)__ldg(zrow + group_of(0)) : 8.f;
             for (int ks = 0; ks < a.nks; ++ks, ++it, ++ia) {
                 const int s = it % NST, sa = ia % NSA;
-                const int g0 = min((ks * BK) / a.G, a.Ng - 1);
-                const int g1 = min((ks * BK + 32) / a.G, a.Ng - 1);
-                const float s0 = __ldg(srow + g0), s1 = __ldg(srow + g1);
-                const float z0 = zrow ? (float)__ldg(zrow + g0) : 8.f;
-                const float z1 = zrow ? (float)__ldg(zrow + g1) : 8.f;
-                const float c0 = -(128.f + z0) * s0, c1 = -(128.f + z1) * s1;
+                float nsc = sc, nzz = zz;
+                if (ks + 1 < a.nks) {
+                    const int g = group_of(ks + 1);
+                    nsc = __ldg(srow + g);
+                    nzz = zrow ? (float)__ldg(zrow + g) : 8.f;
+                }
+                const float cc = -(128.f + zz) * sc;
                 bool ok = mbar_wait(&ctl->tfull[s], (it / NST) & 1, &ctl->abort, a.err);
                 if (ok && ia >= (uint32_t)NSA)
                     ok = mbar_wait(&ctl->aempty[sa], ((ia / NSA) & 1) ^ 1, &ctl->abort, a.err);
                 if (ok) {
-                    const uint4* prow = reinterpret_cast<const uint4*>(ps + s * P_BYTES + r * 32);
-                    const uint4 q0 = prow[0], q1 = prow[1];
-                    const uint32_t wv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                    const uint4 q = *reinterpret_cast<const uint4*>(ps + s * P_BYTES + r * 32 + h * 16);
+                    const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
                     uint8_t* arow = as + sa * A_BYTES + r * 128;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const float sc = j < 4 ? s0 : s1, cc = j < 4 ? c0 : c1;
-                        const uint32_t w = wv[j], wh = w >> 4;
+                    for (int jj = 0; jj < 4; ++jj) {
+                        const int j = 4 * h + jj;               // 16-byte chunk of the row
+                        const uint32_t w = wv[jj], wh = w >> 4;
                         // bf16x2 (128 + c_2i, 128 + c_2i+1) for i = 0..3
                         const uint32_t e = 0x43004300u, m = 0x000F000Fu;
                         const uint32_t p01 = and_or(prmt(w, wh, 0x5410), m, e);
@@ -207,6 +215,8 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                     fence_proxy_async_smem();
                     mbar_arrive(&ctl->afull[sa]);
                 }
+                sc = nsc;
+                zz = nzz;
             }
         }
     } else {
