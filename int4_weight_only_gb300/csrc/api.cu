@@ -130,7 +130,9 @@ size_t w4a16_workspace_bytes(int M, int N, int K, int group_size) {
         if (!plan_gemv(M, N, (int)Kp, group_size, 2, current_sm_count(), &p)) return 0;
         return p.ws_bytes;
     }
-    return 0;
+    GemmPlan g;
+    if (!plan_gemm(M, N, K, current_sm_count(), &g)) return 0;
+    return g.ws_bytes;
 }
 
 int w4a16_linear(const uint16_t* x, const uint8_t* packed, const float* scales,
@@ -152,10 +154,16 @@ int w4a16_linear(const uint16_t* x, const uint8_t* packed, const float* scales,
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (M > 16) {
         if (K % 8 != 0) return W4_ERR_UNSUPPORTED_SHAPE;
+        GemmPlan g;
+        if (!plan_gemm(M, N, K, current_sm_count(), &g)) return W4_ERR_UNSUPPORTED_SHAPE;
+        if (g.S > 1) {
+            if (!workspace || workspace_bytes < g.ws_bytes) return W4_ERR_WORKSPACE;
+            if (!aligned16(workspace)) return W4_ERR_MISALIGNED;
+        }
         int* err = device_error_flag();
         if (!err) return W4_ERR_CUDA;
         return launch_w4a16_gemm(x, packed, scales, zeros, bias, y, M, N, K, (int)Kp,
-                                 group_size, err, current_sm_count(), st);
+                                 group_size, g, workspace, err, st);
     }
 
     GemvPlan p;

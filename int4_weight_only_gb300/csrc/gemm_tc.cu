@@ -8,60 +8,83 @@
 // the shared-memory operand of the tensor-core MMA, so bf16 weights never
 // touch HBM.
 //
-// D[128 weight rows x 256 tokens] (fp32, TMEM) += W_hat[128 x 64] * x[256 x 64]^T
-// per 64-column stage; W_hat = s (code - z) is rounded once to bf16.
+// D[128 weight rows x BN tokens] (fp32, TMEM) += W_hat[128 x 64] * x[BN x 64]^T
+// per 64-column stage; W_hat = s (code - z) is rounded once to bf16.  BN is
+// 128 or 256.  A unit of work is (output tile, K slice).  When a plan splits
+// K S ways, the S units of a tile run side by side (consecutive units go to
+// consecutive CTAs), each writes fp32 partials for the tokens of the other
+// S-1, waits until all S have, and reduces its own 1/S of the tokens in
+// split order 0..S-1 (its own term straight from TMEM), so every output is
+// summed in the same order on every run.
 //
-// Warp roles (448 threads, one CTA per SM, persistent over output tiles):
-//   warp 0     TMA: x tile (256 tokens x 64 columns, bf16, 128-byte swizzle)
-//              and packed tile (128 rows x 32 bytes) into a 4-stage ring
-//   warp 1     allocates 512 TMEM columns (two 256-column accumulators);
-//              one thread issues tcgen05.mma (M=128, N=256, K=16) x 4 per stage
-//   warps 2-9  dequantize (one weight row and 32 columns per thread) into
-//              the 128-byte-swizzled K-major bf16 A operand (3-stage ring)
-//   warps 10-13 epilogue: tcgen05.ld of the accumulator, + bias, bf16 stores
+// Warp roles (704 threads, one CTA per SM, persistent over units):
+//   warp 0      TMA: x tile (BN tokens x 64 columns, bf16, 128-byte swizzle)
+//               and packed tile (128 rows x 32 bytes) into an NST-stage ring
+//   warp 1      allocates 2*BN TMEM columns (two accumulators); one thread
+//               issues tcgen05.mma (M=128, N=BN, K=16) x 4 per stage
+//   warps 2-17  dequantize into the 128-byte-swizzled K-major bf16 A
+//               operand: two groups of 8 warps take alternate stages, one
+//               weight row and 32 columns per thread
+//   warps 18-21 epilogue: tcgen05.ld of the accumulator, + bias, bf16 stores
+//               (or, with K split, the cooperative reduction below)
 // Every mbarrier wait is bounded; a failed wait raises the CTA abort flag and
 // the device error flag, in-flight copies and MMAs are drained before exit.
 #include "w4_device.cuh"
 #include "w4_internal.h"
 
+#include <cstdlib>
+
 namespace w4 {
 namespace {
 
 constexpr int BM = 128;                 // weight rows per tile (MMA M)
-constexpr int BN = 256;                 // tokens per tile (MMA N)
 constexpr int BK = 64;                  // columns per stage
-constexpr int NST = 4;                  // TMA stages
-constexpr int NSA = 3;                  // dequantized A stages
-constexpr int X_BYTES = BN * BK * 2;    // 32 KB
 constexpr int P_BYTES = BM * BK / 2;    // 4 KB
 constexpr int A_BYTES = BM * BK * 2;    // 16 KB
-constexpr int THREADS = 448;
-constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+constexpr int DQ_GROUP_THREADS = 256;   // dequantizing threads per stage
+constexpr int DQ_TPR = DQ_GROUP_THREADS / BM;  // threads per weight row
+constexpr int DQ_COLS = BK / DQ_TPR;     // columns per thread per stage
+constexpr int DQ_CHUNKS = DQ_COLS / 8;   // 16-byte bf16 chunks per thread
+constexpr int EPI_THREADS = 128;
+constexpr int DQ_BASE = 96;             // first dequantizing thread (after 3 role warps)
+
+// DQG groups of DQ_GROUP_THREADS dequantizing threads
+template <int DQG>
+__host__ __device__ constexpr int threads_of() { return DQ_BASE + DQG * DQ_GROUP_THREADS + EPI_THREADS; }
 
 struct GemmArgs {
     const float* scales;
     const uint8_t* zeros;
     const float* bias;
     uint16_t* y;
+    float* partial;     // [S, M, N] when S > 1
+    int* tickets;       // [ntiles] when S > 1
     int* err;
     int M, N, K, G, Ng;
-    int nks;        // k stages
+    int nks;        // k stages over K
     int TB;         // token blocks
     int ntiles;
+    int S, spl;     // K splits, stages per split
+    int units;      // ntiles * S
 };
 
+template <int NST, int NSA, int NSP>
 struct Ctl {
     uint64_t tfull[NST], tempty[NST];
+    uint64_t pfull[NSP], pempty[NSP];
     uint64_t afull[NSA], aempty[NSA];
     uint64_t accfull[2], accempty[2];
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
+    int last;   // the tile's splits are all written (split-K hand-off)
 };
 
-constexpr size_t kSmemBytes = 1024 + (size_t)NST * X_BYTES + (size_t)NSA * A_BYTES +
-                              (size_t)NST * P_BYTES + 256;
+template <int BN, int NST, int NSA, int NSP>
+constexpr size_t smem_bytes() {
+    return 1024 + (size_t)NST * BN * BK * 2 + (size_t)NSA * A_BYTES + (size_t)NSP * P_BYTES +
+           (sizeof(Ctl<NST, NSA, NSP>) + 15) / 16 * 16;
+}
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
     const uint32_t s = smem_u32(p);
@@ -71,23 +94,49 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-__global__ void __launch_bounds__(THREADS, 1)
+__device__ __forceinline__ void unit_of(const GemmArgs& a, int u, int& nb, int& tb, int& tile,
+                                        int& s, int& ks0, int& ks1) {
+    tile = u / a.S;
+    s = u - tile * a.S;
+    nb = tile / a.TB;
+    tb = tile - nb * a.TB;
+    ks0 = s * a.spl;
+    ks1 = min(ks0 + a.spl, a.nks);
+}
+
+template <int BN, int NST, int NSA, int NSP, int DQG>
+__global__ void __launch_bounds__(threads_of<DQG>(), 1)
 k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmP,
                 const GemmArgs a) {
+    constexpr int THREADS = threads_of<DQG>();
+    constexpr int X_BYTES = BN * BK * 2;
+    constexpr uint32_t TMEM_COLS = 2 * BN;
+    constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = align1024(smem_raw);
-    uint8_t* xs = base;                                     // NST x 32 KB
+    uint8_t* xs = base;                                     // NST x X_BYTES
     uint8_t* as = xs + NST * X_BYTES;                       // NSA x 16 KB
-    uint8_t* ps = as + NSA * A_BYTES;                       // NST x 4 KB
-    Ctl* ctl = reinterpret_cast<Ctl*>(ps + NST * P_BYTES);
+    uint8_t* ps = as + NSA * A_BYTES;                       // NSP x 4 KB
+    auto* ctl = reinterpret_cast<Ctl<NST, NSA, NSP>*>(ps + NSP * P_BYTES);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NST; ++i) { mbar_init(&ctl->tfull[i], 1); mbar_init(&ctl->tempty[i], 1); }
-        for (int i = 0; i < NSA; ++i) { mbar_init(&ctl->afull[i], 256); mbar_init(&ctl->aempty[i], 1); }
-        for (int i = 0; i < 2; ++i) { mbar_init(&ctl->accfull[i], 1); mbar_init(&ctl->accempty[i], 128); }
+        for (int i = 0; i < NSP; ++i) {
+            mbar_init(&ctl->pfull[i], 1);
+            mbar_init(&ctl->pempty[i], DQ_GROUP_THREADS / 32);
+        }
+        for (int i = 0; i < NSA; ++i) {
+            mbar_init(&ctl->afull[i], DQ_GROUP_THREADS / 32);
+            mbar_init(&ctl->aempty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&ctl->accfull[i], 1);
+            mbar_init(&ctl->accempty[i], EPI_THREADS);
+        }
         mbar_init(&ctl->drain, 1);
         ctl->abort = 0;
+        ctl->last = 0;
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) { tma_prefetch_desc(&tmX); tma_prefetch_desc(&tmP); }
@@ -97,31 +146,42 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     tc_fence_after();
     const uint32_t tmem_base = ctl->tmem_base;
 
-    if (warp == 0) {
+    if (warp == 0 || warp == 2) {
         // ------------------------------------------------------------ TMA
+        // warp 0 loads the x tiles (NST-stage ring, released by the MMAs),
+        // warp 2 the packed weight tiles (NSP-stage ring, released by the
+        // dequantizing threads once they hold the bytes in registers)
         if (lane == 0) {
-            const uint64_t pol_x = policy_evict_last();
-            const uint64_t pol_w = policy_evict_last();
+            const bool is_x = warp == 0;
+            const int ring = is_x ? NST : NSP;
+            uint64_t* full = is_x ? ctl->tfull : ctl->pfull;
+            uint64_t* empty = is_x ? ctl->tempty : ctl->pempty;
+            const uint64_t pol = is_x ? policy_evict_last() : policy_evict_first();
             uint32_t it = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < a.ntiles && ok; u += gridDim.x) {
-                const int nb = u / a.TB, tb = u - nb * a.TB;
-                for (int ks = 0; ks < a.nks; ++ks, ++it) {
-                    const int s = it % NST;
-                    if (it >= (uint32_t)NST &&
-                        !mbar_wait(&ctl->tempty[s], ((it / NST) & 1) ^ 1, &ctl->abort, a.err)) {
+            for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+                int nb, tb, tile, s, ks0, ks1;
+                unit_of(a, u, nb, tb, tile, s, ks0, ks1);
+                for (int ks = ks0; ks < ks1; ++ks, ++it) {
+                    const int st = it % ring;
+                    if (it >= (uint32_t)ring &&
+                        !mbar_wait(&empty[st], ((it / ring) & 1) ^ 1, &ctl->abort, a.err)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&ctl->tfull[s], X_BYTES + P_BYTES);
-                    tma_load_2d(xs + s * X_BYTES, &tmX, ks * BK, tb * BN, &ctl->tfull[s], pol_x);
-                    tma_load_2d(ps + s * P_BYTES, &tmP, ks * (BK / 2), nb * BM, &ctl->tfull[s], pol_w);
+                    if (is_x) {
+                        mbar_arrive_expect_tx(&full[st], X_BYTES);
+                        tma_load_2d(xs + st * X_BYTES, &tmX, ks * BK, tb * BN, &full[st], pol);
+                    } else {
+                        mbar_arrive_expect_tx(&full[st], P_BYTES);
+                        tma_load_2d(ps + st * P_BYTES, &tmP, ks * (BK / 2), nb * BM, &full[st], pol);
+                    }
                 }
             }
             if (!ok || ctl->abort) {
-                const uint32_t first = it > (uint32_t)NST ? it - NST : 0;
+                const uint32_t first = it > (uint32_t)ring ? it - ring : 0;
                 for (uint32_t j = first; j < it; ++j)
-                    mbar_wait_drain(&ctl->tfull[j % NST], (j / NST) & 1, a.err);
+                    mbar_wait_drain(&full[j % ring], (j / ring) & 1, a.err);
             }
         }
     } else if (warp == 1) {
@@ -129,7 +189,9 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
         if (lane == 0) {
             uint32_t it = 0, ia = 0, tc = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < a.ntiles && ok; u += gridDim.x, ++tc) {
+            for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x, ++tc) {
+                int nb, tb, tile, s, ks0, ks1;
+                unit_of(a, u, nb, tb, tile, s, ks0, ks1);
                 const uint32_t b = tc & 1;
                 if (tc >= 2 && !mbar_wait(&ctl->accempty[b], ((tc / 2) & 1) ^ 1, &ctl->abort, a.err)) {
                     ok = false;
@@ -137,22 +199,22 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                 }
                 tc_fence_after();
                 const uint32_t d = tmem_base + b * BN;
-                for (int ks = 0; ks < a.nks; ++ks, ++it, ++ia) {
-                    const int s = it % NST, sa = ia % NSA;
-                    if (!mbar_wait(&ctl->tfull[s], (it / NST) & 1, &ctl->abort, a.err) ||
+                for (int ks = ks0; ks < ks1; ++ks, ++it, ++ia) {
+                    const int st = it % NST, sa = ia % NSA;
+                    if (!mbar_wait(&ctl->tfull[st], (it / NST) & 1, &ctl->abort, a.err) ||
                         !mbar_wait(&ctl->afull[sa], (ia / NSA) & 1, &ctl->abort, a.err)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t a_addr = smem_u32(as + sa * A_BYTES);
-                    const uint32_t x_addr = smem_u32(xs + s * X_BYTES);
+                    const uint32_t x_addr = smem_u32(xs + st * X_BYTES);
 #pragma unroll
                     for (int i = 0; i < BK / 16; ++i)
                         tc_mma_f16(d, smem_desc_sw128(a_addr + 32 * i),
                                    smem_desc_sw128(x_addr + 32 * i), IDESC,
-                                   (ks | i) != 0 ? 1u : 0u);
-                    tc_commit(&ctl->tempty[s]);
+                                   (ks > ks0 || i > 0) ? 1u : 0u);
+                    tc_commit(&ctl->tempty[st]);
                     tc_commit(&ctl->aempty[sa]);
                 }
                 if (!ok) break;
@@ -162,42 +224,69 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
             tc_commit(&ctl->drain);
             mbar_wait_drain(&ctl->drain, 0, a.err);
         }
-    } else if (warp < 10) {
+    } else if (threadIdx.x < DQ_BASE + DQG * DQ_GROUP_THREADS) {
         // ------------------------------------------------------------ dequantize
-        // 256 threads: weight row r of the tile, columns [32 h, 32 h + 32) of
-        // each 64-column stage
-        const int dw = warp - 2;
-        const int r = (dw & 3) * 32 + lane, h = dw >> 2;
-        uint32_t it = 0, ia = 0;
-        for (int u = blockIdx.x; u < a.ntiles; u += gridDim.x) {
-            const int nb = u / a.TB;
+        // DQ_GROUPS groups take turns stage by stage, so that several stages
+        // are dequantized at once.  In a group, thread (r, h) converts weight
+        // row r, columns [DQ_COLS h, DQ_COLS h + DQ_COLS) of the stage; the
+        // threads of a row are neighbouring lanes, so a warp reads one
+        // contiguous span of the packed tile.
+        constexpr int DQ_GROUPS = DQG;
+        static_assert(NSP % DQ_GROUPS == 0 && NSA >= 2, "stage rings vs dequant groups");
+        const int dt = threadIdx.x - DQ_BASE;
+        const int grp = dt / DQ_GROUP_THREADS, gt = dt % DQ_GROUP_THREADS;
+        const int r = gt / DQ_TPR, h = gt % DQ_TPR;
+        uint32_t it = 0;
+        for (int u = blockIdx.x; u < a.units; u += gridDim.x) {
+            int nb, tb, tile, s, ks0, ks1;
+            unit_of(a, u, nb, tb, tile, s, ks0, ks1);
+            // first stage of this unit that falls to this group
+            const int lead = (int)((grp - it % DQ_GROUPS + DQ_GROUPS) % DQ_GROUPS);
+            it += (uint32_t)lead;
             const int n = min(nb * BM + r, a.N - 1);
             const float* srow = a.scales + (size_t)n * a.Ng;
             const uint8_t* zrow = a.zeros ? a.zeros + (size_t)n * a.Ng : nullptr;
-            // scale (and offset -(128 + z) s) of this thread's 32 columns,
-            // loaded one stage ahead
-            auto group_of = [&](int ks) { return min((ks * BK + 32 * h) / a.G, a.Ng - 1); };
-            float sc = __ldg(srow + group_of(0));
-            float zz = zrow ? (float)__ldg(zrow + group_of(0)) : 8.f;
-            for (int ks = 0; ks < a.nks; ++ks, ++it, ++ia) {
-                const int s = it % NST, sa = ia % NSA;
+            // scale (and offset -(128 + z) s) of this thread's columns,
+            // loaded one turn ahead
+            auto group_of = [&](int ks) { return min((ks * BK + DQ_COLS * h) / a.G, a.Ng - 1); };
+            const int kf = min(ks0 + lead, ks1 - 1);
+            float sc = __ldg(srow + group_of(kf));
+            float zz = zrow ? (float)__ldg(zrow + group_of(kf)) : 8.f;
+            int ks = ks0 + lead;
+            for (; ks < ks1; ks += DQ_GROUPS, it += DQ_GROUPS) {
+                const int sp = it % NSP, sa = it % NSA;
                 float nsc = sc, nzz = zz;
-                if (ks + 1 < a.nks) {
-                    const int g = group_of(ks + 1);
+                if (ks + DQ_GROUPS < ks1) {
+                    const int g = group_of(ks + DQ_GROUPS);
                     nsc = __ldg(srow + g);
                     nzz = zrow ? (float)__ldg(zrow + g) : 8.f;
                 }
                 const float cc = -(128.f + zz) * sc;
-                bool ok = mbar_wait(&ctl->tfull[s], (it / NST) & 1, &ctl->abort, a.err);
-                if (ok && ia >= (uint32_t)NSA)
-                    ok = mbar_wait(&ctl->aempty[sa], ((ia / NSA) & 1) ^ 1, &ctl->abort, a.err);
+                // one arrival per warp on pempty / afull (after __syncwarp),
+                // so a stage costs 2 x 8 barrier updates, not 2 x 256
+                bool ok = __all_sync(0xffffffffu,
+                                     mbar_wait(&ctl->pfull[sp], (it / NSP) & 1, &ctl->abort, a.err));
+                uint32_t wv[DQ_CHUNKS];
                 if (ok) {
-                    const uint4 q = *reinterpret_cast<const uint4*>(ps + s * P_BYTES + r * 32 + h * 16);
-                    const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+                    const uint8_t* prow = ps + sp * P_BYTES + r * (BK / 2) + h * (DQ_COLS / 2);
+                    if constexpr (DQ_CHUNKS == 4) {
+                        const uint4 q = *reinterpret_cast<const uint4*>(prow);
+                        wv[0] = q.x; wv[1] = q.y; wv[2] = q.z; wv[3] = q.w;
+                    } else {
+                        const uint2 q = *reinterpret_cast<const uint2*>(prow);
+                        wv[0] = q.x; wv[1] = q.y;
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&ctl->pempty[sp]);
+                }
+                if (ok && it >= (uint32_t)NSA)
+                    ok = mbar_wait(&ctl->aempty[sa], ((it / NSA) & 1) ^ 1, &ctl->abort, a.err);
+                ok = __all_sync(0xffffffffu, ok);
+                if (ok) {
                     uint8_t* arow = as + sa * A_BYTES + r * 128;
 #pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) {
-                        const int j = 4 * h + jj;               // 16-byte chunk of the row
+                    for (int jj = 0; jj < DQ_CHUNKS; ++jj) {
+                        const int j = DQ_CHUNKS * h + jj;       // 16-byte chunk of the row
                         const uint32_t w = wv[jj], wh = w >> 4;
                         // bf16x2 (128 + c_2i, 128 + c_2i+1) for i = 0..3
                         const uint32_t e = 0x43004300u, m = 0x000F000Fu;
@@ -213,37 +302,105 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                         *reinterpret_cast<uint4*>(arow + ((j ^ (r & 7)) << 4)) = o;
                     }
                     fence_proxy_async_smem();
-                    mbar_arrive(&ctl->afull[sa]);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&ctl->afull[sa]);
                 }
                 sc = nsc;
                 zz = nzz;
             }
+            // `it` now points past this unit by less than DQ_GROUPS stages
+            it -= (uint32_t)(ks - ks1);
         }
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;                            // TMEM lane quarter of this warp
         const int r = q * 32 + lane;
+        const int etid = threadIdx.x - (THREADS - EPI_THREADS);
+        // with K split S ways, split s of a tile reduces tokens [s SL, s SL + SL)
+        // of it (SL a multiple of 32) and hands the rest to the other splits
+        const int SL = ((BN + a.S - 1) / a.S + 31) / 32 * 32;
         uint32_t tc = 0;
-        for (int u = blockIdx.x; u < a.ntiles; u += gridDim.x, ++tc) {
-            const int nb = u / a.TB, tb = u - nb * a.TB;
+        for (int u = blockIdx.x; u < a.units; u += gridDim.x, ++tc) {
+            int nb, tb, tile, s, ks0, ks1;
+            unit_of(a, u, nb, tb, tile, s, ks0, ks1);
             const uint32_t b = tc & 1;
-            const bool ok = mbar_wait(&ctl->accfull[b], (tc / 2) & 1, &ctl->abort, a.err);
+            bool ok = mbar_wait(&ctl->accfull[b], (tc / 2) & 1, &ctl->abort, a.err);
             tc_fence_after();
             const int n = nb * BM + r;
             const float bn = (a.bias && n < a.N) ? __ldg(a.bias + n) : 0.f;
-            if (ok) {
-                for (int j = 0; j < BN / 32; ++j) {
+            const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + b * BN;
+            const int t0 = tb * BN;
+            if (ok && a.S == 1) {
+                for (int j = 0; j < BN / 32 && t0 + j * 32 < a.M; ++j) {
                     uint32_t v[32];
-                    tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + b * BN + j * 32, v);
+                    tmem_ld_32x32b_x32(tacc + j * 32, v);
                     tc_wait_ld();
                     if (n < a.N) {
 #pragma unroll
                         for (int i = 0; i < 32; ++i) {
-                            const int t = tb * BN + j * 32 + i;
+                            const int t = t0 + j * 32 + i;
                             if (t < a.M)
                                 a.y[(size_t)t * a.N + n] = f32_to_bf16_bits(__uint_as_float(v[i]) + bn);
                         }
                     }
+                }
+            } else if (ok) {
+                const int c0 = s * SL, c1 = min(c0 + SL, BN);
+                // 1. fp32 partials of the tokens the other splits reduce
+                for (int j = 0; j < BN / 32 && t0 + j * 32 < a.M; ++j) {
+                    if (j * 32 >= c0 && j * 32 < c1) continue;
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tacc + j * 32, v);
+                    tc_wait_ld();
+                    if (n < a.N) {
+                        float* dst = a.partial + ((size_t)s * a.M + t0 + j * 32) * a.N + n;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (t0 + j * 32 + i < a.M) dst[(size_t)i * a.N] = __uint_as_float(v[i]);
+                    }
+                }
+                // 2. publish them; wait until all S splits of the tile have
+                __threadfence();
+                named_bar_sync(2, EPI_THREADS);
+                if (etid == 0) {
+                    atomicAdd(&a.tickets[tile], 1);
+                    ctl->last = wait_counter_geq(&a.tickets[tile], a.S, &ctl->abort, a.err);
+                }
+                named_bar_sync(2, EPI_THREADS);
+                ok = ctl->last;
+                if (ok) {
+                    __threadfence();
+                    // 3. own slice: partials added in split order 0..S-1, this
+                    //    split's own term read straight from TMEM
+                    for (int j = c0 / 16; j * 16 < c1 && t0 + j * 16 < a.M; ++j) {
+                        float acc[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+                        for (int qq = 0; qq < a.S; ++qq) {
+                            uint32_t v[16];
+                            if (qq == s) {
+                                tmem_ld_32x32b_x16(tacc + j * 16, v);
+                                tc_wait_ld();
+                            } else if (n < a.N) {
+                                const float* src = a.partial + ((size_t)qq * a.M + t0 + j * 16) * a.N + n;
+#pragma unroll
+                                for (int i = 0; i < 16; ++i)
+                                    v[i] = t0 + j * 16 + i < a.M ? __float_as_uint(ld_cg_f32(src + (size_t)i * a.N)) : 0u;
+                            }
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) acc[i] += __uint_as_float(v[i]);
+                        }
+                        if (n < a.N) {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                const int t = t0 + j * 16 + i;
+                                if (t < a.M) a.y[(size_t)t * a.N + n] = f32_to_bf16_bits(acc[i] + bn);
+                            }
+                        }
+                    }
+                    // 4. the last of the S splits to get here resets the counter
+                    named_bar_sync(2, EPI_THREADS);
+                    if (etid == 0 && atomicAdd(&a.tickets[tile], 1) == 2 * a.S - 1) a.tickets[tile] = 0;
                 }
             }
             tc_fence_before();
@@ -259,30 +416,92 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     }
 }
 
+template <int BN, int NST, int NSA, int NSP, int DQG>
+int launch_bn(const uint16_t* x, const uint8_t* packed, const GemmPlan& p, GemmArgs& a,
+              int Kp, cudaStream_t stream) {
+    CUtensorMap tmX, tmP;
+    if (!encode_tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, (uint64_t)a.K, (uint64_t)a.M,
+                        (uint64_t)a.K * 2, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B))
+        return W4_ERR_CUDA;
+    if (!encode_tmap_2d(&tmP, CU_TENSOR_MAP_DATA_TYPE_UINT8, packed, (uint64_t)(Kp / 2),
+                        (uint64_t)a.N, (uint64_t)(Kp / 2), BK / 2, BM, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return W4_ERR_CUDA;
+    constexpr size_t smem = smem_bytes<BN, NST, NSA, NSP>();
+    static_assert(smem <= 232448, "shared memory");
+    auto kern = k_w4a16_gemm_tc<BN, NST, NSA, NSP, DQG>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return W4_ERR_CUDA;
+    kern<<<p.grid, threads_of<DQG>(), smem, stream>>>(tmX, tmP, a);
+    return cudaGetLastError() == cudaSuccess ? W4_OK : W4_ERR_CUDA;
+}
+
 }  // namespace
+
+// Tiles of 128 weight rows x BN tokens; K split S ways when the tiles alone
+// fill the GPU poorly.  Cost: waves x (relative tile time x stages per unit),
+// plus a charge for writing and re-reading fp32 partials when S > 1.
+bool plan_gemm(int M, int N, int K, int sm_count, GemmPlan* out) {
+    if (M < 1 || N < 1 || K < 1 || sm_count < 1) return false;
+    // W4_GEMM_BN (128 or 256) and W4_GEMM_SPLIT (1..8) pin the plan for tuning
+    static const int forced_bn = [] {
+        const char* e = std::getenv("W4_GEMM_BN");
+        const int v = e ? std::atoi(e) : 0;
+        return (v == 128 || v == 256) ? v : 0;
+    }();
+    static const int forced_s = [] {
+        const char* e = std::getenv("W4_GEMM_SPLIT");
+        const int v = e ? std::atoi(e) : 0;
+        return (v >= 1 && v <= 8) ? v : 0;
+    }();
+    const int nks = (K + BK - 1) / BK;
+    double best = 1e30;
+    bool found = false;
+    for (int BN = 256; BN >= 128; BN /= 2) {
+        if (forced_bn && BN != forced_bn) continue;
+        const int TB = (M + BN - 1) / BN;
+        const int ntiles = ((N + BM - 1) / BM) * TB;
+        for (int S = 1; S <= 8 && S <= nks; ++S) {
+            if (forced_s && S != forced_s) continue;
+            const int spl = (nks + S - 1) / S;
+            const int Se = (nks + spl - 1) / spl;
+            if (Se != S) continue;
+            const int units = ntiles * S;
+            const int waves = (units + sm_count - 1) / sm_count;
+            // the dequantized A tile sets the pace, so a 128-token tile takes
+            // as long per stage as a 256-token one; splits add the fp32
+            // partial traffic and the fix-up (about 4 stage-times each)
+            double cost = (double)waves * spl;
+            if (S > 1) cost += 2.0 * waves * S;
+            if (cost < best * (1 - 1e-9)) {
+                best = cost;
+                found = true;
+                GemmPlan p;
+                p.BN = BN; p.TB = TB; p.ntiles = ntiles; p.S = S; p.spl = spl; p.nks = nks;
+                p.units = units;
+                p.grid = units < sm_count ? units : sm_count;
+                p.ws_bytes = S > 1 ? ((size_t)ntiles * 4 + 255) / 256 * 256 + (size_t)S * M * N * 4 : 0;
+                *out = p;
+            }
+        }
+    }
+    return found;
+}
 
 int launch_w4a16_gemm(const uint16_t* x, const uint8_t* packed, const float* scales,
                       const uint8_t* zeros, const float* bias, uint16_t* y, int M, int N, int K,
-                      int Kp, int G, int* err, int sm_count, cudaStream_t stream) {
-    CUtensorMap tmX, tmP;
-    if (!encode_tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, (uint64_t)K, (uint64_t)M,
-                        (uint64_t)K * 2, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B))
-        return W4_ERR_CUDA;
-    if (!encode_tmap_2d(&tmP, CU_TENSOR_MAP_DATA_TYPE_UINT8, packed, (uint64_t)(Kp / 2),
-                        (uint64_t)N, (uint64_t)(Kp / 2), BK / 2, BM, CU_TENSOR_MAP_SWIZZLE_NONE))
-        return W4_ERR_CUDA;
+                      int Kp, int G, const GemmPlan& p, void* workspace, int* err,
+                      cudaStream_t stream) {
     GemmArgs a{};
     a.scales = scales; a.zeros = zeros; a.bias = bias; a.y = y; a.err = err;
     a.M = M; a.N = N; a.K = K; a.G = G; a.Ng = Kp / G;
-    a.nks = (K + BK - 1) / BK;
-    a.TB = (M + BN - 1) / BN;
-    a.ntiles = ((N + BM - 1) / BM) * a.TB;
-    const int grid = a.ntiles < sm_count ? a.ntiles : sm_count;
-    if (cudaFuncSetAttribute(k_w4a16_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmemBytes) != cudaSuccess)
-        return W4_ERR_CUDA;
-    k_w4a16_gemm_tc<<<grid, THREADS, kSmemBytes, stream>>>(tmX, tmP, a);
-    return cudaGetLastError() == cudaSuccess ? W4_OK : W4_ERR_CUDA;
+    a.nks = p.nks; a.TB = p.TB; a.ntiles = p.ntiles; a.S = p.S; a.spl = p.spl; a.units = p.units;
+    if (p.S > 1) {
+        a.tickets = static_cast<int*>(workspace);
+        a.partial = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                             ((size_t)p.ntiles * 4 + 255) / 256 * 256);
+    }
+    if (p.BN == 256) return launch_bn<256, 4, 4, 8, 1>(x, packed, p, a, Kp, stream);
+    return launch_bn<128, 8, 4, 8, 1>(x, packed, p, a, Kp, stream);
 }
 
 }  // namespace w4

@@ -90,32 +90,71 @@ k_pack_rtn(const float* __restrict__ W, int N, int K, int G, int Ng, int symmetr
     }
 }
 
-// One CTA per token.
-__global__ void __launch_bounds__(256)
+// One CTA of 1024 threads per token: the max|x| pass and the quantize pass
+// both read x with 16-byte loads where the row allows it (the second pass
+// hits L1/L2).
+constexpr int kActThreads = 1024;
+
+__global__ void __launch_bounds__(kActThreads)
 k_act_quant(const uint16_t* __restrict__ x, int K, int Kp, int8_t* __restrict__ qx,
             float* __restrict__ sx) {
-    __shared__ float red[8];
+    __shared__ float red[kActThreads / 32];
     const int m = blockIdx.x, tid = threadIdx.x;
     const uint16_t* row = x + (size_t)m * K;
+    int8_t* out = qx + (size_t)m * Kp;
+    const bool vec = (K & 7) == 0 && (reinterpret_cast<uintptr_t>(row) & 15) == 0;
     float mx = 0.f;
-    for (int k = tid; k < K; k += blockDim.x) mx = fmaxf(mx, fabsf(bf16_bits_to_f32(__ldg(row + k))));
+    if (vec) {
+        for (int k = tid * 8; k < K; k += kActThreads * 8) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(row + k));
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w[j] << 16)),
+                                     fabsf(__uint_as_float(w[j] & 0xFFFF0000u))));
+        }
+    } else {
+        for (int k = tid; k < K; k += kActThreads) mx = fmaxf(mx, fabsf(bf16_bits_to_f32(__ldg(row + k))));
+    }
     mx = warp_max(mx);
     if ((tid & 31) == 0) red[tid >> 5] = mx;
     __syncthreads();
     if (tid < 32) {
-        float v = tid < (int)(blockDim.x >> 5) ? red[tid] : 0.f;
+        float v = red[tid];
         v = warp_max(v);
         if (tid == 0) red[0] = v;
     }
     __syncthreads();
     const float s = __fdiv_rn(red[0], 127.0f);
     if (tid == 0) sx[m] = s;
-    int8_t* out = qx + (size_t)m * Kp;
-    for (int k = tid; k < Kp; k += blockDim.x) {
-        int q = 0;
-        if (k < K && s != 0.f)
-            q = (int)fminf(fmaxf(rintf(__fdiv_rn(bf16_bits_to_f32(__ldg(row + k)), s)), -127.f), 127.f);
-        out[k] = (int8_t)q;
+    auto q8 = [&](float v) -> uint32_t {
+        if (s == 0.f) return 0u;
+        return (uint32_t)(uint8_t)(int8_t)(int)fminf(fmaxf(rintf(__fdiv_rn(v, s)), -127.f), 127.f);
+    };
+    if (vec) {
+        // 8 columns per step; columns K..Kp-1 (a multiple of 8 past K) are zero
+        for (int k = tid * 8; k < Kp; k += kActThreads * 8) {
+            uint2 o = make_uint2(0u, 0u);
+            if (k < K) {
+                const uint4 v = __ldg(reinterpret_cast<const uint4*>(row + k));
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                uint32_t b[8];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    b[2 * j] = q8(__uint_as_float(w[j] << 16));
+                    b[2 * j + 1] = q8(__uint_as_float(w[j] & 0xFFFF0000u));
+                }
+                o.x = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
+                o.y = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
+            }
+            *reinterpret_cast<uint2*>(out + k) = o;
+        }
+    } else {
+        for (int k = tid; k < Kp; k += kActThreads) {
+            int q = 0;
+            if (k < K) q = (int)(int8_t)(uint8_t)q8(bf16_bits_to_f32(__ldg(row + k)));
+            out[k] = (int8_t)q;
+        }
     }
 }
 
@@ -134,7 +173,7 @@ int launch_pack_rtn(const float* W, int N, int K, int G, int symmetric, uint8_t*
 
 int launch_act_quant(const uint16_t* x, int M, int K, int Kp, int8_t* qx, float* sx,
                      cudaStream_t stream) {
-    k_act_quant<<<M, 256, 0, stream>>>(x, K, Kp, qx, sx);
+    k_act_quant<<<M, kActThreads, 0, stream>>>(x, K, Kp, qx, sx);
     return cudaGetLastError() == cudaSuccess ? W4_OK : W4_ERR_CUDA;
 }
 

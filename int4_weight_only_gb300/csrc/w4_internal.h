@@ -73,9 +73,22 @@ int launch_w4a8_gemv(const uint8_t* packed, const GemvArgs& a, const GemvPlan& p
 
 // ---------------------------------------------------------------- prefill
 // Tensor-core kernel for M > 16 (requires K % 8 == 0 and 16-byte aligned x).
+struct GemmPlan {
+    int BN = 0;        // tokens per tile (128 or 256)
+    int TB = 0;        // token blocks
+    int ntiles = 0;    // output tiles (128 weight rows x BN tokens)
+    int S = 0;         // K splits
+    int spl = 0;       // 64-column stages per split
+    int nks = 0;       // stages over K
+    int units = 0;     // ntiles * S
+    int grid = 0;      // CTAs launched
+    size_t ws_bytes = 0;
+};
+bool plan_gemm(int M, int N, int K, int sm_count, GemmPlan* plan);
 int launch_w4a16_gemm(const uint16_t* x, const uint8_t* packed, const float* scales,
                       const uint8_t* zeros, const float* bias, uint16_t* y, int M, int N, int K,
-                      int Kp, int G, int* err, int sm_count, cudaStream_t stream);
+                      int Kp, int G, const GemmPlan& p, void* workspace, int* err,
+                      cudaStream_t stream);
 
 // ---------------------------------------------------------------- others
 int launch_pack_rtn(const float* W, int N, int K, int G, int symmetric,
