@@ -8,27 +8,37 @@
 // the shared-memory operand of the tensor-core MMA, so bf16 weights never
 // touch HBM.
 //
-// D[128 weight rows x BN tokens] (fp32, TMEM) += W_hat[128 x 64] * x[BN x 64]^T
-// per 64-column stage; W_hat = s (code - z) is rounded once to bf16.  BN is
-// 128 or 256.  A unit of work is (output tile, K slice).  When a plan splits
-// K S ways, the S units of a tile run side by side (consecutive units go to
-// consecutive CTAs), each writes fp32 partials for the tokens of the other
-// S-1, waits until all S have, and reduces its own 1/S of the tokens in
-// split order 0..S-1 (its own term straight from TMEM), so every output is
-// summed in the same order on every run.
+// D[weight rows x BN tokens] (fp32, TMEM) += W_hat[rows x 64] * x[BN x 64]^T
+// per 64-column stage; W_hat = s (code - z) is rounded once to bf16.  Tiles:
+//   one CTA   128 weight rows x BN tokens (BN 256 or 128), tcgen05.mma
+//             cta_group::1, M = 128;
+//   CTA pair  256 weight rows x 256 tokens on a cluster of two CTAs: each
+//             CTA stages 128 of the tokens (its half of the B operand) and
+//             dequantizes its 128 rows (its half of A); rank 0 issues
+//             tcgen05.mma cta_group::2 with M = 256, N = 256, and each CTA's
+//             TMEM receives its 128 rows x 256 tokens.
+// A unit of work is (output tile, K slice).  When a plan splits K S ways,
+// the S units of a tile run side by side (consecutive units go to
+// consecutive CTAs or pairs), each writes fp32 partials for the tokens of
+// the other S-1, waits until all S have, and reduces its own 1/S of the
+// tokens in split order 0..S-1 (its own term straight from TMEM), so every
+// output is summed in the same order on every run.
 //
-// Warp roles (704 threads, one CTA per SM, persistent over units):
-//   warp 0      TMA: x tile (BN tokens x 64 columns, bf16, 128-byte swizzle)
-//               and packed tile (128 rows x 32 bytes) into an NST-stage ring
-//   warp 1      allocates 2*BN TMEM columns (two accumulators); one thread
-//               issues tcgen05.mma (M=128, N=BN, K=16) x 4 per stage
-//   warps 2-17  dequantize into the 128-byte-swizzled K-major bf16 A
-//               operand: two groups of 8 warps take alternate stages, one
-//               weight row and 32 columns per thread
-//   warps 18-21 epilogue: tcgen05.ld of the accumulator, + bias, bf16 stores
-//               (or, with K split, the cooperative reduction below)
-// Every mbarrier wait is bounded; a failed wait raises the CTA abort flag and
-// the device error flag, in-flight copies and MMAs are drained before exit.
+// Warp roles (96 + 256 DQG + 128 threads, one CTA per SM, persistent):
+//   warp 0      TMA of the x tile (128-byte swizzle) into an NST-stage ring,
+//               released by the MMAs
+//   warp 1      TMEM allocation (2 BN columns: two accumulators); one thread
+//               issues the MMAs (4 x K=16 per stage)
+//   warp 2      TMA of the packed tile (128 rows x 32 bytes) into an
+//               NSP-stage ring, released by the dequantizing warps
+//   next 8 DQG  dequantize into the 128-byte-swizzled K-major bf16 A ring
+//               (NSA stages): DQG groups of 8 warps take turns stage by
+//               stage, one weight row and 32 columns per thread
+//   last 4      epilogue: tcgen05.ld of the accumulator, + bias, bf16 stores
+//               (or the split-K hand-off)
+// Every mbarrier and counter wait is bounded; a failed wait raises the CTA
+// abort flag and the device error flag, in-flight copies and MMAs are
+// drained before exit.
 #include "w4_device.cuh"
 #include "w4_internal.h"
 
@@ -80,9 +90,9 @@ struct Ctl {
     int last;   // the tile's splits are all written (split-K hand-off)
 };
 
-template <int BN, int NST, int NSA, int NSP>
+template <int XR, int NST, int NSA, int NSP>
 constexpr size_t smem_bytes() {
-    return 1024 + (size_t)NST * BN * BK * 2 + (size_t)NSA * A_BYTES + (size_t)NSP * P_BYTES +
+    return 1024 + (size_t)NST * XR * BK * 2 + (size_t)NSA * A_BYTES + (size_t)NSP * P_BYTES +
            (sizeof(Ctl<NST, NSA, NSP>) + 15) / 16 * 16;
 }
 
@@ -104,14 +114,17 @@ __device__ __forceinline__ void unit_of(const GemmArgs& a, int u, int& nb, int& 
     ks1 = min(ks0 + a.spl, a.nks);
 }
 
-template <int BN, int NST, int NSA, int NSP, int DQG>
+template <int BN, int NST, int NSA, int NSP, int DQG, bool PAIR>
 __global__ void __launch_bounds__(threads_of<DQG>(), 1)
 k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmP,
                 const GemmArgs a) {
     constexpr int THREADS = threads_of<DQG>();
-    constexpr int X_BYTES = BN * BK * 2;
+    constexpr int XR = PAIR ? BN / 2 : BN;                  // x rows staged by this CTA
+    constexpr int RB = PAIR ? 2 * BM : BM;                  // weight rows per tile
+    constexpr int X_BYTES = XR * BK * 2;
     constexpr uint32_t TMEM_COLS = 2 * BN;
-    constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+    constexpr uint32_t IDESC = idesc_bf16_f32(RB, BN);
+    constexpr int NCTA = PAIR ? 2 : 1;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = align1024(smem_raw);
     uint8_t* xs = base;                                     // NST x X_BYTES
@@ -119,6 +132,13 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     uint8_t* ps = as + NSA * A_BYTES;                       // NSP x 4 KB
     auto* ctl = reinterpret_cast<Ctl<NST, NSA, NSP>*>(ps + NSP * P_BYTES);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // a pair tile is worked on by the two CTAs of a cluster: rank 0 issues
+    // the MMAs, each CTA stages its half of x and dequantizes its 128 rows
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+    const int slot = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int nslots = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+    // shared::cluster address of a barrier in the rank-0 CTA
+    auto at_rank0 = [&](uint64_t* bar) { return mapa_shared(smem_u32(bar), 0); };
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NST; ++i) { mbar_init(&ctl->tfull[i], 1); mbar_init(&ctl->tempty[i], 1); }
@@ -127,12 +147,12 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
             mbar_init(&ctl->pempty[i], DQ_GROUP_THREADS / 32);
         }
         for (int i = 0; i < NSA; ++i) {
-            mbar_init(&ctl->afull[i], DQ_GROUP_THREADS / 32);
+            mbar_init(&ctl->afull[i], NCTA * DQ_GROUP_THREADS / 32);
             mbar_init(&ctl->aempty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&ctl->accfull[i], 1);
-            mbar_init(&ctl->accempty[i], EPI_THREADS);
+            mbar_init(&ctl->accempty[i], NCTA * EPI_THREADS / 32);
         }
         mbar_init(&ctl->drain, 1);
         ctl->abort = 0;
@@ -140,9 +160,15 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) { tma_prefetch_desc(&tmX); tma_prefetch_desc(&tmP); }
-    if (warp == 1) { tmem_alloc(&ctl->tmem_base, TMEM_COLS); tmem_relinquish(); }
-    tc_fence_before();
-    __syncthreads();
+    if constexpr (PAIR) {
+        if (warp == 1) { tmem_alloc_pair(&ctl->tmem_base, TMEM_COLS); tmem_relinquish_pair(); }
+        tc_fence_before();
+        cluster_sync();             // both CTAs' barriers exist before any remote arrival
+    } else {
+        if (warp == 1) { tmem_alloc(&ctl->tmem_base, TMEM_COLS); tmem_relinquish(); }
+        tc_fence_before();
+        __syncthreads();
+    }
     tc_fence_after();
     const uint32_t tmem_base = ctl->tmem_base;
 
@@ -159,7 +185,7 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
             const uint64_t pol = is_x ? policy_evict_last() : policy_evict_first();
             uint32_t it = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+            for (int u = slot; u < a.units && ok; u += nslots) {
                 int nb, tb, tile, s, ks0, ks1;
                 unit_of(a, u, nb, tb, tile, s, ks0, ks1);
                 for (int ks = ks0; ks < ks1; ++ks, ++it) {
@@ -170,15 +196,25 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                         break;
                     }
                     if (is_x) {
-                        mbar_arrive_expect_tx(&full[st], X_BYTES);
-                        tma_load_2d(xs + st * X_BYTES, &tmX, ks * BK, tb * BN, &full[st], pol);
+                        if constexpr (PAIR) {
+                            // both halves land on the rank-0 barrier
+                            if (rank == 0) mbar_arrive_expect_tx(&full[st], 2 * X_BYTES);
+                            tma_load_2d_pair(xs + st * X_BYTES, &tmX, ks * BK, tb * BN + (int)rank * XR,
+                                             at_rank0(&full[st]), pol);
+                        } else {
+                            mbar_arrive_expect_tx(&full[st], X_BYTES);
+                            tma_load_2d(xs + st * X_BYTES, &tmX, ks * BK, tb * BN, &full[st], pol);
+                        }
                     } else {
                         mbar_arrive_expect_tx(&full[st], P_BYTES);
-                        tma_load_2d(ps + st * P_BYTES, &tmP, ks * (BK / 2), nb * BM, &full[st], pol);
+                        tma_load_2d(ps + st * P_BYTES, &tmP, ks * (BK / 2), nb * RB + (int)rank * BM,
+                                    &full[st], pol);
                     }
                 }
             }
-            if (!ok || ctl->abort) {
+            // (the x copies of rank 1 complete on the rank-0 barrier, which
+            // rank 0 drains; the pair leaves together through cluster_sync)
+            if ((!ok || ctl->abort) && (!PAIR || !is_x || rank == 0)) {
                 const uint32_t first = it > (uint32_t)ring ? it - ring : 0;
                 for (uint32_t j = first; j < it; ++j)
                     mbar_wait_drain(&full[j % ring], (j / ring) & 1, a.err);
@@ -186,14 +222,19 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA
-        if (lane == 0) {
+        if (lane == 0 && rank == 0) {
+            // waits on barriers that the other CTA of a pair also arrives on
+            auto wait = [&](uint64_t* bar, uint32_t parity) {
+                if constexpr (PAIR) return mbar_wait_cluster(bar, parity, &ctl->abort, a.err);
+                else return mbar_wait(bar, parity, &ctl->abort, a.err);
+            };
             uint32_t it = 0, ia = 0, tc = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x, ++tc) {
+            for (int u = slot; u < a.units && ok; u += nslots, ++tc) {
                 int nb, tb, tile, s, ks0, ks1;
                 unit_of(a, u, nb, tb, tile, s, ks0, ks1);
                 const uint32_t b = tc & 1;
-                if (tc >= 2 && !mbar_wait(&ctl->accempty[b], ((tc / 2) & 1) ^ 1, &ctl->abort, a.err)) {
+                if (tc >= 2 && !wait(&ctl->accempty[b], ((tc / 2) & 1) ^ 1)) {
                     ok = false;
                     break;
                 }
@@ -201,27 +242,38 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                 const uint32_t d = tmem_base + b * BN;
                 for (int ks = ks0; ks < ks1; ++ks, ++it, ++ia) {
                     const int st = it % NST, sa = ia % NSA;
-                    if (!mbar_wait(&ctl->tfull[st], (it / NST) & 1, &ctl->abort, a.err) ||
-                        !mbar_wait(&ctl->afull[sa], (ia / NSA) & 1, &ctl->abort, a.err)) {
+                    if (!wait(&ctl->tfull[st], (it / NST) & 1) || !wait(&ctl->afull[sa], (ia / NSA) & 1)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t a_addr = smem_u32(as + sa * A_BYTES);
                     const uint32_t x_addr = smem_u32(xs + st * X_BYTES);
+                    if constexpr (PAIR) {
 #pragma unroll
-                    for (int i = 0; i < BK / 16; ++i)
-                        tc_mma_f16(d, smem_desc_sw128(a_addr + 32 * i),
-                                   smem_desc_sw128(x_addr + 32 * i), IDESC,
-                                   (ks > ks0 || i > 0) ? 1u : 0u);
-                    tc_commit(&ctl->tempty[st]);
-                    tc_commit(&ctl->aempty[sa]);
+                        for (int i = 0; i < BK / 16; ++i)
+                            tc_mma_f16_pair(d, smem_desc_sw128(a_addr + 32 * i),
+                                            smem_desc_sw128(x_addr + 32 * i), IDESC,
+                                            (ks > ks0 || i > 0) ? 1u : 0u);
+                        tc_commit_pair(&ctl->tempty[st], 3);
+                        tc_commit_pair(&ctl->aempty[sa], 3);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < BK / 16; ++i)
+                            tc_mma_f16(d, smem_desc_sw128(a_addr + 32 * i),
+                                       smem_desc_sw128(x_addr + 32 * i), IDESC,
+                                       (ks > ks0 || i > 0) ? 1u : 0u);
+                        tc_commit(&ctl->tempty[st]);
+                        tc_commit(&ctl->aempty[sa]);
+                    }
                 }
                 if (!ok) break;
-                tc_commit(&ctl->accfull[b]);
+                if constexpr (PAIR) tc_commit_pair(&ctl->accfull[b], 3);
+                else tc_commit(&ctl->accfull[b]);
             }
             // every MMA issued by this thread completes before the CTA ends
-            tc_commit(&ctl->drain);
+            if constexpr (PAIR) tc_commit_pair(&ctl->drain, 1);
+            else tc_commit(&ctl->drain);
             mbar_wait_drain(&ctl->drain, 0, a.err);
         }
     } else if (threadIdx.x < DQ_BASE + DQG * DQ_GROUP_THREADS) {
@@ -237,13 +289,13 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
         const int grp = dt / DQ_GROUP_THREADS, gt = dt % DQ_GROUP_THREADS;
         const int r = gt / DQ_TPR, h = gt % DQ_TPR;
         uint32_t it = 0;
-        for (int u = blockIdx.x; u < a.units; u += gridDim.x) {
+        for (int u = slot; u < a.units; u += nslots) {
             int nb, tb, tile, s, ks0, ks1;
             unit_of(a, u, nb, tb, tile, s, ks0, ks1);
             // first stage of this unit that falls to this group
             const int lead = (int)((grp - it % DQ_GROUPS + DQ_GROUPS) % DQ_GROUPS);
             it += (uint32_t)lead;
-            const int n = min(nb * BM + r, a.N - 1);
+            const int n = min(nb * RB + (int)rank * BM + r, a.N - 1);
             const float* srow = a.scales + (size_t)n * a.Ng;
             const uint8_t* zrow = a.zeros ? a.zeros + (size_t)n * a.Ng : nullptr;
             // scale (and offset -(128 + z) s) of this thread's columns,
@@ -303,7 +355,10 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&ctl->afull[sa]);
+                    if (lane == 0) {
+                        if constexpr (PAIR) mbar_arrive_cluster(at_rank0(&ctl->afull[sa]));
+                        else mbar_arrive(&ctl->afull[sa]);
+                    }
                 }
                 sc = nsc;
                 zz = nzz;
@@ -320,13 +375,17 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
         // of it (SL a multiple of 32) and hands the rest to the other splits
         const int SL = ((BN + a.S - 1) / a.S + 31) / 32 * 32;
         uint32_t tc = 0;
-        for (int u = blockIdx.x; u < a.units; u += gridDim.x, ++tc) {
+        for (int u = slot; u < a.units; u += nslots, ++tc) {
             int nb, tb, tile, s, ks0, ks1;
             unit_of(a, u, nb, tb, tile, s, ks0, ks1);
             const uint32_t b = tc & 1;
-            bool ok = mbar_wait(&ctl->accfull[b], (tc / 2) & 1, &ctl->abort, a.err);
+            // the same outcome for all 128 epilogue threads, which then take
+            // the same branch (aligned tcgen05.ld, named barriers)
+            bool ok = named_bar_and(2, EPI_THREADS,
+                                    mbar_wait(&ctl->accfull[b], (tc / 2) & 1, &ctl->abort, a.err));
             tc_fence_after();
-            const int n = nb * BM + r;
+            const int n = nb * RB + (int)rank * BM + r;
+            int* ticket = a.tickets + (size_t)tile * NCTA + rank;   // per 128-row half
             const float bn = (a.bias && n < a.N) ? __ldg(a.bias + n) : 0.f;
             const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + b * BN;
             const int t0 = tb * BN;
@@ -363,8 +422,8 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                 __threadfence();
                 named_bar_sync(2, EPI_THREADS);
                 if (etid == 0) {
-                    atomicAdd(&a.tickets[tile], 1);
-                    ctl->last = wait_counter_geq(&a.tickets[tile], a.S, &ctl->abort, a.err);
+                    atomicAdd(ticket, 1);
+                    ctl->last = wait_counter_geq(ticket, a.S, &ctl->abort, a.err);
                 }
                 named_bar_sync(2, EPI_THREADS);
                 ok = ctl->last;
@@ -400,86 +459,166 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                     }
                     // 4. the last of the S splits to get here resets the counter
                     named_bar_sync(2, EPI_THREADS);
-                    if (etid == 0 && atomicAdd(&a.tickets[tile], 1) == 2 * a.S - 1) a.tickets[tile] = 0;
+                    if (etid == 0 && atomicAdd(ticket, 1) == 2 * a.S - 1) *ticket = 0;
                 }
             }
             tc_fence_before();
-            mbar_arrive(&ctl->accempty[b]);
+            __syncwarp();
+            if (lane == 0) {
+                if constexpr (PAIR) mbar_arrive_cluster(at_rank0(&ctl->accempty[b]));
+                else mbar_arrive(&ctl->accempty[b]);
+            }
         }
     }
 
     tc_fence_before();
-    __syncthreads();
+    if constexpr (PAIR) cluster_sync();     // no CTA leaves while its peer may still use it
+    else __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, TMEM_COLS);
+        if constexpr (PAIR) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+        else tmem_dealloc(tmem_base, TMEM_COLS);
     }
 }
 
-template <int BN, int NST, int NSA, int NSP, int DQG>
-int launch_bn(const uint16_t* x, const uint8_t* packed, const GemmPlan& p, GemmArgs& a,
-              int Kp, cudaStream_t stream) {
-    CUtensorMap tmX, tmP;
-    if (!encode_tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, (uint64_t)a.K, (uint64_t)a.M,
-                        (uint64_t)a.K * 2, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B))
-        return W4_ERR_CUDA;
-    if (!encode_tmap_2d(&tmP, CU_TENSOR_MAP_DATA_TYPE_UINT8, packed, (uint64_t)(Kp / 2),
-                        (uint64_t)a.N, (uint64_t)(Kp / 2), BK / 2, BM, CU_TENSOR_MAP_SWIZZLE_NONE))
-        return W4_ERR_CUDA;
-    constexpr size_t smem = smem_bytes<BN, NST, NSA, NSP>();
+template <int BN, int NST, int NSA, int NSP, int DQG, bool PAIR>
+struct Variant {
+    static constexpr int XR = PAIR ? BN / 2 : BN;
+    static constexpr size_t smem = smem_bytes<XR, NST, NSA, NSP>();
     static_assert(smem <= 232448, "shared memory");
-    auto kern = k_w4a16_gemm_tc<BN, NST, NSA, NSP, DQG>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-        return W4_ERR_CUDA;
-    kern<<<p.grid, threads_of<DQG>(), smem, stream>>>(tmX, tmP, a);
-    return cudaGetLastError() == cudaSuccess ? W4_OK : W4_ERR_CUDA;
-}
+    static constexpr auto kernel = k_w4a16_gemm_tc<BN, NST, NSA, NSP, DQG, PAIR>;
+
+    static bool prepare() {
+        return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)smem) == cudaSuccess;
+    }
+
+    static cudaLaunchConfig_t config(int grid, cudaStream_t stream, cudaLaunchAttribute* at) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)grid);
+        cfg.blockDim = dim3((unsigned)threads_of<DQG>());
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = PAIR ? 2 : 1;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = PAIR ? 1 : 0;
+        return cfg;
+    }
+
+    // CTAs (or CTA pairs) of this variant resident at once on this device:
+    // the split-K hand-off needs every unit of a tile running together, so
+    // grids never exceed it
+    static int slots(int sm_count) {
+        static int cache[64] = {0};
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+        if (cache[dev] == 0) {
+            int n = 0;
+            if (prepare()) {
+                if (PAIR) {
+                    cudaLaunchAttribute at[1];
+                    cudaLaunchConfig_t cfg = config(2 * sm_count, nullptr, at);
+                    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) n = 0;
+                } else {
+                    int per_sm = 0;
+                    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads_of<DQG>(),
+                                                                      smem) == cudaSuccess)
+                        n = per_sm * sm_count;
+                }
+            }
+            cudaGetLastError();
+            cache[dev] = n > 0 ? n : -1;
+        }
+        return cache[dev] > 0 ? cache[dev] : 0;
+    }
+
+    static int launch(const uint16_t* x, const uint8_t* packed, const GemmPlan& p, GemmArgs& a,
+                      int Kp, cudaStream_t stream) {
+        CUtensorMap tmX, tmP;
+        if (!encode_tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, (uint64_t)a.K, (uint64_t)a.M,
+                            (uint64_t)a.K * 2, BK, XR, CU_TENSOR_MAP_SWIZZLE_128B))
+            return W4_ERR_CUDA;
+        if (!encode_tmap_2d(&tmP, CU_TENSOR_MAP_DATA_TYPE_UINT8, packed, (uint64_t)(Kp / 2),
+                            (uint64_t)a.N, (uint64_t)(Kp / 2), BK / 2, BM, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return W4_ERR_CUDA;
+        if (!prepare()) return W4_ERR_CUDA;
+        cudaLaunchAttribute at[1];
+        cudaLaunchConfig_t cfg = config(p.grid, stream, at);
+        if (cudaLaunchKernelEx(&cfg, kernel, tmX, tmP, a) != cudaSuccess) return W4_ERR_CUDA;
+        return W4_OK;
+    }
+};
+
+using Single256 = Variant<256, 4, 4, 8, 1, false>;
+using Single128 = Variant<128, 8, 4, 8, 1, false>;
+using Pair256 = Variant<256, 6, 4, 8, 1, true>;
 
 }  // namespace
 
-// Tiles of 128 weight rows x BN tokens; K split S ways when the tiles alone
-// fill the GPU poorly.  Cost: waves x (relative tile time x stages per unit),
-// plus a charge for writing and re-reading fp32 partials when S > 1.
+// Output tiles are 128 weight rows x BN tokens on one SM, or 256 rows x 256
+// tokens on a CTA pair; K is split S ways when the tiles alone fill the GPU
+// poorly.  Cost = waves x stages per unit x relative stage time, plus a
+// charge per split for the fp32 partials and the hand-off.
 bool plan_gemm(int M, int N, int K, int sm_count, GemmPlan* out) {
     if (M < 1 || N < 1 || K < 1 || sm_count < 1) return false;
-    // W4_GEMM_BN (128 or 256) and W4_GEMM_SPLIT (1..8) pin the plan for tuning
-    static const int forced_bn = [] {
-        const char* e = std::getenv("W4_GEMM_BN");
-        const int v = e ? std::atoi(e) : 0;
-        return (v == 128 || v == 256) ? v : 0;
-    }();
-    static const int forced_s = [] {
-        const char* e = std::getenv("W4_GEMM_SPLIT");
-        const int v = e ? std::atoi(e) : 0;
-        return (v >= 1 && v <= 8) ? v : 0;
-    }();
+    // W4_GEMM_BN (128 or 256), W4_GEMM_SPLIT (1..8) and W4_GEMM_PAIR (0 or 1)
+    // pin the plan (tuning sweeps, tests of every variant); read on every
+    // call, which costs far less than one launch
+    auto env_int = [](const char* name) {
+        const char* e = std::getenv(name);
+        return e ? std::atoi(e) : -1;
+    };
+    const int forced_bn = env_int("W4_GEMM_BN");
+    const int forced_s = env_int("W4_GEMM_SPLIT");
+    const int forced_pair = env_int("W4_GEMM_PAIR");
+    struct Cand {
+        bool pair;
+        int BN;
+        int slots;      // CTAs (pairs) resident at once
+        double stage;   // time of one 64-column stage, relative to one CTA's 128 x 256
+    };
+    // measured on the 7B prefill shapes: a pair stage (256 x 256 on two SMs)
+    // runs 1-3% slower than two single-CTA stages (128 x 256 each); a
+    // 128-token stage takes as long as a 256-token one
+    const Cand cands[3] = {
+        {true, 256, Pair256::slots(sm_count), 1.02},
+        {false, 256, Single256::slots(sm_count), 1.0},
+        {false, 128, Single128::slots(sm_count), 1.0},
+    };
     const int nks = (K + BK - 1) / BK;
     double best = 1e30;
     bool found = false;
-    for (int BN = 256; BN >= 128; BN /= 2) {
-        if (forced_bn && BN != forced_bn) continue;
-        const int TB = (M + BN - 1) / BN;
-        const int ntiles = ((N + BM - 1) / BM) * TB;
+    for (const Cand& c : cands) {
+        if (c.slots < 1) continue;
+        if (forced_pair == 0 && c.pair) continue;
+        if (forced_pair == 1 && !c.pair) continue;
+        if ((forced_bn == 128 || forced_bn == 256) && c.BN != forced_bn) continue;
+        const int RB = c.pair ? 2 * BM : BM;
+        const int TB = (M + c.BN - 1) / c.BN;
+        const int ntiles = ((N + RB - 1) / RB) * TB;
         for (int S = 1; S <= 8 && S <= nks; ++S) {
-            if (forced_s && S != forced_s) continue;
+            if (forced_s >= 1 && forced_s <= 8 && S != forced_s) continue;
             const int spl = (nks + S - 1) / S;
             const int Se = (nks + spl - 1) / spl;
             if (Se != S) continue;
             const int units = ntiles * S;
-            const int waves = (units + sm_count - 1) / sm_count;
-            // the dequantized A tile sets the pace, so a 128-token tile takes
-            // as long per stage as a 256-token one; splits add the fp32
-            // partial traffic and the fix-up (about 4 stage-times each)
-            double cost = (double)waves * spl;
-            if (S > 1) cost += 2.0 * waves * S;
+            const int waves = (units + c.slots - 1) / c.slots;
+            double cost = (double)waves * spl * c.stage;
+            if (S > 1) cost += 2.0 * waves * S * c.stage;
             if (cost < best * (1 - 1e-9)) {
                 best = cost;
                 found = true;
                 GemmPlan p;
-                p.BN = BN; p.TB = TB; p.ntiles = ntiles; p.S = S; p.spl = spl; p.nks = nks;
+                p.pair = c.pair;
+                p.BN = c.BN; p.TB = TB; p.ntiles = ntiles; p.S = S; p.spl = spl; p.nks = nks;
                 p.units = units;
-                p.grid = units < sm_count ? units : sm_count;
-                p.ws_bytes = S > 1 ? ((size_t)ntiles * 4 + 255) / 256 * 256 + (size_t)S * M * N * 4 : 0;
+                p.grid = (c.pair ? 2 : 1) * (units < c.slots ? units : c.slots);
+                const size_t tickets = (size_t)ntiles * (c.pair ? 2 : 1) * 4;
+                p.ticket_bytes = S > 1 ? (tickets + 255) / 256 * 256 : 0;
+                p.ws_bytes = S > 1 ? p.ticket_bytes + (size_t)S * M * N * 4 : 0;
                 *out = p;
             }
         }
@@ -497,11 +636,11 @@ int launch_w4a16_gemm(const uint16_t* x, const uint8_t* packed, const float* sca
     a.nks = p.nks; a.TB = p.TB; a.ntiles = p.ntiles; a.S = p.S; a.spl = p.spl; a.units = p.units;
     if (p.S > 1) {
         a.tickets = static_cast<int*>(workspace);
-        a.partial = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                             ((size_t)p.ntiles * 4 + 255) / 256 * 256);
+        a.partial = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + p.ticket_bytes);
     }
-    if (p.BN == 256) return launch_bn<256, 4, 4, 8, 1>(x, packed, p, a, Kp, stream);
-    return launch_bn<128, 8, 4, 8, 1>(x, packed, p, a, Kp, stream);
+    if (p.pair) return Pair256::launch(x, packed, p, a, Kp, stream);
+    if (p.BN == 256) return Single256::launch(x, packed, p, a, Kp, stream);
+    return Single128::launch(x, packed, p, a, Kp, stream);
 }
 
 }  // namespace w4

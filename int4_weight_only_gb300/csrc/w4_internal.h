@@ -74,14 +74,16 @@ int launch_w4a8_gemv(const uint8_t* packed, const GemvArgs& a, const GemvPlan& p
 // ---------------------------------------------------------------- prefill
 // Tensor-core kernel for M > 16 (requires K % 8 == 0 and 16-byte aligned x).
 struct GemmPlan {
+    bool pair = false; // CTA-pair tiles (256 weight rows, cluster of 2)
     int BN = 0;        // tokens per tile (128 or 256)
     int TB = 0;        // token blocks
-    int ntiles = 0;    // output tiles (128 weight rows x BN tokens)
+    int ntiles = 0;    // output tiles (128 or 256 weight rows x BN tokens)
     int S = 0;         // K splits
     int spl = 0;       // 64-column stages per split
     int nks = 0;       // stages over K
     int units = 0;     // ntiles * S
     int grid = 0;      // CTAs launched
+    size_t ticket_bytes = 0;  // split-K counters at the start of the workspace
     size_t ws_bytes = 0;
 };
 bool plan_gemm(int M, int N, int K, int sm_count, GemmPlan* plan);

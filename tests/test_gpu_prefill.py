@@ -57,6 +57,35 @@ def test_prefill_workloads(w4, M, which):
     assert_close(y[:, torch.as_tensor(rows, device=y.device)], yref, lin.name)
 
 
+@pytest.mark.parametrize("pair,bn,split", [
+    (1, 256, 1), (1, 256, 2), (1, 256, 3), (0, 256, 1), (0, 256, 2), (0, 128, 1), (0, 128, 4),
+])
+@pytest.mark.parametrize("M,N,K,G,sym", [
+    (300, 520, 1000, 64, False), (700, 384, 3584, 128, True), (40, 1000, 512, 32, True),
+])
+def test_prefill_every_variant(w4, monkeypatch, pair, bn, split, M, N, K, G, sym):
+    """Each tile variant (CTA pair 256 x 256, one CTA 128 x 256 / 128 x 128)
+    and K split, pinned through the planner's tuning variables, on ragged
+    shapes: same tolerance, deterministic, no device error."""
+    monkeypatch.setenv("W4_GEMM_PAIR", str(pair))
+    monkeypatch.setenv("W4_GEMM_BN", str(bn))
+    monkeypatch.setenv("W4_GEMM_SPLIT", str(split))
+    seed = M + 3 * N + 7 * K + G + split
+    packed, scales, zeros = WL.make_random_format(N, K, G, sym, seed)
+    x = WL.make_activations(K, M, seed + 1)
+    b = torch.randn(N, generator=torch.Generator().manual_seed(seed + 2)) * 0.1
+    args = (packed.cuda(), scales.cuda(), None if zeros is None else zeros.cuda(), b.cuda(),
+            N, K, G)
+    y = w4.w4a16_linear(x.cuda(), *args)
+    y2 = w4.w4a16_linear(x.cuda(), *args)
+    torch.cuda.synchronize()
+    assert w4.w4_get_device_error() == 0
+    yref = O.w4a16_linear(x, packed.numpy(), scales.numpy(),
+                          None if zeros is None else zeros.numpy(), b.numpy(), K, G)
+    assert_close(y, yref, f"pair{pair} BN{bn} S{split} M{M} N{N} K{K}")
+    assert torch.equal(y, y2), "prefill is not deterministic"
+
+
 def test_prefill_rejects_k_not_multiple_of_8(w4):
     N, K, G = 64, 100, 32
     packed, scales, _ = WL.make_random_format(N, K, G, True, 1)
