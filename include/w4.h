@@ -35,6 +35,14 @@
  *    whole number of 16-byte words).
  *  - Weights (packed, scales, zeros) are assumed constant while a call that
  *    reads them is in flight.
+ *  - The linear entry points use programmatic dependent launch: their
+ *    kernels may start, and read packed, scales, zeros and bias, while the
+ *    kernel enqueued just before them on the stream is still finishing; x,
+ *    the workspace and y are touched only after it has completed.  So the
+ *    kernel immediately before a linear call must not write that call's
+ *    weights or bias.  w4_pack_rtn ends with an empty kernel launched
+ *    without this relaxation, so packing and then calling a linear layer on
+ *    the same stream is safe.
  */
 #ifndef W4_H_
 #define W4_H_
@@ -69,6 +77,13 @@ extern "C" {
 /* Size of the library's built-in split-K scratch used by
  * w4a16_linear_noalloc (4 MiB, held by every GPU that loads the library).  */
 #define W4_NOALLOC_SCRATCH_BYTES (4 << 20)
+
+/* Workspace layout of w4a16_linear / w4a8_linear: the first
+ * W4_WORKSPACE_COUNTER_BYTES hold split-K arrival counters (one int32 per
+ * row block or output tile), the partial sums follow.  No call writes
+ * anything but counters into the prefix, so one zero-filled workspace can
+ * serve calls of different shapes. */
+#define W4_WORKSPACE_COUNTER_BYTES (64 << 10)
 
 /* Largest padded K accepted by the W4A8 path: the kernels accumulate
  * code (0..15) x q_x (-127..127) products in int32, so Kp * 15 * 127 must
@@ -122,10 +137,11 @@ W4_API int w4a16_linear_noalloc(const uint16_t* x, const uint8_t* packed,
 
 /* ---------------------------------------------------------------------------
  * w4a16_workspace_bytes - bytes of device workspace w4a16_linear needs for
- * this shape on the CURRENT device (split-K partial sums and arrival
- * counters).  May be 0.  The workspace must be zero-filled once before its
- * first use; every call leaves its counters at zero again, so it can be
- * reused by later calls on the same stream without clearing.
+ * this shape on the CURRENT device (W4_WORKSPACE_COUNTER_BYTES of arrival
+ * counters, then split-K partial sums).  May be 0.  The workspace must be
+ * zero-filled once before its first use; every call leaves the counters at
+ * zero again, so it can be reused by later calls of any shape on the same
+ * stream without clearing.
  * ------------------------------------------------------------------------- */
 W4_API size_t w4a16_workspace_bytes(int M, int N, int K, int group_size);
 

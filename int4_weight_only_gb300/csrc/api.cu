@@ -87,7 +87,7 @@ int check_group(int K, int G) {
 
 long long padded_k(int K, int G) { return ((long long)K + G - 1) / G * G; }
 
-// Workspace layout: [tickets: NB ints, padded to 256 B][partials].
+// Workspace layout: [counters: kCounterBytes][partials].
 int split_workspace(const GemvPlan& p, void* ws, size_t ws_bytes, int** tickets, void** part) {
     *tickets = nullptr;
     *part = nullptr;
@@ -96,7 +96,7 @@ int split_workspace(const GemvPlan& p, void* ws, size_t ws_bytes, int** tickets,
     if (ws_bytes < p.ws_bytes) return W4_ERR_WORKSPACE;
     if (!aligned16(ws)) return W4_ERR_MISALIGNED;
     *tickets = static_cast<int*>(ws);
-    *part = static_cast<uint8_t*>(ws) + ((size_t)p.NB * 4 + 255) / 256 * 256;
+    *part = static_cast<uint8_t*>(ws) + kCounterBytes;
     return W4_OK;
 }
 

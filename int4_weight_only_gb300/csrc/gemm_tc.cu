@@ -601,6 +601,7 @@ bool plan_gemm(int M, int N, int K, int sm_count, GemmPlan* out) {
         const int ntiles = ((N + RB - 1) / RB) * TB;
         for (int S = 1; S <= 8 && S <= nks; ++S) {
             if (forced_s >= 1 && forced_s <= 8 && S != forced_s) continue;
+            if (S > 1 && (long long)ntiles * (c.pair ? 2 : 1) > kMaxCounters) continue;
             const int spl = (nks + S - 1) / S;
             const int Se = (nks + spl - 1) / spl;
             if (Se != S) continue;
@@ -616,8 +617,7 @@ bool plan_gemm(int M, int N, int K, int sm_count, GemmPlan* out) {
                 p.BN = c.BN; p.TB = TB; p.ntiles = ntiles; p.S = S; p.spl = spl; p.nks = nks;
                 p.units = units;
                 p.grid = (c.pair ? 2 : 1) * (units < c.slots ? units : c.slots);
-                const size_t tickets = (size_t)ntiles * (c.pair ? 2 : 1) * 4;
-                p.ticket_bytes = S > 1 ? (tickets + 255) / 256 * 256 : 0;
+                p.ticket_bytes = S > 1 ? kCounterBytes : 0;
                 p.ws_bytes = S > 1 ? p.ticket_bytes + (size_t)S * M * N * 4 : 0;
                 *out = p;
             }

@@ -1,804 +1,8 @@
-// gemv.cu - decode kernels (M <= 16) for the INT4 weight-only linear layer.
-//
-// W4A16 ("Lab 5: Gemma4 端到端推理优化", sections "INT4 线性量化" and
-// "融合INT4反量化与矩阵乘"): y = x W_hat^T (+b) with W_hat = s (code - z),
-// dequantized in registers next to the multiply, one pass over the packed
-// weights.  W4A8 ("Jetson Orin AGX INT4 推理优化实践", sections
-// "从 FP 线性层到 INT4 DP4A 的数学推导" and "DP4A 做了什么"):
-// acc = sum (code - 8) q_x in int32, y = s_W s_x acc + b.
-//
-// Structure (both kernels): persistent CTAs of 8 consumer warps + 1
-// producer warp, one or two CTAs per SM.  A unit of work is (block of R
-// output rows, slice of the padded K), R in {16, 32, 64, 128}; units are dealt
-// round-robin to the CTAs.  The producer streams 16 KB stages of packed
-// weights (128/R TMA boxes of R rows x 128 bytes, 128-byte swizzle) into a
-// 4-deep ring.  Each stage holds eight 16-row x 256-column boxes; consumer
-// warp w takes row tile w % (R/16) and k-phase w / (R/16), i.e. exactly one
-// such box per stage, and reads it with ldmatrix.  Partial sums of the
-// k-phases are added in shared memory in a fixed order; K slices of a row
-// block (split-K) are added by the last CTA to finish it, also in a fixed
-// order, so results are deterministic.
-//
-// W4A16 inner product: each 32-bit ldmatrix word holds 8 codes of one row;
-// one LOP3 per pair ORs the codes into the mantissa of fp16 1024.0 (both
-// nibbles of a byte fit the 10-bit mantissa, as 1024 + c and 1024 + 16c), and
-// these exact words feed mma.sync m16n8k16 (fp16 inputs, fp32 accumulation)
-// directly as the A operand (16 weight rows), with the activations as the B
-// operand (8 tokens per n-tile).  The activations are converted to fp16
-// exactly: each group's run of columns is scaled by a power of two first (and
-// scaled back at the flush), odd columns also by 1/16.  The order of k inside a 32-column chunk is permuted
-// identically on both operands, so no data shuffles are needed.  All MMAs
-// between two flushes see columns of one group: at the flush the offset
-// terms of that run of columns are removed and the group scale applied to the
-// fp32 partial sums, so the weights stay exact.
-//
-// Launch: programmatic dependent launch.  Before waiting for the previous
-// kernel on the stream, the producer only prefetches the first stages of its
-// first unit into L2; all shared-memory copies and every access to x, the
-// workspace and y come after griddepcontrol.wait.
-#include "w4_device.cuh"
-#include "w4_internal.h"
-
-#include <algorithm>
-#include <cstdlib>
+// gemv.cu - decode planner (plan_gemv) and the launches of the unsplit W4A16
+// kernels and of the W4A8 kernels; the kernels are in gemv_impl.cuh.
+#include "gemv_impl.cuh"
 
 namespace w4 {
-namespace {
-
-constexpr int CW = kGemvConsumerWarps;
-constexpr int NCT = CW * 32;
-constexpr int NS = kGemvStages;
-constexpr int STAGE_BYTES = kGemvStageBytes;
-
-struct SmemCtl {
-    uint64_t full[NS];
-    uint64_t empty[NS];
-    int abort;
-    int last;
-    int sumq[16];          // W4A8: sum of q_x over the slice, per token
-    uint64_t xfull;        // activation slice landed (TMA staging)
-    uint64_t xempty;       // consumers released the activation buffer
-};
-constexpr int kCtlBytes = 256;
-static_assert(sizeof(SmemCtl) <= kCtlBytes, "control block");
-
-__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-    const uint32_t s = smem_u32(p);
-    return p + (((s + 1023u) & ~1023u) - s);
-}
-
-__device__ __forceinline__ void unit_coords(int u, const GemvArgs& a, int& rb, int& s,
-                                            int& ks0, int& ks1) {
-    rb = u / a.S;
-    s = u - rb * a.S;
-    ks0 = s * a.spl;
-    ks1 = min(ks0 + a.spl, a.nst);
-}
-
-__device__ __forceinline__ void lds128(uint32_t addr, uint32_t* v) {
-    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]) : "r"(addr));
-}
-
-__device__ __forceinline__ void lds64(uint32_t addr, uint32_t& a, uint32_t& b) {
-    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(a), "=r"(b) : "r"(addr));
-}
-
-__device__ __forceinline__ void grid_dep_wait() {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-
-__device__ __forceinline__ void grid_dep_launch() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int c0, int c1) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
-                 :: "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1) : "memory");
-}
-
-// Producer: one thread streams every stage of every unit of this CTA.
-__device__ void gemv_producer(const CUtensorMap* tm, uint8_t* wbuf, uint8_t* xbuf,
-                              SmemCtl* ctl, const GemvArgs& a) {
-    const int boxes = 128 / a.R;
-    const int box_bytes = a.R * 128;
-    const int kbytes = a.Kp / 2;
-    // Warm L2 with the first stages of the first unit while the previous
-    // kernel on the stream may still be running (weights are read only).
-    if ((int)blockIdx.x < a.units) {
-        int rb, s, ks0, ks1;
-        unit_coords(blockIdx.x, a, rb, s, ks0, ks1);
-        for (int ks = ks0; ks < min(ks1, ks0 + NS); ++ks)
-            for (int b = 0; b < boxes; ++b) {
-                const int kb = ks * (a.SKE / 2) + b * 128;
-                if (kb < kbytes) tma_prefetch_l2_2d(tm, kb, rb * a.R);
-            }
-    }
-    grid_dep_wait();
-    const uint64_t pol = policy_evict_first();
-    uint32_t it = 0, xi = 0;
-    int pv0 = -1, pv1 = -1;
-    bool ok = true;
-    for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
-        int rb, s, ks0, ks1;
-        unit_coords(u, a, rb, s, ks0, ks1);
-        if (a.xtma && (ks0 != pv0 || ks1 != pv1)) {
-            // the activation slice goes out before this unit's weights
-            if (xi > 0 && !mbar_wait(&ctl->xempty, (xi - 1) & 1, &ctl->abort, a.err)) {
-                ok = false;
-                break;
-            }
-            const int k0 = ks0 * a.SKE;
-            const int ncol = min((ks1 - ks0) * a.SKE, a.K - k0);
-            const uint32_t nbytes = ncol > 0 ? (uint32_t)ncol * 2u : 0u;
-            mbar_arrive_expect_tx(&ctl->xfull, nbytes * (uint32_t)a.M);
-            if (nbytes)
-                for (int m = 0; m < a.M; ++m)
-                    bulk_load(xbuf + (size_t)m * a.XS,
-                              static_cast<const uint16_t*>(a.x) + (size_t)m * a.K + k0, nbytes,
-                              &ctl->xfull);
-            ++xi;
-            pv0 = ks0;
-            pv1 = ks1;
-        }
-        for (int ks = ks0; ks < ks1; ++ks, ++it) {
-            const int slot = it % NS;
-            if (it >= (uint32_t)NS &&
-                !mbar_wait(&ctl->empty[slot], ((it / NS) & 1) ^ 1, &ctl->abort, a.err)) {
-                ok = false;
-                break;
-            }
-            const int kb0 = ks * (a.SKE / 2);
-            const int nbox = min(boxes, (kbytes - kb0 + 127) / 128);   // boxes inside Kp
-            mbar_arrive_expect_tx(&ctl->full[slot], nbox * box_bytes);
-            for (int b = 0; b < nbox; ++b)
-                tma_load_2d(wbuf + slot * STAGE_BYTES + b * box_bytes, tm, kb0 + b * 128,
-                            rb * a.R, &ctl->full[slot], pol);
-        }
-    }
-    if (!ok || ctl->abort) {
-        // A wait gave up: let the copies already issued land before exiting.
-        const uint32_t first = it > (uint32_t)NS ? it - NS : 0;
-        for (uint32_t j = first; j < it; ++j)
-            mbar_wait_drain(&ctl->full[j % NS], (j / NS) & 1, a.err);
-        if (xi > 0) mbar_wait_drain(&ctl->xfull, (xi - 1) & 1, a.err);
-    }
-}
-
-// Activations of one unit into shared memory as fp16, columns [k0, k0+nk).
-// One thread per 8-column block; nk is a multiple of 256, so the 32 blocks
-// of a warp belong to one token and every run of CPG*4 lanes is one segment
-// of CPG*32 columns (one group's share of a box).  bf16 values are exactly
-// representable in fp16 once a segment is scaled by a power of two 2^-e that
-// puts its max|x| in [2^14, 2^15); odd columns of every 8-column block are
-// further divided by 16 (exact) to match the 1024 + 16c weights of
-// nibbles_to_f16x2_biased, and each block is stored in the order
-// (0,4,1,5,2,6,3,7).  Columns >= K are zero.  Per segment and token,
-// xseg[4 * (segment * M + token) + {0, 1, 2}] holds u = 2^e,
-// u * (1024 E + 64 O) and u * (E + O), with E and O the sums of the scaled
-// x over even and odd columns (added in a fixed butterfly order): the MMA of
-// the segment then equals u^-1 * (sum (c - z) x) + C0 + z * C1.
-// FROM_SMEM: the raw bf16 slice was already copied into xbuf (row m at
-// m * XS, natural order) and is converted in place; columns >= K hold stale
-// data there and are replaced by zeros.
-template <int CPG, bool FROM_SMEM>
-__device__ void stage_x_f16(uint8_t* xbuf, float* xseg, const uint16_t* x, int M, int K,
-                            int XS, int k0, int nk, int tid) {
-    constexpr int LPS = CPG * 4;            // lanes (blocks) per segment
-    const int nb = nk >> 3;
-    const bool vec = (K & 7) == 0;
-    for (int idx = tid; idx < M * nb; idx += NCT) {
-        const int m = idx / nb, b = idx - m * nb;
-        const int k = k0 + b * 8;
-        uint32_t q[4];
-        const uint16_t* src = x + (size_t)m * K + k;
-        if (FROM_SMEM) {
-            if (k < K) {
-                const uint4 v = *reinterpret_cast<const uint4*>(xbuf + (size_t)m * XS + b * 16);
-                q[0] = v.x; q[1] = v.y; q[2] = v.z; q[3] = v.w;
-            } else {
-                q[0] = q[1] = q[2] = q[3] = 0u;
-            }
-        } else if (vec && k + 8 <= K) {
-            const uint4 v = __ldg(reinterpret_cast<const uint4*>(src));
-            q[0] = v.x; q[1] = v.y; q[2] = v.z; q[3] = v.w;
-        } else {
-            uint16_t e[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) e[j] = (k + j < K) ? __ldg(src + j) : (uint16_t)0;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) q[j] = (uint32_t)e[2 * j] | ((uint32_t)e[2 * j + 1] << 16);
-        }
-        unsigned mx = 0;                      // bits of max|x| (non-negative floats order as ints)
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            mx = max(mx, max((q[j] << 16) & 0x7FFFFFFFu, q[j] & 0x7FFF0000u));
-#pragma unroll
-        for (int o = 1; o < LPS; o <<= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        const int E = (int)(mx >> 23) - 127;
-        const int e = mx == 0 ? 0 : max(E - 14, -100);
-        const float sc = __int_as_float((127 - e) << 23);
-        float v[8];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            v[2 * j] = __uint_as_float(q[j] << 16) * sc;
-            v[2 * j + 1] = __uint_as_float(q[j] & 0xFFFF0000u) * sc;
-        }
-        float se = (v[0] + v[2]) + (v[4] + v[6]);
-        float so = (v[1] + v[3]) + (v[5] + v[7]);
-#pragma unroll
-        for (int o = 1; o < LPS; o <<= 1) {
-            se += __shfl_xor_sync(0xffffffffu, se, o);
-            so += __shfl_xor_sync(0xffffffffu, so, o);
-        }
-        if ((b % LPS) == 0) {
-            const float u = __int_as_float((127 + e) << 23);
-            *reinterpret_cast<float4*>(xseg + 4 * ((b / LPS) * M + m)) =
-                make_float4(u, u * fmaf(1024.f, se, 64.f * so), u * (se + so), 0.f);
-        }
-        const float s16 = 0.0625f;
-        *reinterpret_cast<uint4*>(xbuf + (size_t)m * XS + b * 16) =
-            make_uint4(pack_f16x2(v[0], v[4]), pack_f16x2(v[1] * s16, v[5] * s16),
-                       pack_f16x2(v[2], v[6]), pack_f16x2(v[3] * s16, v[7] * s16));
-    }
-}
-
-// INT8 activations of one unit, order (0,2,4,6 | 1,3,5,7) per 8-column
-// block to match the byte lanes of (v & 0x0F0F0F0F) and ((v >> 4) & ...);
-// also accumulates sum(q_x) over the slice per token into ctl->sumq (which
-// the caller zeroed).
-__device__ void stage_x_s8(uint8_t* xbuf, SmemCtl* ctl, const int8_t* qx, int M, int Kp,
-                           int XS, int k0, int nk, int tid) {
-    const int nb = nk >> 3;
-    for (int m = 0; m < M; ++m) {
-        int part = 0;
-        for (int b = tid; b < nb; b += NCT) {
-            const int k = k0 + b * 8;
-            uint32_t w0 = 0, w1 = 0;
-            if (k < Kp) {
-                const uint2 v = __ldg(reinterpret_cast<const uint2*>(qx + (size_t)m * Kp + k));
-                w0 = v.x; w1 = v.y;
-            }
-            part = __dp4a((int)w0, 0x01010101, part);
-            part = __dp4a((int)w1, 0x01010101, part);
-            uint2 o;
-            o.x = __byte_perm(w0, w1, 0x6420);
-            o.y = __byte_perm(w0, w1, 0x7531);
-            *reinterpret_cast<uint2*>(xbuf + (size_t)m * XS + b * 8) = o;
-        }
-        part = __reduce_add_sync(0xffffffffu, part);
-        if ((tid & 31) == 0) atomicAdd(&ctl->sumq[m], part);
-    }
-}
-
-// Shared layout of one CTA; identical for both kernels.
-struct Smem {
-    uint8_t* wbuf;
-    SmemCtl* ctl;
-    float* red;
-    uint8_t* xbuf;
-    float* xseg;      // W4A16: per-segment sums of x, after M * XS bytes of xbuf
-};
-
-__device__ __forceinline__ Smem gemv_init(const CUtensorMap* tm, const GemvArgs& a) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* base = align1024(smem_raw);
-    Smem sm;
-    sm.wbuf = base;
-    sm.ctl = reinterpret_cast<SmemCtl*>(base + NS * STAGE_BYTES);
-    sm.red = reinterpret_cast<float*>(base + NS * STAGE_BYTES + kCtlBytes);
-    sm.xbuf = base + NS * STAGE_BYTES + kCtlBytes + a.red;
-    sm.xseg = reinterpret_cast<float*>(sm.xbuf + (size_t)a.M * a.XS);
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < NS; ++i) {
-            mbar_init(&sm.ctl->full[i], 1);
-            mbar_init(&sm.ctl->empty[i], CW);
-        }
-        mbar_init(&sm.ctl->xfull, 1);
-        mbar_init(&sm.ctl->xempty, 1);
-        sm.ctl->abort = 0;
-        sm.ctl->last = 0;
-        for (int i = 0; i < 16; ++i) sm.ctl->sumq[i] = 0;
-        fence_mbar_init();
-    }
-    if (threadIdx.x == NCT) tma_prefetch_desc(tm);
-    grid_dep_launch();
-    __syncthreads();
-    return sm;
-}
-
-// Split-K hand-off: after this CTA's partials are written, the last CTA of
-// row block rb sees ctl->last set.  All consumer threads call it.
-__device__ __forceinline__ bool split_k_arrive(const GemvArgs& a, SmemCtl* ctl, int rb) {
-    __threadfence();
-    named_bar_sync(1, NCT);
-    if (threadIdx.x == 0) ctl->last = (atomicAdd(&a.tickets[rb], 1) == a.S - 1);
-    named_bar_sync(1, NCT);
-    const bool last = ctl->last;
-    if (last) __threadfence();
-    return last;
-}
-
-template <int NT, int CPG, bool ASYM>
-__device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
-    constexpr int SEG = 8 / CPG;
-    constexpr int LOG_CPG = CPG == 8 ? 3 : CPG == 4 ? 2 : CPG == 2 ? 1 : 0;
-    constexpr bool PF = SEG <= 2;           // scales one stage ahead when they are few
-    // kernel arguments in registers (asm statements with memory clobbers
-    // would otherwise force re-reads from parameter space)
-    const int M = a.M, N = a.N, K = a.K, Kp = a.Kp, Ng = a.Ng, SKE = a.SKE, XS = a.XS;
-    const int units = a.units, Sp = a.S, spl = a.spl, nst = a.nst, R = a.R;
-    const float* __restrict__ scales = a.scales;
-    const uint8_t* __restrict__ zeros = a.zeros;
-    const float* __restrict__ bias = a.bias;
-    uint16_t* __restrict__ y = a.y;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int tig = lane & 3, gid = lane >> 2;
-    const int WR = R / 16, WK = CW / WR;
-    const int rt = warp % WR, kp = warp / WR;
-    const uint16_t* x = static_cast<const uint16_t*>(a.x);
-    const uint32_t wbuf_u = smem_u32(sm.wbuf), xbuf_u = smem_u32(sm.xbuf);
-    const int lj = lane >> 3, li = lane & 7;
-    // this warp's 16 x 256 box inside a stage, and the ldmatrix row and
-    // swizzled chunk offset of this lane for each chunk pair
-    const uint32_t l_off = (uint32_t)(kp * R * 128 + (rt * 16 + ((lj & 1) << 3) + li) * 128);
-    uint32_t l_cp[4];
-#pragma unroll
-    for (int cp = 0; cp < 4; ++cp) l_cp[cp] = l_off + ((uint32_t)((2 * cp + (lj >> 1)) ^ li) << 4);
-    uint32_t xrow[NT];
-    int xt[NT][2];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        xrow[nt] = xbuf_u + (uint32_t)(min(nt * 8 + gid, M - 1) * XS + tig * 16 + kp * 512);
-        xt[nt][0] = 4 * min(nt * 8 + 2 * tig, M - 1);
-        xt[nt][1] = 4 * min(nt * 8 + 2 * tig + 1, M - 1);
-    }
-    // group of a segment: segments of CPG*32 columns tile the groups exactly,
-    // so g = segment / (G / (CPG*32)), a shift when that ratio is a power of 2
-    const int gdiv = a.G / (CPG * 32);
-    const int gshift = (gdiv & (gdiv - 1)) == 0 ? __ffs(gdiv) - 1 : -1;
-    const float zc[4] = {0.f, 0.f, 0.f, 0.f};
-    SmemCtl* ctl = sm.ctl;
-    const bool xtma = a.xtma != 0;
-
-    grid_dep_wait();
-    uint32_t it = 0, xi = 0;
-    int prev0 = -1, prev1 = -1;
-    for (int u = blockIdx.x; u < units; u += gridDim.x) {
-        const int rb = u / Sp, s = u - rb * Sp;
-        const int ks0 = s * spl, ks1 = min(ks0 + spl, nst);
-        const int row0 = rb * R + rt * 16;
-        const int nr = min(row0 + gid, N - 1), nr8 = min(row0 + gid + 8, N - 1);
-        const float* sc_r = scales + (size_t)nr * Ng;
-        const float* sc_r8 = scales + (size_t)nr8 * Ng;
-        const uint8_t* zp_r = ASYM ? zeros + (size_t)nr * Ng : nullptr;
-        const uint8_t* zp_r8 = ASYM ? zeros + (size_t)nr8 * Ng : nullptr;
-
-        named_bar_sync(1, NCT);
-        if (ks0 != prev0 || ks1 != prev1) {
-            if (xtma) {
-                // everyone is past the previous slice: release its buffer,
-                // then wait for this slice's copy and convert it in place
-                if (xi > 0 && tid == 0) mbar_arrive(&ctl->xempty);
-                if (mbar_wait(&ctl->xfull, xi & 1, &ctl->abort, a.err))
-                    stage_x_f16<CPG, true>(sm.xbuf, sm.xseg, x, M, K, XS, ks0 * SKE,
-                                           (ks1 - ks0) * SKE, tid);
-                ++xi;
-            } else {
-                stage_x_f16<CPG, false>(sm.xbuf, sm.xseg, x, M, K, XS, ks0 * SKE,
-                                        (ks1 - ks0) * SKE, tid);
-            }
-            named_bar_sync(1, NCT);
-            prev0 = ks0;
-            prev1 = ks1;
-        }
-
-        float acc[NT][4];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) acc[nt][j] = 0.f;
-
-        // The MMA sums x' * w' over each run of CPG chunks (one group), with
-        // w' = 1024 + c on even and 1024 + 16c on odd columns and x' the
-        // segment's scaled activations (odd ones / 16); with the segment's
-        // (u, C0, C1) from staging, acc += s * (u * tmp - C0 - z * C1).
-        float sr[SEG], sr8[SEG], zr[SEG], zr8[SEG];
-        auto load_scales = [&](int kw, float* r_, float* r8_, float* z_, float* z8_) {
-#pragma unroll
-            for (int j = 0; j < SEG; ++j) {
-                const int sg = (kw >> (5 + LOG_CPG)) + j;
-                const int g = min(gshift >= 0 ? (sg >> gshift) : sg / gdiv, Ng - 1);
-                r_[j] = __ldg(sc_r + g);
-                r8_[j] = __ldg(sc_r8 + g);
-                if (ASYM) {
-                    z_[j] = (float)__ldg(zp_r + g);
-                    z8_[j] = (float)__ldg(zp_r8 + g);
-                }
-            }
-        };
-        if (PF) load_scales(min(ks0 * SKE + kp * 256, Kp - 1), sr, sr8, zr, zr8);
-
-        for (int ks = ks0; ks < ks1; ++ks, ++it) {
-            const int slot = it % NS;
-            const int kw = ks * SKE + kp * 256;            // first column of this warp's box
-            float nsr[SEG], nsr8[SEG], nzr[SEG], nzr8[SEG];
-            if (PF && ks + 1 < ks1)
-                load_scales(min(kw + SKE, Kp - 1), nsr, nsr8, nzr, nzr8);
-            if (kw < Kp) {
-                if (!PF) load_scales(kw, sr, sr8, zr, zr8);
-                if (mbar_wait(&ctl->full[slot], (it / NS) & 1, &ctl->abort, a.err)) {
-                    const uint32_t wst = wbuf_u + slot * STAGE_BYTES;
-                    const uint32_t xoff = (uint32_t)(ks - ks0) * (uint32_t)(SKE * 2);
-                    const float* xs_st =
-                        sm.xseg + 4 * ((((ks - ks0) * SKE + kp * 256) >> (5 + LOG_CPG)) * M);
-                    float tmp[NT][4];
-#pragma unroll
-                    for (int cp = 0; cp < 4; ++cp) {
-                        uint32_t r[4];
-                        ldmatrix_x4_nc(wst + l_cp[cp], r[0], r[1], r[2], r[3]);
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const int c = 2 * cp + h;
-                            const int seg = c / CPG;
-                            uint32_t P[4], Q[4];
-                            nibbles_to_f16x2_biased(r[2 * h], P);
-                            nibbles_to_f16x2_biased(r[2 * h + 1], Q);
-#pragma unroll
-                            for (int nt = 0; nt < NT; ++nt) {
-                                uint32_t X[4];
-                                lds128(xrow[nt] + xoff + c * 64, X);
-                                mma_f16_16816(tmp[nt], P[0], Q[0], P[1], Q[1], X[0], X[1],
-                                              (c % CPG == 0) ? zc : tmp[nt]);
-                                mma_f16_16816(tmp[nt], P[2], Q[2], P[3], Q[3], X[2], X[3], tmp[nt]);
-                            }
-                            if ((c + 1) % CPG == 0) {
-#pragma unroll
-                                for (int nt = 0; nt < NT; ++nt) {
-                                    const float4 e0 = *reinterpret_cast<const float4*>(
-                                        xs_st + 4 * seg * M + xt[nt][0]);
-                                    const float4 e1 = *reinterpret_cast<const float4*>(
-                                        xs_st + 4 * seg * M + xt[nt][1]);
-                                    float c00, c01, c10, c11;   // C0 + z C1 per (row, token)
-                                    if (ASYM) {
-                                        c00 = fmaf(zr[seg], e0.z, e0.y);
-                                        c01 = fmaf(zr[seg], e1.z, e1.y);
-                                        c10 = fmaf(zr8[seg], e0.z, e0.y);
-                                        c11 = fmaf(zr8[seg], e1.z, e1.y);
-                                    } else {
-                                        c00 = c10 = fmaf(8.f, e0.z, e0.y);
-                                        c01 = c11 = fmaf(8.f, e1.z, e1.y);
-                                    }
-                                    acc[nt][0] = fmaf(sr[seg], fmaf(e0.x, tmp[nt][0], -c00), acc[nt][0]);
-                                    acc[nt][1] = fmaf(sr[seg], fmaf(e1.x, tmp[nt][1], -c01), acc[nt][1]);
-                                    acc[nt][2] = fmaf(sr8[seg], fmaf(e0.x, tmp[nt][2], -c10), acc[nt][2]);
-                                    acc[nt][3] = fmaf(sr8[seg], fmaf(e1.x, tmp[nt][3], -c11), acc[nt][3]);
-                                }
-                            }
-                        }
-                    }
-                }
-            }
-            if (PF) {
-#pragma unroll
-                for (int j = 0; j < SEG; ++j) {
-                    sr[j] = nsr[j]; sr8[j] = nsr8[j];
-                    if (ASYM) { zr[j] = nzr[j]; zr8[j] = nzr8[j]; }
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl->empty[slot]);
-        }
-
-        // ---- add the k-phases of each row tile, in order 0, 1, ..., WK-1
-        if (WK > 1) {
-            if (kp > 0) {
-                float* dst = sm.red + ((kp - 1) * WR + rt) * (NT * 4 * 32) + lane;
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) dst[(nt * 4 + j) * 32] = acc[nt][j];
-            }
-            named_bar_sync(1, NCT);
-            if (kp == 0) {
-                for (int q = 1; q < WK; ++q) {
-                    const float* src = sm.red + ((q - 1) * WR + rt) * (NT * 4 * 32) + lane;
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) acc[nt][j] += src[(nt * 4 + j) * 32];
-                }
-            }
-        }
-
-        // ---- epilogue: thread holds (token 8nt + 2tig + (j&1), row gid + 8(j>>1))
-        if (Sp == 1) {
-            if (kp == 0) {
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int t = nt * 8 + 2 * tig + (j & 1);
-                        const int n = row0 + gid + 8 * (j >> 1);
-                        if (t < M && n < N) {
-                            const float b = bias ? __ldg(bias + n) : 0.f;
-                            y[(size_t)t * N + n] = f32_to_bf16_bits(acc[nt][j] + b);
-                        }
-                    }
-            }
-        } else {
-            float* part = static_cast<float*>(a.partial);
-            if (kp == 0) {
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int t = nt * 8 + 2 * tig + (j & 1);
-                        const int n = row0 + gid + 8 * (j >> 1);
-                        if (t < M && n < N) part[((size_t)s * M + t) * N + n] = acc[nt][j];
-                    }
-            }
-            if (split_k_arrive(a, ctl, rb)) {
-                if (kp == 0) {
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const int t = nt * 8 + 2 * tig + (j & 1);
-                            const int n = row0 + gid + 8 * (j >> 1);
-                            if (t < M && n < N) {
-                                float v = 0.f;
-                                for (int q = 0; q < Sp; ++q)
-                                    v += ld_cg_f32(part + ((size_t)q * M + t) * N + n);
-                                const float b = bias ? __ldg(bias + n) : 0.f;
-                                y[(size_t)t * N + n] = f32_to_bf16_bits(v + b);
-                            }
-                        }
-                }
-                if (tid == 0) a.tickets[rb] = 0;
-            }
-        }
-    }
-}
-
-template <int MT>
-__device__ void w4a8_consumer(const Smem& sm, const GemvArgs& a) {
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int tig = lane & 3, gid = lane >> 2;
-    const int WR = a.R / 16, WK = CW / WR;
-    const int rt = warp % WR, kp = warp / WR;
-    const int8_t* qx = static_cast<const int8_t*>(a.x);
-    const uint32_t wbuf_u = smem_u32(sm.wbuf), xbuf_u = smem_u32(sm.xbuf);
-    const int lj = lane >> 3, li = lane & 7;
-    const uint32_t l_off = (uint32_t)(kp * a.R * 128 + (rt * 16 + ((lj & 1) << 3) + li) * 128);
-    uint32_t l_cp[4];
-#pragma unroll
-    for (int cp = 0; cp < 4; ++cp) l_cp[cp] = l_off + ((uint32_t)((2 * cp + (lj >> 1)) ^ li) << 4);
-    uint32_t xrow[MT];
-#pragma unroll
-    for (int m = 0; m < MT; ++m)
-        xrow[m] = xbuf_u + (uint32_t)(min(m, a.M - 1) * a.XS + tig * 8 + kp * 256);
-    int* red = reinterpret_cast<int*>(sm.red);
-
-    grid_dep_wait();
-    uint32_t it = 0;
-    int prev0 = -1, prev1 = -1;
-    for (int u = blockIdx.x; u < a.units; u += gridDim.x) {
-        int rb, s, ks0, ks1;
-        unit_coords(u, a, rb, s, ks0, ks1);
-        const int row0 = rb * a.R + rt * 16;
-
-        named_bar_sync(1, NCT);
-        if (ks0 != prev0 || ks1 != prev1) {
-            if (tid < 16) sm.ctl->sumq[tid] = 0;
-            named_bar_sync(1, NCT);
-            stage_x_s8(sm.xbuf, sm.ctl, qx, a.M, a.Kp, a.XS, ks0 * a.SKE, (ks1 - ks0) * a.SKE, tid);
-            named_bar_sync(1, NCT);
-            prev0 = ks0;
-            prev1 = ks1;
-        }
-
-        int acc[MT][2];
-#pragma unroll
-        for (int m = 0; m < MT; ++m) acc[m][0] = acc[m][1] = 0;
-
-        for (int ks = ks0; ks < ks1; ++ks, ++it) {
-            const int slot = it % NS;
-            const int kw = ks * a.SKE + kp * 256;
-            if (kw < a.Kp &&
-                mbar_wait(&sm.ctl->full[slot], (it / NS) & 1, &sm.ctl->abort, a.err)) {
-                const uint32_t wst = wbuf_u + slot * STAGE_BYTES;
-                const uint32_t xoff = (uint32_t)(ks - ks0) * (uint32_t)a.SKE;
-#pragma unroll
-                for (int cp = 0; cp < 4; ++cp) {
-                    uint32_t r[4];
-                    ldmatrix_x4(wst + l_cp[cp], r[0], r[1], r[2], r[3]);
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int c = 2 * cp + h;
-                        const uint32_t lo = r[2 * h] & 0x0F0F0F0Fu, hi = (r[2 * h] >> 4) & 0x0F0F0F0Fu;
-                        const uint32_t lo8 = r[2 * h + 1] & 0x0F0F0F0Fu, hi8 = (r[2 * h + 1] >> 4) & 0x0F0F0F0Fu;
-#pragma unroll
-                        for (int m = 0; m < MT; ++m) {
-                            uint32_t xe, xo;
-                            lds64(xrow[m] + xoff + c * 32, xe, xo);
-                            acc[m][0] = dp4a_us(lo, xe, acc[m][0]);
-                            acc[m][0] = dp4a_us(hi, xo, acc[m][0]);
-                            acc[m][1] = dp4a_us(lo8, xe, acc[m][1]);
-                            acc[m][1] = dp4a_us(hi8, xo, acc[m][1]);
-                        }
-                    }
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.ctl->empty[slot]);
-        }
-
-        // lanes sharing a row, then the k-phases (exact integers)
-#pragma unroll
-        for (int m = 0; m < MT; ++m)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                int v = acc[m][h];
-                v += __shfl_xor_sync(0xffffffffu, v, 1);
-                v += __shfl_xor_sync(0xffffffffu, v, 2);
-                acc[m][h] = v;
-            }
-        if (WK > 1) {
-            if (kp > 0) {
-                int* dst = red + ((kp - 1) * WR + rt) * (MT * 2 * 32) + lane;
-#pragma unroll
-                for (int m = 0; m < MT; ++m)
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) dst[(m * 2 + h) * 32] = acc[m][h];
-            }
-            named_bar_sync(1, NCT);
-            if (kp == 0) {
-                for (int q = 1; q < WK; ++q) {
-                    const int* src = red + ((q - 1) * WR + rt) * (MT * 2 * 32) + lane;
-#pragma unroll
-                    for (int m = 0; m < MT; ++m)
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) acc[m][h] += src[(m * 2 + h) * 32];
-                }
-            }
-        }
-#pragma unroll
-        for (int m = 0; m < MT; ++m)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) acc[m][h] -= 8 * sm.ctl->sumq[min(m, a.M - 1)];
-
-        int32_t* part = static_cast<int32_t*>(a.partial);
-        bool write = kp == 0;
-        if (a.S > 1) {
-            if (kp == 0) {
-#pragma unroll
-                for (int m = 0; m < MT; ++m)
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int n = row0 + gid + 8 * h;
-                        if (m < a.M && (m & 3) == tig && n < a.N)
-                            part[((size_t)s * a.M + m) * a.N + n] = acc[m][h];
-                    }
-            }
-            const bool last = split_k_arrive(a, sm.ctl, rb);
-            write = write && last;
-            if (last && tid == 0) a.tickets[rb] = 0;
-        }
-        if (write) {
-#pragma unroll
-            for (int m = 0; m < MT; ++m)
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int n = row0 + gid + 8 * h;
-                    if (m < a.M && (m & 3) == tig && n < a.N) {
-                        int v = acc[m][h];
-                        if (a.S > 1) {
-                            v = 0;
-                            for (int q = 0; q < a.S; ++q)
-                                v += ld_cg_s32(part + ((size_t)q * a.M + m) * a.N + n);
-                        }
-                        if (a.acc_out) a.acc_out[(size_t)m * a.N + n] = v;
-                        const float sc = __ldg(a.scales + n) * __ldg(a.sx + m);
-                        const float b = a.bias ? __ldg(a.bias + n) : 0.f;
-                        a.y[(size_t)m * a.N + n] = f32_to_bf16_bits(fmaf(sc, (float)v, b));
-                    }
-                }
-        }
-    }
-}
-
-// Kernel instances that the plan may place two to an SM (M <= 8 for W4A16,
-// M <= 4 for W4A8) are compiled for two resident CTAs of 288 threads.
-template <int NT, int CPG, bool ASYM>
-__device__ __forceinline__ void w4a16_body(const CUtensorMap* tm, const GemvArgs& a) {
-    const Smem sm = gemv_init(tm, a);
-    if (threadIdx.x >= NCT) {
-        if (threadIdx.x == NCT) gemv_producer(tm, sm.wbuf, sm.xbuf, sm.ctl, a);
-    } else {
-        w4a16_consumer<NT, CPG, ASYM>(sm, a);
-    }
-}
-
-template <int CPG, bool ASYM>
-__global__ void __launch_bounds__(kGemvThreads, 2)
-k_w4a16_gemv_m8(const __grid_constant__ CUtensorMap tmW, const GemvArgs a) {
-    w4a16_body<1, CPG, ASYM>(&tmW, a);
-}
-
-template <int CPG, bool ASYM>
-__global__ void __launch_bounds__(kGemvThreads, 1)
-k_w4a16_gemv_m16(const __grid_constant__ CUtensorMap tmW, const GemvArgs a) {
-    w4a16_body<2, CPG, ASYM>(&tmW, a);
-}
-
-template <int MT>
-__device__ __forceinline__ void w4a8_body(const CUtensorMap* tm, const GemvArgs& a) {
-    const Smem sm = gemv_init(tm, a);
-    if (threadIdx.x >= NCT) {
-        if (threadIdx.x == NCT) gemv_producer(tm, sm.wbuf, sm.xbuf, sm.ctl, a);
-    } else {
-        w4a8_consumer<MT>(sm, a);
-    }
-}
-
-template <int MT>
-__global__ void __launch_bounds__(kGemvThreads, 2)
-k_w4a8_gemv_m4(const __grid_constant__ CUtensorMap tmW, const GemvArgs a) {
-    w4a8_body<MT>(&tmW, a);
-}
-
-template <int MT>
-__global__ void __launch_bounds__(kGemvThreads, 1)
-k_w4a8_gemv_m16(const __grid_constant__ CUtensorMap tmW, const GemvArgs a) {
-    w4a8_body<MT>(&tmW, a);
-}
-
-template <typename Kern>
-int launch(Kern kern, const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
-           cudaStream_t stream) {
-    CUtensorMap tm;
-    if (!encode_tmap_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, packed, (uint64_t)(a.Kp / 2),
-                        (uint64_t)a.N, (uint64_t)(a.Kp / 2), 128, (uint32_t)p.R,
-                        CU_TENSOR_MAP_SWIZZLE_128B))
-        return W4_ERR_CUDA;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)p.smem) != cudaSuccess)
-        return W4_ERR_CUDA;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.grid);
-    cfg.blockDim = dim3(kGemvThreads);
-    cfg.dynamicSmemBytes = p.smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kern, tm, a) != cudaSuccess) return W4_ERR_CUDA;
-    return cudaGetLastError() == cudaSuccess ? W4_OK : W4_ERR_CUDA;
-}
-
-template <int NT, bool ASYM>
-int launch_w4a16_cpg(int cpg, const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
-                     cudaStream_t st) {
-    if (NT == 1) {
-        switch (cpg) {
-            case 8: return launch(k_w4a16_gemv_m8<8, ASYM>, packed, a, p, st);
-            case 4: return launch(k_w4a16_gemv_m8<4, ASYM>, packed, a, p, st);
-            case 2: return launch(k_w4a16_gemv_m8<2, ASYM>, packed, a, p, st);
-            default: return launch(k_w4a16_gemv_m8<1, ASYM>, packed, a, p, st);
-        }
-    }
-    switch (cpg) {
-        case 8: return launch(k_w4a16_gemv_m16<8, ASYM>, packed, a, p, st);
-        case 4: return launch(k_w4a16_gemv_m16<4, ASYM>, packed, a, p, st);
-        case 2: return launch(k_w4a16_gemv_m16<2, ASYM>, packed, a, p, st);
-        default: return launch(k_w4a16_gemv_m16<1, ASYM>, packed, a, p, st);
-    }
-}
-
-}  // namespace
 
 bool plan_gemv(int M, int N, int Kp, int G, int act_bytes, int sm_count, GemvPlan* out) {
     if (M < 1 || M > 16 || N < 1 || Kp < 1 || G < 32 || sm_count < 1) return false;
@@ -820,12 +24,15 @@ bool plan_gemv(int M, int N, int Kp, int G, int act_bytes, int sm_count, GemvPla
     bool found = false;
     // two CTAs per SM only for the kernel instances compiled for it
     const int cps_max = (act_bytes == 2 ? M <= 8 : M <= 4) ? 2 : 1;
-    // W4_GEMV_ROWS (16, 32, 64 or 128) pins the row-block size for tuning.
-    static const int forced_r = [] {
-        const char* e = std::getenv("W4_GEMV_ROWS");
-        const int v = e ? std::atoi(e) : 0;
-        return (v == 16 || v == 32 || v == 64 || v == 128) ? v : 0;
-    }();
+    // W4_GEMV_ROWS (16, 32, 64 or 128) and W4_GEMV_SPLIT (K splits) pin the
+    // plan for tuning sweeps and tests
+    auto env_int = [](const char* name) {
+        const char* e = std::getenv(name);
+        return e ? std::atoi(e) : 0;
+    };
+    const int fr = env_int("W4_GEMV_ROWS");
+    const int forced_r = (fr == 16 || fr == 32 || fr == 64 || fr == 128) ? fr : 0;
+    const int forced_s = std::max(env_int("W4_GEMV_SPLIT"), 0);
     for (int cps = cps_max; cps >= 1; --cps) {
         // per-CTA shared memory: two CTAs share the SM's 228 KB (1 KB reserved each)
         const size_t cap = cps == 2 ? 115712 : 232448;
@@ -844,6 +51,10 @@ bool plan_gemv(int M, int N, int Kp, int G, int act_bytes, int sm_count, GemvPla
                 const int spl = (nst + S - 1) / S;
                 const int Se = (nst + spl - 1) / spl;
                 if (spl > spl_max) continue;
+                if ((forced_s && Se != forced_s) || (Se > 1 && NB > kMaxCounters)) {
+                    if (Se == nst) break;
+                    continue;
+                }
                 const int units = NB * Se;
                 const int grid = std::min(units, cps * sm_count);
                 const int per_cta = (units + grid - 1) / grid;
@@ -852,6 +63,10 @@ bool plan_gemv(int M, int N, int Kp, int G, int act_bytes, int sm_count, GemvPla
                 const double sm_bytes = (double)per_cta * ctas_on_sm * unit_bytes;
                 double t = std::max(wbytes / bw_total, sm_bytes / bw_sm);
                 t += per_cta * 0.3e-6 + (Se > 1 ? 1.5e-6 : 0.0);
+                // every CTA converts the activation slice of its units
+                // (measured ~0.13 ns per column and token, W4A16)
+                if (act_bytes == 2)
+                    t += per_cta * (0.3e-6 + 0.13e-9 * (double)std::min(spl * SKE, Kp) * M);
                 if (t < best * (1 - 1e-9)) {
                     best = t;
                     found = true;
@@ -861,8 +76,7 @@ bool plan_gemv(int M, int N, int Kp, int G, int act_bytes, int sm_count, GemvPla
                     p.XS = spl * SKE * act_bytes + pad;
                     p.smem = fixed + (size_t)M * p.XS + xseg_bytes(spl * SKE);
                     p.ws_bytes = 0;
-                    if (Se > 1)
-                        p.ws_bytes = ((size_t)NB * 4 + 255) / 256 * 256 + (size_t)Se * M * N * 4;
+                    if (Se > 1) p.ws_bytes = kCounterBytes + (size_t)Se * M * N * 4;
                     *out = p;
                 }
                 if (Se == nst) break;
@@ -874,14 +88,8 @@ bool plan_gemv(int M, int N, int Kp, int G, int act_bytes, int sm_count, GemvPla
 
 int launch_w4a16_gemv(const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
                       cudaStream_t st) {
-    const int gq = a.G / 32;
-    const int cpg = (gq % 8 == 0) ? 8 : (gq % 4 == 0) ? 4 : (gq % 2 == 0) ? 2 : 1;
-    const bool asym = a.zeros != nullptr;
-    if (a.M <= 8)
-        return asym ? launch_w4a16_cpg<1, true>(cpg, packed, a, p, st)
-                    : launch_w4a16_cpg<1, false>(cpg, packed, a, p, st);
-    return asym ? launch_w4a16_cpg<2, true>(cpg, packed, a, p, st)
-                : launch_w4a16_cpg<2, false>(cpg, packed, a, p, st);
+    if (a.S > 1) return launch_w4a16_gemv_split(packed, a, p, st);
+    return launch_w4a16_variant<false>(packed, a, p, st);
 }
 
 int launch_w4a8_gemv(const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,

@@ -78,12 +78,12 @@ extern "C" int w4a16_linear_noalloc(const uint16_t* x, const uint8_t* packed,
         void* base = nullptr;
         int rc = scratch_address(&base);
         if (rc) return rc;
-        const size_t ticket_bytes = ((size_t)p.NB * 4 + 255) / 256 * 256;
+        const size_t ticket_bytes = ((size_t)p.NB * 4 + 255) / 256 * 256;   // counters in use
         // The arrival counters must start at zero; the array keeps whatever
         // the previous call left, so clear them in stream order first.
         if (cudaMemsetAsync(base, 0, ticket_bytes, st) != cudaSuccess) return W4_ERR_CUDA;
         a.tickets = static_cast<int*>(base);
-        a.partial = static_cast<unsigned char*>(base) + ticket_bytes;
+        a.partial = static_cast<unsigned char*>(base) + kCounterBytes;
     }
     a.x = x; a.scales = scales; a.zeros = zeros; a.bias = bias; a.y = y;
     a.xtma = (K % 8) == 0;

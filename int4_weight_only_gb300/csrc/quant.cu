@@ -160,6 +160,8 @@ k_act_quant(const uint16_t* __restrict__ x, int K, int Kp, int8_t* __restrict__ 
 
 }  // namespace
 
+__global__ void k_stream_fence() {}
+
 int launch_pack_rtn(const float* W, int N, int K, int G, int symmetric, uint8_t* packed,
                     float* scales, uint8_t* zeros, cudaStream_t stream) {
     const int Ng = (K + G - 1) / G;
@@ -168,6 +170,11 @@ int launch_pack_rtn(const float* W, int N, int K, int G, int symmetric, uint8_t*
     if (blocks > 0x7fffffffLL) return W4_ERR_UNSUPPORTED_SHAPE;
     k_pack_rtn<<<(unsigned)blocks, 256, 0, stream>>>(W, N, K, G, Ng, symmetric, packed,
                                                      scales, zeros);
+    // An ordinary launch starts only after k_pack_rtn has finished and its
+    // stores are visible; a linear-layer kernel enqueued next may overlap
+    // this empty kernel (programmatic dependent launch) and read the new
+    // weights before its dependency wait.
+    k_stream_fence<<<1, 32, 0, stream>>>();
     return cudaGetLastError() == cudaSuccess ? W4_OK : W4_ERR_CUDA;
 }
 

@@ -275,6 +275,10 @@ __device__ __forceinline__ int ld_cg_s32(const int* p) {
     return v;
 }
 
+// L2-coherent loads (skip L1) for partial sums other CTAs wrote.
+__device__ __forceinline__ float ld_cg(const float* p) { return ld_cg_f32(p); }
+__device__ __forceinline__ int32_t ld_cg(const int32_t* p) { return ld_cg_s32(p); }
+
 __device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
     __nv_bfloat16 h = __float2bfloat16_rn(f);
     return *reinterpret_cast<uint16_t*>(&h);

@@ -66,6 +66,8 @@ struct GemvArgs {
 
 // The launchers encode the tensor map of `packed` for the plan's box shape
 // and launch with programmatic dependent launch enabled.
+int launch_w4a16_gemv_split(const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
+                            cudaStream_t stream);
 int launch_w4a16_gemv(const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
                       cudaStream_t stream);
 int launch_w4a8_gemv(const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
@@ -73,6 +75,11 @@ int launch_w4a8_gemv(const uint8_t* packed, const GemvArgs& a, const GemvPlan& p
 
 // ---------------------------------------------------------------- prefill
 // Tensor-core kernel for M > 16 (requires K % 8 == 0 and 16-byte aligned x).
+// Split-K arrival counters occupy a fixed prefix of every workspace, so the
+// partial sums of one call never land where another call's counters are.
+constexpr size_t kCounterBytes = W4_WORKSPACE_COUNTER_BYTES;
+constexpr int kMaxCounters = (int)(kCounterBytes / 4);
+
 struct GemmPlan {
     bool pair = false; // CTA-pair tiles (256 weight rows, cluster of 2)
     int BN = 0;        // tokens per tile (128 or 256)

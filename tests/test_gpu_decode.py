@@ -189,3 +189,30 @@ def test_w4a8_int32_worst_case(w4):
     oacc, _ = O.w4a8_linear(to_np(qx), np.ones(1, np.float32), to_np(packed),
                             np.ones(N, np.float32), None)
     assert np.array_equal(to_np(acc).astype(np.int64), oacc)
+
+
+def test_workspace_shared_by_shapes(w4, monkeypatch):
+    """One zero-filled workspace serves split-K calls of different shapes.
+    The arrival counters live in a fixed prefix, so the partial sums of a
+    call with few row blocks (N = 512: 4 blocks of 128 rows) never land
+    where a call with many row blocks (N = 12288: 96 blocks) keeps its
+    counters; the calls alternate twice on the same buffer."""
+    monkeypatch.setenv("W4_GEMV_ROWS", "128")
+    monkeypatch.setenv("W4_GEMV_SPLIT", "4")
+    shapes = [(1, 512, 8192, 128, True), (8, 12288, 2048, 32, False)] * 2
+    need = max(w4.w4a16_workspace_bytes(M, N, K, G) for M, N, K, G, _ in shapes)
+    assert need > 0
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    for i, (M, N, K, G, sym) in enumerate(shapes):
+        packed, scales, zeros = WL.make_random_format(N, K, G, sym, 50 + i)
+        x = WL.make_activations(K, M, 60 + i)
+        zc = None if zeros is None else zeros.cuda()
+        y = w4.w4a16_linear(x.cuda(), packed.cuda(), scales.cuda(), zc, None, N, K, G,
+                            workspace=ws)
+        torch.cuda.synchronize()
+        rows = np.arange(N) if N <= 1024 else np.unique(np.concatenate(
+            [np.arange(0, N, 97), np.arange(N - 1024, N, 5)]))
+        yref = O.w4a16_linear(x, packed.numpy()[rows], scales.numpy()[rows],
+                              None if zeros is None else zeros.numpy()[rows], None, K, G)
+        assert_close(y[:, torch.as_tensor(rows, device=y.device)], yref, f"call {i} N{N}")
+    assert w4.w4_get_device_error() == 0
