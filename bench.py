@@ -79,6 +79,8 @@ def source_digest(files) -> str:
 
 
 DECODE_SOURCES = ["int4_weight_only_gb300/csrc/gemv.cu",
+                  "int4_weight_only_gb300/csrc/gemv_split.cu",
+                  "int4_weight_only_gb300/csrc/gemv_impl.cuh",
                   "int4_weight_only_gb300/csrc/w4_device.cuh",
                   "int4_weight_only_gb300/csrc/w4_internal.h"]
 
