@@ -185,11 +185,19 @@ def barrier(world):
 
 
 def max_over_ranks(v: float, world: int) -> float:
+    """The slowest rank's time: the job is done when every replica is."""
     if world <= 1:
         return v
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate_gbs(bytes_per_rank_step: float, steps: int, world: int, sec: float) -> float:
+    """Whole-job throughput: the bytes all `world` replicas streamed over
+    `steps` steps, divided by the slowest rank's time (weak scaling)."""
+    return bytes_per_rank_step * steps * world / sec / 1e9
 
 
 def time_graph_steps(step_fn, K, R, world):
@@ -463,7 +471,7 @@ def run_ours(args, world, rank):
     with ClockSampler(dev) as clk:
         sec = time_graph_steps(ds.step, args.steps, ds.R, world)
     sec = max_over_ranks(sec, world)
-    value = ds.bytes_step * args.steps * world / sec / 1e9
+    value = aggregate_gbs(ds.bytes_step, args.steps, world, sec)
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
@@ -494,7 +502,7 @@ def run_ours(args, world, rank):
     ke = min(args.steps, 2000)
     dt, h2d, d2h = measure_e2e(w4, ds, ke)
     dt = max_over_ranks(dt, world)
-    res["e2e"] = {"value": round(ds.bytes_step * ke * world / dt / 1e9, 1), "unit": "GB/s",
+    res["e2e"] = {"value": round(aggregate_gbs(ds.bytes_step, ke, world, dt), 1), "unit": "GB/s",
                   "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                   "ms_per_step": round(dt / ke * 1e3, 4), "steps": ke}
     del ds
