@@ -172,7 +172,7 @@ int w4a16_linear(const uint16_t* x, const uint8_t* packed, const float* scales,
     rc = split_workspace(p, workspace, workspace_bytes, &a.tickets, &a.partial);
     if (rc) return rc;
     a.x = x; a.scales = scales; a.zeros = zeros; a.bias = bias; a.y = y;
-    a.xtma = (K % 8) == 0;
+    a.xtma = (K % 8) == 0 && gemv_tma_activations();
     a.err = device_error_flag();
     if (!a.err) return W4_ERR_CUDA;
     a.M = M; a.N = N; a.K = K; a.Kp = (int)Kp; a.G = group_size; a.Ng = (int)(Kp / group_size);

@@ -4,6 +4,11 @@
 
 namespace w4 {
 
+bool gemv_tma_activations() {
+    const char* e = std::getenv("W4_GEMV_XTMA");
+    return e && std::atoi(e) == 1;
+}
+
 bool plan_gemv(int M, int N, int Kp, int G, int act_bytes, int sm_count, GemvPlan* out) {
     if (M < 1 || M > 16 || N < 1 || Kp < 1 || G < 32 || sm_count < 1) return false;
     const int gq = G / 32;
@@ -33,7 +38,9 @@ bool plan_gemv(int M, int N, int Kp, int G, int act_bytes, int sm_count, GemvPla
     const int fr = env_int("W4_GEMV_ROWS");
     const int forced_r = (fr == 16 || fr == 32 || fr == 64 || fr == 128) ? fr : 0;
     const int forced_s = std::max(env_int("W4_GEMV_SPLIT"), 0);
+    const int forced_cps = env_int("W4_GEMV_CPS");      // CTAs of this kernel per SM
     for (int cps = cps_max; cps >= 1; --cps) {
+        if ((forced_cps == 1 || forced_cps == 2) && cps != forced_cps) continue;
         // per-CTA shared memory: two CTAs share the SM's 228 KB (1 KB reserved each)
         const size_t cap = cps == 2 ? 115712 : 232448;
         if (fixed >= cap) continue;

@@ -216,3 +216,25 @@ def test_workspace_shared_by_shapes(w4, monkeypatch):
                               None if zeros is None else zeros.numpy()[rows], None, K, G)
         assert_close(y[:, torch.as_tensor(rows, device=y.device)], yref, f"call {i} N{N}")
     assert w4.w4_get_device_error() == 0
+
+
+@pytest.mark.parametrize("xtma", ["0", "1"])
+@pytest.mark.parametrize("M,N,K,G,sym", [(1, 4608, 3584, 128, True), (8, 640, 3840, 32, False),
+                                         (3, 1000, 18944, 128, True)])
+def test_decode_activation_staging_paths(w4, monkeypatch, xtma, M, N, K, G, sym):
+    """Activations read from global memory while converting (default) or
+    first copied into shared memory by a bulk TMA copy (W4_GEMV_XTMA=1):
+    same tolerance, same bits for both."""
+    monkeypatch.setenv("W4_GEMV_XTMA", xtma)
+    seed = M + N + K + G
+    packed, scales, zeros = WL.make_random_format(N, K, G, sym, seed)
+    x = WL.make_activations(K, M, seed + 1)
+    zc = None if zeros is None else zeros.cuda()
+    y = w4.w4a16_linear(x.cuda(), packed.cuda(), scales.cuda(), zc, None, N, K, G)
+    torch.cuda.synchronize()
+    yref = O.w4a16_linear(x, packed.numpy(), scales.numpy(),
+                          None if zeros is None else zeros.numpy(), None, K, G)
+    assert_close(y, yref, f"xtma{xtma} M{M} N{N} K{K}")
+    monkeypatch.setenv("W4_GEMV_XTMA", "1" if xtma == "0" else "0")
+    y2 = w4.w4a16_linear(x.cuda(), packed.cuda(), scales.cuda(), zc, None, N, K, G)
+    assert torch.equal(y, y2), "the two staging paths differ"
