@@ -340,7 +340,7 @@ def cpu_baseline_decode(lins, frac=1 / 16, budget_s=12.0):
     (oracle packing outside the timing; dequantize + fp64 matvec inside)."""
     sample = _oracle_row_sample(lins, frac, seed=7)
     by, t, n = 0.0, 0.0, 0
-    while t < budget_s and n < 50:
+    while t < budget_s and n < 2000:
         t0 = time.perf_counter()
         by += _oracle_step(sample)
         t += time.perf_counter() - t0
