@@ -422,6 +422,9 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
     // group of a segment: segments of CPG*32 columns tile the groups exactly,
     // so g = segment / (G / (CPG*32)), a shift when that ratio is a power of 2
     const int gdiv = a.G / (CPG * 32);
+    // G = 32 with rows of whole 8-group runs: scales and zero points of a
+    // box can be read with vector loads (16 B / 8 B aligned)
+    const bool vec_groups = gdiv == 1 && (Ng % 8) == 0;
     const int gshift = (gdiv & (gdiv - 1)) == 0 ? __ffs(gdiv) - 1 : -1;
     const float zc[4] = {0.f, 0.f, 0.f, 0.f};
     SmemCtl* ctl = sm.ctl;
@@ -445,6 +448,34 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
         const float b_hi = bias ? __ldg(bias + nr8) : 0.f;
         float sr[SEG], sr8[SEG], zr[SEG], zr8[SEG];
         auto load_scales = [&](int kw, float* r_, float* r8_, float* z_, float* z8_) {
+            if constexpr (SEG == 8) {
+                // one group per segment (G = 32): a row's 8 scales (32 B) and
+                // zero points (8 B) of the box are contiguous; vector loads
+                // when they are aligned and inside the row
+                const int g0 = kw >> (5 + LOG_CPG);
+                if (vec_groups && g0 + 8 <= Ng) {
+                    const float4* s4 = reinterpret_cast<const float4*>(sc_r + g0);
+                    const float4* s48 = reinterpret_cast<const float4*>(sc_r8 + g0);
+                    const float4 a0 = __ldg(s4), a1 = __ldg(s4 + 1);
+                    const float4 b0 = __ldg(s48), b1 = __ldg(s48 + 1);
+                    r_[0] = a0.x; r_[1] = a0.y; r_[2] = a0.z; r_[3] = a0.w;
+                    r_[4] = a1.x; r_[5] = a1.y; r_[6] = a1.z; r_[7] = a1.w;
+                    r8_[0] = b0.x; r8_[1] = b0.y; r8_[2] = b0.z; r8_[3] = b0.w;
+                    r8_[4] = b1.x; r8_[5] = b1.y; r8_[6] = b1.z; r8_[7] = b1.w;
+                    if (ASYM) {
+                        const uint2 q = __ldg(reinterpret_cast<const uint2*>(zp_r + g0));
+                        const uint2 q8 = __ldg(reinterpret_cast<const uint2*>(zp_r8 + g0));
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            z_[j] = (float)((q.x >> (8 * j)) & 0xFF);
+                            z_[j + 4] = (float)((q.y >> (8 * j)) & 0xFF);
+                            z8_[j] = (float)((q8.x >> (8 * j)) & 0xFF);
+                            z8_[j + 4] = (float)((q8.y >> (8 * j)) & 0xFF);
+                        }
+                    }
+                    return;
+                }
+            }
 #pragma unroll
             for (int j = 0; j < SEG; ++j) {
                 const int sg = (kw >> (5 + LOG_CPG)) + j;
