@@ -131,7 +131,7 @@ size_t w4a16_workspace_bytes(int M, int N, int K, int group_size) {
         return p.ws_bytes;
     }
     GemmPlan g;
-    if (!plan_gemm(M, N, K, current_sm_count(), &g)) return 0;
+    if (!plan_gemm(M, N, K, group_size, current_sm_count(), &g)) return 0;
     return g.ws_bytes;
 }
 
@@ -155,7 +155,7 @@ int w4a16_linear(const uint16_t* x, const uint8_t* packed, const float* scales,
     if (M > 16) {
         if (K % 8 != 0) return W4_ERR_UNSUPPORTED_SHAPE;
         GemmPlan g;
-        if (!plan_gemm(M, N, K, current_sm_count(), &g)) return W4_ERR_UNSUPPORTED_SHAPE;
+        if (!plan_gemm(M, N, K, group_size, current_sm_count(), &g)) return W4_ERR_UNSUPPORTED_SHAPE;
         if (g.S > 1) {
             if (!workspace || workspace_bytes < g.ws_bytes) return W4_ERR_WORKSPACE;
             if (!aligned16(workspace)) return W4_ERR_MISALIGNED;

@@ -48,13 +48,11 @@ namespace w4 {
 namespace {
 
 constexpr int BM = 128;                 // weight rows per tile (MMA M)
-constexpr int BK = 64;                  // columns per stage
-constexpr int P_BYTES = BM * BK / 2;    // 4 KB
-constexpr int A_BYTES = BM * BK * 2;    // 16 KB
+constexpr int BK = 64;                  // columns per K block (one 128-byte swizzle row)
+constexpr int P_BYTES = BM * BK / 2;    // 4 KB of packed codes per K block
+constexpr int A_BYTES = BM * BK * 2;    // 16 KB of bf16 A per K block
 constexpr int DQ_GROUP_THREADS = 256;   // dequantizing threads per stage
 constexpr int DQ_TPR = DQ_GROUP_THREADS / BM;  // threads per weight row
-constexpr int DQ_COLS = BK / DQ_TPR;     // columns per thread per stage
-constexpr int DQ_CHUNKS = DQ_COLS / 8;   // 16-byte bf16 chunks per thread
 constexpr int EPI_THREADS = 128;
 constexpr int DQ_BASE = 96;             // first dequantizing thread (after 3 role warps)
 
@@ -90,9 +88,11 @@ struct Ctl {
     int last;   // the tile's splits are all written (split-K hand-off)
 };
 
-template <int XR, int NST, int NSA, int NSP>
+// KB: K blocks of 64 columns per stage
+template <int XR, int NST, int NSA, int NSP, int KB>
 constexpr size_t smem_bytes() {
-    return 1024 + (size_t)NST * XR * BK * 2 + (size_t)NSA * A_BYTES + (size_t)NSP * P_BYTES +
+    return 1024 + (size_t)NST * XR * BK * KB * 2 + (size_t)NSA * A_BYTES * KB +
+           (size_t)NSP * P_BYTES * KB +
            (sizeof(Ctl<NST, NSA, NSP>) + 15) / 16 * 16;
 }
 
@@ -114,23 +114,27 @@ __device__ __forceinline__ void unit_of(const GemmArgs& a, int u, int& nb, int& 
     ks1 = min(ks0 + a.spl, a.nks);
 }
 
-template <int BN, int NST, int NSA, int NSP, int DQG, bool PAIR>
+template <int BN, int NST, int NSA, int NSP, int DQG, bool PAIR, int KB>
 __global__ void __launch_bounds__(threads_of<DQG>(), 1)
 k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmP,
                 const GemmArgs a) {
     constexpr int THREADS = threads_of<DQG>();
     constexpr int XR = PAIR ? BN / 2 : BN;                  // x rows staged by this CTA
     constexpr int RB = PAIR ? 2 * BM : BM;                  // weight rows per tile
-    constexpr int X_BYTES = XR * BK * 2;
+    constexpr int SK = BK * KB;                             // columns per stage
+    constexpr int X_BYTES = XR * SK * 2;                    // KB blocks of XR x 128 B
+    constexpr int A_ST = A_BYTES * KB, P_ST = P_BYTES * KB; // A / packed bytes per stage
+    constexpr int DQ_COLS = SK / DQ_TPR;                    // columns per thread per stage
+    constexpr int DQ_CHUNKS = DQ_COLS / 8;                  // 16-byte bf16 chunks per thread
     constexpr uint32_t TMEM_COLS = 2 * BN;
     constexpr uint32_t IDESC = idesc_bf16_f32(RB, BN);
     constexpr int NCTA = PAIR ? 2 : 1;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = align1024(smem_raw);
     uint8_t* xs = base;                                     // NST x X_BYTES
-    uint8_t* as = xs + NST * X_BYTES;                       // NSA x 16 KB
-    uint8_t* ps = as + NSA * A_BYTES;                       // NSP x 4 KB
-    auto* ctl = reinterpret_cast<Ctl<NST, NSA, NSP>*>(ps + NSP * P_BYTES);
+    uint8_t* as = xs + NST * X_BYTES;                       // NSA x A_ST
+    uint8_t* ps = as + NSA * A_ST;                          // NSP x P_ST
+    auto* ctl = reinterpret_cast<Ctl<NST, NSA, NSP>*>(ps + NSP * P_ST);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // a pair tile is worked on by the two CTAs of a cluster: rank 0 issues
     // the MMAs, each CTA stages its half of x and dequantizes its 128 rows
@@ -199,15 +203,18 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                         if constexpr (PAIR) {
                             // both halves land on the rank-0 barrier
                             if (rank == 0) mbar_arrive_expect_tx(&full[st], 2 * X_BYTES);
-                            tma_load_2d_pair(xs + st * X_BYTES, &tmX, ks * BK, tb * BN + (int)rank * XR,
-                                             at_rank0(&full[st]), pol);
+                            for (int kb = 0; kb < KB; ++kb)
+                                tma_load_2d_pair(xs + st * X_BYTES + kb * XR * 128, &tmX, ks * SK + kb * BK,
+                                                 tb * BN + (int)rank * XR, at_rank0(&full[st]), pol);
                         } else {
                             mbar_arrive_expect_tx(&full[st], X_BYTES);
-                            tma_load_2d(xs + st * X_BYTES, &tmX, ks * BK, tb * BN, &full[st], pol);
+                            for (int kb = 0; kb < KB; ++kb)
+                                tma_load_2d(xs + st * X_BYTES + kb * XR * 128, &tmX, ks * SK + kb * BK,
+                                            tb * BN, &full[st], pol);
                         }
                     } else {
-                        mbar_arrive_expect_tx(&full[st], P_BYTES);
-                        tma_load_2d(ps + st * P_BYTES, &tmP, ks * (BK / 2), nb * RB + (int)rank * BM,
+                        mbar_arrive_expect_tx(&full[st], P_ST);
+                        tma_load_2d(ps + st * P_ST, &tmP, ks * (SK / 2), nb * RB + (int)rank * BM,
                                     &full[st], pol);
                     }
                 }
@@ -247,21 +254,22 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_addr = smem_u32(as + sa * A_BYTES);
+                    const uint32_t a_addr = smem_u32(as + sa * A_ST);
                     const uint32_t x_addr = smem_u32(xs + st * X_BYTES);
+                    // K step i: block i / 4 (A_BYTES / XR x 128 B apart), 32 B per step inside it
+                    auto a_k = [&](int i) { return a_addr + (i >> 2) * A_BYTES + 32 * (i & 3); };
+                    auto x_k = [&](int i) { return x_addr + (i >> 2) * (XR * 128) + 32 * (i & 3); };
                     if constexpr (PAIR) {
 #pragma unroll
-                        for (int i = 0; i < BK / 16; ++i)
-                            tc_mma_f16_pair(d, smem_desc_sw128(a_addr + 32 * i),
-                                            smem_desc_sw128(x_addr + 32 * i), IDESC,
+                        for (int i = 0; i < SK / 16; ++i)
+                            tc_mma_f16_pair(d, smem_desc_sw128(a_k(i)), smem_desc_sw128(x_k(i)), IDESC,
                                             (ks > ks0 || i > 0) ? 1u : 0u);
                         tc_commit_pair(&ctl->tempty[st], 3);
                         tc_commit_pair(&ctl->aempty[sa], 3);
                     } else {
 #pragma unroll
-                        for (int i = 0; i < BK / 16; ++i)
-                            tc_mma_f16(d, smem_desc_sw128(a_addr + 32 * i),
-                                       smem_desc_sw128(x_addr + 32 * i), IDESC,
+                        for (int i = 0; i < SK / 16; ++i)
+                            tc_mma_f16(d, smem_desc_sw128(a_k(i)), smem_desc_sw128(x_k(i)), IDESC,
                                        (ks > ks0 || i > 0) ? 1u : 0u);
                         tc_commit(&ctl->tempty[st]);
                         tc_commit(&ctl->aempty[sa]);
@@ -300,7 +308,7 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
             const uint8_t* zrow = a.zeros ? a.zeros + (size_t)n * a.Ng : nullptr;
             // scale (and offset -(128 + z) s) of this thread's columns,
             // loaded one turn ahead
-            auto group_of = [&](int ks) { return min((ks * BK + DQ_COLS * h) / a.G, a.Ng - 1); };
+            auto group_of = [&](int ks) { return min((ks * SK + DQ_COLS * h) / a.G, a.Ng - 1); };
             const int kf = min(ks0 + lead, ks1 - 1);
             float sc = __ldg(srow + group_of(kf));
             float zz = zrow ? (float)__ldg(zrow + group_of(kf)) : 8.f;
@@ -320,10 +328,13 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                                      mbar_wait(&ctl->pfull[sp], (it / NSP) & 1, &ctl->abort, a.err));
                 uint32_t wv[DQ_CHUNKS];
                 if (ok) {
-                    const uint8_t* prow = ps + sp * P_BYTES + r * (BK / 2) + h * (DQ_COLS / 2);
-                    if constexpr (DQ_CHUNKS == 4) {
-                        const uint4 q = *reinterpret_cast<const uint4*>(prow);
-                        wv[0] = q.x; wv[1] = q.y; wv[2] = q.z; wv[3] = q.w;
+                    const uint8_t* prow = ps + sp * P_ST + r * (SK / 2) + h * (DQ_COLS / 2);
+                    if constexpr (DQ_CHUNKS >= 4) {
+#pragma unroll
+                        for (int i = 0; i < DQ_CHUNKS / 4; ++i) {
+                            const uint4 q = *reinterpret_cast<const uint4*>(prow + 16 * i);
+                            wv[4 * i] = q.x; wv[4 * i + 1] = q.y; wv[4 * i + 2] = q.z; wv[4 * i + 3] = q.w;
+                        }
                     } else {
                         const uint2 q = *reinterpret_cast<const uint2*>(prow);
                         wv[0] = q.x; wv[1] = q.y;
@@ -335,10 +346,11 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                     ok = mbar_wait(&ctl->aempty[sa], ((it / NSA) & 1) ^ 1, &ctl->abort, a.err);
                 ok = __all_sync(0xffffffffu, ok);
                 if (ok) {
-                    uint8_t* arow = as + sa * A_BYTES + r * 128;
+                    uint8_t* arow = as + sa * A_ST + r * 128;
 #pragma unroll
                     for (int jj = 0; jj < DQ_CHUNKS; ++jj) {
-                        const int j = DQ_CHUNKS * h + jj;       // 16-byte chunk of the row
+                        const int jg = DQ_CHUNKS * h + jj;      // 16-byte chunk of the stage's row
+                        const int j = jg & 7;                   // chunk inside its K block
                         const uint32_t w = wv[jj], wh = w >> 4;
                         // bf16x2 (128 + c_2i, 128 + c_2i+1) for i = 0..3
                         const uint32_t e = 0x43004300u, m = 0x000F000Fu;
@@ -351,7 +363,7 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                         o.y = pack_bf16x2(fmaf(bf16lo(p23), sc, cc), fmaf(bf16hi(p23), sc, cc));
                         o.z = pack_bf16x2(fmaf(bf16lo(p45), sc, cc), fmaf(bf16hi(p45), sc, cc));
                         o.w = pack_bf16x2(fmaf(bf16lo(p67), sc, cc), fmaf(bf16hi(p67), sc, cc));
-                        *reinterpret_cast<uint4*>(arow + ((j ^ (r & 7)) << 4)) = o;
+                        *reinterpret_cast<uint4*>(arow + (jg >> 3) * A_BYTES + ((j ^ (r & 7)) << 4)) = o;
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
@@ -481,12 +493,12 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     }
 }
 
-template <int BN, int NST, int NSA, int NSP, int DQG, bool PAIR>
+template <int BN, int NST, int NSA, int NSP, int DQG, bool PAIR, int KB>
 struct Variant {
     static constexpr int XR = PAIR ? BN / 2 : BN;
-    static constexpr size_t smem = smem_bytes<XR, NST, NSA, NSP>();
+    static constexpr size_t smem = smem_bytes<XR, NST, NSA, NSP, KB>();
     static_assert(smem <= 232448, "shared memory");
-    static constexpr auto kernel = k_w4a16_gemm_tc<BN, NST, NSA, NSP, DQG, PAIR>;
+    static constexpr auto kernel = k_w4a16_gemm_tc<BN, NST, NSA, NSP, DQG, PAIR, KB>;
 
     static bool prepare() {
         return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -542,7 +554,7 @@ struct Variant {
                             (uint64_t)a.K * 2, BK, XR, CU_TENSOR_MAP_SWIZZLE_128B))
             return W4_ERR_CUDA;
         if (!encode_tmap_2d(&tmP, CU_TENSOR_MAP_DATA_TYPE_UINT8, packed, (uint64_t)(Kp / 2),
-                            (uint64_t)a.N, (uint64_t)(Kp / 2), BK / 2, BM, CU_TENSOR_MAP_SWIZZLE_NONE))
+                            (uint64_t)a.N, (uint64_t)(Kp / 2), BK * KB / 2, BM, CU_TENSOR_MAP_SWIZZLE_NONE))
             return W4_ERR_CUDA;
         if (!prepare()) return W4_ERR_CUDA;
         cudaLaunchAttribute at[1];
@@ -552,9 +564,14 @@ struct Variant {
     }
 };
 
-using Single256 = Variant<256, 4, 4, 8, 1, false>;
-using Single128 = Variant<128, 8, 4, 8, 1, false>;
-using Pair256 = Variant<256, 6, 4, 8, 1, true>;
+using Single256 = Variant<256, 4, 4, 8, 1, false, 1>;
+using Single128 = Variant<128, 8, 4, 8, 1, false, 1>;
+using Pair256 = Variant<256, 6, 4, 8, 1, true, 1>;
+// 128 columns per stage (two K blocks): half the per-stage hand-offs for the
+// same MMA work; group sizes that are multiples of 64 only (a dequantizing
+// thread's 64 columns must lie in one group)
+using Single256K2 = Variant<256, 2, 2, 4, 1, false, 2>;
+using Pair256K2 = Variant<256, 4, 2, 4, 1, true, 2>;
 
 }  // namespace
 
@@ -562,7 +579,7 @@ using Pair256 = Variant<256, 6, 4, 8, 1, true>;
 // tokens on a CTA pair; K is split S ways when the tiles alone fill the GPU
 // poorly.  Cost = waves x stages per unit x relative stage time, plus a
 // charge per split for the fp32 partials and the hand-off.
-bool plan_gemm(int M, int N, int K, int sm_count, GemmPlan* out) {
+bool plan_gemm(int M, int N, int K, int G, int sm_count, GemmPlan* out) {
     if (M < 1 || N < 1 || K < 1 || sm_count < 1) return false;
     // W4_GEMM_BN (128 or 256), W4_GEMM_SPLIT (1..8) and W4_GEMM_PAIR (0 or 1)
     // pin the plan (tuning sweeps, tests of every variant); read on every
@@ -577,18 +594,22 @@ bool plan_gemm(int M, int N, int K, int sm_count, GemmPlan* out) {
     struct Cand {
         bool pair;
         int BN;
+        int kb;         // 64-column K blocks per stage
         int slots;      // CTAs (pairs) resident at once
-        double stage;   // time of one 64-column stage, relative to one CTA's 128 x 256
+        double stage;   // time of one stage, relative to one CTA's 128 x 256 x 64 stage
     };
-    // measured on the 7B prefill shapes: a pair stage (256 x 256 on two SMs)
-    // runs 1-3% slower than two single-CTA stages (128 x 256 each); a
+    // measured on the 7B prefill shapes (gate_up M = 2048): a 128-column
+    // stage takes 1.52 times a 64-column one (1.55 on a pair); a pair stage
+    // (256 x 256 on two SMs) runs 1-3% slower than two single-CTA stages; a
     // 128-token stage takes as long as a 256-token one
-    const Cand cands[3] = {
-        {true, 256, Pair256::slots(sm_count), 1.02},
-        {false, 256, Single256::slots(sm_count), 1.0},
-        {false, 128, Single128::slots(sm_count), 1.0},
+    const int forced_kb = env_int("W4_GEMM_KB");
+    const Cand cands[5] = {
+        {true, 256, 2, Pair256K2::slots(sm_count), 1.55},
+        {false, 256, 2, Single256K2::slots(sm_count), 1.52},
+        {true, 256, 1, Pair256::slots(sm_count), 1.02},
+        {false, 256, 1, Single256::slots(sm_count), 1.0},
+        {false, 128, 1, Single128::slots(sm_count), 1.0},
     };
-    const int nks = (K + BK - 1) / BK;
     double best = 1e30;
     bool found = false;
     for (const Cand& c : cands) {
@@ -596,6 +617,9 @@ bool plan_gemm(int M, int N, int K, int sm_count, GemmPlan* out) {
         if (forced_pair == 0 && c.pair) continue;
         if (forced_pair == 1 && !c.pair) continue;
         if ((forced_bn == 128 || forced_bn == 256) && c.BN != forced_bn) continue;
+        if ((forced_kb == 1 || forced_kb == 2) && c.kb != forced_kb) continue;
+        if (c.kb == 2 && G % 64 != 0) continue;
+        const int nks = (K + BK * c.kb - 1) / (BK * c.kb);
         const int RB = c.pair ? 2 * BM : BM;
         const int TB = (M + c.BN - 1) / c.BN;
         const int ntiles = ((N + RB - 1) / RB) * TB;
@@ -614,6 +638,7 @@ bool plan_gemm(int M, int N, int K, int sm_count, GemmPlan* out) {
                 found = true;
                 GemmPlan p;
                 p.pair = c.pair;
+                p.kb = c.kb;
                 p.BN = c.BN; p.TB = TB; p.ntiles = ntiles; p.S = S; p.spl = spl; p.nks = nks;
                 p.units = units;
                 p.grid = (c.pair ? 2 : 1) * (units < c.slots ? units : c.slots);
@@ -637,6 +662,10 @@ int launch_w4a16_gemm(const uint16_t* x, const uint8_t* packed, const float* sca
     if (p.S > 1) {
         a.tickets = static_cast<int*>(workspace);
         a.partial = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + p.ticket_bytes);
+    }
+    if (p.kb == 2) {
+        if (p.pair) return Pair256K2::launch(x, packed, p, a, Kp, stream);
+        return Single256K2::launch(x, packed, p, a, Kp, stream);
     }
     if (p.pair) return Pair256::launch(x, packed, p, a, Kp, stream);
     if (p.BN == 256) return Single256::launch(x, packed, p, a, Kp, stream);

@@ -86,6 +86,7 @@ constexpr int kMaxCounters = (int)(kCounterBytes / 4);
 
 struct GemmPlan {
     bool pair = false; // CTA-pair tiles (256 weight rows, cluster of 2)
+    int kb = 1;        // 64-column K blocks per stage (1 or 2)
     int BN = 0;        // tokens per tile (128 or 256)
     int TB = 0;        // token blocks
     int ntiles = 0;    // output tiles (128 or 256 weight rows x BN tokens)
@@ -97,7 +98,7 @@ struct GemmPlan {
     size_t ticket_bytes = 0;  // split-K counters at the start of the workspace
     size_t ws_bytes = 0;
 };
-bool plan_gemm(int M, int N, int K, int sm_count, GemmPlan* plan);
+bool plan_gemm(int M, int N, int K, int G, int sm_count, GemmPlan* plan);
 int launch_w4a16_gemm(const uint16_t* x, const uint8_t* packed, const float* scales,
                       const uint8_t* zeros, const float* bias, uint16_t* y, int M, int N, int K,
                       int Kp, int G, const GemmPlan& p, void* workspace, int* err,

@@ -57,16 +57,21 @@ def test_prefill_workloads(w4, M, which):
     assert_close(y[:, torch.as_tensor(rows, device=y.device)], yref, lin.name)
 
 
-@pytest.mark.parametrize("pair,bn,split", [
-    (1, 256, 1), (1, 256, 2), (1, 256, 3), (0, 256, 1), (0, 256, 2), (0, 128, 1), (0, 128, 4),
+@pytest.mark.parametrize("pair,bn,split,kb", [
+    (1, 256, 1, 1), (1, 256, 2, 1), (1, 256, 3, 1), (0, 256, 1, 1), (0, 256, 2, 1), (0, 128, 1, 1),
+    (0, 128, 4, 1), (1, 256, 1, 2), (1, 256, 2, 2), (0, 256, 1, 2), (0, 256, 3, 2),
 ])
 @pytest.mark.parametrize("M,N,K,G,sym", [
     (300, 520, 1000, 64, False), (700, 384, 3584, 128, True), (40, 1000, 512, 32, True),
 ])
-def test_prefill_every_variant(w4, monkeypatch, pair, bn, split, M, N, K, G, sym):
-    """Each tile variant (CTA pair 256 x 256, one CTA 128 x 256 / 128 x 128)
-    and K split, pinned through the planner's tuning variables, on ragged
-    shapes: same tolerance, deterministic, no device error."""
+def test_prefill_every_variant(w4, monkeypatch, pair, bn, split, kb, M, N, K, G, sym):
+    """Each tile variant (CTA pair 256 x 256, one CTA 128 x 256 / 128 x 128,
+    64 or 128 columns per stage) and K split, pinned through the planner's
+    tuning variables, on ragged shapes: same tolerance, deterministic, no
+    device error."""
+    if kb == 2 and G % 64:
+        pytest.skip("128-column stages need group sizes that are multiples of 64")
+    monkeypatch.setenv("W4_GEMM_KB", str(kb))
     monkeypatch.setenv("W4_GEMM_PAIR", str(pair))
     monkeypatch.setenv("W4_GEMM_BN", str(bn))
     monkeypatch.setenv("W4_GEMM_SPLIT", str(split))
@@ -82,7 +87,7 @@ def test_prefill_every_variant(w4, monkeypatch, pair, bn, split, M, N, K, G, sym
     assert w4.w4_get_device_error() == 0
     yref = O.w4a16_linear(x, packed.numpy(), scales.numpy(),
                           None if zeros is None else zeros.numpy(), b.numpy(), K, G)
-    assert_close(y, yref, f"pair{pair} BN{bn} S{split} M{M} N{N} K{K}")
+    assert_close(y, yref, f"pair{pair} BN{bn} S{split} KB{kb} M{M} N{N} K{K}")
     assert torch.equal(y, y2), "prefill is not deterministic"
 
 
