@@ -71,21 +71,28 @@ def padded_k(K: int, group_size: int) -> int:
 
 
 def _ptr(t: Optional[torch.Tensor]):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    # plain ints: the argtypes (c_void_p) convert them without a wrapper object
+    return None if t is None else t.data_ptr()
+
+
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
 
 
 def _stream(t: torch.Tensor, stream=None):
-    if stream is None:
-        stream = torch.cuda.current_stream(t.device)
-    return ctypes.c_void_p(stream.cuda_stream)
+    """cudaStream_t of `stream`, or of the current torch stream of t's device."""
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_stream is not None:
+        return _raw_stream(t.get_device())
+    return torch.cuda.current_stream(t.device).cuda_stream
 
 
 def _need(t, dtype, shape, name):
-    if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
-    if tuple(t.shape) != tuple(shape):
+    if t.shape != shape:
         raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
@@ -103,14 +110,32 @@ _ws = {}
 def _workspace(device: torch.device, nbytes: int) -> Optional[torch.Tensor]:
     """A per-device zero-filled scratch buffer (grown on demand); the kernels
     leave its counters at zero after each call."""
-    if nbytes == 0:
-        return None
     idx = device.index if device.index is not None else torch.cuda.current_device()
     buf = _ws.get(idx)
+    if nbytes == 0:
+        return buf
     if buf is None or buf.numel() < nbytes:
         buf = torch.zeros(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
         _ws[idx] = buf
     return buf
+
+
+W4_ERR_WORKSPACE = -6
+
+
+def _call_with_workspace(fn, name, args_before, args_after, device, workspace, need_bytes):
+    """Call fn(*args_before, ws_ptr, ws_bytes, *args_after).  Without a caller
+    workspace the cached one goes in as it is; only when the library answers
+    that it is too small is the size queried and the buffer grown (so the
+    common call costs no size query)."""
+    ws = workspace if workspace is not None else _ws.get(
+        device.index if device.index is not None else torch.cuda.current_device())
+    wsb = 0 if ws is None else ws.numel() * ws.element_size()
+    rc = fn(*args_before, _ptr(ws), wsb, *args_after)
+    if rc == W4_ERR_WORKSPACE and workspace is None:
+        ws = _workspace(device, need_bytes())
+        rc = fn(*args_before, _ptr(ws), ws.numel() * ws.element_size(), *args_after)
+    _check(name, rc)
 
 
 # ------------------------------------------------------------- entry points
@@ -166,13 +191,12 @@ def w4a16_linear(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
         y = torch.empty(M, N, dtype=torch.bfloat16, device=x.device)
     _need(y, torch.bfloat16, (M, N), "y")
     lib = load()
-    if workspace is None:
-        workspace = _workspace(x.device, lib.w4a16_workspace_bytes(M, N, K, group_size))
-    wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = lib.w4a16_linear(_ptr(x), _ptr(packed), _ptr(scales), _ptr(zeros), _ptr(bias),
-                          _ptr(y), M, N, K, int(group_size), 1 if zeros is None else 0,
-                          _ptr(workspace), wsb, _stream(x, stream))
-    _check("w4a16_linear", rc)
+    _call_with_workspace(
+        lib.w4a16_linear, "w4a16_linear",
+        (_ptr(x), _ptr(packed), _ptr(scales), _ptr(zeros), _ptr(bias), _ptr(y), M, N, K,
+         int(group_size), 1 if zeros is None else 0),
+        (_stream(x, stream),), x.device, workspace,
+        lambda: lib.w4a16_workspace_bytes(M, N, K, group_size))
     return y
 
 
@@ -241,13 +265,12 @@ def w4a8_linear(qx: torch.Tensor, sx: torch.Tensor, packed: torch.Tensor,
     if acc_out is not None:
         _need(acc_out, torch.int32, (M, N), "acc_out")
     lib = load()
-    if workspace is None:
-        workspace = _workspace(qx.device, lib.w4a8_workspace_bytes(M, N, K, group_size))
-    wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = lib.w4a8_linear(_ptr(qx), _ptr(sx), _ptr(packed), _ptr(w_scales), _ptr(bias),
-                         _ptr(y), _ptr(acc_out), M, N, K, int(group_size), _ptr(workspace),
-                         wsb, _stream(qx, stream))
-    _check("w4a8_linear", rc)
+    _call_with_workspace(
+        lib.w4a8_linear, "w4a8_linear",
+        (_ptr(qx), _ptr(sx), _ptr(packed), _ptr(w_scales), _ptr(bias), _ptr(y), _ptr(acc_out),
+         M, N, K, int(group_size)),
+        (_stream(qx, stream),), qx.device, workspace,
+        lambda: lib.w4a8_workspace_bytes(M, N, K, group_size))
     return y, acc_out
 
 

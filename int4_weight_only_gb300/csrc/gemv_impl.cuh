@@ -46,6 +46,8 @@
 
 #include <algorithm>
 #include <cstdlib>
+#include <map>
+#include <mutex>
 
 namespace w4 {
 namespace {
@@ -850,6 +852,22 @@ k_w4a8_gemv_m16(const __grid_constant__ CUtensorMap tmW, const GemvArgs a) {
     w4a8_body<MT>(&tmW, a);
 }
 
+// Largest dynamic shared memory set so far per (kernel, device).
+inline bool raise_smem_limit(const void* kern, size_t bytes) {
+    static std::mutex mu;
+    static std::map<std::pair<const void*, int>, size_t> done;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    std::lock_guard<std::mutex> lk(mu);
+    size_t& cur = done[{kern, dev}];
+    if (bytes <= cur) return true;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
+        cudaSuccess)
+        return false;
+    cur = bytes;
+    return true;
+}
+
 template <typename Kern>
 int launch(Kern kern, const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
            cudaStream_t stream) {
@@ -858,9 +876,10 @@ int launch(Kern kern, const uint8_t* packed, const GemvArgs& a, const GemvPlan& 
                         (uint64_t)a.N, (uint64_t)(a.Kp / 2), 128, (uint32_t)p.R,
                         CU_TENSOR_MAP_SWIZZLE_128B))
         return W4_ERR_CUDA;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)p.smem) != cudaSuccess)
-        return W4_ERR_CUDA;
+    // the dynamic shared-memory limit of this kernel, raised only when a plan
+    // needs more than was set before for this kernel on this device (one
+    // driver call per kernel and size, not per launch)
+    if (!raise_smem_limit(reinterpret_cast<const void*>(kern), p.smem)) return W4_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.grid);
     cfg.blockDim = dim3(kGemvThreads);
