@@ -62,9 +62,50 @@ int* device_error_flag() {
     return static_cast<int*>(p);
 }
 
+// Recently encoded tensor maps, direct-mapped by a hash of every encoding
+// input: a decode call on the same weights reuses its map instead of another
+// driver call (a map depends on nothing but these inputs).
+namespace {
+struct TmapKey {
+    int dtype, swizzle;
+    const void* base;
+    uint64_t dim0, dim1, stride;
+    uint32_t box0, box1;
+    bool operator==(const TmapKey& o) const {
+        return dtype == o.dtype && swizzle == o.swizzle && base == o.base && dim0 == o.dim0 &&
+               dim1 == o.dim1 && stride == o.stride && box0 == o.box0 && box1 == o.box1;
+    }
+};
+struct TmapEntry {
+    bool used = false;
+    TmapKey key{};
+    CUtensorMap map;
+};
+constexpr int kTmapSlots = 256;
+TmapEntry g_tmaps[kTmapSlots];
+std::mutex g_tmap_mu;
+
+size_t tmap_hash(const TmapKey& k) {
+    uint64_t h = reinterpret_cast<uintptr_t>(k.base) * 0x9E3779B97F4A7C15ull;
+    for (uint64_t v : {(uint64_t)k.dtype, (uint64_t)k.swizzle, k.dim0, k.dim1, k.stride,
+                       (uint64_t)k.box0, (uint64_t)k.box1})
+        h = (h ^ v) * 0x100000001B3ull;
+    return (size_t)(h >> 17) % kTmapSlots;
+}
+}  // namespace
+
 bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
                     uint64_t dim0, uint64_t dim1, uint64_t row_stride_bytes,
                     uint32_t box0, uint32_t box1, CUtensorMapSwizzle swizzle) {
+    const TmapKey key{(int)dtype, (int)swizzle, base, dim0, dim1, row_stride_bytes, box0, box1};
+    const size_t slot = tmap_hash(key);
+    {
+        std::lock_guard<std::mutex> lk(g_tmap_mu);
+        if (g_tmaps[slot].used && g_tmaps[slot].key == key) {
+            *map = g_tmaps[slot].map;
+            return true;
+        }
+    }
     auto fn = get_encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {dim0, dim1};
@@ -72,9 +113,15 @@ bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* bas
     cuuint32_t box[2] = {box0, box1};
     cuuint32_t estr[2] = {1, 1};
     std::memset(map, 0, sizeof(*map));
-    return fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    if (fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    std::lock_guard<std::mutex> lk(g_tmap_mu);
+    g_tmaps[slot].used = true;
+    g_tmaps[slot].key = key;
+    g_tmaps[slot].map = *map;
+    return true;
 }
 
 namespace {

@@ -2,6 +2,8 @@
 // kernels and of the W4A8 kernels; the kernels are in gemv_impl.cuh.
 #include "gemv_impl.cuh"
 
+#include <array>
+
 namespace w4 {
 
 bool gemv_tma_activations() {
@@ -9,7 +11,40 @@ bool gemv_tma_activations() {
     return e && std::atoi(e) == 1;
 }
 
+namespace {
+bool plan_gemv_search(int M, int N, int Kp, int G, int act_bytes, int sm_count, GemvPlan* out);
+}
+
+// Plans are cached by their inputs and the tuning variables' values, so
+// repeated calls of one layer skip the search.
 bool plan_gemv(int M, int N, int Kp, int G, int act_bytes, int sm_count, GemvPlan* out) {
+    auto env = [](const char* n) {
+        const char* e = std::getenv(n);
+        return e ? std::atoi(e) : 0;
+    };
+    const std::array<int, 9> key = {M, N, Kp, G, act_bytes, sm_count, env("W4_GEMV_ROWS"),
+                                    env("W4_GEMV_SPLIT"), env("W4_GEMV_CPS")};
+    static std::mutex mu;
+    static std::map<std::array<int, 9>, std::pair<bool, GemvPlan>> cache;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) {
+            if (it->second.first) *out = it->second.second;
+            return it->second.first;
+        }
+    }
+    GemvPlan p;
+    const bool ok = plan_gemv_search(M, N, Kp, G, act_bytes, sm_count, &p);
+    std::lock_guard<std::mutex> lk(mu);
+    if (cache.size() > 4096) cache.clear();
+    cache[key] = {ok, p};
+    if (ok) *out = p;
+    return ok;
+}
+
+namespace {
+bool plan_gemv_search(int M, int N, int Kp, int G, int act_bytes, int sm_count, GemvPlan* out) {
     if (M < 1 || M > 16 || N < 1 || Kp < 1 || G < 32 || sm_count < 1) return false;
     const int gq = G / 32;
     const int cpg = (gq % 8 == 0) ? 8 : (gq % 4 == 0) ? 4 : (gq % 2 == 0) ? 2 : 1;
@@ -92,6 +127,7 @@ bool plan_gemv(int M, int N, int Kp, int G, int act_bytes, int sm_count, GemvPla
     }
     return found;
 }
+}  // namespace
 
 int launch_w4a16_gemv(const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
                       cudaStream_t st) {
