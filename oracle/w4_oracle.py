@@ -18,6 +18,8 @@ Sources (page title, section):
      independently, then interleave.
 [P1a] same page, section "融合INT4反量化与矩阵乘": the additive offset of an
      asymmetric group is (8 - z) s when codes are read as (q - 8).
+[P1f] same page, section "基础": the feed-forward block is
+     W_down [SiLU(W_gate x) (*) (W_up x)] with SiLU(v) = v sigma(v).
 [P2] "【infra之路】12-投机解码、量化与推理引擎对比", section 2.2: symmetric INT8,
      scale = max/127, per-value error <= scale/2.
 [P4] "Jetson Orin AGX INT4 推理优化实践：super 分支从 9 tok/s 到 24 tok/s",
@@ -37,6 +39,9 @@ Readings where the pages are silent (each is also listed in the design notes):
        [0, 15] and 0 is exactly representable.
  (vi)  an all-zero group stores s = 0 (and z = 0); its codes are 8 (sym) or
        0 (asym) and dequantize to exactly 0; no division by zero happens.
+ (ix)  fused gate|up weights: 16-row tiles of 8 gate rows then the same 8
+       up rows (gate row f at 16 (f // 8) + f % 8, up row f 8 rows below);
+       the bias of each projection is added before SiLU and the product.
  (viii) the W4A8 weight scale is max|row|/7 (the symmetric rule of [P1]),
        codes stored as q+8 like W4A16.
  Matmuls are done in fp64 on exactly dequantized weights (s * (code - z) is
@@ -188,6 +193,55 @@ def w4a16_linear(x, packed, scales, zeros, bias, K: int, group_size: int,
         b = np.asarray(bias, dtype=np.float64)
         y = y + (b if rows is None else b[np.asarray(rows)])[None, :]
     return y
+
+
+# ---------------------------------------------------------------------------
+# Fused gate|up projection with SiLU [P1f], reading (ix)
+# ---------------------------------------------------------------------------
+
+def swiglu_rows(F: int):
+    """(gate_rows, up_rows) of the fused [2F] weight matrix, reading (ix)."""
+    f = np.arange(F)
+    gate = 16 * (f // 8) + f % 8
+    return gate, gate + 8
+
+
+def pair_rows(gate, up):
+    """Stack two [F, ...] arrays into the fused [2F, ...] order of reading
+    (ix): out[gate_rows] = gate, out[up_rows] = up."""
+    gate = np.asarray(gate)
+    up = np.asarray(up)
+    F = gate.shape[0]
+    if up.shape != gate.shape or F % 8:
+        raise ValueError("gate and up need equal shapes and F % 8 == 0")
+    g_idx, u_idx = swiglu_rows(F)
+    out = np.empty((2 * F,) + gate.shape[1:], dtype=gate.dtype)
+    out[g_idx] = gate
+    out[u_idx] = up
+    return out
+
+
+def silu_f64(v):
+    """SiLU(v) = v sigma(v) in fp64 [P1f]; sigma is evaluated on the side
+    where exp does not overflow."""
+    v = np.asarray(v, dtype=np.float64)
+    e = np.exp(-np.abs(v))
+    sig = np.where(v >= 0, 1.0 / (1.0 + e), e / (1.0 + e))
+    return v * sig
+
+
+def w4a16_linear_swiglu(x, packed, scales, zeros, bias, F: int, K: int,
+                        group_size: int, cols=None):
+    """y[m, f] = SiLU(g[m, f]) * u[m, f] in fp64, where g and u are the
+    W4A16 linear outputs (bias included) of gate row f and up row f of the
+    fused matrix.  ``cols`` restricts the f computed."""
+    g_idx, u_idx = swiglu_rows(F)
+    if cols is not None:
+        cols = np.asarray(cols)
+        g_idx, u_idx = g_idx[cols], u_idx[cols]
+    g = w4a16_linear(x, packed, scales, zeros, bias, K, group_size, rows=g_idx)
+    u = w4a16_linear(x, packed, scales, zeros, bias, K, group_size, rows=u_idx)
+    return silu_f64(g) * u
 
 
 # ---------------------------------------------------------------------------

@@ -357,3 +357,80 @@ def test_activation_quantize_closed_form_and_padding():
     assert list(qx[0, :4]) == [127, -64, 32, 0]    # 63.5 -> 64 (half-even), 31.75 -> 32
     assert np.all(qx[:, 30:] == 0)
     assert sx[1] == 0 and np.all(qx[1] == 0)       # all-zero token
+
+
+# ---------------------------------------------------------------------------
+# Fused gate|up projection with SiLU ("Lab 5", section 基础)
+# ---------------------------------------------------------------------------
+
+def test_silu_closed_forms():
+    import math
+    v = np.array([0.0, math.log(3.0), -math.log(3.0), 1.0, -1.0, 40.0, -800.0, 800.0])
+    s = O.silu_f64(v)
+    assert s[0] == 0.0
+    # sigma(ln 3) = 3/4 and sigma(-ln 3) = 1/4
+    assert abs(s[1] - 0.75 * math.log(3.0)) < 1e-15
+    assert abs(s[2] + 0.25 * math.log(3.0)) < 1e-15
+    # SiLU(v) - SiLU(-v) = v sigma(v) + v sigma(-v) = v
+    assert abs((s[3] - s[4]) - 1.0) < 1e-15
+    assert abs(s[3] - 1.0 / (1.0 + math.exp(-1.0))) < 1e-15
+    # saturation: SiLU(v) -> v for large v, -> 0 for very negative v, no NaN
+    assert abs(s[5] - 40.0) < 1e-15 and s[7] == 800.0
+    assert s[6] == 0.0 and np.all(np.isfinite(s))
+
+
+def test_swiglu_row_pairing():
+    F = 24
+    g_idx, u_idx = O.swiglu_rows(F)
+    assert sorted(np.concatenate([g_idx, u_idx]).tolist()) == list(range(2 * F))
+    assert list(g_idx[:10]) == [0, 1, 2, 3, 4, 5, 6, 7, 16, 17]
+    assert list(u_idx[:10]) == [8, 9, 10, 11, 12, 13, 14, 15, 24, 25]
+    gate = np.arange(F) + 1000
+    up = np.arange(F) + 2000
+    fused = O.pair_rows(gate, up)
+    assert list(fused[:17]) == ([1000 + i for i in range(8)] + [2000 + i for i in range(8)]
+                                + [1008])
+    with pytest.raises(ValueError):
+        O.pair_rows(np.zeros(12), np.zeros(12))
+
+
+@pytest.mark.parametrize("symmetric", [True, False])
+def test_swiglu_brute_force_loops(symmetric):
+    """Pure-Python loops over bytes and nibbles of the separately packed gate
+    and up matrices: SiLU(sum x w_gate + b_gate) * (sum x w_up + b_up)."""
+    import math
+    F, K, G, M = 16, 40, 16, 2
+    rng = np.random.default_rng(11)
+    Wg = _rand_w(F, K, 1, std=0.5)
+    Wu = _rand_w(F, K, 2, std=0.5)
+    bg = rng.standard_normal(F).astype(np.float32)
+    bu = rng.standard_normal(F).astype(np.float32)
+    x = _bf16_round(rng.standard_normal((M, K)).astype(np.float32))
+    pg, sg, zg = O.pack_rtn(Wg, G, symmetric)
+    pu, su, zu = O.pack_rtn(Wu, G, symmetric)
+    # quantization is row-wise: packing the fused matrix equals fusing the packs
+    pf, sf, zf = O.pack_rtn(O.pair_rows(Wg, Wu), G, symmetric)
+    assert np.array_equal(pf, O.pair_rows(pg, pu))
+    assert np.array_equal(sf, O.pair_rows(sg, su))
+    if not symmetric:
+        assert np.array_equal(zf, O.pair_rows(zg, zu))
+    y = O.w4a16_linear_swiglu(x, pf, sf, zf, O.pair_rows(bg, bu), F, K, G)
+
+    def proj(p, s, z, b, m, f):
+        acc = 0.0
+        for k in range(K):
+            byte = int(p[f, k // 2])
+            code = (byte >> 4) if k % 2 else (byte & 15)
+            zero = 8 if z is None else int(z[f, k // G])
+            acc += float(x[m, k]) * float(s[f, k // G]) * (code - zero)
+        return acc + float(b[f])
+
+    for m in range(M):
+        for f in range(F):
+            g = proj(pg, sg, zg, bg, m, f)
+            u = proj(pu, su, zu, bu, m, f)
+            want = g / (1.0 + math.exp(-g)) * u
+            assert abs(y[m, f] - want) <= 1e-12 * (1.0 + abs(want))
+    cols = np.array([3, 9, 15])
+    assert np.array_equal(O.w4a16_linear_swiglu(x, pf, sf, zf, O.pair_rows(bg, bu), F, K, G,
+                                                cols=cols), y[:, cols])
