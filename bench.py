@@ -464,6 +464,38 @@ def measure_decode_12b(w4, hbm, reps=100):
     return out
 
 
+def measure_swiglu(w4, hbm, reps=200):
+    """Fused gate|up + SiLU (w4a16_linear_swiglu, F = 18944, K = 3584) next
+    to the plain gate|up linear on the same rotated weight copies: the fused
+    call writes M x F outputs instead of M x 2F and needs no separate SiLU
+    kernel."""
+    out = []
+    for M in (1, 8):
+        lin = [l for l in WL.decode_7b(M) if l.name.endswith("gate_up")][0]
+        F = lin.N // 2
+        ds = DecodeSet(w4, [lin], M, min_bytes=3 * L2_BYTES)
+        yF = torch.empty(M, F, dtype=torch.bfloat16, device="cuda")
+
+        def fused(i):
+            d = ds.copies[i % ds.R][0]
+            w4.w4a16_linear_swiglu(d["x"], d["p"], d["s"], d["z"], d["b"], F, lin.K,
+                                   lin.group_size, y=yF)
+        for i in range(3):
+            fused(i)
+            ds.call(0, i)
+        torch.cuda.synchronize()
+        n = reps * ds.R
+        t_lin = time_graph_steps(lambda i: ds.call(0, i), n, ds.R, 1) / n
+        t_fus = time_graph_steps(fused, n, ds.R, 1) / n
+        b = algorithmic_bytes(lin, M) - 2 * M * lin.N + 2 * M * F
+        out.append({"M": M, "F": F, "K": lin.K, "fused_us": round(t_fus * 1e6, 3),
+                    "gate_up_linear_us": round(t_lin * 1e6, 3),
+                    "GB/s": round(b / t_fus / 1e9, 1), "frac": round(b / t_fus / 1e9 / hbm, 4)})
+        del ds
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, world, rank):
     import int4_weight_only_gb300 as w4
     from int4_weight_only_gb300 import build as b
@@ -520,6 +552,7 @@ def run_ours(args, world, rank):
         res["prefill"] = [measure_prefill(w4, M, bf16, peak_kind) for M in (2048, 512)]
         res["w4a8"] = measure_w4a8(w4, hbm)
         res["decode_12b"] = measure_decode_12b(w4, hbm)
+        res["swiglu_7b"] = measure_swiglu(w4, hbm)
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline_decode(lins)
     return res

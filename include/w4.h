@@ -167,6 +167,27 @@ W4_API int w4a16_linear(const uint16_t* x, const uint8_t* packed, const float* s
                  void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * w4a16_linear_swiglu - the gate and up projections of a SwiGLU feed-forward
+ * layer in one pass, y = SiLU(x W_gate^T + b_gate) (*) (x W_up^T + b_up),
+ * SiLU(v) = v * sigmoid(v).  "Lab 5: Gemma4 端到端推理优化", section 基础
+ * (FFN(x) = W_down [SiLU(W_gate x) (*) (W_up x)]); fusing SwiGLU into the
+ * linear is the "kernel fusion" direction of "Jetson Orin AGX INT4
+ * 推理优化实践", section 后续还能继续优化什么.
+ *
+ *  The weights are the 2F x K matrix whose 16-row tiles hold 8 gate rows
+ *  followed by the same 8 up rows (gate row f is row 16 (f/8) + f%8, up row f
+ *  is 8 rows below it), quantized and packed by w4_pack_rtn like any other;
+ *  bias (optional) is ordered the same way, [2F] fp32.  F % 8 == 0.
+ *  x [M, K] bf16, y [M, F] bf16 out.  M <= 16 (the decode kernel; larger M
+ *  returns W4_ERR_UNSUPPORTED_SHAPE).  workspace: w4a16_workspace_bytes(M,
+ *  2F, K, group_size) bytes, as for w4a16_linear.
+ * ------------------------------------------------------------------------- */
+W4_API int w4a16_linear_swiglu(const uint16_t* x, const uint8_t* packed, const float* scales,
+                               const uint8_t* zeros, const float* bias, uint16_t* y, int M,
+                               int F, int K, int group_size, int symmetric, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * w4a8_quantize_act - per-token dynamic INT8 activations ([ORIN]):
  *  s_x[m] = fp32(max_k |x[m,k]| / 127),
  *  qx[m,k] = clip(round(fp32(x[m,k] / s_x[m])), -127, 127) for k < K, 0 for

@@ -21,6 +21,8 @@ _SIGS = {
                                       _c_int, _c_int, _vp]),
     "w4a16_linear": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
                               _c_int, _vp, _c_size, _vp]),
+    "w4a16_linear_swiglu": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
+                                     _c_int, _c_int, _vp, _c_size, _vp]),
     "w4a8_quantize_act": (_c_int, [_vp, _c_int, _c_int, _c_int, _vp, _vp, _vp]),
     "w4a8_workspace_bytes": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
     "w4a8_linear": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
@@ -190,6 +192,8 @@ def w4a16_linear(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
     if y is None:
         y = torch.empty(M, N, dtype=torch.bfloat16, device=x.device)
     _need(y, torch.bfloat16, (M, N), "y")
+    if M == 0:
+        return y                # no tokens: nothing to launch
     lib = load()
     _call_with_workspace(
         lib.w4a16_linear, "w4a16_linear",
@@ -197,6 +201,49 @@ def w4a16_linear(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
          int(group_size), 1 if zeros is None else 0),
         (_stream(x, stream),), x.device, workspace,
         lambda: lib.w4a16_workspace_bytes(M, N, K, group_size))
+    return y
+
+
+def pair_gate_up(gate: torch.Tensor, up: torch.Tensor) -> torch.Tensor:
+    """Rows of gate and up [F, ...] in the order w4a16_linear_swiglu reads:
+    16-row tiles of 8 gate rows followed by the same 8 up rows ([2F, ...]).
+    Works for weight matrices (before w4_pack_rtn) and bias vectors."""
+    F = gate.shape[0]
+    if up.shape != gate.shape or F % 8:
+        raise ValueError("gate and up must have the same shape with a multiple of 8 rows")
+    rest = tuple(gate.shape[1:])
+    return torch.stack([gate.reshape(F // 8, 8, *rest), up.reshape(F // 8, 8, *rest)],
+                       dim=1).reshape(2 * F, *rest).contiguous()
+
+
+def w4a16_linear_swiglu(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
+                        zeros: Optional[torch.Tensor], bias: Optional[torch.Tensor], F: int,
+                        K: int, group_size: int, y=None, workspace=None,
+                        stream=None) -> torch.Tensor:
+    """y [M, F] bf16 = SiLU(x W_gate^T + b_gate) * (x W_up^T + b_up); packed /
+    scales / zeros / bias hold the 2F paired rows (see pair_gate_up)."""
+    M = x.shape[0]
+    _need(x, torch.bfloat16, (M, K), "x")
+    Kp = padded_k(K, group_size)
+    Ng = Kp // group_size
+    _need(packed, torch.uint8, (2 * F, Kp // 2), "packed")
+    _need(scales, torch.float32, (2 * F, Ng), "scales")
+    if zeros is not None:
+        _need(zeros, torch.uint8, (2 * F, Ng), "zeros")
+    if bias is not None:
+        _need(bias, torch.float32, (2 * F,), "bias")
+    if y is None:
+        y = torch.empty(M, F, dtype=torch.bfloat16, device=x.device)
+    _need(y, torch.bfloat16, (M, F), "y")
+    if M == 0:
+        return y                # no tokens: nothing to launch
+    lib = load()
+    _call_with_workspace(
+        lib.w4a16_linear_swiglu, "w4a16_linear_swiglu",
+        (_ptr(x), _ptr(packed), _ptr(scales), _ptr(zeros), _ptr(bias), _ptr(y), M, F, K,
+         int(group_size), 1 if zeros is None else 0),
+        (_stream(x, stream),), x.device, workspace,
+        lambda: lib.w4a16_workspace_bytes(M, 2 * F, K, group_size))
     return y
 
 

@@ -228,6 +228,39 @@ int w4a16_linear(const uint16_t* x, const uint8_t* packed, const float* scales,
     return launch_w4a16_gemv(packed, a, p, st);
 }
 
+int w4a16_linear_swiglu(const uint16_t* x, const uint8_t* packed, const float* scales,
+                        const uint8_t* zeros, const float* bias, uint16_t* y, int M, int F,
+                        int K, int group_size, int symmetric, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+    if (!x || !packed || !scales || !y) return W4_ERR_NULL_PTR;
+    if (symmetric && zeros) return W4_ERR_INVALID_ARG;
+    if (!symmetric && !zeros) return W4_ERR_NULL_PTR;
+    if (M < 0 || F <= 0 || (F % 8) != 0 || F > 0x3fffffff) return W4_ERR_INVALID_ARG;
+    int rc = check_group(K, group_size);
+    if (rc) return rc;
+    const long long Kp = padded_k(K, group_size);
+    if (Kp > 0x7fffffffLL) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(x) || !aligned16(packed)) return W4_ERR_MISALIGNED;
+    if (!aligned4(scales) || (bias && !aligned4(bias)) || (reinterpret_cast<uintptr_t>(y) & 1))
+        return W4_ERR_MISALIGNED;
+    if (M > 16) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (M == 0) return W4_OK;
+    const int N = 2 * F;                        // gate/up row pairs
+    GemvPlan p;
+    if (!plan_gemv(M, N, (int)Kp, group_size, 2, current_sm_count(), &p)) return W4_ERR_UNSUPPORTED_SHAPE;
+    GemvArgs a{};
+    rc = split_workspace(p, workspace, workspace_bytes, &a.tickets, &a.partial);
+    if (rc) return rc;
+    a.x = x; a.scales = scales; a.zeros = zeros; a.bias = bias; a.y = y;
+    a.xtma = (K % 8) == 0 && gemv_tma_activations();
+    a.err = device_error_flag();
+    if (!a.err) return W4_ERR_CUDA;
+    a.M = M; a.N = N; a.K = K; a.Kp = (int)Kp; a.G = group_size; a.Ng = (int)(Kp / group_size);
+    a.R = p.R; a.SKE = p.SKE; a.nst = p.nst; a.S = p.S; a.spl = p.spl; a.units = p.units;
+    a.XS = p.XS; a.red = p.red;
+    return launch_w4a16_swiglu(packed, a, p, static_cast<cudaStream_t>(stream));
+}
+
 int w4a8_quantize_act(const uint16_t* x, int M, int K, int group_size, int8_t* qx,
                       float* sx, void* stream) {
     if (!x || !qx || !sx) return W4_ERR_NULL_PTR;

@@ -347,6 +347,13 @@ __device__ __forceinline__ Smem gemv_init(const CUtensorMap* tm, const GemvArgs&
     return sm;
 }
 
+// SiLU(gate) * up in fp32 (SiLU(v) = v * sigmoid(v)); __expf overflows to
+// inf for very negative v and the reciprocal of inf is 0, the limit.  The
+// correctly rounded reciprocal intrinsic keeps the epilogue branch-free.
+__device__ __forceinline__ float swiglu(float gate, float up) {
+    return gate * __frcp_rn(1.f + __expf(-gate)) * up;
+}
+
 // Sum of S split partials p[0], p[stride], ..., added in split order.  The
 // loads of up to eight splits are issued before any add, so the last CTA of a
 // row block waits for one round trip per eight splits, not one per split.
@@ -387,7 +394,9 @@ __device__ __forceinline__ bool split_k_arrive(const GemvArgs& a, SmemCtl* ctl, 
 // so that the split-K hand-off code does not take part in the register
 // allocation and scheduling of the unsplit kernels' main loop (measured: it
 // slowed that loop by ~4%).
-template <int NT, int CPG, bool ASYM, bool SPLIT>
+// SWIGLU: the rows are gate/up pairs (16-row tiles: 8 gate rows, then the
+// same 8 up rows) and y [M, N/2] = SiLU(gate) * up, SiLU(v) = v / (1 + e^-v).
+template <int NT, int CPG, bool ASYM, bool SPLIT, bool SWIGLU = false>
 __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
     constexpr int SEG = 8 / CPG;
     constexpr int LOG_CPG = CPG == 8 ? 3 : CPG == 4 ? 2 : CPG == 2 ? 1 : 0;
@@ -619,7 +628,20 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
         }
 
         // ---- epilogue: thread holds (token 8nt + 2tig + (j&1), row gid + 8(j>>1))
-        if constexpr (!SPLIT) {
+        if constexpr (SWIGLU && !SPLIT) {
+            if (kp == 0) {
+                const int F = N >> 1, f = (row0 >> 1) + gid;       // this lane's output column
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const int t = nt * 8 + 2 * tig + j;
+                        if (t < M && row0 + gid < N)
+                            y[(size_t)t * F + f] = f32_to_bf16_bits(
+                                swiglu(acc[nt][j] + b_lo, acc[nt][j + 2] + b_hi));
+                    }
+            }
+        } else if constexpr (!SPLIT) {
             if (kp == 0) {
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
@@ -645,6 +667,21 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
             }
             if (split_k_arrive(a, ctl, rb)) {
                 if (kp == 0) {
+                    if constexpr (SWIGLU) {
+                        const int F = N >> 1, f = (row0 >> 1) + gid;
+                        const int ng = row0 + gid, nu = ng + 8;   // gate and up rows
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                            for (int j = 0; j < 2; ++j) {
+                                const int t = nt * 8 + 2 * tig + j;
+                                if (t < M && ng < N) {
+                                    const float g = sum_splits(part + (size_t)t * N + ng, (size_t)M * N, Sp);
+                                    const float u = sum_splits(part + (size_t)t * N + nu, (size_t)M * N, Sp);
+                                    y[(size_t)t * F + f] = f32_to_bf16_bits(swiglu(g + b_lo, u + b_hi));
+                                }
+                            }
+                    } else {
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -656,6 +693,7 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
                                 y[(size_t)t * N + n] = f32_to_bf16_bits(v + ((j >> 1) ? b_hi : b_lo));
                             }
                         }
+                    }
                 }
                 if (tid == 0) a.tickets[rb] = 0;
             }
@@ -808,26 +846,26 @@ __device__ void w4a8_consumer(const Smem& sm, const GemvArgs& a) {
 
 // Kernel instances that the plan may place two to an SM (M <= 8 for W4A16,
 // M <= 4 for W4A8) are compiled for two resident CTAs of 288 threads.
-template <int NT, int CPG, bool ASYM, bool SPLIT>
+template <int NT, int CPG, bool ASYM, bool SPLIT, bool SWIGLU>
 __device__ __forceinline__ void w4a16_body(const CUtensorMap* tm, const GemvArgs& a) {
     const Smem sm = gemv_init(tm, a);
     if (threadIdx.x >= NCT) {
         if (threadIdx.x == NCT) gemv_producer(tm, sm.wbuf, sm.xbuf, sm.ctl, a);
     } else {
-        w4a16_consumer<NT, CPG, ASYM, SPLIT>(sm, a);
+        w4a16_consumer<NT, CPG, ASYM, SPLIT, SWIGLU>(sm, a);
     }
 }
 
-template <int CPG, bool ASYM, bool SPLIT>
+template <int CPG, bool ASYM, bool SPLIT, bool SWIGLU>
 __global__ void __launch_bounds__(kGemvThreads, 2)
 k_w4a16_gemv_m8(const __grid_constant__ CUtensorMap tmW, const GemvArgs a) {
-    w4a16_body<1, CPG, ASYM, SPLIT>(&tmW, a);
+    w4a16_body<1, CPG, ASYM, SPLIT, SWIGLU>(&tmW, a);
 }
 
-template <int CPG, bool ASYM, bool SPLIT>
+template <int CPG, bool ASYM, bool SPLIT, bool SWIGLU>
 __global__ void __launch_bounds__(kGemvThreads, 1)
 k_w4a16_gemv_m16(const __grid_constant__ CUtensorMap tmW, const GemvArgs a) {
-    w4a16_body<2, CPG, ASYM, SPLIT>(&tmW, a);
+    w4a16_body<2, CPG, ASYM, SPLIT, SWIGLU>(&tmW, a);
 }
 
 template <int MT>
@@ -894,37 +932,37 @@ int launch(Kern kern, const uint8_t* packed, const GemvArgs& a, const GemvPlan& 
     return cudaGetLastError() == cudaSuccess ? W4_OK : W4_ERR_CUDA;
 }
 
-template <int NT, bool ASYM, bool SPLIT>
+template <int NT, bool ASYM, bool SPLIT, bool SWIGLU>
 int launch_w4a16_cpg(int cpg, const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
                      cudaStream_t st) {
     if (NT == 1) {
         switch (cpg) {
-            case 8: return launch(k_w4a16_gemv_m8<8, ASYM, SPLIT>, packed, a, p, st);
-            case 4: return launch(k_w4a16_gemv_m8<4, ASYM, SPLIT>, packed, a, p, st);
-            case 2: return launch(k_w4a16_gemv_m8<2, ASYM, SPLIT>, packed, a, p, st);
-            default: return launch(k_w4a16_gemv_m8<1, ASYM, SPLIT>, packed, a, p, st);
+            case 8: return launch(k_w4a16_gemv_m8<8, ASYM, SPLIT, SWIGLU>, packed, a, p, st);
+            case 4: return launch(k_w4a16_gemv_m8<4, ASYM, SPLIT, SWIGLU>, packed, a, p, st);
+            case 2: return launch(k_w4a16_gemv_m8<2, ASYM, SPLIT, SWIGLU>, packed, a, p, st);
+            default: return launch(k_w4a16_gemv_m8<1, ASYM, SPLIT, SWIGLU>, packed, a, p, st);
         }
     }
     switch (cpg) {
-        case 8: return launch(k_w4a16_gemv_m16<8, ASYM, SPLIT>, packed, a, p, st);
-        case 4: return launch(k_w4a16_gemv_m16<4, ASYM, SPLIT>, packed, a, p, st);
-        case 2: return launch(k_w4a16_gemv_m16<2, ASYM, SPLIT>, packed, a, p, st);
-        default: return launch(k_w4a16_gemv_m16<1, ASYM, SPLIT>, packed, a, p, st);
+        case 8: return launch(k_w4a16_gemv_m16<8, ASYM, SPLIT, SWIGLU>, packed, a, p, st);
+        case 4: return launch(k_w4a16_gemv_m16<4, ASYM, SPLIT, SWIGLU>, packed, a, p, st);
+        case 2: return launch(k_w4a16_gemv_m16<2, ASYM, SPLIT, SWIGLU>, packed, a, p, st);
+        default: return launch(k_w4a16_gemv_m16<1, ASYM, SPLIT, SWIGLU>, packed, a, p, st);
     }
 }
 
 // W4A16 decode launch for one K-split case (all group sizes and widths).
-template <bool SPLIT>
+template <bool SPLIT, bool SWIGLU = false>
 int launch_w4a16_variant(const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
                          cudaStream_t st) {
     const int gq = a.G / 32;
     const int cpg = (gq % 8 == 0) ? 8 : (gq % 4 == 0) ? 4 : (gq % 2 == 0) ? 2 : 1;
     const bool asym = a.zeros != nullptr;
     if (a.M <= 8)
-        return asym ? launch_w4a16_cpg<1, true, SPLIT>(cpg, packed, a, p, st)
-                    : launch_w4a16_cpg<1, false, SPLIT>(cpg, packed, a, p, st);
-    return asym ? launch_w4a16_cpg<2, true, SPLIT>(cpg, packed, a, p, st)
-                : launch_w4a16_cpg<2, false, SPLIT>(cpg, packed, a, p, st);
+        return asym ? launch_w4a16_cpg<1, true, SPLIT, SWIGLU>(cpg, packed, a, p, st)
+                    : launch_w4a16_cpg<1, false, SPLIT, SWIGLU>(cpg, packed, a, p, st);
+    return asym ? launch_w4a16_cpg<2, true, SPLIT, SWIGLU>(cpg, packed, a, p, st)
+                : launch_w4a16_cpg<2, false, SPLIT, SWIGLU>(cpg, packed, a, p, st);
 }
 
 }  // namespace

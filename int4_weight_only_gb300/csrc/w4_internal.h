@@ -70,6 +70,9 @@ struct GemvArgs {
 // bulk TMA copy (W4_GEMV_XTMA=1) instead of reading it from global memory
 // while converting it (the default: measured 3.5% faster on the 7B step).
 bool gemv_tma_activations();
+// Decode with the SwiGLU epilogue: a.N = 2F paired gate/up rows, y [M, F].
+int launch_w4a16_swiglu(const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
+                        cudaStream_t stream);
 int launch_w4a16_gemv_split(const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
                             cudaStream_t stream);
 int launch_w4a16_gemv(const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
