@@ -15,6 +15,7 @@
 // Every division is an explicit IEEE round-to-nearest fp32 division and
 // rint() rounds half to even, so the codes are reproducible bit for bit by
 // any scalar fp32 evaluation of the same formulas.
+#include <algorithm>
 #include "w4_device.cuh"
 #include "w4_internal.h"
 
@@ -90,70 +91,139 @@ k_pack_rtn(const float* __restrict__ W, int N, int K, int G, int Ng, int symmetr
     }
 }
 
-// One CTA of 1024 threads per token: the max|x| pass and the quantize pass
-// both read x with 16-byte loads where the row allows it (the second pass
-// hits L1/L2).
-constexpr int kActThreads = 1024;
+// q = clip(rint(fp32(v / s)), -127, 127) as a byte (s > 0), bit-identical to
+// the IEEE quotient without dividing in the common case.  |v| <= 127.x s, and
+// t = v * rcp(s) (product and reciprocal each correctly rounded) differs from
+// v / s by at most three roundings, under 2^-22 |v/s| <= 2^-15, as does
+// fp32(v / s); so both round to the same integer unless t lies within 2^-14
+// of a half-integer.  Only then (or when t is not finite, for a subnormal s)
+// is the quotient computed.
+__device__ __forceinline__ uint32_t quant_s8(float v, float s, float rs) {
+    float t = v * rs;
+    if (!(fabsf(fabsf(t - truncf(t)) - 0.5f) > 0x1p-14f)) t = __fdiv_rn(v, s);
+    return (uint32_t)(uint8_t)(int8_t)(int)fminf(fmaxf(rintf(t), -127.f), 127.f);
+}
 
+// Eight columns (four bf16x2 words) to eight INT8 bytes; all zero when s = 0.
+__device__ __forceinline__ uint2 quant_s8x8(const uint4& v, float s, float rs) {
+    if (s == 0.f) return make_uint2(0u, 0u);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t b[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        b[2 * j] = quant_s8(__uint_as_float(w[j] << 16), s, rs);
+        b[2 * j + 1] = quant_s8(__uint_as_float(w[j] & 0xFFFF0000u), s, rs);
+    }
+    return make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24),
+                      b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
+}
+
+// Grid (C, M): C CTAs of 512 threads per token.  Every CTA reduces max|x|
+// over the whole row (so no CTA waits for another) and quantizes only its
+// share, the 8-column words [c W, (c + 1) W) with W = ceil(Kp / 8 / C); CTA 0
+// stores s_x.  RV > 0: the row has at most RV * 4096 columns and each thread
+// keeps its RV 16-byte words in registers between the two steps (one read of
+// x); RV = 0 (longer rows, C = 1): two passes, the second hitting L1/L2.
+// Launched with programmatic dependent launch: it waits for the kernel before
+// it (which may have written x, or may still be reading qx and sx) before
+// touching memory, and at once lets the next kernel start its prologue (a
+// linear layer prefetches its weights meanwhile and waits for this kernel
+// before reading qx).
+constexpr int kActThreads = 512;
+
+template <int RV>
 __global__ void __launch_bounds__(kActThreads)
 k_act_quant(const uint16_t* __restrict__ x, int K, int Kp, int8_t* __restrict__ qx,
             float* __restrict__ sx) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __shared__ float red[kActThreads / 32];
-    const int m = blockIdx.x, tid = threadIdx.x;
+    const int m = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
     const uint16_t* row = x + (size_t)m * K;
     int8_t* out = qx + (size_t)m * Kp;
     const bool vec = (K & 7) == 0 && (reinterpret_cast<uintptr_t>(row) & 15) == 0;
+    // otherwise 8-byte loads of four columns where K % 4 == 0 allows them
+    const bool vec4 = !vec && (K & 3) == 0 && (reinterpret_cast<uintptr_t>(row) & 7) == 0;
+    const int nw = Kp >> 3;                                   // 8-column words of the output row
+    const int wpc = (nw + gridDim.x - 1) / gridDim.x;
+    const int w0 = c * wpc, w1 = min(w0 + wpc, nw);           // this CTA's share
+    constexpr int NR = RV > 0 ? RV : 1;
+    uint4 keep[NR];
     float mx = 0.f;
-    if (vec) {
-        for (int k = tid * 8; k < K; k += kActThreads * 8) {
-            const uint4 v = __ldg(reinterpret_cast<const uint4*>(row + k));
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    auto max8 = [&](const uint4& v) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w[j] << 16)),
-                                     fabsf(__uint_as_float(w[j] & 0xFFFF0000u))));
+        for (int j = 0; j < 4; ++j)
+            mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w[j] << 16)),
+                                 fabsf(__uint_as_float(w[j] & 0xFFFF0000u))));
+    };
+    if (vec && RV > 0) {
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+            const int k = (r * kActThreads + tid) * 8;
+            keep[r] = k < K ? __ldg(reinterpret_cast<const uint4*>(row + k)) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int r = 0; r < NR; ++r) max8(keep[r]);
+    } else if (vec) {
+        for (int k = tid * 8; k < K; k += kActThreads * 8)
+            max8(__ldg(reinterpret_cast<const uint4*>(row + k)));
+    } else if (vec4) {
+#pragma unroll 4
+        for (int k = tid * 4; k < K; k += kActThreads * 4) {
+            const uint2 v = __ldg(reinterpret_cast<const uint2*>(row + k));
+            mx = fmaxf(mx, fmaxf(fmaxf(fabsf(__uint_as_float(v.x << 16)), fabsf(__uint_as_float(v.x & 0xFFFF0000u))),
+                                 fmaxf(fabsf(__uint_as_float(v.y << 16)), fabsf(__uint_as_float(v.y & 0xFFFF0000u)))));
         }
     } else {
+#pragma unroll 4
         for (int k = tid; k < K; k += kActThreads) mx = fmaxf(mx, fabsf(bf16_bits_to_f32(__ldg(row + k))));
     }
     mx = warp_max(mx);
     if ((tid & 31) == 0) red[tid >> 5] = mx;
     __syncthreads();
     if (tid < 32) {
-        float v = red[tid];
+        float v = tid < kActThreads / 32 ? red[tid] : 0.f;
         v = warp_max(v);
         if (tid == 0) red[0] = v;
     }
     __syncthreads();
     const float s = __fdiv_rn(red[0], 127.0f);
-    if (tid == 0) sx[m] = s;
-    auto q8 = [&](float v) -> uint32_t {
-        if (s == 0.f) return 0u;
-        return (uint32_t)(uint8_t)(int8_t)(int)fminf(fmaxf(rintf(__fdiv_rn(v, s)), -127.f), 127.f);
-    };
+    const float rs = s != 0.f ? __frcp_rn(s) : 0.f;
+    if (tid == 0 && c == 0) sx[m] = s;
     if (vec) {
-        // 8 columns per step; columns K..Kp-1 (a multiple of 8 past K) are zero
-        for (int k = tid * 8; k < Kp; k += kActThreads * 8) {
-            uint2 o = make_uint2(0u, 0u);
-            if (k < K) {
-                const uint4 v = __ldg(reinterpret_cast<const uint4*>(row + k));
-                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-                uint32_t b[8];
+        // word w covers columns 8w .. 8w+7; words at or past K are zero
+        int w = tid;
+        if (RV > 0) {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    b[2 * j] = q8(__uint_as_float(w[j] << 16));
-                    b[2 * j + 1] = q8(__uint_as_float(w[j] & 0xFFFF0000u));
-                }
-                o.x = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
-                o.y = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
+            for (int r = 0; r < NR; ++r, w += kActThreads)
+                if (w >= w0 && w < w1) *reinterpret_cast<uint2*>(out + 8 * w) = quant_s8x8(keep[r], s, rs);
+        }
+        for (; w < w1; w += kActThreads) {
+            if (w < w0) continue;
+            uint2 o = make_uint2(0u, 0u);
+            if (8 * w < K) o = quant_s8x8(__ldg(reinterpret_cast<const uint4*>(row + 8 * w)), s, rs);
+            *reinterpret_cast<uint2*>(out + 8 * w) = o;
+        }
+    } else if (vec4) {
+        // four columns per step; columns K..Kp-1 are zero
+        for (int k = 8 * w0 + tid * 4; k < 8 * w1; k += kActThreads * 4) {
+            uint32_t o = 0u;
+            if (k < K && s != 0.f) {
+                const uint2 v = __ldg(reinterpret_cast<const uint2*>(row + k));
+                o = quant_s8(__uint_as_float(v.x << 16), s, rs) |
+                    (quant_s8(__uint_as_float(v.x & 0xFFFF0000u), s, rs) << 8) |
+                    (quant_s8(__uint_as_float(v.y << 16), s, rs) << 16) |
+                    (quant_s8(__uint_as_float(v.y & 0xFFFF0000u), s, rs) << 24);
             }
-            *reinterpret_cast<uint2*>(out + k) = o;
+            *reinterpret_cast<uint32_t*>(out + k) = o;
         }
     } else {
-        for (int k = tid; k < Kp; k += kActThreads) {
-            int q = 0;
-            if (k < K) q = (int)(int8_t)(uint8_t)q8(bf16_bits_to_f32(__ldg(row + k)));
-            out[k] = (int8_t)q;
+#pragma unroll 4
+        for (int k = 8 * w0 + tid; k < 8 * w1; k += kActThreads) {
+            uint32_t q = 0u;
+            if (k < K && s != 0.f) q = quant_s8(bf16_bits_to_f32(__ldg(row + k)), s, rs);
+            out[k] = (int8_t)(uint8_t)q;
         }
     }
 }
@@ -180,7 +250,26 @@ int launch_pack_rtn(const float* W, int N, int K, int G, int symmetric, uint8_t*
 
 int launch_act_quant(const uint16_t* x, int M, int K, int Kp, int8_t* qx, float* sx,
                      cudaStream_t stream) {
-    k_act_quant<<<M, kActThreads, 0, stream>>>(x, K, Kp, qx, sx);
+    // 16-byte words per thread to hold the row; each CTA quantizes up to
+    // 4096 columns
+    const int v = (K + kActThreads * 8 - 1) / (kActThreads * 8);
+    const int C = v <= 8 ? std::min((Kp + 4095) / 4096, 16) : 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(C, M);
+    cfg.blockDim = dim3(kActThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e;
+    if (v <= 1) e = cudaLaunchKernelEx(&cfg, k_act_quant<1>, x, K, Kp, qx, sx);
+    else if (v <= 2) e = cudaLaunchKernelEx(&cfg, k_act_quant<2>, x, K, Kp, qx, sx);
+    else if (v <= 4) e = cudaLaunchKernelEx(&cfg, k_act_quant<4>, x, K, Kp, qx, sx);
+    else if (v <= 8) e = cudaLaunchKernelEx(&cfg, k_act_quant<8>, x, K, Kp, qx, sx);
+    else e = cudaLaunchKernelEx(&cfg, k_act_quant<0>, x, K, Kp, qx, sx);
+    if (e != cudaSuccess) return W4_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? W4_OK : W4_ERR_CUDA;
 }
 

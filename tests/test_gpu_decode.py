@@ -129,7 +129,9 @@ def test_no_device_error_left(w4):
 
 # ---------------------------------------------------------------- W4A8
 @pytest.mark.parametrize("M,K,G,frac", [(1, 3584, 3584, 0.005), (1, 3580, 3584, 0.005),
-                                        (16, 1000, 1024, 0.0), (3, 18944, 18944, 0.005)])
+                                        (16, 1000, 1024, 0.0), (3, 18944, 18944, 0.005),
+                                        (2, 40000, 40000, 0.005), (3, 8000, 8448, 0.0),
+                                        (4, 100, 128, 0.0), (2, 1001, 1024, 0.01)])
 def test_act_quant_bit_exact(w4, M, K, G, frac):
     x = WL.make_activations(K, M, seed=M + K, outlier_frac=frac)
     x[0, :3] = 0                      # keep a few exact zeros in play
@@ -137,6 +139,44 @@ def test_act_quant_bit_exact(w4, M, K, G, frac):
     oq, osx = O.w4a8_quantize_act(x, O.padded_k(K, G))
     assert np.array_equal(to_np(sx).view(np.uint32), osx.view(np.uint32))
     assert np.array_equal(to_np(qx), oq)
+
+
+@pytest.mark.parametrize("vmax", [1.0, 3.140625, 100.0, 0.0078125, 1e-38])
+def test_act_quant_every_bf16_value(w4, vmax):
+    """Every bf16 value v with |v| <= vmax, both signs, in rows of 16384
+    columns that each also hold vmax (so s_x = fp32(vmax / 127) in every
+    row): q_x bit-exact against the oracle's IEEE division, including the
+    values whose quotient lies next to a half-integer."""
+    top = int(np.array([vmax], np.float32).view(np.uint32)[0] >> 16)
+    bits = np.arange(0, top + 1, dtype=np.uint32)
+    vals = np.concatenate([bits, bits | 0x8000]).astype(np.uint32) << 16
+    vals = vals.view(np.float32)
+    K = 16384
+    per = K - 1
+    rows = -(-len(vals) // per)
+    x = np.zeros((rows, K), np.float32)
+    x[:, 0] = vmax
+    flat = np.zeros(rows * per, np.float32)
+    flat[:len(vals)] = vals
+    x[:, 1:] = flat.reshape(rows, per)
+    xt = torch.from_numpy(x).to(torch.bfloat16)
+    qx, sx = w4.w4a8_quantize_act(xt.cuda(), K)
+    oq, osx = O.w4a8_quantize_act(xt, K)
+    assert np.array_equal(to_np(sx).view(np.uint32), osx.view(np.uint32))
+    assert np.array_equal(to_np(qx), oq)
+
+
+def test_act_quant_ties(w4):
+    """s_x = 1 exactly: x = k + 1/2 are ties of the INT8 grid (half to even)."""
+    x = torch.zeros(2, 256)
+    x[0, 0] = 127.0
+    x[0, 1:9] = torch.tensor([0.5, 1.5, 2.5, -0.5, -1.5, -2.5, 126.5, -126.5])
+    x[1] = torch.linspace(-3, 3, 256)
+    x = x.to(torch.bfloat16)
+    qx, sx = w4.w4a8_quantize_act(x.cuda(), 256)
+    oq, osx = O.w4a8_quantize_act(x, 256)
+    assert list(oq[0, 1:9]) == [0, 2, 2, 0, -2, -2, 126, -126]
+    assert np.array_equal(to_np(qx), oq) and np.array_equal(to_np(sx), osx)
 
 
 def test_act_quant_zero_token(w4):
