@@ -6,9 +6,11 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 from .w4_oracle import (padded_k, rtn_quantize, pack_nibbles, unpack_nibbles,
                         pack_rtn, dequantize_f64, bf16_to_f64, w4a16_linear,
                         swiglu_rows, pair_rows, silu_f64, w4a16_linear_swiglu,
+                        w4a16_grouped_linear,
                         w4a8_quantize_act, w4a8_linear, int32_worst_case)
 
 __all__ = ["padded_k", "rtn_quantize", "pack_nibbles", "unpack_nibbles",
            "pack_rtn", "dequantize_f64", "bf16_to_f64", "w4a16_linear",
            "swiglu_rows", "pair_rows", "silu_f64", "w4a16_linear_swiglu",
+           "w4a16_grouped_linear",
            "w4a8_quantize_act", "w4a8_linear", "int32_worst_case"]

@@ -20,6 +20,11 @@ Sources (page title, section):
      asymmetric group is (8 - z) s when codes are read as (q - 8).
 [P1f] same page, section "基础": the feed-forward block is
      W_down [SiLU(W_gate x) (*) (W_up x)] with SiLU(v) = v sigma(v).
+[P3] "Yeniden paketlenmiş QAT Gemma 4 26B-A4B, tek bir TPU v6e'de FP8
+     işlemenin 1.9 katı verimle sunuluyor", sections "26B'deki boşluk" and
+     "vLLM'in TPU backend'inde değişen ne oldu": expert layers
+     (128 experts, 8 active per token) whose int4 weights with 32-wide
+     groups are multiplied by their tokens in a grouped matmul.
 [P2] "【infra之路】12-投机解码、量化与推理引擎对比", section 2.2: symmetric INT8,
      scale = max/127, per-value error <= scale/2.
 [P4] "Jetson Orin AGX INT4 推理优化实践：super 分支从 9 tok/s 到 24 tok/s",
@@ -42,6 +47,9 @@ Readings where the pages are silent (each is also listed in the design notes):
  (ix)  fused gate|up weights: 16-row tiles of 8 gate rows then the same 8
        up rows (gate row f at 16 (f // 8) + f % 8, up row f 8 rows below);
        the bias of each projection is added before SiLU and the product.
+ (x)   grouped linear: tokens arrive sorted by group with offsets
+       goff[0] = 0 <= ... <= goff[E] = T; group e's weights are rows
+       e N .. e N + N - 1 of the stacked matrix, its bias the same rows.
  (viii) the W4A8 weight scale is max|row|/7 (the symmetric rule of [P1]),
        codes stored as q+8 like W4A16.
  Matmuls are done in fp64 on exactly dequantized weights (s * (code - z) is
@@ -242,6 +250,36 @@ def w4a16_linear_swiglu(x, packed, scales, zeros, bias, F: int, K: int,
     g = w4a16_linear(x, packed, scales, zeros, bias, K, group_size, rows=g_idx)
     u = w4a16_linear(x, packed, scales, zeros, bias, K, group_size, rows=u_idx)
     return silu_f64(g) * u
+
+
+# ---------------------------------------------------------------------------
+# Grouped linear (experts) [P3], reading (x)
+# ---------------------------------------------------------------------------
+
+def w4a16_grouped_linear(x, goff, packed, scales, zeros, bias, E: int, N: int, K: int,
+                         group_size: int, cols=None):
+    """y[t, n] = sum_k x[t, k] W_hat_e[n, k] + b_e[n] for the group e with
+    goff[e] <= t < goff[e+1], in fp64: each group's rows through
+    w4a16_linear with that group's slice of the stacked weights.  ``cols``
+    restricts the output columns n computed."""
+    goff = np.asarray(goff, dtype=np.int64)
+    T = np.asarray(x).shape[0] if not hasattr(x, "shape") else x.shape[0]
+    if goff.shape != (E + 1,) or goff[0] != 0 or goff[-1] != T or np.any(np.diff(goff) < 0):
+        raise ValueError("group offsets must rise from 0 to T")
+    packed = np.asarray(packed).reshape(E, N, -1)
+    scales = np.asarray(scales, dtype=F32).reshape(E, N, -1)
+    zeros = None if zeros is None else np.asarray(zeros).reshape(E, N, -1)
+    bias = None if bias is None else np.asarray(bias, dtype=np.float64).reshape(E, N)
+    ncol = N if cols is None else len(cols)
+    y = np.zeros((T, ncol))
+    for e in range(E):
+        t0, t1 = int(goff[e]), int(goff[e + 1])
+        if t1 == t0:
+            continue
+        y[t0:t1] = w4a16_linear(x[t0:t1], packed[e], scales[e],
+                                None if zeros is None else zeros[e],
+                                None if bias is None else bias[e], K, group_size, rows=cols)
+    return y
 
 
 # ---------------------------------------------------------------------------

@@ -434,3 +434,57 @@ def test_swiglu_brute_force_loops(symmetric):
     cols = np.array([3, 9, 15])
     assert np.array_equal(O.w4a16_linear_swiglu(x, pf, sf, zf, O.pair_rows(bg, bu), F, K, G,
                                                 cols=cols), y[:, cols])
+
+
+# ---------------------------------------------------------------------------
+# Grouped linear over experts ("Yeniden paketlenmiş QAT Gemma 4 26B-A4B, tek
+# bir TPU v6e'de ...", expert layers)
+# ---------------------------------------------------------------------------
+
+def _grouped_case(E, N, K, G, counts, symmetric, seed):
+    rng = np.random.default_rng(seed)
+    W = _rand_w(E * N, K, seed, std=0.1)
+    packed, scales, zeros = O.pack_rtn(W, G, symmetric)
+    T = int(sum(counts))
+    x = _bf16_round(rng.standard_normal((T, K)).astype(np.float32))
+    bias = rng.standard_normal(E * N).astype(np.float32)
+    goff = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    return x, goff, packed, scales, zeros, bias
+
+
+@pytest.mark.parametrize("symmetric", [True, False])
+def test_grouped_equals_dense_product_over_all_experts(symmetric):
+    """Independent formulation: one fp64 product of every token with every
+    expert's dequantized matrix, [T, E*N], from which each row keeps the
+    block of its own expert (found by searching the offsets)."""
+    E, N, K, G = 6, 16, 96, 32
+    counts = [3, 0, 1, 5, 0, 2]
+    x, goff, packed, scales, zeros, bias = _grouped_case(E, N, K, G, counts, symmetric, 4)
+    y = O.w4a16_grouped_linear(x, goff, packed, scales, zeros, bias, E, N, K, G)
+    Wd = O.dequantize_f64(packed, scales, zeros, G)[:, :K]
+    full = x.astype(np.float64) @ Wd.T + bias.astype(np.float64)[None, :]
+    for t in range(x.shape[0]):
+        e = int(np.searchsorted(goff, t, side="right") - 1)
+        assert np.allclose(y[t], full[t, e * N:(e + 1) * N], rtol=0, atol=1e-12)
+    cols = np.array([0, 5, 15])
+    yc = O.w4a16_grouped_linear(x, goff, packed, scales, zeros, bias, E, N, K, G, cols=cols)
+    assert np.array_equal(yc, y[:, cols])
+
+
+def test_grouped_token_order_and_offsets():
+    """Permuting tokens inside a group permutes its rows of y; a group's
+    result depends only on its own tokens; bad offsets are rejected."""
+    E, N, K, G = 3, 8, 64, 32
+    counts = [4, 0, 3]
+    x, goff, packed, scales, zeros, bias = _grouped_case(E, N, K, G, counts, True, 9)
+    y = O.w4a16_grouped_linear(x, goff, packed, scales, None, bias, E, N, K, G)
+    perm = np.array([2, 0, 3, 1, 4, 5, 6])
+    yp = O.w4a16_grouped_linear(x[perm], goff, packed, scales, None, bias, E, N, K, G)
+    assert np.array_equal(yp, y[perm])
+    x2 = x.copy()
+    x2[4:] *= -3.0                       # change group 2's tokens only
+    y2 = O.w4a16_grouped_linear(_bf16_round(x2), goff, packed, scales, None, bias, E, N, K, G)
+    assert np.array_equal(y2[:4], y[:4]) and not np.allclose(y2[4:], y[4:])
+    for bad in ([0, 5, 4, 7], [1, 4, 4, 7], [0, 4, 4, 8]):
+        with pytest.raises(ValueError):
+            O.w4a16_grouped_linear(x, np.array(bad), packed, scales, None, bias, E, N, K, G)
