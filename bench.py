@@ -496,6 +496,86 @@ def measure_swiglu(w4, hbm, reps=200):
     return out
 
 
+def measure_moe(w4, hbm, reps=100):
+    """Expert layer at decode (128 experts, 8 per token, G = 32 symmetric):
+    the grouped call per projection over rotated copies of the stacked
+    expert weights, GB/s over the bytes of the experts that have tokens.
+    For context, the same gate|up work as one w4a16_linear call per active
+    expert (the host knows the counts here; a serving loop would not)."""
+    out = []
+    E = WL.MOE_EXPERTS
+    for batch in (16, 4):
+        counts = WL.moe_route_counts(batch, seed=batch)
+        T, gmax = sum(counts), max(counts)
+        act = [e for e in range(E) if counts[e]]
+        goff = torch.zeros(E + 1, dtype=torch.int32, device="cuda")
+        goff[1:] = torch.cumsum(torch.tensor(counts, dtype=torch.int32, device="cuda"), 0,
+                                dtype=torch.int32)
+        lins = WL.moe_decode(batch)
+        per_copy = sum(E * l.N * l.K * 0.6 for l in lins)
+        R = max(2, math.ceil(3 * L2_BYTES / per_copy))
+        copies = []
+        for r in range(R):
+            cp = []
+            for lin in lins:
+                # random codes and scales drawn on the device (timing only)
+                Kp = -(-lin.K // lin.group_size) * lin.group_size
+                g = torch.Generator(device="cuda")
+                g.manual_seed(lin.seed + r)
+                p = torch.randint(0, 256, (E * lin.N, Kp // 2), generator=g, device="cuda",
+                                  dtype=torch.int32).to(torch.uint8)
+                s = torch.rand(E * lin.N, Kp // lin.group_size, generator=g,
+                               device="cuda") * 0.01 + 1e-4
+                x = WL.make_activations(lin.K, T, seed=30_000 + 7 * r + lin.seed)
+                cp.append(dict(p=p, s=s, x=x.cuda(),
+                               y=torch.empty(T, lin.N, dtype=torch.bfloat16, device="cuda")))
+            copies.append(cp)
+        torch.cuda.synchronize()
+
+        def call(li, i):
+            lin, d = lins[li], copies[i % R][li]
+            w4.w4a16_grouped_linear(d["x"], goff, d["p"], d["s"], None, None, E, lin.N, lin.K,
+                                    lin.group_size, gmax, y=d["y"])
+        for i in range(3):
+            call(0, i)
+            call(1, i)
+        torch.cuda.synchronize()
+        res = {"batch": batch, "tokens_routed": T, "active_experts": len(act), "max_per_expert": gmax}
+        tot_b = tot_t = 0.0
+        for li, lin in enumerate(lins):
+            n = reps * R
+            sec = time_graph_steps(lambda i, li=li: call(li, i), n, R, 1) / n
+            Kp = -(-lin.K // lin.group_size) * lin.group_size
+            b = len(act) * (lin.N * Kp // 2 + 4 * lin.N * (Kp // lin.group_size)) \
+                + 2 * T * lin.K + 2 * T * lin.N
+            tot_b += b
+            tot_t += sec
+            res[lin.name.split("_b")[0] + "_us"] = round(sec * 1e6, 3)
+            res[lin.name.split("_b")[0] + "_GB/s"] = round(b / sec / 1e9, 1)
+        res["GB/s"] = round(tot_b / tot_t / 1e9, 1)
+        res["frac"] = round(tot_b / tot_t / 1e9 / hbm, 4)
+        # context: one w4a16_linear per active expert (gate|up)
+        lin = lins[0]
+        rows = {e: (int(sum(counts[:e])), counts[e]) for e in act}
+
+        def per_expert(i):
+            d = copies[i % R][0]
+            for e in act:
+                t0, c = rows[e]
+                w4.w4a16_linear(d["x"][t0:t0 + c], d["p"][e * lin.N:(e + 1) * lin.N],
+                                d["s"][e * lin.N:(e + 1) * lin.N], None, None, lin.N, lin.K,
+                                lin.group_size, y=d["y"][t0:t0 + c])
+        per_expert(0)
+        torch.cuda.synchronize()
+        n = 5 * R
+        res["gate_up_one_call_per_expert_us"] = round(
+            time_graph_steps(per_expert, n, R, 1) / n * 1e6, 2)
+        out.append(res)
+        del copies
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, world, rank):
     import int4_weight_only_gb300 as w4
     from int4_weight_only_gb300 import build as b
@@ -553,6 +633,7 @@ def run_ours(args, world, rank):
         res["w4a8"] = measure_w4a8(w4, hbm)
         res["decode_12b"] = measure_decode_12b(w4, hbm)
         res["swiglu_7b"] = measure_swiglu(w4, hbm)
+        res["moe_decode"] = measure_moe(w4, hbm)
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline_decode(lins)
     return res

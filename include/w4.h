@@ -73,6 +73,10 @@ extern "C" {
 #define W4_ERR_DEVICE_TIMEOUT      -9  /* a kernel's bounded wait ran out     */
 #define W4_ERR_SCRATCH_LIMIT      -10  /* shape needs more split-K scratch than
                                           W4_NOALLOC_SCRATCH_BYTES            */
+#define W4_ERR_GROUP_TOKENS       -11  /* device flag: a group's offsets were
+                                          invalid or it had more tokens than
+                                          max_group_tokens; its rows of y were
+                                          not written                         */
 
 /* Size of the library's built-in split-K scratch used by
  * w4a16_linear_noalloc (4 MiB, held by every GPU that loads the library).  */
@@ -186,6 +190,41 @@ W4_API int w4a16_linear_swiglu(const uint16_t* x, const uint8_t* packed, const f
                                const uint8_t* zeros, const float* bias, uint16_t* y, int M,
                                int F, int K, int group_size, int symmetric, void* workspace,
                                size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * w4a16_grouped_linear - grouped W4A16 linear over E groups (mixture-of-
+ * experts layers), decode sizes: tokens sorted by group, each group's tokens
+ * multiplied by that group's own quantized matrix in one launch:
+ *  y[t, n] = sum_k x[t, k] * W_hat_e[n, k] (+ bias[e, n])
+ *  for goff[e] <= t < goff[e+1].
+ * The grouped matmul of "Yeniden paketlenmiş QAT Gemma 4 26B-A4B, tek bir
+ * TPU v6e'de FP8 işlemenin 1.9 katı verimle sunuluyor" (expert layers: 128
+ * experts, 8 active per token, int4 with 32-wide groups, each weight chunk
+ * dequantized on chip before the multiply), sections "26B'deki boşluk" and
+ * "vLLM'in TPU backend'inde değişen ne oldu"; the per-group formula is
+ * w4a16_linear's.
+ *
+ *  x         [T, K] bf16, rows sorted by group, 16-byte aligned.
+ *  goff      [E+1] int32 on the device, non-decreasing, goff[0] = 0,
+ *            goff[E] = T (group e's tokens are rows goff[e] .. goff[e+1]-1).
+ *            Read on the device after the previous kernel on the stream has
+ *            finished, so a router kernel may write it just before.
+ *  packed    [E, N, Kp/2] uint8 (w4_pack_rtn of the stacked [E*N, K] weights);
+ *  scales    [E, N, Ng] fp32;  zeros [E, N, Ng] uint8 or NULL (symmetric);
+ *  bias      [E, N] fp32 or NULL.
+ *  y         [T, N] bf16 out.
+ *  max_group_tokens  bound on goff[e+1] - goff[e], 1..16.  A group above it,
+ *            or offsets outside [0, T] or decreasing, is skipped (its rows of y
+ *            are left as they were) and sets W4_ERR_GROUP_TOKENS in the
+ *            device flag that w4_get_device_error returns.
+ *  Groups without tokens cost nothing: the units of work are (group with
+ *  tokens, row block), listed on the device.  E <= 32767, E * N < 2^31.
+ *  No workspace (grouped plans do not split K).
+ * ------------------------------------------------------------------------- */
+W4_API int w4a16_grouped_linear(const uint16_t* x, const int32_t* goff, const uint8_t* packed,
+                                const float* scales, const uint8_t* zeros, const float* bias,
+                                uint16_t* y, int T, int E, int N, int K, int group_size,
+                                int symmetric, int max_group_tokens, void* stream);
 
 /* ---------------------------------------------------------------------------
  * w4a8_quantize_act - per-token dynamic INT8 activations ([ORIN]):

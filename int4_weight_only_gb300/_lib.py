@@ -23,6 +23,8 @@ _SIGS = {
                               _c_int, _vp, _c_size, _vp]),
     "w4a16_linear_swiglu": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
                                      _c_int, _c_int, _vp, _c_size, _vp]),
+    "w4a16_grouped_linear": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
+                                      _c_int, _c_int, _c_int, _c_int, _vp]),
     "w4a8_quantize_act": (_c_int, [_vp, _c_int, _c_int, _c_int, _vp, _vp, _vp]),
     "w4a8_workspace_bytes": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
     "w4a8_linear": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
@@ -244,6 +246,42 @@ def w4a16_linear_swiglu(x: torch.Tensor, packed: torch.Tensor, scales: torch.Ten
          int(group_size), 1 if zeros is None else 0),
         (_stream(x, stream),), x.device, workspace,
         lambda: lib.w4a16_workspace_bytes(M, 2 * F, K, group_size))
+    return y
+
+
+def w4a16_grouped_linear(x: torch.Tensor, goff: torch.Tensor, packed: torch.Tensor,
+                         scales: torch.Tensor, zeros: Optional[torch.Tensor],
+                         bias: Optional[torch.Tensor], E: int, N: int, K: int, group_size: int,
+                         max_group_tokens: int, y=None, stream=None) -> torch.Tensor:
+    """Grouped W4A16 linear: rows goff[e] .. goff[e+1]-1 of x [T, K] (sorted
+    by group) times group e's matrix -> the same rows of y [T, N].  packed /
+    scales / zeros / bias hold the E groups stacked ([E*N, ...] or [E, N, ...]);
+    goff is an int32 CUDA tensor [E+1]."""
+    T = x.shape[0]
+    _need(x, torch.bfloat16, (T, K), "x")
+    Kp = padded_k(K, group_size)
+    Ng = Kp // group_size
+    _need(goff, torch.int32, (E + 1,), "goff")
+    packed = packed.reshape(E * N, -1)
+    scales = scales.reshape(E * N, -1)
+    _need(packed, torch.uint8, (E * N, Kp // 2), "packed")
+    _need(scales, torch.float32, (E * N, Ng), "scales")
+    if zeros is not None:
+        zeros = zeros.reshape(E * N, -1)
+        _need(zeros, torch.uint8, (E * N, Ng), "zeros")
+    if bias is not None:
+        bias = bias.reshape(E * N)
+        _need(bias, torch.float32, (E * N,), "bias")
+    if y is None:
+        y = torch.empty(T, N, dtype=torch.bfloat16, device=x.device)
+    _need(y, torch.bfloat16, (T, N), "y")
+    if T == 0:
+        return y
+    lib = load()
+    _check("w4a16_grouped_linear", lib.w4a16_grouped_linear(
+        _ptr(x), _ptr(goff), _ptr(packed), _ptr(scales), _ptr(zeros), _ptr(bias), _ptr(y),
+        T, E, N, K, int(group_size), 1 if zeros is None else 0, int(max_group_tokens),
+        _stream(x, stream)))
     return y
 
 

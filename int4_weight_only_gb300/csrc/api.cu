@@ -3,6 +3,7 @@
 // the device error flag.  No entry point allocates or frees device memory.
 #include "w4_internal.h"
 
+#include <algorithm>
 #include <cstring>
 #include <cudaTypedefs.h>
 #include <mutex>
@@ -261,6 +262,43 @@ int w4a16_linear_swiglu(const uint16_t* x, const uint8_t* packed, const float* s
     return launch_w4a16_swiglu(packed, a, p, static_cast<cudaStream_t>(stream));
 }
 
+int w4a16_grouped_linear(const uint16_t* x, const int32_t* goff, const uint8_t* packed,
+                         const float* scales, const uint8_t* zeros, const float* bias,
+                         uint16_t* y, int T, int E, int N, int K, int group_size, int symmetric,
+                         int max_group_tokens, void* stream) {
+    if (!x || !goff || !packed || !scales || !y) return W4_ERR_NULL_PTR;
+    if (symmetric && zeros) return W4_ERR_INVALID_ARG;
+    if (!symmetric && !zeros) return W4_ERR_NULL_PTR;
+    if (T < 0 || E <= 0 || E > 32767 || N <= 0 || max_group_tokens < 1 || max_group_tokens > 16)
+        return W4_ERR_INVALID_ARG;
+    if ((long long)E * N > 0x7fffffffLL) return W4_ERR_UNSUPPORTED_SHAPE;
+    int rc = check_group(K, group_size);
+    if (rc) return rc;
+    const long long Kp = padded_k(K, group_size);
+    if (Kp > 0x7fffffffLL) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(x) || !aligned16(packed)) return W4_ERR_MISALIGNED;
+    if (!aligned4(goff) || !aligned4(scales) || (bias && !aligned4(bias)) ||
+        (reinterpret_cast<uintptr_t>(y) & 1))
+        return W4_ERR_MISALIGNED;
+    if (T == 0) return W4_OK;
+    // plan for the rows of the groups that can have tokens (at most T of them)
+    const int active = std::min(E, T);
+    const long long n_eff = std::min((long long)active * N, 0x7fffffffLL);
+    GemvPlan p;
+    if (!plan_gemv(max_group_tokens, (int)n_eff, (int)Kp, group_size, 2, current_sm_count(), &p, E))
+        return W4_ERR_UNSUPPORTED_SHAPE;
+    GemvArgs a{};
+    a.x = x; a.scales = scales; a.zeros = zeros; a.bias = bias; a.y = y;
+    a.err = device_error_flag();
+    if (!a.err) return W4_ERR_CUDA;
+    a.M = T; a.N = N; a.K = K; a.Kp = (int)Kp; a.G = group_size; a.Ng = (int)(Kp / group_size);
+    a.R = p.R; a.SKE = p.SKE; a.nst = p.nst; a.S = 1; a.spl = p.spl; a.units = p.units;
+    a.XS = p.XS; a.red = p.red;
+    a.goff = goff; a.E = E; a.gmax = max_group_tokens; a.NBg = (N + p.R - 1) / p.R;
+    a.list_off = (int)p.list_off;
+    return launch_w4a16_grouped(packed, a, p, static_cast<cudaStream_t>(stream));
+}
+
 int w4a8_quantize_act(const uint16_t* x, int M, int K, int group_size, int8_t* qx,
                       float* sx, void* stream) {
     if (!x || !qx || !sx) return W4_ERR_NULL_PTR;
@@ -342,6 +380,8 @@ const char* w4_error_string(int code) {
         case W4_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait timed out";
         case W4_ERR_SCRATCH_LIMIT:
             return "shape needs more split-K scratch than W4_NOALLOC_SCRATCH_BYTES";
+        case W4_ERR_GROUP_TOKENS:
+            return "a group's offsets were invalid or it had more tokens than max_group_tokens";
         default: return "unknown error code";
     }
 }

@@ -12,20 +12,22 @@ bool gemv_tma_activations() {
 }
 
 namespace {
-bool plan_gemv_search(int M, int N, int Kp, int G, int act_bytes, int sm_count, GemvPlan* out);
+bool plan_gemv_search(int M, int N, int Kp, int G, int act_bytes, int sm_count, GemvPlan* out,
+                      int groups);
 }
 
 // Plans are cached by their inputs and the tuning variables' values, so
 // repeated calls of one layer skip the search.
-bool plan_gemv(int M, int N, int Kp, int G, int act_bytes, int sm_count, GemvPlan* out) {
+bool plan_gemv(int M, int N, int Kp, int G, int act_bytes, int sm_count, GemvPlan* out,
+               int groups) {
     auto env = [](const char* n) {
         const char* e = std::getenv(n);
         return e ? std::atoi(e) : 0;
     };
-    const std::array<int, 9> key = {M, N, Kp, G, act_bytes, sm_count, env("W4_GEMV_ROWS"),
-                                    env("W4_GEMV_SPLIT"), env("W4_GEMV_CPS")};
+    const std::array<int, 10> key = {M, N, Kp, G, act_bytes, sm_count, env("W4_GEMV_ROWS"),
+                                     env("W4_GEMV_SPLIT"), env("W4_GEMV_CPS"), groups};
     static std::mutex mu;
-    static std::map<std::array<int, 9>, std::pair<bool, GemvPlan>> cache;
+    static std::map<std::array<int, 10>, std::pair<bool, GemvPlan>> cache;
     {
         std::lock_guard<std::mutex> lk(mu);
         auto it = cache.find(key);
@@ -35,7 +37,7 @@ bool plan_gemv(int M, int N, int Kp, int G, int act_bytes, int sm_count, GemvPla
         }
     }
     GemvPlan p;
-    const bool ok = plan_gemv_search(M, N, Kp, G, act_bytes, sm_count, &p);
+    const bool ok = plan_gemv_search(M, N, Kp, G, act_bytes, sm_count, &p, groups);
     std::lock_guard<std::mutex> lk(mu);
     if (cache.size() > 4096) cache.clear();
     cache[key] = {ok, p};
@@ -44,7 +46,8 @@ bool plan_gemv(int M, int N, int Kp, int G, int act_bytes, int sm_count, GemvPla
 }
 
 namespace {
-bool plan_gemv_search(int M, int N, int Kp, int G, int act_bytes, int sm_count, GemvPlan* out) {
+bool plan_gemv_search(int M, int N, int Kp, int G, int act_bytes, int sm_count, GemvPlan* out,
+                      int groups) {
     if (M < 1 || M > 16 || N < 1 || Kp < 1 || G < 32 || sm_count < 1) return false;
     const int gq = G / 32;
     const int cpg = (gq % 8 == 0) ? 8 : (gq % 4 == 0) ? 4 : (gq % 2 == 0) ? 2 : 1;
@@ -53,7 +56,9 @@ bool plan_gemv_search(int M, int N, int Kp, int G, int act_bytes, int sm_count, 
     const int red = act_bytes == 2
         ? CW * 32 * ((M > 8 ? 2 : 1) * 4) * 4
         : CW * 32 * (M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16) * 2 * 4;
-    const size_t fixed = 1024 + (size_t)NS * STAGE_BYTES + kCtlBytes + red;
+    // grouped plans keep a list of active group ids (int16) after the activations
+    const size_t list_bytes = groups > 0 ? (((size_t)groups * 2 + 15) & ~(size_t)15) : 0;
+    const size_t fixed = 1024 + (size_t)NS * STAGE_BYTES + kCtlBytes + red + list_bytes;
     // W4A16 also keeps four floats per token and segment of cpg*32 columns
     auto xseg_bytes = [&](int slice) -> size_t {
         return act_bytes == 2 ? (size_t)M * (slice / (cpg * 32)) * 16 : 0;
@@ -93,7 +98,8 @@ bool plan_gemv_search(int M, int N, int Kp, int G, int act_bytes, int sm_count, 
                 const int spl = (nst + S - 1) / S;
                 const int Se = (nst + spl - 1) / spl;
                 if (spl > spl_max) continue;
-                if ((forced_s && Se != forced_s) || (Se > 1 && NB > kMaxCounters)) {
+                if ((forced_s && Se != forced_s) || (Se > 1 && NB > kMaxCounters) ||
+                    (groups > 0 && Se > 1)) {
                     if (Se == nst) break;
                     continue;
                 }
@@ -117,6 +123,7 @@ bool plan_gemv_search(int M, int N, int Kp, int G, int act_bytes, int sm_count, 
                     p.units = units; p.grid = grid; p.cps = cps; p.red = red;
                     p.XS = spl * SKE * act_bytes + pad;
                     p.smem = fixed + (size_t)M * p.XS + xseg_bytes(spl * SKE);
+                    p.list_off = p.smem - list_bytes - 1024;
                     p.ws_bytes = 0;
                     if (Se > 1) p.ws_bytes = kCounterBytes + (size_t)Se * M * N * 4;
                     *out = p;

@@ -65,6 +65,8 @@ struct SmemCtl {
     int sumq[16];          // W4A8: sum of q_x over the slice, per token
     uint64_t xfull;        // activation slice landed (TMA staging)
     uint64_t xempty;       // consumers released the activation buffer
+    uint64_t listready;    // grouped: the active-group list is written
+    int nact;              // grouped: number of active groups
 };
 constexpr int kCtlBytes = 256;
 static_assert(sizeof(SmemCtl) <= kCtlBytes, "control block");
@@ -105,18 +107,21 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int c
 }
 
 // Producer: one thread streams every stage of every unit of this CTA.
+// GROUPED: units are (active group, row block) in the order of the list the
+// consumers build after the dependency wait; rows of group e start at e * N.
+template <bool GROUPED = false>
 __device__ void gemv_producer(const CUtensorMap* tm, uint8_t* wbuf, uint8_t* xbuf,
                               SmemCtl* ctl, const GemvArgs& a) {
     const int boxes = 128 / a.R;
     const int box_bytes = a.R * 128;
     const int kbytes = a.Kp / 2;
     const uint64_t pol = policy_evict_first();
-    auto issue = [&](int slot, int ks, int rb) {
+    auto issue = [&](int slot, int ks, int row) {
         const int kb0 = ks * (a.SKE / 2);
         const int nbox = min(boxes, (kbytes - kb0 + 127) / 128);   // boxes inside Kp
         mbar_arrive_expect_tx(&ctl->full[slot], nbox * box_bytes);
         for (int b = 0; b < nbox; ++b)
-            tma_load_2d(wbuf + slot * STAGE_BYTES + b * box_bytes, tm, kb0 + b * 128, rb * a.R,
+            tma_load_2d(wbuf + slot * STAGE_BYTES + b * box_bytes, tm, kb0 + b * 128, row,
                         &ctl->full[slot], pol);
     };
     // The weights are not written by the kernel before this one on the
@@ -124,7 +129,7 @@ __device__ void gemv_producer(const CUtensorMap* tm, uint8_t* wbuf, uint8_t* xbu
     // stages are prefetched into L2.  (Loading them into shared memory here
     // instead was measured slower: those copies compete with the activation
     // copy that follows the wait for the SM's bandwidth.)
-    if ((int)blockIdx.x < a.units) {
+    if (!GROUPED && (int)blockIdx.x < a.units) {
         int rb, s, ks0, ks1;
         unit_coords(blockIdx.x, a, rb, s, ks0, ks1);
         for (int ks = ks0; ks < min(ks1, ks0 + NS); ++ks)
@@ -134,12 +139,36 @@ __device__ void gemv_producer(const CUtensorMap* tm, uint8_t* wbuf, uint8_t* xbu
             }
     }
     grid_dep_wait();
+    int units = a.units;
+    const int16_t* glist = nullptr;
+    if constexpr (GROUPED) {
+        // which groups have tokens is known only after the wait
+        if (!mbar_wait(&ctl->listready, 0, &ctl->abort, a.err)) return;   // nothing issued yet
+        units = ctl->nact * a.NBg;
+        glist = reinterpret_cast<const int16_t*>(wbuf + a.list_off);
+    }
+    // GROUPED: each CTA takes a contiguous run of units, so that successive
+    // units mostly share a group and its staged activations
+    int u_beg = blockIdx.x, u_end = units, u_step = gridDim.x;
+    if constexpr (GROUPED) {
+        u_beg = (int)(((long long)units * blockIdx.x) / gridDim.x);
+        u_end = (int)(((long long)units * (blockIdx.x + 1)) / gridDim.x);
+        u_step = 1;
+    }
     uint32_t it = 0, xi = 0;
     int pv0 = -1, pv1 = -1;
     bool ok = true;
-    for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
-        int rb, s, ks0, ks1;
-        unit_coords(u, a, rb, s, ks0, ks1);
+    for (int u = u_beg; u < u_end && ok; u += u_step) {
+        int rb, s, ks0, ks1, row;
+        if constexpr (GROUPED) {
+            const int gi = u / a.NBg;
+            rb = u - gi * a.NBg;
+            s = 0; ks0 = 0; ks1 = a.nst;
+            row = (int)glist[gi] * a.N + rb * a.R;
+        } else {
+            unit_coords(u, a, rb, s, ks0, ks1);
+            row = rb * a.R;
+        }
         if (a.xtma && (ks0 != pv0 || ks1 != pv1)) {
             // the activation slice goes out before this unit's weights
             if (xi > 0 && !mbar_wait(&ctl->xempty, (xi - 1) & 1, &ctl->abort, a.err)) {
@@ -166,7 +195,7 @@ __device__ void gemv_producer(const CUtensorMap* tm, uint8_t* wbuf, uint8_t* xbu
                 ok = false;
                 break;
             }
-            issue(slot, ks, rb);
+            issue(slot, ks, row);
         }
     }
     if (!ok || ctl->abort) {
@@ -320,6 +349,7 @@ struct Smem {
     float* xseg;      // W4A16: per-segment sums of x, after M * XS bytes of xbuf
 };
 
+template <bool GROUPED = false>
 __device__ __forceinline__ Smem gemv_init(const CUtensorMap* tm, const GemvArgs& a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = align1024(smem_raw);
@@ -328,7 +358,9 @@ __device__ __forceinline__ Smem gemv_init(const CUtensorMap* tm, const GemvArgs&
     sm.ctl = reinterpret_cast<SmemCtl*>(base + NS * STAGE_BYTES);
     sm.red = reinterpret_cast<float*>(base + NS * STAGE_BYTES + kCtlBytes);
     sm.xbuf = base + NS * STAGE_BYTES + kCtlBytes + a.red;
-    sm.xseg = reinterpret_cast<float*>(sm.xbuf + (size_t)a.M * a.XS);
+    // the activation buffer holds M rows, or the per-group bound when grouped
+    // (a.M is then the total row count of all groups)
+    sm.xseg = reinterpret_cast<float*>(sm.xbuf + (size_t)(GROUPED ? a.gmax : a.M) * a.XS);
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; ++i) {
             mbar_init(&sm.ctl->full[i], 1);
@@ -336,6 +368,7 @@ __device__ __forceinline__ Smem gemv_init(const CUtensorMap* tm, const GemvArgs&
         }
         mbar_init(&sm.ctl->xfull, 1);
         mbar_init(&sm.ctl->xempty, 1);
+        if constexpr (GROUPED) mbar_init(&sm.ctl->listready, 1);
         sm.ctl->abort = 0;
         sm.ctl->last = 0;
         for (int i = 0; i < 16; ++i) sm.ctl->sumq[i] = 0;
@@ -396,15 +429,25 @@ __device__ __forceinline__ bool split_k_arrive(const GemvArgs& a, SmemCtl* ctl, 
 // slowed that loop by ~4%).
 // SWIGLU: the rows are gate/up pairs (16-row tiles: 8 gate rows, then the
 // same 8 up rows) and y [M, N/2] = SiLU(gate) * up, SiLU(v) = v / (1 + e^-v).
-template <int NT, int CPG, bool ASYM, bool SPLIT, bool SWIGLU = false>
+// GROUPED: a grouped linear over E groups (experts): group e multiplies its
+// own tokens, rows goff[e] .. goff[e+1] - 1 of x, by its own N x K matrix
+// (rows e * N .. e * N + N - 1 of the stacked weights) into the same rows
+// of y.  After the dependency wait every CTA lists the groups that have
+// tokens (in group order) and takes a contiguous run of the (active group,
+// row block) units; a group whose offsets are invalid or whose token count
+// exceeds gmax is left out and raises W4_ERR_GROUP_TOKENS.
+template <int NT, int CPG, bool ASYM, bool SPLIT, bool SWIGLU = false, bool GROUPED = false>
 __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
+    static_assert(!(GROUPED && (SPLIT || SWIGLU)), "grouped plans are unsplit, plain epilogue");
     constexpr int SEG = 8 / CPG;
     constexpr int LOG_CPG = CPG == 8 ? 3 : CPG == 4 ? 2 : CPG == 2 ? 1 : 0;
     constexpr bool PF = SEG <= 2;           // scales one stage ahead when they are few
     // kernel arguments in registers (asm statements with memory clobbers
     // would otherwise force re-reads from parameter space)
-    const int M = a.M, N = a.N, K = a.K, Kp = a.Kp, Ng = a.Ng, SKE = a.SKE, XS = a.XS;
-    const int units = a.units, Sp = a.S, spl = a.spl, nst = a.nst, R = a.R;
+    const int N = a.N, K = a.K, Kp = a.Kp, Ng = a.Ng, SKE = a.SKE, XS = a.XS;
+    const int Sp = a.S, spl = a.spl, nst = a.nst, R = a.R;
+    int M = GROUPED ? a.gmax : a.M;            // GROUPED: set per group
+    int units = a.units;                       // GROUPED: from the list
     const float* __restrict__ scales = a.scales;
     const uint8_t* __restrict__ zeros = a.zeros;
     const float* __restrict__ bias = a.bias;
@@ -424,12 +467,15 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
     for (int cp = 0; cp < 4; ++cp) l_cp[cp] = l_off + ((uint32_t)((2 * cp + (lj >> 1)) ^ li) << 4);
     uint32_t xrow[NT];
     int xt[NT][2];
+    auto token_rows = [&]() {
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        xrow[nt] = xbuf_u + (uint32_t)(min(nt * 8 + gid, M - 1) * XS + tig * 16 + kp * 512);
-        xt[nt][0] = 4 * min(nt * 8 + 2 * tig, M - 1);
-        xt[nt][1] = 4 * min(nt * 8 + 2 * tig + 1, M - 1);
-    }
+        for (int nt = 0; nt < NT; ++nt) {
+            xrow[nt] = xbuf_u + (uint32_t)(min(nt * 8 + gid, M - 1) * XS + tig * 16 + kp * 512);
+            xt[nt][0] = 4 * min(nt * 8 + 2 * tig, M - 1);
+            xt[nt][1] = 4 * min(nt * 8 + 2 * tig + 1, M - 1);
+        }
+    };
+    token_rows();
     // group of a segment: segments of CPG*32 columns tile the groups exactly,
     // so g = segment / (G / (CPG*32)), a shift when that ratio is a power of 2
     const int gdiv = a.G / (CPG * 32);
@@ -444,19 +490,84 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
     uint32_t it = 0, xi = 0;
     int prev0 = -1, prev1 = -1;
     bool waited = false;
-    for (int u = blockIdx.x; u < units; u += gridDim.x) {
-        const int rb = u / Sp, s = u - rb * Sp;
-        const int ks0 = s * spl, ks1 = min(ks0 + spl, nst);
+    const int16_t* glist = nullptr;
+    int prev_g = -1;
+    if constexpr (GROUPED) {
+        // groups with tokens, in group order (the same list in every CTA)
+        grid_dep_wait();
+        waited = true;
+        int16_t* list = reinterpret_cast<int16_t*>(sm.wbuf + a.list_off);
+        int* wcnt = reinterpret_cast<int*>(sm.red);
+        int nact = 0;
+        for (int e0 = 0; e0 < a.E; e0 += NCT) {
+            const int e = e0 + tid;
+            bool act = false;
+            if (e < a.E) {
+                const int o0 = __ldg(a.goff + e), o1 = __ldg(a.goff + e + 1);
+                const bool valid = o0 >= 0 && o1 >= o0 && o1 <= a.M;
+                if (!valid || o1 - o0 > a.gmax) atomicCAS(a.err, 0, W4_ERR_GROUP_TOKENS);
+                act = valid && o1 > o0 && o1 - o0 <= a.gmax;
+            }
+            const unsigned bal = __ballot_sync(0xffffffffu, act);
+            if (lane == 0) wcnt[warp] = __popc(bal);
+            named_bar_sync(1, NCT);
+            int before = nact, tot = 0;
+            for (int w = 0; w < CW; ++w) {
+                const int c = wcnt[w];
+                if (w < warp) before += c;
+                tot += c;
+            }
+            if (act) list[before + __popc(bal & ((1u << lane) - 1u))] = (int16_t)e;
+            nact += tot;
+            named_bar_sync(1, NCT);
+        }
+        if (tid == 0) {
+            ctl->nact = nact;
+            mbar_arrive(&ctl->listready);
+        }
+        units = nact * a.NBg;
+        glist = list;
+    }
+    int u_beg = blockIdx.x, u_end = units, u_step = gridDim.x;
+    if constexpr (GROUPED) {                   // the producer's contiguous runs
+        u_beg = (int)(((long long)units * blockIdx.x) / gridDim.x);
+        u_end = (int)(((long long)units * (blockIdx.x + 1)) / gridDim.x);
+        u_step = 1;
+    }
+    for (int u = u_beg; u < u_end; u += u_step) {
+        int rb, s, ks0, ks1, g = 0;
+        if constexpr (GROUPED) {
+            const int gi = u / a.NBg;
+            rb = u - gi * a.NBg;
+            g = glist[gi];
+            s = 0; ks0 = 0; ks1 = nst;
+            if (g != prev_g) {
+                // this group's tokens: rows o0 .. o0 + M - 1 of x and y
+                const int o0 = __ldg(a.goff + g);
+                M = __ldg(a.goff + g + 1) - o0;
+                x = static_cast<const uint16_t*>(a.x) + (size_t)o0 * K;
+                y = a.y + (size_t)o0 * N;
+                token_rows();
+                prev0 = -1;                        // stage this group's activations
+                prev_g = g;
+            }
+        } else {
+            rb = u / Sp;
+            s = u - rb * Sp;
+            ks0 = s * spl;
+            ks1 = min(ks0 + spl, nst);
+        }
+        const size_t wrow = GROUPED ? (size_t)g * N : 0;   // first row of this unit's matrix
         const int row0 = rb * R + rt * 16;
         const int nr = min(row0 + gid, N - 1), nr8 = min(row0 + gid + 8, N - 1);
-        const float* sc_r = scales + (size_t)nr * Ng;
-        const float* sc_r8 = scales + (size_t)nr8 * Ng;
-        const uint8_t* zp_r = ASYM ? zeros + (size_t)nr * Ng : nullptr;
-        const uint8_t* zp_r8 = ASYM ? zeros + (size_t)nr8 * Ng : nullptr;
+        const float* sc_r = scales + (wrow + nr) * Ng;
+        const float* sc_r8 = scales + (wrow + nr8) * Ng;
+        const uint8_t* zp_r = ASYM ? zeros + (wrow + nr) * Ng : nullptr;
+        const uint8_t* zp_r8 = ASYM ? zeros + (wrow + nr8) * Ng : nullptr;
         // bias of this thread's two rows and the scales of the first stage:
         // constant inputs, read before waiting for the previous kernel
-        const float b_lo = bias ? __ldg(bias + nr) : 0.f;
-        const float b_hi = bias ? __ldg(bias + nr8) : 0.f;
+        const float b_lo = bias ? __ldg(bias + wrow + nr) : 0.f;
+        const float b_hi = bias ? __ldg(bias + wrow + nr8) : 0.f;
         float sr[SEG], sr8[SEG], zr[SEG], zr8[SEG];
         auto load_scales = [&](int kw, float* r_, float* r8_, float* z_, float* z8_) {
             if constexpr (SEG == 8) {
@@ -846,26 +957,26 @@ __device__ void w4a8_consumer(const Smem& sm, const GemvArgs& a) {
 
 // Kernel instances that the plan may place two to an SM (M <= 8 for W4A16,
 // M <= 4 for W4A8) are compiled for two resident CTAs of 288 threads.
-template <int NT, int CPG, bool ASYM, bool SPLIT, bool SWIGLU>
+template <int NT, int CPG, bool ASYM, bool SPLIT, bool SWIGLU, bool GROUPED>
 __device__ __forceinline__ void w4a16_body(const CUtensorMap* tm, const GemvArgs& a) {
-    const Smem sm = gemv_init(tm, a);
+    const Smem sm = gemv_init<GROUPED>(tm, a);
     if (threadIdx.x >= NCT) {
-        if (threadIdx.x == NCT) gemv_producer(tm, sm.wbuf, sm.xbuf, sm.ctl, a);
+        if (threadIdx.x == NCT) gemv_producer<GROUPED>(tm, sm.wbuf, sm.xbuf, sm.ctl, a);
     } else {
-        w4a16_consumer<NT, CPG, ASYM, SPLIT, SWIGLU>(sm, a);
+        w4a16_consumer<NT, CPG, ASYM, SPLIT, SWIGLU, GROUPED>(sm, a);
     }
 }
 
-template <int CPG, bool ASYM, bool SPLIT, bool SWIGLU>
+template <int CPG, bool ASYM, bool SPLIT, bool SWIGLU, bool GROUPED = false>
 __global__ void __launch_bounds__(kGemvThreads, 2)
 k_w4a16_gemv_m8(const __grid_constant__ CUtensorMap tmW, const GemvArgs a) {
-    w4a16_body<1, CPG, ASYM, SPLIT, SWIGLU>(&tmW, a);
+    w4a16_body<1, CPG, ASYM, SPLIT, SWIGLU, GROUPED>(&tmW, a);
 }
 
-template <int CPG, bool ASYM, bool SPLIT, bool SWIGLU>
+template <int CPG, bool ASYM, bool SPLIT, bool SWIGLU, bool GROUPED = false>
 __global__ void __launch_bounds__(kGemvThreads, 1)
 k_w4a16_gemv_m16(const __grid_constant__ CUtensorMap tmW, const GemvArgs a) {
-    w4a16_body<2, CPG, ASYM, SPLIT, SWIGLU>(&tmW, a);
+    w4a16_body<2, CPG, ASYM, SPLIT, SWIGLU, GROUPED>(&tmW, a);
 }
 
 template <int MT>
@@ -910,8 +1021,10 @@ template <typename Kern>
 int launch(Kern kern, const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
            cudaStream_t stream) {
     CUtensorMap tm;
+    // grouped launches stack the E groups' rows
+    const uint64_t rows = (uint64_t)a.N * (uint64_t)(a.E > 0 ? a.E : 1);
     if (!encode_tmap_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, packed, (uint64_t)(a.Kp / 2),
-                        (uint64_t)a.N, (uint64_t)(a.Kp / 2), 128, (uint32_t)p.R,
+                        rows, (uint64_t)(a.Kp / 2), 128, (uint32_t)p.R,
                         CU_TENSOR_MAP_SWIZZLE_128B))
         return W4_ERR_CUDA;
     // the dynamic shared-memory limit of this kernel, raised only when a plan
@@ -932,37 +1045,38 @@ int launch(Kern kern, const uint8_t* packed, const GemvArgs& a, const GemvPlan& 
     return cudaGetLastError() == cudaSuccess ? W4_OK : W4_ERR_CUDA;
 }
 
-template <int NT, bool ASYM, bool SPLIT, bool SWIGLU>
+template <int NT, bool ASYM, bool SPLIT, bool SWIGLU, bool GROUPED = false>
 int launch_w4a16_cpg(int cpg, const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
                      cudaStream_t st) {
     if (NT == 1) {
         switch (cpg) {
-            case 8: return launch(k_w4a16_gemv_m8<8, ASYM, SPLIT, SWIGLU>, packed, a, p, st);
-            case 4: return launch(k_w4a16_gemv_m8<4, ASYM, SPLIT, SWIGLU>, packed, a, p, st);
-            case 2: return launch(k_w4a16_gemv_m8<2, ASYM, SPLIT, SWIGLU>, packed, a, p, st);
-            default: return launch(k_w4a16_gemv_m8<1, ASYM, SPLIT, SWIGLU>, packed, a, p, st);
+            case 8: return launch(k_w4a16_gemv_m8<8, ASYM, SPLIT, SWIGLU, GROUPED>, packed, a, p, st);
+            case 4: return launch(k_w4a16_gemv_m8<4, ASYM, SPLIT, SWIGLU, GROUPED>, packed, a, p, st);
+            case 2: return launch(k_w4a16_gemv_m8<2, ASYM, SPLIT, SWIGLU, GROUPED>, packed, a, p, st);
+            default: return launch(k_w4a16_gemv_m8<1, ASYM, SPLIT, SWIGLU, GROUPED>, packed, a, p, st);
         }
     }
     switch (cpg) {
-        case 8: return launch(k_w4a16_gemv_m16<8, ASYM, SPLIT, SWIGLU>, packed, a, p, st);
-        case 4: return launch(k_w4a16_gemv_m16<4, ASYM, SPLIT, SWIGLU>, packed, a, p, st);
-        case 2: return launch(k_w4a16_gemv_m16<2, ASYM, SPLIT, SWIGLU>, packed, a, p, st);
-        default: return launch(k_w4a16_gemv_m16<1, ASYM, SPLIT, SWIGLU>, packed, a, p, st);
+        case 8: return launch(k_w4a16_gemv_m16<8, ASYM, SPLIT, SWIGLU, GROUPED>, packed, a, p, st);
+        case 4: return launch(k_w4a16_gemv_m16<4, ASYM, SPLIT, SWIGLU, GROUPED>, packed, a, p, st);
+        case 2: return launch(k_w4a16_gemv_m16<2, ASYM, SPLIT, SWIGLU, GROUPED>, packed, a, p, st);
+        default: return launch(k_w4a16_gemv_m16<1, ASYM, SPLIT, SWIGLU, GROUPED>, packed, a, p, st);
     }
 }
 
 // W4A16 decode launch for one K-split case (all group sizes and widths).
-template <bool SPLIT, bool SWIGLU = false>
+// The token tile (8 or 16) follows a.M, or the per-group bound when grouped.
+template <bool SPLIT, bool SWIGLU = false, bool GROUPED = false>
 int launch_w4a16_variant(const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
                          cudaStream_t st) {
     const int gq = a.G / 32;
     const int cpg = (gq % 8 == 0) ? 8 : (gq % 4 == 0) ? 4 : (gq % 2 == 0) ? 2 : 1;
     const bool asym = a.zeros != nullptr;
-    if (a.M <= 8)
-        return asym ? launch_w4a16_cpg<1, true, SPLIT, SWIGLU>(cpg, packed, a, p, st)
-                    : launch_w4a16_cpg<1, false, SPLIT, SWIGLU>(cpg, packed, a, p, st);
-    return asym ? launch_w4a16_cpg<2, true, SPLIT, SWIGLU>(cpg, packed, a, p, st)
-                : launch_w4a16_cpg<2, false, SPLIT, SWIGLU>(cpg, packed, a, p, st);
+    if ((GROUPED ? a.gmax : a.M) <= 8)
+        return asym ? launch_w4a16_cpg<1, true, SPLIT, SWIGLU, GROUPED>(cpg, packed, a, p, st)
+                    : launch_w4a16_cpg<1, false, SPLIT, SWIGLU, GROUPED>(cpg, packed, a, p, st);
+    return asym ? launch_w4a16_cpg<2, true, SPLIT, SWIGLU, GROUPED>(cpg, packed, a, p, st)
+                : launch_w4a16_cpg<2, false, SPLIT, SWIGLU, GROUPED>(cpg, packed, a, p, st);
 }
 
 }  // namespace

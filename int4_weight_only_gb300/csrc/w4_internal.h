@@ -42,11 +42,16 @@ struct GemvPlan {
     int red = 0;       // bytes of the cross-warp reduction buffer
     size_t smem = 0;   // dynamic shared memory (bytes)
     size_t ws_bytes = 0;
+    size_t list_off = 0;  // grouped plans: offset of the active-group list in shared memory
 };
 
 // act_bytes: bytes per activation element (2 for bf16, 1 for int8).
+// groups > 0: a grouped plan (one matrix of N rows per group, M = the most
+// tokens of one group, N here = rows of all groups expected to be active):
+// no K split, and room for a list of `groups` group ids.
 // Returns false if no plan fits (M too large).
-bool plan_gemv(int M, int N, int Kp, int G, int act_bytes, int sm_count, GemvPlan* plan);
+bool plan_gemv(int M, int N, int Kp, int G, int act_bytes, int sm_count, GemvPlan* plan,
+               int groups = 0);
 
 struct GemvArgs {
     const void* x;            // bf16 [M, K] (W4A16) or int8 [M, Kp] (W4A8)
@@ -62,6 +67,12 @@ struct GemvArgs {
     int M, N, K, Kp, G, Ng;
     int R, SKE, nst, S, spl, units, XS, red;
     int xtma;                 // activation rows are 16-byte aligned: stage them with TMA
+    // grouped decode: x [M, K] rows sorted by group, goff[E+1] token offsets
+    // of the E groups, weights/scales/zeros/bias stacked [E, N, ...], y [M, N];
+    // at most gmax tokens per group
+    const int* goff;
+    int E, gmax, NBg;         // groups, token bound, row blocks per group
+    int list_off;             // shared-memory offset of the active-group list
 };
 
 // The launchers encode the tensor map of `packed` for the plan's box shape
@@ -75,6 +86,9 @@ int launch_w4a16_swiglu(const uint8_t* packed, const GemvArgs& a, const GemvPlan
                         cudaStream_t stream);
 int launch_w4a16_gemv_split(const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
                             cudaStream_t stream);
+// Grouped decode (MoE experts): the tensor map covers the E * N stacked rows.
+int launch_w4a16_grouped(const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
+                         cudaStream_t stream);
 int launch_w4a16_gemv(const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
                       cudaStream_t stream);
 int launch_w4a8_gemv(const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,

@@ -20,6 +20,14 @@ weights and real activations):
 Every linear gets its own ``torch.Generator('cpu')`` seeded with
 ``seed``; draws happen in the order W, W-outlier columns, x, x-outlier
 positions, bias.
+
+Expert (mixture-of-experts) layers at decode: E = 128 experts with 8 active
+per token and 32-wide groups, as on the Gemma 4 26B-A4B TPU page; the expert
+matrix sizes are not on the pages and are chosen here (hidden 2048, expert
+width 1024: gate|up 2048 x 2048, down 2048 x 1024), symmetric int4.  A batch
+of B tokens routes each token to 8 distinct experts drawn uniformly (seeded),
+so the grouped call sees T = 8 B rows sorted by expert, most experts holding
+0-3 of them.
 """
 from __future__ import annotations
 
@@ -175,3 +183,32 @@ def make_random_format(N: int, K: int, group_size: int, symmetric: bool, seed: i
     if not symmetric:
         zeros = torch.randint(0, 16, (N, Ng), generator=g, dtype=torch.int64).to(torch.uint8)
     return packed, scales, zeros
+
+
+# --------------------------------------------------------------------------
+# Expert layers (grouped decode).
+# --------------------------------------------------------------------------
+
+MOE_EXPERTS, MOE_TOPK, MOE_HIDDEN, MOE_WIDTH, MOE_GROUP = 128, 8, 2048, 1024, 32
+
+
+def moe_route_counts(batch: int, experts: int = MOE_EXPERTS, topk: int = MOE_TOPK,
+                     seed: int = 0) -> List[int]:
+    """Tokens per expert when each of `batch` tokens picks `topk` distinct
+    experts uniformly at random (seeded)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    counts = [0] * experts
+    for _ in range(batch):
+        for e in torch.randperm(experts, generator=g)[:topk].tolist():
+            counts[e] += 1
+    return counts
+
+
+def moe_decode(batch: int = 16) -> List[Linear]:
+    """The two projections of an expert layer, one matrix per expert
+    (N x K per expert; the grouped call stacks the 128 of them)."""
+    return [Linear(f"moe_gate_up_b{batch}", batch * MOE_TOPK, 2 * MOE_WIDTH, MOE_HIDDEN,
+                   MOE_GROUP, True, seed=600),
+            Linear(f"moe_down_b{batch}", batch * MOE_TOPK, MOE_HIDDEN, MOE_WIDTH,
+                   MOE_GROUP, True, seed=601)]
