@@ -682,6 +682,28 @@ def run_case(args):
     import int4_weight_only_gb300 as w4
     from int4_weight_only_gb300 import build as b
     b.build()
+    if args.case.startswith("moe_"):
+        # expert layer, --M = batch of tokens (8 experts each): grouped calls
+        lin = next(l for l in WL.moe_decode(args.M) if l.name.startswith(args.case))
+        E = WL.MOE_EXPERTS
+        counts = WL.moe_route_counts(args.M, seed=args.M)
+        goff = torch.zeros(E + 1, dtype=torch.int32, device="cuda")
+        goff[1:] = torch.cumsum(torch.tensor(counts, dtype=torch.int32, device="cuda"), 0,
+                                dtype=torch.int32)
+        Kp = -(-lin.K // lin.group_size) * lin.group_size
+        g = torch.Generator(device="cuda")
+        g.manual_seed(lin.seed)
+        p = torch.randint(0, 256, (E * lin.N, Kp // 2), generator=g, device="cuda",
+                          dtype=torch.int32).to(torch.uint8)
+        sc = torch.rand(E * lin.N, Kp // lin.group_size, generator=g, device="cuda") * 0.01 + 1e-4
+        x = WL.make_activations(lin.K, sum(counts), seed=lin.seed).cuda()
+        for _ in range(args.reps):
+            w4.w4a16_grouped_linear(x, goff, p, sc, None, None, E, lin.N, lin.K, lin.group_size,
+                                    max(counts))
+        torch.cuda.synchronize()
+        print(json.dumps({"case": lin.name, "batch": args.M, "reps": args.reps,
+                          "device_error": w4.w4_get_device_error()}))
+        return
     allw = (WL.tiny() + WL.decode_7b(args.M) + WL.decode_12b(args.M) + WL.prefill_7b(args.M)
             + WL.w4a8_7b())
     lin = next(l for l in allw if l.name.startswith(args.case))
