@@ -7,10 +7,12 @@ from .w4_oracle import (padded_k, rtn_quantize, pack_nibbles, unpack_nibbles,
                         pack_rtn, dequantize_f64, bf16_to_f64, w4a16_linear,
                         swiglu_rows, pair_rows, silu_f64, w4a16_linear_swiglu,
                         w4a16_grouped_linear,
-                        w4a8_quantize_act, w4a8_linear, int32_worst_case)
+                        w4a8_quantize_act, w4a8_linear, int32_worst_case,
+                        smooth_factors, w4a8_linear_grouped)
 
 __all__ = ["padded_k", "rtn_quantize", "pack_nibbles", "unpack_nibbles",
            "pack_rtn", "dequantize_f64", "bf16_to_f64", "w4a16_linear",
            "swiglu_rows", "pair_rows", "silu_f64", "w4a16_linear_swiglu",
            "w4a16_grouped_linear",
-           "w4a8_quantize_act", "w4a8_linear", "int32_worst_case"]
+           "w4a8_quantize_act", "w4a8_linear", "int32_worst_case",
+           "smooth_factors", "w4a8_linear_grouped"]

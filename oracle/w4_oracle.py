@@ -26,7 +26,11 @@ Sources (page title, section):
      (128 experts, 8 active per token) whose int4 weights with 32-wide
      groups are multiplied by their tokens in a grouped matmul.
 [P2] "【infra之路】12-投机解码、量化与推理引擎对比", section 2.2: symmetric INT8,
-     scale = max/127, per-value error <= scale/2.
+     scale = max/127, per-value error <= scale/2.  Section 2.4 (SmoothQuant):
+     Y = (X diag(s)^-1)(diag(s) W) with s_j = max|X_j|^a / max|W_j|^(1-a),
+     a = 0.5 typically, j an input channel.
+[P5] "LLM 模型壓縮與推理加速實踐-陳磊.pdf", W8A8 slides (模型壓縮-W8A8量化): activation
+     outliers sit in a few channels; a between 0.5 and 0.75, tuned per layer.
 [P4] "Jetson Orin AGX INT4 推理优化实践：super 分支从 9 tok/s 到 24 tok/s",
      section "从 FP 线性层到 INT4 DP4A 的数学推导": per-row INT4 weights
      q^W = clip(round(W/s^W), -8, 7); dynamic per-token INT8 activations
@@ -50,6 +54,12 @@ Readings where the pages are silent (each is also listed in the design notes):
  (x)   grouped linear: tokens arrive sorted by group with offsets
        goff[0] = 0 <= ... <= goff[E] = T; group e's weights are rows
        e N .. e N + N - 1 of the stacked matrix, its bias the same rows.
+ (xi)  smoothing: channel maxima over the calibration tokens and over the
+       output rows; a channel whose activation or weight maximum is 0 gets
+       s = 1.  At inference x' = fp32(x * fp32(1 / s)) (one rounding each),
+       then the INT8 rule of [P4] on x'.
+ (xii) group-wise W4A8: acc_g = sum over the group's columns of
+       (code - 8) q_x in integers; y = s_x * sum_g s_W[n, g] acc_g + b.
  (viii) the W4A8 weight scale is max|row|/7 (the symmetric rule of [P1]),
        codes stored as q+8 like W4A16.
  Matmuls are done in fp64 on exactly dequantized weights (s * (code - z) is
@@ -286,11 +296,14 @@ def w4a16_grouped_linear(x, goff, packed, scales, zeros, bias, E: int, N: int, K
 # W4A8 [P4]
 # ---------------------------------------------------------------------------
 
-def w4a8_quantize_act(x, Kp: int):
+def w4a8_quantize_act(x, Kp: int, inv_s=None):
     """Per-token dynamic INT8: s_x = fp32(max|x| / 127),
     q_x = clip(rint(fp32(x / s_x)), -127, 127); columns K..Kp-1 are 0.
-    Returns (qx int8 [M, Kp], sx fp32 [M])."""
+    With ``inv_s`` (fp32 [K], reading (xi)) x is first smoothed:
+    x' = fp32(x * inv_s).  Returns (qx int8 [M, Kp], sx fp32 [M])."""
     xf = bf16_to_f64(x).astype(F32)
+    if inv_s is not None:
+        xf = (xf * np.asarray(inv_s, dtype=F32)[None, :]).astype(F32)
     M, K = xf.shape
     maxabs = np.abs(xf).max(axis=1) if K > 0 else np.zeros(M, F32)
     sx = (maxabs.astype(F32) / F32(127.0)).astype(F32)
@@ -301,6 +314,44 @@ def w4a8_quantize_act(x, Kp: int):
     qx = np.zeros((M, Kp), dtype=np.int8)
     qx[:, :K] = q.astype(np.int8)
     return qx, sx
+
+
+def smooth_factors(X, W, alpha: float):
+    """SmoothQuant factors [P2] 2.4, reading (xi), in fp64:
+    s_j = max_t |X[t, j]|^alpha / max_n |W[n, j]|^(1 - alpha), and 1 where
+    either maximum is 0.  X: calibration activations [T, K] (bf16 values),
+    W: fp32 [N, K]."""
+    xm = np.abs(bf16_to_f64(X)).max(axis=0)
+    wm = np.abs(np.asarray(W, dtype=np.float64)).max(axis=0)
+    ok = (xm > 0) & (wm > 0)
+    s = np.ones_like(xm)
+    s[ok] = xm[ok] ** alpha / wm[ok] ** (1.0 - alpha)
+    return s
+
+
+def w4a8_linear_grouped(qx, sx, packed, scales, group_size: int, bias=None, rows=None):
+    """Group-wise W4A8, reading (xii): per (token, row, group) the integer
+    acc_g = sum_{k in g} (code - 8) q_x, then
+    y = s_x * sum_g s_W[n, g] * acc_g + b in fp64.  Returns (acc [M, N, Ng]
+    int64, y fp64 [M, N])."""
+    packed = np.asarray(packed)
+    scales = np.asarray(scales, dtype=F32)
+    if rows is not None:
+        rows = np.asarray(rows)
+        packed = packed[rows]
+        scales = scales[rows]
+    q = unpack_nibbles(packed).astype(np.int64) - 8           # [N, Kp]
+    N, Kp = q.shape
+    G = int(group_size)
+    Ng = Kp // G
+    qx64 = np.asarray(qx, dtype=np.int64)                     # [M, Kp]
+    acc = np.einsum("mgk,ngk->mng", qx64.reshape(-1, Ng, G), q.reshape(N, Ng, G))
+    y = np.asarray(sx, np.float64)[:, None] * (acc.astype(np.float64)
+                                                * scales.astype(np.float64)[None]).sum(axis=2)
+    if bias is not None:
+        b = np.asarray(bias, dtype=np.float64)
+        y = y + (b if rows is None else b[rows])[None, :]
+    return acc, y
 
 
 def w4a8_linear(qx, sx, packed, w_scales, bias, rows=None):

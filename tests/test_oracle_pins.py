@@ -488,3 +488,101 @@ def test_grouped_token_order_and_offsets():
     for bad in ([0, 5, 4, 7], [1, 4, 4, 7], [0, 4, 4, 8]):
         with pytest.raises(ValueError):
             O.w4a16_grouped_linear(x, np.array(bad), packed, scales, None, bias, E, N, K, G)
+
+
+# ---------------------------------------------------------------------------
+# Group-wise W4A8 and SmoothQuant smoothing ("【infra之路】12-…", section 2.4;
+# "LLM 模型壓縮與推理加速實踐-陳磊.pdf", W8A8 slides)
+# ---------------------------------------------------------------------------
+
+def test_w4a8_grouped_one_group_is_per_row():
+    rng = np.random.default_rng(3)
+    N, K = 24, 256
+    W = _rand_w(N, K, 5, std=0.3)
+    packed, scales, _ = O.pack_rtn(W, K, True)
+    x = _bf16_round(rng.standard_normal((3, K)).astype(np.float32))
+    qx, sx = O.w4a8_quantize_act(x, K)
+    acc, y = O.w4a8_linear(qx, sx, packed, scales, None)
+    accg, yg = O.w4a8_linear_grouped(qx, sx, packed, scales, K)
+    assert np.array_equal(accg[:, :, 0], acc)
+    assert np.array_equal(yg, y)
+
+
+def test_w4a8_grouped_brute_force_loops():
+    """Pure-Python loops over bytes and nibbles, per group."""
+    rng = np.random.default_rng(8)
+    N, K, G = 5, 96, 32
+    W = _rand_w(N, K, 6, std=0.3)
+    packed, scales, _ = O.pack_rtn(W, G, True)
+    x = _bf16_round(rng.standard_normal((2, K)).astype(np.float32))
+    qx, sx = O.w4a8_quantize_act(x, K)
+    b = rng.standard_normal(N).astype(np.float32)
+    acc, y = O.w4a8_linear_grouped(qx, sx, packed, scales, G, bias=b)
+    for m in range(2):
+        for n in range(N):
+            tot = 0.0
+            for g in range(K // G):
+                a = 0
+                for k in range(g * G, (g + 1) * G):
+                    byte = int(packed[n, k // 2])
+                    code = (byte >> 4) if k % 2 else (byte & 15)
+                    a += (code - 8) * int(qx[m, k])
+                assert acc[m, n, g] == a
+                tot += float(scales[n, g]) * a
+            assert abs(y[m, n] - (float(sx[m]) * tot + float(b[n]))) <= 1e-12 * (1 + abs(y[m, n]))
+
+
+def test_smooth_factors_closed_form():
+    X = np.zeros((3, 4), np.float32)
+    X[0] = [4.0, -1.0, 0.0, 2.0]
+    X[2] = [-2.0, 0.5, 0.0, 1.0]
+    W = np.array([[1.0, 4.0, 3.0, 0.0], [-0.5, -2.0, 1.0, 0.0]], np.float32)
+    s = O.smooth_factors(X, W, 0.5)
+    assert np.allclose(s, [2.0, 0.5, 1.0, 1.0], rtol=0, atol=1e-15)   # zero maxima -> 1
+    # at alpha = 1/2 the smoothed maxima meet at sqrt(max|X_j| max|W_j|)
+    xs = np.abs(X[:, :2] / s[:2]).max(axis=0)
+    ws = np.abs(W[:, :2] * s[:2]).max(axis=0)
+    assert np.allclose(xs, [2.0, 2.0]) and np.allclose(ws, [2.0, 2.0])
+    # alpha = 1 moves all of max|X_j| into the weights, alpha = 0 none of it
+    assert np.allclose(O.smooth_factors(X, W, 1.0)[:2], [4.0, 1.0])
+    assert np.allclose(O.smooth_factors(X, W, 0.0)[:2], [1.0, 0.25])
+
+
+def test_smoothing_keeps_the_product_and_tames_outlier_channels():
+    """(X / s)(W s)^T = X W^T exactly in fp64, and with activation outliers in
+    a few channels the smoothed W4A8 layer is closer to X W^T."""
+    rng = np.random.default_rng(12)
+    T, K, N = 64, 512, 128
+    X = rng.standard_normal((T, K)).astype(np.float32)
+    hot = rng.permutation(K)[:8]
+    X[:, hot] *= 50.0
+    X = _bf16_round(X)
+    W = _rand_w(N, K, 13, std=0.05)
+    s = O.smooth_factors(X, W, 0.5)
+    exact = X.astype(np.float64) @ W.astype(np.float64).T
+    moved = (X.astype(np.float64) / s) @ (W.astype(np.float64) * s).T
+    assert np.allclose(moved, exact, rtol=1e-12, atol=1e-9)
+
+    def w4a8_error(inv_s, Ws):
+        p, sc, _ = O.pack_rtn(Ws.astype(np.float32), K, True)
+        qx, sx = O.w4a8_quantize_act(X, K, inv_s=inv_s)
+        _, y = O.w4a8_linear(qx, sx, p, sc, None)
+        return np.linalg.norm(y - exact) / np.linalg.norm(exact)
+    inv_s = (np.float32(1.0) / s.astype(np.float32)).astype(np.float32)
+    plain = w4a8_error(None, W)
+    smooth = w4a8_error(inv_s, (W * s.astype(np.float32)).astype(np.float32))
+    assert smooth < 0.85 * plain, (smooth, plain)      # measured 0.112 vs 0.142
+
+
+def test_smoothed_act_quant_with_power_of_two_factors():
+    """inv_s a power of two: x * inv_s is exact, so the result is the plain
+    rule on the exactly scaled activations; inv_s = 1 changes nothing."""
+    rng = np.random.default_rng(2)
+    x = _bf16_round(rng.standard_normal((3, 64)).astype(np.float32))
+    q1, s1 = O.w4a8_quantize_act(x, 64)
+    q2, s2 = O.w4a8_quantize_act(x, 64, inv_s=np.ones(64, np.float32))
+    assert np.array_equal(q1, q2) and np.array_equal(s1, s2)
+    inv = np.where(np.arange(64) % 2 == 0, 0.25, 4.0).astype(np.float32)
+    q3, s3 = O.w4a8_quantize_act(x, 64, inv_s=inv)
+    q4, s4 = O.w4a8_quantize_act(_bf16_round(x * inv), 64)
+    assert np.array_equal(q3, q4) and np.array_equal(s3, s4)
