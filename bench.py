@@ -421,9 +421,14 @@ class W4A8Set:
                             lin.group_size, y=d["y"])
 
 
-def measure_w4a8(w4, hbm, reps=200):
+def measure_w4a8(w4, hbm, reps=200, group_size=None):
     """W4A8 linears at M=1: integer GEMV alone (GB/s) and quantize + GEMV."""
     lins = WL.w4a8_7b()
+    if group_size is not None:
+        # group-wise weight scales (one per group_size columns) instead of one per row
+        lins = [WL.Linear(l.name + f"_g{group_size}", l.M, l.N, l.K, group_size, True, l.seed,
+                          x_outlier_frac=l.x_outlier_frac, x_outlier_scale=l.x_outlier_scale,
+                          bias=l.bias, kind="w4a8") for l in lins[:2]]
     ws = W4A8Set(w4, lins, min_bytes=3 * L2_BYTES)
     out = []
     for li, lin in enumerate(lins):
@@ -433,7 +438,7 @@ def measure_w4a8(w4, hbm, reps=200):
         t_lin = time_graph_steps(lambda i, li=li: ws.call(li, i, False), n, ws.R, 1) / n
         t_all = time_graph_steps(lambda i, li=li: ws.call(li, i, True), n, ws.R, 1) / n
         b = ws.bytes_lin[li]
-        out.append({"name": lin.name, "N": lin.N, "K": lin.K, "Kp": lin.group_size,
+        out.append({"name": lin.name, "N": lin.N, "K": lin.K, "group_size": lin.group_size,
                     "linear_us": round(t_lin * 1e6, 3), "linear_GB/s": round(b / t_lin / 1e9, 1),
                     "quant+linear_us": round(t_all * 1e6, 3)})
     tb = sum(ws.bytes_lin)
@@ -442,7 +447,8 @@ def measure_w4a8(w4, hbm, reps=200):
     torch.cuda.empty_cache()
     v = tb / tt / 1e9
     return {"value": round(v, 1), "unit": "GB/s", "per_linear": out,
-            "roofline": {"kernel": "k_w4a8_gemv", "bound": "hbm", "achieved": round(v, 1),
+            "roofline": {"kernel": "k_w4a8_gemv" if group_size is None else "k_w4a8g_gemv",
+                         "bound": "hbm", "achieved": round(v, 1),
                          "peak": hbm, "unit": "GB/s", "frac": round(v / hbm, 4)}}
 
 
@@ -631,6 +637,7 @@ def run_ours(args, world, rank):
     if not args.decode_only:
         res["prefill"] = [measure_prefill(w4, M, bf16, peak_kind) for M in (2048, 512)]
         res["w4a8"] = measure_w4a8(w4, hbm)
+        res["w4a8_g128"] = measure_w4a8(w4, hbm, group_size=128)
         res["decode_12b"] = measure_decode_12b(w4, hbm)
         res["swiglu_7b"] = measure_swiglu(w4, hbm)
         res["moe_decode"] = measure_moe(w4, hbm)

@@ -238,6 +238,36 @@ W4_API int w4a8_quantize_act(const uint16_t* x, int M, int K, int group_size,
                       int8_t* qx, float* sx, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * w4a8_quantize_act_smooth - w4a8_quantize_act on SmoothQuant-smoothed
+ * activations ("【infra之路】12-投机解码、量化与推理引擎对比", section 2.4:
+ * Y = (X diag(s)^-1)(diag(s) W)): x'[m,k] = fp32(x[m,k] * inv_s[k]) (one
+ * rounding), then s_x and qx from x' by the rule above.  The weights must
+ * carry the factors (w4_smooth) before they are packed.
+ *
+ *  inv_s  [K] fp32, 16-byte aligned (1/s from w4_smooth).
+ *  Other arguments and outputs as for w4a8_quantize_act.
+ * ------------------------------------------------------------------------- */
+W4_API int w4a8_quantize_act_smooth(const uint16_t* x, const float* inv_s, int M, int K,
+                                    int group_size, int8_t* qx, float* sx, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * w4_smooth - SmoothQuant calibration of one linear layer (same section; the
+ * factor range and per-layer tuning of alpha: "LLM 模型壓縮與推理加速實踐-
+ * 陳磊.pdf", W8A8 slides):
+ *  s[j]     = max_t |X[t,j]|^alpha / max_n |W[n,j]|^(1 - alpha)  (fp32 powf;
+ *             1 where either maximum is 0),  inv_s[j] = fp32(1 / s[j]),
+ *  W[n,j]  *= s[j]  (in place; pack W afterwards with w4_pack_rtn).
+ *
+ *  X      [T, K] bf16 calibration activations (T >= 0; T = 0 gives s = 1).
+ *  W      [N, K] fp32, device, modified.
+ *  alpha  in [0, 1] (0.5 typical).
+ *  s, inv_s  [K] fp32 out (device).
+ *  Ends with an ordinary (not programmatic) launch, like w4_pack_rtn.
+ * ------------------------------------------------------------------------- */
+W4_API int w4_smooth(const uint16_t* X, int T, float* W, int N, int K, float alpha, float* s,
+                     float* inv_s, void* stream);
+
+/* ---------------------------------------------------------------------------
  * w4a8_workspace_bytes - as w4a16_workspace_bytes, for w4a8_linear.
  * ------------------------------------------------------------------------- */
 W4_API size_t w4a8_workspace_bytes(int M, int N, int K, int group_size);
@@ -246,15 +276,21 @@ W4_API size_t w4a8_workspace_bytes(int M, int N, int K, int group_size);
  * w4a8_linear - INT4 x INT8 integer linear layer ([ORIN]):
  *  acc[m,n] = sum_{k < Kp} (code[n,k] - 8) * qx[m,k]   (exact, int32)
  *  y[m,n]   = s_W[n] * s_x[m] * acc[m,n] + bias[n]      (fp32, stored bf16)
+ *  With group_size < Kp (group-wise weight scales, the per-group use of the
+ *  INT8 rule of "【infra之路】12-投机解码、量化与推理引擎对比", section 2.2):
+ *  acc_g[m,n] = sum over group g's columns of (code - 8) * qx  (int32)
+ *  y[m,n]     = s_x[m] * sum_g s_W[n,g] * acc_g[m,n] + bias[n]  (fp32 sums)
  *
  *  qx, sx     from w4a8_quantize_act (same K and group_size).
- *  packed     [N, Kp/2] uint8 symmetric codes from w4_pack_rtn with
- *             group_size == Kp (one scale per row), 16-byte aligned.
- *  w_scales   [N] fp32 (the [N, 1] scales of that packing).
+ *  packed     [N, Kp/2] uint8 symmetric codes from w4_pack_rtn, 16-byte
+ *             aligned; group_size == Kp (one scale per row) or, group-wise,
+ *             32, 64, 128 or a multiple of 256 (else W4_ERR_UNSUPPORTED_GROUP).
+ *  w_scales   [N, Ng] fp32 (Ng = Kp / group_size; [N] per row).
  *  bias       [N] fp32 or NULL.
  *  y          [M, N] bf16 out.
- *  acc_out    [M, N] int32 out, or NULL.
- *  Requires M <= 16, group_size == Kp and Kp <= W4_W4A8_MAX_KP.
+ *  acc_out    [M, N] int32 out, or NULL; per-row only (group-wise: must be
+ *             NULL, else W4_ERR_INVALID_ARG).
+ *  Requires M <= 16 and Kp <= W4_W4A8_MAX_KP.
  * ------------------------------------------------------------------------- */
 W4_API int w4a8_linear(const int8_t* qx, const float* sx, const uint8_t* packed,
                 const float* w_scales, const float* bias, uint16_t* y,

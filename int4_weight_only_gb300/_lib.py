@@ -26,6 +26,8 @@ _SIGS = {
     "w4a16_grouped_linear": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
                                       _c_int, _c_int, _c_int, _c_int, _vp]),
     "w4a8_quantize_act": (_c_int, [_vp, _c_int, _c_int, _c_int, _vp, _vp, _vp]),
+    "w4a8_quantize_act_smooth": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _vp]),
+    "w4_smooth": (_c_int, [_vp, _c_int, _vp, _c_int, _c_int, ctypes.c_float, _vp, _vp, _vp]),
     "w4a8_workspace_bytes": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
     "w4a8_linear": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
                              _vp, _c_size, _vp]),
@@ -328,18 +330,52 @@ def w4a8_quantize_act(x: torch.Tensor, group_size: int, qx=None, sx=None, stream
     return qx, sx
 
 
+def w4a8_quantize_act_smooth(x: torch.Tensor, inv_s: torch.Tensor, group_size: int, qx=None,
+                             sx=None, stream=None):
+    """w4a8_quantize_act on x * inv_s (SmoothQuant) -> (qx [M, Kp] int8, sx [M] fp32)."""
+    M, K = x.shape
+    _need(x, torch.bfloat16, (M, K), "x")
+    _need(inv_s, torch.float32, (K,), "inv_s")
+    Kp = padded_k(K, group_size)
+    if qx is None:
+        qx = torch.empty(M, Kp, dtype=torch.int8, device=x.device)
+    if sx is None:
+        sx = torch.empty(M, dtype=torch.float32, device=x.device)
+    _need(qx, torch.int8, (M, Kp), "qx")
+    _need(sx, torch.float32, (M,), "sx")
+    _check("w4a8_quantize_act_smooth", load().w4a8_quantize_act_smooth(
+        _ptr(x), _ptr(inv_s), M, K, int(group_size), _ptr(qx), _ptr(sx), _stream(x, stream)))
+    return qx, sx
+
+
+def w4_smooth(X: torch.Tensor, W: torch.Tensor, alpha: float = 0.5, stream=None):
+    """SmoothQuant calibration: returns (s, inv_s) [K] fp32 and multiplies
+    the columns of W [N, K] fp32 (in place) by s."""
+    T, K = X.shape
+    N = W.shape[0]
+    _need(X, torch.bfloat16, (T, K), "X")
+    _need(W, torch.float32, (N, K), "W")
+    s = torch.empty(K, dtype=torch.float32, device=W.device)
+    inv_s = torch.empty(K, dtype=torch.float32, device=W.device)
+    _check("w4_smooth", load().w4_smooth(_ptr(X), T, _ptr(W), N, K, float(alpha), _ptr(s),
+                                         _ptr(inv_s), _stream(W, stream)))
+    return s, inv_s
+
+
 def w4a8_linear(qx: torch.Tensor, sx: torch.Tensor, packed: torch.Tensor,
                 w_scales: torch.Tensor, bias: Optional[torch.Tensor], N: int, K: int,
                 group_size: int, y=None, acc_out=None, want_acc: bool = False,
                 workspace=None, stream=None):
-    """(y [M, N] bf16, acc [M, N] int32 or None)."""
+    """(y [M, N] bf16, acc [M, N] int32 or None).  group_size == Kp: one
+    weight scale per row (w_scales [N] or [N, 1]); smaller: group-wise
+    (w_scales [N, Kp / group_size], no acc)."""
     M, Kp = qx.shape
     _need(qx, torch.int8, (M, padded_k(K, group_size)), "qx")
     _need(sx, torch.float32, (M,), "sx")
     _need(packed, torch.uint8, (N, Kp // 2), "packed")
-    if w_scales.dim() == 2:
-        w_scales = w_scales.reshape(-1)
-    _need(w_scales, torch.float32, (N,), "w_scales")
+    Ng = Kp // group_size
+    w_scales = w_scales.reshape(N, Ng)
+    _need(w_scales, torch.float32, (N, Ng), "w_scales")
     if bias is not None:
         _need(bias, torch.float32, (N,), "bias")
     if y is None:

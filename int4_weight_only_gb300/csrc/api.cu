@@ -310,7 +310,34 @@ int w4a8_quantize_act(const uint16_t* x, int M, int K, int group_size, int8_t* q
     if (!aligned16(qx) || !aligned4(sx) || (reinterpret_cast<uintptr_t>(x) & 1))
         return W4_ERR_MISALIGNED;
     if (M == 0) return W4_OK;
-    return launch_act_quant(x, M, K, (int)Kp, qx, sx, static_cast<cudaStream_t>(stream));
+    return launch_act_quant(x, nullptr, M, K, (int)Kp, qx, sx, static_cast<cudaStream_t>(stream));
+}
+
+int w4a8_quantize_act_smooth(const uint16_t* x, const float* inv_s, int M, int K,
+                             int group_size, int8_t* qx, float* sx, void* stream) {
+    if (!x || !inv_s || !qx || !sx) return W4_ERR_NULL_PTR;
+    if (M < 0) return W4_ERR_INVALID_ARG;
+    int rc = check_group(K, group_size);
+    if (rc) return rc;
+    const long long Kp = padded_k(K, group_size);
+    if (Kp > 0x7fffffffLL) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(qx) || !aligned16(inv_s) || !aligned4(sx) ||
+        (reinterpret_cast<uintptr_t>(x) & 1))
+        return W4_ERR_MISALIGNED;
+    if (M == 0) return W4_OK;
+    return launch_act_quant(x, inv_s, M, K, (int)Kp, qx, sx, static_cast<cudaStream_t>(stream));
+}
+
+int w4_smooth(const uint16_t* X, int T, float* W, int N, int K, float alpha, float* s,
+              float* inv_s, void* stream) {
+    if (!W || !s || !inv_s || (T > 0 && !X)) return W4_ERR_NULL_PTR;
+    if (T < 0 || N <= 0 || K <= 0 || !(alpha >= 0.f && alpha <= 1.f)) return W4_ERR_INVALID_ARG;
+    if ((long long)N * K > 0x7fffffffLL * 256LL || (long long)T * K > 0x7fffffffffffLL)
+        return W4_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned4(W) || !aligned4(s) || !aligned4(inv_s) ||
+        (reinterpret_cast<uintptr_t>(X) & 1))
+        return W4_ERR_MISALIGNED;
+    return launch_smooth(X, T, W, N, K, alpha, s, inv_s, static_cast<cudaStream_t>(stream));
 }
 
 size_t w4a8_workspace_bytes(int M, int N, int K, int group_size) {
@@ -329,7 +356,11 @@ int w4a8_linear(const int8_t* qx, const float* sx, const uint8_t* packed,
     int rc = check_group(K, group_size);
     if (rc) return rc;
     const long long Kp = padded_k(K, group_size);
-    if (Kp != group_size) return W4_ERR_UNSUPPORTED_GROUP;
+    // one group per row (the integer path with exact int32 accumulators), or
+    // group-wise scales (fp32 sums of the groups' integer partials)
+    const bool grouped = Kp != group_size;
+    if (grouped && !w4a8_group_supported(group_size)) return W4_ERR_UNSUPPORTED_GROUP;
+    if (grouped && acc_out) return W4_ERR_INVALID_ARG;
     if (Kp > W4_W4A8_MAX_KP) return W4_ERR_K_TOO_LARGE;
     if (!aligned16(qx) || !aligned16(packed)) return W4_ERR_MISALIGNED;
     if (!aligned4(sx) || !aligned4(w_scales) || (bias && !aligned4(bias)) ||
@@ -345,9 +376,11 @@ int w4a8_linear(const int8_t* qx, const float* sx, const uint8_t* packed,
     a.x = qx; a.sx = sx; a.scales = w_scales; a.bias = bias; a.y = y; a.acc_out = acc_out;
     a.err = device_error_flag();
     if (!a.err) return W4_ERR_CUDA;
-    a.M = M; a.N = N; a.K = K; a.Kp = (int)Kp; a.G = group_size; a.Ng = 1;
+    a.M = M; a.N = N; a.K = K; a.Kp = (int)Kp; a.G = group_size;
+    a.Ng = (int)(Kp / group_size);
     a.R = p.R; a.SKE = p.SKE; a.nst = p.nst; a.S = p.S; a.spl = p.spl; a.units = p.units;
     a.XS = p.XS; a.red = p.red;
+    if (grouped) return launch_w4a8g_gemv(packed, a, p, static_cast<cudaStream_t>(stream));
     return launch_w4a8_gemv(packed, a, p, static_cast<cudaStream_t>(stream));
 }
 

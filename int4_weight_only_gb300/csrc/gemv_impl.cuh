@@ -955,6 +955,203 @@ __device__ void w4a8_consumer(const Smem& sm, const GemvArgs& a) {
     }
 }
 
+// Group-wise W4A8 ("【infra之路】12-投机解码、量化与推理引擎对比", section 2.2
+// rule per group; the per-row layout of w4a8_consumer otherwise): for each
+// group g of G columns the integer acc_g = sum (code - 8) q_x is formed from
+// dp4a partials, y = s_x * sum_g s_W[n, g] acc_g + b.  CPGW = min(G / 32, 8)
+// chunks of 32 columns per group inside a warp's 256-column box (G = 32, 64,
+// 128, or a multiple of 256: one group per box).  Each lane keeps, per
+// (token, row), the integer sums of its 8 columns of the current group,
+// sum code * q and sum q, and at the group's last chunk folds
+// s_g * (sum code * q - 8 sum q) into an fp32 accumulator; the lanes of a row
+// and the k-phase warps then add floats, and K splits add float partials.
+// The box's group scales are loaded before its stage's barrier wait.
+template <int MT, int CPGW>
+__device__ void w4a8g_consumer(const Smem& sm, const GemvArgs& a) {
+    constexpr int GPB = 8 / CPGW;                 // groups per 256-column box
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tig = lane & 3, gid = lane >> 2;
+    const int WR = a.R / 16, WK = CW / WR;
+    const int rt = warp % WR, kp = warp / WR;
+    const int Ng = a.Ng;
+    const int8_t* qx = static_cast<const int8_t*>(a.x);
+    const uint32_t wbuf_u = smem_u32(sm.wbuf), xbuf_u = smem_u32(sm.xbuf);
+    const int lj = lane >> 3, li = lane & 7;
+    const uint32_t l_off = (uint32_t)(kp * a.R * 128 + (rt * 16 + ((lj & 1) << 3) + li) * 128);
+    uint32_t l_cp[4];
+#pragma unroll
+    for (int cp = 0; cp < 4; ++cp) l_cp[cp] = l_off + ((uint32_t)((2 * cp + (lj >> 1)) ^ li) << 4);
+    uint32_t xrow[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+        xrow[m] = xbuf_u + (uint32_t)(min(m, a.M - 1) * a.XS + tig * 8 + kp * 256);
+    float* red = sm.red;
+
+    grid_dep_wait();
+    uint32_t it = 0;
+    int prev0 = -1, prev1 = -1;
+    for (int u = blockIdx.x; u < a.units; u += gridDim.x) {
+        int rb, s, ks0, ks1;
+        unit_coords(u, a, rb, s, ks0, ks1);
+        const int row0 = rb * a.R + rt * 16;
+        const float* sc_lo = a.scales + (size_t)min(row0 + gid, a.N - 1) * Ng;
+        const float* sc_hi = a.scales + (size_t)min(row0 + gid + 8, a.N - 1) * Ng;
+
+        named_bar_sync(1, NCT);
+        if (ks0 != prev0 || ks1 != prev1) {
+            if (tid < 16) sm.ctl->sumq[tid] = 0;
+            named_bar_sync(1, NCT);
+            stage_x_s8(sm.xbuf, sm.ctl, qx, a.M, a.Kp, a.XS, ks0 * a.SKE, (ks1 - ks0) * a.SKE, tid);
+            named_bar_sync(1, NCT);
+            prev0 = ks0;
+            prev1 = ks1;
+        }
+
+        float accf[MT][2];
+#pragma unroll
+        for (int m = 0; m < MT; ++m) accf[m][0] = accf[m][1] = 0.f;
+
+        for (int ks = ks0; ks < ks1; ++ks, ++it) {
+            const int slot = it % NS;
+            const int kw = ks * a.SKE + kp * 256;
+            if (kw < a.Kp) {
+                // this box's groups g0 .. g0 + GPB - 1 (past Ng: zero-filled columns)
+                const int g0 = kw / a.G;
+                float s_lo[GPB], s_hi[GPB];
+#pragma unroll
+                for (int j = 0; j < GPB; ++j) {
+                    s_lo[j] = g0 + j < Ng ? __ldg(sc_lo + g0 + j) : 0.f;
+                    s_hi[j] = g0 + j < Ng ? __ldg(sc_hi + g0 + j) : 0.f;
+                }
+                if (mbar_wait(&sm.ctl->full[slot], (it / NS) & 1, &sm.ctl->abort, a.err)) {
+                    const uint32_t wst = wbuf_u + slot * STAGE_BYTES;
+                    const uint32_t xoff = (uint32_t)(ks - ks0) * (uint32_t)a.SKE;
+                    int accg[MT][2], sq[MT];
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) accg[m][0] = accg[m][1] = sq[m] = 0;
+#pragma unroll
+                    for (int cp = 0; cp < 4; ++cp) {
+                        uint32_t r[4];
+                        ldmatrix_x4(wst + l_cp[cp], r[0], r[1], r[2], r[3]);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int c = 2 * cp + h;
+                            const uint32_t lo = r[2 * h] & 0x0F0F0F0Fu, hi = (r[2 * h] >> 4) & 0x0F0F0F0Fu;
+                            const uint32_t lo8 = r[2 * h + 1] & 0x0F0F0F0Fu, hi8 = (r[2 * h + 1] >> 4) & 0x0F0F0F0Fu;
+#pragma unroll
+                            for (int m = 0; m < MT; ++m) {
+                                uint32_t xe, xo;
+                                lds64(xrow[m] + xoff + c * 32, xe, xo);
+                                accg[m][0] = dp4a_us(lo, xe, accg[m][0]);
+                                accg[m][0] = dp4a_us(hi, xo, accg[m][0]);
+                                accg[m][1] = dp4a_us(lo8, xe, accg[m][1]);
+                                accg[m][1] = dp4a_us(hi8, xo, accg[m][1]);
+                                sq[m] = __dp4a((int)xe, 0x01010101, sq[m]);
+                                sq[m] = __dp4a((int)xo, 0x01010101, sq[m]);
+                            }
+                            if ((c + 1) % CPGW == 0) {         // last chunk of group c / CPGW
+                                const int j = c / CPGW;
+#pragma unroll
+                                for (int m = 0; m < MT; ++m) {
+                                    accf[m][0] = fmaf(s_lo[j], (float)(accg[m][0] - 8 * sq[m]), accf[m][0]);
+                                    accf[m][1] = fmaf(s_hi[j], (float)(accg[m][1] - 8 * sq[m]), accf[m][1]);
+                                    accg[m][0] = accg[m][1] = sq[m] = 0;
+                                }
+                            }
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.ctl->empty[slot]);
+        }
+
+        // lanes sharing a row, then the k-phases (fp32 partials)
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                float v = accf[m][h];
+                v += __shfl_xor_sync(0xffffffffu, v, 1);
+                v += __shfl_xor_sync(0xffffffffu, v, 2);
+                accf[m][h] = v;
+            }
+        if (WK > 1) {
+            if (kp > 0) {
+                float* dst = red + ((kp - 1) * WR + rt) * (MT * 2 * 32) + lane;
+#pragma unroll
+                for (int m = 0; m < MT; ++m)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) dst[(m * 2 + h) * 32] = accf[m][h];
+            }
+            named_bar_sync(1, NCT);
+            if (kp == 0) {
+                for (int q = 1; q < WK; ++q) {
+                    const float* src = red + ((q - 1) * WR + rt) * (MT * 2 * 32) + lane;
+#pragma unroll
+                    for (int m = 0; m < MT; ++m)
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) accf[m][h] += src[(m * 2 + h) * 32];
+                }
+            }
+        }
+
+        float* part = static_cast<float*>(a.partial);
+        bool write = kp == 0;
+        if (a.S > 1) {
+            if (kp == 0) {
+#pragma unroll
+                for (int m = 0; m < MT; ++m)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int n = row0 + gid + 8 * h;
+                        if (m < a.M && (m & 3) == tig && n < a.N)
+                            part[((size_t)s * a.M + m) * a.N + n] = accf[m][h];
+                    }
+            }
+            const bool last = split_k_arrive(a, sm.ctl, rb);
+            write = write && last;
+            if (last && tid == 0) a.tickets[rb] = 0;
+        }
+        if (write) {
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int n = row0 + gid + 8 * h;
+                    if (m < a.M && (m & 3) == tig && n < a.N) {
+                        float v = accf[m][h];
+                        if (a.S > 1) v = sum_splits(part + (size_t)m * a.N + n, (size_t)a.M * a.N, a.S);
+                        const float b = a.bias ? __ldg(a.bias + n) : 0.f;
+                        a.y[(size_t)m * a.N + n] = f32_to_bf16_bits(fmaf(__ldg(a.sx + m), v, b));
+                    }
+                }
+        }
+    }
+}
+
+template <int MT, int CPGW>
+__device__ __forceinline__ void w4a8g_body(const CUtensorMap* tm, const GemvArgs& a) {
+    const Smem sm = gemv_init(tm, a);
+    if (threadIdx.x >= NCT) {
+        if (threadIdx.x == NCT) gemv_producer(tm, sm.wbuf, sm.xbuf, sm.ctl, a);
+    } else {
+        w4a8g_consumer<MT, CPGW>(sm, a);
+    }
+}
+
+template <int MT, int CPGW>
+__global__ void __launch_bounds__(kGemvThreads, 2)
+k_w4a8g_gemv_m4(const __grid_constant__ CUtensorMap tmW, const GemvArgs a) {
+    w4a8g_body<MT, CPGW>(&tmW, a);
+}
+
+template <int MT, int CPGW>
+__global__ void __launch_bounds__(kGemvThreads, 1)
+k_w4a8g_gemv_m16(const __grid_constant__ CUtensorMap tmW, const GemvArgs a) {
+    w4a8g_body<MT, CPGW>(&tmW, a);
+}
+
 // Kernel instances that the plan may place two to an SM (M <= 8 for W4A16,
 // M <= 4 for W4A8) are compiled for two resident CTAs of 288 threads.
 template <int NT, int CPG, bool ASYM, bool SPLIT, bool SWIGLU, bool GROUPED>

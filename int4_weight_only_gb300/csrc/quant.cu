@@ -104,16 +104,44 @@ __device__ __forceinline__ uint32_t quant_s8(float v, float s, float rs) {
     return (uint32_t)(uint8_t)(int8_t)(int)fminf(fmaxf(rintf(t), -127.f), 127.f);
 }
 
-// Eight columns (four bf16x2 words) to eight INT8 bytes; all zero when s = 0.
-__device__ __forceinline__ uint2 quant_s8x8(const uint4& v, float s, float rs) {
-    if (s == 0.f) return make_uint2(0u, 0u);
+// Eight columns k .. k+7 (four bf16x2 words) as fp32, smoothed when
+// inv_s is given: x' = fp32(x * inv_s[k + j]) (the product rounded once).
+// Columns >= K hold zero words and are not smoothed.
+template <bool SMOOTH>
+__device__ __forceinline__ void cols8(const uint4& v, const float* inv_s, int k, int K, float f[8]) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t b[8];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        b[2 * j] = quant_s8(__uint_as_float(w[j] << 16), s, rs);
-        b[2 * j + 1] = quant_s8(__uint_as_float(w[j] & 0xFFFF0000u), s, rs);
+        f[2 * j] = __uint_as_float(w[j] << 16);
+        f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
     }
+    if (SMOOTH && k < K) {
+        const float4 a = __ldg(reinterpret_cast<const float4*>(inv_s + k));
+        const float4 b = __ldg(reinterpret_cast<const float4*>(inv_s + k + 4));
+        f[0] *= a.x; f[1] *= a.y; f[2] *= a.z; f[3] *= a.w;
+        f[4] *= b.x; f[5] *= b.y; f[6] *= b.z; f[7] *= b.w;
+    }
+}
+
+// Four columns k .. k+3 (two bf16x2 words, k < K) as fp32, smoothed as above.
+template <bool SMOOTH>
+__device__ __forceinline__ void cols4(const uint2& v, const float* inv_s, int k, float f[4]) {
+    f[0] = __uint_as_float(v.x << 16);
+    f[1] = __uint_as_float(v.x & 0xFFFF0000u);
+    f[2] = __uint_as_float(v.y << 16);
+    f[3] = __uint_as_float(v.y & 0xFFFF0000u);
+    if (SMOOTH) {
+        const float4 a = __ldg(reinterpret_cast<const float4*>(inv_s + k));
+        f[0] *= a.x; f[1] *= a.y; f[2] *= a.z; f[3] *= a.w;
+    }
+}
+
+// Eight values to eight INT8 bytes; all zero when s = 0.
+__device__ __forceinline__ uint2 quant_s8x8(const float f[8], float s, float rs) {
+    if (s == 0.f) return make_uint2(0u, 0u);
+    uint32_t b[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) b[j] = quant_s8(f[j], s, rs);
     return make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24),
                       b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
 }
@@ -124,6 +152,9 @@ __device__ __forceinline__ uint2 quant_s8x8(const uint4& v, float s, float rs) {
 // stores s_x.  RV > 0: the row has at most RV * 4096 columns and each thread
 // keeps its RV 16-byte words in registers between the two steps (one read of
 // x); RV = 0 (longer rows, C = 1): two passes, the second hitting L1/L2.
+// SMOOTH: the activations are first divided by the SmoothQuant factors, as
+// x * inv_s per column ("【infra之路】12-投机解码、量化与推理引擎对比",
+// section 2.4), and the rule applies to x'.
 // Launched with programmatic dependent launch: it waits for the kernel before
 // it (which may have written x, or may still be reading qx and sx) before
 // touching memory, and at once lets the next kernel start its prologue (a
@@ -131,10 +162,10 @@ __device__ __forceinline__ uint2 quant_s8x8(const uint4& v, float s, float rs) {
 // before reading qx).
 constexpr int kActThreads = 512;
 
-template <int RV>
+template <int RV, bool SMOOTH>
 __global__ void __launch_bounds__(kActThreads)
-k_act_quant(const uint16_t* __restrict__ x, int K, int Kp, int8_t* __restrict__ qx,
-            float* __restrict__ sx) {
+k_act_quant(const uint16_t* __restrict__ x, const float* __restrict__ inv_s, int K, int Kp,
+            int8_t* __restrict__ qx, float* __restrict__ sx) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __shared__ float red[kActThreads / 32];
@@ -148,14 +179,17 @@ k_act_quant(const uint16_t* __restrict__ x, int K, int Kp, int8_t* __restrict__ 
     const int wpc = (nw + gridDim.x - 1) / gridDim.x;
     const int w0 = c * wpc, w1 = min(w0 + wpc, nw);           // this CTA's share
     constexpr int NR = RV > 0 ? RV : 1;
+    auto col1 = [&](int k) -> float {                         // one column, k < K
+        const float v = bf16_bits_to_f32(__ldg(row + k));
+        return SMOOTH ? v * __ldg(inv_s + k) : v;
+    };
     uint4 keep[NR];
     float mx = 0.f;
-    auto max8 = [&](const uint4& v) {
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    auto max8 = [&](const uint4& v, int k) {
+        float f[8];
+        cols8<SMOOTH>(v, inv_s, k, K, f);
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-            mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w[j] << 16)),
-                                 fabsf(__uint_as_float(w[j] & 0xFFFF0000u))));
+        for (int j = 0; j < 8; ++j) mx = fmaxf(mx, fabsf(f[j]));
     };
     if (vec && RV > 0) {
 #pragma unroll
@@ -164,20 +198,20 @@ k_act_quant(const uint16_t* __restrict__ x, int K, int Kp, int8_t* __restrict__ 
             keep[r] = k < K ? __ldg(reinterpret_cast<const uint4*>(row + k)) : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
-        for (int r = 0; r < NR; ++r) max8(keep[r]);
+        for (int r = 0; r < NR; ++r) max8(keep[r], (r * kActThreads + tid) * 8);
     } else if (vec) {
         for (int k = tid * 8; k < K; k += kActThreads * 8)
-            max8(__ldg(reinterpret_cast<const uint4*>(row + k)));
+            max8(__ldg(reinterpret_cast<const uint4*>(row + k)), k);
     } else if (vec4) {
 #pragma unroll 4
         for (int k = tid * 4; k < K; k += kActThreads * 4) {
-            const uint2 v = __ldg(reinterpret_cast<const uint2*>(row + k));
-            mx = fmaxf(mx, fmaxf(fmaxf(fabsf(__uint_as_float(v.x << 16)), fabsf(__uint_as_float(v.x & 0xFFFF0000u))),
-                                 fmaxf(fabsf(__uint_as_float(v.y << 16)), fabsf(__uint_as_float(v.y & 0xFFFF0000u)))));
+            float f[4];
+            cols4<SMOOTH>(__ldg(reinterpret_cast<const uint2*>(row + k)), inv_s, k, f);
+            mx = fmaxf(mx, fmaxf(fmaxf(fabsf(f[0]), fabsf(f[1])), fmaxf(fabsf(f[2]), fabsf(f[3]))));
         }
     } else {
 #pragma unroll 4
-        for (int k = tid; k < K; k += kActThreads) mx = fmaxf(mx, fabsf(bf16_bits_to_f32(__ldg(row + k))));
+        for (int k = tid; k < K; k += kActThreads) mx = fmaxf(mx, fabsf(col1(k)));
     }
     mx = warp_max(mx);
     if ((tid & 31) == 0) red[tid >> 5] = mx;
@@ -197,12 +231,20 @@ k_act_quant(const uint16_t* __restrict__ x, int K, int Kp, int8_t* __restrict__ 
         if (RV > 0) {
 #pragma unroll
             for (int r = 0; r < NR; ++r, w += kActThreads)
-                if (w >= w0 && w < w1) *reinterpret_cast<uint2*>(out + 8 * w) = quant_s8x8(keep[r], s, rs);
+                if (w >= w0 && w < w1) {
+                    float f[8];
+                    cols8<SMOOTH>(keep[r], inv_s, 8 * w, K, f);
+                    *reinterpret_cast<uint2*>(out + 8 * w) = quant_s8x8(f, s, rs);
+                }
         }
         for (; w < w1; w += kActThreads) {
             if (w < w0) continue;
             uint2 o = make_uint2(0u, 0u);
-            if (8 * w < K) o = quant_s8x8(__ldg(reinterpret_cast<const uint4*>(row + 8 * w)), s, rs);
+            if (8 * w < K) {
+                float f[8];
+                cols8<SMOOTH>(__ldg(reinterpret_cast<const uint4*>(row + 8 * w)), inv_s, 8 * w, K, f);
+                o = quant_s8x8(f, s, rs);
+            }
             *reinterpret_cast<uint2*>(out + 8 * w) = o;
         }
     } else if (vec4) {
@@ -210,11 +252,10 @@ k_act_quant(const uint16_t* __restrict__ x, int K, int Kp, int8_t* __restrict__ 
         for (int k = 8 * w0 + tid * 4; k < 8 * w1; k += kActThreads * 4) {
             uint32_t o = 0u;
             if (k < K && s != 0.f) {
-                const uint2 v = __ldg(reinterpret_cast<const uint2*>(row + k));
-                o = quant_s8(__uint_as_float(v.x << 16), s, rs) |
-                    (quant_s8(__uint_as_float(v.x & 0xFFFF0000u), s, rs) << 8) |
-                    (quant_s8(__uint_as_float(v.y << 16), s, rs) << 16) |
-                    (quant_s8(__uint_as_float(v.y & 0xFFFF0000u), s, rs) << 24);
+                float f[4];
+                cols4<SMOOTH>(__ldg(reinterpret_cast<const uint2*>(row + k)), inv_s, k, f);
+                o = quant_s8(f[0], s, rs) | (quant_s8(f[1], s, rs) << 8) |
+                    (quant_s8(f[2], s, rs) << 16) | (quant_s8(f[3], s, rs) << 24);
             }
             *reinterpret_cast<uint32_t*>(out + k) = o;
         }
@@ -222,10 +263,47 @@ k_act_quant(const uint16_t* __restrict__ x, int K, int Kp, int8_t* __restrict__ 
 #pragma unroll 4
         for (int k = 8 * w0 + tid; k < 8 * w1; k += kActThreads) {
             uint32_t q = 0u;
-            if (k < K && s != 0.f) q = quant_s8(bf16_bits_to_f32(__ldg(row + k)), s, rs);
+            if (k < K && s != 0.f) q = quant_s8(col1(k), s, rs);
             out[k] = (int8_t)(uint8_t)q;
         }
     }
+}
+
+// SmoothQuant calibration, step 1: the largest |value| of every column over
+// the rows, as fp32 bit patterns (non-negative floats order as integers) by
+// atomicMax into `colmax` (zeroed by the caller).  BF16: the values are bf16
+// bits, else fp32.  A block covers 256 columns x 64 rows.
+template <bool BF16>
+__global__ void k_col_absmax(const void* __restrict__ v, int rows, int cols, unsigned* colmax) {
+    const int col = blockIdx.x * 256 + threadIdx.x;
+    const int r0 = blockIdx.y * 64;
+    if (col >= cols) return;
+    unsigned mx = 0u;
+    for (int r = r0; r < min(r0 + 64, rows); ++r) {
+        const float f = BF16 ? bf16_bits_to_f32(static_cast<const uint16_t*>(v)[(size_t)r * cols + col])
+                             : static_cast<const float*>(v)[(size_t)r * cols + col];
+        mx = max(mx, __float_as_uint(fabsf(f)));
+    }
+    atomicMax(colmax + col, mx);
+}
+
+// Step 2: s_j = max|X_j|^alpha / max|W_j|^(1 - alpha) (1 where either
+// maximum is 0) and inv_s_j = fp32(1 / s_j), in place over the two maxima.
+__global__ void k_smooth_factors(float* s_xmax, float* inv_wmax, int cols, float alpha) {
+    const int j = blockIdx.x * blockDim.x + threadIdx.x;
+    if (j >= cols) return;
+    const float xm = s_xmax[j], wm = inv_wmax[j];
+    float sj = 1.f;
+    if (xm > 0.f && wm > 0.f) sj = powf(xm, alpha) / powf(wm, 1.f - alpha);
+    s_xmax[j] = sj;
+    inv_wmax[j] = __fdiv_rn(1.f, sj);
+}
+
+// Step 3: W[n, j] *= s_j (the weights take the activations' outliers).
+__global__ void k_scale_cols(float* W, const float* s, int rows, int cols) {
+    const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (size_t)rows * cols) return;
+    W[i] *= __ldg(s + (i % (size_t)cols));
 }
 
 }  // namespace
@@ -248,8 +326,8 @@ int launch_pack_rtn(const float* W, int N, int K, int G, int symmetric, uint8_t*
     return cudaGetLastError() == cudaSuccess ? W4_OK : W4_ERR_CUDA;
 }
 
-int launch_act_quant(const uint16_t* x, int M, int K, int Kp, int8_t* qx, float* sx,
-                     cudaStream_t stream) {
+int launch_act_quant(const uint16_t* x, const float* inv_s, int M, int K, int Kp, int8_t* qx,
+                     float* sx, cudaStream_t stream) {
     // 16-byte words per thread to hold the row; each CTA quantizes up to
     // 4096 columns
     const int v = (K + kActThreads * 8 - 1) / (kActThreads * 8);
@@ -263,13 +341,40 @@ int launch_act_quant(const uint16_t* x, int M, int K, int Kp, int8_t* qx, float*
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    auto go = [&](auto kern) { return cudaLaunchKernelEx(&cfg, kern, x, inv_s, K, Kp, qx, sx); };
     cudaError_t e;
-    if (v <= 1) e = cudaLaunchKernelEx(&cfg, k_act_quant<1>, x, K, Kp, qx, sx);
-    else if (v <= 2) e = cudaLaunchKernelEx(&cfg, k_act_quant<2>, x, K, Kp, qx, sx);
-    else if (v <= 4) e = cudaLaunchKernelEx(&cfg, k_act_quant<4>, x, K, Kp, qx, sx);
-    else if (v <= 8) e = cudaLaunchKernelEx(&cfg, k_act_quant<8>, x, K, Kp, qx, sx);
-    else e = cudaLaunchKernelEx(&cfg, k_act_quant<0>, x, K, Kp, qx, sx);
+    if (inv_s) {
+        if (v <= 1) e = go(k_act_quant<1, true>);
+        else if (v <= 2) e = go(k_act_quant<2, true>);
+        else if (v <= 4) e = go(k_act_quant<4, true>);
+        else if (v <= 8) e = go(k_act_quant<8, true>);
+        else e = go(k_act_quant<0, true>);
+    } else {
+        if (v <= 1) e = go(k_act_quant<1, false>);
+        else if (v <= 2) e = go(k_act_quant<2, false>);
+        else if (v <= 4) e = go(k_act_quant<4, false>);
+        else if (v <= 8) e = go(k_act_quant<8, false>);
+        else e = go(k_act_quant<0, false>);
+    }
     if (e != cudaSuccess) return W4_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? W4_OK : W4_ERR_CUDA;
+}
+
+int launch_smooth(const uint16_t* X, int T, float* W, int N, int K, float alpha, float* s,
+                  float* inv_s, cudaStream_t stream) {
+    if (cudaMemsetAsync(s, 0, sizeof(float) * (size_t)K, stream) != cudaSuccess ||
+        cudaMemsetAsync(inv_s, 0, sizeof(float) * (size_t)K, stream) != cudaSuccess)
+        return W4_ERR_CUDA;
+    const dim3 gx((K + 255) / 256, (T + 63) / 64), gw((K + 255) / 256, (N + 63) / 64);
+    if (T > 0) k_col_absmax<true><<<gx, 256, 0, stream>>>(X, T, K, reinterpret_cast<unsigned*>(s));
+    k_col_absmax<false><<<gw, 256, 0, stream>>>(W, N, K, reinterpret_cast<unsigned*>(inv_s));
+    k_smooth_factors<<<(K + 255) / 256, 256, 0, stream>>>(s, inv_s, K, alpha);
+    const size_t n = (size_t)N * K;
+    k_scale_cols<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(W, s, N, K);
+    // the next linear may start early under programmatic dependent launch
+    // and read its weights before its dependency wait: end with an ordinary
+    // launch, as w4_pack_rtn does
+    k_stream_fence<<<1, 32, 0, stream>>>();
     return cudaGetLastError() == cudaSuccess ? W4_OK : W4_ERR_CUDA;
 }
 

@@ -93,6 +93,11 @@ int launch_w4a16_gemv(const uint8_t* packed, const GemvArgs& a, const GemvPlan& 
                       cudaStream_t stream);
 int launch_w4a8_gemv(const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
                      cudaStream_t stream);
+// Group-wise W4A8 (one weight scale per group of G columns, G < Kp):
+// G = 32, 64, 128 or a multiple of 256.
+bool w4a8_group_supported(int G);
+int launch_w4a8g_gemv(const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
+                      cudaStream_t stream);
 
 // ---------------------------------------------------------------- prefill
 // Tensor-core kernel for M > 16 (requires K % 8 == 0 and 16-byte aligned x).
@@ -125,7 +130,12 @@ int launch_w4a16_gemm(const uint16_t* x, const uint8_t* packed, const float* sca
 int launch_pack_rtn(const float* W, int N, int K, int G, int symmetric,
                     uint8_t* packed, float* scales, uint8_t* zeros,
                     cudaStream_t stream);
-int launch_act_quant(const uint16_t* x, int M, int K, int Kp, int8_t* qx, float* sx,
-                     cudaStream_t stream);
+// inv_s: SmoothQuant column factors 1/s (nullptr: none).
+int launch_act_quant(const uint16_t* x, const float* inv_s, int M, int K, int Kp, int8_t* qx,
+                     float* sx, cudaStream_t stream);
+// SmoothQuant calibration: s, inv_s [K] from X [T, K] bf16 and W [N, K] fp32,
+// then W *= s per column, in place.
+int launch_smooth(const uint16_t* X, int T, float* W, int N, int K, float alpha, float* s,
+                  float* inv_s, cudaStream_t stream);
 
 }  // namespace w4

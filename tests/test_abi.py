@@ -78,10 +78,12 @@ def test_host_argument_checks(lib):
     assert lib.w4a16_linear(*bad) == c["W4_ERR_INVALID_ARG"]
     bad = list(args); bad[6] = 0             # M = 0: nothing to do
     assert lib.w4a16_linear(*bad) == c["W4_OK"]
-    # w4a8_linear: one group per row, the int32 bound, alignment
+    # w4a8_linear: per row or group-wise groups, the int32 bound, alignment
     a8 = [ok16, ok16, ok16, ok16, None, ok16, None, 1, 64, 64, 64, None, 0, None]
-    bad = list(a8); bad[10] = 32
+    bad = list(a8); bad[9] = 192; bad[10] = 96     # group-wise takes 32/64/128/256k
     assert lib.w4a8_linear(*bad) == c["W4_ERR_UNSUPPORTED_GROUP"]
+    bad = list(a8); bad[10] = 32; bad[6] = ok16    # group-wise has no int32 acc_out
+    assert lib.w4a8_linear(*bad) == c["W4_ERR_INVALID_ARG"]
     big = c["W4_W4A8_MAX_KP"] + 32 - (c["W4_W4A8_MAX_KP"] % 32)
     bad = list(a8); bad[9] = big; bad[10] = big
     assert lib.w4a8_linear(*bad) == c["W4_ERR_K_TOO_LARGE"]
