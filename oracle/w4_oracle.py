@@ -16,6 +16,12 @@ Sources (page title, section):
      must dequantize to zero.
 [P1u] same page, section "量化正确性修正": unpack low and high nibbles
      independently, then interleave.
+[P1g] same page, section "从 RTN 到 GPTQ": H = (2/N) X^T X; a dead column
+     (zero diagonal) has its weights zeroed and H_ii = 1; then
+     H <- H + lambda I, lambda = alpha mean(diag H); H^-1 = U^T U, U upper
+     triangular; column i is quantized to q_i, e_i = (w_i - q_i) / U_ii and
+     W[:, i:] <- W[:, i:] - e_i U[i, i:]; L_pred = 1/2 sum ||w_i - q_i||^2 / U_ii^2.
+     The page's implementation works in FP32.
 [P1a] same page, section "融合INT4反量化与矩阵乘": the additive offset of an
      asymmetric group is (8 - z) s when codes are read as (q - 8).
 [P1f] same page, section "基础": the feed-forward block is
@@ -60,6 +66,12 @@ Readings where the pages are silent (each is also listed in the design notes):
        then the INT8 rule of [P4] on x'.
  (xii) group-wise W4A8: acc_g = sum over the group's columns of
        (code - 8) q_x in integers; y = s_x * sum_g s_W[n, g] acc_g + b.
+ (xiii) GPTQ: a group's parameters are fixed when the loop reaches the
+       group's first column, from the group's current (already updated)
+       weights, by the RTN rule; alpha (the damping ratio) defaults to 0.01;
+       the padded columns K..Kp-1 are dead columns.  The oracle propagates
+       in fp64 and takes every rounding decision by the fp32 rule, from the
+       fp32 value of the current weight.
  (viii) the W4A8 weight scale is max|row|/7 (the symmetric rule of [P1]),
        codes stored as q+8 like W4A16.
  Matmuls are done in fp64 on exactly dequantized weights (s * (code - z) is
@@ -83,6 +95,44 @@ def padded_k(K: int, group_size: int) -> int:
 # Quantise [P1], readings (i), (ii), (iv)-(vi)
 # ---------------------------------------------------------------------------
 
+def rtn_params(R, symmetric: bool):
+    """Group parameters of the last axis of R (fp32 [..., G]), readings
+    (ii), (v), (vi): symmetric s = fp32(max|r| / 7), z = 8 (returned as
+    None); asymmetric s = fp32((rmax - rmin) / 15) over the range widened to
+    hold 0, z = rint(fp32(-rmin / s)) in [0, 15]; an all-zero group has s = 0
+    (and z = 0)."""
+    R = np.asarray(R, dtype=F32)
+    if symmetric:
+        maxabs = np.abs(R).max(axis=-1)             # exact in fp32
+        return (maxabs / F32(7.0)).astype(F32), None
+    rmin = np.minimum(R.min(axis=-1), F32(0.0))     # (v)
+    rmax = np.maximum(R.max(axis=-1), F32(0.0))
+    s = ((rmax - rmin).astype(F32) / F32(15.0)).astype(F32)
+    nz = s != 0
+    s_div = np.where(nz, s, F32(1.0)).astype(F32)
+    z = np.clip(np.rint((-rmin) / s_div), 0, 15).astype(F32)
+    z = np.where(nz, z, F32(0.0)).astype(F32)       # (vi)
+    return s, z
+
+
+def rtn_codes(R, s, z, symmetric: bool):
+    """Codes in [0, 15] of fp32 values R [..., G] under group parameters s
+    (and z) with one entry per group (the last axis of R is the group):
+    symmetric q = clip(rint(fp32(r / s)), -8, 7) + 8, asymmetric
+    q = clip(rint(fp32(fp32(r / s) + z)), 0, 15); 8 or 0 where s = 0."""
+    R = np.asarray(R, dtype=F32)
+    nz = s != 0
+    s_div = np.where(nz, s, F32(1.0)).astype(F32)[..., None]
+    if symmetric:
+        q = np.clip(np.rint((R / s_div).astype(F32)), -8, 7)   # fp32 r/s, then rint (i)
+        q = np.where(nz[..., None], q, 0)
+        return (q + 8).astype(np.uint8)
+    t = ((R / s_div).astype(F32) + z[..., None]).astype(F32)  # fp32 add
+    q = np.clip(np.rint(t), 0, 15)
+    q = np.where(nz[..., None], q, 0)
+    return q.astype(np.uint8)
+
+
 def rtn_quantize(W, group_size: int, symmetric: bool):
     """Round-to-nearest INT4 quantisation of W [N, K] (fp32).
 
@@ -96,30 +146,9 @@ def rtn_quantize(W, group_size: int, symmetric: bool):
     Wp = np.zeros((N, Kp), dtype=F32)
     Wp[:, :K] = W                                   # (iv) pads are zeros
     R = Wp.reshape(N, Ng, G)
-    if symmetric:
-        maxabs = np.abs(R).max(axis=2)              # exact in fp32
-        s = (maxabs / F32(7.0)).astype(F32)         # (ii) one fp32 division
-        nz = s != 0
-        s_div = np.where(nz, s, F32(1.0)).astype(F32)
-        q = np.rint(R / s_div[:, :, None])          # fp32 r/s, then rint (i)
-        q = np.clip(q, -8, 7)
-        q = np.where(nz[:, :, None], q, 0)          # (vi)
-        codes = (q + 8).astype(np.uint8)            # stored code = q + 8
-        zeros = None
-    else:
-        rmin = np.minimum(R.min(axis=2), F32(0.0))  # (v)
-        rmax = np.maximum(R.max(axis=2), F32(0.0))
-        s = ((rmax - rmin).astype(F32) / F32(15.0)).astype(F32)
-        nz = s != 0
-        s_div = np.where(nz, s, F32(1.0)).astype(F32)
-        z = np.clip(np.rint((-rmin) / s_div), 0, 15).astype(F32)
-        z = np.where(nz, z, F32(0.0)).astype(F32)   # (vi)
-        t = (R / s_div[:, :, None]).astype(F32) + z[:, :, None]   # fp32 add
-        q = np.clip(np.rint(t.astype(F32)), 0, 15)
-        q = np.where(nz[:, :, None], q, 0)
-        codes = q.astype(np.uint8)
-        zeros = z.astype(np.uint8)
-    return codes.reshape(N, Kp), s.astype(F32), zeros
+    s, z = rtn_params(R, symmetric)
+    codes = rtn_codes(R, s, z, symmetric)
+    return codes.reshape(N, Kp), s, None if symmetric else z.astype(np.uint8)
 
 
 # ---------------------------------------------------------------------------
@@ -260,6 +289,68 @@ def w4a16_linear_swiglu(x, packed, scales, zeros, bias, F: int, K: int,
     g = w4a16_linear(x, packed, scales, zeros, bias, K, group_size, rows=g_idx)
     u = w4a16_linear(x, packed, scales, zeros, bias, K, group_size, rows=u_idx)
     return silu_f64(g) * u
+
+
+# ---------------------------------------------------------------------------
+# GPTQ [P1g], reading (xiii)
+# ---------------------------------------------------------------------------
+
+def gptq_hessian(X, Kp: int):
+    """H = (2 / T) X^T X in fp64 for calibration activations X [T, K]
+    (bf16 values), padded with zero columns to Kp."""
+    Xd = bf16_to_f64(X)
+    T, K = Xd.shape
+    Xp = np.zeros((T, Kp))
+    Xp[:, :K] = Xd
+    return (2.0 / T) * (Xp.T @ Xp)
+
+
+def gptq_quantize(W, X, group_size: int, symmetric: bool, damp: float = 0.01):
+    """GPTQ of W [N, K] (fp32) with calibration X [T, K] (bf16 values), in
+    the page's order: Hessian, dead columns, damping, U with H^-1 = U^T U,
+    then column by column quantize, normalise the error and update the
+    remaining columns.  Library primitives: the fp64 inverse and Cholesky.
+
+    Returns (codes uint8 [N, Kp], scales fp32 [N, Ng], zeros uint8 [N, Ng]
+    or None, loss fp64 [N] (L_pred per row), Hd fp64 [Kp, Kp] the damped
+    Hessian that was factorized, W0 fp64 [N, Kp] the weights after the
+    dead-column step)."""
+    W = np.asarray(W, dtype=F32)
+    N, K = W.shape
+    G = int(group_size)
+    Kp = padded_k(K, G)
+    Ng = Kp // G
+    Wc = np.zeros((N, Kp))
+    Wc[:, :K] = W
+    H = gptq_hessian(X, Kp)
+    dead = np.diag(H) == 0
+    H[dead, dead] = 1.0
+    Wc[:, dead] = 0.0
+    H = H + damp * np.mean(np.diag(H)) * np.eye(Kp)
+    U = np.linalg.cholesky(np.linalg.inv(H)).T      # H^-1 = L L^T, U = L^T
+    W0 = Wc.copy()
+    codes = np.zeros((N, Kp), dtype=np.uint8)
+    scales = np.zeros((N, Ng), dtype=F32)
+    zeros = None if symmetric else np.zeros((N, Ng), dtype=np.uint8)
+    loss = np.zeros(N)
+    for i in range(Kp):
+        g = i // G
+        if i % G == 0:                               # (xiii) the group's parameters
+            sg, zg = rtn_params(Wc[:, i:i + G].astype(F32), symmetric)
+            scales[:, g] = sg
+            if not symmetric:
+                zeros[:, g] = zg.astype(np.uint8)
+        sg = scales[:, g]
+        zg = None if symmetric else zeros[:, g].astype(F32)
+        c = rtn_codes(Wc[:, i:i + 1].astype(F32), sg, zg, symmetric)[:, 0]
+        codes[:, i] = c
+        zq = 8.0 if symmetric else zg.astype(np.float64)
+        q = sg.astype(np.float64) * (c.astype(np.float64) - zq)     # dequantized q_i
+        d = Wc[:, i] - q
+        loss += 0.5 * d * d / U[i, i] ** 2
+        e = d / U[i, i]
+        Wc[:, i:] -= np.outer(e, U[i, i:])
+    return codes, scales, zeros, loss, H, W0
 
 
 # ---------------------------------------------------------------------------

@@ -586,3 +586,87 @@ def test_smoothed_act_quant_with_power_of_two_factors():
     q3, s3 = O.w4a8_quantize_act(x, 64, inv_s=inv)
     q4, s4 = O.w4a8_quantize_act(_bf16_round(x * inv), 64)
     assert np.array_equal(q3, q4) and np.array_equal(s3, s4)
+
+
+# ---------------------------------------------------------------------------
+# GPTQ ("Lab 5: Gemma4 端到端推理优化", section 从 RTN 到 GPTQ)
+# ---------------------------------------------------------------------------
+
+def _dequant(codes, scales, zeros, G):
+    N, Kp = codes.shape
+    z = np.full((N, Kp // G), 8.0) if zeros is None else zeros.astype(np.float64)
+    return (scales.astype(np.float64)[:, :, None]
+            * (codes.reshape(N, Kp // G, G).astype(np.float64) - z[:, :, None])).reshape(N, Kp)
+
+
+def _hadamard(n):
+    h = np.ones((1, 1))
+    while h.shape[0] < n:
+        h = np.block([[h, h], [h, -h]])
+    return h
+
+
+@pytest.mark.parametrize("symmetric,G", [(True, 32), (False, 32), (True, 64)])
+def test_gptq_loss_identity(symmetric, G):
+    """The accumulated L_pred equals 1/2 (w0 - w_hat)^T H (w0 - w_hat) for
+    every row: w0 - w_hat = U^T e and U H U^T = I, so the identity holds
+    exactly for any codes, and breaks if the update, its sign, the row of U
+    or the normalisation is wrong."""
+    rng = np.random.default_rng(7)
+    N, K, T = 12, 96, 80
+    A = rng.standard_normal((K, K)) * 0.3 + np.eye(K)
+    X = _bf16_round((rng.standard_normal((T, K)) @ A).astype(np.float32))
+    W = _rand_w(N, K, 8, std=0.2)
+    codes, scales, zeros, loss, Hd, W0 = O.gptq_quantize(W, X, G, symmetric)
+    D = W0 - _dequant(codes, scales, zeros, G)
+    quad = 0.5 * np.einsum("nk,kj,nj->n", D, Hd, D)
+    assert np.allclose(loss, quad, rtol=1e-9, atol=0)
+
+
+def test_gptq_with_isotropic_hessian_is_rtn():
+    """X a Hadamard matrix (entries +-1, exact in bf16): H = c I, U is
+    diagonal, nothing propagates, and GPTQ gives the RTN codes."""
+    K = 64
+    X = _hadamard(K).astype(np.float32)
+    for symmetric in (True, False):
+        W = _rand_w(10, K, 3, std=0.2)
+        codes, scales, zeros, _, _, _ = O.gptq_quantize(W, X, 32, symmetric)
+        rc, rs, rz = O.rtn_quantize(W, 32, symmetric)
+        assert np.array_equal(codes, rc) and np.array_equal(scales, rs)
+        if not symmetric:
+            assert np.array_equal(zeros, rz)
+
+
+def test_gptq_dead_columns_and_padding():
+    """A channel that is zero in every calibration token, and the padded
+    columns, have their weights zeroed and dequantize to exactly 0."""
+    rng = np.random.default_rng(4)
+    N, K, T, G = 6, 80, 64, 32                         # Kp = 96: 16 padded columns
+    X = _bf16_round(rng.standard_normal((T, K)).astype(np.float32))
+    X[:, 5] = 0.0
+    W = _rand_w(N, K, 9, std=0.2)
+    for symmetric in (True, False):
+        codes, scales, zeros, loss, Hd, W0 = O.gptq_quantize(W, X, G, symmetric)
+        Wq = _dequant(codes, scales, zeros, G)
+        assert np.all(W0[:, 5] == 0) and np.all(Wq[:, 5] == 0)
+        assert np.all(Wq[:, K:] == 0)
+        lam = 0.01 * np.mean(np.diag(Hd)) / 1.01        # diag(Hd) = diag(H) + lam
+        assert abs(Hd[5, 5] - (1.0 + lam)) < 1e-12       # dead: H_55 = 1 before damping
+        assert np.all(np.isfinite(loss))
+
+
+def test_gptq_beats_rtn_on_the_calibration_objective():
+    """||X (W - W_hat)^T||_F is lower than RTN's for correlated activations."""
+    rng = np.random.default_rng(21)
+    N, K, T = 32, 128, 256
+    A = rng.standard_normal((K, K)) * 0.5 + np.eye(K)
+    X = _bf16_round((rng.standard_normal((T, K)) @ A).astype(np.float32))
+    W = _rand_w(N, K, 22, std=0.05)
+    Xd = X.astype(np.float64)
+    for symmetric, G in ((True, 32), (False, 128)):
+        codes, scales, zeros, _, _, _ = O.gptq_quantize(W, X, G, symmetric)
+        rc, rs, rz = O.rtn_quantize(W, G, symmetric)
+        err = lambda Wq: np.linalg.norm(Xd @ (W.astype(np.float64) - Wq[:, :K]).T)
+        g_err = err(_dequant(codes, scales, zeros, G))
+        r_err = err(_dequant(rc, rs, rz, G))
+        assert g_err < 0.8 * r_err, (g_err, r_err)
