@@ -582,6 +582,26 @@ def measure_moe(w4, hbm, reps=100):
     return out
 
 
+def measure_gptq(w4, reps=3):
+    """GPTQ of the 7B fused QKV projection (4608 x 3584, G = 128,
+    symmetric) from 512 calibration tokens, on the device: Hessian, Cholesky,
+    triangular inverse, the column loop and packing, per layer."""
+    g = torch.Generator().manual_seed(9)
+    N, K, T, G = 4608, 3584, 512, 128
+    X = torch.randn(T, K, generator=g).to(torch.bfloat16).cuda()
+    W = (torch.randn(N, K, generator=g) * 0.02).cuda()
+    w4.w4_gptq(X, W, G, True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        w4.w4_gptq(X, W, G, True)
+    e1.record()
+    torch.cuda.synchronize()
+    return {"workload": f"GPTQ {N}x{K}, G={G}, {T} calibration tokens",
+            "ms_per_layer": round(e0.elapsed_time(e1) / reps, 2)}
+
+
 def run_ours(args, world, rank):
     import int4_weight_only_gb300 as w4
     from int4_weight_only_gb300 import build as b
@@ -641,6 +661,7 @@ def run_ours(args, world, rank):
         res["decode_12b"] = measure_decode_12b(w4, hbm)
         res["swiglu_7b"] = measure_swiglu(w4, hbm)
         res["moe_decode"] = measure_moe(w4, hbm)
+        res["gptq"] = measure_gptq(w4)
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline_decode(lins)
     return res

@@ -73,6 +73,9 @@ extern "C" {
 #define W4_ERR_DEVICE_TIMEOUT      -9  /* a kernel's bounded wait ran out     */
 #define W4_ERR_SCRATCH_LIMIT      -10  /* shape needs more split-K scratch than
                                           W4_NOALLOC_SCRATCH_BYTES            */
+#define W4_ERR_NOT_SPD            -12  /* device flag: w4_gptq met a non-positive
+                                          pivot (damped Hessian not positive
+                                          definite in fp32); results unreliable */
 #define W4_ERR_GROUP_TOKENS       -11  /* device flag: a group's offsets were
                                           invalid or it had more tokens than
                                           max_group_tokens; its rows of y were
@@ -225,6 +228,31 @@ W4_API int w4a16_grouped_linear(const uint16_t* x, const int32_t* goff, const ui
                                 const float* scales, const uint8_t* zeros, const float* bias,
                                 uint16_t* y, int T, int E, int N, int K, int group_size,
                                 int symmetric, int max_group_tokens, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * w4_gptq - GPTQ quantization of one linear layer on the GPU, in FP32
+ * ("Lab 5: Gemma4 端到端推理优化", section 从 RTN 到 GPTQ):
+ *  H = (2/T) X^T X; a dead column (H_jj = 0, also every padded column
+ *  K..Kp-1) gets W[:, j] = 0 and H_jj = 1; H += damp * mean(diag H) I;
+ *  H^-1 = U^T U (U upper); then for each column i in order: the group's
+ *  parameters, when i is its first column, from its current weights by the
+ *  rule of w4_pack_rtn; q_i by that rule; e_i = (w_i - q_i) / U_ii;
+ *  W[:, i:] -= e_i U[i, i:];  loss[n] = 1/2 sum_i (w_i - q_i)^2 / U_ii^2.
+ *
+ *  X        [T, K] bf16 calibration activations, T >= 1.
+ *  W        [N, K] fp32 weights (read only).
+ *  group_size, symmetric: as for w4_pack_rtn; damp >= 0 (0.01 typical).
+ *  packed [N, Kp/2], scales [N, Ng], zeros [N, Ng] (asymmetric, else NULL):
+ *           out, the w4_pack_rtn layout.
+ *  loss     [N] fp32 out (L_pred per row).
+ *  workspace: w4_gptq_workspace_bytes(N, K, group_size) bytes, 256-byte
+ *           aligned; its contents need no initialisation.
+ *  A non-positive Cholesky pivot sets W4_ERR_NOT_SPD in the device flag.
+ * ------------------------------------------------------------------------- */
+W4_API size_t w4_gptq_workspace_bytes(int N, int K, int group_size);
+W4_API int w4_gptq(const uint16_t* X, int T, const float* W, int N, int K, int group_size,
+                   int symmetric, float damp, uint8_t* packed, float* scales, uint8_t* zeros,
+                   float* loss, void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
  * w4a8_quantize_act - per-token dynamic INT8 activations ([ORIN]):

@@ -28,6 +28,9 @@ _SIGS = {
     "w4a8_quantize_act": (_c_int, [_vp, _c_int, _c_int, _c_int, _vp, _vp, _vp]),
     "w4a8_quantize_act_smooth": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _vp]),
     "w4_smooth": (_c_int, [_vp, _c_int, _vp, _c_int, _c_int, ctypes.c_float, _vp, _vp, _vp]),
+    "w4_gptq_workspace_bytes": (_c_size, [_c_int, _c_int, _c_int]),
+    "w4_gptq": (_c_int, [_vp, _c_int, _vp, _c_int, _c_int, _c_int, _c_int, ctypes.c_float, _vp,
+                         _vp, _vp, _vp, _vp, _c_size, _vp]),
     "w4a8_workspace_bytes": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
     "w4a8_linear": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
                              _vp, _c_size, _vp]),
@@ -360,6 +363,34 @@ def w4_smooth(X: torch.Tensor, W: torch.Tensor, alpha: float = 0.5, stream=None)
     _check("w4_smooth", load().w4_smooth(_ptr(X), T, _ptr(W), N, K, float(alpha), _ptr(s),
                                          _ptr(inv_s), _stream(W, stream)))
     return s, inv_s
+
+
+def w4_gptq(X: torch.Tensor, W: torch.Tensor, group_size: int, symmetric: bool,
+            damp: float = 0.01, stream=None):
+    """GPTQ of W [N, K] fp32 with calibration X [T, K] bf16 -> (packed
+    [N, Kp/2] u8, scales [N, Ng] f32, zeros [N, Ng] u8 or None, loss [N] f32)."""
+    T, K = X.shape
+    N = W.shape[0]
+    _need(X, torch.bfloat16, (T, K), "X")
+    _need(W, torch.float32, (N, K), "W")
+    Kp = padded_k(K, group_size)
+    Ng = Kp // group_size
+    dev = W.device
+    packed = torch.empty(N, Kp // 2, dtype=torch.uint8, device=dev)
+    scales = torch.empty(N, Ng, dtype=torch.float32, device=dev)
+    zeros = None if symmetric else torch.empty(N, Ng, dtype=torch.uint8, device=dev)
+    loss = torch.empty(N, dtype=torch.float32, device=dev)
+    lib = load()
+    nbytes = lib.w4_gptq_workspace_bytes(N, K, int(group_size))
+    wsv = None                  # no size: the call reports why (group, shape)
+    if nbytes:
+        ws = torch.empty(nbytes + 256, dtype=torch.uint8, device=dev)
+        off = (-ws.data_ptr()) % 256
+        wsv = ws[off:off + nbytes]
+    _check("w4_gptq", lib.w4_gptq(_ptr(X), T, _ptr(W), N, K, int(group_size),
+                                  1 if symmetric else 0, float(damp), _ptr(packed), _ptr(scales),
+                                  _ptr(zeros), _ptr(loss), _ptr(wsv), nbytes, _stream(W, stream)))
+    return packed, scales, zeros, loss
 
 
 def w4a8_linear(qx: torch.Tensor, sx: torch.Tensor, packed: torch.Tensor,

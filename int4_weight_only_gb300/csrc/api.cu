@@ -299,6 +299,35 @@ int w4a16_grouped_linear(const uint16_t* x, const int32_t* goff, const uint8_t* 
     return launch_w4a16_grouped(packed, a, p, static_cast<cudaStream_t>(stream));
 }
 
+size_t w4_gptq_workspace_bytes(int N, int K, int group_size) {
+    if (N <= 0 || check_group(K, group_size)) return 0;
+    const long long Kp = padded_k(K, group_size);
+    if (Kp > 65536) return 0;
+    return gptq_workspace_bytes(N, (int)Kp, gptq_block_cols(group_size));
+}
+
+int w4_gptq(const uint16_t* X, int T, const float* W, int N, int K, int group_size,
+            int symmetric, float damp, uint8_t* packed, float* scales, uint8_t* zeros,
+            float* loss, void* workspace, size_t workspace_bytes, void* stream) {
+    if (!X || !W || !packed || !scales || !loss) return W4_ERR_NULL_PTR;
+    if (symmetric && zeros) return W4_ERR_INVALID_ARG;
+    if (!symmetric && !zeros) return W4_ERR_NULL_PTR;
+    if (T < 1 || N <= 0 || !(damp >= 0.f)) return W4_ERR_INVALID_ARG;
+    int rc = check_group(K, group_size);
+    if (rc) return rc;
+    const long long Kp = padded_k(K, group_size);
+    if (Kp > 65536) return W4_ERR_UNSUPPORTED_SHAPE;      // two Kp x Kp fp32 matrices
+    if (!workspace || workspace_bytes < w4_gptq_workspace_bytes(N, K, group_size))
+        return W4_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255) || !aligned4(W) || !aligned4(scales) ||
+        !aligned4(loss) || (reinterpret_cast<uintptr_t>(X) & 1))
+        return W4_ERR_MISALIGNED;
+    int* err = device_error_flag();
+    if (!err) return W4_ERR_CUDA;
+    return launch_gptq(X, T, W, N, K, (int)Kp, group_size, symmetric, damp, packed, scales, zeros,
+                       loss, workspace, err, static_cast<cudaStream_t>(stream));
+}
+
 int w4a8_quantize_act(const uint16_t* x, int M, int K, int group_size, int8_t* qx,
                       float* sx, void* stream) {
     if (!x || !qx || !sx) return W4_ERR_NULL_PTR;
@@ -413,6 +442,8 @@ const char* w4_error_string(int code) {
         case W4_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait timed out";
         case W4_ERR_SCRATCH_LIMIT:
             return "shape needs more split-K scratch than W4_NOALLOC_SCRATCH_BYTES";
+        case W4_ERR_NOT_SPD:
+            return "GPTQ met a non-positive Cholesky pivot (damped Hessian not positive definite)";
         case W4_ERR_GROUP_TOKENS:
             return "a group's offsets were invalid or it had more tokens than max_group_tokens";
         default: return "unknown error code";

@@ -133,6 +133,13 @@ int launch_pack_rtn(const float* W, int N, int K, int G, int symmetric,
 // inv_s: SmoothQuant column factors 1/s (nullptr: none).
 int launch_act_quant(const uint16_t* x, const float* inv_s, int M, int K, int Kp, int8_t* qx,
                      float* sx, cudaStream_t stream);
+// GPTQ (gptq.cu): column block width for a group size, workspace bytes,
+// and the whole quantizer (Hessian .. packed codes) on one stream.
+int gptq_block_cols(int G);
+size_t gptq_workspace_bytes(int N, int Kp, int B);
+int launch_gptq(const uint16_t* X, int T, const float* W, int N, int K, int Kp, int G,
+                int symmetric, float damp, uint8_t* packed, float* scales, uint8_t* zeros,
+                float* loss, void* ws, int* err, cudaStream_t st);
 // SmoothQuant calibration: s, inv_s [K] from X [T, K] bf16 and W [N, K] fp32,
 // then W *= s per column, in place.
 int launch_smooth(const uint16_t* X, int T, float* W, int N, int K, float alpha, float* s,
