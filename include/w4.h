@@ -76,10 +76,9 @@ extern "C" {
 #define W4_ERR_NOT_SPD            -12  /* device flag: w4_gptq met a non-positive
                                           pivot (damped Hessian not positive
                                           definite in fp32); results unreliable */
-#define W4_ERR_GROUP_TOKENS       -11  /* device flag: a group's offsets were
-                                          invalid or it had more tokens than
-                                          max_group_tokens; its rows of y were
-                                          not written                         */
+#define W4_ERR_GROUP_TOKENS       -11  /* device flag: a group's token offsets
+                                          were invalid; its rows of y were not
+                                          written                             */
 
 /* Size of the library's built-in split-K scratch used by
  * w4a16_linear_noalloc (4 MiB, held by every GPU that loads the library).  */
@@ -216,18 +215,21 @@ W4_API int w4a16_linear_swiglu(const uint16_t* x, const uint8_t* packed, const f
  *  scales    [E, N, Ng] fp32;  zeros [E, N, Ng] uint8 or NULL (symmetric);
  *  bias      [E, N] fp32 or NULL.
  *  y         [T, N] bf16 out.
- *  max_group_tokens  bound on goff[e+1] - goff[e], 1..16.  A group above it,
- *            or offsets outside [0, T] or decreasing, is skipped (its rows of y
- *            are left as they were) and sets W4_ERR_GROUP_TOKENS in the
- *            device flag that w4_get_device_error returns.
- *  Groups without tokens cost nothing: the units of work are (group with
- *  tokens, row block), listed on the device.  E <= 32767, E * N < 2^31.
+ *  tile_tokens  tokens per pass, 1..16 (the token tile of the kernel: 8 or
+ *            16 wide).  A group with more tokens is taken in
+ *            ceil(count / tile_tokens) passes, each reading its weights; the
+ *            best tile is the largest count of a group when that is <= 16.
+ *  A group whose offsets lie outside [0, T] or decrease is skipped (its rows
+ *  of y are left as they were) and sets W4_ERR_GROUP_TOKENS in the device
+ *  flag that w4_get_device_error returns.  Groups without tokens cost
+ *  nothing: the units of work are ((group, token tile), row block), listed
+ *  on the device.  E <= 32767, E * N < 2^31, T / tile_tokens < 65536.
  *  No workspace (grouped plans do not split K).
  * ------------------------------------------------------------------------- */
 W4_API int w4a16_grouped_linear(const uint16_t* x, const int32_t* goff, const uint8_t* packed,
                                 const float* scales, const uint8_t* zeros, const float* bias,
                                 uint16_t* y, int T, int E, int N, int K, int group_size,
-                                int symmetric, int max_group_tokens, void* stream);
+                                int symmetric, int tile_tokens, void* stream);
 
 /* ---------------------------------------------------------------------------
  * w4_gptq - GPTQ quantization of one linear layer on the GPU, in FP32

@@ -257,11 +257,12 @@ def w4a16_linear_swiglu(x: torch.Tensor, packed: torch.Tensor, scales: torch.Ten
 def w4a16_grouped_linear(x: torch.Tensor, goff: torch.Tensor, packed: torch.Tensor,
                          scales: torch.Tensor, zeros: Optional[torch.Tensor],
                          bias: Optional[torch.Tensor], E: int, N: int, K: int, group_size: int,
-                         max_group_tokens: int, y=None, stream=None) -> torch.Tensor:
+                         tile_tokens: int, y=None, stream=None) -> torch.Tensor:
     """Grouped W4A16 linear: rows goff[e] .. goff[e+1]-1 of x [T, K] (sorted
     by group) times group e's matrix -> the same rows of y [T, N].  packed /
     scales / zeros / bias hold the E groups stacked ([E*N, ...] or [E, N, ...]);
-    goff is an int32 CUDA tensor [E+1]."""
+    goff is an int32 CUDA tensor [E+1]; groups are taken in passes of at
+    most tile_tokens (1..16) tokens."""
     T = x.shape[0]
     _need(x, torch.bfloat16, (T, K), "x")
     Kp = padded_k(K, group_size)
@@ -285,7 +286,7 @@ def w4a16_grouped_linear(x: torch.Tensor, goff: torch.Tensor, packed: torch.Tens
     lib = load()
     _check("w4a16_grouped_linear", lib.w4a16_grouped_linear(
         _ptr(x), _ptr(goff), _ptr(packed), _ptr(scales), _ptr(zeros), _ptr(bias), _ptr(y),
-        T, E, N, K, int(group_size), 1 if zeros is None else 0, int(max_group_tokens),
+        T, E, N, K, int(group_size), 1 if zeros is None else 0, int(tile_tokens),
         _stream(x, stream)))
     return y
 

@@ -265,12 +265,13 @@ int w4a16_linear_swiglu(const uint16_t* x, const uint8_t* packed, const float* s
 int w4a16_grouped_linear(const uint16_t* x, const int32_t* goff, const uint8_t* packed,
                          const float* scales, const uint8_t* zeros, const float* bias,
                          uint16_t* y, int T, int E, int N, int K, int group_size, int symmetric,
-                         int max_group_tokens, void* stream) {
+                         int tile_tokens, void* stream) {
     if (!x || !goff || !packed || !scales || !y) return W4_ERR_NULL_PTR;
     if (symmetric && zeros) return W4_ERR_INVALID_ARG;
     if (!symmetric && !zeros) return W4_ERR_NULL_PTR;
-    if (T < 0 || E <= 0 || E > 32767 || N <= 0 || max_group_tokens < 1 || max_group_tokens > 16)
+    if (T < 0 || E <= 0 || E > 32767 || N <= 0 || tile_tokens < 1 || tile_tokens > 16)
         return W4_ERR_INVALID_ARG;
+    if (T / tile_tokens >= 65536) return W4_ERR_UNSUPPORTED_SHAPE;   // tile index: 16 bits
     if ((long long)E * N > 0x7fffffffLL) return W4_ERR_UNSUPPORTED_SHAPE;
     int rc = check_group(K, group_size);
     if (rc) return rc;
@@ -281,11 +282,12 @@ int w4a16_grouped_linear(const uint16_t* x, const int32_t* goff, const uint8_t* 
         (reinterpret_cast<uintptr_t>(y) & 1))
         return W4_ERR_MISALIGNED;
     if (T == 0) return W4_OK;
-    // plan for the rows of the groups that can have tokens (at most T of them)
-    const int active = std::min(E, T);
-    const long long n_eff = std::min((long long)active * N, 0x7fffffffLL);
+    // at most E + T / tile items (each has a token); plan for their rows
+    const long long items = std::min<long long>(T, (long long)E + (T + tile_tokens - 1) / tile_tokens);
+    const long long n_eff = std::min(items * N, 0x7fffffffLL);
+    const int cap = (int)((long long)E + (T + tile_tokens - 1) / tile_tokens);
     GemvPlan p;
-    if (!plan_gemv(max_group_tokens, (int)n_eff, (int)Kp, group_size, 2, current_sm_count(), &p, E))
+    if (!plan_gemv(tile_tokens, (int)n_eff, (int)Kp, group_size, 2, current_sm_count(), &p, cap))
         return W4_ERR_UNSUPPORTED_SHAPE;
     GemvArgs a{};
     a.x = x; a.scales = scales; a.zeros = zeros; a.bias = bias; a.y = y;
@@ -294,8 +296,9 @@ int w4a16_grouped_linear(const uint16_t* x, const int32_t* goff, const uint8_t* 
     a.M = T; a.N = N; a.K = K; a.Kp = (int)Kp; a.G = group_size; a.Ng = (int)(Kp / group_size);
     a.R = p.R; a.SKE = p.SKE; a.nst = p.nst; a.S = 1; a.spl = p.spl; a.units = p.units;
     a.XS = p.XS; a.red = p.red;
-    a.goff = goff; a.E = E; a.gmax = max_group_tokens; a.NBg = (N + p.R - 1) / p.R;
+    a.goff = goff; a.E = E; a.gmax = tile_tokens; a.NBg = (N + p.R - 1) / p.R;
     a.list_off = (int)p.list_off;
+    a.list_cap = cap;
     return launch_w4a16_grouped(packed, a, p, static_cast<cudaStream_t>(stream));
 }
 
@@ -445,7 +448,7 @@ const char* w4_error_string(int code) {
         case W4_ERR_NOT_SPD:
             return "GPTQ met a non-positive Cholesky pivot (damped Hessian not positive definite)";
         case W4_ERR_GROUP_TOKENS:
-            return "a group's offsets were invalid or it had more tokens than max_group_tokens";
+            return "a group's token offsets were invalid (outside [0, T] or decreasing)";
         default: return "unknown error code";
     }
 }

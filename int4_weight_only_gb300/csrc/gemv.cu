@@ -56,8 +56,9 @@ bool plan_gemv_search(int M, int N, int Kp, int G, int act_bytes, int sm_count, 
     const int red = act_bytes == 2
         ? CW * 32 * ((M > 8 ? 2 : 1) * 4) * 4
         : CW * 32 * (M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16) * 2 * 4;
-    // grouped plans keep a list of active group ids (int16) after the activations
-    const size_t list_bytes = groups > 0 ? (((size_t)groups * 2 + 15) & ~(size_t)15) : 0;
+    // grouped plans keep a list of (group, token tile) items (int32) after the
+    // activations; `groups` is its capacity
+    const size_t list_bytes = groups > 0 ? (((size_t)groups * 4 + 15) & ~(size_t)15) : 0;
     const size_t fixed = 1024 + (size_t)NS * STAGE_BYTES + kCtlBytes + red + list_bytes;
     // W4A16 also keeps four floats per token and segment of cpg*32 columns
     auto xseg_bytes = [&](int slice) -> size_t {

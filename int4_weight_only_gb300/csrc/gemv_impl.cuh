@@ -65,8 +65,8 @@ struct SmemCtl {
     int sumq[16];          // W4A8: sum of q_x over the slice, per token
     uint64_t xfull;        // activation slice landed (TMA staging)
     uint64_t xempty;       // consumers released the activation buffer
-    uint64_t listready;    // grouped: the active-group list is written
-    int nact;              // grouped: number of active groups
+    uint64_t listready;    // grouped: the (group, token tile) list is written
+    int nact;              // grouped: number of items in it
 };
 constexpr int kCtlBytes = 256;
 static_assert(sizeof(SmemCtl) <= kCtlBytes, "control block");
@@ -107,8 +107,9 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int c
 }
 
 // Producer: one thread streams every stage of every unit of this CTA.
-// GROUPED: units are (active group, row block) in the order of the list the
-// consumers build after the dependency wait; rows of group e start at e * N.
+// GROUPED: units are ((group, token tile) item, row block) in the order of
+// the list the consumers build after the dependency wait; rows of group e
+// start at e * N.
 template <bool GROUPED = false>
 __device__ void gemv_producer(const CUtensorMap* tm, uint8_t* wbuf, uint8_t* xbuf,
                               SmemCtl* ctl, const GemvArgs& a) {
@@ -140,12 +141,12 @@ __device__ void gemv_producer(const CUtensorMap* tm, uint8_t* wbuf, uint8_t* xbu
     }
     grid_dep_wait();
     int units = a.units;
-    const int16_t* glist = nullptr;
+    const int* glist = nullptr;
     if constexpr (GROUPED) {
         // which groups have tokens is known only after the wait
         if (!mbar_wait(&ctl->listready, 0, &ctl->abort, a.err)) return;   // nothing issued yet
         units = ctl->nact * a.NBg;
-        glist = reinterpret_cast<const int16_t*>(wbuf + a.list_off);
+        glist = reinterpret_cast<const int*>(wbuf + a.list_off);
     }
     // GROUPED: each CTA takes a contiguous run of units, so that successive
     // units mostly share a group and its staged activations
@@ -164,7 +165,7 @@ __device__ void gemv_producer(const CUtensorMap* tm, uint8_t* wbuf, uint8_t* xbu
             const int gi = u / a.NBg;
             rb = u - gi * a.NBg;
             s = 0; ks0 = 0; ks1 = a.nst;
-            row = (int)glist[gi] * a.N + rb * a.R;
+            row = (glist[gi] & 0xFFFF) * a.N + rb * a.R;
         } else {
             unit_coords(u, a, rb, s, ks0, ks1);
             row = rb * a.R;
@@ -432,10 +433,11 @@ __device__ __forceinline__ bool split_k_arrive(const GemvArgs& a, SmemCtl* ctl, 
 // GROUPED: a grouped linear over E groups (experts): group e multiplies its
 // own tokens, rows goff[e] .. goff[e+1] - 1 of x, by its own N x K matrix
 // (rows e * N .. e * N + N - 1 of the stacked weights) into the same rows
-// of y.  After the dependency wait every CTA lists the groups that have
-// tokens (in group order) and takes a contiguous run of the (active group,
-// row block) units; a group whose offsets are invalid or whose token count
-// exceeds gmax is left out and raises W4_ERR_GROUP_TOKENS.
+// of y.  After the dependency wait every CTA lists the (group, token tile)
+// items, tiles of at most gmax tokens, in group order (a block-wide prefix
+// sum of the groups' tile counts), and takes a contiguous run of the
+// (item, row block) units; a group whose offsets are invalid is left out
+// and raises W4_ERR_GROUP_TOKENS.  Item = group | tile << 16.
 template <int NT, int CPG, bool ASYM, bool SPLIT, bool SWIGLU = false, bool GROUPED = false>
 __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
     static_assert(!(GROUPED && (SPLIT || SWIGLU)), "grouped plans are unsplit, plain epilogue");
@@ -490,42 +492,56 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
     uint32_t it = 0, xi = 0;
     int prev0 = -1, prev1 = -1;
     bool waited = false;
-    const int16_t* glist = nullptr;
-    int prev_g = -1;
+    const int* glist = nullptr;
+    int prev_item = -1;
     if constexpr (GROUPED) {
-        // groups with tokens, in group order (the same list in every CTA)
+        // (group, token tile) items in group order, the same list in every CTA
         grid_dep_wait();
         waited = true;
-        int16_t* list = reinterpret_cast<int16_t*>(sm.wbuf + a.list_off);
+        int* list = reinterpret_cast<int*>(sm.wbuf + a.list_off);
         int* wcnt = reinterpret_cast<int*>(sm.red);
-        int nact = 0;
+        int nitems = 0;
         for (int e0 = 0; e0 < a.E; e0 += NCT) {
             const int e = e0 + tid;
-            bool act = false;
+            int nt_e = 0;                                    // this group's tiles
             if (e < a.E) {
                 const int o0 = __ldg(a.goff + e), o1 = __ldg(a.goff + e + 1);
                 const bool valid = o0 >= 0 && o1 >= o0 && o1 <= a.M;
-                if (!valid || o1 - o0 > a.gmax) atomicCAS(a.err, 0, W4_ERR_GROUP_TOKENS);
-                act = valid && o1 > o0 && o1 - o0 <= a.gmax;
+                if (!valid) atomicCAS(a.err, 0, W4_ERR_GROUP_TOKENS);
+                nt_e = valid ? (o1 - o0 + a.gmax - 1) / a.gmax : 0;
             }
-            const unsigned bal = __ballot_sync(0xffffffffu, act);
-            if (lane == 0) wcnt[warp] = __popc(bal);
+            int v = nt_e;                                    // inclusive scan in the warp
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int t = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += t;
+            }
+            if (lane == 31) wcnt[warp] = v;
             named_bar_sync(1, NCT);
-            int before = nact, tot = 0;
+            int before = nitems, tot = 0;
             for (int w = 0; w < CW; ++w) {
                 const int c = wcnt[w];
                 if (w < warp) before += c;
                 tot += c;
             }
-            if (act) list[before + __popc(bal & ((1u << lane) - 1u))] = (int16_t)e;
-            nact += tot;
+            // offsets that overlap can list more tiles than T allows: the
+            // list keeps what fits and the error is flagged
+            for (int t = 0; t < nt_e; ++t) {
+                const int at = before + v - nt_e + t;
+                if (at < a.list_cap) list[at] = e | (t << 16);
+            }
+            nitems += tot;
             named_bar_sync(1, NCT);
         }
+        if (nitems > a.list_cap) {
+            if (tid == 0) atomicCAS(a.err, 0, W4_ERR_GROUP_TOKENS);
+            nitems = a.list_cap;
+        }
         if (tid == 0) {
-            ctl->nact = nact;
+            ctl->nact = nitems;
             mbar_arrive(&ctl->listready);
         }
-        units = nact * a.NBg;
+        units = nitems * a.NBg;
         glist = list;
     }
     int u_beg = blockIdx.x, u_end = units, u_step = gridDim.x;
@@ -539,17 +555,18 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
         if constexpr (GROUPED) {
             const int gi = u / a.NBg;
             rb = u - gi * a.NBg;
-            g = glist[gi];
+            const int item = glist[gi];
+            g = item & 0xFFFF;
             s = 0; ks0 = 0; ks1 = nst;
-            if (g != prev_g) {
-                // this group's tokens: rows o0 .. o0 + M - 1 of x and y
-                const int o0 = __ldg(a.goff + g);
-                M = __ldg(a.goff + g + 1) - o0;
+            if (item != prev_item) {
+                // this tile's tokens: rows o0 .. o0 + M - 1 of x and y
+                const int o0 = __ldg(a.goff + g) + (item >> 16) * a.gmax;
+                M = min(a.gmax, __ldg(a.goff + g + 1) - o0);
                 x = static_cast<const uint16_t*>(a.x) + (size_t)o0 * K;
                 y = a.y + (size_t)o0 * N;
                 token_rows();
-                prev0 = -1;                        // stage this group's activations
-                prev_g = g;
+                prev0 = -1;                        // stage this tile's activations
+                prev_item = item;
             }
         } else {
             rb = u / Sp;

@@ -46,9 +46,9 @@ struct GemvPlan {
 };
 
 // act_bytes: bytes per activation element (2 for bf16, 1 for int8).
-// groups > 0: a grouped plan (one matrix of N rows per group, M = the most
-// tokens of one group, N here = rows of all groups expected to be active):
-// no K split, and room for a list of `groups` group ids.
+// groups > 0: a grouped plan (one matrix of N rows per group, M = the token
+// tile, N here = rows of all items expected): no K split, and room for a
+// list of `groups` (group, token tile) items.
 // Returns false if no plan fits (M too large).
 bool plan_gemv(int M, int N, int Kp, int G, int act_bytes, int sm_count, GemvPlan* plan,
                int groups = 0);
@@ -69,10 +69,11 @@ struct GemvArgs {
     int xtma;                 // activation rows are 16-byte aligned: stage them with TMA
     // grouped decode: x [M, K] rows sorted by group, goff[E+1] token offsets
     // of the E groups, weights/scales/zeros/bias stacked [E, N, ...], y [M, N];
-    // at most gmax tokens per group
+    // groups are taken in tiles of at most gmax tokens
     const int* goff;
     int E, gmax, NBg;         // groups, token bound, row blocks per group
-    int list_off;             // shared-memory offset of the active-group list
+    int list_off;             // shared-memory offset of the (group, token tile) list
+    int list_cap;             // its capacity in items
 };
 
 // The launchers encode the tensor map of `packed` for the plan's box shape

@@ -84,29 +84,37 @@ def test_grouped_single_group_matches_linear(w4):
     _run(w4, 1, 512, 3584, 128, True, [7], seed=3, gmax=7)
 
 
-def test_grouped_bound_and_offsets_errors(w4):
-    """A group above max_group_tokens, or offsets past T, is skipped (its rows
-    keep their old contents), flags W4_ERR_GROUP_TOKENS, and leaves the other
-    groups right."""
+@pytest.mark.parametrize("tile", [1, 4, 16])
+def test_grouped_tiles_larger_groups(w4, tile):
+    """Groups larger than the token tile are taken in several passes: counts
+    up to 41 with tiles of 1, 4 and 16 tokens (ragged last tiles)."""
+    counts = [41, 0, 16, 17, 3, 0, 33, 1]
+    _run(w4, 8, 192, 1024, 64, False, counts, seed=70 + tile, gmax=tile)
+
+
+def test_grouped_bad_offsets(w4):
+    """Offsets past T are skipped (those rows keep their old contents), flag
+    W4_ERR_GROUP_TOKENS, and leave the other groups right."""
     E, N, K, G = 4, 64, 256, 32
-    counts = [2, 5, 0, 3]                    # group 1 exceeds the bound of 4
+    counts = [2, 5, 0, 3]
     packed, scales, _, x, b, goff = _case(E, N, K, G, True, counts, 21)
     y = torch.full((10, N), 7.0, dtype=torch.bfloat16, device="cuda")
-    w4.w4a16_grouped_linear(x.cuda(), torch.tensor(goff, device="cuda"), packed.cuda(),
-                            scales.cuda(), None, b.cuda(), E, N, K, G, 4, y=y)
-    assert w4.w4_get_device_error() == -11
     yref = O.w4a16_grouped_linear(x, goff, packed.numpy(), scales.numpy(), None, b.numpy(),
                                   E, N, K, G)
-    keep = np.r_[0:2, 7:10]
-    assert_close(y[torch.as_tensor(keep, device="cuda")], yref[keep], "other groups")
-    assert torch.all(y[2:7] == 7.0)
     # offsets running past T (the last group claims rows 7..11 of 10)
     bad = torch.tensor([0, 2, 7, 7, 12], dtype=torch.int32, device="cuda")
-    y.fill_(7.0)
     w4.w4a16_grouped_linear(x.cuda(), bad, packed.cuda(), scales.cuda(), None, b.cuda(),
                             E, N, K, G, 8, y=y)
     assert w4.w4_get_device_error() == -11
     assert torch.all(y[7:] == 7.0)
+    assert_close(y[:7], yref[:7], "valid groups")
+    assert w4.w4_get_device_error() == 0
+    # overlapping offsets, each group valid on its own: more tiles than T
+    # allows; the list keeps what fits and the error is flagged
+    lap = torch.tensor([0, 10, 0, 10, 10], dtype=torch.int32, device="cuda")
+    w4.w4a16_grouped_linear(x.cuda(), lap, packed.cuda(), scales.cuda(), None, b.cuda(),
+                            E, N, K, G, 1, y=y)
+    assert w4.w4_get_device_error() == -11
     assert w4.w4_get_device_error() == 0
 
 
@@ -123,7 +131,7 @@ def test_grouped_empty_and_argument_errors(w4):
     with pytest.raises(w4.W4Error) as e:
         w4.w4a16_grouped_linear(x, goff, packed.cuda(), scales.cuda(), None, None, E, N, K, G, 17)
     assert e.value.code == -1
-    # all groups empty except none: every token in group 0, the rest idle
+    # every token in group 0, the rest idle
     y = w4.w4a16_grouped_linear(x, goff, packed.cuda(), scales.cuda(), None, None, E, N, K, G, 4)
     yref = O.w4a16_linear(x.cpu(), packed.numpy()[:N], scales.numpy()[:N], None, None, K, G)
     assert_close(y, yref, "one busy group")
