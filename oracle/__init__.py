@@ -9,7 +9,8 @@ from .w4_oracle import (padded_k, rtn_params, rtn_codes, rtn_quantize, pack_nibb
                         w4a16_grouped_linear,
                         w4a8_quantize_act, w4a8_linear, int32_worst_case,
                         smooth_factors, w4a8_linear_grouped,
-                        gptq_hessian, gptq_quantize)
+                        gptq_hessian, gptq_quantize, round_bf16, pack_rtn_bf16,
+                        dequantize_bf16_params, w4a16_linear_bf16_params)
 
 __all__ = ["padded_k", "rtn_params", "rtn_codes", "rtn_quantize", "pack_nibbles", "unpack_nibbles",
            "pack_rtn", "dequantize_f64", "bf16_to_f64", "w4a16_linear",
@@ -17,4 +18,5 @@ __all__ = ["padded_k", "rtn_params", "rtn_codes", "rtn_quantize", "pack_nibbles"
            "w4a16_grouped_linear",
            "w4a8_quantize_act", "w4a8_linear", "int32_worst_case",
            "smooth_factors", "w4a8_linear_grouped",
-           "gptq_hessian", "gptq_quantize"]
+           "gptq_hessian", "gptq_quantize", "round_bf16", "pack_rtn_bf16",
+           "dequantize_bf16_params", "w4a16_linear_bf16_params"]

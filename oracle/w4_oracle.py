@@ -72,6 +72,10 @@ Readings where the pages are silent (each is also listed in the design notes):
        the padded columns K..Kp-1 are dead columns.  The oracle propagates
        in fp64 and takes every rounding decision by the fp32 rule, from the
        fp32 value of the current weight.
+ (xiv) bf16 parameter layout: the codes are the RTN codes; the stored
+       scale is bf16(s) and, for asymmetric groups, the stored offset is
+       bf16(fp32((8 - z) s)) (round to nearest even each time);
+       w_hat = s_b (code - 8) + o_b.
  (viii) the W4A8 weight scale is max|row|/7 (the symmetric rule of [P1]),
        codes stored as q+8 like W4A16.
  Matmuls are done in fp64 on exactly dequantized weights (s * (code - z) is
@@ -186,6 +190,54 @@ def pack_rtn(W, group_size: int, symmetric: bool):
 # ---------------------------------------------------------------------------
 # Dequantise and matmul in fp64 [P1]
 # ---------------------------------------------------------------------------
+
+def round_bf16(a):
+    """fp32 values rounded to the nearest bf16 (ties to even), as fp32."""
+    b = np.asarray(a, dtype=F32).view(np.uint32).astype(np.uint64)
+    r = (b + 0x7FFF + ((b >> 16) & 1)) >> 16 << 16
+    return (r & 0xFFFFFFFF).astype(np.uint32).view(F32)
+
+
+def pack_rtn_bf16(W, group_size: int, symmetric: bool):
+    """RTN codes with bf16 parameters, reading (xiv) ([P1a] offset (8 - z) s;
+    [P3] bf16 scales): returns (packed, s_b fp32 [N, Ng] holding bf16
+    values, o_b likewise or None when symmetric)."""
+    codes, s, z = rtn_quantize(W, group_size, symmetric)
+    s_b = round_bf16(s)
+    o_b = None
+    if not symmetric:
+        o_b = round_bf16((F32(8.0) - z.astype(F32)) * s)      # fp32 product, then bf16
+    return pack_nibbles(codes), s_b, o_b
+
+
+def dequantize_bf16_params(packed, s_b, o_b, group_size: int, rows=None):
+    """w_hat = s_b (code - 8) + o_b in fp64 (exact for bf16 s_b, o_b)."""
+    packed = np.asarray(packed)
+    s_b = np.asarray(s_b, dtype=F32)
+    if rows is not None:
+        rows = np.asarray(rows)
+        packed, s_b = packed[rows], s_b[rows]
+        o_b = None if o_b is None else np.asarray(o_b)[rows]
+    codes = unpack_nibbles(packed).astype(np.float64)
+    N, Kp = codes.shape
+    G = int(group_size)
+    Ng = Kp // G
+    w = s_b.astype(np.float64)[:, :, None] * (codes.reshape(N, Ng, G) - 8.0)
+    if o_b is not None:
+        w = w + np.asarray(o_b, dtype=F32).astype(np.float64)[:, :, None]
+    return w.reshape(N, Kp)
+
+
+def w4a16_linear_bf16_params(x, packed, s_b, o_b, bias, K: int, group_size: int, rows=None):
+    """w4a16_linear with the bf16 parameter layout, reading (xiv)."""
+    xd = bf16_to_f64(x)
+    Wd = dequantize_bf16_params(packed, s_b, o_b, group_size, rows=rows)[:, :K]
+    y = xd @ Wd.T
+    if bias is not None:
+        b = np.asarray(bias, dtype=np.float64)
+        y = y + (b if rows is None else b[np.asarray(rows)])[None, :]
+    return y
+
 
 def dequantize_f64(packed, scales, zeros, group_size: int, rows=None):
     """W_hat[n, k] = s[n, k // G] * (code[n, k] - z[n, k // G]) in fp64, with

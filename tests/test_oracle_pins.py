@@ -670,3 +670,56 @@ def test_gptq_beats_rtn_on_the_calibration_objective():
         g_err = err(_dequant(codes, scales, zeros, G))
         r_err = err(_dequant(rc, rs, rz, G))
         assert g_err < 0.8 * r_err, (g_err, r_err)
+
+
+# ---------------------------------------------------------------------------
+# bf16 parameter layout: bf16 scales ("Yeniden paketlenmiş QAT Gemma 4 …",
+# TPU W4A16 loads scales in bf16) and the (8 - z) s offset ("Lab 5",
+# 融合INT4反量化与矩阵乘)
+# ---------------------------------------------------------------------------
+
+def test_round_bf16_closed_forms():
+    v = np.array([1 + 2 ** -8, 1 + 3 * 2 ** -8, -(1 + 2 ** -8), 1 + 2 ** -8 + 2 ** -20,
+                  3.0, 0.0, -2.5], np.float32)
+    r = O.round_bf16(v)
+    assert list(r) == [1.0, 1 + 2 ** -6, -1.0, 1 + 2 ** -7, 3.0, 0.0, -2.5]
+    assert np.all(r.view(np.uint32) & 0xFFFF == 0)
+
+
+def test_bf16_params_layout():
+    rng = np.random.default_rng(5)
+    W = _rand_w(24, 256, 31, std=0.3)
+    W[3, :32] = np.abs(W[3, :32])                      # a one-signed group: z at a bound
+    for symmetric in (True, False):
+        packed, s_b, o_b = O.pack_rtn_bf16(W, 32, symmetric)
+        p32, s, z = O.pack_rtn(W, 32, symmetric)
+        assert np.array_equal(packed, p32)             # the codes are RTN's
+        assert np.all(s_b.view(np.uint32) & 0xFFFF == 0)
+        wb = O.dequantize_bf16_params(packed, s_b, o_b, 32)
+        wf = O.dequantize_f64(p32, s, z, 32)
+        # each stored parameter is within half a bf16 step: 8 significant
+        # bits, unit roundoff 2^-8 relative; |code - 8| <= 8
+        zz = np.full(s.shape, 8.0) if z is None else z.astype(np.float64)
+        bound = 2.0 ** -8 * (8 * np.abs(s) + np.abs((8 - zz) * s)).astype(np.float64)
+        assert np.all(np.abs(wb - wf) <= np.repeat(bound, 32, axis=1) * (1 + 1e-6))
+        if symmetric:
+            assert o_b is None
+        else:
+            assert np.all(o_b[z == 8] == 0)
+
+
+def test_bf16_params_exact_for_power_of_two_scales():
+    """When every s is a power of two, s_b = s and the offset is exact, so
+    the two layouts dequantize identically."""
+    rng = np.random.default_rng(6)
+    W = rng.integers(-8, 8, size=(8, 64)).astype(np.float32) * 0.25
+    W[:, ::32] = -8 * 0.25                              # every group spans -2 .. +1.75
+    W[:, 1::32] = 7 * 0.25
+    for symmetric in (True, False):
+        packed, s_b, o_b = O.pack_rtn_bf16(W, 32, symmetric)
+        p32, s, z = O.pack_rtn(W, 32, symmetric)
+        if symmetric:
+            continue                                    # max/7 is not a power of two
+        assert np.array_equal(s_b, s)
+        assert np.array_equal(O.dequantize_bf16_params(packed, s_b, o_b, 32),
+                              O.dequantize_f64(p32, s, z, 32))
