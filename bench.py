@@ -582,6 +582,53 @@ def measure_moe(w4, hbm, reps=100):
     return out
 
 
+def measure_bf16p(w4, hbm, reps=200):
+    """The 7B decode step with the bf16 parameter layout (bf16 scales; the
+    step's linears are symmetric, so no offsets): per linear and per step,
+    GB/s over its own algorithmic bytes (2-byte scales)."""
+    lins = WL.decode_7b(1)
+    copies = []
+    per_copy = sum(algorithmic_bytes(l, 1) for l in lins)
+    R = max(2, math.ceil(3 * L2_BYTES / per_copy))
+    for r in range(R):
+        cp = []
+        for li, lin in enumerate(lins):
+            W = WL.make_inputs(lin).W.cuda() if r == 0 else None
+            if r == 0:
+                p, sb, ob = w4.w4_pack_rtn_bf16(W, lin.group_size, True)
+                del W
+            else:
+                p, sb, ob = copies[0][li]["p"].clone(), copies[0][li]["sb"].clone(), None
+            x = WL.make_activations(lin.K, 1, seed=10_000 + 97 * r + li).cuda()
+            cp.append(dict(p=p, sb=sb, x=x, y=torch.empty(1, lin.N, dtype=torch.bfloat16,
+                                                          device="cuda")))
+        copies.append(cp)
+    torch.cuda.synchronize()
+
+    def call(li, i):
+        lin, d = lins[li], copies[i % R][li]
+        w4.w4a16_linear_bf16p(d["x"], d["p"], d["sb"], None, None, lin.N, lin.K, lin.group_size,
+                              y=d["y"])
+
+    def step(i):
+        for li in range(len(lins)):
+            call(li, i)
+    for i in range(3):
+        step(i)
+    torch.cuda.synchronize()
+    out, tb = [], 0
+    for li, lin in enumerate(lins):
+        n = reps * R
+        sec = time_graph_steps(lambda i, li=li: call(li, i), n, R, 1) / n
+        b = algorithmic_bytes(lin, 1) - 2 * lin.N * (lin.K // lin.group_size)   # 2-byte scales
+        tb += b
+        out.append({"name": lin.name, "us": round(sec * 1e6, 3), "GB/s": round(b / sec / 1e9, 1)})
+    n = reps * R
+    sec = time_graph_steps(step, n, R, 1) / n
+    return {"step_us": round(sec * 1e6, 2), "GB/s": round(tb / sec / 1e9, 1),
+            "frac": round(tb / sec / 1e9 / hbm, 4), "per_linear": out}
+
+
 def measure_gptq(w4, reps=3):
     """GPTQ of the 7B fused QKV projection (4608 x 3584, G = 128,
     symmetric) from 512 calibration tokens, on the device: Hessian, Cholesky,
@@ -662,6 +709,7 @@ def run_ours(args, world, rank):
         res["swiglu_7b"] = measure_swiglu(w4, hbm)
         res["moe_decode"] = measure_moe(w4, hbm)
         res["gptq"] = measure_gptq(w4)
+        res["decode7b_bf16_params"] = measure_bf16p(w4, hbm)
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline_decode(lins)
     return res

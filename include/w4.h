@@ -173,6 +173,31 @@ W4_API int w4a16_linear(const uint16_t* x, const uint8_t* packed, const float* s
                  void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * w4_pack_rtn_bf16 / w4a16_linear_bf16p - the same layer with its group
+ * parameters stored in bf16 (half the parameter bytes): bf16 scales, as the
+ * TPU W4A16 layers load them ("Yeniden paketlenmiş QAT Gemma 4 26B-A4B, tek
+ * bir TPU v6e'de FP8 işlemenin 1.9 katı verimle sunuluyor", section 26B'deki
+ * boşluk), and for asymmetric groups the additive offset (8 - z) s of
+ * codes read as (code - 8) ("Lab 5: Gemma4 端到端推理优化", section
+ * 融合INT4反量化与矩阵乘) instead of the zero point:
+ *  w_hat = s_b (code - 8) + o_b,  s_b = bf16(s),  o_b = bf16(fp32((8 - z) s))
+ * (round to nearest even).  The codes are exactly w4_pack_rtn's.
+ *
+ *  w4_pack_rtn_bf16: W, N, K, group_size, symmetric, packed as for
+ *    w4_pack_rtn; scales_b [N, Ng] bf16 out; offsets_b [N, Ng] bf16 out when
+ *    symmetric == 0, else NULL.
+ *  w4a16_linear_bf16p: as w4a16_linear (same shapes, plans, workspace);
+ *    scales_b and offsets_b (NULL: symmetric) 16-byte aligned.
+ * ------------------------------------------------------------------------- */
+W4_API int w4_pack_rtn_bf16(const float* W, int N, int K, int group_size, int symmetric,
+                            uint8_t* packed, uint16_t* scales_b, uint16_t* offsets_b,
+                            void* stream);
+W4_API int w4a16_linear_bf16p(const uint16_t* x, const uint8_t* packed, const uint16_t* scales_b,
+                              const uint16_t* offsets_b, const float* bias, uint16_t* y, int M,
+                              int N, int K, int group_size, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * w4a16_linear_swiglu - the gate and up projections of a SwiGLU feed-forward
  * layer in one pass, y = SiLU(x W_gate^T + b_gate) (*) (x W_up^T + b_up),
  * SiLU(v) = v * sigmoid(v).  "Lab 5: Gemma4 端到端推理优化", section 基础

@@ -21,6 +21,9 @@ _SIGS = {
                                       _c_int, _c_int, _vp]),
     "w4a16_linear": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
                               _c_int, _vp, _c_size, _vp]),
+    "w4_pack_rtn_bf16": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _vp, _vp]),
+    "w4a16_linear_bf16p": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
+                                    _vp, _c_size, _vp]),
     "w4a16_linear_swiglu": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
                                      _c_int, _c_int, _vp, _c_size, _vp]),
     "w4a16_grouped_linear": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
@@ -206,6 +209,53 @@ def w4a16_linear(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
         lib.w4a16_linear, "w4a16_linear",
         (_ptr(x), _ptr(packed), _ptr(scales), _ptr(zeros), _ptr(bias), _ptr(y), M, N, K,
          int(group_size), 1 if zeros is None else 0),
+        (_stream(x, stream),), x.device, workspace,
+        lambda: lib.w4a16_workspace_bytes(M, N, K, group_size))
+    return y
+
+
+def w4_pack_rtn_bf16(W: torch.Tensor, group_size: int, symmetric: bool, stream=None):
+    """RTN pack with bf16 parameters -> (packed [N, Kp/2] u8, scales [N, Ng]
+    bf16, offsets (8 - z) s [N, Ng] bf16 or None when symmetric)."""
+    N, K = W.shape
+    _need(W, torch.float32, (N, K), "W")
+    Kp = padded_k(K, group_size)
+    Ng = Kp // group_size if group_size > 0 else 0
+    dev = W.device
+    packed = torch.empty(N, Kp // 2, dtype=torch.uint8, device=dev)
+    scales = torch.empty(N, Ng, dtype=torch.bfloat16, device=dev)
+    offs = None if symmetric else torch.empty(N, Ng, dtype=torch.bfloat16, device=dev)
+    _check("w4_pack_rtn_bf16", load().w4_pack_rtn_bf16(
+        _ptr(W), N, K, int(group_size), 1 if symmetric else 0, _ptr(packed), _ptr(scales),
+        _ptr(offs), _stream(W, stream)))
+    return packed, scales, offs
+
+
+def w4a16_linear_bf16p(x: torch.Tensor, packed: torch.Tensor, scales_b: torch.Tensor,
+                       offsets_b: Optional[torch.Tensor], bias: Optional[torch.Tensor], N: int,
+                       K: int, group_size: int, y=None, workspace=None,
+                       stream=None) -> torch.Tensor:
+    """w4a16_linear with bf16 scales (and bf16 (8 - z) s offsets)."""
+    M = x.shape[0]
+    _need(x, torch.bfloat16, (M, K), "x")
+    Kp = padded_k(K, group_size)
+    Ng = Kp // group_size
+    _need(packed, torch.uint8, (N, Kp // 2), "packed")
+    _need(scales_b, torch.bfloat16, (N, Ng), "scales_b")
+    if offsets_b is not None:
+        _need(offsets_b, torch.bfloat16, (N, Ng), "offsets_b")
+    if bias is not None:
+        _need(bias, torch.float32, (N,), "bias")
+    if y is None:
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=x.device)
+    _need(y, torch.bfloat16, (M, N), "y")
+    if M == 0:
+        return y
+    lib = load()
+    _call_with_workspace(
+        lib.w4a16_linear_bf16p, "w4a16_linear_bf16p",
+        (_ptr(x), _ptr(packed), _ptr(scales_b), _ptr(offsets_b), _ptr(bias), _ptr(y), M, N, K,
+         int(group_size)),
         (_stream(x, stream),), x.device, workspace,
         lambda: lib.w4a16_workspace_bytes(M, N, K, group_size))
     return y

@@ -167,7 +167,24 @@ int w4_pack_rtn(const float* W, int N, int K, int group_size, int symmetric,
     if (!aligned16(packed)) return W4_ERR_MISALIGNED;
     if (!aligned4(W) || !aligned4(scales)) return W4_ERR_MISALIGNED;
     return launch_pack_rtn(W, N, K, group_size, symmetric ? 1 : 0, packed, scales, zeros,
-                           static_cast<cudaStream_t>(stream));
+                           nullptr, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+int w4_pack_rtn_bf16(const float* W, int N, int K, int group_size, int symmetric,
+                     uint8_t* packed, uint16_t* scales_b, uint16_t* offsets_b, void* stream) {
+    if (!W || !packed || !scales_b) return W4_ERR_NULL_PTR;
+    if (symmetric && offsets_b) return W4_ERR_INVALID_ARG;
+    if (!symmetric && !offsets_b) return W4_ERR_NULL_PTR;
+    if (N <= 0) return W4_ERR_INVALID_ARG;
+    int rc = check_group(K, group_size);
+    if (rc) return rc;
+    if (padded_k(K, group_size) > 0x7fffffffLL) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(packed)) return W4_ERR_MISALIGNED;
+    if (!aligned4(W) || (reinterpret_cast<uintptr_t>(scales_b) & 1) ||
+        (reinterpret_cast<uintptr_t>(offsets_b) & 1))
+        return W4_ERR_MISALIGNED;
+    return launch_pack_rtn(W, N, K, group_size, symmetric ? 1 : 0, packed, nullptr, nullptr,
+                           scales_b, offsets_b, static_cast<cudaStream_t>(stream));
 }
 
 size_t w4a16_workspace_bytes(int M, int N, int K, int group_size) {
@@ -227,6 +244,50 @@ int w4a16_linear(const uint16_t* x, const uint8_t* packed, const float* scales,
     a.R = p.R; a.SKE = p.SKE; a.nst = p.nst; a.S = p.S; a.spl = p.spl; a.units = p.units;
     a.XS = p.XS; a.red = p.red;
     return launch_w4a16_gemv(packed, a, p, st);
+}
+
+int w4a16_linear_bf16p(const uint16_t* x, const uint8_t* packed, const uint16_t* scales_b,
+                       const uint16_t* offsets_b, const float* bias, uint16_t* y, int M, int N,
+                       int K, int group_size, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+    if (!x || !packed || !scales_b || !y) return W4_ERR_NULL_PTR;
+    if (M < 0 || N <= 0) return W4_ERR_INVALID_ARG;
+    int rc = check_group(K, group_size);
+    if (rc) return rc;
+    const long long Kp = padded_k(K, group_size);
+    if (Kp > 0x7fffffffLL) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(x) || !aligned16(packed) || !aligned16(scales_b) ||
+        (offsets_b && !aligned16(offsets_b)))
+        return W4_ERR_MISALIGNED;
+    if ((bias && !aligned4(bias)) || (reinterpret_cast<uintptr_t>(y) & 1)) return W4_ERR_MISALIGNED;
+    if (M == 0) return W4_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (M > 16) {
+        if (K % 8 != 0) return W4_ERR_UNSUPPORTED_SHAPE;
+        GemmPlan g;
+        if (!plan_gemm(M, N, K, group_size, current_sm_count(), &g)) return W4_ERR_UNSUPPORTED_SHAPE;
+        if (g.S > 1) {
+            if (!workspace || workspace_bytes < g.ws_bytes) return W4_ERR_WORKSPACE;
+            if (!aligned16(workspace)) return W4_ERR_MISALIGNED;
+        }
+        int* err = device_error_flag();
+        if (!err) return W4_ERR_CUDA;
+        return launch_w4a16_gemm(x, packed, nullptr, nullptr, bias, y, M, N, K, (int)Kp,
+                                 group_size, g, workspace, err, st, scales_b, offsets_b);
+    }
+    GemvPlan p;
+    if (!plan_gemv(M, N, (int)Kp, group_size, 2, current_sm_count(), &p)) return W4_ERR_UNSUPPORTED_SHAPE;
+    GemvArgs a{};
+    rc = split_workspace(p, workspace, workspace_bytes, &a.tickets, &a.partial);
+    if (rc) return rc;
+    a.x = x; a.scales_b = scales_b; a.offs_b = offsets_b; a.bias = bias; a.y = y;
+    a.xtma = (K % 8) == 0 && gemv_tma_activations();
+    a.err = device_error_flag();
+    if (!a.err) return W4_ERR_CUDA;
+    a.M = M; a.N = N; a.K = K; a.Kp = (int)Kp; a.G = group_size; a.Ng = (int)(Kp / group_size);
+    a.R = p.R; a.SKE = p.SKE; a.nst = p.nst; a.S = p.S; a.spl = p.spl; a.units = p.units;
+    a.XS = p.XS; a.red = p.red;
+    return launch_w4a16_gemv_bf16p(packed, a, p, st);
 }
 
 int w4a16_linear_swiglu(const uint16_t* x, const uint8_t* packed, const float* scales,

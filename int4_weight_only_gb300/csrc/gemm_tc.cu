@@ -63,6 +63,8 @@ __host__ __device__ constexpr int threads_of() { return DQ_BASE + DQG * DQ_GROUP
 struct GemmArgs {
     const float* scales;
     const uint8_t* zeros;
+    const uint16_t* scales_b;   // bf16 parameter layout (SB): scales, and
+    const uint16_t* offs_b;     // offsets (8 - z) s for asymmetric groups
     const float* bias;
     uint16_t* y;
     float* partial;     // [S, M, N] when S > 1
@@ -114,7 +116,8 @@ __device__ __forceinline__ void unit_of(const GemmArgs& a, int u, int& nb, int& 
     ks1 = min(ks0 + a.spl, a.nks);
 }
 
-template <int BN, int NST, int NSA, int NSP, int DQG, bool PAIR, int KB>
+// SB: bf16 parameters; the dequantized weight is s (code - 8) + o.
+template <int BN, int NST, int NSA, int NSP, int DQG, bool PAIR, int KB, bool SB = false>
 __global__ void __launch_bounds__(threads_of<DQG>(), 1)
 k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmP,
                 const GemmArgs a) {
@@ -306,22 +309,32 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
             const int n = min(nb * RB + (int)rank * BM + r, a.N - 1);
             const float* srow = a.scales + (size_t)n * a.Ng;
             const uint8_t* zrow = a.zeros ? a.zeros + (size_t)n * a.Ng : nullptr;
-            // scale (and offset -(128 + z) s) of this thread's columns,
-            // loaded one turn ahead
+            const uint16_t* sbrow = SB ? a.scales_b + (size_t)n * a.Ng : nullptr;
+            const uint16_t* obrow = SB && a.offs_b ? a.offs_b + (size_t)n * a.Ng : nullptr;
+            // scale and zero point (SB: bf16 scale and offset) of this
+            // thread's columns, loaded one turn ahead
             auto group_of = [&](int ks) { return min((ks * SK + DQ_COLS * h) / a.G, a.Ng - 1); };
+            auto scale_at = [&](int g) -> float {
+                return SB ? __uint_as_float((uint32_t)__ldg(sbrow + g) << 16) : __ldg(srow + g);
+            };
+            auto zero_at = [&](int g) -> float {
+                if constexpr (SB) return obrow ? __uint_as_float((uint32_t)__ldg(obrow + g) << 16) : 0.f;
+                else return zrow ? (float)__ldg(zrow + g) : 8.f;
+            };
             const int kf = min(ks0 + lead, ks1 - 1);
-            float sc = __ldg(srow + group_of(kf));
-            float zz = zrow ? (float)__ldg(zrow + group_of(kf)) : 8.f;
+            float sc = scale_at(group_of(kf));
+            float zz = zero_at(group_of(kf));
             int ks = ks0 + lead;
             for (; ks < ks1; ks += DQ_GROUPS, it += DQ_GROUPS) {
                 const int sp = it % NSP, sa = it % NSA;
                 float nsc = sc, nzz = zz;
                 if (ks + DQ_GROUPS < ks1) {
                     const int g = group_of(ks + DQ_GROUPS);
-                    nsc = __ldg(srow + g);
-                    nzz = zrow ? (float)__ldg(zrow + g) : 8.f;
+                    nsc = scale_at(g);
+                    nzz = zero_at(g);
                 }
-                const float cc = -(128.f + zz) * sc;
+                // (128 + c) s + cc: cc = -(128 + z) s, or with an offset o - 136 s
+                const float cc = SB ? fmaf(-136.f, sc, zz) : -(128.f + zz) * sc;
                 // one arrival per warp on pempty / afull (after __syncwarp),
                 // so a stage costs 2 x 8 barrier updates, not 2 x 256
                 bool ok = __all_sync(0xffffffffu,
@@ -493,12 +506,12 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     }
 }
 
-template <int BN, int NST, int NSA, int NSP, int DQG, bool PAIR, int KB>
+template <int BN, int NST, int NSA, int NSP, int DQG, bool PAIR, int KB, bool SB = false>
 struct Variant {
     static constexpr int XR = PAIR ? BN / 2 : BN;
     static constexpr size_t smem = smem_bytes<XR, NST, NSA, NSP, KB>();
     static_assert(smem <= 232448, "shared memory");
-    static constexpr auto kernel = k_w4a16_gemm_tc<BN, NST, NSA, NSP, DQG, PAIR, KB>;
+    static constexpr auto kernel = k_w4a16_gemm_tc<BN, NST, NSA, NSP, DQG, PAIR, KB, SB>;
 
     static bool prepare() {
         return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -567,11 +580,16 @@ struct Variant {
 using Single256 = Variant<256, 4, 4, 8, 1, false, 1>;
 using Single128 = Variant<128, 8, 4, 8, 1, false, 1>;
 using Pair256 = Variant<256, 6, 4, 8, 1, true, 1>;
+using Single256B = Variant<256, 4, 4, 8, 1, false, 1, true>;
+using Single128B = Variant<128, 8, 4, 8, 1, false, 1, true>;
+using Pair256B = Variant<256, 6, 4, 8, 1, true, 1, true>;
 // 128 columns per stage (two K blocks): half the per-stage hand-offs for the
 // same MMA work; group sizes that are multiples of 64 only (a dequantizing
 // thread's 64 columns must lie in one group)
 using Single256K2 = Variant<256, 2, 2, 4, 1, false, 2>;
 using Pair256K2 = Variant<256, 4, 2, 4, 1, true, 2>;
+using Single256K2B = Variant<256, 2, 2, 4, 1, false, 2, true>;
+using Pair256K2B = Variant<256, 4, 2, 4, 1, true, 2, true>;
 
 }  // namespace
 
@@ -654,14 +672,24 @@ bool plan_gemm(int M, int N, int K, int G, int sm_count, GemmPlan* out) {
 int launch_w4a16_gemm(const uint16_t* x, const uint8_t* packed, const float* scales,
                       const uint8_t* zeros, const float* bias, uint16_t* y, int M, int N, int K,
                       int Kp, int G, const GemmPlan& p, void* workspace, int* err,
-                      cudaStream_t stream) {
+                      cudaStream_t stream, const uint16_t* scales_b, const uint16_t* offs_b) {
     GemmArgs a{};
     a.scales = scales; a.zeros = zeros; a.bias = bias; a.y = y; a.err = err;
+    a.scales_b = scales_b; a.offs_b = offs_b;
     a.M = M; a.N = N; a.K = K; a.G = G; a.Ng = Kp / G;
     a.nks = p.nks; a.TB = p.TB; a.ntiles = p.ntiles; a.S = p.S; a.spl = p.spl; a.units = p.units;
     if (p.S > 1) {
         a.tickets = static_cast<int*>(workspace);
         a.partial = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + p.ticket_bytes);
+    }
+    if (scales_b) {
+        if (p.kb == 2) {
+            if (p.pair) return Pair256K2B::launch(x, packed, p, a, Kp, stream);
+            return Single256K2B::launch(x, packed, p, a, Kp, stream);
+        }
+        if (p.pair) return Pair256B::launch(x, packed, p, a, Kp, stream);
+        if (p.BN == 256) return Single256B::launch(x, packed, p, a, Kp, stream);
+        return Single128B::launch(x, packed, p, a, Kp, stream);
     }
     if (p.kb == 2) {
         if (p.pair) return Pair256K2::launch(x, packed, p, a, Kp, stream);

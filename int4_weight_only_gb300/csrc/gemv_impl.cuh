@@ -438,7 +438,11 @@ __device__ __forceinline__ bool split_k_arrive(const GemvArgs& a, SmemCtl* ctl, 
 // sum of the groups' tile counts), and takes a contiguous run of the
 // (item, row block) units; a group whose offsets are invalid is left out
 // and raises W4_ERR_GROUP_TOKENS.  Item = group | tile << 16.
-template <int NT, int CPG, bool ASYM, bool SPLIT, bool SWIGLU = false, bool GROUPED = false>
+// SB: bf16 parameters (a.scales_b, and for ASYM the offsets a.offs_b =
+// bf16((8 - z) s) in place of zero points): w_hat = s (code - 8) + o, so the
+// fix-up of a run is s (u tmp - C0 - 8 C1) + o C1.
+template <int NT, int CPG, bool ASYM, bool SPLIT, bool SWIGLU = false, bool GROUPED = false,
+          bool SB = false>
 __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
     static_assert(!(GROUPED && (SPLIT || SWIGLU)), "grouped plans are unsplit, plain epilogue");
     constexpr int SEG = 8 / CPG;
@@ -577,53 +581,106 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
         const size_t wrow = GROUPED ? (size_t)g * N : 0;   // first row of this unit's matrix
         const int row0 = rb * R + rt * 16;
         const int nr = min(row0 + gid, N - 1), nr8 = min(row0 + gid + 8, N - 1);
-        const float* sc_r = scales + (wrow + nr) * Ng;
-        const float* sc_r8 = scales + (wrow + nr8) * Ng;
-        const uint8_t* zp_r = ASYM ? zeros + (wrow + nr) * Ng : nullptr;
-        const uint8_t* zp_r8 = ASYM ? zeros + (wrow + nr8) * Ng : nullptr;
+        // the two rows' parameters: fp32 scales and uint8 zero points, or
+        // (SB) bf16 scales and bf16 offsets through the same two pointers
+        const float* sc_r = SB ? reinterpret_cast<const float*>(a.scales_b + (wrow + nr) * Ng)
+                               : scales + (wrow + nr) * Ng;
+        const float* sc_r8 = SB ? reinterpret_cast<const float*>(a.scales_b + (wrow + nr8) * Ng)
+                                : scales + (wrow + nr8) * Ng;
+        const uint8_t* zp_r = !ASYM ? nullptr
+                              : SB ? reinterpret_cast<const uint8_t*>(a.offs_b + (wrow + nr) * Ng)
+                                   : zeros + (wrow + nr) * Ng;
+        const uint8_t* zp_r8 = !ASYM ? nullptr
+                               : SB ? reinterpret_cast<const uint8_t*>(a.offs_b + (wrow + nr8) * Ng)
+                                    : zeros + (wrow + nr8) * Ng;
         // bias of this thread's two rows and the scales of the first stage:
         // constant inputs, read before waiting for the previous kernel
         const float b_lo = bias ? __ldg(bias + wrow + nr) : 0.f;
         const float b_hi = bias ? __ldg(bias + wrow + nr8) : 0.f;
         float sr[SEG], sr8[SEG], zr[SEG], zr8[SEG];
         auto load_scales = [&](int kw, float* r_, float* r8_, float* z_, float* z8_) {
-            if constexpr (SEG == 8) {
-                // one group per segment (G = 32): a row's 8 scales (32 B) and
-                // zero points (8 B) of the box are contiguous; vector loads
-                // when they are aligned and inside the row
-                const int g0 = kw >> (5 + LOG_CPG);
-                if (vec_groups && g0 + 8 <= Ng) {
-                    const float4* s4 = reinterpret_cast<const float4*>(sc_r + g0);
-                    const float4* s48 = reinterpret_cast<const float4*>(sc_r8 + g0);
-                    const float4 a0 = __ldg(s4), a1 = __ldg(s4 + 1);
-                    const float4 b0 = __ldg(s48), b1 = __ldg(s48 + 1);
-                    r_[0] = a0.x; r_[1] = a0.y; r_[2] = a0.z; r_[3] = a0.w;
-                    r_[4] = a1.x; r_[5] = a1.y; r_[6] = a1.z; r_[7] = a1.w;
-                    r8_[0] = b0.x; r8_[1] = b0.y; r8_[2] = b0.z; r8_[3] = b0.w;
-                    r8_[4] = b1.x; r8_[5] = b1.y; r8_[6] = b1.z; r8_[7] = b1.w;
-                    if (ASYM) {
-                        const uint2 q = __ldg(reinterpret_cast<const uint2*>(zp_r + g0));
-                        const uint2 q8 = __ldg(reinterpret_cast<const uint2*>(zp_r8 + g0));
+            if constexpr (SB) {
+                // bf16 scales (z_: offsets); eight 32-wide groups of a box are
+                // one 16-byte load per row when aligned and inside the row
+                auto bf = [](uint32_t w, int hi) { return __uint_as_float(hi ? (w & 0xFFFF0000u) : (w << 16)); };
+                const uint16_t* sb_r = reinterpret_cast<const uint16_t*>(sc_r);
+                const uint16_t* sb_r8 = reinterpret_cast<const uint16_t*>(sc_r8);
+                const uint16_t* ob_r = reinterpret_cast<const uint16_t*>(zp_r);
+                const uint16_t* ob_r8 = reinterpret_cast<const uint16_t*>(zp_r8);
+                if constexpr (SEG == 8) {
+                    const int g0 = kw >> (5 + LOG_CPG);
+                    if (vec_groups && g0 + 8 <= Ng) {
+                        const uint4 a4 = __ldg(reinterpret_cast<const uint4*>(sb_r + g0));
+                        const uint4 b4 = __ldg(reinterpret_cast<const uint4*>(sb_r8 + g0));
+                        const uint32_t aw[4] = {a4.x, a4.y, a4.z, a4.w}, bw[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            z_[j] = (float)((q.x >> (8 * j)) & 0xFF);
-                            z_[j + 4] = (float)((q.y >> (8 * j)) & 0xFF);
-                            z8_[j] = (float)((q8.x >> (8 * j)) & 0xFF);
-                            z8_[j + 4] = (float)((q8.y >> (8 * j)) & 0xFF);
+                        for (int j = 0; j < 8; ++j) {
+                            r_[j] = bf(aw[j >> 1], j & 1);
+                            r8_[j] = bf(bw[j >> 1], j & 1);
                         }
-                    }
-                    return;
-                }
-            }
+                        if (ASYM) {
+                            const uint4 c4 = __ldg(reinterpret_cast<const uint4*>(ob_r + g0));
+                            const uint4 d4 = __ldg(reinterpret_cast<const uint4*>(ob_r8 + g0));
+                            const uint32_t cw[4] = {c4.x, c4.y, c4.z, c4.w}, dw[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
-            for (int j = 0; j < SEG; ++j) {
-                const int sg = (kw >> (5 + LOG_CPG)) + j;
-                const int g = min(gshift >= 0 ? (sg >> gshift) : sg / gdiv, Ng - 1);
-                r_[j] = __ldg(sc_r + g);
-                r8_[j] = __ldg(sc_r8 + g);
-                if (ASYM) {
-                    z_[j] = (float)__ldg(zp_r + g);
-                    z8_[j] = (float)__ldg(zp_r8 + g);
+                            for (int j = 0; j < 8; ++j) {
+                                z_[j] = bf(cw[j >> 1], j & 1);
+                                z8_[j] = bf(dw[j >> 1], j & 1);
+                            }
+                        }
+                        return;
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < SEG; ++j) {
+                    const int sg = (kw >> (5 + LOG_CPG)) + j;
+                    const int g = min(gshift >= 0 ? (sg >> gshift) : sg / gdiv, Ng - 1);
+                    r_[j] = __uint_as_float((uint32_t)__ldg(sb_r + g) << 16);
+                    r8_[j] = __uint_as_float((uint32_t)__ldg(sb_r8 + g) << 16);
+                    if (ASYM) {
+                        z_[j] = __uint_as_float((uint32_t)__ldg(ob_r + g) << 16);
+                        z8_[j] = __uint_as_float((uint32_t)__ldg(ob_r8 + g) << 16);
+                    }
+                }
+            } else {
+                if constexpr (SEG == 8) {
+                    // one group per segment (G = 32): a row's 8 scales (32 B) and
+                    // zero points (8 B) of the box are contiguous; vector loads
+                    // when they are aligned and inside the row
+                    const int g0 = kw >> (5 + LOG_CPG);
+                    if (vec_groups && g0 + 8 <= Ng) {
+                        const float4* s4 = reinterpret_cast<const float4*>(sc_r + g0);
+                        const float4* s48 = reinterpret_cast<const float4*>(sc_r8 + g0);
+                        const float4 a0 = __ldg(s4), a1 = __ldg(s4 + 1);
+                        const float4 b0 = __ldg(s48), b1 = __ldg(s48 + 1);
+                        r_[0] = a0.x; r_[1] = a0.y; r_[2] = a0.z; r_[3] = a0.w;
+                        r_[4] = a1.x; r_[5] = a1.y; r_[6] = a1.z; r_[7] = a1.w;
+                        r8_[0] = b0.x; r8_[1] = b0.y; r8_[2] = b0.z; r8_[3] = b0.w;
+                        r8_[4] = b1.x; r8_[5] = b1.y; r8_[6] = b1.z; r8_[7] = b1.w;
+                        if (ASYM) {
+                            const uint2 q = __ldg(reinterpret_cast<const uint2*>(zp_r + g0));
+                            const uint2 q8 = __ldg(reinterpret_cast<const uint2*>(zp_r8 + g0));
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                z_[j] = (float)((q.x >> (8 * j)) & 0xFF);
+                                z_[j + 4] = (float)((q.y >> (8 * j)) & 0xFF);
+                                z8_[j] = (float)((q8.x >> (8 * j)) & 0xFF);
+                                z8_[j + 4] = (float)((q8.y >> (8 * j)) & 0xFF);
+                            }
+                        }
+                        return;
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < SEG; ++j) {
+                    const int sg = (kw >> (5 + LOG_CPG)) + j;
+                    const int g = min(gshift >= 0 ? (sg >> gshift) : sg / gdiv, Ng - 1);
+                    r_[j] = __ldg(sc_r + g);
+                    r8_[j] = __ldg(sc_r8 + g);
+                    if (ASYM) {
+                        z_[j] = (float)__ldg(zp_r + g);
+                        z8_[j] = (float)__ldg(zp_r8 + g);
+                    }
                 }
             }
         };
@@ -704,7 +761,7 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
                                     const float4 e1 = *reinterpret_cast<const float4*>(
                                         xs_st + 4 * seg * M + xt[nt][1]);
                                     float c00, c01, c10, c11;   // C0 + z C1 per (row, token)
-                                    if (ASYM) {
+                                    if (ASYM && !SB) {
                                         c00 = fmaf(zr[seg], e0.z, e0.y);
                                         c01 = fmaf(zr[seg], e1.z, e1.y);
                                         c10 = fmaf(zr8[seg], e0.z, e0.y);
@@ -712,6 +769,12 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
                                     } else {
                                         c00 = c10 = fmaf(8.f, e0.z, e0.y);
                                         c01 = c11 = fmaf(8.f, e1.z, e1.y);
+                                    }
+                                    if (ASYM && SB) {           // + o C1 (zr: offsets)
+                                        acc[nt][0] = fmaf(zr[seg], e0.z, acc[nt][0]);
+                                        acc[nt][1] = fmaf(zr[seg], e1.z, acc[nt][1]);
+                                        acc[nt][2] = fmaf(zr8[seg], e0.z, acc[nt][2]);
+                                        acc[nt][3] = fmaf(zr8[seg], e1.z, acc[nt][3]);
                                     }
                                     acc[nt][0] = fmaf(sr[seg], fmaf(e0.x, tmp[nt][0], -c00), acc[nt][0]);
                                     acc[nt][1] = fmaf(sr[seg], fmaf(e1.x, tmp[nt][1], -c01), acc[nt][1]);
@@ -1171,26 +1234,26 @@ k_w4a8g_gemv_m16(const __grid_constant__ CUtensorMap tmW, const GemvArgs a) {
 
 // Kernel instances that the plan may place two to an SM (M <= 8 for W4A16,
 // M <= 4 for W4A8) are compiled for two resident CTAs of 288 threads.
-template <int NT, int CPG, bool ASYM, bool SPLIT, bool SWIGLU, bool GROUPED>
+template <int NT, int CPG, bool ASYM, bool SPLIT, bool SWIGLU, bool GROUPED, bool SB>
 __device__ __forceinline__ void w4a16_body(const CUtensorMap* tm, const GemvArgs& a) {
     const Smem sm = gemv_init<GROUPED>(tm, a);
     if (threadIdx.x >= NCT) {
         if (threadIdx.x == NCT) gemv_producer<GROUPED>(tm, sm.wbuf, sm.xbuf, sm.ctl, a);
     } else {
-        w4a16_consumer<NT, CPG, ASYM, SPLIT, SWIGLU, GROUPED>(sm, a);
+        w4a16_consumer<NT, CPG, ASYM, SPLIT, SWIGLU, GROUPED, SB>(sm, a);
     }
 }
 
-template <int CPG, bool ASYM, bool SPLIT, bool SWIGLU, bool GROUPED = false>
+template <int CPG, bool ASYM, bool SPLIT, bool SWIGLU, bool GROUPED = false, bool SB = false>
 __global__ void __launch_bounds__(kGemvThreads, 2)
 k_w4a16_gemv_m8(const __grid_constant__ CUtensorMap tmW, const GemvArgs a) {
-    w4a16_body<1, CPG, ASYM, SPLIT, SWIGLU, GROUPED>(&tmW, a);
+    w4a16_body<1, CPG, ASYM, SPLIT, SWIGLU, GROUPED, SB>(&tmW, a);
 }
 
-template <int CPG, bool ASYM, bool SPLIT, bool SWIGLU, bool GROUPED = false>
+template <int CPG, bool ASYM, bool SPLIT, bool SWIGLU, bool GROUPED = false, bool SB = false>
 __global__ void __launch_bounds__(kGemvThreads, 1)
 k_w4a16_gemv_m16(const __grid_constant__ CUtensorMap tmW, const GemvArgs a) {
-    w4a16_body<2, CPG, ASYM, SPLIT, SWIGLU, GROUPED>(&tmW, a);
+    w4a16_body<2, CPG, ASYM, SPLIT, SWIGLU, GROUPED, SB>(&tmW, a);
 }
 
 template <int MT>
@@ -1259,38 +1322,39 @@ int launch(Kern kern, const uint8_t* packed, const GemvArgs& a, const GemvPlan& 
     return cudaGetLastError() == cudaSuccess ? W4_OK : W4_ERR_CUDA;
 }
 
-template <int NT, bool ASYM, bool SPLIT, bool SWIGLU, bool GROUPED = false>
+template <int NT, bool ASYM, bool SPLIT, bool SWIGLU, bool GROUPED = false, bool SB = false>
 int launch_w4a16_cpg(int cpg, const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
                      cudaStream_t st) {
     if (NT == 1) {
         switch (cpg) {
-            case 8: return launch(k_w4a16_gemv_m8<8, ASYM, SPLIT, SWIGLU, GROUPED>, packed, a, p, st);
-            case 4: return launch(k_w4a16_gemv_m8<4, ASYM, SPLIT, SWIGLU, GROUPED>, packed, a, p, st);
-            case 2: return launch(k_w4a16_gemv_m8<2, ASYM, SPLIT, SWIGLU, GROUPED>, packed, a, p, st);
-            default: return launch(k_w4a16_gemv_m8<1, ASYM, SPLIT, SWIGLU, GROUPED>, packed, a, p, st);
+            case 8: return launch(k_w4a16_gemv_m8<8, ASYM, SPLIT, SWIGLU, GROUPED, SB>, packed, a, p, st);
+            case 4: return launch(k_w4a16_gemv_m8<4, ASYM, SPLIT, SWIGLU, GROUPED, SB>, packed, a, p, st);
+            case 2: return launch(k_w4a16_gemv_m8<2, ASYM, SPLIT, SWIGLU, GROUPED, SB>, packed, a, p, st);
+            default: return launch(k_w4a16_gemv_m8<1, ASYM, SPLIT, SWIGLU, GROUPED, SB>, packed, a, p, st);
         }
     }
     switch (cpg) {
-        case 8: return launch(k_w4a16_gemv_m16<8, ASYM, SPLIT, SWIGLU, GROUPED>, packed, a, p, st);
-        case 4: return launch(k_w4a16_gemv_m16<4, ASYM, SPLIT, SWIGLU, GROUPED>, packed, a, p, st);
-        case 2: return launch(k_w4a16_gemv_m16<2, ASYM, SPLIT, SWIGLU, GROUPED>, packed, a, p, st);
-        default: return launch(k_w4a16_gemv_m16<1, ASYM, SPLIT, SWIGLU, GROUPED>, packed, a, p, st);
+        case 8: return launch(k_w4a16_gemv_m16<8, ASYM, SPLIT, SWIGLU, GROUPED, SB>, packed, a, p, st);
+        case 4: return launch(k_w4a16_gemv_m16<4, ASYM, SPLIT, SWIGLU, GROUPED, SB>, packed, a, p, st);
+        case 2: return launch(k_w4a16_gemv_m16<2, ASYM, SPLIT, SWIGLU, GROUPED, SB>, packed, a, p, st);
+        default: return launch(k_w4a16_gemv_m16<1, ASYM, SPLIT, SWIGLU, GROUPED, SB>, packed, a, p, st);
     }
 }
 
 // W4A16 decode launch for one K-split case (all group sizes and widths).
 // The token tile (8 or 16) follows a.M, or the per-group bound when grouped.
-template <bool SPLIT, bool SWIGLU = false, bool GROUPED = false>
+// SB: bf16 parameters; asymmetric when a.offs_b is set.
+template <bool SPLIT, bool SWIGLU = false, bool GROUPED = false, bool SB = false>
 int launch_w4a16_variant(const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
                          cudaStream_t st) {
     const int gq = a.G / 32;
     const int cpg = (gq % 8 == 0) ? 8 : (gq % 4 == 0) ? 4 : (gq % 2 == 0) ? 2 : 1;
-    const bool asym = a.zeros != nullptr;
+    const bool asym = SB ? a.offs_b != nullptr : a.zeros != nullptr;
     if ((GROUPED ? a.gmax : a.M) <= 8)
-        return asym ? launch_w4a16_cpg<1, true, SPLIT, SWIGLU, GROUPED>(cpg, packed, a, p, st)
-                    : launch_w4a16_cpg<1, false, SPLIT, SWIGLU, GROUPED>(cpg, packed, a, p, st);
-    return asym ? launch_w4a16_cpg<2, true, SPLIT, SWIGLU, GROUPED>(cpg, packed, a, p, st)
-                : launch_w4a16_cpg<2, false, SPLIT, SWIGLU, GROUPED>(cpg, packed, a, p, st);
+        return asym ? launch_w4a16_cpg<1, true, SPLIT, SWIGLU, GROUPED, SB>(cpg, packed, a, p, st)
+                    : launch_w4a16_cpg<1, false, SPLIT, SWIGLU, GROUPED, SB>(cpg, packed, a, p, st);
+    return asym ? launch_w4a16_cpg<2, true, SPLIT, SWIGLU, GROUPED, SB>(cpg, packed, a, p, st)
+                : launch_w4a16_cpg<2, false, SPLIT, SWIGLU, GROUPED, SB>(cpg, packed, a, p, st);
 }
 
 }  // namespace

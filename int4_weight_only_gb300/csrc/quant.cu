@@ -38,7 +38,8 @@ __device__ __forceinline__ float warp_min(float v) {
 __global__ void __launch_bounds__(256)
 k_pack_rtn(const float* __restrict__ W, int N, int K, int G, int Ng, int symmetric,
            uint8_t* __restrict__ packed, float* __restrict__ scales,
-           uint8_t* __restrict__ zeros) {
+           uint8_t* __restrict__ zeros, uint16_t* __restrict__ scales_b,
+           uint16_t* __restrict__ offs_b) {
     const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (wid >= (long long)N * Ng) return;
@@ -67,8 +68,14 @@ k_pack_rtn(const float* __restrict__ W, int N, int K, int G, int Ng, int symmetr
         if (s != 0.f) z = fminf(fmaxf(rintf(__fdiv_rn(-mn, s)), 0.f), 15.f);
     }
     if (lane == 0) {
-        scales[(size_t)n * Ng + g] = s;
-        if (!symmetric) zeros[(size_t)n * Ng + g] = (uint8_t)z;
+        if (scales_b) {
+            // bf16 parameters: bf16(s) and, asymmetric, bf16(fp32((8 - z) s))
+            scales_b[(size_t)n * Ng + g] = f32_to_bf16_bits(s);
+            if (!symmetric) offs_b[(size_t)n * Ng + g] = f32_to_bf16_bits(__fmul_rn(8.f - z, s));
+        } else {
+            scales[(size_t)n * Ng + g] = s;
+            if (!symmetric) zeros[(size_t)n * Ng + g] = (uint8_t)z;
+        }
     }
     // each lane packs 8 consecutive columns into one 32-bit word
     for (int k = k0 + lane * 8; k < k0 + G; k += 256) {
@@ -311,13 +318,14 @@ __global__ void k_scale_cols(float* W, const float* s, int rows, int cols) {
 __global__ void k_stream_fence() {}
 
 int launch_pack_rtn(const float* W, int N, int K, int G, int symmetric, uint8_t* packed,
-                    float* scales, uint8_t* zeros, cudaStream_t stream) {
+                    float* scales, uint8_t* zeros, uint16_t* scales_b, uint16_t* offs_b,
+                    cudaStream_t stream) {
     const int Ng = (K + G - 1) / G;
     const long long warps = (long long)N * Ng;
     const long long blocks = (warps * 32 + 255) / 256;
     if (blocks > 0x7fffffffLL) return W4_ERR_UNSUPPORTED_SHAPE;
     k_pack_rtn<<<(unsigned)blocks, 256, 0, stream>>>(W, N, K, G, Ng, symmetric, packed,
-                                                     scales, zeros);
+                                                     scales, zeros, scales_b, offs_b);
     // An ordinary launch starts only after k_pack_rtn has finished and its
     // stores are visible; a linear-layer kernel enqueued next may overlap
     // this empty kernel (programmatic dependent launch) and read the new

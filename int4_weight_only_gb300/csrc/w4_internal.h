@@ -74,6 +74,10 @@ struct GemvArgs {
     int E, gmax, NBg;         // groups, token bound, row blocks per group
     int list_off;             // shared-memory offset of the (group, token tile) list
     int list_cap;             // its capacity in items
+    // bf16 parameter layout (instead of scales / zeros): bf16 scales [N, Ng]
+    // and, asymmetric, bf16 offsets (8 - z) s [N, Ng]
+    const uint16_t* scales_b;
+    const uint16_t* offs_b;
 };
 
 // The launchers encode the tensor map of `packed` for the plan's box shape
@@ -86,6 +90,9 @@ bool gemv_tma_activations();
 int launch_w4a16_swiglu(const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
                         cudaStream_t stream);
 int launch_w4a16_gemv_split(const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
+                            cudaStream_t stream);
+// Decode with the bf16 parameter layout (a.scales_b, a.offs_b).
+int launch_w4a16_gemv_bf16p(const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
                             cudaStream_t stream);
 // Grouped decode (MoE experts): the tensor map covers the E * N stacked rows.
 int launch_w4a16_grouped(const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
@@ -122,15 +129,19 @@ struct GemmPlan {
     size_t ws_bytes = 0;
 };
 bool plan_gemm(int M, int N, int K, int G, int sm_count, GemmPlan* plan);
+// scales_b (and offs_b for asymmetric groups): the bf16 parameter layout.
 int launch_w4a16_gemm(const uint16_t* x, const uint8_t* packed, const float* scales,
                       const uint8_t* zeros, const float* bias, uint16_t* y, int M, int N, int K,
                       int Kp, int G, const GemmPlan& p, void* workspace, int* err,
-                      cudaStream_t stream);
+                      cudaStream_t stream, const uint16_t* scales_b = nullptr,
+                      const uint16_t* offs_b = nullptr);
 
 // ---------------------------------------------------------------- others
+// scales_b (and offs_b): write the bf16 parameter layout instead of fp32
+// scales and uint8 zero points.
 int launch_pack_rtn(const float* W, int N, int K, int G, int symmetric,
-                    uint8_t* packed, float* scales, uint8_t* zeros,
-                    cudaStream_t stream);
+                    uint8_t* packed, float* scales, uint8_t* zeros, uint16_t* scales_b,
+                    uint16_t* offs_b, cudaStream_t stream);
 // inv_s: SmoothQuant column factors 1/s (nullptr: none).
 int launch_act_quant(const uint16_t* x, const float* inv_s, int M, int K, int Kp, int8_t* qx,
                      float* sx, cudaStream_t stream);
