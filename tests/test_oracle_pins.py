@@ -723,3 +723,30 @@ def test_bf16_params_exact_for_power_of_two_scales():
         assert np.array_equal(s_b, s)
         assert np.array_equal(O.dequantize_bf16_params(packed, s_b, o_b, 32),
                               O.dequantize_f64(p32, s, z, 32))
+
+
+def test_gptq_hessian_closed_form():
+    """X a Hadamard matrix (X^T X = T I): H = (2/T) X^T X = 2 I exactly, with
+    zero rows and columns for the padded positions."""
+    K = 64
+    X = _hadamard(K).astype(np.float32)
+    H = O.gptq_hessian(X, K)
+    assert np.array_equal(H, 2.0 * np.eye(K))
+    Hp = O.gptq_hessian(X[:, :48], 64)          # 48 real columns, 16 padded
+    assert np.all(Hp[48:, :] == 0) and np.all(Hp[:, 48:] == 0)
+    assert np.allclose(np.diag(Hp)[:48], 2.0)
+
+
+def test_bf16_params_linear_reduces_to_the_linear():
+    """With power-of-two scales both layouts describe the same weights, so
+    the two linear oracles agree exactly."""
+    rng = np.random.default_rng(8)
+    W = rng.integers(-8, 8, size=(8, 64)).astype(np.float32) * 0.25
+    W[:, ::32] = -2.0
+    W[:, 1::32] = 1.75
+    x = _bf16_round(rng.standard_normal((3, 64)).astype(np.float32))
+    b = rng.standard_normal(8).astype(np.float32)
+    packed, s_b, o_b = O.pack_rtn_bf16(W, 32, False)
+    p32, s, z = O.pack_rtn(W, 32, False)
+    assert np.array_equal(O.w4a16_linear_bf16_params(x, packed, s_b, o_b, b, 64, 32),
+                          O.w4a16_linear(x, p32, s, z, b, 64, 32))
