@@ -63,9 +63,11 @@ extern "C" {
 #define W4_OK                       0
 #define W4_ERR_INVALID_ARG         -1  /* a size or flag is out of range      */
 #define W4_ERR_NULL_PTR            -2  /* a required pointer is NULL          */
-#define W4_ERR_MISALIGNED          -3  /* packed/x/qx not 16-byte aligned     */
+#define W4_ERR_MISALIGNED          -3  /* a buffer not aligned as the entry
+                                          point states (packed, x, qx: 16 B) */
 #define W4_ERR_UNSUPPORTED_GROUP   -4  /* group_size not a positive mult. of 32,
-                                          or not one group per row for W4A8  */
+                                          or a W4A8 group size the group-wise
+                                          kernel does not take               */
 #define W4_ERR_K_TOO_LARGE         -5  /* W4A8: Kp * 15 * 127 >= 2^31         */
 #define W4_ERR_WORKSPACE           -6  /* workspace NULL or too small         */
 #define W4_ERR_CUDA                -7  /* a CUDA runtime call failed          */
@@ -73,12 +75,12 @@ extern "C" {
 #define W4_ERR_DEVICE_TIMEOUT      -9  /* a kernel's bounded wait ran out     */
 #define W4_ERR_SCRATCH_LIMIT      -10  /* shape needs more split-K scratch than
                                           W4_NOALLOC_SCRATCH_BYTES            */
-#define W4_ERR_NOT_SPD            -12  /* device flag: w4_gptq met a non-positive
-                                          pivot (damped Hessian not positive
-                                          definite in fp32); results unreliable */
 #define W4_ERR_GROUP_TOKENS       -11  /* device flag: a group's token offsets
                                           were invalid; its rows of y were not
                                           written                             */
+#define W4_ERR_NOT_SPD            -12  /* device flag: w4_gptq met a non-positive
+                                          pivot (damped Hessian not positive
+                                          definite in fp32); results unreliable */
 
 /* Size of the library's built-in split-K scratch used by
  * w4a16_linear_noalloc (4 MiB, held by every GPU that loads the library).  */

@@ -96,6 +96,54 @@ def test_host_argument_checks(lib):
     assert lib.w4a8_quantize_act(None, 1, 64, 64, ok16, ok16, None) == c["W4_ERR_NULL_PTR"]
 
 
+def test_host_argument_checks_later_entry_points(lib):
+    """The entry points of the fused, grouped, smoothing, GPTQ and bf16
+    parameter paths reject bad arguments on the host."""
+    c = _codes()
+    P = ctypes.c_void_p
+    ok16 = P(0x10000)
+    odd = P(0x10001)
+    F = ctypes.c_float
+    # w4a16_linear_swiglu: F % 8 != 0, M > 16
+    sw = [ok16, ok16, ok16, None, None, ok16, 1, 64, 64, 32, 1, None, 0, None]
+    bad = list(sw); bad[7] = 12
+    assert lib.w4a16_linear_swiglu(*bad) == c["W4_ERR_INVALID_ARG"]
+    bad = list(sw); bad[6] = 17
+    assert lib.w4a16_linear_swiglu(*bad) == c["W4_ERR_UNSUPPORTED_SHAPE"]
+    # w4a16_grouped_linear: tile 0 and 17, E = 0, misaligned x
+    gr = [ok16, ok16, ok16, ok16, None, None, ok16, 8, 4, 64, 64, 32, 1, 4, None]
+    for i, v in ((13, 0), (13, 17), (8, 0)):
+        bad = list(gr); bad[i] = v
+        assert lib.w4a16_grouped_linear(*bad) == c["W4_ERR_INVALID_ARG"]
+    bad = list(gr); bad[0] = odd
+    assert lib.w4a16_grouped_linear(*bad) == c["W4_ERR_MISALIGNED"]
+    # w4a8_quantize_act_smooth: no factors, misaligned factors
+    assert lib.w4a8_quantize_act_smooth(ok16, None, 1, 64, 64, ok16, ok16, None) == c["W4_ERR_NULL_PTR"]
+    assert lib.w4a8_quantize_act_smooth(ok16, P(0x10004), 1, 64, 64, ok16, ok16, None) == \
+        c["W4_ERR_MISALIGNED"]
+    # w4_smooth: alpha outside [0, 1]
+    assert lib.w4_smooth(ok16, 4, ok16, 4, 64, F(1.5), ok16, ok16, None) == c["W4_ERR_INVALID_ARG"]
+    assert lib.w4_smooth(ok16, 4, ok16, 4, 64, F(-0.1), ok16, ok16, None) == c["W4_ERR_INVALID_ARG"]
+    # w4_gptq: no tokens, bad group, no workspace
+    gq = [ok16, 4, ok16, 8, 64, 32, 1, F(0.01), ok16, ok16, None, ok16, ok16, 1 << 30, None]
+    bad = list(gq); bad[1] = 0
+    assert lib.w4_gptq(*bad) == c["W4_ERR_INVALID_ARG"]
+    bad = list(gq); bad[5] = 48
+    assert lib.w4_gptq(*bad) == c["W4_ERR_UNSUPPORTED_GROUP"]
+    bad = list(gq); bad[12] = None
+    assert lib.w4_gptq(*bad) == c["W4_ERR_WORKSPACE"]
+    assert lib.w4_gptq_workspace_bytes(8, 64, 48) == 0
+    assert lib.w4_gptq_workspace_bytes(8, 64, 32) > 2 * 64 * 64 * 4
+    # bf16 parameters: symmetric with offsets, asymmetric without, misaligned scales
+    assert lib.w4_pack_rtn_bf16(ok16, 4, 64, 32, 1, ok16, ok16, ok16, None) == c["W4_ERR_INVALID_ARG"]
+    assert lib.w4_pack_rtn_bf16(ok16, 4, 64, 32, 0, ok16, ok16, None, None) == c["W4_ERR_NULL_PTR"]
+    bp = [ok16, ok16, ok16, None, None, ok16, 1, 64, 64, 32, None, 0, None]
+    bad = list(bp); bad[2] = P(0x10002)
+    assert lib.w4a16_linear_bf16p(*bad) == c["W4_ERR_MISALIGNED"]
+    bad = list(bp); bad[6] = 0
+    assert lib.w4a16_linear_bf16p(*bad) == c["W4_OK"]
+
+
 def test_w4a8_bound_constant_matches_int32():
     """W4_W4A8_MAX_KP is the largest Kp with Kp * 15 * 127 < 2^31 (codes in
     [0, 15] times q_x in [-127, 127])."""
