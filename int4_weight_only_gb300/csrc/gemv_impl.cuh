@@ -1,6 +1,12 @@
 // gemv_impl.cuh - decode kernels (M <= 16) for the INT4 weight-only linear
-// layer, shared by gemv.cu (planner, unsplit W4A16 and W4A8 launches) and
-// gemv_split.cu (W4A16 launches of K-split plans).
+// layer.  Each translation unit instantiates one family, so that adding a
+// family leaves the others' generated code as it was:
+//   gemv.cu         planner; W4A16 unsplit plans; W4A8 (one scale per row)
+//   gemv_split.cu   W4A16 K-split plans
+//   gemv_swiglu.cu  SWIGLU: gate|up row pairs, SiLU(gate) * up epilogue
+//   gemv_grouped.cu GROUPED: one matrix per group of tokens (experts)
+//   gemv_bf16p.cu   SB: bf16 scales and (8 - z) s offsets
+//   gemv_w4a8g.cu   W4A8 with one scale per group of G columns
 //
 // W4A16 ("Lab 5: Gemma4 端到端推理优化", sections "INT4 线性量化" and
 // "融合INT4反量化与矩阵乘"): y = x W_hat^T (+b) with W_hat = s (code - z),
