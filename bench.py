@@ -612,22 +612,19 @@ def measure_bf16p(w4, hbm, reps=200):
     step's linears are symmetric, so no offsets): per linear and per step,
     GB/s over its own algorithmic bytes (2-byte scales)."""
     lins = WL.decode_7b(1)
-    copies = []
     per_copy = sum(algorithmic_bytes(l, 1) for l in lins)
     R = max(2, math.ceil(3 * L2_BYTES / per_copy))
+    base = []                                   # (packed, bf16 scales) per linear
+    for lin in lins:
+        p, sb, _ = w4.w4_pack_rtn_bf16(WL.make_inputs(lin).W.cuda(), lin.group_size, True)
+        base.append((p, sb))
+    copies = []
     for r in range(R):
-        cp = []
-        for li, lin in enumerate(lins):
-            W = WL.make_inputs(lin).W.cuda() if r == 0 else None
-            if r == 0:
-                p, sb, ob = w4.w4_pack_rtn_bf16(W, lin.group_size, True)
-                del W
-            else:
-                p, sb, ob = copies[0][li]["p"].clone(), copies[0][li]["sb"].clone(), None
-            x = WL.make_activations(lin.K, 1, seed=10_000 + 97 * r + li).cuda()
-            cp.append(dict(p=p, sb=sb, x=x, y=torch.empty(1, lin.N, dtype=torch.bfloat16,
-                                                          device="cuda")))
-        copies.append(cp)
+        copies.append([dict(p=p.clone(), sb=sb.clone(),
+                            x=WL.make_activations(lin.K, 1, seed=10_000 + 97 * r + li).cuda(),
+                            y=torch.empty(1, lin.N, dtype=torch.bfloat16, device="cuda"))
+                       for li, (lin, (p, sb)) in enumerate(zip(lins, base))])
+    del base
     torch.cuda.synchronize()
 
     def call(li, i):
