@@ -110,6 +110,11 @@ DECODE_SOURCES = ["int4_weight_only_gb300/csrc/gemv.cu",
                   "int4_weight_only_gb300/csrc/w4_internal.h"]
 
 
+PREFILL_SOURCES = ["int4_weight_only_gb300/csrc/gemm_tc.cu",
+                   "int4_weight_only_gb300/csrc/w4_device.cuh",
+                   "int4_weight_only_gb300/csrc/w4_internal.h"]
+
+
 def recorded_traffic(kernel: str, digest: str):
     """DRAM bytes from a committed ncu summary (profiles/traffic.json), if
     it was taken on the current kernel source; otherwise None."""
@@ -225,22 +230,36 @@ def aggregate_gbs(bytes_per_rank_step: float, steps: int, world: int, sec: float
     return bytes_per_rank_step * steps * world / sec / 1e9
 
 
-def time_graph_steps(step_fn, K, R, world):
-    """Replay graphs holding exactly K calls step_fn(i); returns seconds."""
+def time_graph_steps(step_fn, K, R, world, reps=1, warm_s=0.0):
+    """Replay graphs holding exactly K calls step_fn(i); returns seconds.
+
+    reps > 1: the K-step region is timed `reps` times (each bracketed by a
+    barrier and a synchronize) and the list of the `reps` times is returned.
+    warm_s: untimed replays for that long first, so that the clocks sampled
+    during the timed regions are those of a loaded GPU."""
     g_full = make_graph(step_fn, R)
     g_rem = make_graph(step_fn, K % R) if K % R else None
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
-    ev0.record()
-    for _ in range(K // R):
-        g_full.replay()
-    if g_rem is not None:
-        g_rem.replay()
-    ev1.record()
-    torch.cuda.synchronize()
-    barrier(world)
-    return ev0.elapsed_time(ev1) / 1e3
+    if warm_s > 0:
+        t_end = time.perf_counter() + warm_s
+        while time.perf_counter() < t_end:
+            for _ in range(max(1, K // R)):
+                g_full.replay()
+            torch.cuda.synchronize()
+    out = []
+    for _ in range(reps):
+        barrier(world)
+        torch.cuda.synchronize()
+        ev0.record()
+        for _ in range(K // R):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        ev1.record()
+        torch.cuda.synchronize()
+        barrier(world)
+        out.append(ev0.elapsed_time(ev1) / 1e3)
+    return out if reps > 1 else out[0]
 
 
 # ---------------------------------------------------------------- our arm
@@ -368,22 +387,122 @@ def _oracle_step(sample):
     return by
 
 
-def cpu_baseline_decode(lins, frac=1 / 16, budget_s=12.0):
-    """The oracle as it stands, timed on a bounded sample of the step: the
-    four decode linears at M=1 restricted to a fixed 1/16 row sample
-    (oracle packing outside the timing; dequantize + fp64 matvec inside)."""
-    sample = _oracle_row_sample(lins, frac, seed=7)
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.startswith("Model name:"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith(("model name", "cpu part")):
+                    return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def _time_oracle_decode(lins, frac, budget_s, seed=7):
+    sample = _oracle_row_sample(lins, frac, seed=seed)
     by, t, n = 0.0, 0.0, 0
     while t < budget_s and n < 2000:
         t0 = time.perf_counter()
         by += _oracle_step(sample)
         t += time.perf_counter() - t0
         n += 1
-    return {"value": round(by / t / 1e9, 4), "unit": "GB/s", "cores": blas_threads(),
-            "kind": "oracle",
-            "sample": f"{n} passes of oracle w4a16_linear (numpy, fp64 dequantize + matvec) over "
-                      f"a fixed {frac:.4f} row sample of each of the four 7B decode linears, "
-                      f"M=1; {t:.1f} s"}
+    return by / t / 1e9, n, t
+
+
+def _time_oracle_w4a8(budget_s, frac=1 / 64):
+    """Oracle W4A8 (per-token INT8 quantize + int64 dot products) on a fixed
+    row sample of the three W4A8 linears at M = 1."""
+    import oracle as O
+    rng = np.random.default_rng(11)
+    sample = []
+    for lin in WL.w4a8_7b():
+        inp = WL.make_inputs(lin)
+        n = max(1, int(round(lin.N * frac)))
+        rows = np.sort(rng.choice(lin.N, n, replace=False))
+        op, os_, _ = O.pack_rtn(inp.W.numpy()[rows], lin.group_size, True)
+        sample.append((lin, inp.x, op, os_, algorithmic_bytes(lin, 1) * n / lin.N))
+    by, t, n = 0.0, 0.0, 0
+    while t < budget_s and n < 2000:
+        t0 = time.perf_counter()
+        for lin, x, op, os_, b in sample:
+            qx, sx = O.w4a8_quantize_act(x, lin.group_size)
+            O.w4a8_linear(qx, sx, op, os_, None)
+            by += b
+        t += time.perf_counter() - t0
+        n += 1
+    return by / t / 1e9, n, t
+
+
+def _time_oracle_prefill(budget_s, rows=16):
+    """Oracle prefill at M = 2048 on a fixed sample of output rows of the
+    two 7B MLP linears (fp64 dequantize + library matmul)."""
+    import oracle as O
+    rng = np.random.default_rng(13)
+    sample = []
+    for lin in WL.prefill_7b(2048):
+        inp = WL.make_inputs(lin)
+        r = np.sort(rng.choice(lin.N, rows, replace=False))
+        sample.append((lin, inp.x, O.pack_rtn(inp.W.numpy()[r], lin.group_size, True)))
+    fl, t, n = 0.0, 0.0, 0
+    while t < budget_s and n < 200:
+        t0 = time.perf_counter()
+        for lin, x, (op, os_, oz) in sample:
+            O.w4a16_linear(x, op, os_, oz, None, lin.K, lin.group_size)
+            fl += 2.0 * 2048 * rows * lin.K
+        t += time.perf_counter() - t0
+        n += 1
+    return fl / t / 1e12, n, t
+
+
+def cpu_baseline(lins, frac=1 / 16):
+    """The oracle as it stands, timed on bounded samples on the host cores:
+    the headline is the four 7B decode linears at M = 1 on a fixed 1/16 row
+    sample (oracle packing outside the timing; fp64 dequantize + matvec
+    inside) with the library's default threads; the same with one thread
+    (a child process with the BLAS/OpenMP thread counts set to 1), the W4A8
+    oracle and the prefill oracle are reported beside it."""
+    v, n, t = _time_oracle_decode(lins, frac, budget_s=8.0)
+    out = {"value": round(v, 4), "unit": "GB/s", "cores": blas_threads(), "kind": "oracle",
+           "sample": f"{n} passes of oracle w4a16_linear (numpy, fp64 dequantize + matvec) over "
+                     f"a fixed {frac:.4f} row sample of each of the four 7B decode linears, "
+                     f"M=1; {t:.1f} s",
+           "cpu_model": cpu_model(), "nproc": os.cpu_count()}
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-worker"],
+                           capture_output=True, text=True, timeout=300, env=env)
+        st = json.loads(r.stdout.strip().splitlines()[-1])
+        out["single_thread"] = {"value": st["value"], "unit": "GB/s", "cores": 1,
+                                "sample": st["sample"]}
+    except Exception as e:       # noqa: BLE001 - reported, not hidden
+        out["single_thread"] = {"error": f"{type(e).__name__}: {e}"[:200]}
+    v8, n8, t8 = _time_oracle_w4a8(budget_s=3.0)
+    out["w4a8"] = {"value": round(v8, 4), "unit": "GB/s", "cores": blas_threads(),
+                   "sample": f"{n8} passes of oracle w4a8_quantize_act + w4a8_linear (int64) "
+                             f"over a fixed 1/64 row sample of the three W4A8 linears; {t8:.1f} s"}
+    vp, npf, tp = _time_oracle_prefill(budget_s=3.0)
+    out["prefill_m2048"] = {"value": round(vp, 5), "unit": "TFLOP/s", "cores": blas_threads(),
+                            "sample": f"{npf} passes of oracle w4a16_linear at M=2048 over 16 "
+                                      f"sampled rows of each 7B MLP linear; {tp:.1f} s"}
+    return out
+
+
+def cpu_worker():
+    """Child process of cpu_baseline: the decode oracle sample with the
+    thread counts the parent set in the environment."""
+    v, n, t = _time_oracle_decode(WL.decode_7b(1), 1 / 16, budget_s=4.0)
+    print(json.dumps({"value": round(v, 4),
+                      "sample": f"{n} passes over the same 1/16 row sample, one thread; "
+                                f"{t:.1f} s"}))
 
 
 def measure_prefill(w4, M, bf16_peak, peak_kind, reps=20):
@@ -405,11 +524,18 @@ def measure_prefill(w4, M, bf16_peak, peak_kind, reps=20):
     del ds
     torch.cuda.empty_cache()
     tf = tot_f / tot_s / 1e12
+    tr = recorded_traffic("k_w4a16_gemm_tc", source_digest(PREFILL_SOURCES))
+    traffic = None
+    if tr is not None and str(M) in tr.get("dram_bytes_per_launch", {}):
+        traffic = tr["dram_bytes_per_launch"][str(M)]
     return {"M": M, "value": round(tf, 1), "unit": "TFLOP/s", "per_linear": out,
             "roofline": {"kernel": "k_w4a16_gemm_tc", "bound": "tensor", "achieved": round(tf, 1),
                          "peak": bf16_peak, "unit": "TFLOP/s", "frac": round(tf / bf16_peak, 4),
                          "peak_kind": f"{peak_kind} bf16_tflops (burst, kernel timed alone)",
-                         "traffic": None}}
+                         "traffic": traffic,
+                         "traffic_note": "DRAM bytes of one launch per linear (gate_up, down) "
+                                         "from an ncu capture of this source" if traffic else
+                                         "no ncu capture recorded for this source"}}
 
 
 class W4A8Set:
@@ -671,6 +797,9 @@ def measure_gptq(w4, reps=3):
             "ms_per_layer": round(e0.elapsed_time(e1) / reps, 2)}
 
 
+HEADLINE_REPS = 10        # timed regions of --steps steps; the median is reported
+
+
 def run_ours(args, world, rank):
     import int4_weight_only_gb300 as w4
     from int4_weight_only_gb300 import build as b
@@ -685,63 +814,90 @@ def run_ours(args, world, rank):
         ds.step(i)
     torch.cuda.synchronize()
     with ClockSampler(dev) as clk:
-        sec = time_graph_steps(ds.step, args.steps, ds.R, world)
-    sec = max_over_ranks(sec, world)
+        secs = time_graph_steps(ds.step, args.steps, ds.R, world, reps=HEADLINE_REPS,
+                                warm_s=0.3)
+    # per rank: the median of the timed regions; the job: the slowest rank
+    sec = max_over_ranks(statistics.median(secs), world)
+    sec_min = max_over_ranks(min(secs), world)
+    sec_max = max_over_ranks(max(secs), world)
     value = aggregate_gbs(ds.bytes_step, args.steps, world, sec)
-    res = {
-        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(sec / args.steps * 1e3, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded Gaussian weights and activations, 7B decode shapes)",
-        "config": {
-            "workload": "decode_7b M=1: qkv 4608x3584, o 3584x3584, gate_up 37888x3584, "
-                        "down 3584x18944; int4 G=128 symmetric; bf16 activations",
-            "M": 1, "bytes_per_step": ds.bytes_step,
-            "l2": f"rotating {ds.R} weight/activation copies ({ds.R * ds.bytes_step / 1e6:.0f} MB "
-                  f"> 2x L2) so every step reads cold HBM",
-            "timing": "CUDA graphs of the w4a16_linear calls, CUDA events, max over ranks",
-            "parallelism": f"replicas x{world}",
-        },
-        "gpu_launches": 4 * args.steps,
-        "clocks": clk.summary(),
-    }
     tr = recorded_traffic("k_w4a16_gemv", source_digest(DECODE_SOURCES))
-    res["roofline"] = {
+    roofline = {
         "kernel": "k_w4a16_gemv (all four launches of a step)", "bound": "hbm",
         "achieved": round(value / world, 1), "peak": hbm, "unit": "GB/s",
         "frac": round(value / world / hbm, 4), "peak_kind": f"{peak_kind} hbm_gbs",
         "traffic": None if tr is None else tr["dram_bytes_per_step"],
         "algorithmic_bytes_per_step": ds.bytes_step,
     }
-    res["per_linear"] = measure_linears(ds, reps=200)
+    per_linear = measure_linears(ds, reps=200)
     ke = min(args.steps, 2000)
     dt, h2d, d2h = measure_e2e(w4, ds, ke)
     dt = max_over_ranks(dt, world)
-    res["e2e"] = {"value": round(aggregate_gbs(ds.bytes_step, ke, world, dt), 1), "unit": "GB/s",
-                  "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                  "ms_per_step": round(dt / ke * 1e3, 4), "steps": ke}
+    e2e = {"value": round(aggregate_gbs(ds.bytes_step, ke, world, dt), 1), "unit": "GB/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "ms_per_step": round(dt / ke * 1e3, 4), "steps": ke}
     del ds
     torch.cuda.empty_cache()
+
+    subs = {}
     if not args.decode_only:
         # the other workloads: a failure is recorded in its own field and
         # does not take the headline measurement with it
-        subs = [("prefill", lambda: [measure_prefill(w4, M, bf16, peak_kind) for M in (2048, 512)]),
+        for name, fn in [
+                ("prefill", lambda: [measure_prefill(w4, M, bf16, peak_kind) for M in (2048, 512)]),
                 ("w4a8", lambda: measure_w4a8(w4, hbm)),
                 ("w4a8_g128", lambda: measure_w4a8(w4, hbm, group_size=128)),
                 ("decode_12b", lambda: measure_decode_12b(w4, hbm)),
                 ("swiglu_7b", lambda: measure_swiglu(w4, hbm)),
                 ("moe_decode", lambda: measure_moe(w4, hbm)),
                 ("gptq", lambda: measure_gptq(w4)),
-                ("decode7b_bf16_params", lambda: measure_bf16p(w4, hbm))]
-        for name, fn in subs:
+                ("decode7b_bf16_params", lambda: measure_bf16p(w4, hbm))]:
             try:
-                res[name] = fn()
+                subs[name] = fn()
             except Exception as e:          # noqa: BLE001 - reported, not hidden
-                res[name] = {"error": f"{type(e).__name__}: {e}"[:300]}
+                subs[name] = {"error": f"{type(e).__name__}: {e}"[:300]}
             torch.cuda.empty_cache()
+
+    # The line: the headline and the short per-config figures first (the
+    # second half of the metric, prefill at M = 2048, included), the long
+    # sub-objects last.
+    res = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(sec / args.steps * 1e3, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded Gaussian weights and activations, 7B decode shapes)",
+        "hbm_frac": round(value / world / hbm, 4),
+    }
+    pf = subs.get("prefill")
+    if isinstance(pf, list):
+        for p in pf:
+            tf = p["value"]
+            res[f"prefill_m{p['M']}_tflops"] = tf
+            res[f"prefill_m{p['M']}_frac_burst"] = round(tf / bf16, 4)
+            res[f"prefill_m{p['M']}_frac_sustained"] = round(tf / bf16_sus, 4)
+    res["per_linear_us"] = {p["name"].replace("decode7b_", ""): p["us"] for p in per_linear}
+    res["headline_timing"] = {
+        "regions": HEADLINE_REPS, "steps_per_region": args.steps, "reported": "median",
+        "ms_per_step_min": round(sec_min / args.steps * 1e3, 5),
+        "ms_per_step_max": round(sec_max / args.steps * 1e3, 5)}
+    res["config"] = {
+        "workload": "decode_7b M=1: qkv 4608x3584, o 3584x3584, gate_up 37888x3584, "
+                    "down 3584x18944; int4 G=128 symmetric; bf16 activations",
+        "M": 1, "bytes_per_step": int(sum(algorithmic_bytes(l, 1) for l in lins)),
+        "l2": "rotating weight/activation copies (> 3x L2) so every step reads cold HBM",
+        "timing": f"CUDA graphs of the w4a16_linear calls, CUDA events; median of "
+                  f"{HEADLINE_REPS} timed regions of --steps steps, max over ranks",
+        "parallelism": f"replicas x{world}",
+    }
+    res["gpu_launches"] = 4 * args.steps * HEADLINE_REPS
+    res["clocks"] = clk.summary()
+    res["roofline"] = roofline
+    res["e2e"] = e2e
     if rank == 0 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline_decode(lins)
+        res["cpu_baseline"] = cpu_baseline(lins)
+    res["per_linear"] = per_linear
+    res.update(subs)
     return res
 
 
@@ -841,7 +997,11 @@ def main():
                     help="run --reps calls of the workload linear whose name starts with this")
     ap.add_argument("--M", type=int, default=1)
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--cpu-worker", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.cpu_worker:
+        cpu_worker()
+        return
     if args.case:
         run_case(args)
         return

@@ -79,6 +79,8 @@ extern "C" int w4a16_linear_noalloc(const uint16_t* x, const uint8_t* packed,
         int rc = scratch_address(&base);
         if (rc) return rc;
         const size_t ticket_bytes = ((size_t)p.NB * 4 + 255) / 256 * 256;   // counters in use
+        // the clear must stay inside the counter prefix, below the partial sums
+        if (ticket_bytes > kCounterBytes) return W4_ERR_UNSUPPORTED_SHAPE;
         // The arrival counters must start at zero; the array keeps whatever
         // the previous call left, so clear them in stream order first.
         if (cudaMemsetAsync(base, 0, ticket_bytes, st) != cudaSuccess) return W4_ERR_CUDA;

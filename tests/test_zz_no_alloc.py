@@ -1,8 +1,11 @@
 """w4a16_linear_noalloc through the C ABI: the entry point for callers that
 cannot allocate device memory (a plugin handed only its input and output
-buffers, or a runtime that forbids cudaMalloc after start-up).  Its output
-must match w4a16_linear's on the same inputs, call after call, although it
-takes its split-K scratch from the library's own fixed array.
+buffers, or a runtime that forbids cudaMalloc after start-up).  It runs the
+same decode kernel and plan as w4a16_linear, taking its split-K scratch from
+the library's own fixed array, so its output must equal w4a16_linear's bit
+for bit and match the fp64 oracle within the layer's tolerance, call after
+call: two calls queued back to back on one stream before a single
+synchronize share the scratch in stream order.
 
 This file is collected last on purpose, so that a run stopping at the first
 failure has already run every other test; it also passes on its own."""
@@ -11,8 +14,9 @@ import ctypes
 import pytest
 import torch
 
+import oracle as O
 import workloads as WL
-from helpers import assert_close, ensure_built, to_np
+from helpers import assert_close, check_band, ensure_built, guarded_empty
 
 pytestmark = pytest.mark.gpu
 
@@ -37,27 +41,40 @@ def _noalloc(lib, x, packed, scales, zeros, bias, y, N, K, G):
                                     x.shape[0], N, K, G, 1 if zeros is None else 0, stream)
 
 
-@pytest.mark.parametrize("M,N,K,G,sym", [
-    (1, 3584, 18944, 128, True),     # the 7B down projection: split-K
-    (16, 4608, 3584, 128, False),    # 16 tokens, asymmetric, split-K
-    (3, 200, 100, 32, True),         # small ragged shape, no split
+@pytest.mark.parametrize("M,N,K,G,sym,split", [
+    (1, 3584, 18944, 128, True, True),     # the 7B down projection: K split over CTAs
+    (16, 4608, 3584, 128, False, True),    # 16 tokens, asymmetric, K split
+    (3, 200, 100, 32, True, False),        # small ragged shape, one pass over K
 ])
-def test_noalloc_matches_workspace_entry_point(w4, M, N, K, G, sym):
+def test_noalloc_matches_workspace_entry_point(w4, M, N, K, G, sym, split):
     lib = w4.load()
+    # a workspace size > 0 is what makes the plan split K, and so use the scratch
+    assert (w4.w4a16_workspace_bytes(M, N, K, G) > 0) == split
     seed = M + N + K
     packed, scales, zeros = WL.make_random_format(N, K, G, sym, seed)
-    packed, scales = packed.cuda(), scales.cuda()
+    bias = torch.randn(N, generator=torch.Generator().manual_seed(seed)) * 0.1
+    x = WL.make_activations(K, M, seed + 1)
+    ref = O.w4a16_linear(x, packed.numpy(), scales.numpy(),
+                         None if zeros is None else zeros.numpy(), bias.numpy(), K, G)
+    packed, scales, bias, x = packed.cuda(), scales.cuda(), bias.cuda(), x.cuda()
     zeros = None if zeros is None else zeros.cuda()
-    bias = (torch.randn(N, generator=torch.Generator().manual_seed(seed)) * 0.1).cuda()
-    x = WL.make_activations(K, M, seed + 1).cuda()
-    y_ref = w4.w4a16_linear(x, packed, scales, zeros, bias, N, K, G)
-    ref = to_np(y_ref).astype("float64")
-    for call in range(2):                       # two calls in a row share the scratch
-        y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    y_ws = w4.w4a16_linear(x, packed, scales, zeros, bias, N, K, G)
+    assert_close(y_ws, ref, "w4a16_linear")
+    # two calls queued back to back, one synchronize: the second call's
+    # counter clear and scratch use follow the first call in stream order
+    outs = []
+    for call in range(2):
+        y, band = guarded_empty((M, N), torch.bfloat16)
+        y.fill_(float("nan"))
         rc = _noalloc(lib, x, packed, scales, zeros, bias, y, N, K, G)
         assert rc == 0, lib.w4_error_string(rc)
-        torch.cuda.synchronize()
-        assert_close(y, ref, f"noalloc call {call}")
+        outs.append((y, band))
+    torch.cuda.synchronize()
+    for call, (y, band) in enumerate(outs):
+        check_band(band, f"noalloc call {call}")
+        assert_close(y, ref, f"noalloc call {call} vs oracle")
+        assert torch.equal(y.view(torch.int16), y_ws.view(torch.int16)), \
+            f"noalloc call {call} differs from w4a16_linear"
     assert w4.w4_get_device_error() == 0
 
 
