@@ -901,6 +901,94 @@ def run_ours(args, world, rank):
     return res
 
 
+def run_sharded(args, world, rank):
+    """The 7B decode step (M = 1) with every linear split over the `world`
+    ranks: --shard n splits the output rows (no exchange), --shard k the
+    input columns in group-aligned slices, with one NCCL all-reduce of the
+    fp32 partials per linear.  Strong scaling: the job is one whole step per
+    iteration, so `value` is the unsharded step's algorithmic bytes per
+    second.  Eager launches (the all-reduce sits between the kernels),
+    CUDA events, median of the timed regions, max over ranks."""
+    import int4_weight_only_gb300 as w4
+    from int4_weight_only_gb300 import build as b
+    from int4_weight_only_gb300.shard import (column_parallel_linear, pack_shard,
+                                              row_parallel_linear)
+    b.build()
+    w4.load()
+    hbm, _, _, peak_kind = load_peaks()
+    lins = WL.decode_7b(1)
+    bytes_step = sum(algorithmic_bytes(l, 1) for l in lins)
+    base = []
+    for lin in lins:
+        inp = WL.make_inputs(lin)
+        sh = pack_shard(inp.W.cuda(), lin.group_size, True, args.shard, world, rank)
+        base.append((lin, sh, inp.x.cuda()))
+        torch.cuda.synchronize()
+    shard_bytes = sum(sh.packed.numel() + 4 * sh.scales.numel() for _, sh, _ in base)
+    R = max(2, math.ceil(3 * L2_BYTES / max(shard_bytes, 1)))
+    copies = []
+    for r in range(R):
+        cp = []
+        for lin, sh, x in base:
+            c = type(sh)(**{**sh.__dict__, "packed": sh.packed.clone(), "scales": sh.scales.clone()})
+            xl = x if args.shard == "n" else x[:, sh.lo:sh.hi].contiguous()
+            y = torch.empty(1, lin.N if args.shard == "k" else sh.width, dtype=torch.bfloat16,
+                            device="cuda")
+            y32 = torch.empty(1, lin.N, dtype=torch.float32, device="cuda")
+            cp.append((c, xl, y, y32))
+        copies.append(cp)
+    torch.cuda.synchronize()
+
+    def step(i):
+        for c, xl, y, y32 in copies[i % R]:
+            if args.shard == "n":
+                column_parallel_linear(xl, c, y=y)
+            else:
+                row_parallel_linear(xl, c, y=y, y32=y32)
+
+    for i in range(max(args.warmup, 3)):
+        step(i)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    secs = []
+    dev = torch.cuda.current_device()
+    with ClockSampler(dev) as clk:
+        for _ in range(HEADLINE_REPS):
+            barrier(world)
+            torch.cuda.synchronize()
+            ev0.record()
+            for i in range(args.steps):
+                step(i)
+            ev1.record()
+            torch.cuda.synchronize()
+            barrier(world)
+            secs.append(ev0.elapsed_time(ev1) / 1e3)
+    sec = max_over_ranks(statistics.median(secs), world)
+    value = bytes_step * args.steps / sec / 1e9
+    launches = 4 * args.steps * HEADLINE_REPS * (2 if args.shard == "k" else 1)
+    return {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(sec / args.steps * 1e3, 5), "higher_is_better": True,
+        "scaling": "strong", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded Gaussian weights and activations, 7B decode shapes)",
+        "config": {"workload": "decode_7b M=1, every linear sharded over the ranks",
+                   "M": 1, "bytes_per_step": bytes_step,
+                   "parallelism": (f"tp{world} column-parallel (output rows), no exchange"
+                                   if args.shard == "n" else
+                                   f"tp{world} row-parallel (group-aligned K slices), "
+                                   f"one fp32 all-reduce per linear"),
+                   "timing": f"eager launches, CUDA events, median of {HEADLINE_REPS} timed "
+                             f"regions of --steps steps, max over ranks",
+                   "l2": f"rotating {R} copies of each rank's shard (> 3x L2)"},
+        "gpu_launches": launches, "clocks": clk.summary(),
+        "roofline": {"kernel": "k_w4a16_gemv (shards)", "bound": "hbm",
+                     "achieved": round(value / world, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(value / world / hbm, 4), "peak_kind": f"{peak_kind} hbm_gbs",
+                     "traffic": None},
+    }
+
+
 # ---------------------------------------------------------------- reference arm
 def run_reference(args):
     """The CPU oracle, as it stands, on the same workload and metric: each
@@ -997,6 +1085,9 @@ def main():
                     help="run --reps calls of the workload linear whose name starts with this")
     ap.add_argument("--M", type=int, default=1)
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--shard", choices=["n", "k"], default=None,
+                    help="time the decode step with every linear split over the ranks: "
+                         "n = output rows, k = group-aligned input columns + all-reduce")
     ap.add_argument("--cpu-worker", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.cpu_worker:
@@ -1015,7 +1106,7 @@ def main():
     torch.cuda.set_device(local)
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
-    res = run_ours(args, world, rank)
+    res = run_sharded(args, world, rank) if args.shard else run_ours(args, world, rank)
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:

@@ -175,6 +175,36 @@ W4_API int w4a16_linear(const uint16_t* x, const uint8_t* packed, const float* s
                  void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * w4a16_linear_partial / w4a16_partial_finish - one layer sharded across GPUs
+ * by its input columns (row-parallel): shard s owns a group-aligned slice
+ * [k0, k1) of K (k0 and k1 multiples of group_size, the last shard holding
+ * the ragged end), packed by w4_pack_rtn from W[:, k0:k1] (its codes and
+ * scales are exactly columns k0/2 .. k1/2 and groups k0/G .. k1/G of the
+ * whole layer's), and its slice x[:, k0:k1] of the activations.  Then
+ *  y = sum_s x_s W_hat_s^T + b:
+ * each shard computes its fp32 partial with w4a16_linear_partial, the
+ * partials are added across shards (one all-reduce, outside this library),
+ * and w4a16_partial_finish adds the bias and rounds to bf16 once.  The
+ * column-parallel split needs no entry point of its own: a shard's rows
+ * n0 .. n1 - 1 are a w4a16_linear of the rows' slice of packed, scales,
+ * zeros and bias.  The pages give the layer and its quantization, not its
+ * distribution ("Lab 5: Gemma4 端到端推理优化", sections "INT4 线性量化"
+ * and "Prefill和Decode分流"); the split is the usual tensor-parallel one.
+ *
+ *  w4a16_linear_partial: x, packed, scales, zeros, M, N, K, group_size,
+ *    symmetric, workspace as for w4a16_linear (K is the slice's width);
+ *    y32 [M, N] fp32 out, 4-byte aligned: sum_k x[m,k] W_hat[n,k], no bias.
+ *  w4a16_partial_finish: ysum [M, N] fp32 (the sum over shards), bias [N]
+ *    fp32 or NULL, y [M, N] bf16 out: y = bf16(ysum + bias).
+ * ------------------------------------------------------------------------- */
+W4_API int w4a16_linear_partial(const uint16_t* x, const uint8_t* packed, const float* scales,
+                                const uint8_t* zeros, float* y32, int M, int N, int K,
+                                int group_size, int symmetric, void* workspace,
+                                size_t workspace_bytes, void* stream);
+W4_API int w4a16_partial_finish(const float* ysum, const float* bias, uint16_t* y, int M, int N,
+                                void* stream);
+
+/* ---------------------------------------------------------------------------
  * w4_pack_rtn_bf16 / w4a16_linear_bf16p - the same layer with its group
  * parameters stored in bf16 (half the parameter bytes): bf16 scales, as the
  * TPU W4A16 layers load them ("Yeniden paketlenmiş QAT Gemma 4 26B-A4B, tek
@@ -361,6 +391,21 @@ W4_API int w4a8_linear(const int8_t* qx, const float* sx, const uint8_t* packed,
  * are then unspecified).  Returns W4_ERR_CUDA if the synchronization fails.
  * ------------------------------------------------------------------------- */
 W4_API int w4_get_device_error(void* stream);
+
+/* ---------------------------------------------------------------------------
+ * w4_set_wait_limit - how long a bounded wait inside the library's kernels
+ * (a stage of a copy pipeline, a device-side list) may take before the
+ * kernel gives up: it then raises W4_ERR_DEVICE_TIMEOUT in the device flag,
+ * every thread of the CTA leaves its loops, the copies it already issued are
+ * allowed to land (these drains always use the default limit), and the
+ * call's outputs are unspecified.  A short limit makes this failure path
+ * run on purpose, which is how it is tested without faulting a GPU.
+ *
+ *  cycles  SM clock cycles; <= 0 restores the default (2e9, about one second
+ *          on a GB300).  Applies to the current device, to kernels that start
+ *          after the value is written: the write is enqueued on `stream`.
+ * ------------------------------------------------------------------------- */
+W4_API int w4_set_wait_limit(long long cycles, void* stream);
 
 /* w4_error_string - static description of a W4_* code (never NULL). */
 W4_API const char* w4_error_string(int code);

@@ -21,6 +21,9 @@ _SIGS = {
                                       _c_int, _c_int, _vp]),
     "w4a16_linear": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
                               _c_int, _vp, _c_size, _vp]),
+    "w4a16_linear_partial": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
+                                      _c_int, _vp, _c_size, _vp]),
+    "w4a16_partial_finish": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _vp]),
     "w4_pack_rtn_bf16": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _vp, _vp]),
     "w4a16_linear_bf16p": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
                                     _vp, _c_size, _vp]),
@@ -38,6 +41,7 @@ _SIGS = {
     "w4a8_linear": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
                              _vp, _c_size, _vp]),
     "w4_get_device_error": (_c_int, [_vp]),
+    "w4_set_wait_limit": (_c_int, [ctypes.c_longlong, _vp]),
     "w4_error_string": (ctypes.c_char_p, [_c_int]),
 }
 EXPORTED = tuple(_SIGS)
@@ -211,6 +215,51 @@ def w4a16_linear(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
          int(group_size), 1 if zeros is None else 0),
         (_stream(x, stream),), x.device, workspace,
         lambda: lib.w4a16_workspace_bytes(M, N, K, group_size))
+    return y
+
+
+def w4a16_linear_partial(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
+                         zeros: Optional[torch.Tensor], N: int, K: int, group_size: int,
+                         y32=None, workspace=None, stream=None) -> torch.Tensor:
+    """y32 [M, N] fp32 = x [M, K] bf16 . W_hat^T without bias: a row-parallel
+    shard's partial sum (K is the shard's slice width)."""
+    M = x.shape[0]
+    _need(x, torch.bfloat16, (M, K), "x")
+    Kp = padded_k(K, group_size)
+    Ng = Kp // group_size
+    _need(packed, torch.uint8, (N, Kp // 2), "packed")
+    _need(scales, torch.float32, (N, Ng), "scales")
+    if zeros is not None:
+        _need(zeros, torch.uint8, (N, Ng), "zeros")
+    if y32 is None:
+        y32 = torch.empty(M, N, dtype=torch.float32, device=x.device)
+    _need(y32, torch.float32, (M, N), "y32")
+    if M == 0:
+        return y32
+    lib = load()
+    _call_with_workspace(
+        lib.w4a16_linear_partial, "w4a16_linear_partial",
+        (_ptr(x), _ptr(packed), _ptr(scales), _ptr(zeros), _ptr(y32), M, N, K,
+         int(group_size), 1 if zeros is None else 0),
+        (_stream(x, stream),), x.device, workspace,
+        lambda: lib.w4a16_workspace_bytes(M, N, K, group_size))
+    return y32
+
+
+def w4a16_partial_finish(ysum: torch.Tensor, bias: Optional[torch.Tensor], y=None,
+                         stream=None) -> torch.Tensor:
+    """y [M, N] bf16 = ysum [M, N] fp32 (+ bias [N] fp32), one rounding."""
+    M, N = ysum.shape
+    _need(ysum, torch.float32, (M, N), "ysum")
+    if bias is not None:
+        _need(bias, torch.float32, (N,), "bias")
+    if y is None:
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=ysum.device)
+    _need(y, torch.bfloat16, (M, N), "y")
+    if M == 0:
+        return y
+    _check("w4a16_partial_finish", load().w4a16_partial_finish(
+        _ptr(ysum), _ptr(bias), _ptr(y), M, N, _stream(ysum, stream)))
     return y
 
 
@@ -480,3 +529,10 @@ def w4a8_linear(qx: torch.Tensor, sx: torch.Tensor, packed: torch.Tensor,
 def w4_get_device_error(stream=None) -> int:
     s = stream if stream is not None else torch.cuda.current_stream()
     return int(load().w4_get_device_error(ctypes.c_void_p(s.cuda_stream)))
+
+
+def w4_set_wait_limit(cycles: int, stream=None) -> None:
+    """Limit (SM clock cycles) of the kernels' bounded waits on the current
+    device; 0 restores the default (about one second)."""
+    s = stream if stream is not None else torch.cuda.current_stream()
+    _check("w4_set_wait_limit", load().w4_set_wait_limit(int(cycles), ctypes.c_void_p(s.cuda_stream)))

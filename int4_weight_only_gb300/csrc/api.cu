@@ -1,16 +1,20 @@
 // api.cu - the extern "C" entry points of libw4 (declared in include/w4.h):
 // argument checks on the host, kernel selection, tensor-map encoding, and
 // the device error flag.  No entry point allocates or frees device memory.
+#include "w4_device.cuh"
 #include "w4_internal.h"
 
 #include <algorithm>
+#include <cstddef>
 #include <cstring>
 #include <cudaTypedefs.h>
 #include <mutex>
 
 namespace w4 {
 
-__device__ int g_device_error;           // set by bounded waits that give up
+// error flag (set by bounded waits that give up and by data checks) and the
+// wait limit, one block per device
+__device__ DeviceStatus g_status = {0, 0, 0};
 
 namespace {
 
@@ -58,7 +62,7 @@ int* device_error_flag() {
     if (d < 0) return nullptr;
     if (d < kMaxDevices && cache[d]) return cache[d];
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
     if (d < kMaxDevices) cache[d] = static_cast<int*>(p);
     return static_cast<int*>(p);
 }
@@ -244,6 +248,58 @@ int w4a16_linear(const uint16_t* x, const uint8_t* packed, const float* scales,
     a.R = p.R; a.SKE = p.SKE; a.nst = p.nst; a.S = p.S; a.spl = p.spl; a.units = p.units;
     a.XS = p.XS; a.red = p.red;
     return launch_w4a16_gemv(packed, a, p, st);
+}
+
+int w4a16_linear_partial(const uint16_t* x, const uint8_t* packed, const float* scales,
+                         const uint8_t* zeros, float* y32, int M, int N, int K, int group_size,
+                         int symmetric, void* workspace, size_t workspace_bytes, void* stream) {
+    if (!x || !packed || !scales || !y32) return W4_ERR_NULL_PTR;
+    if (symmetric && zeros) return W4_ERR_INVALID_ARG;
+    if (!symmetric && !zeros) return W4_ERR_NULL_PTR;
+    if (M < 0 || N <= 0) return W4_ERR_INVALID_ARG;
+    int rc = check_group(K, group_size);
+    if (rc) return rc;
+    const long long Kp = padded_k(K, group_size);
+    if (Kp > 0x7fffffffLL) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(x) || !aligned16(packed)) return W4_ERR_MISALIGNED;
+    if (!aligned4(scales) || !aligned4(y32)) return W4_ERR_MISALIGNED;
+    if (M == 0) return W4_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (M > 16) {
+        if (K % 8 != 0) return W4_ERR_UNSUPPORTED_SHAPE;
+        GemmPlan g;
+        if (!plan_gemm(M, N, K, group_size, current_sm_count(), &g)) return W4_ERR_UNSUPPORTED_SHAPE;
+        if (g.S > 1) {
+            if (!workspace || workspace_bytes < g.ws_bytes) return W4_ERR_WORKSPACE;
+            if (!aligned16(workspace)) return W4_ERR_MISALIGNED;
+        }
+        int* err = device_error_flag();
+        if (!err) return W4_ERR_CUDA;
+        return launch_w4a16_gemm(x, packed, scales, zeros, nullptr, nullptr, M, N, K, (int)Kp,
+                                 group_size, g, workspace, err, st, nullptr, nullptr, y32);
+    }
+    GemvPlan p;
+    if (!plan_gemv(M, N, (int)Kp, group_size, 2, current_sm_count(), &p)) return W4_ERR_UNSUPPORTED_SHAPE;
+    GemvArgs a{};
+    rc = split_workspace(p, workspace, workspace_bytes, &a.tickets, &a.partial);
+    if (rc) return rc;
+    a.x = x; a.scales = scales; a.zeros = zeros; a.bias = nullptr; a.y = nullptr; a.y32 = y32;
+    a.xtma = (K % 8) == 0 && gemv_tma_activations();
+    a.err = device_error_flag();
+    if (!a.err) return W4_ERR_CUDA;
+    a.M = M; a.N = N; a.K = K; a.Kp = (int)Kp; a.G = group_size; a.Ng = (int)(Kp / group_size);
+    a.R = p.R; a.SKE = p.SKE; a.nst = p.nst; a.S = p.S; a.spl = p.spl; a.units = p.units;
+    a.XS = p.XS; a.red = p.red;
+    return launch_w4a16_gemv_f32(packed, a, p, st);
+}
+
+int w4a16_partial_finish(const float* ysum, const float* bias, uint16_t* y, int M, int N,
+                         void* stream) {
+    if (!ysum || !y) return W4_ERR_NULL_PTR;
+    if (M < 0 || N <= 0) return W4_ERR_INVALID_ARG;
+    if (!aligned4(ysum) || (bias && !aligned4(bias)) || (reinterpret_cast<uintptr_t>(y) & 1))
+        return W4_ERR_MISALIGNED;
+    return launch_partial_finish(ysum, bias, y, M, N, static_cast<cudaStream_t>(stream));
 }
 
 int w4a16_linear_bf16p(const uint16_t* x, const uint8_t* packed, const uint16_t* scales_b,
@@ -489,6 +545,17 @@ int w4_get_device_error(void* stream) {
     if (cudaMemcpy(flag, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
         return W4_ERR_CUDA;
     return v;
+}
+
+int w4_set_wait_limit(long long cycles, void* stream) {
+    int* flag = device_error_flag();
+    if (!flag) return W4_ERR_CUDA;
+    const long long v = cycles > 0 ? cycles : 0;
+    char* block = reinterpret_cast<char*>(flag);
+    if (cudaMemcpyAsync(block + offsetof(DeviceStatus, wait_limit), &v, sizeof(v),
+                        cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return W4_ERR_CUDA;
+    return W4_OK;
 }
 
 const char* w4_error_string(int code) {

@@ -18,11 +18,10 @@
 //             tcgen05.mma cta_group::2 with M = 256, N = 256, and each CTA's
 //             TMEM receives its 128 rows x 256 tokens.
 // A unit of work is (output tile, K slice).  When a plan splits K S ways,
-// the S units of a tile run side by side (consecutive units go to
-// consecutive CTAs or pairs), each writes fp32 partials for the tokens of
-// the other S-1, waits until all S have, and reduces its own 1/S of the
-// tokens in split order 0..S-1 (its own term straight from TMEM), so every
-// output is summed in the same order on every run.
+// each unit writes its fp32 partial tile to the workspace and takes a
+// ticket; the last of the tile's S units to arrive adds the partials in
+// split order 0..S-1 (its own term straight from TMEM), so every output is
+// summed in the same order on every run and no unit ever waits for another.
 //
 // Warp roles (96 + 256 DQG + 128 threads, one CTA per SM, persistent):
 //   warp 0      TMA of the x tile (128-byte swizzle) into an NST-stage ring,
@@ -35,7 +34,8 @@
 //               (NSA stages): DQG groups of 8 warps take turns stage by
 //               stage, one weight row and 32 columns per thread
 //   last 4      epilogue: tcgen05.ld of the accumulator, + bias, bf16 stores
-//               (or the split-K hand-off)
+//               (or fp32 stores without bias for a row-parallel shard's
+//               partial sums; or the split-K hand-off)
 // Every mbarrier and counter wait is bounded; a failed wait raises the CTA
 // abort flag and the device error flag, in-flight copies and MMAs are
 // drained before exit.
@@ -67,6 +67,7 @@ struct GemmArgs {
     const uint16_t* offs_b;     // offsets (8 - z) s for asymmetric groups
     const float* bias;
     uint16_t* y;
+    float* y32;         // fp32 outputs without bias instead of y (row-parallel partials)
     float* partial;     // [S, M, N] when S > 1
     int* tickets;       // [ntiles] when S > 1
     int* err;
@@ -396,9 +397,6 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
         const int q = warp & 3;                            // TMEM lane quarter of this warp
         const int r = q * 32 + lane;
         const int etid = threadIdx.x - (THREADS - EPI_THREADS);
-        // with K split S ways, split s of a tile reduces tokens [s SL, s SL + SL)
-        // of it (SL a multiple of 32) and hands the rest to the other splits
-        const int SL = ((BN + a.S - 1) / a.S + 31) / 32 * 32;
         uint32_t tc = 0;
         for (int u = slot; u < a.units; u += nslots, ++tc) {
             int nb, tb, tile, s, ks0, ks1;
@@ -423,16 +421,16 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
 #pragma unroll
                         for (int i = 0; i < 32; ++i) {
                             const int t = t0 + j * 32 + i;
-                            if (t < a.M)
-                                a.y[(size_t)t * a.N + n] = f32_to_bf16_bits(__uint_as_float(v[i]) + bn);
+                            if (t < a.M) {
+                                if (a.y32) a.y32[(size_t)t * a.N + n] = __uint_as_float(v[i]);
+                                else a.y[(size_t)t * a.N + n] = f32_to_bf16_bits(__uint_as_float(v[i]) + bn);
+                            }
                         }
                     }
                 }
             } else if (ok) {
-                const int c0 = s * SL, c1 = min(c0 + SL, BN);
-                // 1. fp32 partials of the tokens the other splits reduce
+                // 1. this split's fp32 partial tile into the workspace
                 for (int j = 0; j < BN / 32 && t0 + j * 32 < a.M; ++j) {
-                    if (j * 32 >= c0 && j * 32 < c1) continue;
                     uint32_t v[32];
                     tmem_ld_32x32b_x32(tacc + j * 32, v);
                     tc_wait_ld();
@@ -443,20 +441,20 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                             if (t0 + j * 32 + i < a.M) dst[(size_t)i * a.N] = __uint_as_float(v[i]);
                     }
                 }
-                // 2. publish them; wait until all S splits of the tile have
+                // 2. publish it and take a ticket; the last of the S splits
+                //    to arrive reduces the whole tile, so no split ever waits
+                //    for another (nothing depends on the S units being
+                //    resident at the same time)
                 __threadfence();
                 named_bar_sync(2, EPI_THREADS);
-                if (etid == 0) {
-                    atomicAdd(ticket, 1);
-                    ctl->last = wait_counter_geq(ticket, a.S, &ctl->abort, a.err);
-                }
+                if (etid == 0) ctl->last = atomicAdd(ticket, 1) == a.S - 1;
                 named_bar_sync(2, EPI_THREADS);
-                ok = ctl->last;
-                if (ok) {
+                if (ctl->last) {
                     __threadfence();
-                    // 3. own slice: partials added in split order 0..S-1, this
-                    //    split's own term read straight from TMEM
-                    for (int j = c0 / 16; j * 16 < c1 && t0 + j * 16 < a.M; ++j) {
+                    // 3. partials added in split order 0..S-1 (this split's own
+                    //    term straight from TMEM), the same order whichever
+                    //    split arrives last
+                    for (int j = 0; j < BN / 16 && t0 + j * 16 < a.M; ++j) {
                         float acc[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) acc[i] = 0.f;
@@ -478,13 +476,15 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
 #pragma unroll
                             for (int i = 0; i < 16; ++i) {
                                 const int t = t0 + j * 16 + i;
-                                if (t < a.M) a.y[(size_t)t * a.N + n] = f32_to_bf16_bits(acc[i] + bn);
+                                if (t < a.M) {
+                                    if (a.y32) a.y32[(size_t)t * a.N + n] = acc[i];
+                                    else a.y[(size_t)t * a.N + n] = f32_to_bf16_bits(acc[i] + bn);
+                                }
                             }
                         }
                     }
-                    // 4. the last of the S splits to get here resets the counter
-                    named_bar_sync(2, EPI_THREADS);
-                    if (etid == 0 && atomicAdd(ticket, 1) == 2 * a.S - 1) *ticket = 0;
+                    // 4. every split has taken its ticket: reset the counter
+                    if (etid == 0) *ticket = 0;
                 }
             }
             tc_fence_before();
@@ -534,8 +534,7 @@ struct Variant {
     }
 
     // CTAs (or CTA pairs) of this variant resident at once on this device:
-    // the split-K hand-off needs every unit of a tile running together, so
-    // grids never exceed it
+    // the persistent grid is at most this
     static int slots(int sm_count) {
         static int cache[64] = {0};
         int dev = 0;
@@ -650,7 +649,9 @@ bool plan_gemm(int M, int N, int K, int G, int sm_count, GemmPlan* out) {
             const int units = ntiles * S;
             const int waves = (units + c.slots - 1) / c.slots;
             double cost = (double)waves * spl * c.stage;
-            if (S > 1) cost += 2.0 * waves * S * c.stage;
+            // split charge: each split writes its fp32 tile and the last one
+            // to arrive reads the other S - 1 back
+            if (S > 1) cost += 3.0 * waves * S * c.stage;
             if (cost < best * (1 - 1e-9)) {
                 best = cost;
                 found = true;
@@ -672,9 +673,10 @@ bool plan_gemm(int M, int N, int K, int G, int sm_count, GemmPlan* out) {
 int launch_w4a16_gemm(const uint16_t* x, const uint8_t* packed, const float* scales,
                       const uint8_t* zeros, const float* bias, uint16_t* y, int M, int N, int K,
                       int Kp, int G, const GemmPlan& p, void* workspace, int* err,
-                      cudaStream_t stream, const uint16_t* scales_b, const uint16_t* offs_b) {
+                      cudaStream_t stream, const uint16_t* scales_b, const uint16_t* offs_b,
+                      float* y32) {
     GemmArgs a{};
-    a.scales = scales; a.zeros = zeros; a.bias = bias; a.y = y; a.err = err;
+    a.scales = scales; a.zeros = zeros; a.bias = bias; a.y = y; a.y32 = y32; a.err = err;
     a.scales_b = scales_b; a.offs_b = offs_b;
     a.M = M; a.N = N; a.K = K; a.G = G; a.Ng = Kp / G;
     a.nks = p.nks; a.TB = p.TB; a.ntiles = p.ntiles; a.S = p.S; a.spl = p.spl; a.units = p.units;

@@ -7,6 +7,7 @@
 //   gemv_grouped.cu GROUPED: one matrix per group of tokens (experts)
 //   gemv_bf16p.cu   SB: bf16 scales and (8 - z) s offsets
 //   gemv_w4a8g.cu   W4A8 with one scale per group of G columns
+//   gemv_f32.cu     F32: fp32 partial outputs of a row-parallel shard
 //
 // W4A16 ("Lab 5: Gemma4 端到端推理优化", sections "INT4 线性量化" and
 // "融合INT4反量化与矩阵乘"): y = x W_hat^T (+b) with W_hat = s (code - z),
@@ -447,10 +448,13 @@ __device__ __forceinline__ bool split_k_arrive(const GemvArgs& a, SmemCtl* ctl, 
 // SB: bf16 parameters (a.scales_b, and for ASYM the offsets a.offs_b =
 // bf16((8 - z) s) in place of zero points): w_hat = s (code - 8) + o, so the
 // fix-up of a run is s (u tmp - C0 - 8 C1) + o C1.
+// F32: fp32 outputs a.y32 without the bias (the partial sum of a row-
+// parallel shard, added across shards and finished by w4a16_partial_finish).
 template <int NT, int CPG, bool ASYM, bool SPLIT, bool SWIGLU = false, bool GROUPED = false,
-          bool SB = false>
+          bool SB = false, bool F32 = false>
 __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
     static_assert(!(GROUPED && (SPLIT || SWIGLU)), "grouped plans are unsplit, plain epilogue");
+    static_assert(!(F32 && (SWIGLU || GROUPED || SB)), "fp32 partial outputs: plain layer only");
     constexpr int SEG = 8 / CPG;
     constexpr int LOG_CPG = CPG == 8 ? 3 : CPG == 4 ? 2 : CPG == 2 ? 1 : 0;
     constexpr bool PF = SEG <= 2;           // scales one stage ahead when they are few
@@ -846,8 +850,10 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
                     for (int j = 0; j < 4; ++j) {
                         const int t = nt * 8 + 2 * tig + (j & 1);
                         const int n = row0 + gid + 8 * (j >> 1);
-                        if (t < M && n < N)
-                            y[(size_t)t * N + n] = f32_to_bf16_bits(acc[nt][j] + ((j >> 1) ? b_hi : b_lo));
+                        if (t < M && n < N) {
+                            if constexpr (F32) a.y32[(size_t)t * N + n] = acc[nt][j];
+                            else y[(size_t)t * N + n] = f32_to_bf16_bits(acc[nt][j] + ((j >> 1) ? b_hi : b_lo));
+                        }
                     }
             }
         } else {
@@ -887,7 +893,8 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
                             const int n = row0 + gid + 8 * (j >> 1);
                             if (t < M && n < N) {
                                 const float v = sum_splits(part + (size_t)t * N + n, (size_t)M * N, Sp);
-                                y[(size_t)t * N + n] = f32_to_bf16_bits(v + ((j >> 1) ? b_hi : b_lo));
+                                if constexpr (F32) a.y32[(size_t)t * N + n] = v;
+                                else y[(size_t)t * N + n] = f32_to_bf16_bits(v + ((j >> 1) ? b_hi : b_lo));
                             }
                         }
                     }
@@ -1240,26 +1247,28 @@ k_w4a8g_gemv_m16(const __grid_constant__ CUtensorMap tmW, const GemvArgs a) {
 
 // Kernel instances that the plan may place two to an SM (M <= 8 for W4A16,
 // M <= 4 for W4A8) are compiled for two resident CTAs of 288 threads.
-template <int NT, int CPG, bool ASYM, bool SPLIT, bool SWIGLU, bool GROUPED, bool SB>
+template <int NT, int CPG, bool ASYM, bool SPLIT, bool SWIGLU, bool GROUPED, bool SB, bool F32>
 __device__ __forceinline__ void w4a16_body(const CUtensorMap* tm, const GemvArgs& a) {
     const Smem sm = gemv_init<GROUPED>(tm, a);
     if (threadIdx.x >= NCT) {
         if (threadIdx.x == NCT) gemv_producer<GROUPED>(tm, sm.wbuf, sm.xbuf, sm.ctl, a);
     } else {
-        w4a16_consumer<NT, CPG, ASYM, SPLIT, SWIGLU, GROUPED, SB>(sm, a);
+        w4a16_consumer<NT, CPG, ASYM, SPLIT, SWIGLU, GROUPED, SB, F32>(sm, a);
     }
 }
 
-template <int CPG, bool ASYM, bool SPLIT, bool SWIGLU, bool GROUPED = false, bool SB = false>
+template <int CPG, bool ASYM, bool SPLIT, bool SWIGLU, bool GROUPED = false, bool SB = false,
+          bool F32 = false>
 __global__ void __launch_bounds__(kGemvThreads, 2)
 k_w4a16_gemv_m8(const __grid_constant__ CUtensorMap tmW, const GemvArgs a) {
-    w4a16_body<1, CPG, ASYM, SPLIT, SWIGLU, GROUPED, SB>(&tmW, a);
+    w4a16_body<1, CPG, ASYM, SPLIT, SWIGLU, GROUPED, SB, F32>(&tmW, a);
 }
 
-template <int CPG, bool ASYM, bool SPLIT, bool SWIGLU, bool GROUPED = false, bool SB = false>
+template <int CPG, bool ASYM, bool SPLIT, bool SWIGLU, bool GROUPED = false, bool SB = false,
+          bool F32 = false>
 __global__ void __launch_bounds__(kGemvThreads, 1)
 k_w4a16_gemv_m16(const __grid_constant__ CUtensorMap tmW, const GemvArgs a) {
-    w4a16_body<2, CPG, ASYM, SPLIT, SWIGLU, GROUPED, SB>(&tmW, a);
+    w4a16_body<2, CPG, ASYM, SPLIT, SWIGLU, GROUPED, SB, F32>(&tmW, a);
 }
 
 template <int MT>
@@ -1328,39 +1337,42 @@ int launch(Kern kern, const uint8_t* packed, const GemvArgs& a, const GemvPlan& 
     return cudaGetLastError() == cudaSuccess ? W4_OK : W4_ERR_CUDA;
 }
 
-template <int NT, bool ASYM, bool SPLIT, bool SWIGLU, bool GROUPED = false, bool SB = false>
+template <int NT, bool ASYM, bool SPLIT, bool SWIGLU = false, bool GROUPED = false,
+          bool SB = false, bool F32 = false>
 int launch_w4a16_cpg(int cpg, const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
                      cudaStream_t st) {
     if (NT == 1) {
         switch (cpg) {
-            case 8: return launch(k_w4a16_gemv_m8<8, ASYM, SPLIT, SWIGLU, GROUPED, SB>, packed, a, p, st);
-            case 4: return launch(k_w4a16_gemv_m8<4, ASYM, SPLIT, SWIGLU, GROUPED, SB>, packed, a, p, st);
-            case 2: return launch(k_w4a16_gemv_m8<2, ASYM, SPLIT, SWIGLU, GROUPED, SB>, packed, a, p, st);
-            default: return launch(k_w4a16_gemv_m8<1, ASYM, SPLIT, SWIGLU, GROUPED, SB>, packed, a, p, st);
+            case 8: return launch(k_w4a16_gemv_m8<8, ASYM, SPLIT, SWIGLU, GROUPED, SB, F32>, packed, a, p, st);
+            case 4: return launch(k_w4a16_gemv_m8<4, ASYM, SPLIT, SWIGLU, GROUPED, SB, F32>, packed, a, p, st);
+            case 2: return launch(k_w4a16_gemv_m8<2, ASYM, SPLIT, SWIGLU, GROUPED, SB, F32>, packed, a, p, st);
+            default: return launch(k_w4a16_gemv_m8<1, ASYM, SPLIT, SWIGLU, GROUPED, SB, F32>, packed, a, p, st);
         }
     }
     switch (cpg) {
-        case 8: return launch(k_w4a16_gemv_m16<8, ASYM, SPLIT, SWIGLU, GROUPED, SB>, packed, a, p, st);
-        case 4: return launch(k_w4a16_gemv_m16<4, ASYM, SPLIT, SWIGLU, GROUPED, SB>, packed, a, p, st);
-        case 2: return launch(k_w4a16_gemv_m16<2, ASYM, SPLIT, SWIGLU, GROUPED, SB>, packed, a, p, st);
-        default: return launch(k_w4a16_gemv_m16<1, ASYM, SPLIT, SWIGLU, GROUPED, SB>, packed, a, p, st);
+        case 8: return launch(k_w4a16_gemv_m16<8, ASYM, SPLIT, SWIGLU, GROUPED, SB, F32>, packed, a, p, st);
+        case 4: return launch(k_w4a16_gemv_m16<4, ASYM, SPLIT, SWIGLU, GROUPED, SB, F32>, packed, a, p, st);
+        case 2: return launch(k_w4a16_gemv_m16<2, ASYM, SPLIT, SWIGLU, GROUPED, SB, F32>, packed, a, p, st);
+        default: return launch(k_w4a16_gemv_m16<1, ASYM, SPLIT, SWIGLU, GROUPED, SB, F32>, packed, a, p, st);
     }
 }
 
 // W4A16 decode launch for one K-split case (all group sizes and widths).
 // The token tile (8 or 16) follows a.M, or the per-group bound when grouped.
-// SB: bf16 parameters; asymmetric when a.offs_b is set.
-template <bool SPLIT, bool SWIGLU = false, bool GROUPED = false, bool SB = false>
+// SB: bf16 parameters; asymmetric when a.offs_b is set.  F32: fp32 outputs
+// a.y32 without bias.
+template <bool SPLIT, bool SWIGLU = false, bool GROUPED = false, bool SB = false,
+          bool F32 = false>
 int launch_w4a16_variant(const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
                          cudaStream_t st) {
     const int gq = a.G / 32;
     const int cpg = (gq % 8 == 0) ? 8 : (gq % 4 == 0) ? 4 : (gq % 2 == 0) ? 2 : 1;
     const bool asym = SB ? a.offs_b != nullptr : a.zeros != nullptr;
     if ((GROUPED ? a.gmax : a.M) <= 8)
-        return asym ? launch_w4a16_cpg<1, true, SPLIT, SWIGLU, GROUPED, SB>(cpg, packed, a, p, st)
-                    : launch_w4a16_cpg<1, false, SPLIT, SWIGLU, GROUPED, SB>(cpg, packed, a, p, st);
-    return asym ? launch_w4a16_cpg<2, true, SPLIT, SWIGLU, GROUPED, SB>(cpg, packed, a, p, st)
-                : launch_w4a16_cpg<2, false, SPLIT, SWIGLU, GROUPED, SB>(cpg, packed, a, p, st);
+        return asym ? launch_w4a16_cpg<1, true, SPLIT, SWIGLU, GROUPED, SB, F32>(cpg, packed, a, p, st)
+                    : launch_w4a16_cpg<1, false, SPLIT, SWIGLU, GROUPED, SB, F32>(cpg, packed, a, p, st);
+    return asym ? launch_w4a16_cpg<2, true, SPLIT, SWIGLU, GROUPED, SB, F32>(cpg, packed, a, p, st)
+                : launch_w4a16_cpg<2, false, SPLIT, SWIGLU, GROUPED, SB, F32>(cpg, packed, a, p, st);
 }
 
 }  // namespace

@@ -11,9 +11,26 @@
 
 namespace w4 {
 
-// A bounded wait gives up after this many SM clock cycles (about one second
-// at the GB300's clocks), records W4_ERR_DEVICE_TIMEOUT and returns false.
+// A bounded wait gives up after a limit of SM clock cycles, records
+// W4_ERR_DEVICE_TIMEOUT and returns false.  The default is about one second
+// at the GB300's clocks.
 constexpr long long kWaitLimitCycles = 2000000000LL;
+
+// The library's device status block (one per device): the error flag that
+// kernels set, then the wait limit (w4_set_wait_limit; 0 = the default).
+// Kernels receive the flag's address and read the limit from the same block
+// when a wait starts to take long.  Drains of copies already issued always
+// wait up to the default, so nothing is left in flight when a CTA exits.
+struct DeviceStatus {
+    int err;
+    int reserved;
+    long long wait_limit;
+};
+
+__device__ __forceinline__ long long wait_limit_of(const int* err) {
+    const long long v = reinterpret_cast<const volatile DeviceStatus*>(err)->wait_limit;
+    return v > 0 ? v : kWaitLimitCycles;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -58,10 +75,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           volatile int* abort, int* err) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
+    const long long lim = wait_limit_of(err);
     while (true) {
         if (*abort) return false;
         if (mbar_try_wait(bar, parity)) return true;
-        if (clock64() - t0 > kWaitLimitCycles) {
+        if (clock64() - t0 > lim) {
             *abort = 1;
             atomicCAS(err, 0, W4_ERR_DEVICE_TIMEOUT);
             return false;
@@ -80,26 +98,6 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, 
         }
     }
     return true;
-}
-
-// Waits until the global counter *p reaches `target` (acquire at GPU scope),
-// bounded like mbar_wait.  Only for counters that CTAs resident at the same
-// time increment.
-__device__ __forceinline__ bool wait_counter_geq(const int* p, int target, volatile int* abort,
-                                                 int* err) {
-    const long long t0 = clock64();
-    while (true) {
-        int v;
-        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-        if (v >= target) return true;
-        if (*abort) return false;
-        if (clock64() - t0 > kWaitLimitCycles) {
-            *abort = 1;
-            atomicCAS(err, 0, W4_ERR_DEVICE_TIMEOUT);
-            return false;
-        }
-        __nanosleep(100);
-    }
 }
 
 // ---------------------------------------------------------------- TMA
@@ -434,10 +432,11 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
                                                   volatile int* abort, int* err) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
     const long long t0 = clock64();
+    const long long lim = wait_limit_of(err);
     while (true) {
         if (*abort) return false;
         if (mbar_try_wait_cluster(bar, parity)) return true;
-        if (clock64() - t0 > kWaitLimitCycles) {
+        if (clock64() - t0 > lim) {
             *abort = 1;
             atomicCAS(err, 0, W4_ERR_DEVICE_TIMEOUT);
             return false;

@@ -78,6 +78,8 @@ struct GemvArgs {
     // and, asymmetric, bf16 offsets (8 - z) s [N, Ng]
     const uint16_t* scales_b;
     const uint16_t* offs_b;
+    // fp32 outputs [M, N] without bias (row-parallel partial sums), instead of y
+    float* y32;
 };
 
 // The launchers encode the tensor map of `packed` for the plan's box shape
@@ -99,6 +101,9 @@ int launch_w4a16_grouped(const uint8_t* packed, const GemvArgs& a, const GemvPla
                          cudaStream_t stream);
 int launch_w4a16_gemv(const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
                       cudaStream_t stream);
+// Decode with fp32 outputs a.y32 and no bias (split and unsplit plans).
+int launch_w4a16_gemv_f32(const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
+                          cudaStream_t stream);
 int launch_w4a8_gemv(const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
                      cudaStream_t stream);
 // Group-wise W4A8 (one weight scale per group of G columns, G < Kp):
@@ -130,11 +135,15 @@ struct GemmPlan {
 };
 bool plan_gemm(int M, int N, int K, int G, int sm_count, GemmPlan* plan);
 // scales_b (and offs_b for asymmetric groups): the bf16 parameter layout.
+// y32 (instead of y): fp32 outputs without the bias.
 int launch_w4a16_gemm(const uint16_t* x, const uint8_t* packed, const float* scales,
                       const uint8_t* zeros, const float* bias, uint16_t* y, int M, int N, int K,
                       int Kp, int G, const GemmPlan& p, void* workspace, int* err,
                       cudaStream_t stream, const uint16_t* scales_b = nullptr,
-                      const uint16_t* offs_b = nullptr);
+                      const uint16_t* offs_b = nullptr, float* y32 = nullptr);
+// ysum [M, N] fp32 + bias -> y bf16 (the last step of a row-parallel layer).
+int launch_partial_finish(const float* ysum, const float* bias, uint16_t* y, int M, int N,
+                          cudaStream_t stream);
 
 // ---------------------------------------------------------------- others
 // scales_b (and offs_b): write the bf16 parameter layout instead of fp32

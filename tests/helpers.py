@@ -84,6 +84,15 @@ class GuardedW4:
                          [("y", (x.shape[0], N), torch.bfloat16)],
                          x, packed, scales, zeros, bias, N, K, group_size, **kw)
 
+    def w4a16_linear_partial(self, x, packed, scales, zeros, N, K, group_size, **kw):
+        return self._run(self._mod.w4a16_linear_partial, "w4a16_linear_partial",
+                         [("y32", (x.shape[0], N), torch.float32)],
+                         x, packed, scales, zeros, N, K, group_size, **kw)
+
+    def w4a16_partial_finish(self, ysum, bias, **kw):
+        return self._run(self._mod.w4a16_partial_finish, "w4a16_partial_finish",
+                         [("y", tuple(ysum.shape), torch.bfloat16)], ysum, bias, **kw)
+
     def w4a16_linear_bf16p(self, x, packed, scales_b, offsets_b, bias, N, K, group_size, **kw):
         return self._run(self._mod.w4a16_linear_bf16p, "w4a16_linear_bf16p",
                          [("y", (x.shape[0], N), torch.bfloat16)],

@@ -144,6 +144,32 @@ def test_host_argument_checks_later_entry_points(lib):
     assert lib.w4a16_linear_bf16p(*bad) == c["W4_OK"]
 
 
+def test_host_argument_checks_shard_entry_points(lib):
+    """w4a16_linear_partial and w4a16_partial_finish reject bad arguments on
+    the host; M = 0 enqueues nothing."""
+    c = _codes()
+    P = ctypes.c_void_p
+    ok16 = P(0x10000)
+    odd = P(0x10001)
+    pa = [ok16, ok16, ok16, None, ok16, 1, 64, 64, 32, 1, None, 0, None]
+    bad = list(pa); bad[4] = None
+    assert lib.w4a16_linear_partial(*bad) == c["W4_ERR_NULL_PTR"]
+    bad = list(pa); bad[4] = P(0x10002)            # fp32 output, 4-byte aligned
+    assert lib.w4a16_linear_partial(*bad) == c["W4_ERR_MISALIGNED"]
+    bad = list(pa); bad[0] = odd
+    assert lib.w4a16_linear_partial(*bad) == c["W4_ERR_MISALIGNED"]
+    bad = list(pa); bad[8] = 40
+    assert lib.w4a16_linear_partial(*bad) == c["W4_ERR_UNSUPPORTED_GROUP"]
+    bad = list(pa); bad[9] = 0                     # asymmetric without zeros
+    assert lib.w4a16_linear_partial(*bad) == c["W4_ERR_NULL_PTR"]
+    bad = list(pa); bad[5] = 0
+    assert lib.w4a16_linear_partial(*bad) == c["W4_OK"]
+    assert lib.w4a16_partial_finish(None, None, ok16, 1, 8, None) == c["W4_ERR_NULL_PTR"]
+    assert lib.w4a16_partial_finish(ok16, None, odd, 1, 8, None) == c["W4_ERR_MISALIGNED"]
+    assert lib.w4a16_partial_finish(ok16, None, ok16, 1, 0, None) == c["W4_ERR_INVALID_ARG"]
+    assert lib.w4a16_partial_finish(ok16, None, ok16, 0, 8, None) == c["W4_OK"]
+
+
 def test_w4a8_bound_constant_matches_int32():
     """W4_W4A8_MAX_KP is the largest Kp with Kp * 15 * 127 < 2^31 (codes in
     [0, 15] times q_x in [-127, 127])."""
