@@ -398,14 +398,34 @@ W4_API int w4_get_device_error(void* stream);
  * kernel gives up: it then raises W4_ERR_DEVICE_TIMEOUT in the device flag,
  * every thread of the CTA leaves its loops, the copies it already issued are
  * allowed to land (these drains always use the default limit), and the
- * call's outputs are unspecified.  A short limit makes this failure path
- * run on purpose, which is how it is tested without faulting a GPU.
+ * call's outputs are unspecified.  A wait whose data does arrive can outlast
+ * the limit, since the hardware suspends a waiting thread until its barrier
+ * completes or its own time-out; with w4_set_fault_injection a wait that can
+ * never complete runs out, which is how this path is tested without a fault.
  *
  *  cycles  SM clock cycles; <= 0 restores the default (2e9, about one second
  *          on a GB300).  Applies to the current device, to kernels that start
  *          after the value is written: the write is enqueued on `stream`.
  * ------------------------------------------------------------------------- */
 W4_API int w4_set_wait_limit(long long cycles, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * w4_set_fault_injection - a switch for failure tests: it makes one wait of
+ * the grouped decode kernel (w4a16_grouped_linear) impossible to complete,
+ * so that the bounded-wait path above runs without any fault.  The pages
+ * have no counterpart; it exists to test the library.
+ *
+ *  mode  0: off (the default).  1: the kernel's consumers never publish the
+ *        list of groups, so its copy producer waits until the limit and
+ *        issues nothing.  2: the consumers never free a slot of the copy
+ *        ring, so the producer waits until the limit with copies in flight,
+ *        which it lets land before its CTA exits.  Either way the call
+ *        returns, W4_ERR_DEVICE_TIMEOUT is raised, and its outputs are
+ *        unspecified.  Other entry points ignore the switch.
+ *  Enqueued on `stream`, for kernels that start after it; applies to the
+ *  current device.  Returns W4_ERR_INVALID_ARG for other modes.
+ * ------------------------------------------------------------------------- */
+W4_API int w4_set_fault_injection(int mode, void* stream);
 
 /* w4_error_string - static description of a W4_* code (never NULL). */
 W4_API const char* w4_error_string(int code);

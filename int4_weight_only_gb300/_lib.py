@@ -42,6 +42,7 @@ _SIGS = {
                              _vp, _c_size, _vp]),
     "w4_get_device_error": (_c_int, [_vp]),
     "w4_set_wait_limit": (_c_int, [ctypes.c_longlong, _vp]),
+    "w4_set_fault_injection": (_c_int, [_c_int, _vp]),
     "w4_error_string": (ctypes.c_char_p, [_c_int]),
 }
 EXPORTED = tuple(_SIGS)
@@ -536,3 +537,11 @@ def w4_set_wait_limit(cycles: int, stream=None) -> None:
     device; 0 restores the default (about one second)."""
     s = stream if stream is not None else torch.cuda.current_stream()
     _check("w4_set_wait_limit", load().w4_set_wait_limit(int(cycles), ctypes.c_void_p(s.cuda_stream)))
+
+
+def w4_set_fault_injection(mode: int, stream=None) -> None:
+    """Failure-test switch of the grouped decode kernel (0 off, 1 the group
+    list is never published, 2 ring slots are never freed)."""
+    s = stream if stream is not None else torch.cuda.current_stream()
+    _check("w4_set_fault_injection",
+           load().w4_set_fault_injection(int(mode), ctypes.c_void_p(s.cuda_stream)))

@@ -68,7 +68,7 @@ struct GemmArgs {
     const float* bias;
     uint16_t* y;
     float* y32;         // fp32 outputs without bias instead of y (row-parallel partials)
-    float* partial;     // [S, M, N] when S > 1
+    float* partial;     // S > 1: [ntiles, S, CTAs per tile, BN / 32, 128 rows, 32] fp32
     int* tickets;       // [ntiles] when S > 1
     int* err;
     int M, N, K, G, Ng;
@@ -429,53 +429,62 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                     }
                 }
             } else if (ok) {
-                // 1. this split's fp32 partial tile into the workspace
+                // 1. this split's fp32 partial tile into the workspace, in the
+                //    accumulator's own layout: per 32-token block, thread r
+                //    holds row r's 32 tokens as 128 contiguous bytes (eight
+                //    16-byte stores; a warp writes 4 KB in one run)
+                float* ptile = a.partial + (((size_t)tile * a.S) * NCTA + rank) * (BM * BN);
+                const size_t split_stride = (size_t)NCTA * BM * BN;     // floats between splits
                 for (int j = 0; j < BN / 32 && t0 + j * 32 < a.M; ++j) {
                     uint32_t v[32];
                     tmem_ld_32x32b_x32(tacc + j * 32, v);
                     tc_wait_ld();
-                    if (n < a.N) {
-                        float* dst = a.partial + ((size_t)s * a.M + t0 + j * 32) * a.N + n;
+                    uint4* dst = reinterpret_cast<uint4*>(ptile + s * split_stride +
+                                                          (size_t)j * (BM * 32) + r * 32);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (t0 + j * 32 + i < a.M) dst[(size_t)i * a.N] = __uint_as_float(v[i]);
-                    }
+                    for (int i = 0; i < 8; ++i)
+                        dst[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
                 }
                 // 2. publish it and take a ticket; the last of the S splits
                 //    to arrive reduces the whole tile, so no split ever waits
                 //    for another (nothing depends on the S units being
                 //    resident at the same time)
-                __threadfence();
                 named_bar_sync(2, EPI_THREADS);
-                if (etid == 0) ctl->last = atomicAdd(ticket, 1) == a.S - 1;
+                if (etid == 0) ctl->last = atom_add_acq_rel_gpu(ticket, 1) == a.S - 1;
                 named_bar_sync(2, EPI_THREADS);
                 if (ctl->last) {
-                    __threadfence();
                     // 3. partials added in split order 0..S-1 (this split's own
                     //    term straight from TMEM), the same order whichever
-                    //    split arrives last
-                    for (int j = 0; j < BN / 16 && t0 + j * 16 < a.M; ++j) {
-                        float acc[16];
+                    //    split arrives last; the other splits' 128-byte runs
+                    //    are loaded eight 16-byte words at a time
+                    for (int j = 0; j < BN / 32 && t0 + j * 32 < a.M; ++j) {
+                        float acc[32];
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+                        for (int i = 0; i < 32; ++i) acc[i] = 0.f;
                         for (int qq = 0; qq < a.S; ++qq) {
-                            uint32_t v[16];
+                            uint32_t v[32];
                             if (qq == s) {
-                                tmem_ld_32x32b_x16(tacc + j * 16, v);
+                                tmem_ld_32x32b_x32(tacc + j * 32, v);
                                 tc_wait_ld();
-                            } else if (n < a.N) {
-                                const float* src = a.partial + ((size_t)qq * a.M + t0 + j * 16) * a.N + n;
+                            } else {
+                                const uint4* src = reinterpret_cast<const uint4*>(
+                                    ptile + qq * split_stride + (size_t)j * (BM * 32) + r * 32);
+                                uint4 w[8];
 #pragma unroll
-                                for (int i = 0; i < 16; ++i)
-                                    v[i] = t0 + j * 16 + i < a.M ? __float_as_uint(ld_cg_f32(src + (size_t)i * a.N)) : 0u;
+                                for (int i = 0; i < 8; ++i) w[i] = ld_cg_v4(src + i);
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) {
+                                    v[4 * i] = w[i].x; v[4 * i + 1] = w[i].y;
+                                    v[4 * i + 2] = w[i].z; v[4 * i + 3] = w[i].w;
+                                }
                             }
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) acc[i] += __uint_as_float(v[i]);
+                            for (int i = 0; i < 32; ++i) acc[i] += __uint_as_float(v[i]);
                         }
                         if (n < a.N) {
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                const int t = t0 + j * 16 + i;
+                            for (int i = 0; i < 32; ++i) {
+                                const int t = t0 + j * 32 + i;
                                 if (t < a.M) {
                                     if (a.y32) a.y32[(size_t)t * a.N + n] = acc[i];
                                     else a.y[(size_t)t * a.N + n] = f32_to_bf16_bits(acc[i] + bn);
@@ -651,7 +660,7 @@ bool plan_gemm(int M, int N, int K, int G, int sm_count, GemmPlan* out) {
             double cost = (double)waves * spl * c.stage;
             // split charge: each split writes its fp32 tile and the last one
             // to arrive reads the other S - 1 back
-            if (S > 1) cost += 3.0 * waves * S * c.stage;
+            if (S > 1) cost += 2.0 * waves * S * c.stage;
             if (cost < best * (1 - 1e-9)) {
                 best = cost;
                 found = true;
@@ -662,7 +671,11 @@ bool plan_gemm(int M, int N, int K, int G, int sm_count, GemmPlan* out) {
                 p.units = units;
                 p.grid = (c.pair ? 2 : 1) * (units < c.slots ? units : c.slots);
                 p.ticket_bytes = S > 1 ? kCounterBytes : 0;
-                p.ws_bytes = S > 1 ? p.ticket_bytes + (size_t)S * M * N * 4 : 0;
+                // split partials: one 128-row x BN-token fp32 tile per split,
+                // per CTA of each output tile
+                p.ws_bytes = S > 1 ? p.ticket_bytes + (size_t)S * ntiles * (c.pair ? 2 : 1) *
+                                                          BM * c.BN * 4
+                                   : 0;
                 *out = p;
             }
         }

@@ -6,9 +6,10 @@
 
 namespace w4 {
 
-bool gemv_tma_activations() {
+bool gemv_tma_activations(int M) {
     const char* e = std::getenv("W4_GEMV_XTMA");
-    return e && std::atoi(e) == 1;
+    if (e) return std::atoi(e) == 1;
+    return M >= 4;
 }
 
 namespace {

@@ -217,14 +217,18 @@ __device__ void gemv_producer(const CUtensorMap* tm, uint8_t* wbuf, uint8_t* xbu
 
 // Activations of one unit into shared memory as fp16, columns [k0, k0+nk).
 // nk is a multiple of 256, so the slice is a whole number of segments of
-// CPG*32 columns (one group's share of a box).  L neighbouring lanes take
-// one (token, segment), L = 16, 8 or 4 (the most that still covers the slice
-// in one pass of the 256 threads, at least 4; at most the segment's CPG*4
-// blocks): lane l converts the segment's 8-column blocks l, l+L, ..., and
-// log2(L) shuffle steps combine a segment.  bf16 values are
-// exactly representable in fp16 once a segment is scaled by a power of two
-// 2^-e that puts its max|x| in [2^14, 2^15); odd columns of every 8-column
-// block are further divided by 16 (exact) to match the 1024 + 16c weights of
+// CPG*32 columns (one group's share of a box, BLK = CPG*4 blocks of 8
+// columns).  An item is one (token, segment); L neighbouring lanes take it,
+// lane l converting the segment's blocks l, l+L, ... (BPL = BLK/L of them),
+// and log2(L) shuffle steps combine the segment.  L is chosen on the fly: the
+// fewest passes of the 256 threads over the items with at most 8 blocks a
+// lane (4 in the 96-register instances), then the most lanes that keep that
+// number of passes.  Each lane first
+// loads all its blocks into registers and only then uses them, so a pass costs
+// one load latency, not one per block.  bf16 values are exactly
+// representable in fp16 once a segment is scaled by a power of two 2^-e that
+// puts its max|x| in [2^14, 2^15); odd columns of every 8-column block are
+// further divided by 16 (exact) to match the 1024 + 16c weights of
 // nibbles_to_f16x2_biased, and each block is stored in the order
 // (0,4,1,5,2,6,3,7).  Columns >= K are zero.  Per segment and token,
 // xseg[4 * (segment * M + token) + {0, 1, 2}] holds u = 2^e,
@@ -235,13 +239,12 @@ __device__ void gemv_producer(const CUtensorMap* tm, uint8_t* wbuf, uint8_t* xbu
 // FROM_SMEM: the raw bf16 slice was already copied into xbuf (row m at
 // m * XS, natural order) and is converted in place; columns >= K hold stale
 // data there and are replaced by zeros.
-template <int CPG, bool FROM_SMEM>
-__device__ void stage_x_f16(uint8_t* xbuf, float* xseg, const uint16_t* x, int M, int K,
-                            int XS, int k0, int nk, int tid) {
-    const int nseg = nk / (CPG * 32);
-    int lg = 2;                                      // log2 of lanes per segment
-    while (lg < 4 && (4 << lg) <= CPG * 4 * 2 && M * nseg * (2 << lg) <= NCT) ++lg;
-    const int L = 1 << lg, BPL = CPG * 4 / L;        // lanes, blocks per lane
+template <int CPG, int L, bool FROM_SMEM>
+__device__ __forceinline__ void stage_x_f16_lanes(uint8_t* xbuf, float* xseg, const uint16_t* x,
+                                                  int M, int K, int XS, int k0, int nseg,
+                                                  int tid) {
+    constexpr int BLK = CPG * 4, BPL = BLK / L;
+    static_assert(BPL >= 1 && BPL <= 8 && L <= 32, "lanes per segment");
     const int items = M * nseg * L;
     const bool vec = (K & 7) == 0;
     const int lane = tid & 31;
@@ -250,64 +253,64 @@ __device__ void stage_x_f16(uint8_t* xbuf, float* xseg, const uint16_t* x, int M
     for (int base = tid - lane; base < items; base += NCT) {
         const int idx = base + lane;
         const bool on = idx < items;
-        const int l = idx & (L - 1), ts = on ? idx >> lg : 0;
+        const int l = idx & (L - 1), ts = on ? idx / L : 0;
         const int m = ts / nseg, sg = ts - m * nseg;
-        auto load = [&](int i, uint32_t* q) {
-            const int b = sg * (4 * CPG) + l + L * i;   // block within the slice
+        uint32_t q[BPL][4];
+#pragma unroll
+        for (int i = 0; i < BPL; ++i) {
+            const int b = sg * BLK + l + L * i;          // block within the slice
             const int k = k0 + b * 8;
             const uint16_t* src = x + (size_t)m * K + k;
-            if (FROM_SMEM) {
+            if (!on) {
+                q[i][0] = q[i][1] = q[i][2] = q[i][3] = 0u;
+            } else if (FROM_SMEM) {
                 if (k < K) {
                     const uint4 v = *reinterpret_cast<const uint4*>(xbuf + (size_t)m * XS + b * 16);
-                    q[0] = v.x; q[1] = v.y; q[2] = v.z; q[3] = v.w;
+                    q[i][0] = v.x; q[i][1] = v.y; q[i][2] = v.z; q[i][3] = v.w;
                 } else {
-                    q[0] = q[1] = q[2] = q[3] = 0u;
+                    q[i][0] = q[i][1] = q[i][2] = q[i][3] = 0u;
                 }
             } else if (vec && k + 8 <= K) {
                 const uint4 v = __ldg(reinterpret_cast<const uint4*>(src));
-                q[0] = v.x; q[1] = v.y; q[2] = v.z; q[3] = v.w;
+                q[i][0] = v.x; q[i][1] = v.y; q[i][2] = v.z; q[i][3] = v.w;
             } else {
                 uint16_t e[8];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) e[j] = (k + j < K) ? __ldg(src + j) : (uint16_t)0;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) q[j] = (uint32_t)e[2 * j] | ((uint32_t)e[2 * j + 1] << 16);
-            }
-        };
-        unsigned mx = 0;                      // bits of max|x| (non-negative floats order as ints)
-        if (on) {
-            for (int i = 0; i < BPL; ++i) {
-                uint32_t q[4];
-                load(i, q);
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    mx = max(mx, max((q[j] << 16) & 0x7FFFFFFFu, q[j] & 0x7FFF0000u));
+                for (int j = 0; j < 4; ++j) q[i][j] = (uint32_t)e[2 * j] | ((uint32_t)e[2 * j + 1] << 16);
             }
         }
+        unsigned mx = 0;                      // bits of max|x| (non-negative floats order as ints)
+#pragma unroll
+        for (int i = 0; i < BPL; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                mx = max(mx, max((q[i][j] << 16) & 0x7FFFFFFFu, q[i][j] & 0x7FFF0000u));
+#pragma unroll
         for (int o = 1; o < L; o <<= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         const int E = (int)(mx >> 23) - 127;
         const int e = mx == 0 ? 0 : max(E - 14, -100);
         const float sc = __int_as_float((127 - e) << 23);
         float se = 0.f, so = 0.f;
-        if (on) {
-            for (int i = 0; i < BPL; ++i) {
-                uint32_t q[4];
-                load(i, q);
-                float v[8];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    v[2 * j] = __uint_as_float(q[j] << 16) * sc;
-                    v[2 * j + 1] = __uint_as_float(q[j] & 0xFFFF0000u) * sc;
-                }
-                se += (v[0] + v[2]) + (v[4] + v[6]);
-                so += (v[1] + v[3]) + (v[5] + v[7]);
-                const float s16 = 0.0625f;
-                const int b = sg * (4 * CPG) + l + L * i;
+        for (int i = 0; i < BPL; ++i) {
+            float v[8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                v[2 * j] = __uint_as_float(q[i][j] << 16) * sc;
+                v[2 * j + 1] = __uint_as_float(q[i][j] & 0xFFFF0000u) * sc;
+            }
+            se += (v[0] + v[2]) + (v[4] + v[6]);
+            so += (v[1] + v[3]) + (v[5] + v[7]);
+            const float s16 = 0.0625f;
+            const int b = sg * BLK + l + L * i;
+            if (on)
                 *reinterpret_cast<uint4*>(xbuf + (size_t)m * XS + b * 16) =
                     make_uint4(pack_f16x2(v[0], v[4]), pack_f16x2(v[1] * s16, v[5] * s16),
                                pack_f16x2(v[2], v[6]), pack_f16x2(v[3] * s16, v[7] * s16));
-            }
         }
+#pragma unroll
         for (int o = 1; o < L; o <<= 1) {
             se += __shfl_xor_sync(0xffffffffu, se, o);
             so += __shfl_xor_sync(0xffffffffu, so, o);
@@ -317,6 +320,31 @@ __device__ void stage_x_f16(uint8_t* xbuf, float* xseg, const uint16_t* x, int M
             *reinterpret_cast<float4*>(xseg + 4 * (sg * M + m)) =
                 make_float4(u, u * fmaf(1024.f, se, 64.f * so), u * (se + so), 0.f);
         }
+    }
+}
+
+// MAXBPL: at most this many blocks (4 registers each) a lane, so that the
+// staging fits the register budget of the kernel instance it is inlined in.
+template <int CPG, bool FROM_SMEM, int MAXBPL>
+__device__ __forceinline__ void stage_x_f16(uint8_t* xbuf, float* xseg, const uint16_t* x, int M,
+                                            int K, int XS, int k0, int nk, int tid) {
+    constexpr int BLK = CPG * 4;
+    constexpr int LMIN = BLK > MAXBPL ? BLK / MAXBPL : 1;
+    const int nseg = nk / (CPG * 32);
+    const int items = M * nseg;
+    const int passes = (items * LMIN + NCT - 1) / NCT;
+    int L = LMIN;
+    while (L * 2 <= BLK && L * 2 <= 32 && (items * L * 2 + NCT - 1) / NCT <= passes) L *= 2;
+    switch (L) {
+#define W4_STAGE_CASE(LL)                                                                      \
+    case LL:                                                                                   \
+        if constexpr (LL >= LMIN && LL <= BLK && LL <= 32)                                     \
+            stage_x_f16_lanes<CPG, LL, FROM_SMEM>(xbuf, xseg, x, M, K, XS, k0, nseg, tid);     \
+        break;
+        W4_STAGE_CASE(1) W4_STAGE_CASE(2) W4_STAGE_CASE(4) W4_STAGE_CASE(8) W4_STAGE_CASE(16)
+        W4_STAGE_CASE(32)
+#undef W4_STAGE_CASE
+        default: break;
     }
 }
 
@@ -396,39 +424,33 @@ __device__ __forceinline__ float swiglu(float gate, float up) {
 }
 
 // Sum of S split partials p[0], p[stride], ..., added in split order.  The
-// loads of up to eight splits are issued before any add, so the last CTA of a
-// row block waits for one round trip per eight splits, not one per split.
-template <typename T>
+// loads of up to CH splits are issued before any add, so the last CTA of a
+// row block waits for one round trip per CH splits, not one per split.
+template <typename T, int CH = 8>
 __device__ __forceinline__ T sum_splits(const T* p, size_t stride, int S) {
     T v = 0;
-    int q = 0;
-    for (; q + 8 <= S; q += 8) {
-        T t[8];
+    for (int q = 0; q < S; q += CH) {
+        T t[CH];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) t[i] = ld_cg(p + (size_t)(q + i) * stride);
+        for (int i = 0; i < CH; ++i)
+            if (q + i < S) t[i] = ld_cg(p + (size_t)(q + i) * stride);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v += t[i];
+        for (int i = 0; i < CH; ++i)
+            if (q + i < S) v += t[i];
     }
-    T t[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-        if (q + i < S) t[i] = ld_cg(p + (size_t)(q + i) * stride);
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-        if (q + i < S) v += t[i];
     return v;
 }
 
 // Split-K hand-off: after this CTA's partials are written, the last CTA of
-// row block rb sees ctl->last set.  All consumer threads call it.
+// row block rb sees ctl->last set.  All consumer threads call it.  The CTA
+// barrier orders every thread's partial stores before thread 0's ticket,
+// whose acquire-release add at GPU scope publishes them to, and in the last
+// CTA makes visible, the other splits' stores (no full fence per thread).
 __device__ __forceinline__ bool split_k_arrive(const GemvArgs& a, SmemCtl* ctl, int rb) {
-    __threadfence();
     named_bar_sync(1, NCT);
-    if (threadIdx.x == 0) ctl->last = (atomicAdd(&a.tickets[rb], 1) == a.S - 1);
+    if (threadIdx.x == 0) ctl->last = atom_add_acq_rel_gpu(&a.tickets[rb], 1) == a.S - 1;
     named_bar_sync(1, NCT);
-    const bool last = ctl->last;
-    if (last) __threadfence();
-    return last;
+    return ctl->last;
 }
 
 // SPLIT: the plan splits K (Sp > 1).  The two cases are separate kernels
@@ -508,10 +530,12 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
     bool waited = false;
     const int* glist = nullptr;
     int prev_item = -1;
+    int inject = 0;                            // GROUPED: failure-test switches
     if constexpr (GROUPED) {
         // (group, token tile) items in group order, the same list in every CTA
         grid_dep_wait();
         waited = true;
+        inject = fault_injection_of(a.err);
         int* list = reinterpret_cast<int*>(sm.wbuf + a.list_off);
         int* wcnt = reinterpret_cast<int*>(sm.red);
         int nitems = 0;
@@ -553,7 +577,7 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
         }
         if (tid == 0) {
             ctl->nact = nitems;
-            mbar_arrive(&ctl->listready);
+            if (!(inject & kInjectNoList)) mbar_arrive(&ctl->listready);
         }
         units = nitems * a.NBg;
         glist = list;
@@ -707,12 +731,12 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
                 // then wait for this slice's copy and convert it in place
                 if (xi > 0 && tid == 0) mbar_arrive(&ctl->xempty);
                 if (mbar_wait(&ctl->xfull, xi & 1, &ctl->abort, a.err))
-                    stage_x_f16<CPG, true>(sm.xbuf, sm.xseg, x, M, K, XS, ks0 * SKE,
-                                           (ks1 - ks0) * SKE, tid);
+                    stage_x_f16<CPG, true, NT == 1 ? (SPLIT ? 2 : 4) : 8>(sm.xbuf, sm.xseg, x, M, K, XS,
+                                                            ks0 * SKE, (ks1 - ks0) * SKE, tid);
                 ++xi;
             } else {
-                stage_x_f16<CPG, false>(sm.xbuf, sm.xseg, x, M, K, XS, ks0 * SKE,
-                                        (ks1 - ks0) * SKE, tid);
+                stage_x_f16<CPG, false, NT == 1 ? (SPLIT ? 2 : 4) : 8>(sm.xbuf, sm.xseg, x, M, K, XS,
+                                                         ks0 * SKE, (ks1 - ks0) * SKE, tid);
             }
             named_bar_sync(1, NCT);
             prev0 = ks0;
@@ -804,7 +828,7 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl->empty[slot]);
+            if (lane == 0 && !(GROUPED && (inject & kInjectNoRelease))) mbar_arrive(&ctl->empty[slot]);
         }
 
         // ---- add the k-phases of each row tile, in order 0, 1, ..., WK-1

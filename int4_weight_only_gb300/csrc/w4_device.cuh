@@ -17,15 +17,27 @@ namespace w4 {
 constexpr long long kWaitLimitCycles = 2000000000LL;
 
 // The library's device status block (one per device): the error flag that
-// kernels set, then the wait limit (w4_set_wait_limit; 0 = the default).
-// Kernels receive the flag's address and read the limit from the same block
-// when a wait starts to take long.  Drains of copies already issued always
-// wait up to the default, so nothing is left in flight when a CTA exits.
+// kernels set, the fault-injection switch of the failure tests
+// (w4_set_fault_injection), then the wait limit (w4_set_wait_limit; 0 = the
+// default).  Kernels receive the flag's address and read the limit from the
+// same block when a wait starts to take long.  Drains of copies already
+// issued always wait up to the default, so nothing is left in flight when a
+// CTA exits.
 struct DeviceStatus {
     int err;
-    int reserved;
+    int inject;
     long long wait_limit;
 };
+
+// Fault-injection switches (read once per CTA by the grouped decode kernel
+// only): a wait that nothing will ever complete, so the failure path runs
+// without any fault.
+constexpr int kInjectNoList = 1;     // the consumers never publish the group list
+constexpr int kInjectNoRelease = 2;  // the consumers never free a ring slot
+
+__device__ __forceinline__ int fault_injection_of(const int* err) {
+    return reinterpret_cast<const volatile DeviceStatus*>(err)->inject;
+}
 
 __device__ __forceinline__ long long wait_limit_of(const int* err) {
     const long long v = reinterpret_cast<const volatile DeviceStatus*>(err)->wait_limit;
@@ -274,6 +286,25 @@ __device__ __forceinline__ int ld_cg_s32(const int* p) {
 }
 
 // L2-coherent loads (skip L1) for partial sums other CTAs wrote.
+// Atomic add with acquire-release semantics at GPU scope (returns the old
+// value): a split-K ticket.  Taken by one thread after a CTA barrier, it
+// publishes the CTA's earlier stores and, for the last arriver, makes the
+// other CTAs' stores visible to the loads that follow the next barrier.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v) {
+    int old;
+    asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;"
+                 : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+// 16-byte L2-coherent load (skips L1) of words another CTA wrote.
+__device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
 __device__ __forceinline__ float ld_cg(const float* p) { return ld_cg_f32(p); }
 __device__ __forceinline__ int32_t ld_cg(const int32_t* p) { return ld_cg_s32(p); }
 
@@ -340,11 +371,16 @@ __device__ __forceinline__ void tc_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// 32 consecutive columns of this warp's 32 TMEM lanes (one lane per thread).
+// 16 / 32 consecutive columns of this warp's 32 TMEM lanes (one lane per
+// thread).  The load and its tcgen05.wait::ld are one asm statement: the
+// load writes its registers asynchronously, so with a separate wait the
+// compiler could schedule register-only uses of the outputs (adds,
+// conversions) between the two, reading them before they land.
 __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t* r) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
           "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
           "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
@@ -355,7 +391,8 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t* r) 
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
         "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
           "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
           "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),

@@ -85,9 +85,10 @@ struct GemvArgs {
 // The launchers encode the tensor map of `packed` for the plan's box shape
 // and launch with programmatic dependent launch enabled.
 // Whether decode CTAs copy their activation slice into shared memory with a
-// bulk TMA copy (W4_GEMV_XTMA=1) instead of reading it from global memory
-// while converting it (the default: measured 3.5% faster on the 7B step).
-bool gemv_tma_activations();
+// bulk TMA copy before converting it (from 4 tokens up), instead of reading
+// it from global memory while converting it (1-3 tokens: measured 3.5%
+// faster on the 7B step at one token).  W4_GEMV_XTMA=0/1 overrides.
+bool gemv_tma_activations(int M);
 // Decode with the SwiGLU epilogue: a.N = 2F paired gate/up rows, y [M, F].
 int launch_w4a16_swiglu(const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
                         cudaStream_t stream);

@@ -4,13 +4,20 @@ Every wait in the library's kernels gives up after a limit of SM clock
 cycles (w4_set_wait_limit; about one second by default): the kernel raises
 W4_ERR_DEVICE_TIMEOUT in the device flag, every thread of the CTA leaves its
 loops, the producer lets the copies it already issued land, and the call
-returns with unspecified outputs.  A one-cycle limit makes a wait run out on
-a call whose copy pipeline must wait: the 7B down projection streams eight
-16 KB stages per CTA through a four-deep ring, so each producer waits for its
-consumers to free a slot; a grouped call's producer waits for the consumers
-to list the groups.  The tests check that such a call returns, that the flag
-reports the timeout, and that the next call with the default limit is right
-(so the split-K counters were left at zero and the context is usable)."""
+returns with unspecified outputs.  A wait whose data arrives completes in the
+hardware's own suspend of the waiting thread, so the tests make a wait that
+can never complete (w4_set_fault_injection, grouped decode kernel):
+
+* mode 1: the consumers never publish the group list, so the copy producer
+  times out before issuing anything;
+* mode 2: the consumers never free a ring slot, so the producer times out
+  with copies in flight (K = 16384: every unit has at least eight stages for
+  a four-deep ring) and drains them before its CTA exits.
+
+Each test checks that the call returns, that the flag reports the timeout,
+and that the next calls with the switch off and the default limit are right:
+the grouped call and a split-K decode call (so the device and the split-K
+counters are in order)."""
 import pytest
 import torch
 
@@ -21,6 +28,7 @@ from helpers import assert_close, ensure_built
 pytestmark = pytest.mark.gpu
 
 W4_ERR_DEVICE_TIMEOUT = -9
+SHORT_LIMIT = 20000            # SM cycles, ~10 us
 
 
 @pytest.fixture(scope="module")
@@ -30,30 +38,9 @@ def w4():
     return ensure_built()
 
 
-def test_decode_wait_runs_out_and_next_call_is_right(w4):
-    N, K, G = 3584, 18944, 128
-    assert w4.w4a16_workspace_bytes(1, N, K, G) > 0          # split-K plan
-    packed, scales, _ = WL.make_random_format(N, K, G, True, 3)
-    x = WL.make_activations(K, 1, 4)
-    ref = O.w4a16_linear(x, packed.numpy(), scales.numpy(), None, None, K, G)
-    packed, scales, xd = packed.cuda(), scales.cuda(), x.cuda()
-    assert w4.w4_get_device_error() == 0
-    w4.w4_set_wait_limit(1)
-    try:
-        w4.w4a16_linear(xd, packed, scales, None, None, N, K, G)
-        err = w4.w4_get_device_error()
-    finally:
-        w4.w4_set_wait_limit(0)
-    assert err == W4_ERR_DEVICE_TIMEOUT
-    for _ in range(2):
-        y = w4.w4a16_linear(xd, packed, scales, None, None, N, K, G)
-        assert_close(y, ref, "call after the timeout")
-        assert w4.w4_get_device_error() == 0
-
-
-def test_grouped_wait_runs_out_and_next_call_is_right(w4):
-    E, N, K, G = 8, 256, 1024, 32
-    counts = [3, 0, 5, 1, 0, 2, 7, 1]
+def _grouped_case():
+    E, N, K, G = 4, 128, 16384, 128
+    counts = [3, 0, 6, 2]
     T = sum(counts)
     packed, scales, _ = WL.make_random_format(E * N, K, G, True, 5)
     x = WL.make_activations(K, T, 6)
@@ -61,24 +48,52 @@ def test_grouped_wait_runs_out_and_next_call_is_right(w4):
     goff[1:] = torch.cumsum(torch.tensor(counts, dtype=torch.int32), 0)
     ref = O.w4a16_grouped_linear(x, goff.numpy(), packed.numpy(), scales.numpy(), None, None,
                                  E, N, K, G)
-    args = (x.cuda(), goff.cuda(), packed.cuda(), scales.cuda(), None, None, E, N, K, G, 8)
-    w4.w4_set_wait_limit(1)
+    # one-token tiles: the activation slice of a whole 16384-column row
+    # then fits the shared memory of a grouped plan (which never splits K)
+    args = (x.cuda(), goff.cuda(), packed.cuda(), scales.cuda(), None, None, E, N, K, G, 1)
+    return args, ref
+
+
+def _split_k_case():
+    N, K, G = 3584, 18944, 128
+    packed, scales, _ = WL.make_random_format(N, K, G, True, 3)
+    x = WL.make_activations(K, 1, 4)
+    ref = O.w4a16_linear(x, packed.numpy(), scales.numpy(), None, None, K, G)
+    return (x.cuda(), packed.cuda(), scales.cuda(), None, None, N, K, G), ref
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+def test_wait_runs_out_and_next_calls_are_right(w4, mode):
+    gargs, gref = _grouped_case()
+    dargs, dref = _split_k_case()
+    assert w4.w4a16_workspace_bytes(1, dargs[5], dargs[6], dargs[7]) > 0   # split-K plan
+    assert w4.w4_get_device_error() == 0
+    w4.w4_set_wait_limit(SHORT_LIMIT)
+    w4.w4_set_fault_injection(mode)
     try:
-        w4.w4a16_grouped_linear(*args)
+        w4.w4a16_grouped_linear(*gargs)
         err = w4.w4_get_device_error()
     finally:
+        w4.w4_set_fault_injection(0)
         w4.w4_set_wait_limit(0)
     assert err == W4_ERR_DEVICE_TIMEOUT
-    y = w4.w4a16_grouped_linear(*args)
-    assert_close(y, ref, "grouped call after the timeout")
+    for _ in range(2):
+        assert_close(w4.w4a16_grouped_linear(*gargs), gref, "grouped call after the timeout")
+        assert_close(w4.w4a16_linear(*dargs), dref, "split-K call after the timeout")
     assert w4.w4_get_device_error() == 0
 
 
-def test_default_limit_restored(w4):
-    """With the default limit an ordinary call raises nothing."""
-    lin = WL.tiny()[0]
-    packed, scales, _ = WL.make_random_format(lin.N, lin.K, lin.group_size, True, 9)
-    x = WL.make_activations(lin.K, 1, 10)
-    w4.w4a16_linear(x.cuda(), packed.cuda(), scales.cuda(), None, None, lin.N, lin.K,
-                    lin.group_size)
-    assert w4.w4_get_device_error() == 0
+def test_switch_is_ignored_elsewhere_and_rejects_bad_modes(w4):
+    """Only the grouped kernel reads the switch: a plain decode call with it
+    on is right and raises nothing."""
+    dargs, dref = _split_k_case()
+    w4.w4_set_fault_injection(2)
+    try:
+        y = w4.w4a16_linear(*dargs)
+        err = w4.w4_get_device_error()
+    finally:
+        w4.w4_set_fault_injection(0)
+    assert err == 0
+    assert_close(y, dref, "plain decode with the switch on")
+    with pytest.raises(w4.W4Error):
+        w4.w4_set_fault_injection(4)
