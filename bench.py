@@ -538,6 +538,27 @@ def measure_prefill(w4, M, bf16_peak, peak_kind, reps=20):
                                          "no ncu capture recorded for this source"}}
 
 
+def measure_mid_m(w4, hbm, bf16_peak, reps=20):
+    """The 7B gate_up and down linears from M = 16 (the largest decode size)
+    through the tensor-core path at M = 17 .. 128: per M and linear, time,
+    algorithmic GB/s and TFLOP/s (where the decode/prefill threshold sits)."""
+    out = []
+    for M in (16, 17, 32, 64, 128):
+        lins = [l for l in WL.decode_7b(M) if l.name.endswith(("gate_up", "down"))]
+        ds = DecodeSet(w4, lins, M, min_bytes=3 * L2_BYTES)
+        ds.step(0)
+        torch.cuda.synchronize()
+        per = measure_linears(ds, reps)
+        for p, lin in zip(per, lins):
+            sec = p["us"] * 1e-6
+            out.append({"M": M, "name": lin.name.replace("decode7b_", ""), "us": p["us"],
+                        "GB/s": p["GB/s"], "hbm_frac": round(p["GB/s"] / hbm, 4),
+                        "TFLOP/s": round(2.0 * M * lin.N * lin.K / sec / 1e12, 1)})
+        del ds
+        torch.cuda.empty_cache()
+    return out
+
+
 class W4A8Set:
     """Rotated copies of the W4A8 linears: per call, dynamic INT8 activation
     quantization then the integer GEMV."""
@@ -848,6 +869,7 @@ def run_ours(args, world, rank):
                 ("w4a8", lambda: measure_w4a8(w4, hbm)),
                 ("w4a8_g128", lambda: measure_w4a8(w4, hbm, group_size=128)),
                 ("decode_12b", lambda: measure_decode_12b(w4, hbm)),
+                ("mid_m", lambda: measure_mid_m(w4, hbm, bf16)),
                 ("swiglu_7b", lambda: measure_swiglu(w4, hbm)),
                 ("moe_decode", lambda: measure_moe(w4, hbm)),
                 ("gptq", lambda: measure_gptq(w4)),

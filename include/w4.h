@@ -251,6 +251,31 @@ W4_API int w4a16_linear_swiglu(const uint16_t* x, const uint8_t* packed, const f
                                size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * w4a16_linear_swiglu_q8 - w4a16_linear_swiglu that also emits the INT8
+ * activations of the W4A8 layer that follows it, in the same launch: the
+ * per-token dynamic quantization folded into the op before the integer
+ * GEMV ("Jetson Orin AGX INT4 推理优化实践", section 后续还能继续优化什么,
+ * item 2; the rule of [ORIN], as w4a8_quantize_act applies it to y):
+ *  y        as w4a16_linear_swiglu, [M, F] bf16 out, 16-byte aligned;
+ *  qx       [M, Fp] int8 out, Fp = ceil(F / q_group_size) * q_group_size,
+ *           16-byte aligned, columns F .. Fp-1 zero;
+ *  sx       [M] fp32 out;
+ *  q_group_size  the group size of the W4A8 layer that reads qx (a positive
+ *           multiple of 32; its padded K is Fp).
+ * qx and sx equal w4a8_quantize_act(y, q_group_size) bit for bit.  The last
+ * row block to finish reads y back and quantizes it, so the workspace is
+ * required even when the plan does not split K: at least
+ * max(w4a16_workspace_bytes(M, 2F, K, group_size), W4_WORKSPACE_COUNTER_BYTES)
+ * bytes, zero-filled once (its counters are left at zero).  M <= 16.
+ * ------------------------------------------------------------------------- */
+W4_API int w4a16_linear_swiglu_q8(const uint16_t* x, const uint8_t* packed,
+                                  const float* scales, const uint8_t* zeros,
+                                  const float* bias, uint16_t* y, int8_t* qx, float* sx,
+                                  int M, int F, int K, int group_size, int symmetric,
+                                  int q_group_size, void* workspace, size_t workspace_bytes,
+                                  void* stream);
+
+/* ---------------------------------------------------------------------------
  * w4a16_grouped_linear - grouped W4A16 linear over E groups (mixture-of-
  * experts layers), decode sizes: tokens sorted by group, each group's tokens
  * multiplied by that group's own quantized matrix in one launch:

@@ -29,6 +29,8 @@ _SIGS = {
                                     _vp, _c_size, _vp]),
     "w4a16_linear_swiglu": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
                                      _c_int, _c_int, _vp, _c_size, _vp]),
+    "w4a16_linear_swiglu_q8": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int,
+                                        _c_int, _c_int, _c_int, _c_int, _vp, _c_size, _vp]),
     "w4a16_grouped_linear": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
                                       _c_int, _c_int, _c_int, _c_int, _vp]),
     "w4a8_quantize_act": (_c_int, [_vp, _c_int, _c_int, _c_int, _vp, _vp, _vp]),
@@ -352,6 +354,46 @@ def w4a16_linear_swiglu(x: torch.Tensor, packed: torch.Tensor, scales: torch.Ten
         (_stream(x, stream),), x.device, workspace,
         lambda: lib.w4a16_workspace_bytes(M, 2 * F, K, group_size))
     return y
+
+
+def w4a16_linear_swiglu_q8(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
+                           zeros: Optional[torch.Tensor], bias: Optional[torch.Tensor], F: int,
+                           K: int, group_size: int, q_group_size: int, y=None, qx=None, sx=None,
+                           workspace=None, stream=None):
+    """w4a16_linear_swiglu that also returns the INT8 activations of the
+    W4A8 layer after it: (y [M, F] bf16, qx [M, Fp] int8, sx [M] fp32),
+    Fp = F padded to q_group_size; qx, sx = w4a8_quantize_act(y)."""
+    M = x.shape[0]
+    _need(x, torch.bfloat16, (M, K), "x")
+    Kp = padded_k(K, group_size)
+    Ng = Kp // group_size
+    Fp = padded_k(F, q_group_size)
+    _need(packed, torch.uint8, (2 * F, Kp // 2), "packed")
+    _need(scales, torch.float32, (2 * F, Ng), "scales")
+    if zeros is not None:
+        _need(zeros, torch.uint8, (2 * F, Ng), "zeros")
+    if bias is not None:
+        _need(bias, torch.float32, (2 * F,), "bias")
+    dev = x.device
+    if y is None:
+        y = torch.empty(M, F, dtype=torch.bfloat16, device=dev)
+    if qx is None:
+        qx = torch.empty(M, Fp, dtype=torch.int8, device=dev)
+    if sx is None:
+        sx = torch.empty(M, dtype=torch.float32, device=dev)
+    _need(y, torch.bfloat16, (M, F), "y")
+    _need(qx, torch.int8, (M, Fp), "qx")
+    _need(sx, torch.float32, (M,), "sx")
+    if M == 0:
+        return y, qx, sx
+    lib = load()
+    _call_with_workspace(
+        lib.w4a16_linear_swiglu_q8, "w4a16_linear_swiglu_q8",
+        (_ptr(x), _ptr(packed), _ptr(scales), _ptr(zeros), _ptr(bias), _ptr(y), _ptr(qx),
+         _ptr(sx), M, F, K, int(group_size), 1 if zeros is None else 0, int(q_group_size)),
+        (_stream(x, stream),), dev, workspace,
+        lambda: max(lib.w4a16_workspace_bytes(M, 2 * F, K, group_size), 64 << 10))
+    return y, qx, sx
 
 
 def w4a16_grouped_linear(x: torch.Tensor, goff: torch.Tensor, packed: torch.Tensor,

@@ -379,6 +379,48 @@ int w4a16_linear_swiglu(const uint16_t* x, const uint8_t* packed, const float* s
     return launch_w4a16_swiglu(packed, a, p, static_cast<cudaStream_t>(stream));
 }
 
+int w4a16_linear_swiglu_q8(const uint16_t* x, const uint8_t* packed, const float* scales,
+                           const uint8_t* zeros, const float* bias, uint16_t* y, int8_t* qx,
+                           float* sx, int M, int F, int K, int group_size, int symmetric,
+                           int q_group_size, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+    if (!x || !packed || !scales || !y || !qx || !sx) return W4_ERR_NULL_PTR;
+    if (symmetric && zeros) return W4_ERR_INVALID_ARG;
+    if (!symmetric && !zeros) return W4_ERR_NULL_PTR;
+    if (M < 0 || F <= 0 || (F % 8) != 0 || F > 0x3fffffff) return W4_ERR_INVALID_ARG;
+    int rc = check_group(K, group_size);
+    if (rc) return rc;
+    if (q_group_size <= 0 || (q_group_size % 32) != 0) return W4_ERR_UNSUPPORTED_GROUP;
+    const long long Kp = padded_k(K, group_size);
+    const long long Fp = padded_k(F, q_group_size);
+    if (Kp > 0x7fffffffLL || Fp > 0x7fffffffLL) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(x) || !aligned16(packed) || !aligned16(y) || !aligned16(qx))
+        return W4_ERR_MISALIGNED;
+    if (!aligned4(scales) || (bias && !aligned4(bias)) || !aligned4(sx)) return W4_ERR_MISALIGNED;
+    if (M > 16) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (M == 0) return W4_OK;
+    const int N = 2 * F;                        // gate/up row pairs
+    GemvPlan p;
+    if (!plan_gemv(M, N, (int)Kp, group_size, 2, current_sm_count(), &p)) return W4_ERR_UNSUPPORTED_SHAPE;
+    // the completion ticket sits in the counter prefix: a workspace is
+    // needed even when the plan does not split K
+    if (!workspace || workspace_bytes < std::max(p.ws_bytes, kCounterBytes)) return W4_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return W4_ERR_MISALIGNED;
+    GemvArgs a{};
+    rc = split_workspace(p, workspace, workspace_bytes, &a.tickets, &a.partial);
+    if (rc) return rc;
+    a.done = static_cast<int*>(workspace) + (kMaxCounters - 1);
+    a.qx = qx; a.sx_out = sx; a.Fp = (int)Fp;
+    a.x = x; a.scales = scales; a.zeros = zeros; a.bias = bias; a.y = y;
+    a.xtma = (K % 8) == 0 && gemv_tma_activations(M);
+    a.err = device_error_flag();
+    if (!a.err) return W4_ERR_CUDA;
+    a.M = M; a.N = N; a.K = K; a.Kp = (int)Kp; a.G = group_size; a.Ng = (int)(Kp / group_size);
+    a.R = p.R; a.SKE = p.SKE; a.nst = p.nst; a.S = p.S; a.spl = p.spl; a.units = p.units;
+    a.XS = p.XS; a.red = p.red;
+    return launch_w4a16_swiglu_q8(packed, a, p, static_cast<cudaStream_t>(stream));
+}
+
 int w4a16_grouped_linear(const uint16_t* x, const int32_t* goff, const uint8_t* packed,
                          const float* scales, const uint8_t* zeros, const float* bias,
                          uint16_t* y, int T, int E, int N, int K, int group_size, int symmetric,

@@ -68,7 +68,7 @@ struct GemmArgs {
     const float* bias;
     uint16_t* y;
     float* y32;         // fp32 outputs without bias instead of y (row-parallel partials)
-    float* partial;     // S > 1: [ntiles, S, CTAs per tile, BN / 32, 128 rows, 32] fp32
+    float* partial;     // S > 1: [ntiles, S, CTAs per tile, BN tokens, 128 rows] fp32
     int* tickets;       // [ntiles] when S > 1
     int* err;
     int M, N, K, G, Ng;
@@ -429,21 +429,22 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                     }
                 }
             } else if (ok) {
-                // 1. this split's fp32 partial tile into the workspace, in the
-                //    accumulator's own layout: per 32-token block, thread r
-                //    holds row r's 32 tokens as 128 contiguous bytes (eight
-                //    16-byte stores; a warp writes 4 KB in one run)
+                // 1. this split's fp32 partial tile into the workspace: one
+                //    contiguous region per (tile, split, CTA), token-major
+                //    with the 128 rows innermost, so that every warp store
+                //    (and every load of the reduction) covers 32 consecutive
+                //    floats.  (A layout with each thread's 32 tokens
+                //    contiguous, stored as 16-byte words at a 128-byte stride
+                //    across the warp, gave wrong accumulators in the CTA's
+                //    later units in the parity tests; see the design notes.)
                 float* ptile = a.partial + (((size_t)tile * a.S) * NCTA + rank) * (BM * BN);
                 const size_t split_stride = (size_t)NCTA * BM * BN;     // floats between splits
                 for (int j = 0; j < BN / 32 && t0 + j * 32 < a.M; ++j) {
                     uint32_t v[32];
                     tmem_ld_32x32b_x32(tacc + j * 32, v);
-                    tc_wait_ld();
-                    uint4* dst = reinterpret_cast<uint4*>(ptile + s * split_stride +
-                                                          (size_t)j * (BM * 32) + r * 32);
+                    float* dst = ptile + s * split_stride + (size_t)j * (BM * 32) + r;
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        dst[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                    for (int i = 0; i < 32; ++i) dst[(size_t)i * BM] = __uint_as_float(v[i]);
                 }
                 // 2. publish it and take a ticket; the last of the S splits
                 //    to arrive reduces the whole tile, so no split ever waits
@@ -455,8 +456,8 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                 if (ctl->last) {
                     // 3. partials added in split order 0..S-1 (this split's own
                     //    term straight from TMEM), the same order whichever
-                    //    split arrives last; the other splits' 128-byte runs
-                    //    are loaded eight 16-byte words at a time
+                    //    split arrives last; the 32 loads of a block are
+                    //    independent, so they are in flight together
                     for (int j = 0; j < BN / 32 && t0 + j * 32 < a.M; ++j) {
                         float acc[32];
 #pragma unroll
@@ -465,18 +466,10 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                             uint32_t v[32];
                             if (qq == s) {
                                 tmem_ld_32x32b_x32(tacc + j * 32, v);
-                                tc_wait_ld();
                             } else {
-                                const uint4* src = reinterpret_cast<const uint4*>(
-                                    ptile + qq * split_stride + (size_t)j * (BM * 32) + r * 32);
-                                uint4 w[8];
+                                const float* src = ptile + qq * split_stride + (size_t)j * (BM * 32) + r;
 #pragma unroll
-                                for (int i = 0; i < 8; ++i) w[i] = ld_cg_v4(src + i);
-#pragma unroll
-                                for (int i = 0; i < 8; ++i) {
-                                    v[4 * i] = w[i].x; v[4 * i + 1] = w[i].y;
-                                    v[4 * i + 2] = w[i].z; v[4 * i + 3] = w[i].w;
-                                }
+                                for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(ld_cg_f32(src + (size_t)i * BM));
                             }
 #pragma unroll
                             for (int i = 0; i < 32; ++i) acc[i] += __uint_as_float(v[i]);

@@ -100,7 +100,9 @@ bool plan_gemv_search(int M, int N, int Kp, int G, int act_bytes, int sm_count, 
                 const int spl = (nst + S - 1) / S;
                 const int Se = (nst + spl - 1) / spl;
                 if (spl > spl_max) continue;
-                if ((forced_s && Se != forced_s) || (Se > 1 && NB > kMaxCounters) ||
+                // the last counter of the prefix is the completion ticket of
+                // the SwiGLU call with INT8 outputs, never a row block's
+                if ((forced_s && Se != forced_s) || (Se > 1 && NB >= kMaxCounters) ||
                     (groups > 0 && Se > 1)) {
                     if (Se == nst) break;
                     continue;

@@ -8,6 +8,7 @@
 //   gemv_bf16p.cu   SB: bf16 scales and (8 - z) s offsets
 //   gemv_w4a8g.cu   W4A8 with one scale per group of G columns
 //   gemv_f32.cu     F32: fp32 partial outputs of a row-parallel shard
+//   gemv_swiglu_q8.cu Q8: SWIGLU with INT8 outputs for the W4A8 GEMV
 //
 // W4A16 ("Lab 5: Gemma4 端到端推理优化", sections "INT4 线性量化" and
 // "融合INT4反量化与矩阵乘"): y = x W_hat^T (+b) with W_hat = s (code - z),
@@ -453,6 +454,63 @@ __device__ __forceinline__ bool split_k_arrive(const GemvArgs& a, SmemCtl* ctl, 
     return ctl->last;
 }
 
+// The INT8 epilogue of the fused SwiGLU call ("Jetson Orin AGX INT4
+// 推理优化实践", section 后续还能继续优化什么, item 2: the activation
+// quantization folded into the op before the integer GEMV).  Called by every
+// consumer thread of a CTA once its row block's y is stored.  A completion
+// ticket counts the row blocks; the CTA that completes the last one reads
+// y [M, F] back (the other CTAs' stores are published by their
+// acquire-release tickets) and applies the per-token rule exactly as
+// w4a8_quantize_act does: s_x = fp32(max|y| / 127), q = clip(rint(fp32(y /
+// s_x)), -127, 127), columns F .. Fp-1 zero.  It then resets the ticket.
+__device__ __forceinline__ void swiglu_q8_finish(const GemvArgs& a, SmemCtl* ctl, float* red, int tid) {
+    named_bar_sync(1, NCT);                  // this CTA's y stores are all issued
+    if (tid == 0) ctl->last = atom_add_acq_rel_gpu(a.done, 1) == a.units / a.S - 1;
+    named_bar_sync(1, NCT);
+    if (!ctl->last) return;
+    const int F = a.N >> 1, nw = F >> 3, nwp = a.Fp >> 3;
+    const int warp = tid >> 5, lane = tid & 31;
+    for (int m = 0; m < a.M; ++m) {
+        const uint16_t* row = a.y + (size_t)m * F;
+        float mx = 0.f;
+        for (int w = tid; w < nw; w += NCT) {
+            const uint4 v = ld_cg_v4(row + 8 * w);
+            const uint32_t q[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(q[j] << 16)),
+                                     fabsf(__uint_as_float(q[j] & 0xFFFF0000u))));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (lane == 0) red[warp] = mx;
+        named_bar_sync(1, NCT);
+        float tot = 0.f;
+#pragma unroll
+        for (int w = 0; w < CW; ++w) tot = fmaxf(tot, red[w]);
+        const float sc = __fdiv_rn(tot, 127.0f);
+        const float rs = sc != 0.f ? __frcp_rn(sc) : 0.f;
+        if (tid == 0) a.sx_out[m] = sc;
+        for (int w = tid; w < nwp; w += NCT) {
+            uint2 o = make_uint2(0u, 0u);
+            if (w < nw) {
+                const uint4 v = ld_cg_v4(row + 8 * w);
+                const uint32_t q[4] = {v.x, v.y, v.z, v.w};
+                float f[8];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    f[2 * j] = __uint_as_float(q[j] << 16);
+                    f[2 * j + 1] = __uint_as_float(q[j] & 0xFFFF0000u);
+                }
+                o = quant_s8x8(f, sc, rs);
+            }
+            *reinterpret_cast<uint2*>(a.qx + (size_t)m * a.Fp + 8 * w) = o;
+        }
+        named_bar_sync(1, NCT);              // red is reused by the next token
+    }
+    if (tid == 0) *a.done = 0;
+}
+
 // SPLIT: the plan splits K (Sp > 1).  The two cases are separate kernels
 // so that the split-K hand-off code does not take part in the register
 // allocation and scheduling of the unsplit kernels' main loop (measured: it
@@ -472,11 +530,14 @@ __device__ __forceinline__ bool split_k_arrive(const GemvArgs& a, SmemCtl* ctl, 
 // fix-up of a run is s (u tmp - C0 - 8 C1) + o C1.
 // F32: fp32 outputs a.y32 without the bias (the partial sum of a row-
 // parallel shard, added across shards and finished by w4a16_partial_finish).
+// Q8 (with SWIGLU): the last row block to finish also quantizes the whole
+// output y [M, F] to INT8 (swiglu_q8_finish).
 template <int NT, int CPG, bool ASYM, bool SPLIT, bool SWIGLU = false, bool GROUPED = false,
-          bool SB = false, bool F32 = false>
+          bool SB = false, bool F32 = false, bool Q8 = false>
 __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
     static_assert(!(GROUPED && (SPLIT || SWIGLU)), "grouped plans are unsplit, plain epilogue");
     static_assert(!(F32 && (SWIGLU || GROUPED || SB)), "fp32 partial outputs: plain layer only");
+    static_assert(!Q8 || (SWIGLU && !GROUPED && !SB && !F32), "INT8 outputs: SwiGLU epilogue only");
     constexpr int SEG = 8 / CPG;
     constexpr int LOG_CPG = CPG == 8 ? 3 : CPG == 4 ? 2 : CPG == 2 ? 1 : 0;
     constexpr bool PF = SEG <= 2;           // scales one stage ahead when they are few
@@ -866,6 +927,7 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
                                 swiglu(acc[nt][j] + b_lo, acc[nt][j + 2] + b_hi));
                     }
             }
+            if constexpr (Q8) swiglu_q8_finish(a, ctl, sm.red, tid);
         } else if constexpr (!SPLIT) {
             if (kp == 0) {
 #pragma unroll
@@ -924,6 +986,7 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
                     }
                 }
                 if (tid == 0) a.tickets[rb] = 0;
+                if constexpr (Q8) swiglu_q8_finish(a, ctl, sm.red, tid);
             }
         }
     }
@@ -1271,28 +1334,29 @@ k_w4a8g_gemv_m16(const __grid_constant__ CUtensorMap tmW, const GemvArgs a) {
 
 // Kernel instances that the plan may place two to an SM (M <= 8 for W4A16,
 // M <= 4 for W4A8) are compiled for two resident CTAs of 288 threads.
-template <int NT, int CPG, bool ASYM, bool SPLIT, bool SWIGLU, bool GROUPED, bool SB, bool F32>
+template <int NT, int CPG, bool ASYM, bool SPLIT, bool SWIGLU, bool GROUPED, bool SB, bool F32,
+          bool Q8>
 __device__ __forceinline__ void w4a16_body(const CUtensorMap* tm, const GemvArgs& a) {
     const Smem sm = gemv_init<GROUPED>(tm, a);
     if (threadIdx.x >= NCT) {
         if (threadIdx.x == NCT) gemv_producer<GROUPED>(tm, sm.wbuf, sm.xbuf, sm.ctl, a);
     } else {
-        w4a16_consumer<NT, CPG, ASYM, SPLIT, SWIGLU, GROUPED, SB, F32>(sm, a);
+        w4a16_consumer<NT, CPG, ASYM, SPLIT, SWIGLU, GROUPED, SB, F32, Q8>(sm, a);
     }
 }
 
 template <int CPG, bool ASYM, bool SPLIT, bool SWIGLU, bool GROUPED = false, bool SB = false,
-          bool F32 = false>
+          bool F32 = false, bool Q8 = false>
 __global__ void __launch_bounds__(kGemvThreads, 2)
 k_w4a16_gemv_m8(const __grid_constant__ CUtensorMap tmW, const GemvArgs a) {
-    w4a16_body<1, CPG, ASYM, SPLIT, SWIGLU, GROUPED, SB, F32>(&tmW, a);
+    w4a16_body<1, CPG, ASYM, SPLIT, SWIGLU, GROUPED, SB, F32, Q8>(&tmW, a);
 }
 
 template <int CPG, bool ASYM, bool SPLIT, bool SWIGLU, bool GROUPED = false, bool SB = false,
-          bool F32 = false>
+          bool F32 = false, bool Q8 = false>
 __global__ void __launch_bounds__(kGemvThreads, 1)
 k_w4a16_gemv_m16(const __grid_constant__ CUtensorMap tmW, const GemvArgs a) {
-    w4a16_body<2, CPG, ASYM, SPLIT, SWIGLU, GROUPED, SB, F32>(&tmW, a);
+    w4a16_body<2, CPG, ASYM, SPLIT, SWIGLU, GROUPED, SB, F32, Q8>(&tmW, a);
 }
 
 template <int MT>
@@ -1362,22 +1426,22 @@ int launch(Kern kern, const uint8_t* packed, const GemvArgs& a, const GemvPlan& 
 }
 
 template <int NT, bool ASYM, bool SPLIT, bool SWIGLU = false, bool GROUPED = false,
-          bool SB = false, bool F32 = false>
+          bool SB = false, bool F32 = false, bool Q8 = false>
 int launch_w4a16_cpg(int cpg, const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
                      cudaStream_t st) {
     if (NT == 1) {
         switch (cpg) {
-            case 8: return launch(k_w4a16_gemv_m8<8, ASYM, SPLIT, SWIGLU, GROUPED, SB, F32>, packed, a, p, st);
-            case 4: return launch(k_w4a16_gemv_m8<4, ASYM, SPLIT, SWIGLU, GROUPED, SB, F32>, packed, a, p, st);
-            case 2: return launch(k_w4a16_gemv_m8<2, ASYM, SPLIT, SWIGLU, GROUPED, SB, F32>, packed, a, p, st);
-            default: return launch(k_w4a16_gemv_m8<1, ASYM, SPLIT, SWIGLU, GROUPED, SB, F32>, packed, a, p, st);
+            case 8: return launch(k_w4a16_gemv_m8<8, ASYM, SPLIT, SWIGLU, GROUPED, SB, F32, Q8>, packed, a, p, st);
+            case 4: return launch(k_w4a16_gemv_m8<4, ASYM, SPLIT, SWIGLU, GROUPED, SB, F32, Q8>, packed, a, p, st);
+            case 2: return launch(k_w4a16_gemv_m8<2, ASYM, SPLIT, SWIGLU, GROUPED, SB, F32, Q8>, packed, a, p, st);
+            default: return launch(k_w4a16_gemv_m8<1, ASYM, SPLIT, SWIGLU, GROUPED, SB, F32, Q8>, packed, a, p, st);
         }
     }
     switch (cpg) {
-        case 8: return launch(k_w4a16_gemv_m16<8, ASYM, SPLIT, SWIGLU, GROUPED, SB, F32>, packed, a, p, st);
-        case 4: return launch(k_w4a16_gemv_m16<4, ASYM, SPLIT, SWIGLU, GROUPED, SB, F32>, packed, a, p, st);
-        case 2: return launch(k_w4a16_gemv_m16<2, ASYM, SPLIT, SWIGLU, GROUPED, SB, F32>, packed, a, p, st);
-        default: return launch(k_w4a16_gemv_m16<1, ASYM, SPLIT, SWIGLU, GROUPED, SB, F32>, packed, a, p, st);
+        case 8: return launch(k_w4a16_gemv_m16<8, ASYM, SPLIT, SWIGLU, GROUPED, SB, F32, Q8>, packed, a, p, st);
+        case 4: return launch(k_w4a16_gemv_m16<4, ASYM, SPLIT, SWIGLU, GROUPED, SB, F32, Q8>, packed, a, p, st);
+        case 2: return launch(k_w4a16_gemv_m16<2, ASYM, SPLIT, SWIGLU, GROUPED, SB, F32, Q8>, packed, a, p, st);
+        default: return launch(k_w4a16_gemv_m16<1, ASYM, SPLIT, SWIGLU, GROUPED, SB, F32, Q8>, packed, a, p, st);
     }
 }
 
@@ -1386,17 +1450,17 @@ int launch_w4a16_cpg(int cpg, const uint8_t* packed, const GemvArgs& a, const Ge
 // SB: bf16 parameters; asymmetric when a.offs_b is set.  F32: fp32 outputs
 // a.y32 without bias.
 template <bool SPLIT, bool SWIGLU = false, bool GROUPED = false, bool SB = false,
-          bool F32 = false>
+          bool F32 = false, bool Q8 = false>
 int launch_w4a16_variant(const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
                          cudaStream_t st) {
     const int gq = a.G / 32;
     const int cpg = (gq % 8 == 0) ? 8 : (gq % 4 == 0) ? 4 : (gq % 2 == 0) ? 2 : 1;
     const bool asym = SB ? a.offs_b != nullptr : a.zeros != nullptr;
     if ((GROUPED ? a.gmax : a.M) <= 8)
-        return asym ? launch_w4a16_cpg<1, true, SPLIT, SWIGLU, GROUPED, SB, F32>(cpg, packed, a, p, st)
-                    : launch_w4a16_cpg<1, false, SPLIT, SWIGLU, GROUPED, SB, F32>(cpg, packed, a, p, st);
-    return asym ? launch_w4a16_cpg<2, true, SPLIT, SWIGLU, GROUPED, SB, F32>(cpg, packed, a, p, st)
-                : launch_w4a16_cpg<2, false, SPLIT, SWIGLU, GROUPED, SB, F32>(cpg, packed, a, p, st);
+        return asym ? launch_w4a16_cpg<1, true, SPLIT, SWIGLU, GROUPED, SB, F32, Q8>(cpg, packed, a, p, st)
+                    : launch_w4a16_cpg<1, false, SPLIT, SWIGLU, GROUPED, SB, F32, Q8>(cpg, packed, a, p, st);
+    return asym ? launch_w4a16_cpg<2, true, SPLIT, SWIGLU, GROUPED, SB, F32, Q8>(cpg, packed, a, p, st)
+                : launch_w4a16_cpg<2, false, SPLIT, SWIGLU, GROUPED, SB, F32, Q8>(cpg, packed, a, p, st);
 }
 
 }  // namespace

@@ -98,19 +98,6 @@ k_pack_rtn(const float* __restrict__ W, int N, int K, int G, int Ng, int symmetr
     }
 }
 
-// q = clip(rint(fp32(v / s)), -127, 127) as a byte (s > 0), bit-identical to
-// the IEEE quotient without dividing in the common case.  |v| <= 127.x s, and
-// t = v * rcp(s) (product and reciprocal each correctly rounded) differs from
-// v / s by at most three roundings, under 2^-22 |v/s| <= 2^-15, as does
-// fp32(v / s); so both round to the same integer unless t lies within 2^-14
-// of a half-integer.  Only then (or when t is not finite, for a subnormal s)
-// is the quotient computed.
-__device__ __forceinline__ uint32_t quant_s8(float v, float s, float rs) {
-    float t = v * rs;
-    if (!(fabsf(fabsf(t - truncf(t)) - 0.5f) > 0x1p-14f)) t = __fdiv_rn(v, s);
-    return (uint32_t)(uint8_t)(int8_t)(int)fminf(fmaxf(rintf(t), -127.f), 127.f);
-}
-
 // Eight columns k .. k+7 (four bf16x2 words) as fp32, smoothed when
 // inv_s is given: x' = fp32(x * inv_s[k + j]) (the product rounded once).
 // Columns >= K hold zero words and are not smoothed.
@@ -141,16 +128,6 @@ __device__ __forceinline__ void cols4(const uint2& v, const float* inv_s, int k,
         const float4 a = __ldg(reinterpret_cast<const float4*>(inv_s + k));
         f[0] *= a.x; f[1] *= a.y; f[2] *= a.z; f[3] *= a.w;
     }
-}
-
-// Eight values to eight INT8 bytes; all zero when s = 0.
-__device__ __forceinline__ uint2 quant_s8x8(const float f[8], float s, float rs) {
-    if (s == 0.f) return make_uint2(0u, 0u);
-    uint32_t b[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) b[j] = quant_s8(f[j], s, rs);
-    return make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24),
-                      b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
 }
 
 // Grid (C, M): C CTAs of 512 threads per token.  Every CTA reduces max|x|

@@ -80,6 +80,12 @@ struct GemvArgs {
     const uint16_t* offs_b;
     // fp32 outputs [M, N] without bias (row-parallel partial sums), instead of y
     float* y32;
+    // SwiGLU with INT8 outputs: qx [M, Fp] int8, sx_out [M], and the row-block
+    // completion ticket (the last counter of the workspace prefix)
+    int8_t* qx;
+    float* sx_out;
+    int Fp;
+    int* done;
 };
 
 // The launchers encode the tensor map of `packed` for the plan's box shape
@@ -92,6 +98,9 @@ bool gemv_tma_activations(int M);
 // Decode with the SwiGLU epilogue: a.N = 2F paired gate/up rows, y [M, F].
 int launch_w4a16_swiglu(const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
                         cudaStream_t stream);
+// The same with the INT8 epilogue (a.qx, a.sx_out, a.Fp, a.done).
+int launch_w4a16_swiglu_q8(const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
+                           cudaStream_t stream);
 int launch_w4a16_gemv_split(const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
                             cudaStream_t stream);
 // Decode with the bf16 parameter layout (a.scales_b, a.offs_b).

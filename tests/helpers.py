@@ -103,6 +103,15 @@ class GuardedW4:
                          [("y", (x.shape[0], F), torch.bfloat16)],
                          x, packed, scales, zeros, bias, F, K, group_size, **kw)
 
+    def w4a16_linear_swiglu_q8(self, x, packed, scales, zeros, bias, F, K, group_size,
+                               q_group_size, **kw):
+        Fp = self._mod.padded_k(F, q_group_size) if q_group_size > 0 else None
+        return self._run(self._mod.w4a16_linear_swiglu_q8, "w4a16_linear_swiglu_q8",
+                         [("y", (x.shape[0], F), torch.bfloat16),
+                          ("qx", None if Fp is None else (x.shape[0], Fp), torch.int8),
+                          ("sx", (x.shape[0],), torch.float32)],
+                         x, packed, scales, zeros, bias, F, K, group_size, q_group_size, **kw)
+
     def w4a16_grouped_linear(self, x, goff, packed, scales, zeros, bias, E, N, K, group_size,
                              tile_tokens, **kw):
         return self._run(self._mod.w4a16_grouped_linear, "w4a16_grouped_linear",
