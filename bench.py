@@ -658,17 +658,36 @@ def measure_swiglu(w4, hbm, reps=200):
             d = ds.copies[i % ds.R][0]
             w4.w4a16_linear_swiglu(d["x"], d["p"], d["s"], d["z"], d["b"], F, lin.K,
                                    lin.group_size, y=yF)
+        # the same with the INT8 activations of the W4A8 down projection
+        # (one scale per row, Fp = F): fused, and as two launches
+        qx = torch.empty(M, F, dtype=torch.int8, device="cuda")
+        sx = torch.empty(M, dtype=torch.float32, device="cuda")
+
+        def fused_q8(i):
+            d = ds.copies[i % ds.R][0]
+            w4.w4a16_linear_swiglu_q8(d["x"], d["p"], d["s"], d["z"], d["b"], F, lin.K,
+                                      lin.group_size, F, y=yF, qx=qx, sx=sx)
+
+        def two_launch_q8(i):
+            fused(i)
+            w4.w4a8_quantize_act(yF, F, qx=qx, sx=sx)
         for i in range(3):
             fused(i)
             ds.call(0, i)
+            fused_q8(i)
+            two_launch_q8(i)
         torch.cuda.synchronize()
         n = reps * ds.R
         t_lin = time_graph_steps(lambda i: ds.call(0, i), n, ds.R, 1) / n
         t_fus = time_graph_steps(fused, n, ds.R, 1) / n
+        t_q8 = time_graph_steps(fused_q8, n, ds.R, 1) / n
+        t_2l = time_graph_steps(two_launch_q8, n, ds.R, 1) / n
         b = algorithmic_bytes(lin, M) - 2 * M * lin.N + 2 * M * F
         out.append({"M": M, "F": F, "K": lin.K, "fused_us": round(t_fus * 1e6, 3),
                     "gate_up_linear_us": round(t_lin * 1e6, 3),
-                    "GB/s": round(b / t_fus / 1e9, 1), "frac": round(b / t_fus / 1e9 / hbm, 4)})
+                    "GB/s": round(b / t_fus / 1e9, 1), "frac": round(b / t_fus / 1e9 / hbm, 4),
+                    "fused_int8_us": round(t_q8 * 1e6, 3),
+                    "swiglu_then_quantize_us": round(t_2l * 1e6, 3)})
         del ds
         torch.cuda.empty_cache()
     return out
@@ -752,6 +771,70 @@ def measure_moe(w4, hbm, reps=100):
         del copies
         torch.cuda.empty_cache()
     return out
+
+
+def measure_moe_prefill(w4, hbm, batch=512, reps=20):
+    """Expert layer at prefill (batch 512, 8 of 128 experts per token: 4096
+    routed rows, 32 per expert on average): the grouped call per projection
+    with 64-token tiles on the tensor-core kernel, TFLOP/s over 2 T N K and
+    GB/s over the active experts' bytes; for context the same call with
+    16-token tiles (the decode kernel, which re-reads each expert's weights
+    once per tile)."""
+    E = WL.MOE_EXPERTS
+    counts = WL.moe_route_counts(batch, seed=batch)
+    T = sum(counts)
+    act = sum(1 for c in counts if c)
+    goff = torch.zeros(E + 1, dtype=torch.int32, device="cuda")
+    goff[1:] = torch.cumsum(torch.tensor(counts, dtype=torch.int32, device="cuda"), 0,
+                            dtype=torch.int32)
+    lins = WL.moe_decode(batch)
+    per_copy = sum(E * l.N * l.K * 0.6 for l in lins)
+    R = max(2, math.ceil(3 * L2_BYTES / per_copy))
+    copies = []
+    for r in range(R):
+        cp = []
+        for lin in lins:
+            Kp = -(-lin.K // lin.group_size) * lin.group_size
+            g = torch.Generator(device="cuda")
+            g.manual_seed(lin.seed + 50 + r)
+            p = torch.randint(0, 256, (E * lin.N, Kp // 2), generator=g, device="cuda",
+                              dtype=torch.int32).to(torch.uint8)
+            s = torch.rand(E * lin.N, Kp // lin.group_size, generator=g,
+                           device="cuda") * 0.01 + 1e-4
+            x = WL.make_activations(lin.K, T, seed=40_000 + 7 * r + lin.seed)
+            cp.append(dict(p=p, s=s, x=x.cuda(),
+                           y=torch.empty(T, lin.N, dtype=torch.bfloat16, device="cuda")))
+        copies.append(cp)
+    torch.cuda.synchronize()
+    res = {"batch": batch, "tokens_routed": T, "active_experts": act,
+           "max_per_expert": max(counts)}
+    for tile in (64, 16):
+        def call(li, i, tile=tile):
+            lin, d = lins[li], copies[i % R][li]
+            w4.w4a16_grouped_linear(d["x"], goff, d["p"], d["s"], None, None, E, lin.N, lin.K,
+                                    lin.group_size, tile, y=d["y"])
+        for i in range(3):
+            call(0, i)
+            call(1, i)
+        torch.cuda.synchronize()
+        tot_f = tot_t = 0.0
+        for li, lin in enumerate(lins):
+            n = reps * R
+            sec = time_graph_steps(lambda i, li=li: call(li, i), n, R, 1) / n
+            f = 2.0 * T * lin.N * lin.K
+            Kp = -(-lin.K // lin.group_size) * lin.group_size
+            b = act * (lin.N * Kp // 2 + 4 * lin.N * (Kp // lin.group_size)) \
+                + 2 * T * lin.K + 2 * T * lin.N
+            tot_f += f
+            tot_t += sec
+            key = f"{lin.name.split('_b')[0]}_tile{tile}"
+            res[key + "_us"] = round(sec * 1e6, 2)
+            res[key + "_TFLOP/s"] = round(f / sec / 1e12, 1)
+            res[key + "_GB/s"] = round(b / sec / 1e9, 1)
+        res[f"tile{tile}_TFLOP/s"] = round(tot_f / tot_t / 1e12, 1)
+    del copies
+    torch.cuda.empty_cache()
+    return res
 
 
 def measure_bf16p(w4, hbm, reps=200):
@@ -872,6 +955,7 @@ def run_ours(args, world, rank):
                 ("mid_m", lambda: measure_mid_m(w4, hbm, bf16)),
                 ("swiglu_7b", lambda: measure_swiglu(w4, hbm)),
                 ("moe_decode", lambda: measure_moe(w4, hbm)),
+                ("moe_prefill", lambda: measure_moe_prefill(w4, hbm)),
                 ("gptq", lambda: measure_gptq(w4)),
                 ("decode7b_bf16_params", lambda: measure_bf16p(w4, hbm))]:
             try:

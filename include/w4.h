@@ -262,9 +262,10 @@ W4_API int w4a16_linear_swiglu(const uint16_t* x, const uint8_t* packed, const f
  *  sx       [M] fp32 out;
  *  q_group_size  the group size of the W4A8 layer that reads qx (a positive
  *           multiple of 32; its padded K is Fp).
- * qx and sx equal w4a8_quantize_act(y, q_group_size) bit for bit.  The last
- * row block to finish reads y back and quantizes it, so the workspace is
- * required even when the plan does not split K: at least
+ * qx and sx equal w4a8_quantize_act(y, q_group_size) bit for bit.  Each
+ * CTA folds the max |y| per token of the outputs it wrote into the
+ * workspace; the last CTA to finish reads y back and quantizes it, so the
+ * workspace is required even when the plan does not split K: at least
  * max(w4a16_workspace_bytes(M, 2F, K, group_size), W4_WORKSPACE_COUNTER_BYTES)
  * bytes, zero-filled once (its counters are left at zero).  M <= 16.
  * ------------------------------------------------------------------------- */
@@ -297,16 +298,21 @@ W4_API int w4a16_linear_swiglu_q8(const uint16_t* x, const uint8_t* packed,
  *  scales    [E, N, Ng] fp32;  zeros [E, N, Ng] uint8 or NULL (symmetric);
  *  bias      [E, N] fp32 or NULL.
  *  y         [T, N] bf16 out.
- *  tile_tokens  tokens per pass, 1..16 (the token tile of the kernel: 8 or
- *            16 wide).  A group with more tokens is taken in
+ *  tile_tokens  tokens per pass.  1..16: the decode kernel (token tiles 8
+ *            or 16 wide); a group with more tokens is taken in
  *            ceil(count / tile_tokens) passes, each reading its weights; the
  *            best tile is the largest count of a group when that is <= 16.
+ *            17..256: the tensor-core (tcgen05) kernel for groups of many
+ *            tokens (prefill), in tiles of 64 tokens (tile_tokens <= 64) or
+ *            256, each tile dequantizing its group's weights on chip once;
+ *            requires K % 8 == 0 and supports up to a few hundred groups
+ *            (W4_ERR_UNSUPPORTED_SHAPE beyond).
  *  A group whose offsets lie outside [0, T] or decrease is skipped (its rows
  *  of y are left as they were) and sets W4_ERR_GROUP_TOKENS in the device
  *  flag that w4_get_device_error returns.  Groups without tokens cost
  *  nothing: the units of work are ((group, token tile), row block), listed
- *  on the device.  E <= 32767, E * N < 2^31, T / tile_tokens < 65536.
- *  No workspace (grouped plans do not split K).
+ *  on the device.  E <= 32767, E * N < 2^31, T / tile_tokens < 65536 (decode
+ *  tiles).  No workspace (grouped plans do not split K).
  * ------------------------------------------------------------------------- */
 W4_API int w4a16_grouped_linear(const uint16_t* x, const int32_t* goff, const uint8_t* packed,
                                 const float* scales, const uint8_t* zeros, const float* bias,

@@ -404,7 +404,8 @@ def w4a16_grouped_linear(x: torch.Tensor, goff: torch.Tensor, packed: torch.Tens
     by group) times group e's matrix -> the same rows of y [T, N].  packed /
     scales / zeros / bias hold the E groups stacked ([E*N, ...] or [E, N, ...]);
     goff is an int32 CUDA tensor [E+1]; groups are taken in passes of at
-    most tile_tokens (1..16) tokens."""
+    most tile_tokens tokens: 1..16 on the decode kernel, 17..256 on the
+    tensor-core kernel (tiles of 64 or 256 tokens, K % 8 == 0)."""
     T = x.shape[0]
     _need(x, torch.bfloat16, (T, K), "x")
     Kp = padded_k(K, group_size)

@@ -409,7 +409,9 @@ int w4a16_linear_swiglu_q8(const uint16_t* x, const uint8_t* packed, const float
     GemvArgs a{};
     rc = split_workspace(p, workspace, workspace_bytes, &a.tickets, &a.partial);
     if (rc) return rc;
+    // the last 17 counters of the prefix: 16 per-token maxima, the ticket
     a.done = static_cast<int*>(workspace) + (kMaxCounters - 1);
+    a.ymax = reinterpret_cast<unsigned*>(static_cast<int*>(workspace) + (kMaxCounters - 17));
     a.qx = qx; a.sx_out = sx; a.Fp = (int)Fp;
     a.x = x; a.scales = scales; a.zeros = zeros; a.bias = bias; a.y = y;
     a.xtma = (K % 8) == 0 && gemv_tma_activations(M);
@@ -428,9 +430,9 @@ int w4a16_grouped_linear(const uint16_t* x, const int32_t* goff, const uint8_t* 
     if (!x || !goff || !packed || !scales || !y) return W4_ERR_NULL_PTR;
     if (symmetric && zeros) return W4_ERR_INVALID_ARG;
     if (!symmetric && !zeros) return W4_ERR_NULL_PTR;
-    if (T < 0 || E <= 0 || E > 32767 || N <= 0 || tile_tokens < 1 || tile_tokens > 16)
+    if (T < 0 || E <= 0 || E > 32767 || N <= 0 || tile_tokens < 1 || tile_tokens > 256)
         return W4_ERR_INVALID_ARG;
-    if (T / tile_tokens >= 65536) return W4_ERR_UNSUPPORTED_SHAPE;   // tile index: 16 bits
+    if (tile_tokens <= 16 && T / tile_tokens >= 65536) return W4_ERR_UNSUPPORTED_SHAPE;   // 16-bit tile index
     if ((long long)E * N > 0x7fffffffLL) return W4_ERR_UNSUPPORTED_SHAPE;
     int rc = check_group(K, group_size);
     if (rc) return rc;
@@ -441,6 +443,16 @@ int w4a16_grouped_linear(const uint16_t* x, const int32_t* goff, const uint8_t* 
         (reinterpret_cast<uintptr_t>(y) & 1))
         return W4_ERR_MISALIGNED;
     if (T == 0) return W4_OK;
+    if (tile_tokens > 16) {
+        // groups of many tokens: tensor-core tiles of 64 or 256 tokens, each
+        // group's weights dequantized once per tile
+        if (K % 8 != 0) return W4_ERR_UNSUPPORTED_SHAPE;
+        int* err = device_error_flag();
+        if (!err) return W4_ERR_CUDA;
+        return launch_w4a16_grouped_gemm(x, goff, packed, scales, zeros, bias, y, T, E, N, K,
+                                         (int)Kp, group_size, tile_tokens, err,
+                                         static_cast<cudaStream_t>(stream));
+    }
     // at most E + T / tile items (each has a token); plan for their rows
     const long long items = std::min<long long>(T, (long long)E + (T + tile_tokens - 1) / tile_tokens);
     const long long n_eff = std::min(items * N, 0x7fffffffLL);

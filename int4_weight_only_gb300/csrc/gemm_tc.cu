@@ -77,6 +77,11 @@ struct GemmArgs {
     int ntiles;
     int S, spl;     // K splits, stages per split
     int units;      // ntiles * S
+    // grouped launches (experts): x [T = M, K] rows sorted by group, goff[E+1]
+    // token offsets on the device, weights / scales / bias stacked [E * Ne, ...],
+    // y [T, Ne]; NBg row blocks per group
+    const int* goff;
+    int E, Ne, NBg;
 };
 
 template <int NST, int NSA, int NSP>
@@ -107,21 +112,61 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-__device__ __forceinline__ void unit_of(const GemmArgs& a, int u, int& nb, int& tb, int& tile,
-                                        int& s, int& ks0, int& ks1) {
-    tile = u / a.S;
-    s = u - tile * a.S;
-    nb = tile / a.TB;
-    tb = tile - nb * a.TB;
-    ks0 = s * a.spl;
-    ks1 = min(ks0 + a.spl, a.nks);
+// One unit of work: output tile `tile` (split s, stages [ks0, ks1)), the
+// weight rows gbase + nloc0 .. (of which the first nlim are the layer's),
+// the token rows [t0, tend).
+struct Unit {
+    int tile, s, ks0, ks1;
+    int gbase;     // first weight row of the unit's matrix (group e: e * Ne)
+    int nloc0;     // first row of the tile inside that matrix (= y column)
+    int nlim;      // rows of the matrix (N, or Ne when grouped) = y row stride
+    int t0, tend;  // token rows of x and y
+};
+
+// GRP: a grouped launch; gpre[e] is the number of token tiles of the groups
+// before e (gpre[E] = all tiles), units are (tile item, row block).
+template <bool GRP, int BN, int RB>
+__device__ __forceinline__ Unit unit_of(const GemmArgs& a, int u, const int* gpre) {
+    Unit w;
+    if constexpr (GRP) {
+        const int item = u / a.NBg, nb = u - item * a.NBg;
+        int lo = 0, hi = a.E - 1;                    // the group whose tiles hold item
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (gpre[mid] <= item) lo = mid; else hi = mid - 1;
+        }
+        const int o0 = __ldg(a.goff + lo), o1 = __ldg(a.goff + lo + 1);
+        w.tile = u; w.s = 0; w.ks0 = 0; w.ks1 = a.nks;
+        w.gbase = lo * a.Ne; w.nloc0 = nb * RB; w.nlim = a.Ne;
+        w.t0 = o0 + (item - gpre[lo]) * BN;
+        w.tend = min(o1, w.t0 + BN);
+    } else {
+        w.tile = u / a.S;
+        w.s = u - w.tile * a.S;
+        const int nb = w.tile / a.TB, tb = w.tile - nb * a.TB;
+        w.ks0 = w.s * a.spl;
+        w.ks1 = min(w.ks0 + a.spl, a.nks);
+        w.gbase = 0; w.nloc0 = nb * RB; w.nlim = a.N;
+        w.t0 = tb * BN; w.tend = a.M;
+    }
+    return w;
 }
 
 // SB: bf16 parameters; the dequantized weight is s (code - 8) + o.
-template <int BN, int NST, int NSA, int NSP, int DQG, bool PAIR, int KB, bool SB = false>
+// GRP: a grouped linear over E groups (experts), the grouped matmul of "Yeniden
+// paketlenmiş QAT Gemma 4 26B-A4B, tek bir TPU v6e'de FP8 işlemenin 1.9 katı
+// verimle sunuluyor", section "vLLM'in TPU backend'inde değişen ne oldu", for
+// groups of many tokens: group e's tokens, rows goff[e] .. goff[e+1] - 1 of x,
+// times its own Ne x K matrix, in tiles of BN tokens.  Before the role split
+// warp 2 validates the offsets and writes the tiles' prefix sum to shared
+// memory; every role then maps a unit to (group, token tile, row block).  A
+// tile's rows past its group are computed but not stored.  No K split.
+template <int BN, int NST, int NSA, int NSP, int DQG, bool PAIR, int KB, bool SB = false,
+          bool GRP = false>
 __global__ void __launch_bounds__(threads_of<DQG>(), 1)
 k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmP,
                 const GemmArgs a) {
+    static_assert(!(GRP && PAIR), "grouped tiles run on single CTAs");
     constexpr int THREADS = threads_of<DQG>();
     constexpr int XR = PAIR ? BN / 2 : BN;                  // x rows staged by this CTA
     constexpr int RB = PAIR ? 2 * BM : BM;                  // weight rows per tile
@@ -139,6 +184,9 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     uint8_t* as = xs + NST * X_BYTES;                       // NSA x A_ST
     uint8_t* ps = as + NSA * A_ST;                          // NSP x P_ST
     auto* ctl = reinterpret_cast<Ctl<NST, NSA, NSP>*>(ps + NSP * P_ST);
+    // grouped: tiles before each group, E + 1 ints after the control block
+    int* gpre = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(ctl) +
+                                       (sizeof(Ctl<NST, NSA, NSP>) + 15) / 16 * 16);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // a pair tile is worked on by the two CTAs of a cluster: rank 0 issues
     // the MMAs, each CTA stages its half of x and dequantizes its 128 rows
@@ -168,6 +216,35 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) { tma_prefetch_desc(&tmX); tma_prefetch_desc(&tmP); }
+    if constexpr (GRP) {
+        if (warp == 2) {
+            // group e has ceil(count / BN) token tiles; offsets outside [0, T]
+            // or decreasing leave the group out and raise W4_ERR_GROUP_TOKENS
+            int run = 0;
+            if (lane == 0) gpre[0] = 0;
+            for (int e0 = 0; e0 < a.E; e0 += 32) {
+                const int e = e0 + lane;
+                int n = 0;
+                if (e < a.E) {
+                    const int o0 = __ldg(a.goff + e), o1 = __ldg(a.goff + e + 1);
+                    const bool ok = o0 >= 0 && o1 >= o0 && o1 <= a.M;
+                    if (!ok) atomicCAS(a.err, 0, W4_ERR_GROUP_TOKENS);
+                    n = ok ? (o1 - o0 + BN - 1) / BN : 0;
+                }
+                int v = n;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int t = __shfl_up_sync(0xffffffffu, v, o);
+                    if (lane >= o) v += t;
+                }
+                if (e < a.E) gpre[e + 1] = run + v;
+                run += __shfl_sync(0xffffffffu, v, 31);
+            }
+            // offsets valid one by one can still overlap and list more tiles
+            // than T tokens need; every access stays in bounds, but flag it
+            if (lane == 0 && run > a.E + (a.M + BN - 1) / BN) atomicCAS(a.err, 0, W4_ERR_GROUP_TOKENS);
+        }
+    }
     if constexpr (PAIR) {
         if (warp == 1) { tmem_alloc_pair(&ctl->tmem_base, TMEM_COLS); tmem_relinquish_pair(); }
         tc_fence_before();
@@ -179,6 +256,7 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     }
     tc_fence_after();
     const uint32_t tmem_base = ctl->tmem_base;
+    const int units = GRP ? gpre[a.E] * a.NBg : a.units;
 
     if (warp == 0 || warp == 2) {
         // ------------------------------------------------------------ TMA
@@ -193,9 +271,9 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
             const uint64_t pol = is_x ? policy_evict_last() : policy_evict_first();
             uint32_t it = 0;
             bool ok = true;
-            for (int u = slot; u < a.units && ok; u += nslots) {
-                int nb, tb, tile, s, ks0, ks1;
-                unit_of(a, u, nb, tb, tile, s, ks0, ks1);
+            for (int u = slot; u < units && ok; u += nslots) {
+                const Unit w = unit_of<GRP, BN, RB>(a, u, gpre);
+                const int ks0 = w.ks0, ks1 = w.ks1;
                 for (int ks = ks0; ks < ks1; ++ks, ++it) {
                     const int st = it % ring;
                     if (it >= (uint32_t)ring &&
@@ -209,17 +287,17 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                             if (rank == 0) mbar_arrive_expect_tx(&full[st], 2 * X_BYTES);
                             for (int kb = 0; kb < KB; ++kb)
                                 tma_load_2d_pair(xs + st * X_BYTES + kb * XR * 128, &tmX, ks * SK + kb * BK,
-                                                 tb * BN + (int)rank * XR, at_rank0(&full[st]), pol);
+                                                 w.t0 + (int)rank * XR, at_rank0(&full[st]), pol);
                         } else {
                             mbar_arrive_expect_tx(&full[st], X_BYTES);
                             for (int kb = 0; kb < KB; ++kb)
                                 tma_load_2d(xs + st * X_BYTES + kb * XR * 128, &tmX, ks * SK + kb * BK,
-                                            tb * BN, &full[st], pol);
+                                            w.t0, &full[st], pol);
                         }
                     } else {
                         mbar_arrive_expect_tx(&full[st], P_ST);
-                        tma_load_2d(ps + st * P_ST, &tmP, ks * (SK / 2), nb * RB + (int)rank * BM,
-                                    &full[st], pol);
+                        tma_load_2d(ps + st * P_ST, &tmP, ks * (SK / 2),
+                                    w.gbase + w.nloc0 + (int)rank * BM, &full[st], pol);
                     }
                 }
             }
@@ -241,9 +319,9 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
             };
             uint32_t it = 0, ia = 0, tc = 0;
             bool ok = true;
-            for (int u = slot; u < a.units && ok; u += nslots, ++tc) {
-                int nb, tb, tile, s, ks0, ks1;
-                unit_of(a, u, nb, tb, tile, s, ks0, ks1);
+            for (int u = slot; u < units && ok; u += nslots, ++tc) {
+                const Unit w = unit_of<GRP, BN, RB>(a, u, gpre);
+                const int ks0 = w.ks0, ks1 = w.ks1;
                 const uint32_t b = tc & 1;
                 if (tc >= 2 && !wait(&ctl->accempty[b], ((tc / 2) & 1) ^ 1)) {
                     ok = false;
@@ -301,13 +379,13 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
         const int grp = dt / DQ_GROUP_THREADS, gt = dt % DQ_GROUP_THREADS;
         const int r = gt / DQ_TPR, h = gt % DQ_TPR;
         uint32_t it = 0;
-        for (int u = slot; u < a.units; u += nslots) {
-            int nb, tb, tile, s, ks0, ks1;
-            unit_of(a, u, nb, tb, tile, s, ks0, ks1);
+        for (int u = slot; u < units; u += nslots) {
+            const Unit w = unit_of<GRP, BN, RB>(a, u, gpre);
+            const int ks0 = w.ks0, ks1 = w.ks1;
             // first stage of this unit that falls to this group
             const int lead = (int)((grp - it % DQ_GROUPS + DQ_GROUPS) % DQ_GROUPS);
             it += (uint32_t)lead;
-            const int n = min(nb * RB + (int)rank * BM + r, a.N - 1);
+            const int n = w.gbase + min(w.nloc0 + (int)rank * BM + r, w.nlim - 1);
             const float* srow = a.scales + (size_t)n * a.Ng;
             const uint8_t* zrow = a.zeros ? a.zeros + (size_t)n * a.Ng : nullptr;
             const uint16_t* sbrow = SB ? a.scales_b + (size_t)n * a.Ng : nullptr;
@@ -398,32 +476,33 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
         const int r = q * 32 + lane;
         const int etid = threadIdx.x - (THREADS - EPI_THREADS);
         uint32_t tc = 0;
-        for (int u = slot; u < a.units; u += nslots, ++tc) {
-            int nb, tb, tile, s, ks0, ks1;
-            unit_of(a, u, nb, tb, tile, s, ks0, ks1);
+        for (int u = slot; u < units; u += nslots, ++tc) {
+            const Unit w = unit_of<GRP, BN, RB>(a, u, gpre);
+            const int tile = w.tile, s = w.s;
             const uint32_t b = tc & 1;
             // the same outcome for all 128 epilogue threads, which then take
             // the same branch (aligned tcgen05.ld, named barriers)
             bool ok = named_bar_and(2, EPI_THREADS,
                                     mbar_wait(&ctl->accfull[b], (tc / 2) & 1, &ctl->abort, a.err));
             tc_fence_after();
-            const int n = nb * RB + (int)rank * BM + r;
+            const int n = w.nloc0 + (int)rank * BM + r;        // output column
+            const int NO = w.nlim, TE = w.tend;                 // y row stride, token limit
             int* ticket = a.tickets + (size_t)tile * NCTA + rank;   // per 128-row half
-            const float bn = (a.bias && n < a.N) ? __ldg(a.bias + n) : 0.f;
+            const float bn = (a.bias && n < NO) ? __ldg(a.bias + w.gbase + n) : 0.f;
             const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + b * BN;
-            const int t0 = tb * BN;
+            const int t0 = w.t0;
             if (ok && a.S == 1) {
-                for (int j = 0; j < BN / 32 && t0 + j * 32 < a.M; ++j) {
+                for (int j = 0; j < BN / 32 && t0 + j * 32 < TE; ++j) {
                     uint32_t v[32];
                     tmem_ld_32x32b_x32(tacc + j * 32, v);
                     tc_wait_ld();
-                    if (n < a.N) {
+                    if (n < NO) {
 #pragma unroll
                         for (int i = 0; i < 32; ++i) {
                             const int t = t0 + j * 32 + i;
-                            if (t < a.M) {
-                                if (a.y32) a.y32[(size_t)t * a.N + n] = __uint_as_float(v[i]);
-                                else a.y[(size_t)t * a.N + n] = f32_to_bf16_bits(__uint_as_float(v[i]) + bn);
+                            if (t < TE) {
+                                if (a.y32) a.y32[(size_t)t * NO + n] = __uint_as_float(v[i]);
+                                else a.y[(size_t)t * NO + n] = f32_to_bf16_bits(__uint_as_float(v[i]) + bn);
                             }
                         }
                     }
@@ -439,7 +518,7 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                 //    later units in the parity tests; see the design notes.)
                 float* ptile = a.partial + (((size_t)tile * a.S) * NCTA + rank) * (BM * BN);
                 const size_t split_stride = (size_t)NCTA * BM * BN;     // floats between splits
-                for (int j = 0; j < BN / 32 && t0 + j * 32 < a.M; ++j) {
+                for (int j = 0; j < BN / 32 && t0 + j * 32 < TE; ++j) {
                     uint32_t v[32];
                     tmem_ld_32x32b_x32(tacc + j * 32, v);
                     float* dst = ptile + s * split_stride + (size_t)j * (BM * 32) + r;
@@ -458,7 +537,7 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                     //    term straight from TMEM), the same order whichever
                     //    split arrives last; the 32 loads of a block are
                     //    independent, so they are in flight together
-                    for (int j = 0; j < BN / 32 && t0 + j * 32 < a.M; ++j) {
+                    for (int j = 0; j < BN / 32 && t0 + j * 32 < TE; ++j) {
                         float acc[32];
 #pragma unroll
                         for (int i = 0; i < 32; ++i) acc[i] = 0.f;
@@ -474,13 +553,13 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
 #pragma unroll
                             for (int i = 0; i < 32; ++i) acc[i] += __uint_as_float(v[i]);
                         }
-                        if (n < a.N) {
+                        if (n < NO) {
 #pragma unroll
                             for (int i = 0; i < 32; ++i) {
                                 const int t = t0 + j * 32 + i;
-                                if (t < a.M) {
-                                    if (a.y32) a.y32[(size_t)t * a.N + n] = acc[i];
-                                    else a.y[(size_t)t * a.N + n] = f32_to_bf16_bits(acc[i] + bn);
+                                if (t < TE) {
+                                    if (a.y32) a.y32[(size_t)t * NO + n] = acc[i];
+                                    else a.y[(size_t)t * NO + n] = f32_to_bf16_bits(acc[i] + bn);
                                 }
                             }
                         }
@@ -508,16 +587,20 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     }
 }
 
-template <int BN, int NST, int NSA, int NSP, int DQG, bool PAIR, int KB, bool SB = false>
+template <int BN, int NST, int NSA, int NSP, int DQG, bool PAIR, int KB, bool SB = false,
+          bool GRP = false>
 struct Variant {
     static constexpr int XR = PAIR ? BN / 2 : BN;
     static constexpr size_t smem = smem_bytes<XR, NST, NSA, NSP, KB>();
-    static_assert(smem <= 232448, "shared memory");
-    static constexpr auto kernel = k_w4a16_gemm_tc<BN, NST, NSA, NSP, DQG, PAIR, KB, SB>;
+    static constexpr size_t kSmemMax = 232448;
+    static_assert(smem <= kSmemMax, "shared memory");
+    static constexpr auto kernel = k_w4a16_gemm_tc<BN, NST, NSA, NSP, DQG, PAIR, KB, SB, GRP>;
+    // grouped: the largest group count whose tile prefix sum fits
+    static constexpr int kMaxGroups = (int)((kSmemMax - smem) / 4) - 1;
 
     static bool prepare() {
         return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)smem) == cudaSuccess;
+                                    (int)(GRP ? kSmemMax : smem)) == cudaSuccess;
     }
 
     static cudaLaunchConfig_t config(int grid, cudaStream_t stream, cudaLaunchAttribute* at) {
@@ -573,8 +656,31 @@ struct Variant {
         if (!prepare()) return W4_ERR_CUDA;
         cudaLaunchAttribute at[1];
         cudaLaunchConfig_t cfg = config(p.grid, stream, at);
+        if (GRP) cfg.dynamicSmemBytes = smem + ((size_t)(a.E + 1) * 4 + 15) / 16 * 16;
         if (cudaLaunchKernelEx(&cfg, kernel, tmX, tmP, a) != cudaSuccess) return W4_ERR_CUDA;
         return W4_OK;
+    }
+
+    // A grouped launch: x [T, K] rows sorted by group, the E groups' Ne x K
+    // matrices stacked (the tensor map covers E * Ne rows), no K split.
+    static int launch_grouped(const uint16_t* x, const int* goff, const uint8_t* packed,
+                              const float* scales, const uint8_t* zeros, const float* bias,
+                              uint16_t* y, int T, int E, int Ne, int K, int Kp, int G, int* err,
+                              int sm_count, cudaStream_t stream) {
+        if (E > kMaxGroups) return W4_ERR_UNSUPPORTED_SHAPE;
+        GemmArgs a{};
+        a.scales = scales; a.zeros = zeros; a.bias = bias; a.y = y; a.err = err;
+        a.goff = goff; a.E = E; a.Ne = Ne; a.NBg = (Ne + BM - 1) / BM;
+        a.M = T; a.N = E * Ne; a.K = K; a.G = G; a.Ng = Kp / G;
+        a.nks = (K + BK * KB - 1) / (BK * KB);
+        a.S = 1; a.spl = a.nks; a.TB = 1;
+        GemmPlan p;
+        const long long ub = ((long long)E + (T + BN - 1) / BN) * a.NBg;   // units at most
+        const int sl = slots(sm_count);
+        if (sl < 1) return W4_ERR_CUDA;
+        p.grid = (int)(ub < sl ? ub : sl);
+        if (p.grid < 1) return W4_OK;
+        return launch(x, packed, p, a, Kp, stream);
     }
 };
 
@@ -588,7 +694,19 @@ using Pair256B = Variant<256, 6, 4, 8, 1, true, 1, true>;
 // same MMA work; group sizes that are multiples of 64 only (a dequantizing
 // thread's 64 columns must lie in one group)
 using Single256K2 = Variant<256, 2, 2, 4, 1, false, 2>;
+// 64-token tiles for small and mid-range M (17 .. ~128 tokens) and expert
+// groups of a few dozen tokens: the MMA is 1/4 of a 256-token stage, so the
+// dequantized A ring is deeper to keep several stages in flight
+using Single64K2 = Variant<64, 4, 3, 6, 1, false, 2>;
+using Single64 = Variant<64, 8, 6, 12, 1, false, 1>;
+using Single64K2B = Variant<64, 4, 3, 6, 1, false, 2, true>;
+using Single64B = Variant<64, 8, 6, 12, 1, false, 1, true>;
 using Pair256K2 = Variant<256, 4, 2, 4, 1, true, 2>;
+// grouped (experts) launches: 64- and 256-token tiles
+using Grp64K2 = Variant<64, 4, 3, 6, 1, false, 2, false, true>;
+using Grp64 = Variant<64, 8, 6, 12, 1, false, 1, false, true>;
+using Grp256K2 = Variant<256, 2, 2, 4, 1, false, 2, false, true>;
+using Grp256 = Variant<256, 4, 4, 8, 1, false, 1, false, true>;
 using Single256K2B = Variant<256, 2, 2, 4, 1, false, 2, true>;
 using Pair256K2B = Variant<256, 4, 2, 4, 1, true, 2, true>;
 
@@ -597,10 +715,12 @@ using Pair256K2B = Variant<256, 4, 2, 4, 1, true, 2, true>;
 // Output tiles are 128 weight rows x BN tokens on one SM, or 256 rows x 256
 // tokens on a CTA pair; K is split S ways when the tiles alone fill the GPU
 // poorly.  Cost = waves x stages per unit x relative stage time, plus a
-// charge per split for the fp32 partials and the hand-off.
+// charge per split for the fp32 partials and the hand-off.  A stage is bound
+// by dequantizing its 128 rows at every tile width, so CTAs that share an SM
+// share its rate: the stage time is multiplied by the CTAs per SM.
 bool plan_gemm(int M, int N, int K, int G, int sm_count, GemmPlan* out) {
     if (M < 1 || N < 1 || K < 1 || sm_count < 1) return false;
-    // W4_GEMM_BN (128 or 256), W4_GEMM_SPLIT (1..8) and W4_GEMM_PAIR (0 or 1)
+    // W4_GEMM_BN (64, 128 or 256), W4_GEMM_SPLIT (1..8) and W4_GEMM_PAIR (0 or 1)
     // pin the plan (tuning sweeps, tests of every variant); read on every
     // call, which costs far less than one launch
     auto env_int = [](const char* name) {
@@ -622,12 +742,16 @@ bool plan_gemm(int M, int N, int K, int G, int sm_count, GemmPlan* out) {
     // (256 x 256 on two SMs) runs 1-3% slower than two single-CTA stages; a
     // 128-token stage takes as long as a 256-token one
     const int forced_kb = env_int("W4_GEMM_KB");
-    const Cand cands[5] = {
+    // 64-token tiles: 0.96 of a 256-token stage (swept at M = 17 .. 2048 on
+    // the 7B gate|up and down shapes)
+    const Cand cands[7] = {
         {true, 256, 2, Pair256K2::slots(sm_count), 1.55},
         {false, 256, 2, Single256K2::slots(sm_count), 1.52},
         {true, 256, 1, Pair256::slots(sm_count), 1.02},
         {false, 256, 1, Single256::slots(sm_count), 1.0},
         {false, 128, 1, Single128::slots(sm_count), 1.0},
+        {false, 64, 2, Single64K2::slots(sm_count), 1.46},
+        {false, 64, 1, Single64::slots(sm_count), 0.96},
     };
     double best = 1e30;
     bool found = false;
@@ -635,9 +759,11 @@ bool plan_gemm(int M, int N, int K, int G, int sm_count, GemmPlan* out) {
         if (c.slots < 1) continue;
         if (forced_pair == 0 && c.pair) continue;
         if (forced_pair == 1 && !c.pair) continue;
-        if ((forced_bn == 128 || forced_bn == 256) && c.BN != forced_bn) continue;
+        if ((forced_bn == 64 || forced_bn == 128 || forced_bn == 256) && c.BN != forced_bn) continue;
         if ((forced_kb == 1 || forced_kb == 2) && c.kb != forced_kb) continue;
         if (c.kb == 2 && G % 64 != 0) continue;
+        const int per_sm = std::max(1, (c.pair ? 2 * c.slots : c.slots) / sm_count);
+        const double stage = c.stage * per_sm;
         const int nks = (K + BK * c.kb - 1) / (BK * c.kb);
         const int RB = c.pair ? 2 * BM : BM;
         const int TB = (M + c.BN - 1) / c.BN;
@@ -650,10 +776,10 @@ bool plan_gemm(int M, int N, int K, int G, int sm_count, GemmPlan* out) {
             if (Se != S) continue;
             const int units = ntiles * S;
             const int waves = (units + c.slots - 1) / c.slots;
-            double cost = (double)waves * spl * c.stage;
+            double cost = (double)waves * spl * stage;
             // split charge: each split writes its fp32 tile and the last one
             // to arrive reads the other S - 1 back
-            if (S > 1) cost += 2.0 * waves * S * c.stage;
+            if (S > 1) cost += 2.0 * waves * S * stage;
             if (cost < best * (1 - 1e-9)) {
                 best = cost;
                 found = true;
@@ -690,6 +816,12 @@ int launch_w4a16_gemm(const uint16_t* x, const uint8_t* packed, const float* sca
         a.tickets = static_cast<int*>(workspace);
         a.partial = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + p.ticket_bytes);
     }
+    if (p.BN == 64) {
+        if (scales_b) return p.kb == 2 ? Single64K2B::launch(x, packed, p, a, Kp, stream)
+                                       : Single64B::launch(x, packed, p, a, Kp, stream);
+        return p.kb == 2 ? Single64K2::launch(x, packed, p, a, Kp, stream)
+                         : Single64::launch(x, packed, p, a, Kp, stream);
+    }
     if (scales_b) {
         if (p.kb == 2) {
             if (p.pair) return Pair256K2B::launch(x, packed, p, a, Kp, stream);
@@ -706,6 +838,23 @@ int launch_w4a16_gemm(const uint16_t* x, const uint8_t* packed, const float* sca
     if (p.pair) return Pair256::launch(x, packed, p, a, Kp, stream);
     if (p.BN == 256) return Single256::launch(x, packed, p, a, Kp, stream);
     return Single128::launch(x, packed, p, a, Kp, stream);
+}
+
+int launch_w4a16_grouped_gemm(const uint16_t* x, const int* goff, const uint8_t* packed,
+                              const float* scales, const uint8_t* zeros, const float* bias,
+                              uint16_t* y, int T, int E, int Ne, int K, int Kp, int G, int tile,
+                              int* err, cudaStream_t stream) {
+    const int sm = current_sm_count();
+    const bool kb2 = G % 64 == 0;
+    if (tile <= 64)
+        return kb2 ? Grp64K2::launch_grouped(x, goff, packed, scales, zeros, bias, y, T, E, Ne, K,
+                                             Kp, G, err, sm, stream)
+                   : Grp64::launch_grouped(x, goff, packed, scales, zeros, bias, y, T, E, Ne, K, Kp,
+                                           G, err, sm, stream);
+    return kb2 ? Grp256K2::launch_grouped(x, goff, packed, scales, zeros, bias, y, T, E, Ne, K, Kp,
+                                          G, err, sm, stream)
+               : Grp256::launch_grouped(x, goff, packed, scales, zeros, bias, y, T, E, Ne, K, Kp, G,
+                                        err, sm, stream);
 }
 
 }  // namespace w4

@@ -70,7 +70,8 @@ struct SmemCtl {
     uint64_t empty[NS];
     int abort;
     int last;
-    int sumq[16];          // W4A8: sum of q_x over the slice, per token
+    int sumq[16];          // W4A8: sum of q_x over the slice, per token; W4A16
+                           // with INT8 outputs: the CTA's max|y| per token (fp32 bits)
     uint64_t xfull;        // activation slice landed (TMA staging)
     uint64_t xempty;       // consumers released the activation buffer
     uint64_t listready;    // grouped: the (group, token tile) list is written
@@ -456,58 +457,79 @@ __device__ __forceinline__ bool split_k_arrive(const GemvArgs& a, SmemCtl* ctl, 
 
 // The INT8 epilogue of the fused SwiGLU call ("Jetson Orin AGX INT4
 // 推理优化实践", section 后续还能继续优化什么, item 2: the activation
-// quantization folded into the op before the integer GEMV).  Called by every
-// consumer thread of a CTA once its row block's y is stored.  A completion
-// ticket counts the row blocks; the CTA that completes the last one reads
-// y [M, F] back (the other CTAs' stores are published by their
-// acquire-release tickets) and applies the per-token rule exactly as
-// w4a8_quantize_act does: s_x = fp32(max|y| / 127), q = clip(rint(fp32(y /
-// s_x)), -127, 127), columns F .. Fp-1 zero.  It then resets the ticket.
-__device__ __forceinline__ void swiglu_q8_finish(const GemvArgs& a, SmemCtl* ctl, float* red, int tid) {
-    named_bar_sync(1, NCT);                  // this CTA's y stores are all issued
-    if (tid == 0) ctl->last = atom_add_acq_rel_gpu(a.done, 1) == a.units / a.S - 1;
+// quantization folded into the op before the integer GEMV).
+// The INT8 epilogue of the fused SwiGLU call ("Jetson Orin AGX INT4
+// 推理优化实践", section 后续还能继续优化什么, item 2: the activation
+// quantization folded into the op before the integer GEMV).
+// q8_cta_max, called by all lanes of an epilogue warp per stored output: the
+// max of |y| (bf16-rounded, as stored) over the lanes that hold the same
+// token, then one shared-memory atomic max per token into ctl->sumq (|y| >= 0
+// orders as an integer).
+__device__ __forceinline__ void q8_cta_max(SmemCtl* ctl, float v, int t, int M, int lane,
+                                           bool valid) {
+    float m = valid ? fabsf(__uint_as_float((uint32_t)f32_to_bf16_bits(v) << 16)) : 0.f;
+    // lanes with the same tig hold the same tokens: combine over gid
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+    if ((lane >> 2) == 0 && t < M && m > 0.f) atomicMax(&ctl->sumq[t], __float_as_int(m));
+}
+
+// Called by every consumer thread once its CTA has no units left.  The CTA
+// adds its maxima with one atomic max per token on a.ymax, then takes a
+// ticket; the CTA that
+// takes the last one has every token's max|y| and every CTA's y stores
+// (the acquire-release tickets publish them) and quantizes y [M, F] in one
+// pass exactly as w4a8_quantize_act does: s_x = fp32(max|y| / 127),
+// q = clip(rint(fp32(y / s_x)), -127, 127), columns F .. Fp-1 zero.  It then
+// clears the maxima and the ticket.
+// IN: 16-byte loads in flight per thread in that pass.
+template <int IN>
+__device__ __forceinline__ void swiglu_q8_finish(const GemvArgs& a, SmemCtl* ctl, float* red,
+                                                 int tid) {
+    named_bar_sync(1, NCT);                  // the CTA's shared maxima are final
+    if (tid < a.M && ctl->sumq[tid] != 0) atomicMax(a.ymax + tid, (unsigned)ctl->sumq[tid]);
+    named_bar_sync(1, NCT);                  // this CTA's y stores and maxima are all issued
+    if (tid == 0) ctl->last = atom_add_acq_rel_gpu(a.done, 1) == (int)gridDim.x - 1;
     named_bar_sync(1, NCT);
     if (!ctl->last) return;
     const int F = a.N >> 1, nw = F >> 3, nwp = a.Fp >> 3;
-    const int warp = tid >> 5, lane = tid & 31;
-    for (int m = 0; m < a.M; ++m) {
-        const uint16_t* row = a.y + (size_t)m * F;
-        float mx = 0.f;
-        for (int w = tid; w < nw; w += NCT) {
-            const uint4 v = ld_cg_v4(row + 8 * w);
-            const uint32_t q[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(q[j] << 16)),
-                                     fabsf(__uint_as_float(q[j] & 0xFFFF0000u))));
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        if (lane == 0) red[warp] = mx;
-        named_bar_sync(1, NCT);
-        float tot = 0.f;
-#pragma unroll
-        for (int w = 0; w < CW; ++w) tot = fmaxf(tot, red[w]);
-        const float sc = __fdiv_rn(tot, 127.0f);
-        const float rs = sc != 0.f ? __frcp_rn(sc) : 0.f;
-        if (tid == 0) a.sx_out[m] = sc;
-        for (int w = tid; w < nwp; w += NCT) {
-            uint2 o = make_uint2(0u, 0u);
-            if (w < nw) {
-                const uint4 v = ld_cg_v4(row + 8 * w);
-                const uint32_t q[4] = {v.x, v.y, v.z, v.w};
-                float f[8];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    f[2 * j] = __uint_as_float(q[j] << 16);
-                    f[2 * j + 1] = __uint_as_float(q[j] & 0xFFFF0000u);
-                }
-                o = quant_s8x8(f, sc, rs);
-            }
-            *reinterpret_cast<uint2*>(a.qx + (size_t)m * a.Fp + 8 * w) = o;
-        }
-        named_bar_sync(1, NCT);              // red is reused by the next token
+    if (tid < a.M) {
+        const float mx = __uint_as_float(ld_cg_s32(reinterpret_cast<const int*>(a.ymax) + tid));
+        const float sc = __fdiv_rn(mx, 127.0f);
+        red[2 * tid] = sc;
+        red[2 * tid + 1] = sc != 0.f ? __frcp_rn(sc) : 0.f;
+        a.sx_out[tid] = sc;
     }
+    named_bar_sync(1, NCT);
+    // all (token, 8-column word) pairs
+    const int total = a.M * nwp;
+    for (int base = tid; base < total; base += IN * NCT) {
+        uint4 v[IN];
+#pragma unroll
+        for (int i = 0; i < IN; ++i) {
+            const int idx = base + i * NCT, m = idx / nwp, w = idx - m * nwp;
+            v[i] = (idx < total && w < nw) ? ld_cg_v4(a.y + (size_t)m * F + 8 * w)
+                                           : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int i = 0; i < IN; ++i) {
+            const int idx = base + i * NCT;
+            if (idx >= total) break;
+            const int m = idx / nwp, w = idx - m * nwp;
+            const uint32_t q[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+            float f[8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                f[2 * j] = __uint_as_float(q[j] << 16);
+                f[2 * j + 1] = __uint_as_float(q[j] & 0xFFFF0000u);
+            }
+            *reinterpret_cast<uint2*>(a.qx + (size_t)m * a.Fp + 8 * w) =
+                w < nw ? quant_s8x8(f, red[2 * m], red[2 * m + 1]) : make_uint2(0u, 0u);
+        }
+    }
+    named_bar_sync(1, NCT);
+    if (tid < a.M) a.ymax[tid] = 0u;
     if (tid == 0) *a.done = 0;
 }
 
@@ -530,8 +552,8 @@ __device__ __forceinline__ void swiglu_q8_finish(const GemvArgs& a, SmemCtl* ctl
 // fix-up of a run is s (u tmp - C0 - 8 C1) + o C1.
 // F32: fp32 outputs a.y32 without the bias (the partial sum of a row-
 // parallel shard, added across shards and finished by w4a16_partial_finish).
-// Q8 (with SWIGLU): the last row block to finish also quantizes the whole
-// output y [M, F] to INT8 (swiglu_q8_finish).
+// Q8 (with SWIGLU): the last CTA to finish also quantizes the whole output
+// y [M, F] to INT8 (swiglu_q8_finish).
 template <int NT, int CPG, bool ASYM, bool SPLIT, bool SWIGLU = false, bool GROUPED = false,
           bool SB = false, bool F32 = false, bool Q8 = false>
 __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
@@ -922,12 +944,11 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
                         const int t = nt * 8 + 2 * tig + j;
-                        if (t < M && row0 + gid < N)
-                            y[(size_t)t * F + f] = f32_to_bf16_bits(
-                                swiglu(acc[nt][j] + b_lo, acc[nt][j + 2] + b_hi));
+                        const float v = swiglu(acc[nt][j] + b_lo, acc[nt][j + 2] + b_hi);
+                        if (t < M && row0 + gid < N) y[(size_t)t * F + f] = f32_to_bf16_bits(v);
+                        if constexpr (Q8) q8_cta_max(ctl, v, t, M, lane, t < M && row0 + gid < N);
                     }
             }
-            if constexpr (Q8) swiglu_q8_finish(a, ctl, sm.red, tid);
         } else if constexpr (!SPLIT) {
             if (kp == 0) {
 #pragma unroll
@@ -964,11 +985,14 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
 #pragma unroll
                             for (int j = 0; j < 2; ++j) {
                                 const int t = nt * 8 + 2 * tig + j;
+                                float v = 0.f;
                                 if (t < M && ng < N) {
                                     const float g = sum_splits(part + (size_t)t * N + ng, (size_t)M * N, Sp);
                                     const float u = sum_splits(part + (size_t)t * N + nu, (size_t)M * N, Sp);
-                                    y[(size_t)t * F + f] = f32_to_bf16_bits(swiglu(g + b_lo, u + b_hi));
+                                    v = swiglu(g + b_lo, u + b_hi);
+                                    y[(size_t)t * F + f] = f32_to_bf16_bits(v);
                                 }
+                                if constexpr (Q8) q8_cta_max(ctl, v, t, M, lane, t < M && ng < N);
                             }
                     } else {
 #pragma unroll
@@ -986,10 +1010,11 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
                     }
                 }
                 if (tid == 0) a.tickets[rb] = 0;
-                if constexpr (Q8) swiglu_q8_finish(a, ctl, sm.red, tid);
             }
         }
     }
+    // (eight loads in flight fit the registers of the one-tile kernels)
+    if constexpr (Q8) swiglu_q8_finish<NT == 1 ? 8 : 4>(a, ctl, sm.red, tid);
 }
 
 template <int MT>

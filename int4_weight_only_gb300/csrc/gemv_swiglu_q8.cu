@@ -1,6 +1,6 @@
 // gemv_swiglu_q8.cu - launches of the fused gate|up + SiLU decode kernels
-// whose last row block also writes the INT8 activations of the W4A8 down
-// projection (Q8 instances; kernels in gemv_impl.cuh).  Their own
+// whose last CTA to finish also writes the INT8 activations of the W4A8
+// down projection (Q8 instances; kernels in gemv_impl.cuh).  Their own
 // translation unit, so that the other instances keep their code generation.
 #include "gemv_impl.cuh"
 

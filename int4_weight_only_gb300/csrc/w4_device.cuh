@@ -314,12 +314,27 @@ __device__ __forceinline__ uint32_t quant_s8(float v, float s, float rs) {
     return (uint32_t)(uint8_t)(int8_t)(int)fminf(fmaxf(rintf(t), -127.f), 127.f);
 }
 
-// Eight values to eight INT8 bytes; all zero when s = 0.
+// Eight values to eight INT8 bytes, as quant_s8 each; all zero when s = 0.
+// One branch for the eight (the quotient is rarely needed), so that the
+// eight products, tests and conversions are independent instructions.
 __device__ __forceinline__ uint2 quant_s8x8(const float f[8], float s, float rs) {
     if (s == 0.f) return make_uint2(0u, 0u);
+    float t[8];
+    bool near = false;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        t[j] = f[j] * rs;
+        near |= !(fabsf(fabsf(t[j] - truncf(t[j])) - 0.5f) > 0x1p-14f);
+    }
+    if (near) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (!(fabsf(fabsf(t[j] - truncf(t[j])) - 0.5f) > 0x1p-14f)) t[j] = __fdiv_rn(f[j], s);
+    }
     uint32_t b[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) b[j] = quant_s8(f[j], s, rs);
+    for (int j = 0; j < 8; ++j)
+        b[j] = (uint32_t)(uint8_t)(int8_t)(int)fminf(fmaxf(rintf(t[j]), -127.f), 127.f);
     return make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24),
                       b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
 }

@@ -80,12 +80,13 @@ struct GemvArgs {
     const uint16_t* offs_b;
     // fp32 outputs [M, N] without bias (row-parallel partial sums), instead of y
     float* y32;
-    // SwiGLU with INT8 outputs: qx [M, Fp] int8, sx_out [M], and the row-block
+    // SwiGLU with INT8 outputs: qx [M, Fp] int8, sx_out [M], the CTA
     // completion ticket (the last counter of the workspace prefix)
     int8_t* qx;
     float* sx_out;
     int Fp;
     int* done;
+    unsigned* ymax;           // [16] per-token max|y| (fp32 bits), zero between calls
 };
 
 // The launchers encode the tensor map of `packed` for the plan's box shape
@@ -151,6 +152,14 @@ int launch_w4a16_gemm(const uint16_t* x, const uint8_t* packed, const float* sca
                       int Kp, int G, const GemmPlan& p, void* workspace, int* err,
                       cudaStream_t stream, const uint16_t* scales_b = nullptr,
                       const uint16_t* offs_b = nullptr, float* y32 = nullptr);
+// Grouped (experts) prefill on the tensor cores: group e's tokens, rows
+// goff[e] .. goff[e+1] - 1 of x [T, K], times its Ne x K matrix (rows
+// e * Ne .. of the stacked weights), in tiles of 64 (tile <= 64) or 256
+// tokens; requires K % 8 == 0 and a 16-byte aligned x.
+int launch_w4a16_grouped_gemm(const uint16_t* x, const int* goff, const uint8_t* packed,
+                              const float* scales, const uint8_t* zeros, const float* bias,
+                              uint16_t* y, int T, int E, int Ne, int K, int Kp, int G, int tile,
+                              int* err, cudaStream_t stream);
 // ysum [M, N] fp32 + bias -> y bf16 (the last step of a row-parallel layer).
 int launch_partial_finish(const float* ysum, const float* bias, uint16_t* y, int M, int N,
                           cudaStream_t stream);

@@ -112,7 +112,7 @@ def test_host_argument_checks_later_entry_points(lib):
     assert lib.w4a16_linear_swiglu(*bad) == c["W4_ERR_UNSUPPORTED_SHAPE"]
     # w4a16_grouped_linear: tile 0 and 17, E = 0, misaligned x
     gr = [ok16, ok16, ok16, ok16, None, None, ok16, 8, 4, 64, 64, 32, 1, 4, None]
-    for i, v in ((13, 0), (13, 17), (8, 0)):
+    for i, v in ((13, 0), (13, 257), (8, 0)):
         bad = list(gr); bad[i] = v
         assert lib.w4a16_grouped_linear(*bad) == c["W4_ERR_INVALID_ARG"]
     bad = list(gr); bad[0] = odd

@@ -129,7 +129,7 @@ def test_grouped_empty_and_argument_errors(w4):
     x = WL.make_activations(K, 4, 2).cuda()
     goff = torch.tensor([0, 4, 4, 4, 4], dtype=torch.int32, device="cuda")
     with pytest.raises(w4.W4Error) as e:
-        w4.w4a16_grouped_linear(x, goff, packed.cuda(), scales.cuda(), None, None, E, N, K, G, 17)
+        w4.w4a16_grouped_linear(x, goff, packed.cuda(), scales.cuda(), None, None, E, N, K, G, 257)
     assert e.value.code == -1
     # every token in group 0, the rest idle
     y = w4.w4a16_grouped_linear(x, goff, packed.cuda(), scales.cuda(), None, None, E, N, K, G, 4)

@@ -60,6 +60,7 @@ def test_prefill_workloads(w4, M, which):
 @pytest.mark.parametrize("pair,bn,split,kb", [
     (1, 256, 1, 1), (1, 256, 2, 1), (1, 256, 3, 1), (0, 256, 1, 1), (0, 256, 2, 1), (0, 128, 1, 1),
     (0, 128, 4, 1), (1, 256, 1, 2), (1, 256, 2, 2), (0, 256, 1, 2), (0, 256, 3, 2),
+    (0, 64, 1, 1), (0, 64, 3, 1), (0, 64, 1, 2), (0, 64, 2, 2),
 ])
 @pytest.mark.parametrize("M,N,K,G,sym", [
     (300, 520, 1000, 64, False), (700, 384, 3584, 128, True), (40, 1000, 512, 32, True),

@@ -31,23 +31,25 @@ def w4():
     return ensure_built()
 
 
-def _case(M, F, K, G, sym, seed, zero_token=False):
+def _case(M, F, K, G, sym, seed, zero_token=False, bias=True):
     packed, scales, zeros = WL.make_random_format(2 * F, K, G, sym, seed)
     x = WL.make_activations(K, M, seed + 1)
     if zero_token:
         x[M - 1] = 0
-    b = torch.randn(2 * F, generator=torch.Generator().manual_seed(seed + 2)) * 0.5
+    b = (torch.randn(2 * F, generator=torch.Generator().manual_seed(seed + 2)) * 0.5
+         if bias else None)
     return packed, scales, zeros, x, b
 
 
-def _check(w4, M, F, K, G, sym, Gq, seed, zero_token=False):
-    packed, scales, zeros, x, b = _case(M, F, K, G, sym, seed, zero_token)
+def _check(w4, M, F, K, G, sym, Gq, seed, zero_token=False, bias=True):
+    packed, scales, zeros, x, b = _case(M, F, K, G, sym, seed, zero_token, bias)
     args = (x.cuda(), packed.cuda(), scales.cuda(), None if zeros is None else zeros.cuda(),
-            b.cuda(), F, K, G)
+            None if b is None else b.cuda(), F, K, G)
     y, qx, sx = w4.w4a16_linear_swiglu_q8(*args, Gq)
     torch.cuda.synchronize()
     yref = O.w4a16_linear_swiglu(x, packed.numpy(), scales.numpy(),
-                                 None if zeros is None else zeros.numpy(), b.numpy(), F, K, G)
+                                 None if zeros is None else zeros.numpy(),
+                                 None if b is None else b.numpy(), F, K, G)
     assert_close(y, yref, f"swiglu_q8 y M{M} F{F} K{K}")
     Fp = O.padded_k(F, Gq)
     oq, osx = O.w4a8_quantize_act(y.cpu(), Fp)
@@ -74,9 +76,11 @@ def test_swiglu_q8_matches_oracle_and_two_launches(w4, M, F, K, G, sym, Gq):
     _check(w4, M, F, K, G, sym, Gq, seed=M + F + K)
 
 
-@pytest.mark.parametrize("rows", ["16", "128"])
-@pytest.mark.parametrize("split", ["1", "3"])
+@pytest.mark.parametrize("rows,split", [("16", "1"), ("16", "2"), ("16", "4"),
+                                        ("128", "1"), ("128", "3")])
 def test_swiglu_q8_every_plan(w4, rows, split):
+    """Forced stage heights and K splits (K = 8192: four 2048-column stages
+    of 16 rows, thirty-two 256-column stages of 128 rows)."""
     old = {k: os.environ.get(k) for k in ("W4_GEMV_ROWS", "W4_GEMV_SPLIT")}
     os.environ["W4_GEMV_ROWS"], os.environ["W4_GEMV_SPLIT"] = rows, split
     try:
@@ -90,12 +94,28 @@ def test_swiglu_q8_every_plan(w4, rows, split):
 
 
 def test_swiglu_q8_zero_token_and_reuse(w4):
-    """A token of zeros gets s_x = 0 and q_x = 0; two calls in a row on the
-    same workspace (its completion counter returns to zero)."""
+    """A token of zeros (no bias, so its y is zero) gets s_x = 0 and q_x = 0;
+    two calls in a row on the same workspace (its completion counter and
+    token maxima return to zero)."""
     for _ in range(2):
-        y, qx, sx = _check(w4, 3, 256, 1024, 128, True, 128, seed=5, zero_token=True)
+        y, qx, sx = _check(w4, 3, 256, 1024, 128, True, 128, seed=5, zero_token=True,
+                           bias=False)
         assert float(sx[2]) == 0.0 and not to_np(qx)[2].any()
     assert w4.w4_get_device_error() == 0
+
+
+def test_swiglu_q8_maxima_do_not_carry_over(w4):
+    """The per-token maxima live in the shared workspace: a call whose y is
+    a thousand times smaller than the previous call's still gets its own
+    s_x (a stale maximum would give larger scales and mostly-zero codes)."""
+    packed, scales, zeros, x, b = _case(16, 512, 1024, 128, True, 9, bias=False)
+    for xs in (x, x * 1e-3):
+        xs = xs.to(torch.bfloat16)
+        args = (xs.cuda(), packed.cuda(), scales.cuda(), None, None, 512, 1024, 128)
+        y, qx, sx = w4.w4a16_linear_swiglu_q8(*args, 128)
+        oq, osx = O.w4a8_quantize_act(y.cpu(), 512)
+        assert np.array_equal(to_np(sx).view(np.uint32), osx.view(np.uint32))
+        assert np.array_equal(to_np(qx), oq)
 
 
 def test_swiglu_q8_argument_errors(w4):
