@@ -241,7 +241,7 @@ int w4a16_linear(const uint16_t* x, const uint8_t* packed, const float* scales,
     rc = split_workspace(p, workspace, workspace_bytes, &a.tickets, &a.partial);
     if (rc) return rc;
     a.x = x; a.scales = scales; a.zeros = zeros; a.bias = bias; a.y = y;
-    a.xtma = (K % 8) == 0 && gemv_tma_activations(M);
+    a.xtma = (K % 8) == 0 && gemv_tma_activations(p);
     a.err = device_error_flag();
     if (!a.err) return W4_ERR_CUDA;
     a.M = M; a.N = N; a.K = K; a.Kp = (int)Kp; a.G = group_size; a.Ng = (int)(Kp / group_size);
@@ -284,7 +284,7 @@ int w4a16_linear_partial(const uint16_t* x, const uint8_t* packed, const float* 
     rc = split_workspace(p, workspace, workspace_bytes, &a.tickets, &a.partial);
     if (rc) return rc;
     a.x = x; a.scales = scales; a.zeros = zeros; a.bias = nullptr; a.y = nullptr; a.y32 = y32;
-    a.xtma = (K % 8) == 0 && gemv_tma_activations(M);
+    a.xtma = (K % 8) == 0 && gemv_tma_activations(p);
     a.err = device_error_flag();
     if (!a.err) return W4_ERR_CUDA;
     a.M = M; a.N = N; a.K = K; a.Kp = (int)Kp; a.G = group_size; a.Ng = (int)(Kp / group_size);
@@ -337,7 +337,7 @@ int w4a16_linear_bf16p(const uint16_t* x, const uint8_t* packed, const uint16_t*
     rc = split_workspace(p, workspace, workspace_bytes, &a.tickets, &a.partial);
     if (rc) return rc;
     a.x = x; a.scales_b = scales_b; a.offs_b = offsets_b; a.bias = bias; a.y = y;
-    a.xtma = (K % 8) == 0 && gemv_tma_activations(M);
+    a.xtma = (K % 8) == 0 && gemv_tma_activations(p);
     a.err = device_error_flag();
     if (!a.err) return W4_ERR_CUDA;
     a.M = M; a.N = N; a.K = K; a.Kp = (int)Kp; a.G = group_size; a.Ng = (int)(Kp / group_size);
@@ -370,7 +370,7 @@ int w4a16_linear_swiglu(const uint16_t* x, const uint8_t* packed, const float* s
     rc = split_workspace(p, workspace, workspace_bytes, &a.tickets, &a.partial);
     if (rc) return rc;
     a.x = x; a.scales = scales; a.zeros = zeros; a.bias = bias; a.y = y;
-    a.xtma = (K % 8) == 0 && gemv_tma_activations(M);
+    a.xtma = (K % 8) == 0 && gemv_tma_activations(p);
     a.err = device_error_flag();
     if (!a.err) return W4_ERR_CUDA;
     a.M = M; a.N = N; a.K = K; a.Kp = (int)Kp; a.G = group_size; a.Ng = (int)(Kp / group_size);
@@ -414,7 +414,7 @@ int w4a16_linear_swiglu_q8(const uint16_t* x, const uint8_t* packed, const float
     a.ymax = reinterpret_cast<unsigned*>(static_cast<int*>(workspace) + (kMaxCounters - 17));
     a.qx = qx; a.sx_out = sx; a.Fp = (int)Fp;
     a.x = x; a.scales = scales; a.zeros = zeros; a.bias = bias; a.y = y;
-    a.xtma = (K % 8) == 0 && gemv_tma_activations(M);
+    a.xtma = (K % 8) == 0 && gemv_tma_activations(p);
     a.err = device_error_flag();
     if (!a.err) return W4_ERR_CUDA;
     a.M = M; a.N = N; a.K = K; a.Kp = (int)Kp; a.G = group_size; a.Ng = (int)(Kp / group_size);

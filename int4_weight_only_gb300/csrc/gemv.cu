@@ -6,10 +6,10 @@
 
 namespace w4 {
 
-bool gemv_tma_activations(int M) {
+bool gemv_tma_activations(const GemvPlan& p) {
     const char* e = std::getenv("W4_GEMV_XTMA");
     if (e) return std::atoi(e) == 1;
-    return M >= 4;
+    return !p.f16;
 }
 
 namespace {
@@ -21,14 +21,15 @@ bool plan_gemv_search(int M, int N, int Kp, int G, int act_bytes, int sm_count, 
 // repeated calls of one layer skip the search.
 bool plan_gemv(int M, int N, int Kp, int G, int act_bytes, int sm_count, GemvPlan* out,
                int groups) {
-    auto env = [](const char* n) {
+    auto env = [](const char* n) {       // unset: 0; set: 1 + its value
         const char* e = std::getenv(n);
-        return e ? std::atoi(e) : 0;
+        return e ? 1 + std::atoi(e) : 0;
     };
-    const std::array<int, 10> key = {M, N, Kp, G, act_bytes, sm_count, env("W4_GEMV_ROWS"),
-                                     env("W4_GEMV_SPLIT"), env("W4_GEMV_CPS"), groups};
+    const std::array<int, 11> key = {M, N, Kp, G, act_bytes, sm_count, env("W4_GEMV_ROWS"),
+                                     env("W4_GEMV_SPLIT"), env("W4_GEMV_CPS"),
+                                     env("W4_GEMV_F16"), groups};
     static std::mutex mu;
-    static std::map<std::array<int, 10>, std::pair<bool, GemvPlan>> cache;
+    static std::map<std::array<int, 11>, std::pair<bool, GemvPlan>> cache;
     {
         std::lock_guard<std::mutex> lk(mu);
         auto it = cache.find(key);
@@ -50,9 +51,22 @@ namespace {
 bool plan_gemv_search(int M, int N, int Kp, int G, int act_bytes, int sm_count, GemvPlan* out,
                       int groups) {
     if (M < 1 || M > 16 || N < 1 || Kp < 1 || G < 32 || sm_count < 1) return false;
+    const int pad = act_bytes == 2 ? 64 : 16;
+    // W4A16 inner loop: fp16 for one or two tokens with groups of 64 or more
+    // columns (its unpacking takes the fewest ALU operations per weight, and
+    // its per-group offset removal and activation conversion, which grow with
+    // the tokens, stay small), else bf16 (no conversion of the activations;
+    // measured faster from 4 tokens, and at any M for G = 32).
+    // W4_GEMV_F16=0/1 overrides where the group size allows.
+    const char* ef = std::getenv("W4_GEMV_F16");
+    const bool f16 = act_bytes == 2 && G % 64 == 0 && (ef ? std::atoi(ef) == 1 : M <= 2);
     const int gq = G / 32;
     const int cpg = (gq % 8 == 0) ? 8 : (gq % 4 == 0) ? 4 : (gq % 2 == 0) ? 2 : 1;
-    const int pad = act_bytes == 2 ? 64 : 16;
+    // the fp16 path also keeps four floats per token and segment of cpg*32
+    // columns
+    auto xseg_bytes = [&](int slice) -> size_t {
+        return f16 ? (size_t)M * (slice / (cpg * 32)) * 16 : 0;
+    };
     // cross-warp reduction buffer: per thread NT*4 floats (W4A16) or MT*2 ints (W4A8)
     const int red = act_bytes == 2
         ? CW * 32 * ((M > 8 ? 2 : 1) * 4) * 4
@@ -61,10 +75,6 @@ bool plan_gemv_search(int M, int N, int Kp, int G, int act_bytes, int sm_count, 
     // activations; `groups` is its capacity
     const size_t list_bytes = groups > 0 ? (((size_t)groups * 4 + 15) & ~(size_t)15) : 0;
     const size_t fixed = 1024 + (size_t)NS * STAGE_BYTES + kCtlBytes + red + list_bytes;
-    // W4A16 also keeps four floats per token and segment of cpg*32 columns
-    auto xseg_bytes = [&](int slice) -> size_t {
-        return act_bytes == 2 ? (size_t)M * (slice / (cpg * 32)) * 16 : 0;
-    };
     const double wbytes = (double)N * Kp / 2.0;
     const double bw_total = 6.5e12, bw_sm = 70e9;
     double best = 1e30;
@@ -93,7 +103,7 @@ bool plan_gemv_search(int M, int N, int Kp, int G, int act_bytes, int sm_count, 
             const int nst = (Kp + SKE - 1) / SKE;
             const int NB = (N + R - 1) / R;
             const int spl_max =
-                (int)(per_tok / ((long)SKE * act_bytes + (act_bytes == 2 ? SKE / (2 * cpg) : 0)));
+                (int)(per_tok / ((long)SKE * act_bytes + (f16 ? SKE / (2 * cpg) : 0)));
             if (spl_max < 1) continue;
             const int s_min = (nst + spl_max - 1) / spl_max;
             for (int S = s_min; S <= nst && S <= s_min + 64; ++S) {
@@ -116,10 +126,12 @@ bool plan_gemv_search(int M, int N, int Kp, int G, int act_bytes, int sm_count, 
                 const double sm_bytes = (double)per_cta * ctas_on_sm * unit_bytes;
                 double t = std::max(wbytes / bw_total, sm_bytes / bw_sm);
                 t += per_cta * 0.3e-6 + (Se > 1 ? 1.5e-6 : 0.0);
-                // every CTA converts the activation slice of its units
-                // (measured ~0.13 ns per column and token, W4A16)
+                // every CTA waits for the activation slice of its units (and
+                // on the fp16 path converts it: measured ~0.13 ns per column
+                // and token)
                 if (act_bytes == 2)
-                    t += per_cta * (0.3e-6 + 0.13e-9 * (double)std::min(spl * SKE, Kp) * M);
+                    t += per_cta * (0.3e-6 + (f16 ? 0.13e-9 : 0.02e-9) *
+                                                 (double)std::min(spl * SKE, Kp) * M);
                 if (t < best * (1 - 1e-9)) {
                     best = t;
                     found = true;
@@ -128,6 +140,7 @@ bool plan_gemv_search(int M, int N, int Kp, int G, int act_bytes, int sm_count, 
                     p.units = units; p.grid = grid; p.cps = cps; p.red = red;
                     p.XS = spl * SKE * act_bytes + pad;
                     p.smem = fixed + (size_t)M * p.XS + xseg_bytes(spl * SKE);
+                    p.f16 = f16;
                     p.list_off = p.smem - list_bytes - 1024;
                     p.ws_bytes = 0;
                     if (Se > 1) p.ws_bytes = kCounterBytes + (size_t)Se * M * N * 4;

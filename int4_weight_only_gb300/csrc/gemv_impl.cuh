@@ -31,17 +31,19 @@
 //
 // W4A16 inner product: each 32-bit ldmatrix word holds 8 codes of one row;
 // one LOP3 per pair ORs the codes into the mantissa of fp16 1024.0 (both
-// nibbles of a byte fit the 10-bit mantissa, as 1024 + c and 1024 + 16c), and
-// these exact words feed mma.sync m16n8k16 (fp16 inputs, fp32 accumulation)
-// directly as the A operand (16 weight rows), with the activations as the B
-// operand (8 tokens per n-tile).  The activations are converted to fp16
-// exactly: each group's run of columns is scaled by a power of two first (and
-// scaled back at the flush), odd columns also by 1/16.  The order of k inside a 32-column chunk is permuted
-// identically on both operands, so no data shuffles are needed.  All MMAs
-// between two flushes see columns of one group: at the flush the offset
-// terms of that run of columns are removed and the group scale applied to the
-// fp32 partial sums, so the weights stay exact.
-//
+// nibbles of a byte fit the 10-bit mantissa, as 1024 + c and 1024 + 16c),
+// and one f16x2 subtraction of the row's 1024 + z (1024 + 16z) leaves
+// (c - z) and 16 (c - z), small integers held exactly.  These words feed
+// mma.sync m16n8k16 (fp16 inputs, fp32 accumulation) as the A operand (16
+// weight rows), with the activations as the B operand (8 tokens per n-tile).
+// The activations are converted to fp16 exactly: each token's slice is
+// scaled by a power of two first (undone in the epilogue), odd columns also
+// by 1/16.  The order of k inside a 32-column chunk is permuted identically
+// on both operands, so no data shuffles are needed.  Every product is exact
+// in fp32; the MMAs of one group's run of columns accumulate into a fresh
+// register set, which is then scaled by the group's s and added to the
+// running sums.
+
 // Launch: programmatic dependent launch.  Before waiting for the previous
 // kernel on the stream, each CTA reads only constant inputs: the producer
 // prefetches the first stages of its first unit into L2, the consumers load
@@ -217,7 +219,42 @@ __device__ void gemv_producer(const CUtensorMap* tm, uint8_t* wbuf, uint8_t* xbu
     }
 }
 
-// Activations of one unit into shared memory as fp16, columns [k0, k0+nk).
+// Activations of one unit in shared memory: bf16 rows of columns [k0,
+// k0+nk) as they are in x (nk a multiple of 256), columns >= K zero (the
+// padded weights there are zero, but stale shared memory could hold NaNs).
+// FROM_SMEM: the producer's copy of the first ncol columns has landed (K a
+// multiple of 8), only the zero tail is written; otherwise the threads copy
+// the slice from global memory.
+template <bool FROM_SMEM>
+__device__ __forceinline__ void stage_x_bf16(uint8_t* xbuf, const uint16_t* x, int M, int K,
+                                             int XS, int k0, int nk, int tid) {
+    const int nblk = nk >> 3;
+    const int ncol = min(nk, K - k0);                  // columns inside x
+    const int b0 = FROM_SMEM ? ncol >> 3 : 0;          // first block written here
+    const int nb = nblk - b0, items = M * nb;
+    const bool vec = (K & 7) == 0;
+    for (int i = tid; i < items; i += NCT) {
+        const int m = i / nb, b = b0 + (i - m * nb);
+        const int k = k0 + b * 8;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (!FROM_SMEM) {
+            const uint16_t* src = x + (size_t)m * K + k;
+            if (vec && k + 8 <= K) {
+                v = __ldg(reinterpret_cast<const uint4*>(src));
+            } else if (k < K) {
+                uint16_t e[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) e[j] = (k + j < K) ? __ldg(src + j) : (uint16_t)0;
+                v = make_uint4((uint32_t)e[0] | ((uint32_t)e[1] << 16), (uint32_t)e[2] | ((uint32_t)e[3] << 16),
+                               (uint32_t)e[4] | ((uint32_t)e[5] << 16), (uint32_t)e[6] | ((uint32_t)e[7] << 16));
+            }
+        }
+        *reinterpret_cast<uint4*>(xbuf + (size_t)m * XS + b * 16) = v;
+    }
+}
+
+// F16 path: activations of one unit into shared memory as fp16, columns
+// [k0, k0+nk).
 // nk is a multiple of 256, so the slice is a whole number of segments of
 // CPG*32 columns (one group's share of a box, BLK = CPG*4 blocks of 8
 // columns).  An item is one (token, segment); L neighbouring lanes take it,
@@ -384,7 +421,7 @@ struct Smem {
     SmemCtl* ctl;
     float* red;
     uint8_t* xbuf;
-    float* xseg;      // W4A16: per-segment sums of x, after M * XS bytes of xbuf
+    float* xseg;      // F16 path: per-segment sums of x, after M * XS bytes of xbuf
 };
 
 template <bool GROUPED = false>
@@ -555,11 +592,12 @@ __device__ __forceinline__ void swiglu_q8_finish(const GemvArgs& a, SmemCtl* ctl
 // Q8 (with SWIGLU): the last CTA to finish also quantizes the whole output
 // y [M, F] to INT8 (swiglu_q8_finish).
 template <int NT, int CPG, bool ASYM, bool SPLIT, bool SWIGLU = false, bool GROUPED = false,
-          bool SB = false, bool F32 = false, bool Q8 = false>
+          bool SB = false, bool F32 = false, bool Q8 = false, bool F16 = false>
 __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
     static_assert(!(GROUPED && (SPLIT || SWIGLU)), "grouped plans are unsplit, plain epilogue");
     static_assert(!(F32 && (SWIGLU || GROUPED || SB)), "fp32 partial outputs: plain layer only");
     static_assert(!Q8 || (SWIGLU && !GROUPED && !SB && !F32), "INT8 outputs: SwiGLU epilogue only");
+    static_assert(!F16 || NT == 1, "the fp16 path takes one token tile");
     constexpr int SEG = 8 / CPG;
     constexpr int LOG_CPG = CPG == 8 ? 3 : CPG == 4 ? 2 : CPG == 2 ? 1 : 0;
     constexpr bool PF = SEG <= 2;           // scales one stage ahead when they are few
@@ -587,7 +625,7 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
 #pragma unroll
     for (int cp = 0; cp < 4; ++cp) l_cp[cp] = l_off + ((uint32_t)((2 * cp + (lj >> 1)) ^ li) << 4);
     uint32_t xrow[NT];
-    int xt[NT][2];
+    int xt[NT][2];                             // F16: this thread's tokens in xseg
     auto token_rows = [&]() {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
@@ -811,15 +849,24 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
         if (ks0 != prev0 || ks1 != prev1) {
             if (xtma) {
                 // everyone is past the previous slice: release its buffer,
-                // then wait for this slice's copy and convert it in place
-                if (xi > 0 && tid == 0) mbar_arrive(&ctl->xempty);
-                if (mbar_wait(&ctl->xfull, xi & 1, &ctl->abort, a.err))
-                    stage_x_f16<CPG, true, NT == 1 ? (SPLIT ? 2 : 4) : 8>(sm.xbuf, sm.xseg, x, M, K, XS,
-                                                            ks0 * SKE, (ks1 - ks0) * SKE, tid);
+                // then wait for this slice's copy and zero its tail
+                if (xi > 0 && tid == 0) {
+                    fence_proxy_async_smem();     // zero tails written here, then the copy
+                    mbar_arrive(&ctl->xempty);
+                }
+                if (mbar_wait(&ctl->xfull, xi & 1, &ctl->abort, a.err)) {
+                    if constexpr (F16)
+                        stage_x_f16<CPG, true, SPLIT ? 2 : 4>(sm.xbuf, sm.xseg, x, M, K, XS,
+                                                             ks0 * SKE, (ks1 - ks0) * SKE, tid);
+                    else
+                        stage_x_bf16<true>(sm.xbuf, x, M, K, XS, ks0 * SKE, (ks1 - ks0) * SKE, tid);
+                }
                 ++xi;
+            } else if constexpr (F16) {
+                stage_x_f16<CPG, false, SPLIT ? 2 : 4>(sm.xbuf, sm.xseg, x, M, K, XS, ks0 * SKE,
+                                                      (ks1 - ks0) * SKE, tid);
             } else {
-                stage_x_f16<CPG, false, NT == 1 ? (SPLIT ? 2 : 4) : 8>(sm.xbuf, sm.xseg, x, M, K, XS,
-                                                         ks0 * SKE, (ks1 - ks0) * SKE, tid);
+                stage_x_bf16<false>(sm.xbuf, x, M, K, XS, ks0 * SKE, (ks1 - ks0) * SKE, tid);
             }
             named_bar_sync(1, NCT);
             prev0 = ks0;
@@ -832,10 +879,16 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) acc[nt][j] = 0.f;
 
-        // The MMA sums x' * w' over each run of CPG chunks (one group), with
-        // w' = 1024 + c on even and 1024 + 16c on odd columns and x' the
-        // segment's scaled activations (odd ones / 16); with the segment's
-        // (u, C0, C1) from staging, acc += s * (u * tmp - C0 - z * C1).
+        // bf16 path: the MMA sums (c - z) x over each run of CPG chunks (one
+        // group), c - z exact in bf16 (the 128 + z offsets are subtracted from
+        // the unpacked words), x the bf16 activations as they are: tmp = sum
+        // (c - z) x, every product exact in fp32, and acc += s * tmp.  SB with
+        // offsets: c - 8 in place of c - z, and a second MMA with weights 1
+        // gives C1 = sum x, so acc += s * tmp + o * C1.
+        // F16 path: the MMA sums x' * w' with w' = 1024 + c on even and
+        // 1024 + 16c on odd columns and x' the segment's scaled activations
+        // (odd ones / 16); with the segment's (u, C0, C1) from staging,
+        // acc += s * (u * tmp - C0 - z * C1).
 
         for (int ks = ks0; ks < ks1; ++ks, ++it) {
             const int slot = it % NS;
@@ -848,55 +901,115 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
                 if (mbar_wait(&ctl->full[slot], (it / NS) & 1, &ctl->abort, a.err)) {
                     const uint32_t wst = wbuf_u + slot * STAGE_BYTES;
                     const uint32_t xoff = (uint32_t)(ks - ks0) * (uint32_t)(SKE * 2);
-                    const float* xs_st =
-                        sm.xseg + 4 * ((((ks - ks0) * SKE + kp * 256) >> (5 + LOG_CPG)) * M);
-                    float tmp[NT][4];
-#pragma unroll
-                    for (int cp = 0; cp < 4; ++cp) {
-                        uint32_t r[4];
-                        ldmatrix_x4_nc(wst + l_cp[cp], r[0], r[1], r[2], r[3]);
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const int c = 2 * cp + h;
-                            const int seg = c / CPG;
-                            uint32_t P[4], Q[4];
-                            nibbles_to_f16x2_biased(r[2 * h], P);
-                            nibbles_to_f16x2_biased(r[2 * h + 1], Q);
-#pragma unroll
-                            for (int nt = 0; nt < NT; ++nt) {
-                                uint32_t X[4];
-                                lds128(xrow[nt] + xoff + c * 64, X);
-                                mma_f16_16816(tmp[nt], P[0], Q[0], P[1], Q[1], X[0], X[1],
-                                              (c % CPG == 0) ? zc : tmp[nt]);
-                                mma_f16_16816(tmp[nt], P[2], Q[2], P[3], Q[3], X[2], X[3], tmp[nt]);
-                            }
-                            if ((c + 1) % CPG == 0) {
-#pragma unroll
+                    if constexpr (F16) {
+                        const float* xs_st =
+                            sm.xseg + 4 * ((((ks - ks0) * SKE + kp * 256) >> (5 + LOG_CPG)) * M);
+                        float tmp[NT][4];
+    #pragma unroll
+                        for (int cp = 0; cp < 4; ++cp) {
+                            uint32_t r[4];
+                            ldmatrix_x4_nc(wst + l_cp[cp], r[0], r[1], r[2], r[3]);
+    #pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                const int c = 2 * cp + h;
+                                const int seg = c / CPG;
+                                uint32_t P[4], Q[4];
+                                nibbles_to_f16x2_biased(r[2 * h], P);
+                                nibbles_to_f16x2_biased(r[2 * h + 1], Q);
+    #pragma unroll
                                 for (int nt = 0; nt < NT; ++nt) {
-                                    const float4 e0 = *reinterpret_cast<const float4*>(
-                                        xs_st + 4 * seg * M + xt[nt][0]);
-                                    const float4 e1 = *reinterpret_cast<const float4*>(
-                                        xs_st + 4 * seg * M + xt[nt][1]);
-                                    float c00, c01, c10, c11;   // C0 + z C1 per (row, token)
-                                    if (ASYM && !SB) {
-                                        c00 = fmaf(zr[seg], e0.z, e0.y);
-                                        c01 = fmaf(zr[seg], e1.z, e1.y);
-                                        c10 = fmaf(zr8[seg], e0.z, e0.y);
-                                        c11 = fmaf(zr8[seg], e1.z, e1.y);
-                                    } else {
-                                        c00 = c10 = fmaf(8.f, e0.z, e0.y);
-                                        c01 = c11 = fmaf(8.f, e1.z, e1.y);
+                                    uint32_t X[4];
+                                    lds128(xrow[nt] + xoff + c * 64, X);
+                                    mma_f16_16816(tmp[nt], P[0], Q[0], P[1], Q[1], X[0], X[1],
+                                                  (c % CPG == 0) ? zc : tmp[nt]);
+                                    mma_f16_16816(tmp[nt], P[2], Q[2], P[3], Q[3], X[2], X[3], tmp[nt]);
+                                }
+                                if ((c + 1) % CPG == 0) {
+    #pragma unroll
+                                    for (int nt = 0; nt < NT; ++nt) {
+                                        const float4 e0 = *reinterpret_cast<const float4*>(
+                                            xs_st + 4 * seg * M + xt[nt][0]);
+                                        const float4 e1 = *reinterpret_cast<const float4*>(
+                                            xs_st + 4 * seg * M + xt[nt][1]);
+                                        float c00, c01, c10, c11;   // C0 + z C1 per (row, token)
+                                        if (ASYM && !SB) {
+                                            c00 = fmaf(zr[seg], e0.z, e0.y);
+                                            c01 = fmaf(zr[seg], e1.z, e1.y);
+                                            c10 = fmaf(zr8[seg], e0.z, e0.y);
+                                            c11 = fmaf(zr8[seg], e1.z, e1.y);
+                                        } else {
+                                            c00 = c10 = fmaf(8.f, e0.z, e0.y);
+                                            c01 = c11 = fmaf(8.f, e1.z, e1.y);
+                                        }
+                                        if (ASYM && SB) {           // + o C1 (zr: offsets)
+                                            acc[nt][0] = fmaf(zr[seg], e0.z, acc[nt][0]);
+                                            acc[nt][1] = fmaf(zr[seg], e1.z, acc[nt][1]);
+                                            acc[nt][2] = fmaf(zr8[seg], e0.z, acc[nt][2]);
+                                            acc[nt][3] = fmaf(zr8[seg], e1.z, acc[nt][3]);
+                                        }
+                                        acc[nt][0] = fmaf(sr[seg], fmaf(e0.x, tmp[nt][0], -c00), acc[nt][0]);
+                                        acc[nt][1] = fmaf(sr[seg], fmaf(e1.x, tmp[nt][1], -c01), acc[nt][1]);
+                                        acc[nt][2] = fmaf(sr8[seg], fmaf(e0.x, tmp[nt][2], -c10), acc[nt][2]);
+                                        acc[nt][3] = fmaf(sr8[seg], fmaf(e1.x, tmp[nt][3], -c11), acc[nt][3]);
                                     }
-                                    if (ASYM && SB) {           // + o C1 (zr: offsets)
-                                        acc[nt][0] = fmaf(zr[seg], e0.z, acc[nt][0]);
-                                        acc[nt][1] = fmaf(zr[seg], e1.z, acc[nt][1]);
-                                        acc[nt][2] = fmaf(zr8[seg], e0.z, acc[nt][2]);
-                                        acc[nt][3] = fmaf(zr8[seg], e1.z, acc[nt][3]);
+                                }
+                            }
+                        }
+                    } else {
+                        float tmp[NT][4];
+                        float c1[(ASYM && SB) ? NT : 1][4];
+    #pragma unroll
+                        for (int cp = 0; cp < 4; ++cp) {
+                            uint32_t r[4];
+                            ldmatrix_x4_nc(wst + l_cp[cp], r[0], r[1], r[2], r[3]);
+    #pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                const int c = 2 * cp + h;
+                                const int seg = c / CPG;
+                                // bf16 pairs 128 + z of the two rows (z = 8 unless ASYM && !SB)
+                                uint32_t o = 0x43084308u, oh = 0x43084308u;
+                                if constexpr (ASYM && !SB) {
+                                    o = (0x4300u + (uint32_t)(int)zr[seg]) * 0x10001u;
+                                    oh = (0x4300u + (uint32_t)(int)zr8[seg]) * 0x10001u;
+                                }
+                                // thread tig holds codes k = 8 tig .. 8 tig + 7 of the
+                                // chunk (rows gid, gid + 8) and reads x at the same k
+                                uint32_t P[4], Q[4];
+                                nibbles_to_bf16x2_pairs(r[2 * h], P);
+                                nibbles_to_bf16x2_pairs(r[2 * h + 1], Q);
+    #pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    P[i] = sub_bf16x2(P[i], o);
+                                    Q[i] = sub_bf16x2(Q[i], oh);
+                                }
+    #pragma unroll
+                                for (int nt = 0; nt < NT; ++nt) {
+                                    uint32_t X[4];
+                                    lds128(xrow[nt] + xoff + c * 64, X);
+                                    mma_bf16_16816(tmp[nt], P[0], Q[0], P[1], Q[1], X[0], X[1],
+                                                   (c % CPG == 0) ? zc : tmp[nt]);
+                                    mma_bf16_16816(tmp[nt], P[2], Q[2], P[3], Q[3], X[2], X[3], tmp[nt]);
+                                    if constexpr (ASYM && SB) {
+                                        const uint32_t one = 0x3F803F80u;          // bf16 pairs (1, 1)
+                                        mma_bf16_16816(c1[nt], one, one, one, one, X[0], X[1],
+                                                       (c % CPG == 0) ? zc : c1[nt]);
+                                        mma_bf16_16816(c1[nt], one, one, one, one, X[2], X[3], c1[nt]);
                                     }
-                                    acc[nt][0] = fmaf(sr[seg], fmaf(e0.x, tmp[nt][0], -c00), acc[nt][0]);
-                                    acc[nt][1] = fmaf(sr[seg], fmaf(e1.x, tmp[nt][1], -c01), acc[nt][1]);
-                                    acc[nt][2] = fmaf(sr8[seg], fmaf(e0.x, tmp[nt][2], -c10), acc[nt][2]);
-                                    acc[nt][3] = fmaf(sr8[seg], fmaf(e1.x, tmp[nt][3], -c11), acc[nt][3]);
+                                }
+                                if ((c + 1) % CPG == 0) {
+    #pragma unroll
+                                    for (int nt = 0; nt < NT; ++nt) {
+                                        if constexpr (ASYM && SB) {       // + o C1 (zr: offsets)
+                                            acc[nt][0] = fmaf(zr[seg], c1[nt][0], acc[nt][0]);
+                                            acc[nt][1] = fmaf(zr[seg], c1[nt][1], acc[nt][1]);
+                                            acc[nt][2] = fmaf(zr8[seg], c1[nt][2], acc[nt][2]);
+                                            acc[nt][3] = fmaf(zr8[seg], c1[nt][3], acc[nt][3]);
+                                        }
+                                        acc[nt][0] = fmaf(sr[seg], tmp[nt][0], acc[nt][0]);
+                                        acc[nt][1] = fmaf(sr[seg], tmp[nt][1], acc[nt][1]);
+                                        acc[nt][2] = fmaf(sr8[seg], tmp[nt][2], acc[nt][2]);
+                                        acc[nt][3] = fmaf(sr8[seg], tmp[nt][3], acc[nt][3]);
+                                    }
                                 }
                             }
                         }
@@ -1360,14 +1473,22 @@ k_w4a8g_gemv_m16(const __grid_constant__ CUtensorMap tmW, const GemvArgs a) {
 // Kernel instances that the plan may place two to an SM (M <= 8 for W4A16,
 // M <= 4 for W4A8) are compiled for two resident CTAs of 288 threads.
 template <int NT, int CPG, bool ASYM, bool SPLIT, bool SWIGLU, bool GROUPED, bool SB, bool F32,
-          bool Q8>
+          bool Q8, bool F16 = false>
 __device__ __forceinline__ void w4a16_body(const CUtensorMap* tm, const GemvArgs& a) {
     const Smem sm = gemv_init<GROUPED>(tm, a);
     if (threadIdx.x >= NCT) {
         if (threadIdx.x == NCT) gemv_producer<GROUPED>(tm, sm.wbuf, sm.xbuf, sm.ctl, a);
     } else {
-        w4a16_consumer<NT, CPG, ASYM, SPLIT, SWIGLU, GROUPED, SB, F32, Q8>(sm, a);
+        w4a16_consumer<NT, CPG, ASYM, SPLIT, SWIGLU, GROUPED, SB, F32, Q8, F16>(sm, a);
     }
+}
+
+// One token tile on the fp16 path (1 or 2 tokens, groups of 64 or more).
+template <int CPG, bool ASYM, bool SPLIT, bool SWIGLU, bool GROUPED = false, bool SB = false,
+          bool F32 = false, bool Q8 = false>
+__global__ void __launch_bounds__(kGemvThreads, 2)
+k_w4a16_gemv_m2(const __grid_constant__ CUtensorMap tmW, const GemvArgs a) {
+    w4a16_body<1, CPG, ASYM, SPLIT, SWIGLU, GROUPED, SB, F32, Q8, true>(&tmW, a);
 }
 
 template <int CPG, bool ASYM, bool SPLIT, bool SWIGLU, bool GROUPED = false, bool SB = false,
@@ -1454,6 +1575,14 @@ template <int NT, bool ASYM, bool SPLIT, bool SWIGLU = false, bool GROUPED = fal
           bool SB = false, bool F32 = false, bool Q8 = false>
 int launch_w4a16_cpg(int cpg, const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
                      cudaStream_t st) {
+    if (NT == 1 && p.f16) {
+        switch (cpg) {
+            case 8: return launch(k_w4a16_gemv_m2<8, ASYM, SPLIT, SWIGLU, GROUPED, SB, F32, Q8>, packed, a, p, st);
+            case 4: return launch(k_w4a16_gemv_m2<4, ASYM, SPLIT, SWIGLU, GROUPED, SB, F32, Q8>, packed, a, p, st);
+            case 2: return launch(k_w4a16_gemv_m2<2, ASYM, SPLIT, SWIGLU, GROUPED, SB, F32, Q8>, packed, a, p, st);
+            default: return W4_ERR_UNSUPPORTED_GROUP;
+        }
+    }
     if (NT == 1) {
         switch (cpg) {
             case 8: return launch(k_w4a16_gemv_m8<8, ASYM, SPLIT, SWIGLU, GROUPED, SB, F32, Q8>, packed, a, p, st);

@@ -88,7 +88,7 @@ extern "C" int w4a16_linear_noalloc(const uint16_t* x, const uint8_t* packed,
         a.partial = static_cast<unsigned char*>(base) + kCounterBytes;
     }
     a.x = x; a.scales = scales; a.zeros = zeros; a.bias = bias; a.y = y;
-    a.xtma = (K % 8) == 0 && gemv_tma_activations(M);
+    a.xtma = (K % 8) == 0 && gemv_tma_activations(p);
     a.err = device_error_flag();
     if (!a.err) return W4_ERR_CUDA;
     a.M = M; a.N = N; a.K = K; a.Kp = (int)Kp; a.G = group_size;

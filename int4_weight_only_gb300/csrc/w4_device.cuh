@@ -217,32 +217,25 @@ __device__ __forceinline__ uint32_t and_or(uint32_t x, uint32_t mask, uint32_t b
     return r;
 }
 
+// a - b on bf16 pairs (exact for the small integers it is used on).
 __device__ __forceinline__ uint32_t sub_bf16x2(uint32_t a, uint32_t b) {
     uint32_t r;
     asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
     return r;
 }
 
-// Eight 4-bit codes c0..c7 (c_i in bits 4i..4i+3 of v) -> four bf16x2 words
-// holding (c_i - z, c_{i+4} - z) for i = 0..3, exactly.  The nibble is OR-ed
-// into the mantissa of bf16 128.0 (0x4300), which gives 128 + c exactly;
-// subtracting 128 + z (zb = 0x4300 + z in both halves) leaves c - z.
-__device__ __forceinline__ void nibbles_to_bf16x2(uint32_t v, uint32_t zb, uint32_t* o) {
-    const uint32_t m = 0x000F000Fu, e = 0x43004300u;
-    o[0] = sub_bf16x2(and_or(v, m, e), zb);
-    o[1] = sub_bf16x2(and_or(v >> 4, m, e), zb);
-    o[2] = sub_bf16x2(and_or(v >> 8, m, e), zb);
-    o[3] = sub_bf16x2(and_or(v >> 12, m, e), zb);
-}
-
-// Same eight codes -> four bf16x2 words (128 + c_i, 128 + c_{i+4}), exact;
-// the caller removes the 128 + z offset after the dot product.
-__device__ __forceinline__ void nibbles_to_bf16x2_biased(uint32_t v, uint32_t* o) {
-    const uint32_t m = 0x000F000Fu, e = 0x43004300u;
-    o[0] = and_or(v, m, e);
-    o[1] = and_or(v >> 4, m, e);
-    o[2] = and_or(v >> 8, m, e);
-    o[3] = and_or(v >> 12, m, e);
+// Eight 4-bit codes c0..c7 of v (c_i in bits 4i..4i+3) -> four bf16x2 words
+// (128 + c0, 128 + c1), (128 + c2, 128 + c3), (128 + c4, 128 + c5),
+// (128 + c6, 128 + c7), exact: bf16 128.0 (0x4300) has seven mantissa bits
+// of spacing 1, so a code OR-ed into the low four gives 128 + c.  A byte
+// permute puts the two codes of one byte (from v and from v >> 4) into the
+// two halves, one LOP3 masks them and adds the exponent.
+__device__ __forceinline__ void nibbles_to_bf16x2_pairs(uint32_t v, uint32_t* o) {
+    const uint32_t vh = v >> 4, m = 0x000F000Fu, e = 0x43004300u;
+    o[0] = and_or(__byte_perm(v, vh, 0x4400), m, e);
+    o[1] = and_or(__byte_perm(v, vh, 0x5511), m, e);
+    o[2] = and_or(__byte_perm(v, vh, 0x6622), m, e);
+    o[3] = and_or(__byte_perm(v, vh, 0x7733), m, e);
 }
 
 // Eight codes c0..c7 of v -> four fp16x2 words, exact:

@@ -43,6 +43,7 @@ struct GemvPlan {
     size_t smem = 0;   // dynamic shared memory (bytes)
     size_t ws_bytes = 0;
     size_t list_off = 0;  // grouped plans: offset of the active-group list in shared memory
+    bool f16 = false;  // W4A16: the fp16 inner loop (1-2 tokens, G >= 64), else bf16
 };
 
 // act_bytes: bytes per activation element (2 for bf16, 1 for int8).
@@ -92,10 +93,11 @@ struct GemvArgs {
 // The launchers encode the tensor map of `packed` for the plan's box shape
 // and launch with programmatic dependent launch enabled.
 // Whether decode CTAs copy their activation slice into shared memory with a
-// bulk TMA copy before converting it (from 4 tokens up), instead of reading
-// it from global memory while converting it (1-3 tokens: measured 3.5%
-// faster on the 7B step at one token).  W4_GEMV_XTMA=0/1 overrides.
-bool gemv_tma_activations(int M);
+// bulk TMA copy (the bf16 path, which uses the slice as it is), instead of
+// reading it from global memory while converting it (the fp16 path of 1-2
+// tokens: measured 3.5% faster on the 7B step at one token).
+// W4_GEMV_XTMA=0/1 overrides.
+bool gemv_tma_activations(const GemvPlan& p);
 // Decode with the SwiGLU epilogue: a.N = 2F paired gate/up rows, y [M, F].
 int launch_w4a16_swiglu(const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
                         cudaStream_t stream);

@@ -18,6 +18,9 @@ Each test checks that the call returns, that the flag reports the timeout,
 and that the next calls with the switch off and the default limit are right:
 the grouped call and a split-K decode call (so the device and the split-K
 counters are in order)."""
+import contextlib
+import os
+
 import pytest
 import torch
 
@@ -54,6 +57,21 @@ def _grouped_case():
     return args, ref
 
 
+@contextlib.contextmanager
+def _split4():
+    """The planner's knob pins four K slices (grouped plans never split, so
+    it is set only around the plain decode calls)."""
+    old = os.environ.get("W4_GEMV_SPLIT")
+    os.environ["W4_GEMV_SPLIT"] = "4"
+    try:
+        yield
+    finally:
+        if old is None:
+            os.environ.pop("W4_GEMV_SPLIT", None)
+        else:
+            os.environ["W4_GEMV_SPLIT"] = old
+
+
 def _split_k_case():
     N, K, G = 3584, 18944, 128
     packed, scales, _ = WL.make_random_format(N, K, G, True, 3)
@@ -66,7 +84,8 @@ def _split_k_case():
 def test_wait_runs_out_and_next_calls_are_right(w4, mode):
     gargs, gref = _grouped_case()
     dargs, dref = _split_k_case()
-    assert w4.w4a16_workspace_bytes(1, dargs[5], dargs[6], dargs[7]) > 0   # split-K plan
+    with _split4():
+        assert w4.w4a16_workspace_bytes(1, dargs[5], dargs[6], dargs[7]) > 0   # split-K plan
     assert w4.w4_get_device_error() == 0
     w4.w4_set_wait_limit(SHORT_LIMIT)
     w4.w4_set_fault_injection(mode)
@@ -79,7 +98,8 @@ def test_wait_runs_out_and_next_calls_are_right(w4, mode):
     assert err == W4_ERR_DEVICE_TIMEOUT
     for _ in range(2):
         assert_close(w4.w4a16_grouped_linear(*gargs), gref, "grouped call after the timeout")
-        assert_close(w4.w4a16_linear(*dargs), dref, "split-K call after the timeout")
+        with _split4():
+            assert_close(w4.w4a16_linear(*dargs), dref, "split-K call after the timeout")
     assert w4.w4_get_device_error() == 0
 
 
@@ -89,7 +109,8 @@ def test_switch_is_ignored_elsewhere_and_rejects_bad_modes(w4):
     dargs, dref = _split_k_case()
     w4.w4_set_fault_injection(2)
     try:
-        y = w4.w4a16_linear(*dargs)
+        with _split4():
+            y = w4.w4a16_linear(*dargs)
         err = w4.w4_get_device_error()
     finally:
         w4.w4_set_fault_injection(0)

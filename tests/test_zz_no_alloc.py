@@ -46,9 +46,12 @@ def _noalloc(lib, x, packed, scales, zeros, bias, y, N, K, G):
     (16, 4608, 3584, 128, False, True),    # 16 tokens, asymmetric, K split
     (3, 200, 100, 32, True, False),        # small ragged shape, one pass over K
 ])
-def test_noalloc_matches_workspace_entry_point(w4, M, N, K, G, sym, split):
+def test_noalloc_matches_workspace_entry_point(w4, monkeypatch, M, N, K, G, sym, split):
     lib = w4.load()
-    # a workspace size > 0 is what makes the plan split K, and so use the scratch
+    # the split is pinned (the planner's knob) so that the scratch path runs
+    # whatever the cost model prefers; a workspace size > 0 is what makes the
+    # plan split K, and so use the scratch
+    monkeypatch.setenv("W4_GEMV_SPLIT", "2" if split else "1")
     assert (w4.w4a16_workspace_bytes(M, N, K, G) > 0) == split
     seed = M + N + K
     packed, scales, zeros = WL.make_random_format(N, K, G, sym, seed)
@@ -78,10 +81,12 @@ def test_noalloc_matches_workspace_entry_point(w4, M, N, K, G, sym, split):
     assert w4.w4_get_device_error() == 0
 
 
-def test_noalloc_rejects_shapes_beyond_its_scratch(w4):
-    """16 tokens x 16384 outputs x K=32768 needs >= 8 K-splits of
-    16 x 16384 fp32 partials (8 MiB), more than the 4 MiB built in."""
+def test_noalloc_rejects_shapes_beyond_its_scratch(w4, monkeypatch):
+    """16 tokens x 16384 outputs x K=32768 with the plan pinned to 8 K
+    slices needs 8 x 16 x 16384 fp32 partials (8 MiB), more than the 4 MiB
+    built in."""
     lib = w4.load()
+    monkeypatch.setenv("W4_GEMV_SPLIT", "8")
     M, N, K, G = 16, 16384, 32768, 128
     assert w4.w4a16_workspace_bytes(M, N, K, G) > W4_NOALLOC_SCRATCH_BYTES
     x = torch.zeros(M, K, dtype=torch.bfloat16, device="cuda")
