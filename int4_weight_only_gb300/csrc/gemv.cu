@@ -25,11 +25,11 @@ bool plan_gemv(int M, int N, int Kp, int G, int act_bytes, int sm_count, GemvPla
         const char* e = std::getenv(n);
         return e ? 1 + std::atoi(e) : 0;
     };
-    const std::array<int, 11> key = {M, N, Kp, G, act_bytes, sm_count, env("W4_GEMV_ROWS"),
+    const std::array<int, 12> key = {M, N, Kp, G, act_bytes, sm_count, env("W4_GEMV_ROWS"),
                                      env("W4_GEMV_SPLIT"), env("W4_GEMV_CPS"),
-                                     env("W4_GEMV_F16"), groups};
+                                     env("W4_GEMV_F16"), env("W4_GEMV_CSPLIT"), groups};
     static std::mutex mu;
-    static std::map<std::array<int, 11>, std::pair<bool, GemvPlan>> cache;
+    static std::map<std::array<int, 12>, std::pair<bool, GemvPlan>> cache;
     {
         std::lock_guard<std::mutex> lk(mu);
         auto it = cache.find(key);
@@ -59,6 +59,15 @@ bool plan_gemv_search(int M, int N, int Kp, int G, int act_bytes, int sm_count, 
     // measured faster from 4 tokens, and at any M for G = 32).
     // W4_GEMV_F16=0/1 overrides where the group size allows.
     const char* ef = std::getenv("W4_GEMV_F16");
+    // K splits added in a cluster where they fit, for 3-8 tokens (measured:
+    // 11% faster than the global hand-off on the 12B down projection at 4
+    // tokens; 2.6% slower on the 7B step at one token, whose launches
+    // overlap the previous kernel's tail, which whole clusters wait out;
+    // slower at 16 tokens, where the one-wave limit leaves SMs idle).
+    // W4_GEMV_CSPLIT=0 turns it off, =1 allows it at any M.
+    const char* ec = std::getenv("W4_GEMV_CSPLIT");
+    const bool csplit_ok = act_bytes == 2 && groups == 0 &&
+                           (ec ? std::atoi(ec) == 1 : (M >= 3 && M <= 8));
     const bool f16 = act_bytes == 2 && G % 64 == 0 && (ef ? std::atoi(ef) == 1 : M <= 2);
     const int gq = G / 32;
     const int cpg = (gq % 8 == 0) ? 8 : (gq % 4 == 0) ? 4 : (gq % 2 == 0) ? 2 : 1;
@@ -124,8 +133,17 @@ bool plan_gemv_search(int M, int N, int Kp, int G, int act_bytes, int sm_count, 
                 const int ctas_on_sm = (grid + sm_count - 1) / sm_count;
                 const double unit_bytes = (double)R * std::min(spl * SKE, Kp) / 2.0;
                 const double sm_bytes = (double)per_cta * ctas_on_sm * unit_bytes;
+                // cluster split: up to 8 splits, one wave, the other ranks'
+                // sums in rank 0's shared memory (the k-phase register layout)
+                const size_t crecv = (size_t)(Se - 1) * (R / 16) * (M > 8 ? 2 : 1) * 512;
+                const bool csplit = csplit_ok && Se > 1 && Se <= 8 && units <= grid &&
+                                    fixed + (size_t)M * (spl * SKE * act_bytes + pad) +
+                                            xseg_bytes(spl * SKE) + crecv <= cap;
                 double t = std::max(wbytes / bw_total, sm_bytes / bw_sm);
-                t += per_cta * 0.3e-6 + (Se > 1 ? 1.5e-6 : 0.0);
+                // the hand-off of the splits: a global ticket and a round
+                // trip of partial sums, or (cluster) one arrival in
+                // distributed shared memory
+                t += per_cta * 0.3e-6 + (Se > 1 ? (csplit ? 0.9e-6 : 1.5e-6) : 0.0);
                 // every CTA waits for the activation slice of its units (and
                 // on the fp16 path converts it: measured ~0.13 ns per column
                 // and token)
@@ -141,6 +159,11 @@ bool plan_gemv_search(int M, int N, int Kp, int G, int act_bytes, int sm_count, 
                     p.XS = spl * SKE * act_bytes + pad;
                     p.smem = fixed + (size_t)M * p.XS + xseg_bytes(spl * SKE);
                     p.f16 = f16;
+                    p.csplit = csplit;
+                    if (csplit) {
+                        p.smem += crecv;
+                        p.crecv_off = p.smem - 1024 - crecv;   // from the aligned base
+                    }
                     p.list_off = p.smem - list_bytes - 1024;
                     p.ws_bytes = 0;
                     if (Se > 1) p.ws_bytes = kCounterBytes + (size_t)Se * M * N * 4;

@@ -58,6 +58,7 @@
 #include <cstdlib>
 #include <map>
 #include <mutex>
+#include <tuple>
 
 namespace w4 {
 namespace {
@@ -78,6 +79,7 @@ struct SmemCtl {
     uint64_t xempty;       // consumers released the activation buffer
     uint64_t listready;    // grouped: the (group, token tile) list is written
     int nact;              // grouped: number of items in it
+    uint64_t cready;       // cluster split, rank 0: the other ranks' partials landed
 };
 constexpr int kCtlBytes = 256;
 static_assert(sizeof(SmemCtl) <= kCtlBytes, "control block");
@@ -444,6 +446,7 @@ __device__ __forceinline__ Smem gemv_init(const CUtensorMap* tm, const GemvArgs&
         mbar_init(&sm.ctl->xfull, 1);
         mbar_init(&sm.ctl->xempty, 1);
         if constexpr (GROUPED) mbar_init(&sm.ctl->listready, 1);
+        if (a.csplit) mbar_init(&sm.ctl->cready, a.S - 1);
         sm.ctl->abort = 0;
         sm.ctl->last = 0;
         for (int i = 0; i < 16; ++i) sm.ctl->sumq[i] = 0;
@@ -452,6 +455,9 @@ __device__ __forceinline__ Smem gemv_init(const CUtensorMap* tm, const GemvArgs&
     if (threadIdx.x == NCT) tma_prefetch_desc(tm);
     grid_dep_launch();
     __syncthreads();
+    // cluster split: every rank's barriers are initialized before any remote
+    // arrival (all threads of every CTA of the cluster pass here once)
+    if (a.csplit) cluster_sync();
     return sm;
 }
 
@@ -492,9 +498,6 @@ __device__ __forceinline__ bool split_k_arrive(const GemvArgs& a, SmemCtl* ctl, 
     return ctl->last;
 }
 
-// The INT8 epilogue of the fused SwiGLU call ("Jetson Orin AGX INT4
-// 推理优化实践", section 后续还能继续优化什么, item 2: the activation
-// quantization folded into the op before the integer GEMV).
 // The INT8 epilogue of the fused SwiGLU call ("Jetson Orin AGX INT4
 // 推理优化实践", section 后续还能继续优化什么, item 2: the activation
 // quantization folded into the op before the integer GEMV).
@@ -1048,8 +1051,48 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
             }
         }
 
+        // ---- cluster split: ranks 1..S-1 store their sums into rank 0's
+        // receive buffer (slot s-1, the register layout of the k-phase
+        // buffer) and arrive on its barrier; rank 0 adds them in split order
+        // and writes y like an unsplit plan.  One unit per CTA.
+        bool direct = !SPLIT;                  // this CTA writes y from acc
+        if constexpr (SPLIT) {
+            if (a.csplit) {
+                const int slot_floats = WR * NT * 4 * 32;
+                float* recv = reinterpret_cast<float*>(sm.wbuf + a.crecv_off);
+                const int idx0 = rt * (NT * 4 * 32) + lane;
+                if (s > 0) {
+                    if (kp == 0) {
+                        const uint32_t dst = mapa_shared(smem_u32(recv + (s - 1) * slot_floats + idx0), 0);
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                st_shared_cluster(dst + 4u * (uint32_t)((nt * 4 + j) * 32), acc[nt][j]);
+                    }
+                    named_bar_sync(1, NCT);
+                    if (tid == 0) mbar_arrive_release_cluster(mapa_shared(smem_u32(&ctl->cready), 0));
+                } else {
+                    direct = mbar_wait_cluster(&ctl->cready, 0, &ctl->abort, a.err);
+                    // after an abort elsewhere, still let the other ranks'
+                    // stores into this CTA land before it can exit
+                    if (!direct) mbar_wait_drain(&ctl->cready, 0, a.err);
+                    if (direct && kp == 0) {
+                        for (int q = 1; q < Sp; ++q) {
+                            const float* src = recv + (q - 1) * slot_floats + idx0;
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) acc[nt][j] += src[(nt * 4 + j) * 32];
+                        }
+                    }
+                }
+            }
+        }
+
         // ---- epilogue: thread holds (token 8nt + 2tig + (j&1), row gid + 8(j>>1))
-        if constexpr (SWIGLU && !SPLIT) {
+        if (direct) {
+        if constexpr (SWIGLU) {
             if (kp == 0) {
                 const int F = N >> 1, f = (row0 >> 1) + gid;       // this lane's output column
 #pragma unroll
@@ -1062,7 +1105,7 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
                         if constexpr (Q8) q8_cta_max(ctl, v, t, M, lane, t < M && row0 + gid < N);
                     }
             }
-        } else if constexpr (!SPLIT) {
+        } else {
             if (kp == 0) {
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
@@ -1076,7 +1119,8 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
                         }
                     }
             }
-        } else {
+        }
+        } else if (SPLIT && !a.csplit) {
             float* part = static_cast<float*>(a.partial);
             if (kp == 0) {
 #pragma unroll
@@ -1543,9 +1587,32 @@ inline bool raise_smem_limit(const void* kern, size_t bytes) {
     return true;
 }
 
+// Whether `grid` CTAs in clusters of S fit on the device at once with this
+// launch's shared memory (cached per kernel, device, size and S).
 template <typename Kern>
-int launch(Kern kern, const uint8_t* packed, const GemvArgs& a, const GemvPlan& p,
+bool clusters_fit(const void* key, Kern kern, const cudaLaunchConfig_t& cfg, int S, int grid) {
+    static std::mutex mu;
+    static std::map<std::tuple<const void*, int, size_t, int>, int> done;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    std::lock_guard<std::mutex> lk(mu);
+    const auto k = std::make_tuple(key, dev, cfg.dynamicSmemBytes, S);
+    auto it = done.find(k);
+    if (it == done.end()) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            n = 0;
+        }
+        it = done.emplace(k, n).first;
+    }
+    return (long long)it->second * S >= grid;
+}
+
+template <typename Kern>
+int launch(Kern kern, const uint8_t* packed, const GemvArgs& a0, const GemvPlan& p,
            cudaStream_t stream) {
+    GemvArgs a = a0;
     CUtensorMap tm;
     // grouped launches stack the E groups' rows
     const uint64_t rows = (uint64_t)a.N * (uint64_t)(a.E > 0 ? a.E : 1);
@@ -1562,11 +1629,28 @@ int launch(Kern kern, const uint8_t* packed, const GemvArgs& a, const GemvPlan& 
     cfg.blockDim = dim3(kGemvThreads);
     cfg.dynamicSmemBytes = p.smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    a.csplit = 0;
+    if (p.csplit) {
+        // clusters of the S splits of a row block, when the whole grid fits
+        // on the GPU at once as clusters (else the global hand-off, which the
+        // same kernel and workspace also support)
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = (unsigned)p.S;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
+        if (clusters_fit(reinterpret_cast<const void*>(kern), kern, cfg, p.S, p.grid)) {
+            a.csplit = 1;
+            a.crecv_off = (int)p.crecv_off;
+        } else {
+            cfg.numAttrs = 1;
+        }
+    }
     if (cudaLaunchKernelEx(&cfg, kern, tm, a) != cudaSuccess) return W4_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? W4_OK : W4_ERR_CUDA;
 }

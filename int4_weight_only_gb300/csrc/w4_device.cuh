@@ -489,6 +489,19 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
                  :: "r"(cluster_addr) : "memory");
 }
 
+// Arrive on an mbarrier of another CTA of the cluster with release semantics
+// at cluster scope: this CTA's earlier stores into that CTA's shared memory
+// (st_shared_cluster) are visible to whoever completes the wait.
+__device__ __forceinline__ void mbar_arrive_release_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];"
+                 :: "r"(cluster_addr) : "memory");
+}
+
+// Store to shared memory of a CTA of the cluster (address from mapa_shared).
+__device__ __forceinline__ void st_shared_cluster(uint32_t cluster_addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" :: "r"(cluster_addr), "f"(v) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(

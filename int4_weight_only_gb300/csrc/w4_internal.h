@@ -44,6 +44,12 @@ struct GemvPlan {
     size_t ws_bytes = 0;
     size_t list_off = 0;  // grouped plans: offset of the active-group list in shared memory
     bool f16 = false;  // W4A16: the fp16 inner loop (1-2 tokens, G >= 64), else bf16
+    // K splits added inside a thread-block cluster: the S CTAs of a row block
+    // form one cluster, ranks 1..S-1 store their partial sums into rank 0's
+    // shared memory (a receive buffer at crecv_off), rank 0 adds them in
+    // split order and writes y.  One unit per CTA; S <= 8.
+    bool csplit = false;
+    size_t crecv_off = 0;
 };
 
 // act_bytes: bytes per activation element (2 for bf16, 1 for int8).
@@ -88,6 +94,8 @@ struct GemvArgs {
     int Fp;
     int* done;
     unsigned* ymax;           // [16] per-token max|y| (fp32 bits), zero between calls
+    int csplit;               // K splits added in a cluster (GemvPlan::csplit)
+    int crecv_off;            // shared-memory offset of the cluster receive buffer
 };
 
 // The launchers encode the tensor map of `packed` for the plan's box shape

@@ -262,8 +262,9 @@ def test_workspace_shared_by_shapes(w4, monkeypatch):
 @pytest.mark.parametrize("M,N,K,G,sym", [(1, 4608, 3584, 128, True), (8, 640, 3840, 32, False),
                                          (3, 1000, 18944, 128, True)])
 def test_decode_activation_staging_paths(w4, monkeypatch, xtma, M, N, K, G, sym):
-    """Activations read from global memory while converting (default) or
-    first copied into shared memory by a bulk TMA copy (W4_GEMV_XTMA=1):
+    """Activations read from global memory by the consumer threads
+    (W4_GEMV_XTMA=0, the default of the fp16 loop) or first copied into
+    shared memory by a bulk TMA copy (=1, the default of the bf16 loop):
     same tolerance, same bits for both."""
     monkeypatch.setenv("W4_GEMV_XTMA", xtma)
     seed = M + N + K + G
@@ -278,3 +279,42 @@ def test_decode_activation_staging_paths(w4, monkeypatch, xtma, M, N, K, G, sym)
     monkeypatch.setenv("W4_GEMV_XTMA", "1" if xtma == "0" else "0")
     y2 = w4.w4a16_linear(x.cuda(), packed.cuda(), scales.cuda(), zc, None, N, K, G)
     assert torch.equal(y, y2), "the two staging paths differ"
+
+
+@pytest.mark.parametrize("f16", ["0", "1"])
+@pytest.mark.parametrize("csplit", ["0", "1"])
+@pytest.mark.parametrize("M,N,K,G,sym,split", [
+    (1, 1024, 8192, 128, True, "4"),       # 7B-down-like, one token
+    (2, 520, 7680, 64, False, "3"),        # asymmetric, ragged rows
+    (8, 640, 15360, 128, True, "8"),       # eight splits: the largest cluster
+    (16, 384, 8192, 128, False, "2"),      # two token tiles
+])
+def test_decode_inner_loops_and_split_handoffs(w4, monkeypatch, f16, csplit, M, N, K, G, sym,
+                                               split):
+    """Both inner loops (fp16 with the 1024 + c words, W4_GEMV_F16=1, for 1-2
+    tokens; bf16 with c - z words, =0) and both hand-offs of a K split (the
+    partial sums through a global ticket, W4_GEMV_CSPLIT=0, or through
+    distributed shared memory inside a cluster, =1) against the oracle; the
+    two hand-offs add the same fp32 partials in the same split order, so
+    they agree bit for bit."""
+    if f16 == "1" and M > 2:
+        pytest.skip("the fp16 loop takes 1-2 tokens")
+    monkeypatch.setenv("W4_GEMV_F16", f16)
+    monkeypatch.setenv("W4_GEMV_SPLIT", split)
+    seed = M + N + K + G + int(split)
+    packed, scales, zeros = WL.make_random_format(N, K, G, sym, seed)
+    x = WL.make_activations(K, M, seed + 1)
+    b = torch.randn(N, generator=torch.Generator().manual_seed(seed + 2)) * 0.1
+    args = (x.cuda(), packed.cuda(), scales.cuda(), None if zeros is None else zeros.cuda(),
+            b.cuda(), N, K, G)
+    assert w4.w4a16_workspace_bytes(M, N, K, G) > 0          # the split plan was taken
+    monkeypatch.setenv("W4_GEMV_CSPLIT", csplit)
+    y = w4.w4a16_linear(*args)
+    torch.cuda.synchronize()
+    yref = O.w4a16_linear(x, packed.numpy(), scales.numpy(),
+                          None if zeros is None else zeros.numpy(), b.numpy(), K, G)
+    assert_close(y, yref, f"f16{f16} csplit{csplit} M{M} N{N} K{K} S{split}")
+    monkeypatch.setenv("W4_GEMV_CSPLIT", "1" if csplit == "0" else "0")
+    y2 = w4.w4a16_linear(*args)
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16)), "the two hand-offs differ"
+    assert w4.w4_get_device_error() == 0
