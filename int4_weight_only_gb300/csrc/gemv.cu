@@ -136,7 +136,7 @@ bool plan_gemv_search(int M, int N, int Kp, int G, int act_bytes, int sm_count, 
                 // cluster split: up to 8 splits, one wave, the other ranks'
                 // sums in rank 0's shared memory (the k-phase register layout)
                 const size_t crecv = (size_t)(Se - 1) * (R / 16) * (M > 8 ? 2 : 1) * 512;
-                const bool csplit = csplit_ok && Se > 1 && Se <= 8 && units <= grid &&
+                const bool csplit = csplit_ok && !f16 && Se > 1 && Se <= 8 && units <= grid &&
                                     fixed + (size_t)M * (spl * SKE * act_bytes + pad) +
                                             xseg_bytes(spl * SKE) + crecv <= cap;
                 double t = std::max(wbytes / bw_total, sm_bytes / bw_sm);

@@ -1056,7 +1056,9 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
         // buffer) and arrive on its barrier; rank 0 adds them in split order
         // and writes y like an unsplit plan.  One unit per CTA.
         bool direct = !SPLIT;                  // this CTA writes y from acc
-        if constexpr (SPLIT) {
+        // (not compiled into the fp16-loop instances, whose 1-2 token plans
+        // never take it: left out, their code stays as measured)
+        if constexpr (SPLIT && !F16) {
             if (a.csplit) {
                 const int slot_floats = WR * NT * 4 * 32;
                 float* recv = reinterpret_cast<float*>(sm.wbuf + a.crecv_off);
@@ -1120,7 +1122,7 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
                     }
             }
         }
-        } else if (SPLIT && !a.csplit) {
+        } else if (SPLIT && (F16 || !a.csplit)) {
             float* part = static_cast<float*>(a.partial);
             if (kp == 0) {
 #pragma unroll

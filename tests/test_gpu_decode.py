@@ -294,11 +294,13 @@ def test_decode_inner_loops_and_split_handoffs(w4, monkeypatch, f16, csplit, M, 
     """Both inner loops (fp16 with the 1024 + c words, W4_GEMV_F16=1, for 1-2
     tokens; bf16 with c - z words, =0) and both hand-offs of a K split (the
     partial sums through a global ticket, W4_GEMV_CSPLIT=0, or through
-    distributed shared memory inside a cluster, =1) against the oracle; the
-    two hand-offs add the same fp32 partials in the same split order, so
-    they agree bit for bit."""
+    distributed shared memory inside a cluster, =1; the fp16 loop has only
+    the first) against the oracle; the two hand-offs add the same fp32
+    partials in the same split order, so they agree bit for bit."""
     if f16 == "1" and M > 2:
         pytest.skip("the fp16 loop takes 1-2 tokens")
+    if f16 == "1" and csplit == "1":
+        pytest.skip("the fp16 loop's plans hand splits off through the workspace only")
     monkeypatch.setenv("W4_GEMV_F16", f16)
     monkeypatch.setenv("W4_GEMV_SPLIT", split)
     seed = M + N + K + G + int(split)
