@@ -15,6 +15,7 @@ asymmetric decode), reported as sub-objects of the one JSON line.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -1163,6 +1164,8 @@ def run_case(args):
     allw = (WL.tiny() + WL.decode_7b(args.M) + WL.decode_12b(args.M) + WL.prefill_7b(args.M)
             + WL.w4a8_7b())
     lin = next(l for l in allw if l.name.startswith(args.case))
+    if args.G:                                 # e.g. the W4A8 linear with G = 128 scales
+        lin = dataclasses.replace(lin, group_size=args.G)
     inp = WL.make_inputs(lin, args.M)
     p, sc, z = w4.w4_pack_rtn(inp.W.cuda(), lin.group_size, lin.symmetric)
     x = inp.x.cuda()
@@ -1190,6 +1193,7 @@ def main():
     ap.add_argument("--case", default=None,
                     help="run --reps calls of the workload linear whose name starts with this")
     ap.add_argument("--M", type=int, default=1)
+    ap.add_argument("--G", type=int, default=0, help="--case: override the group size")
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--shard", choices=["n", "k"], default=None,
                     help="time the decode step with every linear split over the ranks: "
