@@ -140,10 +140,22 @@ bool plan_gemv_search(int M, int N, int Kp, int G, int act_bytes, int sm_count, 
                                     fixed + (size_t)M * (spl * SKE * act_bytes + pad) +
                                             xseg_bytes(spl * SKE) + crecv <= cap;
                 double t = std::max(wbytes / bw_total, sm_bytes / bw_sm);
+                if (f16) {
+                    // one or two tokens: the stream is the whole cost, so
+                    // CTAs spread unevenly over the SMs (the busiest SMs set
+                    // the pace) and one CTA's own rate (~35 GB/s) count too
+                    const double imb = (double)ctas_on_sm * sm_count / grid;
+                    t = std::max({wbytes / bw_total * imb, sm_bytes / bw_sm,
+                                  per_cta * unit_bytes / 35e9});
+                }
                 // the hand-off of the splits: a global ticket and a round
                 // trip of partial sums, or (cluster) one arrival in
                 // distributed shared memory
                 t += per_cta * 0.3e-6 + (Se > 1 ? (csplit ? 0.9e-6 : 1.5e-6) : 0.0);
+                // the global hand-off reads back every split's partials
+                // (measured on the 7B down projection: 64-row blocks split 5
+                // ways 11.5 us, 128-row blocks split 10 ways 12.0 us)
+                if (Se > 1 && !csplit) t += 0.08e-6 * (Se - 1);
                 // every CTA waits for the activation slice of its units (and
                 // on the fp16 path converts it: measured ~0.13 ns per column
                 // and token)
