@@ -264,8 +264,10 @@ W4_API int w4a16_linear_swiglu(const uint16_t* x, const uint8_t* packed, const f
  *           multiple of 32; its padded K is Fp).
  * qx and sx equal w4a8_quantize_act(y, q_group_size) bit for bit.  Each
  * CTA folds the max |y| per token of the outputs it wrote into the
- * workspace; the last CTA to finish reads y back and quantizes it, so the
- * workspace is required even when the plan does not split K: at least
+ * workspace; after a grid-wide barrier (the kernel is launched
+ * cooperatively when the device allows it) every CTA quantizes a share of
+ * y, else the last CTA to finish quantizes all of it.  The workspace is
+ * therefore required even when the plan does not split K: at least
  * max(w4a16_workspace_bytes(M, 2F, K, group_size), W4_WORKSPACE_COUNTER_BYTES)
  * bytes, zero-filled once (its counters are left at zero).  M <= 16.
  * ------------------------------------------------------------------------- */

@@ -4,6 +4,8 @@
 #include "w4_device.cuh"
 #include "w4_internal.h"
 
+#include <cstdlib>
+
 #include <algorithm>
 #include <cstddef>
 #include <cstring>
@@ -409,9 +411,14 @@ int w4a16_linear_swiglu_q8(const uint16_t* x, const uint8_t* packed, const float
     GemvArgs a{};
     rc = split_workspace(p, workspace, workspace_bytes, &a.tickets, &a.partial);
     if (rc) return rc;
-    // the last 17 counters of the prefix: 16 per-token maxima, the ticket
+    // the last 34 counters of the prefix: two buffers of 16 per-token maxima,
+    // the call generation, the arrival counter
     a.done = static_cast<int*>(workspace) + (kMaxCounters - 1);
-    a.ymax = reinterpret_cast<unsigned*>(static_cast<int*>(workspace) + (kMaxCounters - 17));
+    a.ymax = reinterpret_cast<unsigned*>(static_cast<int*>(workspace) + (kMaxCounters - 34));
+    // the grid-wide hand-off (cooperative launch); W4_GEMV_COOP=0 keeps the
+    // last-CTA path, for tests of both
+    const char* ecoop = std::getenv("W4_GEMV_COOP");
+    a.coop = (ecoop && std::atoi(ecoop) == 0) ? 0 : 1;
     a.qx = qx; a.sx_out = sx; a.Fp = (int)Fp;
     a.x = x; a.scales = scales; a.zeros = zeros; a.bias = bias; a.y = y;
     a.xtma = (K % 8) == 0 && gemv_tma_activations(p);

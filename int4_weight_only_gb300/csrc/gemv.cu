@@ -119,10 +119,10 @@ bool plan_gemv_search(int M, int N, int Kp, int G, int act_bytes, int sm_count, 
                 const int spl = (nst + S - 1) / S;
                 const int Se = (nst + spl - 1) / spl;
                 if (spl > spl_max) continue;
-                // the last 17 counters of the prefix belong to the SwiGLU
-                // call with INT8 outputs (token maxima and its completion
-                // ticket), never to a row block
-                if ((forced_s && Se != forced_s) || (Se > 1 && NB > kMaxCounters - 17) ||
+                // the last 34 counters of the prefix belong to the SwiGLU
+                // call with INT8 outputs (token maxima, generation, arrival
+                // count), never to a row block
+                if ((forced_s && Se != forced_s) || (Se > 1 && NB > kMaxCounters - 34) ||
                     (groups > 0 && Se > 1)) {
                     if (Se == nst) break;
                     continue;

@@ -80,6 +80,7 @@ struct SmemCtl {
     uint64_t listready;    // grouped: the (group, token tile) list is written
     int nact;              // grouped: number of items in it
     uint64_t cready;       // cluster split, rank 0: the other ranks' partials landed
+    int gen;               // INT8 outputs: the call's generation (maxima buffer parity)
 };
 constexpr int kCtlBytes = 256;
 static_assert(sizeof(SmemCtl) <= kCtlBytes, "control block");
@@ -516,46 +517,81 @@ __device__ __forceinline__ void q8_cta_max(SmemCtl* ctl, float v, int t, int M, 
 }
 
 // Called by every consumer thread once its CTA has no units left.  The CTA
-// adds its maxima with one atomic max per token on a.ymax, then takes a
-// ticket; the CTA that
-// takes the last one has every token's max|y| and every CTA's y stores
-// (the acquire-release tickets publish them) and quantizes y [M, F] in one
-// pass exactly as w4a8_quantize_act does: s_x = fp32(max|y| / 127),
-// q = clip(rint(fp32(y / s_x)), -127, 127), columns F .. Fp-1 zero.  It then
-// clears the maxima and the ticket.
-// IN: 16-byte loads in flight per thread in that pass.
+// adds its maxima with one atomic max per token on a.ymax[buffer], where the
+// buffer is the parity of the call's generation a.gen[0] (so that a call
+// never meets the previous call's maxima), then:
+// * cooperative launch (a.coop, every CTA resident): a grid-wide barrier
+//   (an acquire-release arrival count; the last CTA to arrive clears the
+//   count and the other buffer, then releases the next generation, which
+//   the others wait for with the usual bound), after which every CTA
+//   quantizes its own share of y;
+// * otherwise the CTA that takes the last ticket, which sees every CTA's y
+//   and maxima, quantizes all of y.
+// The rule is w4a8_quantize_act's: s_x = fp32(max|y| / 127), q = clip(rint(
+// fp32(y / s_x)), -127, 127), columns F .. Fp-1 zero.
+// IN: 16-byte loads in flight per thread in a pass.
 template <int IN>
 __device__ __forceinline__ void swiglu_q8_finish(const GemvArgs& a, SmemCtl* ctl, float* red,
                                                  int tid) {
+    int* genp = a.done - 1;
+    if (tid == 0) ctl->gen = ld_acquire_gpu(genp);      // this call's generation
     named_bar_sync(1, NCT);                  // the CTA's shared maxima are final
-    if (tid < a.M && ctl->sumq[tid] != 0) atomicMax(a.ymax + tid, (unsigned)ctl->sumq[tid]);
+    const int g0 = ctl->gen;
+    unsigned* ymax = a.ymax + 16 * (g0 & 1);
+    if (tid < a.M && ctl->sumq[tid] != 0) atomicMax(ymax + tid, (unsigned)ctl->sumq[tid]);
     named_bar_sync(1, NCT);                  // this CTA's y stores and maxima are all issued
-    if (tid == 0) ctl->last = atom_add_acq_rel_gpu(a.done, 1) == (int)gridDim.x - 1;
-    named_bar_sync(1, NCT);
-    if (!ctl->last) return;
     const int F = a.N >> 1, nw = F >> 3, nwp = a.Fp >> 3;
+    const int total = a.M * nwp;
+    int w0 = 0, w1 = total;                  // this CTA's share of the (token, word) pairs
+    if (a.coop) {
+        if (tid == 0) {
+            int ok = 1;
+            if (atom_add_acq_rel_gpu(a.done, 1) == (int)gridDim.x - 1) {
+                *a.done = 0;
+                unsigned* other = a.ymax + 16 * ((g0 + 1) & 1);   // the previous call's
+                for (int i = 0; i < 16; ++i) other[i] = 0u;
+                st_release_gpu(genp, g0 + 1);
+            } else {
+                const long long t0 = clock64(), lim = wait_limit_of(a.err);
+                while (ld_acquire_gpu(genp) == g0) {
+                    if (clock64() - t0 > lim) {
+                        atomicCAS(a.err, 0, W4_ERR_DEVICE_TIMEOUT);
+                        ok = 0;
+                        break;
+                    }
+                }
+            }
+            ctl->last = ok;
+        }
+        named_bar_sync(1, NCT);
+        if (!ctl->last) return;
+        w0 = (int)(((long long)total * blockIdx.x) / gridDim.x);
+        w1 = (int)(((long long)total * (blockIdx.x + 1)) / gridDim.x);
+    } else {
+        if (tid == 0) ctl->last = atom_add_acq_rel_gpu(a.done, 1) == (int)gridDim.x - 1;
+        named_bar_sync(1, NCT);
+        if (!ctl->last) return;
+    }
     if (tid < a.M) {
-        const float mx = __uint_as_float(ld_cg_s32(reinterpret_cast<const int*>(a.ymax) + tid));
+        const float mx = __uint_as_float(ld_cg_s32(reinterpret_cast<const int*>(ymax) + tid));
         const float sc = __fdiv_rn(mx, 127.0f);
         red[2 * tid] = sc;
         red[2 * tid + 1] = sc != 0.f ? __frcp_rn(sc) : 0.f;
-        a.sx_out[tid] = sc;
+        if (!a.coop || blockIdx.x == 0) a.sx_out[tid] = sc;
     }
     named_bar_sync(1, NCT);
-    // all (token, 8-column word) pairs
-    const int total = a.M * nwp;
-    for (int base = tid; base < total; base += IN * NCT) {
+    for (int base = w0 + tid; base < w1; base += IN * NCT) {
         uint4 v[IN];
 #pragma unroll
         for (int i = 0; i < IN; ++i) {
             const int idx = base + i * NCT, m = idx / nwp, w = idx - m * nwp;
-            v[i] = (idx < total && w < nw) ? ld_cg_v4(a.y + (size_t)m * F + 8 * w)
-                                           : make_uint4(0u, 0u, 0u, 0u);
+            v[i] = (idx < w1 && w < nw) ? ld_cg_v4(a.y + (size_t)m * F + 8 * w)
+                                        : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
         for (int i = 0; i < IN; ++i) {
             const int idx = base + i * NCT;
-            if (idx >= total) break;
+            if (idx >= w1) break;
             const int m = idx / nwp, w = idx - m * nwp;
             const uint32_t q[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
             float f[8];
@@ -568,9 +604,11 @@ __device__ __forceinline__ void swiglu_q8_finish(const GemvArgs& a, SmemCtl* ctl
                 w < nw ? quant_s8x8(f, red[2 * m], red[2 * m + 1]) : make_uint2(0u, 0u);
         }
     }
-    named_bar_sync(1, NCT);
-    if (tid < a.M) a.ymax[tid] = 0u;
-    if (tid == 0) *a.done = 0;
+    if (!a.coop) {
+        named_bar_sync(1, NCT);
+        if (tid < a.M) ymax[tid] = 0u;
+        if (tid == 0) *a.done = 0;
+    }
 }
 
 // SPLIT: the plan splits K (Sp > 1).  The two cases are separate kernels
@@ -1637,6 +1675,43 @@ int launch(Kern kern, const uint8_t* packed, const GemvArgs& a0, const GemvPlan&
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     a.csplit = 0;
+    if (a0.coop) {
+        // the INT8 epilogue's grid-wide hand-off needs every CTA resident:
+        // a cooperative launch (with programmatic launch where the driver
+        // accepts both; the outcome is remembered per kernel and device),
+        // else a plain launch whose last CTA quantizes alone
+        static std::mutex mu;
+        static std::map<std::pair<const void*, int>, int> mode;   // 1 coop+PDL, 2 coop, 3 plain
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return W4_ERR_CUDA;
+        int m;
+        {
+            std::lock_guard<std::mutex> lk(mu);
+            m = mode[{reinterpret_cast<const void*>(kern), dev}];
+        }
+        attr[1].id = cudaLaunchAttributeCooperative;
+        attr[1].val.cooperative = 1;
+        for (int mt = m ? m : 1; mt <= 3; ++mt) {
+            a.coop = mt < 3 ? 1 : 0;
+            if (mt == 1) {
+                cfg.attrs = attr;
+                cfg.numAttrs = 2;
+            } else if (mt == 2) {
+                cfg.attrs = attr + 1;
+                cfg.numAttrs = 1;
+            } else {
+                cfg.attrs = attr;
+                cfg.numAttrs = 1;
+            }
+            if (cudaLaunchKernelEx(&cfg, kern, tm, a) == cudaSuccess) {
+                std::lock_guard<std::mutex> lk(mu);
+                mode[{reinterpret_cast<const void*>(kern), dev}] = mt;
+                return cudaGetLastError() == cudaSuccess ? W4_OK : W4_ERR_CUDA;
+            }
+            cudaGetLastError();
+        }
+        return W4_ERR_CUDA;
+    }
     if (p.csplit) {
         // clusters of the S splits of a row block, when the whole grid fits
         // on the GPU at once as clusters (else the global hand-off, which the

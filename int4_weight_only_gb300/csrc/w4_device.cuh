@@ -217,6 +217,16 @@ __device__ __forceinline__ uint32_t and_or(uint32_t x, uint32_t mask, uint32_t b
     return r;
 }
 
+// Acquire load / release store of a flag at GPU scope.
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_gpu(int* p, int v) {
+    asm volatile("st.release.gpu.global.s32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+
 // a - b on bf16 pairs (exact for the small integers it is used on).
 __device__ __forceinline__ uint32_t sub_bf16x2(uint32_t a, uint32_t b) {
     uint32_t r;

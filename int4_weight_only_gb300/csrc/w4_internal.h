@@ -88,13 +88,15 @@ struct GemvArgs {
     // fp32 outputs [M, N] without bias (row-parallel partial sums), instead of y
     float* y32;
     // SwiGLU with INT8 outputs: qx [M, Fp] int8, sx_out [M], the CTA
-    // completion ticket (the last counter of the workspace prefix)
+    // arrival counter (the last counter of the workspace prefix; the one
+    // before it holds the call generation)
     int8_t* qx;
     float* sx_out;
     int Fp;
     int* done;
-    unsigned* ymax;           // [16] per-token max|y| (fp32 bits), zero between calls
+    unsigned* ymax;           // [2][16] per-token max|y| (fp32 bits), by generation parity
     int csplit;               // K splits added in a cluster (GemvPlan::csplit)
+    int coop;                 // INT8 outputs: ask for a cooperative launch (grid-wide hand-off)
     int crecv_off;            // shared-memory offset of the cluster receive buffer
 };
 

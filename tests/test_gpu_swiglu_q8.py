@@ -64,6 +64,7 @@ def _check(w4, M, F, K, G, sym, Gq, seed, zero_token=False, bias=True):
     return y, qx, sx
 
 
+@pytest.mark.parametrize("coop", ["1", "0"])
 @pytest.mark.parametrize("M,F,K,G,sym,Gq", [
     (1, 18944, 3584, 128, True, 18944),     # 7B MLP: the W4A8 down projection per row
     (8, 18944, 3584, 128, True, 128),       # the same, 8 tokens, group-wise W4A8
@@ -72,8 +73,13 @@ def _check(w4, M, F, K, G, sym, Gq, seed, zero_token=False, bias=True):
     (3, 200, 100, 32, False, 64),           # ragged K, asymmetric
     (1, 512, 16384, 128, True, 512),        # split-K plan
 ])
-def test_swiglu_q8_matches_oracle_and_two_launches(w4, M, F, K, G, sym, Gq):
+def test_swiglu_q8_matches_oracle_and_two_launches(w4, monkeypatch, coop, M, F, K, G, sym, Gq):
+    """Both hand-offs of the quantization: every CTA quantizes its share
+    after a grid-wide barrier (cooperative launch, the default), or the last
+    CTA quantizes all of y (W4_GEMV_COOP=0)."""
+    monkeypatch.setenv("W4_GEMV_COOP", coop)
     _check(w4, M, F, K, G, sym, Gq, seed=M + F + K)
+    _check(w4, M, F, K, G, sym, Gq, seed=M + F + K + 1)     # a second call: next generation
 
 
 @pytest.mark.parametrize("rows,split", [("16", "1"), ("16", "2"), ("16", "4"),
@@ -104,12 +110,16 @@ def test_swiglu_q8_zero_token_and_reuse(w4):
     assert w4.w4_get_device_error() == 0
 
 
-def test_swiglu_q8_maxima_do_not_carry_over(w4):
+@pytest.mark.parametrize("coop", ["1", "0", "alt"])
+def test_swiglu_q8_maxima_do_not_carry_over(w4, monkeypatch, coop):
     """The per-token maxima live in the shared workspace: a call whose y is
-    a thousand times smaller than the previous call's still gets its own
-    s_x (a stale maximum would give larger scales and mostly-zero codes)."""
+    a thousand times smaller (or larger) than the previous call's still gets
+    its own s_x (a stale maximum would give larger scales and mostly-zero
+    codes), for either hand-off and for the two alternating."""
     packed, scales, zeros, x, b = _case(16, 512, 1024, 128, True, 9, bias=False)
-    for xs in (x, x * 1e-3):
+    for i, xs in enumerate((x, x * 1e-3, x * 1e3, x)):
+        # alt: the two hand-offs in turn on the same workspace
+        monkeypatch.setenv("W4_GEMV_COOP", str(i % 2) if coop == "alt" else coop)
         xs = xs.to(torch.bfloat16)
         args = (xs.cuda(), packed.cuda(), scales.cuda(), None, None, 512, 1024, 128)
         y, qx, sx = w4.w4a16_linear_swiglu_q8(*args, 128)
