@@ -946,18 +946,18 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
                         const float* xs_st =
                             sm.xseg + 4 * ((((ks - ks0) * SKE + kp * 256) >> (5 + LOG_CPG)) * M);
                         float tmp[NT][4];
-    #pragma unroll
+#pragma unroll
                         for (int cp = 0; cp < 4; ++cp) {
                             uint32_t r[4];
                             ldmatrix_x4_nc(wst + l_cp[cp], r[0], r[1], r[2], r[3]);
-    #pragma unroll
+#pragma unroll
                             for (int h = 0; h < 2; ++h) {
                                 const int c = 2 * cp + h;
                                 const int seg = c / CPG;
                                 uint32_t P[4], Q[4];
                                 nibbles_to_f16x2_biased(r[2 * h], P);
                                 nibbles_to_f16x2_biased(r[2 * h + 1], Q);
-    #pragma unroll
+#pragma unroll
                                 for (int nt = 0; nt < NT; ++nt) {
                                     uint32_t X[4];
                                     lds128(xrow[nt] + xoff + c * 64, X);
@@ -966,7 +966,7 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
                                     mma_f16_16816(tmp[nt], P[2], Q[2], P[3], Q[3], X[2], X[3], tmp[nt]);
                                 }
                                 if ((c + 1) % CPG == 0) {
-    #pragma unroll
+#pragma unroll
                                     for (int nt = 0; nt < NT; ++nt) {
                                         const float4 e0 = *reinterpret_cast<const float4*>(
                                             xs_st + 4 * seg * M + xt[nt][0]);
@@ -999,11 +999,11 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
                     } else {
                         float tmp[NT][4];
                         float c1[(ASYM && SB) ? NT : 1][4];
-    #pragma unroll
+#pragma unroll
                         for (int cp = 0; cp < 4; ++cp) {
                             uint32_t r[4];
                             ldmatrix_x4_nc(wst + l_cp[cp], r[0], r[1], r[2], r[3]);
-    #pragma unroll
+#pragma unroll
                             for (int h = 0; h < 2; ++h) {
                                 const int c = 2 * cp + h;
                                 const int seg = c / CPG;
@@ -1018,12 +1018,12 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
                                 uint32_t P[4], Q[4];
                                 nibbles_to_bf16x2_pairs(r[2 * h], P);
                                 nibbles_to_bf16x2_pairs(r[2 * h + 1], Q);
-    #pragma unroll
+#pragma unroll
                                 for (int i = 0; i < 4; ++i) {
                                     P[i] = sub_bf16x2(P[i], o);
                                     Q[i] = sub_bf16x2(Q[i], oh);
                                 }
-    #pragma unroll
+#pragma unroll
                                 for (int nt = 0; nt < NT; ++nt) {
                                     uint32_t X[4];
                                     lds128(xrow[nt] + xoff + c * 64, X);
@@ -1038,7 +1038,7 @@ __device__ void w4a16_consumer(const Smem& sm, const GemvArgs& a) {
                                     }
                                 }
                                 if ((c + 1) % CPG == 0) {
-    #pragma unroll
+#pragma unroll
                                     for (int nt = 0; nt < NT; ++nt) {
                                         if constexpr (ASYM && SB) {       // + o C1 (zr: offsets)
                                             acc[nt][0] = fmaf(zr[seg], c1[nt][0], acc[nt][0]);
