@@ -935,7 +935,7 @@ def run_ours(args, world, rank):
         "algorithmic_bytes_per_step": ds.bytes_step,
     }
     per_linear = measure_linears(ds, reps=200)
-    ke = min(args.steps, 2000)
+    ke = max(200, min(args.steps, 2000))     # enough steps for a stable host-side rate
     dt, h2d, d2h = measure_e2e(w4, ds, ke)
     dt = max_over_ranks(dt, world)
     e2e = {"value": round(aggregate_gbs(ds.bytes_step, ke, world, dt), 1), "unit": "GB/s",
