@@ -439,11 +439,18 @@ k_w4a16_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                 ok = __all_sync(0xffffffffu, ok);
                 if (ok) {
                     uint8_t* arow = as + sa * A_ST + r * 128;
+                    // With two K blocks a stage, the two threads of a row (h = 0, 1:
+                    // neighbouring lanes) write one chunk each of blocks 0 and 1; in
+                    // the same swizzled position they would hit the same banks, so
+                    // h = 1 takes its chunks in the order jj ^ 4 (a select between
+                    // two register indices, no dynamic indexing)
+                    constexpr int HX = DQ_CHUNKS == 8 ? 4 : 0;
 #pragma unroll
                     for (int jj = 0; jj < DQ_CHUNKS; ++jj) {
-                        const int jg = DQ_CHUNKS * h + jj;      // 16-byte chunk of the stage's row
+                        const int lc = h ? (jj ^ HX) : jj;      // this thread's chunk
+                        const int jg = DQ_CHUNKS * h + lc;      // 16-byte chunk of the stage's row
                         const int j = jg & 7;                   // chunk inside its K block
-                        const uint32_t w = wv[jj], wh = w >> 4;
+                        const uint32_t w = h ? wv[jj ^ HX] : wv[jj], wh = w >> 4;
                         // bf16x2 (128 + c_2i, 128 + c_2i+1) for i = 0..3
                         const uint32_t e = 0x43004300u, m = 0x000F000Fu;
                         const uint32_t p01 = and_or(prmt(w, wh, 0x5410), m, e);
