@@ -140,14 +140,14 @@ __device__ void gemv_producer(const CUtensorMap* tm, uint8_t* wbuf, uint8_t* xbu
                         &ctl->full[slot], pol);
     };
     // The weights are not written by the kernel before this one on the
-    // stream, so while it may still be running the first unit's first NS
+    // stream, so while it may still be running the first unit's first a.pf
     // stages are prefetched into L2.  (Loading them into shared memory here
     // instead was measured slower: those copies compete with the activation
     // copy that follows the wait for the SM's bandwidth.)
     if (!GROUPED && (int)blockIdx.x < a.units) {
         int rb, s, ks0, ks1;
         unit_coords(blockIdx.x, a, rb, s, ks0, ks1);
-        for (int ks = ks0; ks < min(ks1, ks0 + NS); ++ks)
+        for (int ks = ks0; ks < min(ks1, ks0 + a.pf); ++ks)
             for (int b = 0; b < boxes; ++b) {
                 const int kb = ks * (a.SKE / 2) + b * 128;
                 if (kb < kbytes) tma_prefetch_l2_2d(tm, kb, rb * a.R);
@@ -1653,6 +1653,18 @@ template <typename Kern>
 int launch(Kern kern, const uint8_t* packed, const GemvArgs& a0, const GemvPlan& p,
            cudaStream_t stream) {
     GemvArgs a = a0;
+    // stages of the first unit prefetched into L2 before the dependency wait
+    // (W4_GEMV_PF, 0..4).  W4A16: one, measured on the 7B step at one token:
+    // the prefetches compete with the previous kernel's tail and this
+    // kernel's activation reads, so a deeper prefetch that helps a linear
+    // alone (two stages: gate_up 14.8 -> 14.4 us) slows the chain (0: 3,516
+    // GB/s, 1: 3,698, 2: 3,659, 3: 3,581, 4: 3,533).  W4A8 (a.sx set): the
+    // whole ring, since its predecessor is the short activation quantizer
+    // (with one stage the quantizer + up pair went from 8.3 to 9.3 us)
+    {
+        const char* e = std::getenv("W4_GEMV_PF");
+        a.pf = e ? std::max(0, std::min(NS, std::atoi(e))) : (a0.sx ? NS : 1);
+    }
     CUtensorMap tm;
     // grouped launches stack the E groups' rows
     const uint64_t rows = (uint64_t)a.N * (uint64_t)(a.E > 0 ? a.E : 1);

@@ -97,6 +97,7 @@ struct GemvArgs {
     unsigned* ymax;           // [2][16] per-token max|y| (fp32 bits), by generation parity
     int csplit;               // K splits added in a cluster (GemvPlan::csplit)
     int coop;                 // INT8 outputs: ask for a cooperative launch (grid-wide hand-off)
+    int pf;                   // stages of the first unit prefetched into L2 before the wait
     int crecv_off;            // shared-memory offset of the cluster receive buffer
 };
 
