@@ -22,7 +22,7 @@
 // output rows, slice of the padded K), R in {16, 32, 64, 128}; units are dealt
 // round-robin to the CTAs.  The producer streams 16 KB stages of packed
 // weights (128/R TMA boxes of R rows x 128 bytes, 128-byte swizzle) into a
-// 4-deep ring.  Each stage holds eight 16-row x 256-column boxes; consumer
+// 3-deep ring.  Each stage holds eight 16-row x 256-column boxes; consumer
 // warp w takes row tile w % (R/16) and k-phase w / (R/16), i.e. exactly one
 // such box per stage, and reads it with ldmatrix.  Partial sums of the
 // k-phases are added in shared memory in a fixed order; K slices of a row

@@ -23,7 +23,11 @@ bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* bas
 // warp; a unit of work is (block of R output rows, slice of the padded K).
 // A pipeline stage is 16 KB of packed weights: 128/R boxes of R rows x 128
 // bytes (256 columns each), i.e. R rows x 32768/R columns.
-constexpr int kGemvStages = 4;                 // pipeline depth (16 KB stages)
+// pipeline depth of the decode kernels' weight ring (16 KB stages); swept
+// on the full bench: 3 beat 4 on the 7B step (3,748 vs 3,701 GB/s), the
+// fused gate|up + SiLU at 8 tokens (19.1 vs 21.8 us) and the 12B shapes from
+// 4 tokens, at 1-1.5% on the W4A8 GEMVs; 2, 6 and 8 were slower on the step
+constexpr int kGemvStages = 3;
 constexpr int kGemvStageBytes = 16384;
 constexpr int kGemvConsumerWarps = 8;
 constexpr int kGemvThreads = 32 * (kGemvConsumerWarps + 1);

@@ -12,7 +12,7 @@ can never complete (w4_set_fault_injection, grouped decode kernel):
   times out before issuing anything;
 * mode 2: the consumers never free a ring slot, so the producer times out
   with copies in flight (K = 16384: every unit has at least eight stages for
-  a four-deep ring) and drains them before its CTA exits.
+  a three-deep ring) and drains them before its CTA exits.
 
 Each test checks that the call returns, that the flag reports the timeout,
 and that the next calls with the switch off and the default limit are right:
