@@ -393,6 +393,39 @@ W4_API int w4_smooth(const uint16_t* X, int T, float* W, int N, int K, float alp
 W4_API size_t w4a8_workspace_bytes(int M, int N, int K, int group_size);
 
 /* ---------------------------------------------------------------------------
+ * w4_decode_plan - the launch plan the library picks for a decode call
+ * (M <= 16) of one layer, computed on the host alone: no device is touched,
+ * so it answers for any SM count, with or without a GPU.  The pages have no
+ * counterpart; it exposes the library's own planner for inspection and
+ * tests.
+ *
+ *  kind      0: w4a16_linear (and the calls that share its plans:
+ *            _partial, _bf16p, _noalloc); 1: w4a8_linear (per-row or
+ *            group-wise scales).
+ *  M, N, K, group_size  as for those calls; 1 <= M <= 16.
+ *  sm_count  SMs of the device the plan is for (152 on a GB300).
+ *  out       host array of W4_DECODE_PLAN_FIELDS int64, written on success:
+ *    [0] rows of a unit (16, 32, 64 or 128)   [1] K splits S
+ *    [2] stages per split                      [3] stages over the padded K
+ *    [4] K columns per stage (32768 / rows: 16 KB of packed codes)
+ *    [5] units (row blocks x S)                [6] CTAs launched
+ *    [7] CTAs per SM the plan is sized for     [8] dynamic shared memory per
+ *        CTA (bytes)                            [9] workspace bytes (0
+ *        without a K split; else W4_WORKSPACE_COUNTER_BYTES + S*M*N*4)
+ *    [10] 1: the fp16 inner loop (1-2 tokens), 0: bf16 (W4A16) or int8
+ *    [11] 1: the K splits hand off inside a thread-block cluster, 0: the
+ *         global last-arriver hand-off (or no split)
+ *  The tuning variables W4_GEMV_ROWS, W4_GEMV_SPLIT, W4_GEMV_CPS,
+ *  W4_GEMV_F16 and W4_GEMV_CSPLIT apply as they do to the calls.
+ *  Returns W4_ERR_NULL_PTR, W4_ERR_INVALID_ARG (kind, M, N or sm_count out
+ *  of range), W4_ERR_UNSUPPORTED_GROUP, W4_ERR_K_TOO_LARGE (kind 1) or
+ *  W4_ERR_UNSUPPORTED_SHAPE (no plan fits) as the calls would.
+ * ------------------------------------------------------------------------- */
+#define W4_DECODE_PLAN_FIELDS 12
+W4_API int w4_decode_plan(int kind, int M, int N, int K, int group_size, int sm_count,
+                          long long* out);
+
+/* ---------------------------------------------------------------------------
  * w4a8_linear - INT4 x INT8 integer linear layer ([ORIN]):
  *  acc[m,n] = sum_{k < Kp} (code[n,k] - 8) * qx[m,k]   (exact, int32)
  *  y[m,n]   = s_W[n] * s_x[m] * acc[m,n] + bias[n]      (fp32, stored bf16)

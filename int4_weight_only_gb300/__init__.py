@@ -12,6 +12,7 @@ from ._lib import (W4Error, lib_path, load, w4_pack_rtn, w4a16_workspace_bytes,
                    w4a16_linear_partial, w4a16_partial_finish,
                    w4_pack_rtn_bf16, w4a16_linear_bf16p,
                    w4a16_grouped_linear, w4a8_quantize_act, w4a8_workspace_bytes, w4a8_linear,
+                   w4_decode_plan, DECODE_PLAN_FIELDS,
                    w4a8_quantize_act_smooth, w4_smooth, w4_gptq,
                    w4_get_device_error, w4_set_wait_limit, w4_set_fault_injection,
                    w4_error_string, padded_k,
@@ -23,6 +24,7 @@ __all__ = ["W4Error", "lib_path", "load", "w4_pack_rtn", "w4a16_workspace_bytes"
            "w4a16_linear_partial", "w4a16_partial_finish",
            "w4_pack_rtn_bf16", "w4a16_linear_bf16p",
            "w4a16_grouped_linear", "w4a8_quantize_act", "w4a8_workspace_bytes", "w4a8_linear",
+           "w4_decode_plan", "DECODE_PLAN_FIELDS",
            "w4a8_quantize_act_smooth", "w4_smooth", "w4_gptq",
            "w4_get_device_error", "w4_set_wait_limit", "w4_set_fault_injection", "w4_error_string", "padded_k",
            "EXPORTED"]

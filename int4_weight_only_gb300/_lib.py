@@ -40,6 +40,7 @@ _SIGS = {
     "w4_gptq": (_c_int, [_vp, _c_int, _vp, _c_int, _c_int, _c_int, _c_int, ctypes.c_float, _vp,
                          _vp, _vp, _vp, _vp, _c_size, _vp]),
     "w4a8_workspace_bytes": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
+    "w4_decode_plan": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _vp]),
     "w4a8_linear": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
                              _vp, _c_size, _vp]),
     "w4_get_device_error": (_c_int, [_vp]),
@@ -190,6 +191,21 @@ def w4a16_workspace_bytes(M: int, N: int, K: int, group_size: int) -> int:
 
 def w4a8_workspace_bytes(M: int, N: int, K: int, group_size: int) -> int:
     return int(load().w4a8_workspace_bytes(M, N, K, group_size))
+
+
+DECODE_PLAN_FIELDS = ("rows", "splits", "stages_per_split", "stages", "stage_cols", "units",
+                      "grid", "ctas_per_sm", "smem", "workspace", "fp16_loop", "cluster_split")
+
+
+def w4_decode_plan(kind: str, M: int, N: int, K: int, group_size: int,
+                   sm_count: int) -> dict:
+    """The decode launch plan of one layer ("w4a16" or "w4a8"), from the host
+    planner alone (no device needed), as a dict of DECODE_PLAN_FIELDS."""
+    out = (ctypes.c_longlong * len(DECODE_PLAN_FIELDS))()
+    k = {"w4a16": 0, "w4a8": 1}[kind]
+    _check("w4_decode_plan", load().w4_decode_plan(k, M, N, K, group_size, sm_count,
+                                                   ctypes.addressof(out)))
+    return dict(zip(DECODE_PLAN_FIELDS, (int(v) for v in out)))
 
 
 def w4a16_linear(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,

@@ -557,6 +557,29 @@ size_t w4a8_workspace_bytes(int M, int N, int K, int group_size) {
     return p.ws_bytes;
 }
 
+int w4_decode_plan(int kind, int M, int N, int K, int group_size, int sm_count,
+                   long long* out) {
+    if (!out) return W4_ERR_NULL_PTR;
+    if ((kind != 0 && kind != 1) || M < 1 || M > 16 || N <= 0 || sm_count < 1)
+        return W4_ERR_INVALID_ARG;
+    int rc = check_group(K, group_size);
+    if (rc) return rc;
+    const long long Kp = padded_k(K, group_size);
+    if (Kp > 0x7fffffffLL) return W4_ERR_UNSUPPORTED_SHAPE;
+    if (kind == 1) {
+        if (Kp != group_size && !w4a8_group_supported(group_size)) return W4_ERR_UNSUPPORTED_GROUP;
+        if (Kp > W4_W4A8_MAX_KP) return W4_ERR_K_TOO_LARGE;
+    }
+    GemvPlan p;
+    if (!plan_gemv(M, N, (int)Kp, group_size, kind == 0 ? 2 : 1, sm_count, &p))
+        return W4_ERR_UNSUPPORTED_SHAPE;
+    const long long v[W4_DECODE_PLAN_FIELDS] = {
+        p.R, p.S, p.spl, p.nst, p.SKE, p.units, p.grid, p.cps, (long long)p.smem,
+        (long long)p.ws_bytes, p.f16 ? 1 : 0, p.csplit ? 1 : 0};
+    for (int i = 0; i < W4_DECODE_PLAN_FIELDS; ++i) out[i] = v[i];
+    return W4_OK;
+}
+
 int w4a8_linear(const int8_t* qx, const float* sx, const uint8_t* packed,
                 const float* w_scales, const float* bias, uint16_t* y, int32_t* acc_out,
                 int M, int N, int K, int group_size, void* workspace, size_t workspace_bytes,

@@ -320,3 +320,15 @@ def test_decode_inner_loops_and_split_handoffs(w4, monkeypatch, f16, csplit, M, 
     y2 = w4.w4a16_linear(*args)
     assert torch.equal(y.view(torch.int16), y2.view(torch.int16)), "the two hand-offs differ"
     assert w4.w4_get_device_error() == 0
+
+
+@pytest.mark.parametrize("M,N,K,G", [(1, 3584, 18944, 128), (1, 37888, 3584, 128),
+                                     (4, 3840, 15360, 32), (16, 4608, 3584, 128)])
+def test_host_plan_matches_the_device_calls(w4, M, N, K, G):
+    """w4_decode_plan (host planner, any SM count) gives the workspace the
+    calls ask for on this device, for both kinds of decode call."""
+    sm = torch.cuda.get_device_properties(0).multi_processor_count
+    assert w4.w4_decode_plan("w4a16", M, N, K, G, sm)["workspace"] == \
+        w4.w4a16_workspace_bytes(M, N, K, G)
+    assert w4.w4_decode_plan("w4a8", M, N, K, G, sm)["workspace"] == \
+        w4.w4a8_workspace_bytes(M, N, K, G)
