@@ -68,6 +68,10 @@ constexpr int NCT = CW * 32;
 constexpr int NS = kGemvStages;
 constexpr int STAGE_BYTES = kGemvStageBytes;
 
+// the producer's mark in the first segment's (unused) fourth sum on the fp16
+// path, until the consumers' staging writes 0 there
+constexpr uint32_t kXsegSentinel = 0xFFFFFFFFu;
+
 struct SmemCtl {
     uint64_t full[NS];
     uint64_t empty[NS];
@@ -139,6 +143,19 @@ __device__ void gemv_producer(const CUtensorMap* tm, uint8_t* wbuf, uint8_t* xbu
             tma_load_2d(wbuf + slot * STAGE_BYTES + b * box_bytes, tm, kb0 + b * 128, row,
                         &ctl->full[slot], pol);
     };
+    // fp16 path with the activations read by the consumers: after a.xfirst
+    // stages of the first unit the rest of the ring is held until the
+    // consumers have staged their slice, so that their activation loads do
+    // not queue behind every CTA's whole ring of weight copies.  Their
+    // staging writes 0 into the unused fourth sum of the first segment; the
+    // producer leaves a sentinel there first (the consumers start staging
+    // only after the dependency wait and an activation load) and watches it.
+    // A hint only: the watch gives up after about two microseconds, and the
+    // word is never read by the arithmetic.
+    int hold = GROUPED ? -1 : a.xfirst;
+    volatile uint32_t* const xflag =
+        reinterpret_cast<volatile uint32_t*>(xbuf + (size_t)a.M * a.XS) + 3;
+    if (hold >= 0) *xflag = kXsegSentinel;
     // The weights are not written by the kernel before this one on the
     // stream, so while it may still be running the first unit's first a.pf
     // stages are prefetched into L2.  (Loading them into shared memory here
@@ -205,6 +222,10 @@ __device__ void gemv_producer(const CUtensorMap* tm, uint8_t* wbuf, uint8_t* xbu
         }
         for (int ks = ks0; ks < ks1; ++ks, ++it) {
             const int slot = it % NS;
+            if (hold >= 0 && it == (uint32_t)hold) {
+                for (int i = 0; i < 64 && *xflag == kXsegSentinel; ++i) __nanosleep(16);
+                hold = -1;
+            }
             if (it >= (uint32_t)NS &&
                 !mbar_wait(&ctl->empty[slot], ((it / NS) & 1) ^ 1, &ctl->abort, a.err)) {
                 ok = false;
@@ -451,6 +472,7 @@ __device__ __forceinline__ Smem gemv_init(const CUtensorMap* tm, const GemvArgs&
         sm.ctl->abort = 0;
         sm.ctl->last = 0;
         for (int i = 0; i < 16; ++i) sm.ctl->sumq[i] = 0;
+
         fence_mbar_init();
     }
     if (threadIdx.x == NCT) tma_prefetch_desc(tm);
@@ -1664,6 +1686,17 @@ int launch(Kern kern, const uint8_t* packed, const GemvArgs& a0, const GemvPlan&
     {
         const char* e = std::getenv("W4_GEMV_PF");
         a.pf = e ? std::max(0, std::min(NS, std::atoi(e))) : (a0.sx ? NS : 1);
+        // the hold (W4_GEMV_XFIRST=n stages before it, -1 none) exists only
+        // on the fp16 path with the activations read by the consumers, whose
+        // staging writes the per-segment sums it watches.  Default 2 (the
+        // last stage of the 3-deep ring waits), measured on the 7B step at
+        // one token: no hold 3,723 / 3,710 GB/s, after 1 stage 3,660 /
+        // 3,656, after 2 3,764 / 3,758 (gate_up 14.7 -> 14.35 us, down 11.76
+        // -> 11.28; qkv and o, two stages a CTA, are not held)
+        const char* ex = std::getenv("W4_GEMV_XFIRST");
+        a.xfirst = (!a0.sx && a0.E <= 0 && p.f16 && !a0.xtma)
+                       ? (ex ? std::max(-1, std::atoi(ex)) : 2)
+                       : -1;
     }
     CUtensorMap tm;
     // grouped launches stack the E groups' rows

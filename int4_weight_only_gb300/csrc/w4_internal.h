@@ -102,6 +102,7 @@ struct GemvArgs {
     int csplit;               // K splits added in a cluster (GemvPlan::csplit)
     int coop;                 // INT8 outputs: ask for a cooperative launch (grid-wide hand-off)
     int pf;                   // stages of the first unit prefetched into L2 before the wait
+    int xfirst;               // fp16 path: stages issued before holding for the staged activations (-1: no hold)
     int crecv_off;            // shared-memory offset of the cluster receive buffer
 };
 
