@@ -332,3 +332,32 @@ def test_host_plan_matches_the_device_calls(w4, M, N, K, G):
         w4.w4a16_workspace_bytes(M, N, K, G)
     assert w4.w4_decode_plan("w4a8", M, N, K, G, sm)["workspace"] == \
         w4.w4a8_workspace_bytes(M, N, K, G)
+
+
+@pytest.mark.parametrize("M,N,K,G,sym,split", [(1, 3584, 18944, 128, True, "5"),
+                                               (2, 4608, 3584, 64, False, "1"),
+                                               (1, 1000, 4100, 128, True, "0")])
+def test_activation_hold_is_only_timing(w4, monkeypatch, M, N, K, G, sym, split):
+    """The fp16 loop's producer holding its ring until the activations are
+    staged (W4_GEMV_XFIRST = stages before the hold; -1 none, 0 all held)
+    changes when copies are issued, never what is computed: every setting
+    gives the same bits, and they match the oracle (K = 4100: a ragged
+    slice whose activations are read without vector loads)."""
+    if split != "0":
+        monkeypatch.setenv("W4_GEMV_SPLIT", split)
+    seed = M + N + K
+    packed, scales, zeros = WL.make_random_format(N, K, G, sym, seed)
+    x = WL.make_activations(K, M, seed + 1)
+    args = (x.cuda(), packed.cuda(), scales.cuda(), None if zeros is None else zeros.cuda(),
+            None, N, K, G)
+    outs = []
+    for hold in ("-1", "0", "1", "2", "3"):
+        monkeypatch.setenv("W4_GEMV_XFIRST", hold)
+        outs.append(w4.w4a16_linear(*args))
+    torch.cuda.synchronize()
+    yref = O.w4a16_linear(x, packed.numpy(), scales.numpy(),
+                          None if zeros is None else zeros.numpy(), None, K, G)
+    assert_close(outs[0], yref, f"hold M{M} N{N} K{K}")
+    for y in outs[1:]:
+        assert torch.equal(y.view(torch.int16), outs[0].view(torch.int16))
+    assert w4.w4_get_device_error() == 0
