@@ -7,7 +7,7 @@ the library through ctypes on the current torch stream.  Every step of the
 computation runs in the library's CUDA kernels; there is no fallback.
 """
 from ._lib import (W4Error, lib_path, load, w4_pack_rtn, w4a16_workspace_bytes,
-                   w4a16_linear, W4A16Linear, w4a16_linear_noalloc, w4a16_linear_swiglu, w4a16_linear_swiglu_q8,
+                   w4a16_linear, w4a16_linear_noalloc, w4a16_linear_swiglu, w4a16_linear_swiglu_q8,
                    pair_gate_up,
                    w4a16_linear_partial, w4a16_partial_finish,
                    w4_pack_rtn_bf16, w4a16_linear_bf16p,
@@ -19,7 +19,7 @@ from ._lib import (W4Error, lib_path, load, w4_pack_rtn, w4a16_workspace_bytes,
                    EXPORTED)
 
 __all__ = ["W4Error", "lib_path", "load", "w4_pack_rtn", "w4a16_workspace_bytes",
-           "w4a16_linear", "W4A16Linear", "w4a16_linear_noalloc", "w4a16_linear_swiglu", "w4a16_linear_swiglu_q8",
+           "w4a16_linear", "w4a16_linear_noalloc", "w4a16_linear_swiglu", "w4a16_linear_swiglu_q8",
            "pair_gate_up",
            "w4a16_linear_partial", "w4a16_partial_finish",
            "w4_pack_rtn_bf16", "w4a16_linear_bf16p",

@@ -237,49 +237,6 @@ def w4a16_linear(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
     return y
 
 
-class W4A16Linear:
-    """One layer's device parameters for repeated w4a16_linear calls: the
-    packed codes, scales, zero points and bias are checked once, here; each
-    call checks only x and y (the per-token part of the marshalling) and
-    calls w4a16_linear.  The object keeps references to the tensors, whose
-    storage must not change while it is in use."""
-
-    def __init__(self, packed: torch.Tensor, scales: torch.Tensor,
-                 zeros: Optional[torch.Tensor], bias: Optional[torch.Tensor], N: int, K: int,
-                 group_size: int):
-        Kp = padded_k(K, group_size)
-        Ng = Kp // group_size
-        _need(packed, torch.uint8, (N, Kp // 2), "packed")
-        _need(scales, torch.float32, (N, Ng), "scales")
-        if zeros is not None:
-            _need(zeros, torch.uint8, (N, Ng), "zeros")
-        if bias is not None:
-            _need(bias, torch.float32, (N,), "bias")
-        self.N, self.K, self.group_size = int(N), int(K), int(group_size)
-        self.device = packed.device
-        self._tensors = (packed, scales, zeros, bias)
-        self._params = (_ptr(packed), _ptr(scales), _ptr(zeros), _ptr(bias))
-        self._sym = 1 if zeros is None else 0
-
-    def __call__(self, x: torch.Tensor, y=None, workspace=None, stream=None) -> torch.Tensor:
-        M = x.shape[0]
-        N, K, G = self.N, self.K, self.group_size
-        _need(x, torch.bfloat16, (M, K), "x")
-        if y is None:
-            y = torch.empty(M, N, dtype=torch.bfloat16, device=x.device)
-        else:
-            _need(y, torch.bfloat16, (M, N), "y")
-        if M == 0:
-            return y
-        lib = load()
-        _call_with_workspace(
-            lib.w4a16_linear, "w4a16_linear",
-            (_ptr(x),) + self._params + (_ptr(y), M, N, K, G, self._sym),
-            (_stream(x, stream),), self.device, workspace,
-            lambda: lib.w4a16_workspace_bytes(M, N, K, G))
-        return y
-
-
 def w4a16_linear_partial(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
                          zeros: Optional[torch.Tensor], N: int, K: int, group_size: int,
                          y32=None, workspace=None, stream=None) -> torch.Tensor:

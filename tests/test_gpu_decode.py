@@ -361,37 +361,3 @@ def test_activation_hold_is_only_timing(w4, monkeypatch, M, N, K, G, sym, split)
     for y in outs[1:]:
         assert torch.equal(y.view(torch.int16), outs[0].view(torch.int16))
     assert w4.w4_get_device_error() == 0
-
-
-@pytest.mark.parametrize("M,N,K,G,sym", [(1, 3584, 18944, 128, True), (4, 4608, 3584, 32, False),
-                                         (40, 512, 1024, 128, True), (0, 256, 512, 64, True)])
-def test_prepared_layer_equals_the_call(w4, M, N, K, G, sym):
-    """W4A16Linear (parameters checked once, then per-call x and y) runs
-    w4a16_linear: the same bits with y given or allocated, the oracle's
-    result, and shape errors on x and y."""
-    seed = M + N + K
-    packed, scales, zeros = WL.make_random_format(N, K, G, sym, seed)
-    b = (torch.randn(N, generator=torch.Generator().manual_seed(seed)) * 0.1).cuda()
-    x = WL.make_activations(K, M, seed + 1).cuda()
-    packed, scales = packed.cuda(), scales.cuda()
-    zeros = None if zeros is None else zeros.cuda()
-    layer = w4.W4A16Linear(packed, scales, zeros, b, N, K, G)
-    y_fn = w4.w4a16_linear(x, packed, scales, zeros, b, N, K, G)
-    y1 = layer(x)
-    y2 = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
-    assert layer(x, y=y2) is y2
-    torch.cuda.synchronize()
-    assert y1.shape == (M, N)
-    assert torch.equal(y1.view(torch.int16), y_fn.view(torch.int16))
-    assert torch.equal(y2.view(torch.int16), y_fn.view(torch.int16))
-    if M:
-        yref = O.w4a16_linear(x.cpu(), packed.cpu().numpy(), scales.cpu().numpy(),
-                              None if zeros is None else zeros.cpu().numpy(), b.cpu().numpy(), K, G)
-        assert_close(y1, yref, f"prepared layer M{M} N{N} K{K}")
-    with pytest.raises(ValueError):
-        layer(torch.zeros(max(M, 1), K + 1, dtype=torch.bfloat16, device="cuda"))
-    with pytest.raises(ValueError):
-        layer(x, y=torch.empty(M, N + 1, dtype=torch.bfloat16, device="cuda"))
-    with pytest.raises(ValueError):
-        w4.W4A16Linear(packed, scales, zeros, b, N, K + G, G)     # packed too narrow for K
-    assert w4.w4_get_device_error() == 0
