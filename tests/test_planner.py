@@ -9,12 +9,23 @@ tuning variables pin what they name.  The plans tuned on the GB300 for the
 7B decode shapes are pinned too, so that a change of the cost model shows
 up here before it shows up as a slower bench."""
 import itertools
+import os
+import re
 
 import pytest
 
-from helpers import ensure_built
+from helpers import ROOT, ensure_built
 
-W4_WORKSPACE_COUNTER_BYTES = 64 << 10
+
+def _header_int(name):
+    """An integer #define of include/w4.h (a number or a shift of numbers)."""
+    src = open(os.path.join(ROOT, "include", "w4.h")).read()
+    expr = re.search(r"#define\s+" + name + r"\s+\(?([0-9<\s]+)\)?", src).group(1)
+    a, _, b = expr.partition("<<")
+    return int(a) << int(b) if b else int(a)
+
+
+W4_WORKSPACE_COUNTER_BYTES = _header_int("W4_WORKSPACE_COUNTER_BYTES")
 MAX_COUNTERS = W4_WORKSPACE_COUNTER_BYTES // 4
 SMEM_PER_CTA = 232448          # 227 KB
 SMEM_HALF = 115712             # two CTAs on one SM's 228 KB, 1 KB reserved each
