@@ -417,8 +417,8 @@ W4_API size_t w4a8_workspace_bytes(int M, int N, int K, int group_size);
  *         global last-arriver hand-off (or no split)
  *  The tuning variables W4_GEMV_ROWS, W4_GEMV_SPLIT, W4_GEMV_CPS,
  *  W4_GEMV_F16 and W4_GEMV_CSPLIT apply as they do to the calls.
- *  Returns W4_ERR_NULL_PTR, W4_ERR_INVALID_ARG (kind, M, N or sm_count out
- *  of range), W4_ERR_UNSUPPORTED_GROUP, W4_ERR_K_TOO_LARGE (kind 1) or
+ *  Returns W4_ERR_NULL_PTR, W4_ERR_INVALID_ARG (kind, M, N, K or sm_count
+ *  out of range), W4_ERR_UNSUPPORTED_GROUP, W4_ERR_K_TOO_LARGE (kind 1) or
  *  W4_ERR_UNSUPPORTED_SHAPE (no plan fits) as the calls would.
  * ------------------------------------------------------------------------- */
 #define W4_DECODE_PLAN_FIELDS 12
